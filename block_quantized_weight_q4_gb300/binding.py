@@ -1,0 +1,155 @@
+"""ctypes binding over libqmv.so (C ABI declared in include/qmv.h).
+
+Argument marshalling only: tensors are passed as raw device pointers with the current
+torch CUDA stream; every step of the computation runs in the library's kernels.  If the
+library has not been built, every call raises: there is no CPU fallback.
+
+Format (Krafla ".mlb model format v1", "Body"): a matrix image is the q array, zero
+padding to 64 bytes, then the d array; W below is a uint8 CUDA tensor holding it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+Q8_0 = 1
+Q4_0 = 2
+SCALE_F32 = 0
+SCALE_F16 = 1
+X_F32 = 0
+X_BF16 = 1
+
+OK = 0
+E_FORMAT = 2
+E_SHAPE = 3
+E_ARG = 4
+E_ALIGN = 5
+E_CUDA = 6
+E_TIMEOUT = 7
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_lib = None
+
+
+class QmvError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: status {status} ({strerror(status)})")
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libqmv.so")
+
+
+def load_library():
+    """Load libqmv.so (raises OSError if it was not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise OSError(f"libqmv.so not built ({path}); run block_quantized_weight_q4_gb300.build")
+    lib = ctypes.CDLL(path)
+    i64, i32, vp, sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+    lib.qmv_weight_bytes.restype = sz
+    lib.qmv_weight_bytes.argtypes = [i32, i32, i64, i64]
+    lib.qmv_scale_offset.restype = i64
+    lib.qmv_scale_offset.argtypes = [i32, i32, i64, i64]
+    lib.qmv_matrix_wtype.restype = i32
+    lib.qmv_matrix_wtype.argtypes = [i32, ctypes.c_uint32, i32, i32]
+    lib.qmv_matvec.restype = i32
+    lib.qmv_matvec.argtypes = [i32, i32, i64, i64, vp, vp, i32, vp, i32, vp]
+    lib.qmv_dequant.restype = i32
+    lib.qmv_dequant.argtypes = [i32, i32, i64, i64, vp, vp, vp]
+    lib.qmv_validate.restype = i32
+    lib.qmv_validate.argtypes = [i32, i32, i64, i64, vp, vp, vp]
+    lib.qmv_check_device.restype = i32
+    lib.qmv_check_device.argtypes = []
+    lib.qmv_strerror.restype = ctypes.c_char_p
+    lib.qmv_strerror.argtypes = [i32]
+    _lib = lib
+    return lib
+
+
+def strerror(status: int) -> str:
+    try:
+        return load_library().qmv_strerror(status).decode()
+    except OSError:
+        return "libqmv not loaded"
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise QmvError(status, where)
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _x_dtype(x) -> int:
+    import torch
+    if x.dtype == torch.float32:
+        return X_F32
+    if x.dtype == torch.bfloat16:
+        return X_BF16
+    raise TypeError("x must be float32 or bfloat16")
+
+
+def weight_bytes(wtype: int, scale_dtype: int, rows: int, cols: int) -> int:
+    return int(load_library().qmv_weight_bytes(wtype, scale_dtype, rows, cols))
+
+
+def scale_offset(wtype: int, scale_dtype: int, rows: int, cols: int) -> int:
+    return int(load_library().qmv_scale_offset(wtype, scale_dtype, rows, cols))
+
+
+def matrix_wtype(file_wtype: int, q8_mask: int, class_bit: int, shared_classifier: bool = False) -> int:
+    return int(load_library().qmv_matrix_wtype(file_wtype, q8_mask, class_bit, int(bool(shared_classifier))))
+
+
+def matvec(wtype: int, scale_dtype: int, rows: int, cols: int, W, x, y=None, stream=None):
+    """y = W x.  W: uint8 CUDA tensor (matrix image); x: (batch, cols) float32/bfloat16
+    CUDA tensor; y: optional (batch, rows) float32 CUDA tensor.  Returns y."""
+    import torch
+    if x.dim() == 1:
+        x = x.unsqueeze(0)
+    batch = x.shape[0]
+    if x.shape[1] != cols or not x.is_contiguous():
+        raise ValueError("x must be a contiguous (batch, cols) tensor")
+    if y is None:
+        y = torch.empty((batch, rows), dtype=torch.float32, device=x.device)
+    if y.dtype != torch.float32 or tuple(y.shape) != (batch, rows) or not y.is_contiguous():
+        raise ValueError("y must be a contiguous float32 (batch, rows) tensor")
+    st = load_library().qmv_matvec(wtype, scale_dtype, rows, cols, W.data_ptr(), x.data_ptr(), _x_dtype(x),
+                                   y.data_ptr(), batch, _stream(stream))
+    _check(st, "qmv_matvec")
+    return y
+
+
+def dequant(wtype: int, scale_dtype: int, rows: int, cols: int, W, out=None, stream=None):
+    """float32 (rows, cols) = level * d.  Returns out."""
+    import torch
+    if out is None:
+        out = torch.empty((rows, cols), dtype=torch.float32, device=W.device)
+    st = load_library().qmv_dequant(wtype, scale_dtype, rows, cols, W.data_ptr(), out.data_ptr(), _stream(stream))
+    _check(st, "qmv_dequant")
+    return out
+
+
+def validate(wtype: int, scale_dtype: int, rows: int, cols: int, W, stream=None) -> int:
+    """Index of the first Q8_0 quant byte equal to -128, or -1 (waits for the stream)."""
+    import torch
+    first = torch.empty(1, dtype=torch.int64, device=W.device)
+    st = load_library().qmv_validate(wtype, scale_dtype, rows, cols, W.data_ptr(), first.data_ptr(),
+                                     _stream(stream))
+    _check(st, "qmv_validate")
+    return int(first.item())
+
+
+def last_error() -> int:
+    """Synchronize the device; return and clear the kernels' status word."""
+    return int(load_library().qmv_check_device())

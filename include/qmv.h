@@ -1,0 +1,141 @@
+/*
+ * qmv.h -- C ABI of libqmv: products against block-quantized (Q8_0 / Q4_0) weight
+ * matrices on NVIDIA GB300 (sm_103a).
+ *
+ * Format (Krafla ".mlb model format v1" page, sections "Body", "Q8_0", "Q4_0"):
+ *   A rows x cols matrix (cols a multiple of 32) is two arrays written one after the
+ *   other, each zero-padded to a multiple of 64 bytes (the pad after the last array is
+ *   optional and never read here):
+ *     q : Q8_0: rows*cols int8 quants, row-major.
+ *         Q4_0: rows*cols/2 bytes; block k of row r is the 16 bytes at r*cols/2 + 16k;
+ *               byte j holds element j in its low nibble and element j+16 in its high
+ *               nibble; the weight is (nibble - 8) * d.
+ *     d : rows*cols/32 scales, one per block of 32 consecutive weights of a row (scale
+ *         index r*cols/32 + k); float32, or IEEE binary16 when the file's scale_f16
+ *         flag is 1.  Q8_0 weight = q * d.
+ *   The product is y[r] = sum_c W[r][c] * x[c] ("one row per output").
+ *
+ * Conventions for every entry point:
+ *   - W points at the q array.  The d array starts at W + qmv_scale_offset(...), i.e.
+ *     at q's size rounded up to 64 bytes, exactly as in the file.  W must be a device
+ *     pointer aligned to 16 bytes (the file format gives 64).
+ *   - x is batch x cols, row-major, float32 or bfloat16; y is batch x rows float32,
+ *     row-major.  Device pointers, 16-byte aligned for x and out, 4 for y.
+ *   - All memory is owned by the caller; the library allocates no device memory per
+ *     call.  Work is enqueued on `stream` (0 = the legacy default stream) of the calling
+ *     thread's current device, and the call returns without waiting, except where noted.
+ *   - Argument errors are found on the host, before anything is launched; nothing is
+ *     written then.  A CUDA launch error returns QMV_E_CUDA.
+ *   - Errors met inside a running kernel (a bounded wait that ran out) are recorded in
+ *     a per-device status word that qmv_check_device() returns; the kernel then returns
+ *     without finishing its output.
+ */
+#ifndef QMV_H
+#define QMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* wtype: the .mlb header's wtype field (offset 44). */
+#define QMV_Q8_0 1
+#define QMV_Q4_0 2
+
+/* scale_dtype: the header's scale_f16 field (offset 120). */
+#define QMV_SCALE_F32 0
+#define QMV_SCALE_F16 1
+
+/* x_dtype: element type of the activations. */
+#define QMV_X_F32 0
+#define QMV_X_BF16 1
+
+/* Status codes.  QMV_E_FORMAT and QMV_E_SHAPE mirror the loader's ML_E_FORMAT and
+ * ML_E_SHAPE classes (Krafla page, "Validation done by the loader"): an unknown enum
+ * value or an invalid quant is a format error; a zero dimension, cols not a multiple of
+ * 32, or a size that overflows is a shape error. */
+#define QMV_OK 0
+#define QMV_E_FORMAT 2
+#define QMV_E_SHAPE 3
+#define QMV_E_ARG 4     /* null pointer, negative batch                             */
+#define QMV_E_ALIGN 5   /* a pointer not aligned as stated above                    */
+#define QMV_E_CUDA 6    /* a CUDA call failed (launch error, no device, no sm_103a) */
+#define QMV_E_TIMEOUT 7 /* a kernel's bounded wait ran out (see qmv_check_device)   */
+
+/* q8_mask class bits (Krafla page, header offset 72, "q8_mask bits, one per matrix
+ * class").  wq/wk also cover wg and lqkv; wv covers lz; wo covers lout. */
+#define QMV_CLASS_TOK_EMB 1
+#define QMV_CLASS_WCLS 2
+#define QMV_CLASS_WQ_WK 4
+#define QMV_CLASS_WV 8
+#define QMV_CLASS_WO 16
+#define QMV_CLASS_W1_W3 32
+#define QMV_CLASS_W2 64
+
+/* Bytes of a matrix image: q, its padding to 64, then d (no trailing pad).
+ * Overflow-checked ("All size arithmetic is overflow-checked").  Returns 0 for an
+ * invalid wtype, scale_dtype or shape.  Host only. */
+size_t qmv_weight_bytes(int wtype, int scale_dtype, int64_t rows, int64_t cols);
+
+/* Offset of the d array from W (q's size rounded up to 64).  -1 if invalid.  Host only. */
+int64_t qmv_scale_offset(int wtype, int scale_dtype, int64_t rows, int64_t cols);
+
+/* Storage type of one matrix of a mixed model (Krafla page, header offset 72): a Q4_0
+ * file stores the classes whose bit is set in q8_mask as Q8_0; with a shared classifier
+ * (header offset 48 non-zero) tok_emb is Q8_0 when bit 1 or bit 2 is set.  A Q8_0 file
+ * stores everything as Q8_0.  class_bit is one QMV_CLASS_* value.  Returns QMV_Q8_0 or
+ * QMV_Q4_0, or -1 for an unknown file_wtype or class bit.  Host only. */
+int qmv_matrix_wtype(int file_wtype, uint32_t q8_mask, int class_bit, int shared_classifier);
+
+/* y = W x for a batch of activation vectors (Krafla page, "Matrices are stored row by
+ * row, one row per output: y[r] = sum_c W[r][c] x[c]").
+ *   W     : device, the matrix image described above (q array first).
+ *   x     : device, batch x cols, x_dtype (QMV_X_F32 or QMV_X_BF16), row-major.
+ *   y     : device, batch x rows float32, row-major; fully overwritten.
+ *   batch : number of activation vectors, >= 0; 0 launches nothing and returns QMV_OK.
+ * Each block contributes d * sum_j level_j * x_j; sums are kept in float32.  Batches of
+ * 1-15 run the decode kernels (weights decoded in registers, tensor-core mma on the
+ * exact integer levels); larger batches run the prefill kernel (weights dequantized to
+ * bfloat16 in shared memory, tcgen05 MMA into tensor memory).  Products agree with an
+ * exact evaluation to within 1e-3 * sum_c |W[r][c] x[c]| per output.  A Q8_0 byte of
+ * -128 is not rejected here: it decodes as -128 * d (see qmv_validate).
+ * Returns QMV_OK, or QMV_E_FORMAT / QMV_E_SHAPE / QMV_E_ARG / QMV_E_ALIGN before any
+ * launch, or QMV_E_CUDA. */
+int qmv_matvec(int wtype, int scale_dtype, int64_t rows, int64_t cols, const void *W,
+               const void *x, int x_dtype, float *y, int batch, cudaStream_t stream);
+
+/* out[r][c] = level * d as float32, with one float32 multiplication rounded to nearest
+ * even (Krafla page, "Q8_0" and "Q4_0"; f16 scales are first converted exactly to
+ * float32, "The runtime converts f16 scales to f32 exactly").  No flush of subnormals;
+ * NaN and infinite scales propagate by IEEE rules.
+ *   out : device, rows x cols float32, row-major, 16-byte aligned; fully overwritten.
+ * Returns as qmv_matvec. */
+int qmv_dequant(int wtype, int scale_dtype, int64_t rows, int64_t cols, const void *W,
+                float *out, cudaStream_t stream);
+
+/* The loader's quant check (Krafla page, "Q8_0": "The loader rejects any byte equal to
+ * -128", reported as ML_E_FORMAT).  Scans the q array on the device and writes to
+ * *first_bad (device, 8-byte aligned) the smallest byte index into q that holds -128,
+ * or -1 when there is none.  Q4_0 has no invalid nibble ("Any d and nibbles are valid
+ * input to the runtime"), so for Q4_0 it writes -1.  Asynchronous: the caller reads
+ * *first_bad after the stream has reached this point.  Returns as qmv_matvec. */
+int qmv_validate(int wtype, int scale_dtype, int64_t rows, int64_t cols, const void *W,
+                 int64_t *first_bad, cudaStream_t stream);
+
+/* Synchronizes the current device, then returns and clears the status word that the
+ * kernels set when a bounded wait runs out (QMV_E_TIMEOUT); QMV_OK when none was set,
+ * QMV_E_CUDA when the device reports a CUDA error. */
+int qmv_check_device(void);
+
+/* Short English text for a status code; never NULL. */
+const char *qmv_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMV_H */

@@ -1,0 +1,201 @@
+"""Plain CPU oracle for block-quantized (Q8_0 / Q4_0) weight matrices.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the CPU-baseline
+leg of ``bench.py`` may use this package; the CUDA library and its Python binding never
+import it.  The arithmetic lives in ``qmv_oracle.c`` (plain C, one weight at a time,
+products in double precision), written from the Krafla ".mlb model format v1" page:
+sections "Body" (two arrays q then d, each padded to 64 bytes), "Q8_0", "Q4_0",
+"Quantization rule" and "Validation done by the loader".  This module only compiles
+that file with gcc and marshals numpy arrays to it.
+
+Parity unpinned: the writer-only corner readings (an f16 Q8_0 scale that rounds to
+zero, the all-zero Q4_0 block, ties of the largest magnitude); everything else is
+pinned by ``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "qmv_oracle.c")
+_LIB = os.path.join(_HERE, "_build", "liboracle.so")
+
+Q8_0 = 1
+Q4_0 = 2
+OK = 0
+E_FORMAT = 2
+E_SHAPE = 3
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no fast-math, no FMA contraction)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+           "-shared", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    lib = ctypes.CDLL(build())
+    i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+    lib.oracle_weight_bytes.restype = i64
+    lib.oracle_weight_bytes.argtypes = [i32, i32, i64, i64]
+    lib.oracle_scale_offset.restype = i64
+    lib.oracle_scale_offset.argtypes = [i32, i32, i64, i64]
+    lib.oracle_f16_value.restype = ctypes.c_float
+    lib.oracle_f16_value.argtypes = [ctypes.c_uint16]
+    lib.oracle_f16_bits_rne.restype = ctypes.c_uint16
+    lib.oracle_f16_bits_rne.argtypes = [ctypes.c_float]
+    lib.oracle_bf16_value.restype = ctypes.c_float
+    lib.oracle_bf16_value.argtypes = [ctypes.c_uint16]
+    lib.oracle_level.restype = i32
+    lib.oracle_level.argtypes = [vp, i32, i64, i64, i64]
+    lib.oracle_scale.restype = ctypes.c_float
+    lib.oracle_scale.argtypes = [vp, i32, i32, i64, i64, i64, i64]
+    lib.oracle_dequant.restype = i32
+    lib.oracle_dequant.argtypes = [i32, i32, i64, i64, vp, vp]
+    lib.oracle_matvec.restype = i32
+    lib.oracle_matvec.argtypes = [i32, i32, i64, i64, vp, vp, i32, i32, vp, vp]
+    lib.oracle_matvec_rows.restype = i32
+    lib.oracle_matvec_rows.argtypes = [i32, i32, i64, i64, vp, vp, i32, i32, vp, i64, vp, vp]
+    lib.oracle_validate.restype = i32
+    lib.oracle_validate.argtypes = [i32, i32, i64, i64, vp]
+    lib.oracle_quant_q8_block.restype = i32
+    lib.oracle_quant_q8_block.argtypes = [vp, i32, vp, vp]
+    lib.oracle_quant_q4_round_block.restype = i32
+    lib.oracle_quant_q4_round_block.argtypes = [vp, i32, vp, vp]
+    lib.oracle_quantize.restype = i32
+    lib.oracle_quantize.argtypes = [i32, i32, i64, i64, vp, vp]
+    _lib = lib
+    return lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+def weight_bytes(wtype: int, scale_f16: int, rows: int, cols: int) -> int:
+    return int(_load().oracle_weight_bytes(wtype, scale_f16, rows, cols))
+
+
+def scale_offset(wtype: int, scale_f16: int, rows: int, cols: int) -> int:
+    return int(_load().oracle_scale_offset(wtype, scale_f16, rows, cols))
+
+
+def f16_value(code: int) -> float:
+    return float(_load().oracle_f16_value(code))
+
+
+def f16_bits_rne(v: float) -> int:
+    return int(_load().oracle_f16_bits_rne(v))
+
+
+def bf16_value(code: int) -> float:
+    return float(_load().oracle_bf16_value(code))
+
+
+def level(W: np.ndarray, wtype: int, cols: int, r: int, c: int) -> int:
+    return int(_load().oracle_level(_ptr(W), wtype, cols, r, c))
+
+
+def scale(W: np.ndarray, wtype: int, scale_f16: int, rows: int, cols: int, r: int, k: int) -> float:
+    return float(_load().oracle_scale(_ptr(W), wtype, scale_f16, rows, cols, r, k))
+
+
+def dequant(W: np.ndarray, wtype: int, scale_f16: int, rows: int, cols: int) -> np.ndarray:
+    """float32 rows x cols, w = level * d (one float32 multiply)."""
+    out = np.empty((rows, cols), dtype=np.float32)
+    st = _load().oracle_dequant(wtype, scale_f16, rows, cols, _ptr(W), _ptr(out))
+    if st != OK:
+        raise ValueError(f"oracle_dequant status {st}")
+    return out
+
+
+def _x_args(x: np.ndarray):
+    if x.dtype == np.float32:
+        return 0
+    if x.dtype == np.uint16:  # bfloat16 codes
+        return 1
+    raise TypeError("x must be float32 or uint16 bfloat16 codes")
+
+
+def matvec(W: np.ndarray, wtype: int, scale_f16: int, rows: int, cols: int, x: np.ndarray):
+    """y (batch x rows, float64) and absref = sum |w x| (same shape) for x (batch x cols)."""
+    x = np.ascontiguousarray(x)
+    batch = x.shape[0]
+    assert x.shape == (batch, cols)
+    y = np.empty((batch, rows), dtype=np.float64)
+    a = np.empty((batch, rows), dtype=np.float64)
+    st = _load().oracle_matvec(wtype, scale_f16, rows, cols, _ptr(W), _ptr(x), _x_args(x),
+                               batch, _ptr(y), _ptr(a))
+    if st != OK:
+        raise ValueError(f"oracle_matvec status {st}")
+    return y, a
+
+
+def matvec_rows(W: np.ndarray, wtype: int, scale_f16: int, rows: int, cols: int,
+                x: np.ndarray, row_ids):
+    """Like matvec but only for the listed rows: returns (batch x len(row_ids)) arrays."""
+    x = np.ascontiguousarray(x)
+    batch = x.shape[0]
+    ids = np.ascontiguousarray(np.asarray(row_ids, dtype=np.int64))
+    y = np.empty((batch, ids.size), dtype=np.float64)
+    a = np.empty((batch, ids.size), dtype=np.float64)
+    st = _load().oracle_matvec_rows(wtype, scale_f16, rows, cols, _ptr(W), _ptr(x), _x_args(x),
+                                    batch, _ptr(ids), ids.size, _ptr(y), _ptr(a))
+    if st != OK:
+        raise ValueError(f"oracle_matvec_rows status {st}")
+    return y, a
+
+
+def validate(W: np.ndarray, wtype: int, scale_f16: int, rows: int, cols: int) -> int:
+    return int(_load().oracle_validate(wtype, scale_f16, rows, cols, _ptr(W)))
+
+
+def quant_q8_block(x: np.ndarray, scale_f16: int):
+    """(status, q int8[32], stored scale bits) for one block by the Q8_0 rule."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    assert x.size == 32
+    q = np.zeros(32, dtype=np.int8)
+    bits = np.zeros(1, dtype=np.uint32)
+    st = _load().oracle_quant_q8_block(_ptr(x), scale_f16, _ptr(q), _ptr(bits))
+    return int(st), q, int(bits[0])
+
+
+def quant_q4_round_block(x: np.ndarray, scale_f16: int):
+    """(status, 16 packed bytes, stored scale bits) for one block by the Q4_0 round rule."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    assert x.size == 32
+    qs = np.zeros(16, dtype=np.uint8)
+    bits = np.zeros(1, dtype=np.uint32)
+    st = _load().oracle_quant_q4_round_block(_ptr(x), scale_f16, _ptr(qs), _ptr(bits))
+    return int(st), qs, int(bits[0])
+
+
+def quantize(src: np.ndarray, wtype: int, scale_f16: int) -> np.ndarray:
+    """Matrix bytes (two-array layout) from float32 rows x cols by the writer rules."""
+    src = np.ascontiguousarray(src, dtype=np.float32)
+    rows, cols = src.shape
+    n = weight_bytes(wtype, scale_f16, rows, cols)
+    if n < 0:
+        raise ValueError("bad shape")
+    W = np.zeros(n, dtype=np.uint8)
+    st = _load().oracle_quantize(wtype, scale_f16, rows, cols, _ptr(src), _ptr(W))
+    if st != OK:
+        raise ValueError(f"oracle_quantize status {st}")
+    return W

@@ -1,0 +1,146 @@
+"""The pins catch plausible mistakes in the oracle.
+
+Each case copies oracle/qmv_oracle.c, plants one mistake by text substitution (a swapped
+nibble half, a dropped level offset, a transposed index, wrong padding, a lost sign...),
+builds the copy with gcc into a temporary directory and runs the page-derived pin checks
+against it.  At least one check must fail for every mutant, and all checks must pass for
+the unmodified copy.  Everything happens on the CPU; the real oracle is not touched.
+"""
+import ctypes
+import os
+import subprocess
+import tempfile
+
+import numpy as np
+import pytest
+
+from block_quantized_weight_q4_gb300 import inputs
+from conftest import read_cases, read_rows
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "qmv_oracle.c")
+
+MUTANTS = {
+    "nibble_halves_swapped": ("(j < 16) ? (byte & 0x0f) : (byte >> 4)", "(j < 16) ? (byte >> 4) : (byte & 0x0f)"),
+    "level_offset_dropped": ("return nibble - 8;", "return nibble;"),
+    "level_offset_off_by_one": ("return nibble - 8;", "return nibble - 7;"),
+    "scale_index_transposed": ("int64_t idx = r * (cols / 32) + k;", "int64_t idx = k * rows + r;"),
+    "pad_to_32": ("return ((n + 63) / 64) * 64;", "return ((n + 31) / 32) * 32;"),
+    "q4_row_stride": ("W[r * (cols / 2) + 16 * k + (j % 16)]", "W[r * cols + 16 * k + (j % 16)]"),
+    "q4_byte_in_block": ("W[r * (cols / 2) + 16 * k + (j % 16)]", "W[r * (cols / 2) + 16 * k + j / 2]"),
+    "q8_unsigned": ("return (int)(int8_t)W[r * cols + c];", "return (int)W[r * cols + c];"),
+    "f16_bias": ("mag = ldexp((double)(1024 + m), e - 25);", "mag = ldexp((double)(1024 + m), e - 24);"),
+    "f16_subnormal": ("mag = ldexp((double)m, -24);", "mag = ldexp((double)m, -23);"),
+    "f16_implicit_bit": ("mag = ldexp((double)(1024 + m), e - 25);", "mag = ldexp((double)m, e - 25);"),
+    "x_transposed": ("((const float *)x)[b * cols + c]", "((const float *)x)[c * cols + b]"),
+    "absref_not_abs": ("acc_abs += fabs(t);", "acc_abs += t;"),
+    "validate_wrong_byte": ("if (W[i] == 0x80)", "if (W[i] == 0x7f)"),
+    "q8_size_halved": ("int64_t q = (wtype == ORACLE_Q8_0) ? n : n / 2;", "int64_t q = n / 2;"),
+    "f16_scale_size": ("int64_t dsz = nscales * (scale_f16 ? 2 : 4);", "int64_t dsz = nscales * 4;"),
+    "f16_scale_read_as_f32": ("if (scale_f16) {\n        const uint8_t *p = W + off + 2 * idx;",
+                              "if (0) {\n        const uint8_t *p = W + off + 2 * idx;"),
+}
+
+
+class Orc:
+    """Minimal ctypes view of one build of the oracle source."""
+
+    def __init__(self, so):
+        lib = ctypes.CDLL(so)
+        i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+        lib.oracle_weight_bytes.restype = i64
+        lib.oracle_weight_bytes.argtypes = [i32, i32, i64, i64]
+        lib.oracle_f16_value.restype = ctypes.c_float
+        lib.oracle_f16_value.argtypes = [ctypes.c_uint16]
+        lib.oracle_dequant.restype = i32
+        lib.oracle_dequant.argtypes = [i32, i32, i64, i64, vp, vp]
+        lib.oracle_matvec.restype = i32
+        lib.oracle_matvec.argtypes = [i32, i32, i64, i64, vp, vp, i32, i32, vp, vp]
+        lib.oracle_validate.restype = i32
+        lib.oracle_validate.argtypes = [i32, i32, i64, i64, vp]
+        self.lib = lib
+
+    def dequant(self, W, wt, sf, rows, cols):
+        out = np.empty((rows, cols), np.float32)
+        assert self.lib.oracle_dequant(wt, sf, rows, cols, W.ctypes.data, out.ctypes.data) == 0
+        return out
+
+    def matvec(self, W, wt, sf, rows, cols, x):
+        x = np.ascontiguousarray(x)
+        y = np.empty((x.shape[0], rows))
+        a = np.empty_like(y)
+        assert self.lib.oracle_matvec(wt, sf, rows, cols, W.ctypes.data, x.ctypes.data,
+                                      int(x.dtype == np.uint16), x.shape[0], y.ctypes.data, a.ctypes.data) == 0
+        return y, a
+
+
+def pin_checks(o):
+    """Yields (name, passed) for the page-derived checks."""
+    for wt, sf, rows, cols, expect, *_ in read_rows("sizes_worked_examples.txt"):
+        yield "size", o.lib.oracle_weight_bytes(int(wt), int(sf), int(rows), int(cols)) == int(expect)
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = codes.view(np.float16).astype(np.float32)
+    got = np.array([o.lib.oracle_f16_value(int(c)) for c in codes], np.float32)
+    fin = ~np.isnan(ref)
+    yield "f16", bool(np.array_equal(got[fin], ref[fin]))
+    for case in read_cases("hand_blocks.txt"):
+        wt, sf = int(case["wtype"][0]), int(case["scale_f16"][0])
+        qb = np.array([int(b, 16) for b in case["bytes"]], np.uint8)
+        d = (np.array([int(case["scale_code"][0], 16)], np.uint16) if sf
+             else np.array([float(case["scale"][0])], np.float32).view(np.uint32))
+        W = inputs.assemble(wt, sf, 1, 32, qb, d)
+        expect = np.array([float(v) for v in case["weights"]], np.float32)
+        yield "hand", bool(np.array_equal(o.dequant(W, wt, sf, 1, 32)[0], expect))
+    # scale index / row addressing: w[r][c] = 2^(3r + c//32)
+    rows, cols = 3, 96
+    q = np.full(rows * cols // 2, 0x99, np.uint8)
+    dv = np.array([2.0 ** (3 * r + k) for r in range(rows) for k in range(3)], np.float32)
+    for sf in (0, 1):
+        codes2 = dv.astype(np.float16).view(np.uint16) if sf else dv.view(np.uint32)
+        W = inputs.assemble(2, sf, rows, cols, q, codes2)
+        exp = np.array([[2.0 ** (3 * r + c // 32) for c in range(cols)] for r in range(rows)], np.float32)
+        yield "scale_index", bool(np.array_equal(o.dequant(W, 2, sf, rows, cols), exp))
+    # one-hot product on random Q4_0 / Q8_0 matrices vs the dequantized columns
+    for wt in (1, 2):
+        m = inputs.make_matrix(wt, 0, 5, 96, seed=3)
+        deq = o.dequant(m.W, wt, 0, 5, 96)
+        y, a = o.matvec(m.W, wt, 0, 5, 96, np.eye(96, dtype=np.float32))
+        yield "one_hot", bool(np.array_equal(y.astype(np.float32), deq.T) and np.array_equal(a, np.abs(y)))
+    # the Q8 -128 check
+    m = inputs.make_matrix(1, 0, 4, 64, seed=1)
+    W = m.W.copy()
+    W[77] = 0x80
+    yield "validate", o.lib.oracle_validate(1, 0, 4, 64, W.ctypes.data) == 2 and \
+        o.lib.oracle_validate(1, 0, 4, 64, m.W.ctypes.data) == 0
+
+
+def build_variant(tmp, name, text):
+    c = os.path.join(tmp, f"{name}.c")
+    so = os.path.join(tmp, f"{name}.so")
+    with open(c, "w") as f:
+        f.write(text)
+    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-o", so, c, "-lm"],
+                   check=True)
+    return Orc(so)
+
+
+@pytest.fixture(scope="module")
+def tmpdir():
+    with tempfile.TemporaryDirectory() as d:
+        yield d
+
+
+def test_unmodified_copy_passes_all_pins(tmpdir):
+    o = build_variant(tmpdir, "orig", open(SRC).read())
+    failed = [n for n, ok in pin_checks(o) if not ok]
+    assert not failed, failed
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(tmpdir, name):
+    old, new = MUTANTS[name]
+    text = open(SRC).read()
+    assert text.count(old) >= 1, f"mutation site not found: {old}"
+    o = build_variant(tmpdir, name, text.replace(old, new))
+    results = list(pin_checks(o))
+    assert any(not ok for _, ok in results), f"mutant {name} passed every pin"
