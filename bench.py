@@ -1,0 +1,361 @@
+#!/usr/bin/env python
+"""Benchmark: quantized GEMV weight GB/s (and fraction of HBM peak) and tokens/s per layer.
+
+Workload (default): one Llama-7B-shaped decode layer, Q4_0 with f16 scales, batch 1,
+bfloat16 activations: wq, wo 4096x4096; wk, wv 1024x4096; w1, w3 11008x4096; w2 4096x11008
+(99,680,256 weight bytes).  A step is the seven products y = W x of the layer, issued as
+one CUDA graph of seven libqmv launches.  Weights are seeded synthetic data; distinct
+copies of the layer rotate from step to step so that every step streams its weights from
+HBM (the copies together are more than 4x the L2 size).
+
+Prints one JSON line.  --impl reference times the CPU oracle (the plain C checker) on a
+bounded sample of the same workload instead.
+
+Timing: warm-up steps, then K timed steps between CUDA events on the launching stream,
+synchronized on both sides; with several GPUs every rank runs its own replica (nothing is
+exchanged) and the slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from block_quantized_weight_q4_gb300 import inputs  # noqa: E402
+
+METRIC = "quantized GEMV weight GB/s (fraction of GB300 HBM peak) and tokens/s per layer"
+UNIT = "GB/s"
+WORKLOAD = "llama7b"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle sample")
+    return ap.parse_args()
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d.get("hbm_gbs", FALLBACK_HBM_GBS)), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def layer_specs():
+    return inputs.WORKLOADS[WORKLOAD].matrices
+
+
+def layer_bytes(specs):
+    return sum(inputs.array_offsets(s.wtype, s.scale_f16, s.rows, s.cols)[1] +
+               inputs.array_offsets(s.wtype, s.scale_f16, s.rows, s.cols)[2] for s in specs)
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.path = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        busy = [s for s in sm if mx and s >= 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ CPU oracle sample
+def oracle_sample(specs, seconds):
+    """Time the oracle on the first rows of each matrix of the layer.
+
+    Returns a dict: value (GB/s of weight bytes), cores, sample (text), rows, bytes, seconds."""
+    import oracle
+    oracle.build()
+    mats, xs = [], []
+    for i, s in enumerate(specs):
+        mats.append(inputs.make_matrix(s.wtype, s.scale_f16, s.rows, s.cols, seed=inputs.matrix_seed(WORKLOAD, i)))
+        xs.append(inputs.make_x(1, s.cols, True, seed=inputs.x_seed(WORKLOAD, i)))
+
+    def run(nrows):
+        nbytes = 0
+        t0 = time.perf_counter()
+        for m, x, s in zip(mats, xs, specs):
+            r = min(nrows, s.rows)
+            oracle.matvec_rows(m.W, s.wtype, s.scale_f16, s.rows, s.cols, x, np.arange(r))
+            nbytes += r * s.cols * (0.5 if s.wtype == 2 else 1.0) + r * (s.cols // 32) * (2 if s.scale_f16 else 4)
+        return time.perf_counter() - t0, int(nbytes)
+
+    t1, _ = run(1)  # calibration: one row of every matrix
+    nrows = max(1, int(seconds / max(t1, 1e-9)))
+    dt, nbytes = run(nrows)
+    desc = (f"first {nrows} rows of each of the 7 layer matrices, batch 1, bf16 x "
+            f"({nbytes / 1e6:.2f} MB of the layer's {layer_bytes(specs) / 1e6:.2f} MB), single thread")
+    return {"value": nbytes / dt / 1e9, "cores": 1, "sample": desc, "rows": nrows, "bytes": nbytes,
+            "seconds": dt, "run": run}
+
+
+def run_reference(args, world, rank):
+    """The oracle as it stands, timed on the host cores; rank 0 only."""
+    if rank != 0:
+        return
+    specs = layer_specs()
+    per_step = 90.0 / max(1, args.steps + args.warmup)  # whole run within about 1.5 minutes
+    smp = oracle_sample(specs, min(per_step, 2.0))
+    times = []
+    for step in range(args.warmup + args.steps):
+        dt, nbytes = smp["run"](smp["rows"])
+        if step >= args.warmup:
+            times.append(dt)
+    t = sum(times) / len(times)
+    v = smp["bytes"] / t / 1e9
+    out = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": "llama7b_decode_layer_q4_0_f16_batch1", "sample": smp["sample"]},
+           "cpu_baseline": {"value": v, "unit": UNIT, "cores": smp["cores"], "kind": "oracle",
+                            "sample": smp["sample"]},
+           "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_ours(args, world, rank, local):
+    import torch
+    import block_quantized_weight_q4_gb300 as qmv
+    from block_quantized_weight_q4_gb300.build import build
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (no CPU fallback)")
+    torch.cuda.set_device(local)
+    build()
+    qmv.load_library()
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+
+    specs = layer_specs()
+    lb = layer_bytes(specs)
+    ncopy = max(2, -(-4 * l2 // lb) + 1)
+
+    # seeded synthetic weights (host), uploaded once, then cloned into rotating copies
+    Ws = []
+    for i, s in enumerate(specs):
+        m = inputs.make_matrix(s.wtype, s.scale_f16, s.rows, s.cols, seed=inputs.matrix_seed(WORKLOAD, i))
+        Ws.append(torch.from_numpy(m.W).to(dev))
+    copies = [[w if c == 0 else w.clone() for w in Ws] for c in range(ncopy)]
+    xs_host = [inputs.make_x(1, s.cols, True, seed=inputs.x_seed(WORKLOAD, i)) for i, s in enumerate(specs)]
+    xs = [torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16) for x in xs_host]
+    ys = [torch.empty((1, s.rows), dtype=torch.float32, device=dev) for s in specs]
+
+    def step(c, stream=None):
+        for s, W, x, y in zip(specs, copies[c], xs, ys):
+            qmv.matvec(s.wtype, s.scale_f16, s.rows, s.cols, W, x, y, stream)
+
+    # eager warm-up (sets kernel attributes), then one graph per weight copy
+    for c in range(ncopy):
+        step(c)
+    torch.cuda.synchronize()
+    graphs = []
+    cap = torch.cuda.Stream()
+    for c in range(ncopy):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            step(c)
+        graphs.append(g)
+    torch.cuda.synchronize()
+
+    for i in range(args.warmup):
+        graphs[i % ncopy].replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        graphs[(args.warmup + i) % ncopy].replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    ms = max_over_ranks(ms, world)
+    status = qmv.last_error()
+    if status != 0:
+        raise SystemExit(f"device status {status} after the timed region")
+
+    value = lb * world / (ms * 1e-3) / 1e9
+    tokens_per_s = 1.0 / (ms * 1e-3)
+
+    # per-matrix kernel durations (same launches, back to back, rotating copies)
+    per_matrix = {}
+    reps = 200
+    for i, s in enumerate(specs):
+        mb = inputs.array_offsets(s.wtype, s.scale_f16, s.rows, s.cols)
+        nb = mb[1] + mb[2]
+        for c in range(ncopy):
+            qmv.matvec(s.wtype, s.scale_f16, s.rows, s.cols, copies[c][i], xs[i], ys[i])
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for r in range(reps):
+            qmv.matvec(s.wtype, s.scale_f16, s.rows, s.cols, copies[r % ncopy][i], xs[i], ys[i])
+        b.record(stream)
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / reps
+        per_matrix[s.name] = {"us": round(us, 3), "gbs": round(nb / (us * 1e-6) / 1e9, 1)}
+
+    # end to end through the public API: pinned host x in, y back to pinned host
+    x_all = np.concatenate([x.reshape(-1) for x in xs_host])
+    xh = torch.from_numpy(x_all.view(np.int16)).pin_memory()
+    xd = torch.empty_like(xh, device=dev)
+    offs = np.cumsum([0] + [s.cols for s in specs])
+    yd = torch.empty(sum(s.rows for s in specs), dtype=torch.float32, device=dev)
+    yh = torch.empty_like(yd, device="cpu").pin_memory()
+    yoffs = np.cumsum([0] + [s.rows for s in specs])
+    e2e_steps = max(10, min(args.steps, 2000))
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for it in range(e2e_steps):
+        c = it % ncopy
+        xd.copy_(xh, non_blocking=True)
+        xb = xd.view(torch.bfloat16)
+        for i, s in enumerate(specs):
+            qmv.matvec(s.wtype, s.scale_f16, s.rows, s.cols, copies[c][i], xb[offs[i]:offs[i + 1]].view(1, s.cols),
+                       yd[yoffs[i]:yoffs[i + 1]].view(1, s.rows))
+        yh.copy_(yd, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    e2e_s = max_over_ranks(e2e_s, world)
+    e2e = {"value": lb * world / e2e_s / 1e9, "unit": UNIT, "h2d_bytes_per_step": int(xh.numel() * 2),
+           "d2h_bytes_per_step": int(yd.numel() * 4), "ms_per_step": e2e_s * 1e3}
+
+    peak, peak_src = measured_peaks()
+    achieved = lb / (ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": None, "peak_source": peak_src,
+                "kernel": "matvec_mma_kernel<Q4_0, f16 scales, bf16 x>",
+                "bytes_per_launch": round(lb / len(specs)),
+                "avg_launch_us": round(ms * 1e3 / len(specs), 3)}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        smp = oracle_sample(specs, args.cpu_seconds)
+        cpu = {"value": smp["value"], "unit": UNIT, "cores": smp["cores"], "kind": "oracle", "sample": smp["sample"]}
+
+    if rank == 0:
+        out = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+               "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+               "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+               "config": {"workload": "llama7b_decode_layer_q4_0_f16_batch1",
+                          "matrices": {s.name: [s.rows, s.cols] for s in specs}, "batch": 1,
+                          "x_dtype": "bf16", "weight_bytes_per_step": lb, "parallelism": f"replicas{world}",
+                          "l2_defeat": f"{ncopy} rotating weight copies, {ncopy * lb / 1e6:.0f} MB > 4x L2 "
+                                       f"({l2 / 1e6:.0f} MB)",
+                          "step": "one CUDA graph of 7 libqmv launches"},
+               "tokens_per_s_per_layer": round(tokens_per_s * world, 1),
+               "per_matrix": per_matrix, "e2e": e2e, "roofline": roofline, "cpu_baseline": cpu,
+               "clocks": clk, "gpu_launches": len(specs) * args.steps}
+        print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

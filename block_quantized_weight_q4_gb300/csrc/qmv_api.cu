@@ -1,0 +1,190 @@
+// qmv_api.cu -- the C ABI of libqmv (declared in include/qmv.h): argument checks, the
+// layout of a matrix image, kernel selection and the per-device status word.
+//
+// Layout (Krafla ".mlb model format v1", "Body"): q array, zero padding to a multiple of 64
+// bytes, d array.  Checks follow the loader's classes ("Validation done by the loader"):
+// unknown enum -> format error; zero dimension, cols not a multiple of 32, overflow -> shape.
+#include <mutex>
+
+#include "qmv_common.cuh"
+#include "qmv_internal.h"
+
+namespace qmv {
+
+// The per-device status word (one copy per device that loads the library).
+__device__ int g_device_status = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[kMaxDevices];
+bool g_dev_ready[kMaxDevices] = {};
+
+struct Layout {
+  int64_t q_bytes, d_off, d_bytes;
+};
+
+int make_layout(int wtype, int scale_dtype, int64_t rows, int64_t cols, Layout* L) {
+  if (wtype != QMV_Q8_0 && wtype != QMV_Q4_0) return QMV_E_FORMAT;
+  if (scale_dtype != QMV_SCALE_F32 && scale_dtype != QMV_SCALE_F16) return QMV_E_FORMAT;
+  if (rows <= 0 || cols <= 0 || cols % 32 != 0) return QMV_E_SHAPE;
+  if (rows > INT64_MAX / cols) return QMV_E_SHAPE;
+  const int64_t n = rows * cols;
+  if (n > INT64_MAX / 4) return QMV_E_SHAPE;
+  L->q_bytes = (wtype == QMV_Q8_0) ? n : n / 2;
+  L->d_bytes = (n / 32) * (scale_dtype == QMV_SCALE_F16 ? 2 : 4);
+  L->d_off = (L->q_bytes + 63) / 64 * 64;
+  if (L->d_off > INT64_MAX - L->d_bytes) return QMV_E_SHAPE;
+  return QMV_OK;
+}
+
+int make_ref(int wtype, int scale_dtype, int64_t rows, int64_t cols, const void* W, MatrixRef* m) {
+  Layout L;
+  const int st = make_layout(wtype, scale_dtype, rows, cols, &L);
+  if (st != QMV_OK) return st;
+  if (W == nullptr) return QMV_E_ARG;
+  if (reinterpret_cast<uintptr_t>(W) % 16 != 0) return QMV_E_ALIGN;
+  m->wtype = wtype;
+  m->scale_f16 = scale_dtype == QMV_SCALE_F16;
+  m->rows = rows;
+  m->cols = cols;
+  m->q = static_cast<const uint8_t*>(W);
+  m->d = m->q + L.d_off;
+  return QMV_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+}  // namespace
+
+cudaError_t current_device_info(DeviceInfo* info) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  if (!g_dev_ready[dev]) {
+    DeviceInfo d{};
+    d.device = dev;
+    if ((err = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+    if ((err = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess) return err;
+    if ((err = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess) return err;
+    int optin = 0;
+    if ((err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return err;
+    d.smem_optin = (size_t)optin;
+    void* sym = nullptr;
+    if ((err = cudaGetSymbolAddress(&sym, g_device_status)) != cudaSuccess) return err;
+    d.status = static_cast<int*>(sym);
+    g_dev[dev] = d;
+    g_dev_ready[dev] = true;
+  }
+  *info = g_dev[dev];
+  return cudaSuccess;
+}
+
+}  // namespace qmv
+
+using namespace qmv;
+
+extern "C" {
+
+size_t qmv_weight_bytes(int wtype, int scale_dtype, int64_t rows, int64_t cols) {
+  Layout L;
+  if (make_layout(wtype, scale_dtype, rows, cols, &L) != QMV_OK) return 0;
+  return (size_t)(L.d_off + L.d_bytes);
+}
+
+int64_t qmv_scale_offset(int wtype, int scale_dtype, int64_t rows, int64_t cols) {
+  Layout L;
+  if (make_layout(wtype, scale_dtype, rows, cols, &L) != QMV_OK) return -1;
+  return L.d_off;
+}
+
+int qmv_matrix_wtype(int file_wtype, uint32_t q8_mask, int class_bit, int shared_classifier) {
+  if (file_wtype != QMV_Q8_0 && file_wtype != QMV_Q4_0) return -1;
+  switch (class_bit) {
+    case QMV_CLASS_TOK_EMB: case QMV_CLASS_WCLS: case QMV_CLASS_WQ_WK: case QMV_CLASS_WV:
+    case QMV_CLASS_WO: case QMV_CLASS_W1_W3: case QMV_CLASS_W2: break;
+    default: return -1;
+  }
+  if (file_wtype == QMV_Q8_0) return QMV_Q8_0;
+  uint32_t bits = (uint32_t)class_bit;
+  if (class_bit == QMV_CLASS_TOK_EMB && shared_classifier) bits |= QMV_CLASS_WCLS;
+  return (q8_mask & bits) ? QMV_Q8_0 : QMV_Q4_0;
+}
+
+int qmv_matvec(int wtype, int scale_dtype, int64_t rows, int64_t cols, const void* W, const void* x,
+               int x_dtype, float* y, int batch, cudaStream_t stream) {
+  MatrixRef m;
+  int st = make_ref(wtype, scale_dtype, rows, cols, W, &m);
+  if (st != QMV_OK) return st;
+  if (x_dtype != QMV_X_F32 && x_dtype != QMV_X_BF16) return QMV_E_FORMAT;
+  if (batch < 0) return QMV_E_ARG;
+  if (batch == 0) return QMV_OK;
+  if (x == nullptr || y == nullptr) return QMV_E_ARG;
+  if (!aligned(x, 16) || !aligned(y, 4)) return QMV_E_ALIGN;
+  if (rows > INT64_MAX / batch) return QMV_E_SHAPE;
+  DeviceInfo dev;
+  if (current_device_info(&dev) != cudaSuccess) return QMV_E_CUDA;
+  const bool xb = x_dtype == QMV_X_BF16;
+  const size_t xsz = xb ? 2 : 4;
+  const bool fast = matvec_mma_supported(m);
+  for (int b0 = 0; b0 < batch; b0 += 8) {
+    const int nb = (batch - b0) < 8 ? (batch - b0) : 8;
+    const void* xp = static_cast<const uint8_t*>(x) + (size_t)b0 * (size_t)cols * xsz;
+    float* yp = y + (size_t)b0 * (size_t)rows;
+    const cudaError_t err = fast ? launch_matvec_mma(m, xp, xb, yp, nb, dev, stream)
+                                 : launch_matvec_simple(m, xp, xb, yp, nb, dev, stream);
+    if (err != cudaSuccess) return QMV_E_CUDA;
+  }
+  return QMV_OK;
+}
+
+int qmv_dequant(int wtype, int scale_dtype, int64_t rows, int64_t cols, const void* W, float* out,
+                cudaStream_t stream) {
+  MatrixRef m;
+  int st = make_ref(wtype, scale_dtype, rows, cols, W, &m);
+  if (st != QMV_OK) return st;
+  if (out == nullptr) return QMV_E_ARG;
+  if (!aligned(out, 16)) return QMV_E_ALIGN;
+  return launch_dequant(m, out, stream) == cudaSuccess ? QMV_OK : QMV_E_CUDA;
+}
+
+int qmv_validate(int wtype, int scale_dtype, int64_t rows, int64_t cols, const void* W, int64_t* first_bad,
+                 cudaStream_t stream) {
+  MatrixRef m;
+  int st = make_ref(wtype, scale_dtype, rows, cols, W, &m);
+  if (st != QMV_OK) return st;
+  if (first_bad == nullptr) return QMV_E_ARG;
+  if (!aligned(first_bad, 8)) return QMV_E_ALIGN;
+  return launch_validate(m, first_bad, stream) == cudaSuccess ? QMV_OK : QMV_E_CUDA;
+}
+
+int qmv_check_device(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return QMV_E_CUDA;
+  DeviceInfo dev;
+  if (current_device_info(&dev) != cudaSuccess) return QMV_E_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return QMV_E_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return QMV_E_CUDA;
+  }
+  return v;
+}
+
+const char* qmv_strerror(int status) {
+  switch (status) {
+    case QMV_OK: return "ok";
+    case QMV_E_FORMAT: return "format error (unknown wtype/scale/x dtype, or an invalid quant)";
+    case QMV_E_SHAPE: return "shape error (zero dimension, cols not a multiple of 32, or size overflow)";
+    case QMV_E_ARG: return "invalid argument (null pointer or negative batch)";
+    case QMV_E_ALIGN: return "misaligned pointer (W and x need 16 bytes, y 4, out 16, first_bad 8)";
+    case QMV_E_CUDA: return "CUDA error (launch failed, no device, or no sm_103a device)";
+    case QMV_E_TIMEOUT: return "a kernel's bounded wait ran out; its output is incomplete";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,175 @@
+// qmv_common.cuh -- device helpers shared by the libqmv kernels (sm_103a).
+//
+// Format facts used throughout (Krafla ".mlb model format v1", "Body", "Q8_0", "Q4_0"):
+//   q array first, d array at round_up(q bytes, 64); one scale per 32 consecutive
+//   weights of a row; Q4_0 block = 16 bytes, byte j = element j (low nibble) and
+//   element j+16 (high nibble), weight (nibble - 8) * d; Q8_0 weight = int8 * d.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/qmv.h"
+
+namespace qmv {
+
+// A kernel whose bounded wait runs out records QMV_E_TIMEOUT in the per-device status word
+// (passed to it as a pointer) and returns; qmv_check_device() reads and clears it.
+__device__ __forceinline__ void record_status(int* status, int code) { atomicCAS(status, 0, code); }
+
+// ---------------------------------------------------------------------------- numbers
+__device__ __forceinline__ float f16_bits_to_f32(uint16_t h) {
+  return __half2float(__ushort_as_half(h));
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+
+// ---------------------------------------------------------------------------- smem / PTX
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of an mbarrier, giving up after about `limit_cycles` SM cycles.
+// Returns false on time-out (the caller records QMV_E_TIMEOUT and unwinds).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  long long limit_cycles = 4000000000LL) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (clock64() - t0 > limit_cycles) return false;
+  }
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// L2 policy for data read exactly once (the weight stream): evict first.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// Bulk (non-tensor) asynchronous copy global -> shared, completion counted in bytes on an
+// mbarrier.  dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst_smem, const void* src_gmem, uint32_t bytes,
+                                             uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst_smem)),
+      "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// ldmatrix: four 8x8 matrices of 16-bit elements; lane l supplies the address of row
+// (l % 8) of matrix (l / 8); thread (g = lane/4, t = lane%4) receives, for each matrix,
+// the 32-bit word t of row g.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3,
+                                            uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// D = A(16x16 bf16, row) * B(16x8 bf16, col) + C, f32 accumulate.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1, const float (&c)[4]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%10, %11, %12, %13};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t lop_and_or(uint32_t a, uint32_t mask, uint32_t orv) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(mask), "r"(orv));  // (a & b) | c
+  return r;
+}
+
+// bf16x2 a - b (exact here: both operands are small integers).
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// Four Q4_0 quant bytes (bytes i = 0..3 of one 32-bit word, nibbles lo_i / hi_i) to
+// exact bfloat16 levels (nibble - 8), packed in pairs:
+//   p0 = (lo0, lo2)  p1 = (hi0, hi2)  p2 = (lo1, lo3)  p3 = (hi1, hi3)   (low half first)
+// 0x4300 | n is the bfloat16 of 128 + n (n < 16 sits in the mantissa), and
+// (128 + n) - 136 = n - 8 is exact.
+__device__ __forceinline__ void q4_word_to_bf16_levels(uint32_t w, uint32_t& p0, uint32_t& p1, uint32_t& p2,
+                                                       uint32_t& p3) {
+  constexpr uint32_t kMask = 0x000F000Fu;
+  constexpr uint32_t kMagic = 0x43004300u;   // bf16 128.0 in both halves
+  constexpr uint32_t kOffset = 0x43084308u;  // bf16 136.0 in both halves
+  p0 = bf16x2_sub(lop_and_or(w, kMask, kMagic), kOffset);
+  p1 = bf16x2_sub(lop_and_or(w >> 4, kMask, kMagic), kOffset);
+  p2 = bf16x2_sub(lop_and_or(w >> 8, kMask, kMagic), kOffset);
+  p3 = bf16x2_sub(lop_and_or(w >> 12, kMask, kMagic), kOffset);
+}
+
+// Four Q8_0 quant bytes q0..q3 (one word) to exact bfloat16 levels in pairs
+//   p0 = (q0, q2)  p2 = (q1, q3)
+// via float32: 0x4B000000 | u is 2^23 + u; with u = q + 128 the float32 subtraction of
+// 2^23 + 128 gives q exactly, and an integer of magnitude <= 128 is exact in bfloat16,
+// so its bfloat16 code is the upper half of its float32 code.
+__device__ __forceinline__ void q8_word_to_bf16_levels(uint32_t w, uint32_t& p0, uint32_t& p2) {
+  const uint32_t u = w ^ 0x80808080u;  // q + 128 in each byte
+  const float bias = 8388736.0f;       // 2^23 + 128
+  const float f0 = __uint_as_float(prmt(u, 0x4B000000u, 0x7440)) - bias;
+  const float f1 = __uint_as_float(prmt(u, 0x4B000000u, 0x7441)) - bias;
+  const float f2 = __uint_as_float(prmt(u, 0x4B000000u, 0x7442)) - bias;
+  const float f3 = __uint_as_float(prmt(u, 0x4B000000u, 0x7443)) - bias;
+  p0 = prmt(__float_as_uint(f0), __float_as_uint(f2), 0x7632);
+  p2 = prmt(__float_as_uint(f1), __float_as_uint(f3), 0x7632);
+}
+
+// Round-to-nearest-even bfloat16 pair from two floats: low half from lo, high half from hi.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+}  // namespace qmv

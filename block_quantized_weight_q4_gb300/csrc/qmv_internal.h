@@ -1,0 +1,42 @@
+// qmv_internal.h -- launchers shared between the libqmv translation units (host side).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace qmv {
+
+// Validated description of one matrix image (see include/qmv.h).
+struct MatrixRef {
+  int wtype;        // QMV_Q8_0 or QMV_Q4_0
+  int scale_f16;    // 0: f32 scales, 1: f16 scales
+  int64_t rows;
+  int64_t cols;     // multiple of 32
+  const uint8_t* q; // q array (device)
+  const uint8_t* d; // d array (device) = q + round_up(q bytes, 64)
+};
+
+struct DeviceInfo {
+  int device;
+  int sm_count;
+  int cc_major, cc_minor;
+  size_t smem_optin;
+  int* status;  // device address of this device's status word
+};
+
+// Cached properties of the current device.
+cudaError_t current_device_info(DeviceInfo* info);
+
+cudaError_t launch_dequant(const MatrixRef& m, float* out, cudaStream_t stream);
+cudaError_t launch_validate(const MatrixRef& m, int64_t* first_bad, cudaStream_t stream);
+
+// Any shape with cols % 32 == 0; batch 1..8 per call.
+cudaError_t launch_matvec_simple(const MatrixRef& m, const void* x, bool x_bf16, float* y, int batch,
+                                 const DeviceInfo& dev, cudaStream_t stream);
+
+// cols % 256 == 0; batch 1..8 per call.
+bool matvec_mma_supported(const MatrixRef& m);
+cudaError_t launch_matvec_mma(const MatrixRef& m, const void* x, bool x_bf16, float* y, int batch,
+                              const DeviceInfo& dev, cudaStream_t stream);
+
+}  // namespace qmv

@@ -1,0 +1,101 @@
+"""The C-ABI library on the CPU: it builds, loads, exports every declared symbol, and its
+host-only logic (sizes, class dispatch, argument checks) behaves as include/qmv.h states.
+No test here launches a kernel: every call with device pointers fails its checks first."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+from block_quantized_weight_q4_gb300 import binding
+from block_quantized_weight_q4_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return binding.load_library()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "qmv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(qmv_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert "qmv_matvec" in names and "qmv_dequant" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_weight_bytes_agree_with_oracle(lib):
+    for wt in (1, 2):
+        for sf in (0, 1):
+            for rows, cols in [(1, 32), (3, 96), (7, 64), (256, 256), (151936, 896), (4096, 11008)]:
+                assert binding.weight_bytes(wt, sf, rows, cols) == oracle.weight_bytes(wt, sf, rows, cols)
+                assert binding.scale_offset(wt, sf, rows, cols) == oracle.scale_offset(wt, sf, rows, cols)
+
+
+@pytest.mark.parametrize("args", [(2, 1, 1, 48), (2, 1, 0, 32), (2, 1, 1, 0), (1, 0, -1, 32),
+                                  (3, 0, 1, 32), (2, 2, 1, 32), (2, 1, 2**40, 2**40)])
+def test_weight_bytes_invalid(lib, args):
+    assert binding.weight_bytes(*args) == 0
+    assert binding.scale_offset(*args) == -1
+
+
+def test_q8_mask_dispatch(lib):
+    # Krafla header offset 72: classes with their bit set are Q8_0 in a Q4_0 file.
+    m = binding.matrix_wtype
+    assert m(2, 2, 2) == 1 and m(2, 2, 4) == 2 and m(2, 0, 2) == 2
+    assert m(2, 4 | 64, 4) == 1 and m(2, 4 | 64, 64) == 1 and m(2, 4 | 64, 32) == 2
+    # a Q8_0 file stores everything as Q8_0
+    assert all(m(1, 0, c) == 1 for c in (1, 2, 4, 8, 16, 32, 64))
+    # shared classifier: tok_emb is Q8_0 if bit 1 or bit 2 is set
+    assert m(2, 2, 1, True) == 1 and m(2, 2, 1, False) == 2 and m(2, 1, 1, True) == 1
+    assert m(2, 0, 3) == -1 and m(5, 0, 2) == -1
+
+
+FAKE = 0x10000  # never dereferenced: every call below fails its host checks first
+
+
+def call_matvec(lib, wt=2, sf=1, rows=64, cols=64, W=FAKE, x=FAKE, xd=1, y=FAKE, batch=1):
+    return lib.qmv_matvec(wt, sf, rows, cols, W, x, xd, y, batch, None)
+
+
+def test_matvec_argument_errors(lib):
+    assert call_matvec(lib, wt=3) == binding.E_FORMAT
+    assert call_matvec(lib, sf=2) == binding.E_FORMAT
+    assert call_matvec(lib, xd=2) == binding.E_FORMAT
+    assert call_matvec(lib, cols=48) == binding.E_SHAPE
+    assert call_matvec(lib, rows=0) == binding.E_SHAPE
+    assert call_matvec(lib, rows=2**40, cols=2**40) == binding.E_SHAPE
+    assert call_matvec(lib, W=0) == binding.E_ARG
+    assert call_matvec(lib, x=0) == binding.E_ARG
+    assert call_matvec(lib, y=0) == binding.E_ARG
+    assert call_matvec(lib, batch=-1) == binding.E_ARG
+    assert call_matvec(lib, W=FAKE + 8) == binding.E_ALIGN
+    assert call_matvec(lib, x=FAKE + 4) == binding.E_ALIGN
+    assert call_matvec(lib, y=FAKE + 2) == binding.E_ALIGN
+    # an empty batch is a no-op, checked before any device work
+    assert call_matvec(lib, batch=0, x=0, y=0) == binding.OK
+
+
+def test_dequant_and_validate_argument_errors(lib):
+    assert lib.qmv_dequant(2, 1, 64, 48, FAKE, FAKE, None) == binding.E_SHAPE
+    assert lib.qmv_dequant(2, 1, 64, 64, FAKE, 0, None) == binding.E_ARG
+    assert lib.qmv_dequant(2, 1, 64, 64, FAKE, FAKE + 4, None) == binding.E_ALIGN
+    assert lib.qmv_dequant(0, 1, 64, 64, FAKE, FAKE, None) == binding.E_FORMAT
+    assert lib.qmv_validate(1, 0, 64, 64, FAKE, 0, None) == binding.E_ARG
+    assert lib.qmv_validate(1, 0, 64, 64, FAKE, FAKE + 4, None) == binding.E_ALIGN
+    assert lib.qmv_validate(1, 0, 0, 64, FAKE, FAKE, None) == binding.E_SHAPE
+
+
+def test_strerror_never_null(lib):
+    for s in (0, 2, 3, 4, 5, 6, 7, 99, -1):
+        assert isinstance(lib.qmv_strerror(s), bytes) and lib.qmv_strerror(s)

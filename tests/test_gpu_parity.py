@@ -1,0 +1,238 @@
+"""CUDA path vs the CPU oracle, through the C ABI (libqmv.so via the ctypes binding).
+
+Bars: dequantization bit-exact; products within |y_gpu - y_ref| <= 1e-3 * sum_c |w x| per
+element (exactly equal where that sum is 0); where every partial sum is exactly
+representable (one-hot x, integer x with power-of-two scales) the product is bit-exact.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from block_quantized_weight_q4_gb300 import inputs
+from helpers import assert_bits_equal, check_product, dev_u8, dev_x
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def qmv():
+    import torch
+    from block_quantized_weight_q4_gb300.build import build
+    import block_quantized_weight_q4_gb300 as q
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    build()
+    q.load_library()
+    yield q
+    assert q.last_error() == 0
+
+
+def gpu_dequant(q, m):
+    return q.dequant(m.wtype, m.scale_f16, m.rows, m.cols, dev_u8(m.W)).cpu().numpy()
+
+
+def gpu_matvec(q, m, x):
+    import torch
+    y = q.matvec(m.wtype, m.scale_f16, m.rows, m.cols, dev_u8(m.W), dev_x(x))
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+SHAPES = [(1, 32), (3, 96), (7, 64), (33, 256), (17, 160), (64, 1024), (100, 4096), (5, 11008)]
+TYPES = [(1, 0), (1, 1), (2, 0), (2, 1)]
+
+
+# ---------------------------------------------------------------- dequant
+@pytest.mark.parametrize("wt,sf", TYPES)
+@pytest.mark.parametrize("rows,cols", SHAPES)
+def test_dequant_bit_exact(qmv, wt, sf, rows, cols):
+    m = inputs.make_matrix(wt, sf, rows, cols, seed=rows + cols + 10 * wt + sf)
+    assert_bits_equal(gpu_dequant(qmv, m), oracle.dequant(m.W, wt, sf, rows, cols), f"{wt},{sf},{rows}x{cols}")
+
+
+@pytest.mark.parametrize("wt,sf", TYPES)
+def test_dequant_special_scales(qmv, wt, sf):
+    # "Any d and nibbles are valid input": negative, zero, subnormal, huge, inf, NaN scales
+    rows, cols = 4, 256
+    m = inputs.make_matrix(wt, sf, rows, cols, seed=5)
+    if sf:
+        specials = np.array([0x8000, 0x0000, 0x0001, 0x03FF, 0x7BFF, 0xFBFF, 0x7C00, 0xFC00, 0x7E00,
+                             0x3C00, 0xBC00, 0x0400, 0x8001, 0x2E66, 0x1234, 0x7FFF], np.uint16)
+    else:
+        specials = np.array([-0.0, 0.0, 1e-45, 1.1754942e-38, 3.4028235e38, -3.4028235e38, np.inf, -np.inf,
+                             np.nan, 1.0, -1.0, 1.1754944e-38, -1e-45, 0.1, 7e-39, 1e-40], np.float32).view(np.uint32)
+    codes = m.d_codes.reshape(-1).copy()
+    codes[:specials.size] = specials
+    W = inputs.assemble(wt, sf, rows, cols, m.q, codes)
+    m2 = inputs.Matrix(wt, sf, rows, cols, W, m.q, codes)
+    assert_bits_equal(gpu_dequant(qmv, m2), oracle.dequant(W, wt, sf, rows, cols), "special scales")
+
+
+# ---------------------------------------------------------------- products
+@pytest.mark.parametrize("wt,sf", TYPES)
+@pytest.mark.parametrize("rows,cols", SHAPES)
+@pytest.mark.parametrize("xbf16", [True, False])
+@pytest.mark.parametrize("batch", [1, 3, 8, 11])
+def test_matvec_tolerance(qmv, wt, sf, rows, cols, xbf16, batch):
+    m = inputs.make_matrix(wt, sf, rows, cols, seed=rows * 3 + cols + wt)
+    x = inputs.make_x(batch, cols, xbf16, seed=rows + batch)
+    y_ref, absref = oracle.matvec(m.W, wt, sf, rows, cols, x)
+    check_product(gpu_matvec(qmv, m, x), y_ref, absref, TOL, f"{wt},{sf},{rows}x{cols},b{batch}")
+
+
+@pytest.mark.parametrize("wt,sf", TYPES)
+@pytest.mark.parametrize("rows,cols", [(16, 256), (21, 512), (3, 96), (40, 1024)])
+@pytest.mark.parametrize("xbf16", [True, False])
+def test_matvec_exact_integer_pow2(qmv, wt, sf, rows, cols, xbf16):
+    # integer x in [-4, 4], d = 2^e with e in [-4, 0]: every partial sum is a multiple of
+    # 2^-4 well below 2^20, exact in float32 in any order, so the result is bit-exact.
+    rng = np.random.default_rng(rows + cols)
+    m = inputs.make_matrix(wt, sf, rows, cols, seed=7)
+    codes = inputs.pow2_scales(rng, rows * cols // 32, sf)
+    W = inputs.assemble(wt, sf, rows, cols, m.q, codes)
+    m2 = inputs.Matrix(wt, sf, rows, cols, W, m.q, codes)
+    x = inputs.make_int_x(8, cols, xbf16, seed=3)
+    y_ref, _ = oracle.matvec(W, wt, sf, rows, cols, x)
+    y = gpu_matvec(qmv, m2, x)
+    assert np.array_equal(y.astype(np.float64), y_ref)
+
+
+@pytest.mark.parametrize("wt,sf", TYPES)
+@pytest.mark.parametrize("cols", [96, 512])
+def test_matvec_one_hot_is_dequant(qmv, wt, sf, cols):
+    # x = e_c: one non-zero term, so y[b][r] is level * d rounded once: the dequantized weight.
+    rows = 37
+    m = inputs.make_matrix(wt, sf, rows, cols, seed=cols)
+    picks = [0, 5, 31, 32, cols - 1, cols // 2, 17, cols - 33]
+    x = np.zeros((8, cols), np.float32)
+    for b, c in enumerate(picks):
+        x[b, c] = 1.0
+    deq = oracle.dequant(m.W, wt, sf, rows, cols)
+    for xb in (x, inputs.bf16_codes(x)):
+        y = gpu_matvec(qmv, m, xb)
+        assert_bits_equal(y, deq[:, picks].T, "one-hot")
+
+
+@pytest.mark.parametrize("wt", [1, 2])
+def test_zero_level_rows_give_exact_zero(qmv, wt):
+    # rows whose levels are all 0 have sum |w x| = 0: the product must be exactly 0
+    rows, cols = 24, 512
+    m = inputs.make_matrix(wt, 1, rows, cols, seed=2)
+    q = m.q.copy().reshape(rows, -1)
+    q[::3] = 0x88 if wt == 2 else 0x00
+    W = inputs.assemble(wt, 1, rows, cols, q.reshape(-1), m.d_codes)
+    m2 = inputs.Matrix(wt, 1, rows, cols, W, q.reshape(-1), m.d_codes)
+    x = inputs.make_x(4, cols, True, seed=1)
+    y_ref, absref = oracle.matvec(W, wt, 1, rows, cols, x)
+    y = gpu_matvec(qmv, m2, x)
+    assert np.all(y[:, ::3] == 0.0)
+    check_product(y, y_ref, absref, TOL, "zero rows")
+
+
+def test_q8_minus_128_decodes_faithfully(qmv):
+    # -128 is not rejected by the product (only by validate); it decodes as -128 * d.
+    rows, cols = 16, 256
+    m = inputs.make_matrix(1, 0, rows, cols, seed=4)
+    q = m.q.copy()
+    q[::7] = 0x80
+    W = inputs.assemble(1, 0, rows, cols, q, m.d_codes)
+    m2 = inputs.Matrix(1, 0, rows, cols, W, q, m.d_codes)
+    x = inputs.make_x(2, cols, True, seed=2)
+    y_ref, absref = oracle.matvec(W, 1, 0, rows, cols, x)
+    check_product(gpu_matvec(qmv, m2, x), y_ref, absref, TOL, "q8 -128")
+    assert_bits_equal(gpu_dequant(qmv, m2), oracle.dequant(W, 1, 0, rows, cols), "q8 -128 dequant")
+
+
+def test_output_guards_untouched(qmv):
+    import torch
+    for wt, rows, cols in [(2, 37, 512), (1, 5, 96), (2, 33, 4096)]:
+        m = inputs.make_matrix(wt, 1, rows, cols, seed=9)
+        x = dev_x(inputs.make_x(3, cols, True, seed=9))
+        buf = torch.full((3 * rows + 64,), 12345.0, dtype=torch.float32, device="cuda")
+        y = buf[32:32 + 3 * rows].view(3, rows)
+        qmv.matvec(wt, 1, rows, cols, dev_u8(m.W), x, y)
+        torch.cuda.synchronize()
+        b = buf.cpu().numpy()
+        assert np.all(b[:32] == 12345.0) and np.all(b[32 + 3 * rows:] == 12345.0)
+
+
+def test_batch_zero_is_noop(qmv):
+    import torch
+    m = inputs.make_matrix(2, 1, 16, 256, seed=1)
+    x = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    y = torch.full((0, 16), 1.0, device="cuda")
+    qmv.matvec(2, 1, 16, 256, dev_u8(m.W), x, y)
+    torch.cuda.synchronize()
+
+
+def test_nonfinite_scales_propagate_in_products(qmv):
+    rows, cols = 16, 256
+    m = inputs.make_matrix(2, 0, rows, cols, seed=3)
+    codes = m.d_codes.reshape(-1).copy()
+    codes[0] = np.array([np.inf], np.float32).view(np.uint32)[0]      # row 0 block 0
+    codes[8 * 3 + 1] = np.array([np.nan], np.float32).view(np.uint32)[0]  # row 3 block 1
+    W = inputs.assemble(2, 0, rows, cols, m.q, codes)
+    m2 = inputs.Matrix(2, 0, rows, cols, W, m.q, codes)
+    x = inputs.make_x(1, cols, True, seed=1)
+    y_ref, absref = oracle.matvec(W, 2, 0, rows, cols, x)
+    y = gpu_matvec(qmv, m2, x)
+    assert np.isnan(y[0, 3]) and np.isnan(y_ref[0, 3])
+    assert (np.isinf(y[0, 0]) or np.isnan(y[0, 0])) and (np.isinf(y_ref[0, 0]) or np.isnan(y_ref[0, 0]))
+    ok = np.ones(rows, bool)
+    ok[[0, 3]] = False
+    check_product(y[:, ok], y_ref[:, ok], absref[:, ok], TOL, "finite rows")
+
+
+# ---------------------------------------------------------------- validate
+def test_validate_finds_first_minus_128(qmv):
+    m = inputs.make_matrix(1, 0, 64, 1024, seed=1)
+    assert qmv.validate(1, 0, 64, 1024, dev_u8(m.W)) == -1
+    W = m.W.copy()
+    W[[70000, 5000, 65535]] = 0x80
+    assert qmv.validate(1, 0, 64, 1024, dev_u8(W)) == 5000
+    assert oracle.validate(W, 1, 0, 64, 1024) == oracle.E_FORMAT
+    m4 = inputs.make_matrix(2, 0, 64, 1024, seed=1)
+    W4 = m4.W.copy()
+    W4[:100] = 0x80
+    assert qmv.validate(2, 0, 64, 1024, dev_u8(W4)) == -1
+
+
+# ---------------------------------------------------------------- full-size workloads
+def sample_rows(rows, rng, n=24):
+    ids = set(range(min(8, rows))) | set(range(max(0, rows - 8), rows))
+    ids |= set(rng.integers(0, rows, n).tolist())
+    return np.array(sorted(ids), dtype=np.int64)
+
+
+@pytest.mark.parametrize("name", ["q8_256", "q4_4096", "llama7b", "mixed_qwen", "prefill"])
+def test_workload_full_size(qmv, name):
+    """Every matrix of the workload at its full size, every batch size it names, through
+    the same calls the benchmark times; checked on sampled rows (first, last, random)."""
+    import torch
+    wl = inputs.WORKLOADS[name]
+    rng = np.random.default_rng(17)
+    for i, spec in enumerate(wl.matrices):
+        wt = spec.wtype
+        if wl.q8_mask:
+            wt = qmv.matrix_wtype(wl.file_wtype, wl.q8_mask, spec.cls)
+            assert wt == spec.wtype
+        m = inputs.make_matrix(wt, spec.scale_f16, spec.rows, spec.cols, seed=inputs.matrix_seed(name, i))
+        Wd = dev_u8(m.W)
+        ids = sample_rows(spec.rows, rng)
+        xdt = [wl.x_bf16] + ([False] if wl.extra_x_f32 else [])
+        for xb in xdt:
+            for batch in wl.batches:
+                x = inputs.make_x(batch, spec.cols, xb, seed=inputs.x_seed(name, i))
+                y = qmv.matvec(wt, spec.scale_f16, spec.rows, spec.cols, Wd, dev_x(x))
+                torch.cuda.synchronize()
+                y_ref, absref = oracle.matvec_rows(m.W, wt, spec.scale_f16, spec.rows, spec.cols, x, ids)
+                check_product(y.cpu().numpy()[:, ids], y_ref, absref, TOL, f"{name}/{spec.name}/b{batch}")
+        # dequant of the sampled rows, bit-exact
+        out = qmv.dequant(wt, spec.scale_f16, spec.rows, spec.cols, Wd)
+        sub_q = m.q.reshape(spec.rows, -1)[ids].reshape(-1)
+        sub_d = m.d_codes[ids].reshape(-1)
+        sub = inputs.assemble(wt, spec.scale_f16, ids.size, spec.cols, sub_q, sub_d)
+        assert_bits_equal(out[torch.from_numpy(ids).cuda()].cpu().numpy(), oracle.dequant(sub, wt, spec.scale_f16, ids.size, spec.cols),
+                          f"{name}/{spec.name} dequant")
+        del Wd, out
