@@ -4,22 +4,30 @@
 //   y[n][r] = sum_k d[r][k] * sum_{j<32} level[r][32k+j] * x[n][32k+j]
 // with level = nibble - 8 (Q4_0) or the int8 quant (Q8_0), d the block's scale.
 //
-// How (one warp = one tile of 16 rows x a slice of the columns):
-//   * Weight stream.  Each warp owns a ring of S shared-memory stages.  A stage holds 16
-//     rows x 256 weights of q plus their 8 scales per row; the 32 lanes each issue one
-//     cp.async.bulk per stage (lanes 0-15 the q runs of rows 0-15, lanes 16-31 their scale
-//     runs), completing on the stage's mbarrier.  S-1 stages are always in flight.
-//   * Unpack.  ldmatrix hands thread (g = lane/4, t = lane%4) the 4 quant bytes 4t..4t+3 of
-//     a block for row g and for row g+8.  They become exact bfloat16 levels in registers
-//     (Q4_0: 0x4300|nibble = 128+n, minus 136; Q8_0: via the float32 2^23 trick).
+// How:
+//   * Work.  A warp owns tiles of 16*MT rows (MT = 2 for Q4_0, 1 for Q8_0: one or two 16-row
+//     MMA tiles sharing the activation fragments); the columns are cut into chunks of 256
+//     weights (8 blocks).  A CTA of 4 warps takes items of (4/ks) tiles x ks column slices
+//     and walks its items persistently (item = blockIdx.x, + gridDim.x, ...); each warp sees
+//     one continuous stream of stages across its items.
+//   * Streams.  Each warp has its own ring of S shared-memory stages.  Lane 0 fills a stage
+//     with 2-D TMA loads: the (16*MT)-row x 128-byte q box (128-byte swizzle; two boxes for
+//     Q8_0), the (16*MT)-row x 8-scale d box, and the batch x 256 activation box.  Rows past
+//     the end of the matrix read as zeros and are never stored.
+//   * Unpack.  ldmatrix (addresses swizzled like the TMA box) hands thread (g = lane/4,
+//     t = lane%4) the 4 quant bytes 4t..4t+3 of a block for rows g and g+8.  They become
+//     exact bfloat16 levels in registers (Q4_0: 0x4300|nibble = 128+n, minus 136; Q8_0:
+//     through the float32 2^23 trick), paired as elements (4t, 4t+1) and (4t+2, 4t+3).
 //   * Block dot.  Per block, two m16n8k16 bf16 MMAs (elements 0-15 and 16-31 of the block)
 //     into a zeroed f32 fragment give sum_j level*x for 16 rows x 8 activation vectors.
-//     Inside an MMA the k order is permuted (slot 2t <-> element 4t, 2t+1 <-> 4t+2,
-//     2t+8 <-> 4t+1, 2t+9 <-> 4t+3); the B fragment (x) uses the same permutation.
-//   * Scale and accumulate.  acc += d[row][block] * fragment, in float32 FFMA.
-//   * Split-K.  The warps of a CTA that share a tile add their partial sums through shared
+//     Inside an MMA, k slots (2t, 2t+1, 2t+8, 2t+9) hold elements (4t .. 4t+3) of the half
+//     block, for A and B alike, so thread t's B fragment is the 8 contiguous bytes
+//     x[n][4t .. 4t+3] of vector n = g: one shared-memory load.  Lanes whose g is past the
+//     batch read a zero area instead.
+//   * Scale and accumulate.  acc += d[row][block] * fragment, float32 FFMA.
+//   * Split-K.  Warps of one item that share a tile add their partial sums through shared
 //     memory in a fixed order; one warp writes y.
-// f32 activations are split x = hi + lo (two bfloat16s, hi = RN(x)) and take two MMAs,
+// f32 activations are split x = hi + lo (two bfloat16s, hi = RN(x)) and take two MMAs each,
 // which keeps 16 significant bits of x.
 #include "qmv_common.cuh"
 #include "qmv_internal.h"
@@ -28,295 +36,393 @@ namespace qmv {
 
 namespace {
 
-constexpr int kWarps = 4;     // warps per CTA
-constexpr int kTK = 256;      // weights per stage and row
+constexpr int kWarps = 4;            // warps per CTA
+constexpr int kTK = 256;             // weights per stage and row
 constexpr int kBlocksPerStage = kTK / 32;
+constexpr int kRows = 16;            // rows per MMA tile
+constexpr int kBox = 128;            // q box inner extent in bytes (the 128-byte swizzle span)
+constexpr int kMaxBatch = 8;         // activation vectors per pass (the MMA's N)
 
-template <int WT, bool F16>
+template <int WT, bool F16, bool XBF16>
 struct Cfg {
-  static constexpr int QROW = (WT == QMV_Q4_0) ? kTK / 2 : kTK;  // q bytes per row per stage
-  static constexpr int QPITCH = QROW + 16;                       // padded: conflict-free ldmatrix
-  static constexpr int DROW = kBlocksPerStage * (F16 ? 2 : 4);   // scale bytes per row per stage
-  static constexpr int STAGE_BYTES = 16 * QPITCH + 16 * DROW;
-  static constexpr int S = (WT == QMV_Q4_0) ? 6 : 4;             // ring depth
-  static constexpr int WARP_BYTES = S * STAGE_BYTES;
-  static constexpr int RED_BYTES = kWarps * 16 * 8 * 4;
-  static constexpr int SMEM_BYTES = kWarps * WARP_BYTES + RED_BYTES + kWarps * S * 8;
+  static constexpr int MT = (WT == QMV_Q4_0) ? 2 : 1;           // 16-row MMA tiles per warp tile
+  static constexpr int WROWS = MT * kRows;                        // rows per warp tile
+  static constexpr int NQBOX = (WT == QMV_Q4_0) ? 1 : 2;        // q boxes per stage
+  static constexpr int Q_BOX_BYTES = WROWS * kBox;
+  static constexpr int Q_STAGE = NQBOX * Q_BOX_BYTES;             // bytes, multiple of 1024
+  static constexpr int QROW = NQBOX * kBox;                        // q bytes per row per stage
+  static constexpr int DROW = kBlocksPerStage * (F16 ? 2 : 4);    // scale bytes per row per stage
+  static constexpr int D_STAGE = WROWS * DROW;                     // multiple of 128
+  static constexpr int XROW = kTK * (XBF16 ? 2 : 4);              // activation bytes per vector per stage
+  static constexpr int S = 3;                                      // ring depth
+  static constexpr int Q_WARP = S * Q_STAGE;
+  static constexpr int D_WARP = S * D_STAGE;
+  static constexpr int RED_FLOATS = kWarps * WROWS * 8;
+  static constexpr int ZERO_BYTES = 128;
+  // fixed part: q rings, d rings, zero area, reduction buffer, barriers; the activation
+  // rings (S x batch x XROW per warp) follow
+  static constexpr int OFF_D = kWarps * Q_WARP;
+  static constexpr int OFF_ZERO = OFF_D + kWarps * D_WARP;
+  static constexpr int OFF_RED = OFF_ZERO + ZERO_BYTES;
+  static constexpr int OFF_BAR = OFF_RED + RED_FLOATS * 4;
+  static constexpr int OFF_X = OFF_BAR + ((kWarps * S * 8 + 127) / 128) * 128;
+  static int smem_bytes(int batch) { return 1024 + OFF_X + kWarps * S * batch * XROW; }
 };
 
 struct Params {
-  const uint8_t* q;
-  const uint8_t* d;
-  const void* x;
   float* y;
-  int64_t rows;
-  int64_t cols;
+  int rows;
+  int cols;
   int batch;    // 1..8
-  int64_t ntiles;
-  int ks;       // k-slices per tile (1, 2, 4)
-  int* status;  // per-device status word
+  int ntiles;
+  int nchunks;  // cols / 256
+  int ks;       // column slices per tile (1, 2, 4)
+  int nitems;
+  int* status;
 };
 
-// B fragments (x) for one 16-element half of block kb, batch vector n = g, permuted to
-// match the A fragment's k order.
-template <bool XBF16>
-__device__ __forceinline__ void load_b(const Params& p, int g, int t, int64_t kb, int half, uint32_t (&bh)[2],
-                                       uint32_t (&bl)[2]) {
-  bh[0] = bh[1] = bl[0] = bl[1] = 0u;
-  if (g >= p.batch) return;
-  const int64_t off = (int64_t)g * p.cols + kb * 32 + half * 16 + 4 * t;
-  if (XBF16) {
-    const uint2 v = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(p.x) + off));
-    bh[0] = prmt(v.x, v.y, 0x5410);  // (e0, e2)
-    bh[1] = prmt(v.x, v.y, 0x7632);  // (e1, e3)
-  } else {
-    const float4 v = __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.x) + off));
-    bh[0] = pack_bf16x2(v.x, v.z);
-    bh[1] = pack_bf16x2(v.y, v.w);
-    bl[0] = pack_bf16x2(v.x - __uint_as_float(bh[0] << 16), v.z - __uint_as_float(bh[0] & 0xFFFF0000u));
-    bl[1] = pack_bf16x2(v.y - __uint_as_float(bh[1] << 16), v.w - __uint_as_float(bh[1] & 0xFFFF0000u));
-  }
-}
-
 template <int WT, bool F16, bool XBF16>
-__global__ void __launch_bounds__(kWarps * 32) matvec_mma_kernel(const Params p) {
-  using C = Cfg<WT, F16>;
-  extern __shared__ __align__(128) uint8_t smem[];
+__global__ void __launch_bounds__(kWarps * 32) matvec_mma_kernel(const __grid_constant__ CUtensorMap tq,
+                                                                 const __grid_constant__ CUtensorMap td,
+                                                                 const __grid_constant__ CUtensorMap tx,
+                                                                 const Params p) {
+  using C = Cfg<WT, F16, XBF16>;
+  constexpr int MT = C::MT;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);  // 1024-aligned: swizzle atoms
+
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2;
   const int t = lane & 3;
 
-  uint8_t* ring = smem + warp * C::WARP_BYTES;
-  float* red = reinterpret_cast<float*>(smem + kWarps * C::WARP_BYTES);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * C::WARP_BYTES + C::RED_BYTES) + warp * C::S;
+  const int x_stage = p.batch * C::XROW;
+  uint8_t* qring = smem + warp * C::Q_WARP;
+  uint8_t* dring = smem + C::OFF_D + warp * C::D_WARP;
+  uint8_t* xring = smem + C::OFF_X + warp * C::S * x_stage;
+  uint8_t* zero = smem + C::OFF_ZERO;
+  float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + warp * C::S;
 
-  const int tiles_per_cta = kWarps / p.ks;
+  const int tiles_per_item = kWarps / p.ks;
   const int tile_local = warp / p.ks;
   const int kslice = warp % p.ks;
-  const int64_t tile = (int64_t)blockIdx.x * tiles_per_cta + tile_local;
-  const bool active = tile < p.ntiles;
-  const int64_t row0 = tile * 16;
+  const int c_begin = kslice * p.nchunks / p.ks;
+  const int per_item = (kslice + 1) * p.nchunks / p.ks - c_begin;  // >= 1 (host keeps nchunks >= ks)
+  const int my_items = (p.nitems - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+  const int total = my_items * per_item;
+  const int tile_step = (int)gridDim.x * tiles_per_item;  // tile distance between consecutive items
+  const uint32_t stage_tx = (uint32_t)(C::Q_STAGE + C::D_STAGE + x_stage);
 
-  const int64_t nchunks = p.cols / kTK;
-  const int64_t c_begin = kslice * nchunks / p.ks;
-  const int64_t c_end = (kslice + 1) * nchunks / p.ks;
-  const int niter = active ? (int)(c_end - c_begin) : 0;
-
-  const int64_t nblk = p.cols / 32;
-  const int64_t qrow_bytes = (WT == QMV_Q4_0) ? p.cols / 2 : p.cols;
-  const int nvalid = active ? (p.rows - row0 < 16 ? (int)(p.rows - row0) : 16) : 0;
-  const uint32_t stage_tx = (uint32_t)nvalid * (C::QROW + C::DROW);
-
+  if (threadIdx.x < C::ZERO_BYTES / 4) reinterpret_cast<uint32_t*>(zero)[threadIdx.x] = 0u;
   if (lane == 0) {
     for (int s = 0; s < C::S; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
+    prefetch_tmap(&tq);
+    prefetch_tmap(&td);
+    prefetch_tmap(&tx);
   }
-  __syncwarp();
+  __syncthreads();  // zero area and barriers visible
+  const uint64_t pol_stream = l2_policy_evict_first();
 
-  const uint64_t pol = l2_policy_evict_first();
-  const int my_row = lane & 15;
-  const bool my_valid = my_row < nvalid;
-
-  // issue chunk (c_begin + i) into stage i % S
-  auto issue = [&](int i) {
-    const int s = i % C::S;
-    uint8_t* st = ring + s * C::STAGE_BYTES;
-    const int64_t c = c_begin + i;
-    if (lane == 0) mbar_arrive_expect_tx(&bars[s], stage_tx);
-    __syncwarp();
-    fence_proxy_async_smem();
-    if (my_valid) {
-      const int64_t r = row0 + my_row;
-      if (lane < 16) {
-        bulk_copy_g2s(st + my_row * C::QPITCH, p.q + r * qrow_bytes + c * C::QROW, C::QROW, &bars[s], pol);
+  // producer position (lane 0 issues): ring slot, tile and chunk of the next stage
+  int ps = 0, ptile = (int)blockIdx.x * tiles_per_item + tile_local, pj = 0;
+  auto issue_next = [&]() {
+    if (lane == 0) {
+      if (ptile < p.ntiles) {
+        const int c = c_begin + pj;
+        mbar_arrive_expect_tx(&bars[ps], stage_tx);
+        fence_proxy_async_smem();
+#pragma unroll
+        for (int b = 0; b < C::NQBOX; ++b)
+          tma_load_2d(qring + ps * C::Q_STAGE + b * C::Q_BOX_BYTES, &tq, c * C::QROW + b * kBox, ptile * C::WROWS,
+                      &bars[ps], pol_stream);
+        tma_load_2d(dring + ps * C::D_STAGE, &td, c * C::DROW, ptile * C::WROWS, &bars[ps], pol_stream);
+        tma_load_2d_keep(xring + ps * x_stage, &tx, c * kTK, 0, &bars[ps]);
       } else {
-        bulk_copy_g2s(st + 16 * C::QPITCH + my_row * C::DROW,
-                      p.d + (r * nblk + c * kBlocksPerStage) * (F16 ? 2 : 4), C::DROW, &bars[s], pol);
+        mbar_arrive(&bars[ps]);  // a tile past the end: complete the phase with no data
       }
+    }
+    ps = (ps + 1 == C::S) ? 0 : ps + 1;
+    if (++pj == per_item) {
+      pj = 0;
+      ptile += tile_step;
     }
   };
 
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  const int pre = niter < C::S - 1 ? niter : C::S - 1;
-  for (int i = 0; i < pre; ++i) issue(i);
-
-  // ldmatrix row address for this lane: matrix m = lane/8 covers rows (m&1)*8 .. +7
+  // ldmatrix: lane supplies row (lane & 7) + 8 * (matrix & 1), 16-byte chunk (matrix >> 1)
   const int lm = lane >> 3;
   const int lrow = (lane & 7) + ((lm & 1) << 3);
-  const int lsub = lm >> 1;  // which 16-byte chunk of the pair
+  const int lsub = lm >> 1;
+  const int sw = lrow & 7;  // 128-byte swizzle: physical chunk = logical chunk ^ (row & 7)
+  // B fragment source of this lane: vector g of the stage's activation box, or the zero area
+  constexpr int XESZ = XBF16 ? 2 : 4;
+  const bool xlive = g < p.batch;
+  const uint32_t xblk = xlive ? 32 * XESZ : 0;   // byte step per block
+  const uint32_t xhalf = xlive ? 16 * XESZ : 0;  // byte step to elements 16..31
+  const uint32_t xlane = (xlive ? (uint32_t)(g * C::XROW) : 0u) + 4 * XESZ * t;
 
+  const int pre = total < C::S - 1 ? total : C::S - 1;
+  for (int i = 0; i < pre; ++i) issue_next();
+  int issued = pre;
+
+  float acc[MT][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
   bool failed = false;
-  for (int it = 0; it < niter; ++it) {
-    if (it + C::S - 1 < niter) issue(it + C::S - 1);
-    const int s = it % C::S;
-    if (!mbar_wait_bounded(&bars[s], (uint32_t)(it / C::S) & 1u)) {
-      record_status(p.status, QMV_E_TIMEOUT);
-      // drain this warp's other copies in flight (bounded), then stop
-      const int issued = (it + C::S - 1 < niter) ? it + C::S : niter;
-      for (int j = it + 1; j < issued; ++j) mbar_wait_bounded(&bars[j % C::S], (uint32_t)(j / C::S) & 1u);
-      failed = true;
-      break;
-    }
-    const uint8_t* st = ring + s * C::STAGE_BYTES;
-    const uint32_t qbase = smem_u32(st) + lrow * C::QPITCH + lsub * 16;
-    const uint8_t* dst = st + 16 * C::QPITCH;
-
-    // scales of rows g and g+8 for the 8 blocks of this stage, as float32
-    float dg[kBlocksPerStage], dh[kBlocksPerStage];
-    if (F16) {
-      const uint4 a = *reinterpret_cast<const uint4*>(dst + g * C::DROW);
-      const uint4 b = *reinterpret_cast<const uint4*>(dst + (g + 8) * C::DROW);
-      const uint32_t wa[4] = {a.x, a.y, a.z, a.w};
-      const uint32_t wb[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        dg[2 * k] = f16_bits_to_f32((uint16_t)(wa[k] & 0xFFFF));
-        dg[2 * k + 1] = f16_bits_to_f32((uint16_t)(wa[k] >> 16));
-        dh[2 * k] = f16_bits_to_f32((uint16_t)(wb[k] & 0xFFFF));
-        dh[2 * k + 1] = f16_bits_to_f32((uint16_t)(wb[k] >> 16));
+  int cs = 0;          // consumer ring slot
+  uint32_t phase = 0;  // its parity
+  int ctile = (int)blockIdx.x * tiles_per_item + tile_local, cj = 0;
+  for (int it = 0; it < total; ++it) {
+    const bool valid = ctile < p.ntiles;
+    if (!failed) {
+      if (it + C::S - 1 < total) {
+        issue_next();
+        issued = it + C::S;
       }
-    } else {
-      const float4* a = reinterpret_cast<const float4*>(dst + g * C::DROW);
-      const float4* b = reinterpret_cast<const float4*>(dst + (g + 8) * C::DROW);
+      if (!mbar_wait_bounded(&bars[cs], phase)) {
+        record_status(p.status, QMV_E_TIMEOUT);
+        failed = true;
+      } else if (valid) {
+        const uint32_t qs = smem_u32(qring + cs * C::Q_STAGE);
+        const uint8_t* ds = dring + cs * C::D_STAGE;
+        const uint32_t xs = (xlive ? smem_u32(xring + cs * x_stage) : smem_u32(zero)) + xlane;
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const float4 u = a[k], v = b[k];
-        dg[4 * k] = u.x; dg[4 * k + 1] = u.y; dg[4 * k + 2] = u.z; dg[4 * k + 3] = u.w;
-        dh[4 * k] = v.x; dh[4 * k + 1] = v.y; dh[4 * k + 2] = v.z; dh[4 * k + 3] = v.w;
-      }
-    }
-
-    const int64_t kb0 = (c_begin + it) * kBlocksPerStage;
-    if (WT == QMV_Q4_0) {
+        for (int bp = 0; bp < kBlocksPerStage / 2; ++bp) {
+          uint32_t w[MT][4];  // Q4_0: [tile][row g blk 2bp, row g+8 blk 2bp, row g blk 2bp+1, row g+8 blk 2bp+1]
+          if (WT == QMV_Q4_0) {
 #pragma unroll
-      for (int bp = 0; bp < kBlocksPerStage / 2; ++bp) {
-        uint32_t w[4];  // row g blk 2bp, row g+8 blk 2bp, row g blk 2bp+1, row g+8 blk 2bp+1
-        ldmatrix_x4(w[0], w[1], w[2], w[3], qbase + bp * 32);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int kbl = 2 * bp + h;
-          uint32_t ag[4], ah[4];
-          q4_word_to_bf16_levels(w[2 * h], ag[0], ag[1], ag[2], ag[3]);
-          q4_word_to_bf16_levels(w[2 * h + 1], ah[0], ah[1], ah[2], ah[3]);
-          uint32_t bh0[2], bl0[2], bh1[2], bl1[2];
-          load_b<XBF16>(p, g, t, kb0 + kbl, 0, bh0, bl0);
-          load_b<XBF16>(p, g, t, kb0 + kbl, 1, bh1, bl1);
-          float c[4] = {0.f, 0.f, 0.f, 0.f};
-          // elements 0..15 (low nibbles): A = (lo0,lo2),(lo1,lo3) of rows g / g+8
-          mma_bf16_16816(c, ag[0], ah[0], ag[2], ah[2], bh0[0], bh0[1], c);
-          // elements 16..31 (high nibbles)
-          mma_bf16_16816(c, ag[1], ah[1], ag[3], ah[3], bh1[0], bh1[1], c);
-          if (!XBF16) {
-            mma_bf16_16816(c, ag[0], ah[0], ag[2], ah[2], bl0[0], bl0[1], c);
-            mma_bf16_16816(c, ag[1], ah[1], ag[3], ah[3], bl1[0], bl1[1], c);
+            for (int mt = 0; mt < MT; ++mt)
+              ldmatrix_x4(w[mt][0], w[mt][1], w[mt][2], w[mt][3],
+                          qs + (16 * mt + lrow) * kBox + (((2 * bp + lsub) ^ sw) << 4));
           }
-          acc[0] = fmaf(dg[kbl], c[0], acc[0]);
-          acc[1] = fmaf(dg[kbl], c[1], acc[1]);
-          acc[2] = fmaf(dh[kbl], c[2], acc[2]);
-          acc[3] = fmaf(dh[kbl], c[3], acc[3]);
-        }
-      }
-    } else {
+          // scales of blocks 2bp, 2bp+1 for rows g + 16 mt (h = 0) and g + 8 + 16 mt (h = 1)
+          float dsc[MT][2][2];
 #pragma unroll
-      for (int kbl = 0; kbl < kBlocksPerStage; ++kbl) {
-        uint32_t w[4];  // row g half 0, row g+8 half 0, row g half 1, row g+8 half 1
-        ldmatrix_x4(w[0], w[1], w[2], w[3], qbase + kbl * 32);
-        uint32_t ag0[2], ah0[2], ag1[2], ah1[2];
-        q8_word_to_bf16_levels(w[0], ag0[0], ag0[1]);
-        q8_word_to_bf16_levels(w[1], ah0[0], ah0[1]);
-        q8_word_to_bf16_levels(w[2], ag1[0], ag1[1]);
-        q8_word_to_bf16_levels(w[3], ah1[0], ah1[1]);
-        uint32_t bh0[2], bl0[2], bh1[2], bl1[2];
-        load_b<XBF16>(p, g, t, kb0 + kbl, 0, bh0, bl0);
-        load_b<XBF16>(p, g, t, kb0 + kbl, 1, bh1, bl1);
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_bf16_16816(c, ag0[0], ah0[0], ag0[1], ah0[1], bh0[0], bh0[1], c);
-        mma_bf16_16816(c, ag1[0], ah1[0], ag1[1], ah1[1], bh1[0], bh1[1], c);
-        if (!XBF16) {
-          mma_bf16_16816(c, ag0[0], ah0[0], ag0[1], ah0[1], bl0[0], bl0[1], c);
-          mma_bf16_16816(c, ag1[0], ah1[0], ag1[1], ah1[1], bl1[0], bl1[1], c);
+          for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint8_t* dr = ds + (16 * mt + 8 * h + g) * C::DROW;
+              if (F16) {
+                const uint32_t v = *reinterpret_cast<const uint32_t*>(dr + 4 * bp);
+                dsc[mt][h][0] = f16_bits_to_f32((uint16_t)(v & 0xFFFF));
+                dsc[mt][h][1] = f16_bits_to_f32((uint16_t)(v >> 16));
+              } else {
+                const float2 v = *reinterpret_cast<const float2*>(dr + 8 * bp);
+                dsc[mt][h][0] = v.x;
+                dsc[mt][h][1] = v.y;
+              }
+            }
+          }
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb) {
+            const int k = 2 * bp + hb;
+            // B fragments: [half][pair]; hi/lo split for f32 activations
+            uint32_t xh[2][2], xl[2][2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t a = xs + k * xblk + h * xhalf;
+              if (XBF16) {
+                lds_u32x2(a, xh[h][0], xh[h][1]);
+              } else {
+                float v[4];
+                lds_f32x4(a, v);
+                xh[h][0] = pack_bf16x2(v[0], v[1]);
+                xh[h][1] = pack_bf16x2(v[2], v[3]);
+                xl[h][0] = pack_bf16x2(v[0] - __uint_as_float(xh[h][0] << 16),
+                                       v[1] - __uint_as_float(xh[h][0] & 0xFFFF0000u));
+                xl[h][1] = pack_bf16x2(v[2] - __uint_as_float(xh[h][1] << 16),
+                                       v[3] - __uint_as_float(xh[h][1] & 0xFFFF0000u));
+              }
+            }
+            if (WT == QMV_Q4_0) {
+#pragma unroll
+              for (int mt = 0; mt < MT; ++mt) {
+                uint32_t g01, g23, gh01, gh23, h01, h23, hh01, hh23;
+                q4_word_to_bf16_levels(w[mt][2 * hb], g01, g23, gh01, gh23);      // row g
+                q4_word_to_bf16_levels(w[mt][2 * hb + 1], h01, h23, hh01, hh23);  // row g + 8
+                float c[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_bf16_16816(c, g01, h01, g23, h23, xh[0][0], xh[0][1], c);      // elements 0..15
+                mma_bf16_16816(c, gh01, hh01, gh23, hh23, xh[1][0], xh[1][1], c);  // elements 16..31
+                if (!XBF16) {
+                  mma_bf16_16816(c, g01, h01, g23, h23, xl[0][0], xl[0][1], c);
+                  mma_bf16_16816(c, gh01, hh01, gh23, hh23, xl[1][0], xl[1][1], c);
+                }
+                acc[mt][0] = fmaf(dsc[mt][0][hb], c[0], acc[mt][0]);
+                acc[mt][1] = fmaf(dsc[mt][0][hb], c[1], acc[mt][1]);
+                acc[mt][2] = fmaf(dsc[mt][1][hb], c[2], acc[mt][2]);
+                acc[mt][3] = fmaf(dsc[mt][1][hb], c[3], acc[mt][3]);
+              }
+            } else {
+              // Q8_0: block k = chunks 2k, 2k+1 of the stage (box k / 4)
+              uint32_t q[4];  // row g half 0, row g+8 half 0, row g half 1, row g+8 half 1
+              const int chunk = 2 * (k & 3) + lsub;
+              ldmatrix_x4(q[0], q[1], q[2], q[3], qs + (k >> 2) * C::Q_BOX_BYTES + lrow * kBox + ((chunk ^ sw) << 4));
+              uint32_t g0a, g0b, h0a, h0b, g1a, g1b, h1a, h1b;
+              q8_word_to_bf16_levels(q[0], g0a, g0b);
+              q8_word_to_bf16_levels(q[1], h0a, h0b);
+              q8_word_to_bf16_levels(q[2], g1a, g1b);
+              q8_word_to_bf16_levels(q[3], h1a, h1b);
+              float c[4] = {0.f, 0.f, 0.f, 0.f};
+              mma_bf16_16816(c, g0a, h0a, g0b, h0b, xh[0][0], xh[0][1], c);
+              mma_bf16_16816(c, g1a, h1a, g1b, h1b, xh[1][0], xh[1][1], c);
+              if (!XBF16) {
+                mma_bf16_16816(c, g0a, h0a, g0b, h0b, xl[0][0], xl[0][1], c);
+                mma_bf16_16816(c, g1a, h1a, g1b, h1b, xl[1][0], xl[1][1], c);
+              }
+              acc[0][0] = fmaf(dsc[0][0][hb], c[0], acc[0][0]);
+              acc[0][1] = fmaf(dsc[0][0][hb], c[1], acc[0][1]);
+              acc[0][2] = fmaf(dsc[0][1][hb], c[2], acc[0][2]);
+              acc[0][3] = fmaf(dsc[0][1][hb], c[3], acc[0][3]);
+            }
+          }
         }
-        acc[0] = fmaf(dg[kbl], c[0], acc[0]);
-        acc[1] = fmaf(dg[kbl], c[1], acc[1]);
-        acc[2] = fmaf(dh[kbl], c[2], acc[2]);
-        acc[3] = fmaf(dh[kbl], c[3], acc[3]);
       }
+      __syncwarp();
     }
-    __syncwarp();
-  }
 
-  // split-K: partials to shared memory, fixed-order sum, coalesced store of y
-  float* my = red + warp * 128;  // [16 rows][8 vectors]
-  my[g * 8 + 2 * t] = acc[0];
-  my[g * 8 + 2 * t + 1] = acc[1];
-  my[(g + 8) * 8 + 2 * t] = acc[2];
-  my[(g + 8) * 8 + 2 * t + 1] = acc[3];
-  __syncthreads();
-  if (active && kslice == 0 && !failed) {
+    if (cj == per_item - 1) {  // end of an item: add the column slices, store y
+      const int row0 = ctile * C::WROWS;
+      if (p.ks == 1) {
+        if (valid && !failed) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int v = i * 32 + lane;
-      const int n = v >> 4;
-      const int r = v & 15;
-      if (n < p.batch && r < nvalid) {
-        float s = 0.f;
-        for (int k = 0; k < p.ks; ++k) s += red[(warp + k) * 128 + r * 8 + n];
-        p.y[(int64_t)n * p.rows + row0 + r] = s;
+          for (int mt = 0; mt < MT; ++mt) {
+            const int r0 = row0 + 16 * mt + g, r1 = r0 + 8;
+            const int n0 = 2 * t, n1 = 2 * t + 1;
+            if (n0 < p.batch && r0 < p.rows) p.y[(size_t)n0 * p.rows + r0] = acc[mt][0];
+            if (n1 < p.batch && r0 < p.rows) p.y[(size_t)n1 * p.rows + r0] = acc[mt][1];
+            if (n0 < p.batch && r1 < p.rows) p.y[(size_t)n0 * p.rows + r1] = acc[mt][2];
+            if (n1 < p.batch && r1 < p.rows) p.y[(size_t)n1 * p.rows + r1] = acc[mt][3];
+          }
+        }
+      } else {
+        float* my = red + warp * (C::WROWS * 8);  // [rows][8 vectors]
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          my[(16 * mt + g) * 8 + 2 * t] = acc[mt][0];
+          my[(16 * mt + g) * 8 + 2 * t + 1] = acc[mt][1];
+          my[(16 * mt + g + 8) * 8 + 2 * t] = acc[mt][2];
+          my[(16 * mt + g + 8) * 8 + 2 * t + 1] = acc[mt][3];
+        }
+        __syncthreads();
+        if (kslice == 0 && valid && !failed) {
+#pragma unroll
+          for (int i = 0; i < C::WROWS * 8 / 32; ++i) {
+            const int v = i * 32 + lane;
+            const int n = v / C::WROWS;
+            const int r = v % C::WROWS;
+            if (n < p.batch && row0 + r < p.rows) {
+              float sum = 0.f;
+              for (int k = 0; k < p.ks; ++k) sum += red[(warp + k) * (C::WROWS * 8) + r * 8 + n];
+              p.y[(size_t)n * p.rows + row0 + r] = sum;
+            }
+          }
+        }
+        __syncthreads();
       }
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
     }
+    cs = (cs + 1 == C::S) ? 0 : cs + 1;
+    if (cs == 0) phase ^= 1u;
+    if (++cj == per_item) {
+      cj = 0;
+      ctile += tile_step;
+    }
+  }
+  if (failed) {
+    // let this warp's copies still in flight land before the CTA's shared memory is released
+    for (int j = 0; j < issued; ++j) mbar_wait_bounded(&bars[j % C::S], (uint32_t)(j / C::S) & 1u, 400000000LL);
   }
 }
 
 template <int WT, bool F16, bool XBF16>
-cudaError_t launch_typed(const Params& p, int grid, int dev, cudaStream_t stream) {
-  using C = Cfg<WT, F16>;
+cudaError_t launch_typed(const MatrixRef& m, const void* x, Params p, const DeviceInfo& dev, cudaStream_t stream) {
+  using C = Cfg<WT, F16, XBF16>;
   auto kern = matvec_mma_kernel<WT, F16, XBF16>;
-  static bool attr_set[64] = {};  // per device: raise the dynamic shared memory limit once
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  // per device and batch: shared-memory limit raised and occupancy known
+  static bool ready[64][kMaxBatch + 1] = {};
+  static int ctas_per_sm[64][kMaxBatch + 1] = {};
+  if (dev.device < 0 || dev.device >= 64 || p.batch < 1 || p.batch > kMaxBatch) return cudaErrorInvalidValue;
+  const int smem = C::smem_bytes(p.batch);
+  if (!ready[dev.device][p.batch]) {
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::smem_bytes(kMaxBatch));
     if (err != cudaSuccess) return err;
-    attr_set[dev] = true;
+    int n = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kWarps * 32, smem);
+    if (err != cudaSuccess) return err;
+    ctas_per_sm[dev.device][p.batch] = n > 0 ? n : 1;
+    ready[dev.device][p.batch] = true;
   }
-  kern<<<grid, kWarps * 32, C::SMEM_BYTES, stream>>>(p);
+  const int slots = ctas_per_sm[dev.device][p.batch] * dev.sm_count;
+
+  p.ntiles = (int)((m.rows + C::WROWS - 1) / C::WROWS);
+  // column split: fewest stages on the critical path (waves x stages per item), then fewest slices
+  int best_ks = 1;
+  long best_cost = -1;
+  for (int ks = 1; ks <= kWarps; ks *= 2) {
+    if (p.nchunks < ks) break;
+    const int tpi = kWarps / ks;
+    const long items = (p.ntiles + tpi - 1) / tpi;
+    const long grid = items < slots ? items : slots;
+    const long waves = (items + grid - 1) / grid;
+    const long cost = waves * ((p.nchunks + ks - 1) / ks);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best_ks = ks;
+    }
+  }
+  p.ks = best_ks;
+  const int tpi = kWarps / best_ks;
+  p.nitems = (p.ntiles + tpi - 1) / tpi;
+  const int grid = p.nitems < slots ? p.nitems : slots;
+
+  CUtensorMap tq, td, tx;
+  const uint64_t qrow = (WT == QMV_Q4_0) ? (uint64_t)m.cols / 2 : (uint64_t)m.cols;
+  const uint64_t drow = (uint64_t)(m.cols / 32) * (F16 ? 2 : 4);
+  cudaError_t err = encode_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, m.q, qrow, (uint64_t)m.rows, qrow, kBox,
+                                   C::WROWS, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (err != cudaSuccess) return err;
+  err = encode_tmap_2d(&td, CU_TENSOR_MAP_DATA_TYPE_UINT8, m.d, drow, (uint64_t)m.rows, drow, C::DROW, C::WROWS,
+                       CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (err != cudaSuccess) return err;
+  err = encode_tmap_2d(&tx, XBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, x,
+                       (uint64_t)m.cols, (uint64_t)p.batch, (uint64_t)m.cols * (XBF16 ? 2 : 4), kTK, p.batch,
+                       CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (err != cudaSuccess) return err;
+  kern<<<grid, kWarps * 32, smem, stream>>>(tq, td, tx, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-bool matvec_mma_supported(const MatrixRef& m) { return m.cols % kTK == 0; }
+bool matvec_mma_supported(const MatrixRef& m) {
+  return m.cols % kTK == 0 && m.rows < (1LL << 31) - 64 && m.cols < (1LL << 30);
+}
 
 cudaError_t launch_matvec_mma(const MatrixRef& m, const void* x, bool x_bf16, float* y, int batch,
                               const DeviceInfo& dev, cudaStream_t stream) {
   Params p;
-  p.q = m.q;
-  p.d = m.d;
-  p.x = x;
   p.y = y;
-  p.rows = m.rows;
-  p.cols = m.cols;
+  p.rows = (int)m.rows;
+  p.cols = (int)m.cols;
   p.batch = batch;
   p.status = dev.status;
-  p.ntiles = (m.rows + 15) / 16;
-  const int64_t nchunks = m.cols / kTK;
-  // enough warps in flight to cover HBM latency: split the columns while tiles are few
-  const int64_t target = (int64_t)dev.sm_count * 8;
-  int ks = 1;
-  while (ks < kWarps && p.ntiles * ks < target && nchunks >= 2 * ks) ks *= 2;
-  p.ks = ks;
-  const int64_t tiles_per_cta = kWarps / ks;
-  const int grid = (int)((p.ntiles + tiles_per_cta - 1) / tiles_per_cta);
+  p.ntiles = 0;
+  p.nchunks = (int)(m.cols / kTK);
+  p.ks = 1;
+  p.nitems = 0;
   if (m.wtype == QMV_Q4_0) {
-    if (m.scale_f16) return x_bf16 ? launch_typed<QMV_Q4_0, true, true>(p, grid, dev.device, stream)
-                                   : launch_typed<QMV_Q4_0, true, false>(p, grid, dev.device, stream);
-    return x_bf16 ? launch_typed<QMV_Q4_0, false, true>(p, grid, dev.device, stream)
-                  : launch_typed<QMV_Q4_0, false, false>(p, grid, dev.device, stream);
+    if (m.scale_f16) return x_bf16 ? launch_typed<QMV_Q4_0, true, true>(m, x, p, dev, stream)
+                                   : launch_typed<QMV_Q4_0, true, false>(m, x, p, dev, stream);
+    return x_bf16 ? launch_typed<QMV_Q4_0, false, true>(m, x, p, dev, stream)
+                  : launch_typed<QMV_Q4_0, false, false>(m, x, p, dev, stream);
   }
-  if (m.scale_f16) return x_bf16 ? launch_typed<QMV_Q8_0, true, true>(p, grid, dev.device, stream)
-                                 : launch_typed<QMV_Q8_0, true, false>(p, grid, dev.device, stream);
-  return x_bf16 ? launch_typed<QMV_Q8_0, false, true>(p, grid, dev.device, stream)
-                : launch_typed<QMV_Q8_0, false, false>(p, grid, dev.device, stream);
+  if (m.scale_f16) return x_bf16 ? launch_typed<QMV_Q8_0, true, true>(m, x, p, dev, stream)
+                                 : launch_typed<QMV_Q8_0, true, false>(m, x, p, dev, stream);
+  return x_bf16 ? launch_typed<QMV_Q8_0, false, true>(m, x, p, dev, stream)
+                : launch_typed<QMV_Q8_0, false, false>(m, x, p, dev, stream);
 }
 
 }  // namespace qmv

@@ -7,11 +7,12 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
-#include "../../include/qmv.h"
+#include "qmv.h"
 
 namespace qmv {
 
@@ -94,6 +95,39 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst_smem, const void* src_gm
       : "memory");
 }
 
+// 2-D tiled TMA load of one box into shared memory (coordinates: x innermost, in elements).
+__device__ __forceinline__ void tma_load_2d(void* dst_smem, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst_smem)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// The same without a cache hint (data that many CTAs re-read, such as the activations).
+__device__ __forceinline__ void tma_load_2d_keep(void* dst_smem, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst_smem)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Shared-memory loads by 32-bit shared address (ordered after the barrier waits).
+__device__ __forceinline__ void lds_u32x2(uint32_t addr, uint32_t& a, uint32_t& b) {
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(addr) : "memory");
+}
+
+__device__ __forceinline__ void lds_f32x4(uint32_t addr, float (&v)[4]) {
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]) : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 // ldmatrix: four 8x8 matrices of 16-bit elements; lane l supplies the address of row
 // (l % 8) of matrix (l / 8); thread (g = lane/4, t = lane%4) receives, for each matrix,
 // the 32-bit word t of row g.
@@ -101,13 +135,14 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t& r0, uint32_t& r1, uint32_t
                                             uint32_t addr) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
+               : "r"(addr)
+               : "memory");
 }
 
 // D = A(16x16 bf16, row) * B(16x8 bf16, col) + C, f32 accumulate.
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                                uint32_t a3, uint32_t b0, uint32_t b1, const float (&c)[4]) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
       "{%10, %11, %12, %13};"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
@@ -133,36 +168,39 @@ __device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
   return r;
 }
 
-// Four Q4_0 quant bytes (bytes i = 0..3 of one 32-bit word, nibbles lo_i / hi_i) to
-// exact bfloat16 levels (nibble - 8), packed in pairs:
-//   p0 = (lo0, lo2)  p1 = (hi0, hi2)  p2 = (lo1, lo3)  p3 = (hi1, hi3)   (low half first)
-// 0x4300 | n is the bfloat16 of 128 + n (n < 16 sits in the mantissa), and
-// (128 + n) - 136 = n - 8 is exact.
-__device__ __forceinline__ void q4_word_to_bf16_levels(uint32_t w, uint32_t& p0, uint32_t& p1, uint32_t& p2,
-                                                       uint32_t& p3) {
+// Four Q4_0 quant bytes (bytes i = 0..3 of one 32-bit word; byte i holds element i in its
+// low nibble lo_i and element i+16 in its high nibble hi_i) to exact bfloat16 levels
+// (nibble - 8), in natural pairs (low half first):
+//   lo01 = (lo0, lo1)  lo23 = (lo2, lo3)  hi01 = (hi0, hi1)  hi23 = (hi2, hi3)
+// prmt spreads bytes 0,1 (2,3) into the two 16-bit halves; 0x4300 | n is the bfloat16 of
+// 128 + n (n < 16 sits in the mantissa), and (128 + n) - 136 = n - 8 is exact.
+__device__ __forceinline__ void q4_word_to_bf16_levels(uint32_t w, uint32_t& lo01, uint32_t& lo23, uint32_t& hi01,
+                                                       uint32_t& hi23) {
   constexpr uint32_t kMask = 0x000F000Fu;
   constexpr uint32_t kMagic = 0x43004300u;   // bf16 128.0 in both halves
   constexpr uint32_t kOffset = 0x43084308u;  // bf16 136.0 in both halves
-  p0 = bf16x2_sub(lop_and_or(w, kMask, kMagic), kOffset);
-  p1 = bf16x2_sub(lop_and_or(w >> 4, kMask, kMagic), kOffset);
-  p2 = bf16x2_sub(lop_and_or(w >> 8, kMask, kMagic), kOffset);
-  p3 = bf16x2_sub(lop_and_or(w >> 12, kMask, kMagic), kOffset);
+  const uint32_t b01 = prmt(w, 0u, 0x4140);  // bytes: w.b0, 0, w.b1, 0
+  const uint32_t b23 = prmt(w, 0u, 0x4342);  // bytes: w.b2, 0, w.b3, 0
+  lo01 = bf16x2_sub(lop_and_or(b01, kMask, kMagic), kOffset);
+  hi01 = bf16x2_sub(lop_and_or(b01 >> 4, kMask, kMagic), kOffset);
+  lo23 = bf16x2_sub(lop_and_or(b23, kMask, kMagic), kOffset);
+  hi23 = bf16x2_sub(lop_and_or(b23 >> 4, kMask, kMagic), kOffset);
 }
 
-// Four Q8_0 quant bytes q0..q3 (one word) to exact bfloat16 levels in pairs
-//   p0 = (q0, q2)  p2 = (q1, q3)
+// Four Q8_0 quant bytes q0..q3 (one word) to exact bfloat16 levels in natural pairs
+//   q01 = (q0, q1)  q23 = (q2, q3)
 // via float32: 0x4B000000 | u is 2^23 + u; with u = q + 128 the float32 subtraction of
 // 2^23 + 128 gives q exactly, and an integer of magnitude <= 128 is exact in bfloat16,
 // so its bfloat16 code is the upper half of its float32 code.
-__device__ __forceinline__ void q8_word_to_bf16_levels(uint32_t w, uint32_t& p0, uint32_t& p2) {
+__device__ __forceinline__ void q8_word_to_bf16_levels(uint32_t w, uint32_t& q01, uint32_t& q23) {
   const uint32_t u = w ^ 0x80808080u;  // q + 128 in each byte
   const float bias = 8388736.0f;       // 2^23 + 128
   const float f0 = __uint_as_float(prmt(u, 0x4B000000u, 0x7440)) - bias;
   const float f1 = __uint_as_float(prmt(u, 0x4B000000u, 0x7441)) - bias;
   const float f2 = __uint_as_float(prmt(u, 0x4B000000u, 0x7442)) - bias;
   const float f3 = __uint_as_float(prmt(u, 0x4B000000u, 0x7443)) - bias;
-  p0 = prmt(__float_as_uint(f0), __float_as_uint(f2), 0x7632);
-  p2 = prmt(__float_as_uint(f1), __float_as_uint(f3), 0x7632);
+  q01 = prmt(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
+  q23 = prmt(__float_as_uint(f2), __float_as_uint(f3), 0x7632);
 }
 
 // Round-to-nearest-even bfloat16 pair from two floats: low half from lo, high half from hi.

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace qmv {
@@ -23,6 +24,13 @@ struct DeviceInfo {
   size_t smem_optin;
   int* status;  // device address of this device's status word
 };
+
+// 2-D tiled tensor map over a row-major array: inner_elems elements of `dtype`
+// (a CUtensorMapDataType) per row, `outer` rows, rows row_stride_bytes apart; box of
+// box_inner x box_outer elements; swizzle is a CUtensorMapSwizzle; out-of-range reads
+// are zero-filled.
+cudaError_t encode_tmap_2d(CUtensorMap* map, int dtype, const void* base, uint64_t inner_elems, uint64_t outer,
+                           uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, int swizzle);
 
 // Cached properties of the current device.
 cudaError_t current_device_info(DeviceInfo* info);
