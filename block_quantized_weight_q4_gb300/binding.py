@@ -59,6 +59,8 @@ def load_library():
     lib.qmv_matrix_wtype.argtypes = [i32, ctypes.c_uint32, i32, i32]
     lib.qmv_matvec.restype = i32
     lib.qmv_matvec.argtypes = [i32, i32, i64, i64, vp, vp, i32, vp, i32, vp]
+    lib.qmv_matvec_grouped.restype = i32
+    lib.qmv_matvec_grouped.argtypes = [i32, i32, i32, i32, vp, i32, ctypes.c_uint, vp]
     lib.qmv_dequant.restype = i32
     lib.qmv_dequant.argtypes = [i32, i32, i64, i64, vp, vp, vp]
     lib.qmv_validate.restype = i32
@@ -128,6 +130,38 @@ def matvec(wtype: int, scale_dtype: int, rows: int, cols: int, W, x, y=None, str
                                    y.data_ptr(), batch, _stream(stream))
     _check(st, "qmv_matvec")
     return y
+
+
+class Problem(ctypes.Structure):
+    """qmv_problem of include/qmv.h."""
+    _fields_ = [("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("W", ctypes.c_void_p),
+                ("x", ctypes.c_void_p), ("y", ctypes.c_void_p)]
+
+
+FLAG_OVERLAP = 1
+MAX_GROUP = 8
+
+
+def matvec_grouped(wtype: int, scale_dtype: int, problems, overlap: bool = False, stream=None):
+    """Several products in one launch.  problems: list of (rows, cols, W, x, y) with W a
+    uint8 CUDA tensor, x (batch, cols) and y (batch, rows) CUDA tensors; all share wtype,
+    scale_dtype, the x dtype and batch.  overlap: QMV_FLAG_OVERLAP (the weights must not be
+    written by the preceding kernel on the stream)."""
+    n = len(problems)
+    if not 1 <= n <= MAX_GROUP:
+        raise ValueError("1..8 problems per group")
+    arr = (Problem * n)()
+    batch = problems[0][3].shape[0]
+    xdt = _x_dtype(problems[0][3])
+    for i, (rows, cols, W, x, y) in enumerate(problems):
+        if x.shape != (batch, cols) or tuple(y.shape) != (batch, rows) or _x_dtype(x) != xdt:
+            raise ValueError("every problem needs x (batch, cols) of one dtype and y (batch, rows)")
+        if not (x.is_contiguous() and y.is_contiguous()):
+            raise ValueError("x and y must be contiguous")
+        arr[i] = Problem(rows, cols, W.data_ptr(), x.data_ptr(), y.data_ptr())
+    st = load_library().qmv_matvec_grouped(wtype, scale_dtype, xdt, batch, ctypes.addressof(arr), n,
+                                           FLAG_OVERLAP if overlap else 0, _stream(stream))
+    _check(st, "qmv_matvec_grouped")
 
 
 def dequant(wtype: int, scale_dtype: int, rows: int, cols: int, W, out=None, stream=None):

@@ -27,8 +27,17 @@
 //   * Scale and accumulate.  acc += d[row][block] * fragment, float32 FFMA.
 //   * Split-K.  Warps of one item that share a tile add their partial sums through shared
 //     memory in a fixed order; one warp writes y.
+//   * Groups.  One launch may carry up to 8 problems of the same types and batch (for
+//     example the projections of a layer that read the same input); items of all problems
+//     form one list that the persistent CTAs walk.
+//   * Overlap with the preceding kernel (optional, programmatic dependent launch).  The
+//     weight boxes of the first stages are requested before griddepcontrol.wait; the
+//     activations are read and y is written only after it.  The weights must then not be
+//     written by the preceding kernel.
 // f32 activations are split x = hi + lo (two bfloat16s, hi = RN(x)) and take two MMAs each,
 // which keeps 16 significant bits of x.
+#include <cstring>
+
 #include "qmv_common.cuh"
 #include "qmv_internal.h"
 
@@ -42,6 +51,7 @@ constexpr int kBlocksPerStage = kTK / 32;
 constexpr int kRows = 16;            // rows per MMA tile
 constexpr int kBox = 128;            // q box inner extent in bytes (the 128-byte swizzle span)
 constexpr int kMaxBatch = 8;         // activation vectors per pass (the MMA's N)
+constexpr int kMaxProblems = 8;      // problems per grouped launch
 
 template <int WT, bool F16, bool XBF16>
 struct Cfg {
@@ -69,23 +79,53 @@ struct Cfg {
   static int smem_bytes(int batch) { return 1024 + OFF_X + kWarps * S * batch * XROW; }
 };
 
-struct Params {
+struct Problem {
   float* y;
   int rows;
   int cols;
-  int batch;    // 1..8
-  int ntiles;
+  int ntiles;   // warp tiles (16*MT rows)
   int nchunks;  // cols / 256
-  int ks;       // column slices per tile (1, 2, 4)
-  int nitems;
-  int* status;
+  int item0;    // first item of this problem in the group's item list
 };
 
+struct Params {
+  int nprob;
+  int batch;    // 1..8
+  int ks;       // column slices per tile (1, 2, 4); at most every problem's nchunks
+  int nitems;
+  int* status;
+  Problem pr[kMaxProblems];
+};
+
+struct Maps {  // per problem: q (128-byte swizzle), d, and activation tensor maps
+  CUtensorMap q[kMaxProblems];
+  CUtensorMap d[kMaxProblems];
+  CUtensorMap x[kMaxProblems];
+};
+
+// Position of a warp in its stream of stages: item (global index), its problem and warp
+// tile, this warp's first chunk and chunk count in the item, and the position within.
+struct Cursor {
+  int item, prob, tile, c0, n, j;
+};
+
+__device__ __forceinline__ void cursor_load(Cursor& c, const Params& p, int tiles_per_item, int tile_local,
+                                            int kslice) {
+  if (c.item >= p.nitems) return;
+  int pr = 0;
+  while (pr + 1 < p.nprob && c.item >= p.pr[pr + 1].item0) ++pr;
+  c.prob = pr;
+  c.tile = (c.item - p.pr[pr].item0) * tiles_per_item + tile_local;
+  const int nch = p.pr[pr].nchunks;
+  const int lg = p.ks == 1 ? 0 : (p.ks == 2 ? 1 : 2);  // ks is 1, 2 or 4
+  c.c0 = (kslice * nch) >> lg;
+  c.n = (((kslice + 1) * nch) >> lg) - c.c0;
+  c.j = 0;
+}
+
 template <int WT, bool F16, bool XBF16>
-__global__ void __launch_bounds__(kWarps * 32) matvec_mma_kernel(const __grid_constant__ CUtensorMap tq,
-                                                                 const __grid_constant__ CUtensorMap td,
-                                                                 const __grid_constant__ CUtensorMap tx,
-                                                                 const Params p) {
+__global__ void __launch_bounds__(kWarps * 32) matvec_mma_kernel(const __grid_constant__ Maps maps,
+                                                                 const __grid_constant__ Params p) {
   using C = Cfg<WT, F16, XBF16>;
   constexpr int MT = C::MT;
   extern __shared__ uint8_t smem_raw[];
@@ -108,48 +148,70 @@ __global__ void __launch_bounds__(kWarps * 32) matvec_mma_kernel(const __grid_co
   const int tiles_per_item = kWarps / p.ks;
   const int tile_local = warp / p.ks;
   const int kslice = warp % p.ks;
-  const int c_begin = kslice * p.nchunks / p.ks;
-  const int per_item = (kslice + 1) * p.nchunks / p.ks - c_begin;  // >= 1 (host keeps nchunks >= ks)
-  const int my_items = (p.nitems - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
-  const int total = my_items * per_item;
-  const int tile_step = (int)gridDim.x * tiles_per_item;  // tile distance between consecutive items
   const uint32_t stage_tx = (uint32_t)(C::Q_STAGE + C::D_STAGE + x_stage);
 
   if (threadIdx.x < C::ZERO_BYTES / 4) reinterpret_cast<uint32_t*>(zero)[threadIdx.x] = 0u;
   if (lane == 0) {
     for (int s = 0; s < C::S; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
-    prefetch_tmap(&tq);
-    prefetch_tmap(&td);
-    prefetch_tmap(&tx);
   }
   __syncthreads();  // zero area and barriers visible
   const uint64_t pol_stream = l2_policy_evict_first();
 
-  // producer position (lane 0 issues): ring slot, tile and chunk of the next stage
-  int ps = 0, ptile = (int)blockIdx.x * tiles_per_item + tile_local, pj = 0;
-  auto issue_next = [&]() {
+  // producer cursor: runs S-1 stages ahead of the consumer cursor
+  Cursor pc;
+  pc.item = (int)blockIdx.x;
+  cursor_load(pc, p, tiles_per_item, tile_local, kslice);
+  int ps = 0;
+  int issued = 0;
+  // fill ring slot ps from the producer cursor; with_x = false defers the activation box
+  auto issue = [&](bool with_x) {
     if (lane == 0) {
-      if (ptile < p.ntiles) {
-        const int c = c_begin + pj;
+      const Problem& P = p.pr[pc.prob];
+      if (pc.tile < P.ntiles) {
+        const int c = pc.c0 + pc.j;
         mbar_arrive_expect_tx(&bars[ps], stage_tx);
         fence_proxy_async_smem();
 #pragma unroll
         for (int b = 0; b < C::NQBOX; ++b)
-          tma_load_2d(qring + ps * C::Q_STAGE + b * C::Q_BOX_BYTES, &tq, c * C::QROW + b * kBox, ptile * C::WROWS,
-                      &bars[ps], pol_stream);
-        tma_load_2d(dring + ps * C::D_STAGE, &td, c * C::DROW, ptile * C::WROWS, &bars[ps], pol_stream);
-        tma_load_2d_keep(xring + ps * x_stage, &tx, c * kTK, 0, &bars[ps]);
+          tma_load_2d(qring + ps * C::Q_STAGE + b * C::Q_BOX_BYTES, &maps.q[pc.prob], c * C::QROW + b * kBox,
+                      pc.tile * C::WROWS, &bars[ps], pol_stream);
+        tma_load_2d(dring + ps * C::D_STAGE, &maps.d[pc.prob], c * C::DROW, pc.tile * C::WROWS, &bars[ps],
+                    pol_stream);
+        if (with_x) tma_load_2d_keep(xring + ps * x_stage, &maps.x[pc.prob], c * kTK, 0, &bars[ps]);
       } else {
-        mbar_arrive(&bars[ps]);  // a tile past the end: complete the phase with no data
+        mbar_arrive(&bars[ps]);  // a tile past the end of its problem: complete the phase, no data
       }
     }
-    ps = (ps + 1 == C::S) ? 0 : ps + 1;
-    if (++pj == per_item) {
-      pj = 0;
-      ptile += tile_step;
+  };
+  auto advance = [&](Cursor& c) {
+    if (++c.j == c.n) {
+      c.item += (int)gridDim.x;
+      cursor_load(c, p, tiles_per_item, tile_local, kslice);
     }
   };
+
+  // prologue: weight boxes of the first S-1 stages may be requested before the preceding
+  // kernel has finished; activations only after griddepcontrol.wait
+  int pre_c[C::S], pre_prob[C::S];
+  bool pre_valid[C::S];
+  int pre = 0;
+  while (pre < C::S - 1 && pc.item < p.nitems) {
+    pre_c[pre] = pc.c0 + pc.j;
+    pre_prob[pre] = pc.prob;
+    pre_valid[pre] = pc.tile < p.pr[pc.prob].ntiles;
+    issue(false);
+    ps = (ps + 1 == C::S) ? 0 : ps + 1;
+    advance(pc);
+    ++pre;
+  }
+  issued = pre;
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  if (lane == 0) {
+    for (int i = 0; i < pre; ++i)
+      if (pre_valid[i]) tma_load_2d_keep(xring + i * x_stage, &maps.x[pre_prob[i]], pre_c[i] * kTK, 0, &bars[i]);
+  }
 
   // ldmatrix: lane supplies row (lane & 7) + 8 * (matrix & 1), 16-byte chunk (matrix >> 1)
   const int lm = lane >> 3;
@@ -163,28 +225,32 @@ __global__ void __launch_bounds__(kWarps * 32) matvec_mma_kernel(const __grid_co
   const uint32_t xhalf = xlive ? 16 * XESZ : 0;  // byte step to elements 16..31
   const uint32_t xlane = (xlive ? (uint32_t)(g * C::XROW) : 0u) + 4 * XESZ * t;
 
-  const int pre = total < C::S - 1 ? total : C::S - 1;
-  for (int i = 0; i < pre; ++i) issue_next();
-  int issued = pre;
-
   float acc[MT][4];
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
   bool failed = false;
   int cs = 0;          // consumer ring slot
   uint32_t phase = 0;  // its parity
-  int ctile = (int)blockIdx.x * tiles_per_item + tile_local, cj = 0;
-  for (int it = 0; it < total; ++it) {
-    const bool valid = ctile < p.ntiles;
+  int consumed = 0;
+  Cursor cc;
+  cc.item = (int)blockIdx.x;
+  cursor_load(cc, p, tiles_per_item, tile_local, kslice);
+  while (cc.item < p.nitems) {
+    const Problem& P = p.pr[cc.prob];
+    const bool valid = cc.tile < P.ntiles;
     if (!failed) {
-      if (it + C::S - 1 < total) {
-        issue_next();
-        issued = it + C::S;
+      if (pc.item < p.nitems) {
+        issue(true);
+        ps = (ps + 1 == C::S) ? 0 : ps + 1;
+        advance(pc);
+        ++issued;
       }
       if (!mbar_wait_bounded(&bars[cs], phase)) {
         record_status(p.status, QMV_E_TIMEOUT);
         failed = true;
-      } else if (valid) {
+      } else {
+        ++consumed;
+        if (valid) {
         const uint32_t qs = smem_u32(qring + cs * C::Q_STAGE);
         const uint8_t* ds = dring + cs * C::D_STAGE;
         const uint32_t xs = (xlive ? smem_u32(xring + cs * x_stage) : smem_u32(zero)) + xlane;
@@ -278,22 +344,23 @@ __global__ void __launch_bounds__(kWarps * 32) matvec_mma_kernel(const __grid_co
             }
           }
         }
+        }
       }
       __syncwarp();
     }
 
-    if (cj == per_item - 1) {  // end of an item: add the column slices, store y
-      const int row0 = ctile * C::WROWS;
+    if (cc.j == cc.n - 1) {  // end of an item: add the column slices, store y
+      const int row0 = cc.tile * C::WROWS;
       if (p.ks == 1) {
         if (valid && !failed) {
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
             const int r0 = row0 + 16 * mt + g, r1 = r0 + 8;
             const int n0 = 2 * t, n1 = 2 * t + 1;
-            if (n0 < p.batch && r0 < p.rows) p.y[(size_t)n0 * p.rows + r0] = acc[mt][0];
-            if (n1 < p.batch && r0 < p.rows) p.y[(size_t)n1 * p.rows + r0] = acc[mt][1];
-            if (n0 < p.batch && r1 < p.rows) p.y[(size_t)n0 * p.rows + r1] = acc[mt][2];
-            if (n1 < p.batch && r1 < p.rows) p.y[(size_t)n1 * p.rows + r1] = acc[mt][3];
+            if (n0 < p.batch && r0 < P.rows) P.y[(size_t)n0 * P.rows + r0] = acc[mt][0];
+            if (n1 < p.batch && r0 < P.rows) P.y[(size_t)n1 * P.rows + r0] = acc[mt][1];
+            if (n0 < p.batch && r1 < P.rows) P.y[(size_t)n0 * P.rows + r1] = acc[mt][2];
+            if (n1 < p.batch && r1 < P.rows) P.y[(size_t)n1 * P.rows + r1] = acc[mt][3];
           }
         }
       } else {
@@ -312,10 +379,10 @@ __global__ void __launch_bounds__(kWarps * 32) matvec_mma_kernel(const __grid_co
             const int v = i * 32 + lane;
             const int n = v / C::WROWS;
             const int r = v % C::WROWS;
-            if (n < p.batch && row0 + r < p.rows) {
+            if (n < p.batch && row0 + r < P.rows) {
               float sum = 0.f;
               for (int k = 0; k < p.ks; ++k) sum += red[(warp + k) * (C::WROWS * 8) + r * 8 + n];
-              p.y[(size_t)n * p.rows + row0 + r] = sum;
+              P.y[(size_t)n * P.rows + row0 + r] = sum;
             }
           }
         }
@@ -326,48 +393,68 @@ __global__ void __launch_bounds__(kWarps * 32) matvec_mma_kernel(const __grid_co
     }
     cs = (cs + 1 == C::S) ? 0 : cs + 1;
     if (cs == 0) phase ^= 1u;
-    if (++cj == per_item) {
-      cj = 0;
-      ctile += tile_step;
-    }
+    advance(cc);
   }
   if (failed) {
     // let this warp's copies still in flight land before the CTA's shared memory is released
-    for (int j = 0; j < issued; ++j) mbar_wait_bounded(&bars[j % C::S], (uint32_t)(j / C::S) & 1u, 400000000LL);
+    for (int j = consumed; j < issued; ++j)
+      mbar_wait_bounded(&bars[j % C::S], (uint32_t)(j / C::S) & 1u, 400000000LL);
   }
 }
 
 template <int WT, bool F16, bool XBF16>
-cudaError_t launch_typed(const MatrixRef& m, const void* x, Params p, const DeviceInfo& dev, cudaStream_t stream) {
+cudaError_t launch_typed(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, int batch,
+                         bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
   using C = Cfg<WT, F16, XBF16>;
   auto kern = matvec_mma_kernel<WT, F16, XBF16>;
   // per device and batch: shared-memory limit raised and occupancy known
   static bool ready[64][kMaxBatch + 1] = {};
   static int ctas_per_sm[64][kMaxBatch + 1] = {};
-  if (dev.device < 0 || dev.device >= 64 || p.batch < 1 || p.batch > kMaxBatch) return cudaErrorInvalidValue;
-  const int smem = C::smem_bytes(p.batch);
-  if (!ready[dev.device][p.batch]) {
+  if (dev.device < 0 || dev.device >= 64 || batch < 1 || batch > kMaxBatch || n < 1 || n > kMaxProblems)
+    return cudaErrorInvalidValue;
+  const int smem = C::smem_bytes(batch);
+  if (!ready[dev.device][batch]) {
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::smem_bytes(kMaxBatch));
     if (err != cudaSuccess) return err;
-    int n = 0;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kWarps * 32, smem);
+    int k = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&k, kern, kWarps * 32, smem);
     if (err != cudaSuccess) return err;
-    ctas_per_sm[dev.device][p.batch] = n > 0 ? n : 1;
-    ready[dev.device][p.batch] = true;
+    ctas_per_sm[dev.device][batch] = k > 0 ? k : 1;
+    ready[dev.device][batch] = true;
   }
-  const int slots = ctas_per_sm[dev.device][p.batch] * dev.sm_count;
+  const long slots = (long)ctas_per_sm[dev.device][batch] * dev.sm_count;
 
-  p.ntiles = (int)((m.rows + C::WROWS - 1) / C::WROWS);
-  // column split: fewest stages on the critical path (waves x stages per item), then fewest slices
+  Params p{};
+  p.nprob = n;
+  p.batch = batch;
+  p.status = dev.status;
+  int min_chunks = 1 << 30;
+  for (int i = 0; i < n; ++i) {
+    p.pr[i].y = ys[i];
+    p.pr[i].rows = (int)ms[i].rows;
+    p.pr[i].cols = (int)ms[i].cols;
+    p.pr[i].ntiles = (int)((ms[i].rows + C::WROWS - 1) / C::WROWS);
+    p.pr[i].nchunks = (int)(ms[i].cols / kTK);
+    if (p.pr[i].nchunks < min_chunks) min_chunks = p.pr[i].nchunks;
+  }
+  // column split: fewest stages on the critical path, estimated as the stages of an even
+  // share of all items plus one item's stages (the tail), plus half a stage per item for the
+  // CTA-wide reduction that a split needs; ties go to fewer slices
   int best_ks = 1;
   long best_cost = -1;
-  for (int ks = 1; ks <= kWarps; ks *= 2) {
-    if (p.nchunks < ks) break;
+  for (int ks = 1; ks <= kWarps && ks <= min_chunks; ks *= 2) {
     const int tpi = kWarps / ks;
-    const long items = (p.ntiles + tpi - 1) / tpi;
+    long items = 0, units = 0, longest = 0;
+    for (int i = 0; i < n; ++i) {
+      const long it = (p.pr[i].ntiles + tpi - 1) / tpi;
+      const long st = (p.pr[i].nchunks + ks - 1) / ks;
+      items += it;
+      units += it * st;
+      if (st > longest) longest = st;
+    }
     const long grid = items < slots ? items : slots;
-    const long waves = (items + grid - 1) / grid;
-    const long cost = waves * ((p.nchunks + ks - 1) / ks);
+    const long per_cta = (items + grid - 1) / grid;
+    const long cost = 2 * ((units + grid - 1) / grid + longest) + (ks > 1 ? per_cta : 0);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best_ks = ks;
@@ -375,24 +462,43 @@ cudaError_t launch_typed(const MatrixRef& m, const void* x, Params p, const Devi
   }
   p.ks = best_ks;
   const int tpi = kWarps / best_ks;
-  p.nitems = (p.ntiles + tpi - 1) / tpi;
-  const int grid = p.nitems < slots ? p.nitems : slots;
+  int items = 0;
+  for (int i = 0; i < n; ++i) {
+    p.pr[i].item0 = items;
+    items += (p.pr[i].ntiles + tpi - 1) / tpi;
+  }
+  p.nitems = items;
+  const int grid = (int)(items < slots ? items : slots);
 
-  CUtensorMap tq, td, tx;
-  const uint64_t qrow = (WT == QMV_Q4_0) ? (uint64_t)m.cols / 2 : (uint64_t)m.cols;
-  const uint64_t drow = (uint64_t)(m.cols / 32) * (F16 ? 2 : 4);
-  cudaError_t err = encode_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, m.q, qrow, (uint64_t)m.rows, qrow, kBox,
-                                   C::WROWS, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (err != cudaSuccess) return err;
-  err = encode_tmap_2d(&td, CU_TENSOR_MAP_DATA_TYPE_UINT8, m.d, drow, (uint64_t)m.rows, drow, C::DROW, C::WROWS,
-                       CU_TENSOR_MAP_SWIZZLE_NONE);
-  if (err != cudaSuccess) return err;
-  err = encode_tmap_2d(&tx, XBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, x,
-                       (uint64_t)m.cols, (uint64_t)p.batch, (uint64_t)m.cols * (XBF16 ? 2 : 4), kTK, p.batch,
-                       CU_TENSOR_MAP_SWIZZLE_NONE);
-  if (err != cudaSuccess) return err;
-  kern<<<grid, kWarps * 32, smem, stream>>>(tq, td, tx, p);
-  return cudaGetLastError();
+  Maps maps;
+  memset(&maps, 0, sizeof(maps));
+  for (int i = 0; i < n; ++i) {
+    const MatrixRef& m = ms[i];
+    const uint64_t qrow = (WT == QMV_Q4_0) ? (uint64_t)m.cols / 2 : (uint64_t)m.cols;
+    const uint64_t drow = (uint64_t)(m.cols / 32) * (F16 ? 2 : 4);
+    cudaError_t err = encode_tmap_2d(&maps.q[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, m.q, qrow, (uint64_t)m.rows, qrow,
+                                     kBox, C::WROWS, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (err != cudaSuccess) return err;
+    err = encode_tmap_2d(&maps.d[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, m.d, drow, (uint64_t)m.rows, drow, C::DROW,
+                         C::WROWS, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (err != cudaSuccess) return err;
+    err = encode_tmap_2d(&maps.x[i], XBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, xs[i],
+                         (uint64_t)m.cols, (uint64_t)batch, (uint64_t)m.cols * (XBF16 ? 2 : 4), kTK, batch,
+                         CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (err != cudaSuccess) return err;
+  }
+
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, maps, p);
 }
 
 }  // namespace
@@ -401,28 +507,21 @@ bool matvec_mma_supported(const MatrixRef& m) {
   return m.cols % kTK == 0 && m.rows < (1LL << 31) - 64 && m.cols < (1LL << 30);
 }
 
-cudaError_t launch_matvec_mma(const MatrixRef& m, const void* x, bool x_bf16, float* y, int batch,
-                              const DeviceInfo& dev, cudaStream_t stream) {
-  Params p;
-  p.y = y;
-  p.rows = (int)m.rows;
-  p.cols = (int)m.cols;
-  p.batch = batch;
-  p.status = dev.status;
-  p.ntiles = 0;
-  p.nchunks = (int)(m.cols / kTK);
-  p.ks = 1;
-  p.nitems = 0;
+int matvec_mma_max_problems() { return kMaxProblems; }
+
+cudaError_t launch_matvec_mma(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool x_bf16,
+                              int batch, bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
+  const MatrixRef& m = ms[0];
   if (m.wtype == QMV_Q4_0) {
-    if (m.scale_f16) return x_bf16 ? launch_typed<QMV_Q4_0, true, true>(m, x, p, dev, stream)
-                                   : launch_typed<QMV_Q4_0, true, false>(m, x, p, dev, stream);
-    return x_bf16 ? launch_typed<QMV_Q4_0, false, true>(m, x, p, dev, stream)
-                  : launch_typed<QMV_Q4_0, false, false>(m, x, p, dev, stream);
+    if (m.scale_f16) return x_bf16 ? launch_typed<QMV_Q4_0, true, true>(ms, xs, ys, n, batch, pdl, dev, stream)
+                                   : launch_typed<QMV_Q4_0, true, false>(ms, xs, ys, n, batch, pdl, dev, stream);
+    return x_bf16 ? launch_typed<QMV_Q4_0, false, true>(ms, xs, ys, n, batch, pdl, dev, stream)
+                  : launch_typed<QMV_Q4_0, false, false>(ms, xs, ys, n, batch, pdl, dev, stream);
   }
-  if (m.scale_f16) return x_bf16 ? launch_typed<QMV_Q8_0, true, true>(m, x, p, dev, stream)
-                                 : launch_typed<QMV_Q8_0, true, false>(m, x, p, dev, stream);
-  return x_bf16 ? launch_typed<QMV_Q8_0, false, true>(m, x, p, dev, stream)
-                : launch_typed<QMV_Q8_0, false, false>(m, x, p, dev, stream);
+  if (m.scale_f16) return x_bf16 ? launch_typed<QMV_Q8_0, true, true>(ms, xs, ys, n, batch, pdl, dev, stream)
+                                 : launch_typed<QMV_Q8_0, true, false>(ms, xs, ys, n, batch, pdl, dev, stream);
+  return x_bf16 ? launch_typed<QMV_Q8_0, false, true>(ms, xs, ys, n, batch, pdl, dev, stream)
+                : launch_typed<QMV_Q8_0, false, false>(ms, xs, ys, n, batch, pdl, dev, stream);
 }
 
 }  // namespace qmv

@@ -114,31 +114,62 @@ int qmv_matrix_wtype(int file_wtype, uint32_t q8_mask, int class_bit, int shared
   return (q8_mask & bits) ? QMV_Q8_0 : QMV_Q4_0;
 }
 
-int qmv_matvec(int wtype, int scale_dtype, int64_t rows, int64_t cols, const void* W, const void* x,
-               int x_dtype, float* y, int batch, cudaStream_t stream) {
-  MatrixRef m;
-  int st = make_ref(wtype, scale_dtype, rows, cols, W, &m);
-  if (st != QMV_OK) return st;
+int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const qmv_problem* problems, int n,
+                       unsigned flags, cudaStream_t stream) {
+  if (problems == nullptr || n < 1 || n > QMV_MAX_GROUP) return QMV_E_ARG;
   if (x_dtype != QMV_X_F32 && x_dtype != QMV_X_BF16) return QMV_E_FORMAT;
   if (batch < 0) return QMV_E_ARG;
+  if ((flags & ~QMV_FLAG_OVERLAP) != 0) return QMV_E_ARG;
+  MatrixRef ms[QMV_MAX_GROUP];
+  for (int i = 0; i < n; ++i) {
+    const qmv_problem& pr = problems[i];
+    const int st = make_ref(wtype, scale_dtype, pr.rows, pr.cols, pr.W, &ms[i]);
+    if (st != QMV_OK) return st;
+    if (batch == 0) continue;
+    if (pr.x == nullptr || pr.y == nullptr) return QMV_E_ARG;
+    if (!aligned(pr.x, 16) || !aligned(pr.y, 4)) return QMV_E_ALIGN;
+    if (pr.rows > INT64_MAX / batch) return QMV_E_SHAPE;
+  }
   if (batch == 0) return QMV_OK;
-  if (x == nullptr || y == nullptr) return QMV_E_ARG;
-  if (!aligned(x, 16) || !aligned(y, 4)) return QMV_E_ALIGN;
-  if (rows > INT64_MAX / batch) return QMV_E_SHAPE;
   DeviceInfo dev;
   if (current_device_info(&dev) != cudaSuccess) return QMV_E_CUDA;
   const bool xb = x_dtype == QMV_X_BF16;
   const size_t xsz = xb ? 2 : 4;
-  const bool fast = matvec_mma_supported(m);
+  const bool pdl = (flags & QMV_FLAG_OVERLAP) != 0;
+  // problems the tensor-core kernel takes go in one launch per pass of 8 vectors; the rest
+  // run the general kernel one by one
+  MatrixRef fast[QMV_MAX_GROUP];
+  const void* fx[QMV_MAX_GROUP];
+  float* fy[QMV_MAX_GROUP];
   for (int b0 = 0; b0 < batch; b0 += 8) {
     const int nb = (batch - b0) < 8 ? (batch - b0) : 8;
-    const void* xp = static_cast<const uint8_t*>(x) + (size_t)b0 * (size_t)cols * xsz;
-    float* yp = y + (size_t)b0 * (size_t)rows;
-    const cudaError_t err = fast ? launch_matvec_mma(m, xp, xb, yp, nb, dev, stream)
-                                 : launch_matvec_simple(m, xp, xb, yp, nb, dev, stream);
-    if (err != cudaSuccess) return QMV_E_CUDA;
+    int nf = 0;
+    for (int i = 0; i < n; ++i) {
+      const void* xp = static_cast<const uint8_t*>(problems[i].x) + (size_t)b0 * (size_t)ms[i].cols * xsz;
+      float* yp = problems[i].y + (size_t)b0 * (size_t)ms[i].rows;
+      if (matvec_mma_supported(ms[i])) {
+        fast[nf] = ms[i];
+        fx[nf] = xp;
+        fy[nf] = yp;
+        ++nf;
+      } else if (launch_matvec_simple(ms[i], xp, xb, yp, nb, dev, stream) != cudaSuccess) {
+        return QMV_E_CUDA;
+      }
+    }
+    if (nf > 0 && launch_matvec_mma(fast, fx, fy, nf, xb, nb, pdl, dev, stream) != cudaSuccess) return QMV_E_CUDA;
   }
   return QMV_OK;
+}
+
+int qmv_matvec(int wtype, int scale_dtype, int64_t rows, int64_t cols, const void* W, const void* x,
+               int x_dtype, float* y, int batch, cudaStream_t stream) {
+  qmv_problem pr;
+  pr.rows = rows;
+  pr.cols = cols;
+  pr.W = W;
+  pr.x = x;
+  pr.y = y;
+  return qmv_matvec_grouped(wtype, scale_dtype, x_dtype, batch, &pr, 1, 0u, stream);
 }
 
 int qmv_dequant(int wtype, int scale_dtype, int64_t rows, int64_t cols, const void* W, float* out,

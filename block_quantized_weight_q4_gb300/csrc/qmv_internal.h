@@ -42,9 +42,12 @@ cudaError_t launch_validate(const MatrixRef& m, int64_t* first_bad, cudaStream_t
 cudaError_t launch_matvec_simple(const MatrixRef& m, const void* x, bool x_bf16, float* y, int batch,
                                  const DeviceInfo& dev, cudaStream_t stream);
 
-// cols % 256 == 0; batch 1..8 per call.
+// cols % 256 == 0; 1..matvec_mma_max_problems() problems of the same wtype, scale type and
+// x type per launch (ms[i], xs[i], ys[i]); batch 1..8.  pdl: launch as a programmatic
+// dependent of the preceding kernel (weights are read before that kernel finishes).
 bool matvec_mma_supported(const MatrixRef& m);
-cudaError_t launch_matvec_mma(const MatrixRef& m, const void* x, bool x_bf16, float* y, int batch,
-                              const DeviceInfo& dev, cudaStream_t stream);
+int matvec_mma_max_problems();
+cudaError_t launch_matvec_mma(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool x_bf16,
+                              int batch, bool pdl, const DeviceInfo& dev, cudaStream_t stream);
 
 }  // namespace qmv

@@ -97,16 +97,45 @@ int qmv_matrix_wtype(int file_wtype, uint32_t q8_mask, int class_bit, int shared
  *   x     : device, batch x cols, x_dtype (QMV_X_F32 or QMV_X_BF16), row-major.
  *   y     : device, batch x rows float32, row-major; fully overwritten.
  *   batch : number of activation vectors, >= 0; 0 launches nothing and returns QMV_OK.
- * Each block contributes d * sum_j level_j * x_j; sums are kept in float32.  Batches of
- * 1-15 run the decode kernels (weights decoded in registers, tensor-core mma on the
- * exact integer levels); larger batches run the prefill kernel (weights dequantized to
- * bfloat16 in shared memory, tcgen05 MMA into tensor memory).  Products agree with an
+ * Each block contributes d * sum_j level_j * x_j; sums are kept in float32.  The
+ * activations run in passes of up to 8 vectors through the decode kernels (weights
+ * decoded in registers to exact bfloat16 levels, tensor-core mma, f32 scale and
+ * accumulate).  Products agree with an
  * exact evaluation to within 1e-3 * sum_c |W[r][c] x[c]| per output.  A Q8_0 byte of
  * -128 is not rejected here: it decodes as -128 * d (see qmv_validate).
  * Returns QMV_OK, or QMV_E_FORMAT / QMV_E_SHAPE / QMV_E_ARG / QMV_E_ALIGN before any
  * launch, or QMV_E_CUDA. */
 int qmv_matvec(int wtype, int scale_dtype, int64_t rows, int64_t cols, const void *W,
                const void *x, int x_dtype, float *y, int batch, cudaStream_t stream);
+
+/* One problem of a grouped product: y = W x for this matrix with its own activations.
+ * Layout and alignment of W, x and y as for qmv_matvec. */
+typedef struct qmv_problem {
+  int64_t rows;
+  int64_t cols;
+  const void *W;
+  const void *x;
+  float *y;
+} qmv_problem;
+
+#define QMV_MAX_GROUP 8
+
+/* Flags of qmv_matvec_grouped.
+ * QMV_FLAG_OVERLAP: launch as a programmatic dependent of the kernel that precedes it on
+ *   the stream, so that this launch's first weight tiles are fetched while that kernel
+ *   finishes.  Activations are read, and y written, only after the preceding kernel has
+ *   completed; the WEIGHTS however may be read earlier, so they must not be written by
+ *   the immediately preceding kernel (true for model weights after loading). */
+#define QMV_FLAG_OVERLAP 1u
+
+/* Several products in one launch (Krafla page, "Body": the projections of a layer, e.g.
+ * wq, wk, wv reading the same normalized input, or w1 and w3).  All n problems share
+ * wtype, scale_dtype, x_dtype and batch; each has its own rows, cols, W, x and y.  Same
+ * results as n calls of qmv_matvec.  problems is a host array of n entries, read during
+ * the call only; 1 <= n <= QMV_MAX_GROUP, else QMV_E_ARG.  Returns as qmv_matvec (the
+ * first failing problem decides the code; nothing is launched then). */
+int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const qmv_problem *problems, int n,
+                       unsigned flags, cudaStream_t stream);
 
 /* out[r][c] = level * d as float32, with one float32 multiplication rounded to nearest
  * even (Krafla page, "Q8_0" and "Q4_0"; f16 scales are first converted exactly to

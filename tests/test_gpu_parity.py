@@ -236,3 +236,58 @@ def test_workload_full_size(qmv, name):
         assert_bits_equal(out[torch.from_numpy(ids).cuda()].cpu().numpy(), oracle.dequant(sub, wt, spec.scale_f16, ids.size, spec.cols),
                           f"{name}/{spec.name} dequant")
         del Wd, out
+
+
+# ---------------------------------------------------------------- grouped launches
+@pytest.mark.parametrize("wt,sf", TYPES)
+@pytest.mark.parametrize("batch", [1, 5, 8])
+@pytest.mark.parametrize("overlap", [False, True])
+def test_grouped_matches_oracle(qmv, wt, sf, batch, overlap):
+    # mixed shapes in one call, one of them on the general path (cols % 256 != 0)
+    import torch
+    shapes = [(40, 512), (7, 256), (100, 1024), (33, 96), (64, 2048)]
+    probs, refs = [], []
+    for i, (rows, cols) in enumerate(shapes):
+        m = inputs.make_matrix(wt, sf, rows, cols, seed=50 + i)
+        x = inputs.make_x(batch, cols, True, seed=60 + i)
+        y = torch.full((batch, rows), 7.0, device="cuda")
+        probs.append((rows, cols, dev_u8(m.W), dev_x(x), y))
+        refs.append(oracle.matvec(m.W, wt, sf, rows, cols, x))
+    qmv.matvec_grouped(wt, sf, probs, overlap=overlap)
+    torch.cuda.synchronize()
+    for (rows, cols, _, _, y), (y_ref, absref) in zip(probs, refs):
+        check_product(y.cpu().numpy(), y_ref, absref, TOL, f"grouped {rows}x{cols}")
+
+
+def test_grouped_in_graph_with_overlap(qmv):
+    # a chain of grouped launches captured in a CUDA graph with programmatic overlap; each
+    # stage's input is the previous stage's output (activations produced on the GPU)
+    import torch
+    rows, cols = 256, 256
+    mats = [inputs.make_matrix(2, 1, rows, cols, seed=70 + i) for i in range(3)]
+    Ws = [dev_u8(m.W) for m in mats]
+    x0 = dev_x(inputs.make_x(1, cols, True, seed=5))
+    ys = [torch.empty((1, rows), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    yf = [torch.empty((1, rows), device="cuda") for _ in range(3)]
+    s = torch.cuda.Stream()
+    def chain():
+        x = x0
+        for i in range(3):
+            qmv.matvec_grouped(2, 1, [(rows, cols, Ws[i], x, yf[i])], overlap=True)
+            ys[i].copy_(yf[i])  # a torch kernel between our launches
+            x = ys[i]
+    with torch.cuda.stream(s):
+        chain()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        chain()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    x = inputs.make_x(1, cols, True, seed=5)
+    for i in range(3):
+        y_ref, absref = oracle.matvec(mats[i].W, 2, 1, rows, cols, x)
+        got = yf[i].cpu().numpy()
+        check_product(got, y_ref, absref, TOL, f"chain {i}")
+        x = inputs.bf16_codes(got.astype(np.float32))
