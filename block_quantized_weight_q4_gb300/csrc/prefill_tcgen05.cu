@@ -1,0 +1,353 @@
+// prefill_tcgen05.cu -- the batched product Y = X W^T for 16..128 activation vectors per pass
+// on the 5th-generation tensor core.
+//
+// What is computed (Krafla ".mlb model format v1", "Q8_0", "Q4_0", "Body"): for each row r
+// and vector n, y[n][r] = sum_c w[r][c] * x[n][c], where each weight is first dequantized
+// exactly as qmv_dequant does (fl32(level * d)) and then rounded to bfloat16; products and
+// sums are formed by the tensor core in float32.
+//
+// One CTA owns 128 rows (the MMA's M) over all columns; the activation vectors are the MMA's
+// N (their count rounded up to 16).  Roles:
+//   warp 0     TMA producer: raw stages (128 rows x 256 weights of q, 128 x 8 scales) and
+//              X stages (N x 64 bf16, 128-byte swizzle), each filling a ring slot and
+//              completing on its mbarrier.
+//   warp 1     allocates tensor memory (128 lanes x 128 f32 columns); lane 0 issues, per
+//              64-column stage, four tcgen05.mma (M 128, N, K 16, bf16 in, f32 accumulate)
+//              from the bf16 weight stage and the X stage, then commits to the stage's
+//              "empty" barrier; after the last stage it commits to "accumulator full".
+//   warps 2-9  dequantize: thread (row, half) turns one 32-weight block of its row into 32
+//              bf16 weights written in the MMA's K-major 128-byte-swizzled layout; then they
+//              read the accumulator from tensor memory (each warp its 32-lane quarter, half
+//              of the columns) and store y.
+// Every wait is bounded; a wait that runs out records QMV_E_TIMEOUT and the roles unwind.
+#include "qmv_common.cuh"
+#include "qmv_internal.h"
+#include "tcgen05.cuh"
+
+namespace qmv {
+
+namespace {
+
+constexpr int kPM = 128;      // rows of W per CTA tile = MMA M = tensor-memory lanes
+constexpr int kKB = 64;       // columns per MMA stage: one 128-byte swizzle span of bf16
+constexpr int kRawK = 256;    // columns per raw (quantized) stage
+constexpr int kKS = 4;        // ring depth of the bf16-weight and X stages
+constexpr int kRS = 2;        // ring depth of the raw stages
+constexpr int kDeqWarps = 8;  // dequantize, then drain the accumulator
+constexpr int kThreads = 32 * (2 + kDeqWarps);
+constexpr int kMaxN = 128;    // activation vectors per pass
+constexpr int kTmemCols = 128;
+
+template <int WT, bool F16>
+struct PCfg {
+  static constexpr int QRAW_ROW = (WT == QMV_Q4_0) ? kRawK / 2 : kRawK;  // q bytes per row per raw stage
+  static constexpr int NQBOX = QRAW_ROW / 128;                           // 128-byte q boxes per raw stage
+  static constexpr int Q_RAW = kPM * QRAW_ROW;
+  static constexpr int ESZ = F16 ? 2 : 4;
+  static constexpr int DROW = (kRawK / 32) * ESZ;                        // scale bytes per row per raw stage
+  static constexpr int D_RAW = kPM * DROW;
+  static constexpr int A_STAGE = kPM * 128;                              // 128 rows x 64 bf16
+  static constexpr int X_STAGE = kMaxN * 128;                            // up to 128 vectors x 64 bf16
+  static constexpr int OFF_X = kKS * A_STAGE;
+  static constexpr int OFF_Q = OFF_X + kKS * X_STAGE;
+  static constexpr int OFF_D = OFF_Q + kRS * Q_RAW;
+  static constexpr int OFF_BAR = OFF_D + kRS * D_RAW;
+  // barriers: raw_full[kRS], raw_empty[kRS], x_full[kKS], a_full[kKS], empty[kKS], acc_full
+  static constexpr int NBARS = 2 * kRS + 3 * kKS + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;  // tensor-memory base, failure flag
+  static constexpr int SMEM = 1024 + OFF_MISC + 16;
+};
+
+struct PParams {
+  float* y;
+  int rows;
+  int cols;
+  int batch;  // vectors in this pass (1..128)
+  int npad;   // batch rounded up to 16
+  int* status;
+};
+
+// float32 of (nibble - 8): 0x4B000000 | n is 2^23 + n exactly.
+__device__ __forceinline__ float q4_level(uint32_t w, int shift) {
+  return __fsub_rn(__uint_as_float(lop_and_or(w >> shift, 0xFu, 0x4B000000u)), 8388616.0f);
+}
+
+// One Q4_0 block (quant bytes in w[0..3], byte j = word j/4 bits 8(j%4)) to 32 bf16 weights
+// RN(fl32(level * d)) in element order: out[0..7] elements 0..15 (low nibbles of bytes
+// 0..15), out[8..15] elements 16..31 (high nibbles).
+__device__ __forceinline__ void q4_block_to_bf16(const uint32_t (&w)[4], float d, uint32_t (&out)[16]) {
+#pragma unroll
+  for (int j = 0; j < 16; j += 2) {
+    const uint32_t wi = w[j >> 2];
+    const int sh = 8 * (j & 3);
+    out[j >> 1] = pack_bf16x2(__fmul_rn(q4_level(wi, sh), d), __fmul_rn(q4_level(wi, sh + 8), d));
+    out[8 + (j >> 1)] = pack_bf16x2(__fmul_rn(q4_level(wi, sh + 4), d), __fmul_rn(q4_level(wi, sh + 12), d));
+  }
+}
+
+// One Q8_0 block (32 int8 quants in w[0..7]) to 32 bf16 weights RN(fl32(q * d)), in order.
+__device__ __forceinline__ void q8_block_to_bf16(const uint32_t (&w)[8], float d, uint32_t (&out)[16]) {
+  const float bias = 8388736.0f;  // 2^23 + 128
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t u = w[i] ^ 0x80808080u;  // q + 128 per byte
+    const float f0 = __fsub_rn(__uint_as_float(prmt(u, 0x4B000000u, 0x7440)), bias);
+    const float f1 = __fsub_rn(__uint_as_float(prmt(u, 0x4B000000u, 0x7441)), bias);
+    const float f2 = __fsub_rn(__uint_as_float(prmt(u, 0x4B000000u, 0x7442)), bias);
+    const float f3 = __fsub_rn(__uint_as_float(prmt(u, 0x4B000000u, 0x7443)), bias);
+    out[2 * i] = pack_bf16x2(__fmul_rn(f0, d), __fmul_rn(f1, d));
+    out[2 * i + 1] = pack_bf16x2(__fmul_rn(f2, d), __fmul_rn(f3, d));
+  }
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ void lds128(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr) : "memory");
+}
+
+// Bounded wait that gives up at once when another role has already failed.
+__device__ __forceinline__ bool pwait(uint64_t* bar, uint32_t parity, volatile int* failed, int* status) {
+  if (*failed) return false;
+  if (mbar_wait_bounded(bar, parity)) return true;
+  record_status(status, QMV_E_TIMEOUT);
+  *failed = 1;
+  return false;
+}
+
+template <int WT, bool F16>
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tq,
+                                                              const __grid_constant__ CUtensorMap td,
+                                                              const __grid_constant__ CUtensorMap tx,
+                                                              const PParams p) {
+  using C = PCfg<WT, F16>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);  // 1024-aligned: swizzle atoms
+  const uint32_t sbase = smem_u32(smem);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* raw_full = bars;
+  uint64_t* raw_empty = bars + kRS;
+  uint64_t* x_full = bars + 2 * kRS;
+  uint64_t* a_full = x_full + kKS;
+  uint64_t* empty = a_full + kKS;
+  uint64_t* acc_full = empty + kKS;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* failed = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  const int row0 = (int)blockIdx.x * kPM;
+  const int nkb = p.cols / kKB;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRS; ++i) {
+      mbar_init(&raw_full[i], 1);
+      mbar_init(&raw_empty[i], kDeqWarps);
+    }
+    for (int i = 0; i < kKS; ++i) {
+      mbar_init(&x_full[i], 1);
+      mbar_init(&a_full[i], kDeqWarps);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(acc_full, 1);
+    *failed = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tq);
+    prefetch_tmap(&td);
+    prefetch_tmap(&tx);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_first();
+      int raw_issued = 0, x_issued = 0;
+      for (int kb = 0; kb < nkb && !*failed; ++kb) {
+        if (kb % 4 == 0) {
+          const int q = kb / 4, r = q % kRS;
+          if (q >= kRS && !pwait(&raw_empty[r], (uint32_t)((q / kRS - 1) & 1), failed, p.status)) break;
+          mbar_arrive_expect_tx(&raw_full[r], C::Q_RAW + C::D_RAW);
+#pragma unroll
+          for (int b = 0; b < C::NQBOX; ++b)
+            tma_load_2d(smem + C::OFF_Q + r * C::Q_RAW + b * (kPM * 128), &tq, q * C::QRAW_ROW + b * 128, row0,
+                        &raw_full[r], pol);
+          tma_load_2d(smem + C::OFF_D + r * C::D_RAW, &td, q * C::DROW, row0, &raw_full[r], pol);
+          raw_issued = q + 1;
+        }
+        const int s = kb % kKS;
+        if (kb >= kKS && !pwait(&empty[s], (uint32_t)((kb / kKS - 1) & 1), failed, p.status)) break;
+        mbar_arrive_expect_tx(&x_full[s], (uint32_t)(p.npad * 128));
+        tma_load_2d_keep(smem + C::OFF_X + s * C::X_STAGE, &tx, kb * kKB, 0, &x_full[s]);
+        x_issued = kb + 1;
+      }
+      if (*failed) {
+        // let the copies still in flight land before the shared memory is released
+        for (int r = 0; r < kRS && r < raw_issued; ++r) {
+          const int last = raw_issued - 1 - ((raw_issued - 1 - r) % kRS);  // last raw stage in slot r
+          mbar_wait_bounded(&raw_full[last % kRS], (uint32_t)((last / kRS) & 1), 400000000LL);
+        }
+        for (int s = 0; s < kKS && s < x_issued; ++s) {
+          const int last = x_issued - 1 - ((x_issued - 1 - s) % kKS);
+          mbar_wait_bounded(&x_full[last % kKS], (uint32_t)((last / kKS) & 1), 400000000LL);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kPM, p.npad);
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int s = kb % kKS;
+        const uint32_t ph = (uint32_t)((kb / kKS) & 1);
+        if (!pwait(&x_full[s], ph, failed, p.status) || !pwait(&a_full[s], ph, failed, p.status)) break;
+        tc_fence_after();
+        const uint32_t a0 = sbase + s * C::A_STAGE;
+        const uint32_t b0 = sbase + C::OFF_X + s * C::X_STAGE;
+#pragma unroll
+        for (int k = 0; k < kKB / 16; ++k)
+          tc_mma_f16(tmem, smem_desc_sw128(a0 + 32 * k), smem_desc_sw128(b0 + 32 * k), idesc, (kb | k) != 0);
+        tc_commit(smem_u32(&empty[s]));
+      }
+      tc_commit(smem_u32(acc_full));  // arrives once every MMA issued above has completed
+    }
+  } else {
+    // ---------------------------------------------------------------- dequantize, then drain
+    const int dt = threadIdx.x - 64;
+    const int row = dt & (kPM - 1);
+    const int h = dt >> 7;  // which block of each 64-column stage
+    const int sw = row & 7;
+    const uint32_t a_row = (uint32_t)((row >> 3) * 1024 + sw * 128);
+    for (int kb = 0; kb < nkb; ++kb) {
+      const int q = kb / 4, r = q % kRS;
+      if (kb % 4 == 0 && !pwait(&raw_full[r], (uint32_t)((q / kRS) & 1), failed, p.status)) break;
+      const int s = kb % kKS;
+      if (kb >= kKS && !pwait(&empty[s], (uint32_t)((kb / kKS - 1) & 1), failed, p.status)) break;
+      const int blk = 2 * (kb & 3) + h;  // block of the raw stage
+      float d;
+      if (F16) {
+        d = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(smem + C::OFF_D + r * C::D_RAW + row * C::DROW + 2 * blk));
+      } else {
+        d = *reinterpret_cast<const float*>(smem + C::OFF_D + r * C::D_RAW + row * C::DROW + 4 * blk);
+      }
+      uint32_t out[16];
+      const uint32_t qrow = sbase + C::OFF_Q + r * C::Q_RAW + row * 128;
+      if (WT == QMV_Q4_0) {
+        uint32_t w[4];
+        lds128(qrow + ((blk ^ sw) << 4), w[0], w[1], w[2], w[3]);
+        q4_block_to_bf16(w, d, out);
+      } else {
+        uint32_t w[8];
+        const uint32_t box = qrow + (blk >> 2) * (kPM * 128);
+        const int c0 = 2 * (blk & 3);
+        lds128(box + ((c0 ^ sw) << 4), w[0], w[1], w[2], w[3]);
+        lds128(box + (((c0 + 1) ^ sw) << 4), w[4], w[5], w[6], w[7]);
+        q8_block_to_bf16(w, d, out);
+      }
+      const uint32_t arow = sbase + s * C::A_STAGE + a_row;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        sts128(arow + (((4 * h + j) ^ sw) << 4), out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
+      fence_proxy_async_smem();  // the tensor core reads these stores through the async proxy
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&a_full[s]);
+        if ((kb & 3) == 3) mbar_arrive(&raw_empty[r]);
+      }
+    }
+    // drain the accumulator: warp w reads tensor-memory lanes 32*(w%4) .. +31 (its rows) and
+    // every other 16-column chunk
+    const bool ok = mbar_wait_bounded(acc_full, 0u);
+    if (!ok) {
+      record_status(p.status, QMV_E_TIMEOUT);
+      *failed = 1;
+    }
+    tc_fence_after();
+    if (ok && !*failed) {
+      const int quarter = warp & 3;
+      const int half = (warp - 2) >> 2;
+      const int grow = row0 + quarter * 32 + lane;
+      for (int c = half * 16; c < p.npad; c += 32) {
+        uint32_t v[16];
+        tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c, v);
+        tmem_ld_wait();
+        if (grow < p.rows) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (c + i < p.batch) p.y[(size_t)(c + i) * p.rows + grow] = __uint_as_float(v[i]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+bool prefill_supported(const MatrixRef& m, bool x_bf16) {
+  return x_bf16 && m.cols % kRawK == 0 && m.rows < (1LL << 31) - kPM && m.cols < (1LL << 30);
+}
+
+int prefill_max_batch() { return kMaxN; }
+
+template <int WT, bool F16>
+static cudaError_t launch_prefill_typed(const MatrixRef& m, const void* x, float* y, int batch, const DeviceInfo& dev,
+                                        cudaStream_t stream) {
+  using C = PCfg<WT, F16>;
+  auto kern = prefill_kernel<WT, F16>;
+  static bool ready[64] = {};
+  if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+  if (!ready[dev.device]) {
+    const cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (err != cudaSuccess) return err;
+    ready[dev.device] = true;
+  }
+  PParams p;
+  p.y = y;
+  p.rows = (int)m.rows;
+  p.cols = (int)m.cols;
+  p.batch = batch;
+  p.npad = (batch + 15) / 16 * 16;
+  p.status = dev.status;
+  CUtensorMap tq, td, tx;
+  const uint64_t qrow = (WT == QMV_Q4_0) ? (uint64_t)m.cols / 2 : (uint64_t)m.cols;
+  const uint64_t drow = (uint64_t)(m.cols / 32) * C::ESZ;
+  cudaError_t err = encode_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, m.q, qrow, (uint64_t)m.rows, qrow, 128, kPM,
+                                   CU_TENSOR_MAP_SWIZZLE_128B);
+  if (err != cudaSuccess) return err;
+  err = encode_tmap_2d(&td, CU_TENSOR_MAP_DATA_TYPE_UINT8, m.d, drow, (uint64_t)m.rows, drow, C::DROW, kPM,
+                       CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (err != cudaSuccess) return err;
+  err = encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)m.cols, (uint64_t)batch,
+                       (uint64_t)m.cols * 2, kKB, p.npad, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (err != cudaSuccess) return err;
+  const int grid = (int)((m.rows + kPM - 1) / kPM);
+  kern<<<grid, kThreads, C::SMEM, stream>>>(tq, td, tx, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill(const MatrixRef& m, const void* x, float* y, int batch, const DeviceInfo& dev,
+                           cudaStream_t stream) {
+  if (batch < 1 || batch > kMaxN) return cudaErrorInvalidValue;
+  if (m.wtype == QMV_Q4_0) {
+    return m.scale_f16 ? launch_prefill_typed<QMV_Q4_0, true>(m, x, y, batch, dev, stream)
+                       : launch_prefill_typed<QMV_Q4_0, false>(m, x, y, batch, dev, stream);
+  }
+  return m.scale_f16 ? launch_prefill_typed<QMV_Q8_0, true>(m, x, y, batch, dev, stream)
+                     : launch_prefill_typed<QMV_Q8_0, false>(m, x, y, batch, dev, stream);
+}
+
+}  // namespace qmv

@@ -17,6 +17,7 @@ __device__ int g_device_status = 0;
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr int kPrefillMinBatch = 16;  // from here on the tensor-memory kernel takes bf16 batches
 std::mutex g_dev_mutex;
 DeviceInfo g_dev[kMaxDevices];
 bool g_dev_ready[kMaxDevices] = {};
@@ -136,6 +137,24 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
   const bool xb = x_dtype == QMV_X_BF16;
   const size_t xsz = xb ? 2 : 4;
   const bool pdl = (flags & QMV_FLAG_OVERLAP) != 0;
+  // 16 or more bf16 vectors: the tensor-memory kernel, per problem, in passes of up to 128
+  bool use_prefill[QMV_MAX_GROUP];
+  bool any_decode = false;
+  for (int i = 0; i < n; ++i) {
+    use_prefill[i] = batch >= kPrefillMinBatch && prefill_supported(ms[i], xb);
+    if (use_prefill[i]) {
+      const int pmax = prefill_max_batch();
+      for (int b0 = 0; b0 < batch; b0 += pmax) {
+        const int nb = (batch - b0) < pmax ? (batch - b0) : pmax;
+        const void* xp = static_cast<const uint8_t*>(problems[i].x) + (size_t)b0 * (size_t)ms[i].cols * xsz;
+        float* yp = problems[i].y + (size_t)b0 * (size_t)ms[i].rows;
+        if (launch_prefill(ms[i], xp, yp, nb, dev, stream) != cudaSuccess) return QMV_E_CUDA;
+      }
+    } else {
+      any_decode = true;
+    }
+  }
+  if (!any_decode) return QMV_OK;
   // problems the tensor-core kernel takes go in one launch per pass of 8 vectors; the rest
   // run the general kernel one by one
   MatrixRef fast[QMV_MAX_GROUP];
@@ -145,6 +164,7 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
     const int nb = (batch - b0) < 8 ? (batch - b0) : 8;
     int nf = 0;
     for (int i = 0; i < n; ++i) {
+      if (use_prefill[i]) continue;
       const void* xp = static_cast<const uint8_t*>(problems[i].x) + (size_t)b0 * (size_t)ms[i].cols * xsz;
       float* yp = problems[i].y + (size_t)b0 * (size_t)ms[i].rows;
       if (matvec_mma_supported(ms[i])) {

@@ -50,4 +50,12 @@ int matvec_mma_max_problems();
 cudaError_t launch_matvec_mma(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool x_bf16,
                               int batch, bool pdl, const DeviceInfo& dev, cudaStream_t stream);
 
+// Batched product on the 5th-generation tensor core (weights dequantized to bf16 in shared
+// memory, tcgen05 MMA into tensor memory): bf16 activations, cols % 256 == 0, 1..128
+// vectors per launch (meant for 16 and more).
+bool prefill_supported(const MatrixRef& m, bool x_bf16);
+int prefill_max_batch();
+cudaError_t launch_prefill(const MatrixRef& m, const void* x, float* y, int batch, const DeviceInfo& dev,
+                           cudaStream_t stream);
+
 }  // namespace qmv

@@ -97,10 +97,13 @@ int qmv_matrix_wtype(int file_wtype, uint32_t q8_mask, int class_bit, int shared
  *   x     : device, batch x cols, x_dtype (QMV_X_F32 or QMV_X_BF16), row-major.
  *   y     : device, batch x rows float32, row-major; fully overwritten.
  *   batch : number of activation vectors, >= 0; 0 launches nothing and returns QMV_OK.
- * Each block contributes d * sum_j level_j * x_j; sums are kept in float32.  The
- * activations run in passes of up to 8 vectors through the decode kernels (weights
- * decoded in registers to exact bfloat16 levels, tensor-core mma, f32 scale and
- * accumulate).  Products agree with an
+ * Each block contributes d * sum_j level_j * x_j; sums are kept in float32.  Batches
+ * below 16 (and float32 activations) run in passes of up to 8 vectors through the decode
+ * kernels (weights decoded in registers to exact bfloat16 levels, tensor-core mma, f32
+ * scale and accumulate).  bfloat16 batches of 16 and more (cols % 256 == 0) run in passes
+ * of up to 128 through the prefill kernel (each weight dequantized as qmv_dequant does and
+ * rounded to bfloat16 in shared memory, tcgen05 MMA into tensor memory, f32 accumulate).
+ * Products agree with an
  * exact evaluation to within 1e-3 * sum_c |W[r][c] x[c]| per output.  A Q8_0 byte of
  * -128 is not rejected here: it decodes as -128 * d (see qmv_validate).
  * Returns QMV_OK, or QMV_E_FORMAT / QMV_E_SHAPE / QMV_E_ARG / QMV_E_ALIGN before any

@@ -1,0 +1,136 @@
+"""The tcgen05 prefill path (bf16 activations, 16..128 vectors per pass) vs the oracle.
+
+The prefill kernel rounds each dequantized weight to bfloat16 before the tensor-core
+product, so each term carries a relative error of at most 2^-9.  Over rows of 1024 and
+more columns (the prefill workloads have 4096 and 14336) that averages well inside
+|y - y_ref| <= 1e-3 * sum |w x|; on short rows it can use a good part of the bar, so
+there the check is against the bf16-weight product itself.  Where the bf16 weights are
+exact (power-of-two scales) and every partial sum is an exact dyadic number, the product
+is bit-exact.  Batches below 16 go to the decode kernels (covered in test_gpu_parity.py).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from block_quantized_weight_q4_gb300 import inputs
+from helpers import check_product, dev_u8, dev_x
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-3
+TYPES = [(1, 0), (1, 1), (2, 0), (2, 1)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def qmv():
+    import torch
+    from block_quantized_weight_q4_gb300.build import build
+    import block_quantized_weight_q4_gb300 as q
+    assert torch.cuda.is_available()
+    build()
+    q.load_library()
+    yield q
+    assert q.last_error() == 0
+
+
+def run(q, m, x):
+    import torch
+    y = q.matvec(m.wtype, m.scale_f16, m.rows, m.cols, dev_u8(m.W), dev_x(x))
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+def bf16_weight_product(W, wt, sf, rows, cols, x):
+    """The product the prefill design computes, evaluated in float64: the oracle's
+    dequantized weights rounded to bfloat16 (ties to even), times the activations."""
+    deq = oracle.dequant(W, wt, sf, rows, cols)
+    wb = (inputs.bf16_codes(deq).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    xf = (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return xf @ wb.T
+
+
+@pytest.mark.parametrize("wt,sf", TYPES)
+@pytest.mark.parametrize("rows,cols", [(128, 1024), (200, 2048), (37, 4096), (300, 1024)])
+@pytest.mark.parametrize("batch", [16, 17, 64, 100, 128, 130])
+def test_prefill_random(qmv, wt, sf, rows, cols, batch):
+    # the 1e-3 bar against the exact oracle; bf16 weights round each term by at most 2^-9,
+    # which averages out over rows of 1024 and more columns (the prefill workloads use
+    # 4096 and 14336)
+    m = inputs.make_matrix(wt, sf, rows, cols, seed=rows + cols + batch)
+    x = inputs.make_x(batch, cols, True, seed=batch)
+    y_ref, absref = oracle.matvec(m.W, wt, sf, rows, cols, x)
+    y = run(qmv, m, x)
+    check_product(y, y_ref, absref, TOL, f"prefill {wt},{sf} {rows}x{cols} b{batch}")
+    # and the tensor core adds the bf16-weight terms with float32 care: within 2^-16 of
+    # sum |w x| of the bf16-weight product
+    check_product(y, bf16_weight_product(m.W, wt, sf, rows, cols, x), absref, 2.0 ** -16, "bf16 product")
+
+
+@pytest.mark.parametrize("wt,sf", TYPES)
+@pytest.mark.parametrize("rows,cols", [(128, 256), (33, 512)])
+def test_prefill_short_rows_follow_bf16_product(qmv, wt, sf, rows, cols):
+    # short rows: the bf16 rounding can use a good part of the 1e-3 bar, so the check here
+    # is against the bf16-weight product the design defines
+    m = inputs.make_matrix(wt, sf, rows, cols, seed=cols + wt)
+    x = inputs.make_x(40, cols, True, seed=2)
+    _, absref = oracle.matvec(m.W, wt, sf, rows, cols, x)
+    check_product(run(qmv, m, x), bf16_weight_product(m.W, wt, sf, rows, cols, x), absref, 2.0 ** -16,
+                  "short rows")
+
+
+@pytest.mark.parametrize("wt,sf", TYPES)
+@pytest.mark.parametrize("batch", [16, 48, 128])
+def test_prefill_exact_pow2(qmv, wt, sf, batch):
+    # power-of-two scales make every bf16 weight exact (levels have <= 8 bits); integer x in
+    # [-4, 4]: all partial sums are exact, so the tensor-core result equals the oracle.
+    rows, cols = 160, 768
+    rng = np.random.default_rng(batch + wt)
+    m = inputs.make_matrix(wt, sf, rows, cols, seed=3)
+    codes = inputs.pow2_scales(rng, rows * cols // 32, sf)
+    W = inputs.assemble(wt, sf, rows, cols, m.q, codes)
+    m2 = inputs.Matrix(wt, sf, rows, cols, W, m.q, codes)
+    x = inputs.make_int_x(batch, cols, True, seed=4)
+    y_ref, _ = oracle.matvec(W, wt, sf, rows, cols, x)
+    assert np.array_equal(run(qmv, m2, x).astype(np.float64), y_ref)
+
+
+def test_prefill_one_hot_pow2_is_dequant(qmv):
+    rows, cols, batch = 129, 512, 32
+    rng = np.random.default_rng(8)
+    m = inputs.make_matrix(2, 1, rows, cols, seed=8)
+    codes = inputs.pow2_scales(rng, rows * cols // 32, 1, -6, 3)
+    W = inputs.assemble(2, 1, rows, cols, m.q, codes)
+    m2 = inputs.Matrix(2, 1, rows, cols, W, m.q, codes)
+    picks = rng.integers(0, cols, batch)
+    x = np.zeros((batch, cols), np.float32)
+    x[np.arange(batch), picks] = 1.0
+    deq = oracle.dequant(W, 2, 1, rows, cols)
+    y = run(qmv, m2, inputs.bf16_codes(x))
+    assert np.array_equal(y, deq[:, picks].T)
+
+
+def test_prefill_zero_rows_exact(qmv):
+    rows, cols, batch = 140, 512, 24
+    m = inputs.make_matrix(2, 1, rows, cols, seed=9)
+    q = m.q.copy().reshape(rows, -1)
+    q[::5] = 0x88
+    W = inputs.assemble(2, 1, rows, cols, q.reshape(-1), m.d_codes)
+    m2 = inputs.Matrix(2, 1, rows, cols, W, q.reshape(-1), m.d_codes)
+    x = inputs.make_x(batch, cols, True, seed=9)
+    y_ref, absref = oracle.matvec(W, 2, 1, rows, cols, x)
+    y = run(qmv, m2, x)
+    assert np.all(y[:, ::5] == 0.0)
+    check_product(y, y_ref, absref, TOL, "prefill zero rows")
+
+
+def test_prefill_output_guards(qmv):
+    import torch
+    rows, cols, batch = 130, 256, 20
+    m = inputs.make_matrix(2, 1, rows, cols, seed=10)
+    x = dev_x(inputs.make_x(batch, cols, True, seed=10))
+    buf = torch.full((batch * rows + 256,), 4321.0, device="cuda")
+    y = buf[128:128 + batch * rows].view(batch, rows)
+    qmv.matvec(2, 1, rows, cols, dev_u8(m.W), x, y)
+    torch.cuda.synchronize()
+    b = buf.cpu().numpy()
+    assert np.all(b[:128] == 4321.0) and np.all(b[128 + batch * rows:] == 4321.0)
