@@ -52,6 +52,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-configs", action="store_true", help="only the headline workload")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle sample")
     return ap.parse_args()
 
@@ -83,13 +84,18 @@ def max_over_ranks(v, world):
     return float(t.item())
 
 
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
 def measured_peaks():
+    """(HBM GB/s, dense bf16 TFLOP/s burst, source) from the generated peaks file."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return float(d.get("hbm_gbs", FALLBACK_HBM_GBS)), "measured"
-    return FALLBACK_HBM_GBS, "fallback"
+        return (float(d.get("hbm_gbs", FALLBACK_HBM_GBS)), float(d.get("bf16_tflops", FALLBACK_BF16_TFLOPS)),
+                "measured")
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def layer_specs():
@@ -99,6 +105,24 @@ def layer_specs():
 def layer_bytes(specs):
     return sum(inputs.array_offsets(s.wtype, s.scale_f16, s.rows, s.cols)[1] +
                inputs.array_offsets(s.wtype, s.scale_f16, s.rows, s.cols)[2] for s in specs)
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, or None
+    when the kernel source changed since the capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "roofline_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        parts = line.split()
+        if len(parts) == 4 and not line.startswith("#") and parts[3] == workload:
+            src = os.path.join(ROOT, parts[0])
+            if not os.path.exists(src):
+                return None
+            h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+            return int(parts[2]) if h == parts[1] else None
+    return None
 
 
 # ------------------------------------------------------------------ clocks
@@ -205,6 +229,125 @@ def run_reference(args, world, rank):
            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
 
+
+
+# ------------------------------------------------------------------ other workloads
+def _graph_time_us(torch, launches, cap, replays=5):
+    """Per-launch GPU time of a list of launch closures, replayed as one CUDA graph."""
+    for f in launches[:2]:
+        f()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        for f in launches:
+            f()
+    g.replay()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for _ in range(replays):
+        g.replay()
+    b.record(st)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e3 / (replays * len(launches))
+
+
+def other_workloads(torch, qmv, dev, l2, cap, peak_hbm, peak_tf):
+    """The remaining workloads, each timed on its own (weight copies rotate past 4x L2)."""
+    res = {}
+
+    def copies_for(W, nbytes, minimum=2):
+        n = max(minimum, -(-4 * l2 // nbytes) + 1)
+        return [W] + [W.clone() for _ in range(n - 1)]
+
+    def xdev(x):
+        if x.dtype == np.uint16:
+            return torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(x).to(dev)
+
+    # Q8_0 256 x 256, f32 scales, f32 x, batch 1, seed 0: a few microseconds of launch latency
+    m = inputs.make_matrix(1, 0, 256, 256, seed=0)
+    W = torch.from_numpy(m.W).to(dev)
+    x = xdev(inputs.make_x(1, 256, False, seed=0))
+    y = torch.empty((1, 256), device=dev)
+    us = _graph_time_us(torch, [lambda: qmv.matvec(1, 0, 256, 256, W, x, y)] * 64, cap)
+    res["q8_256_f32x_b1"] = {"us_per_product": round(us, 3), "weight_gbs": round(m.W.size / us / 1e3, 1),
+                             "note": "73,728 weight bytes: bound by launch latency, not HBM"}
+
+    # Q4_0 4096 x 4096, f16 scales, bf16 x, batch 1: a stream of products over rotating copies,
+    # plain and with programmatic overlap between consecutive launches
+    m = inputs.make_matrix(2, 1, 4096, 4096, seed=0)
+    Ws = copies_for(torch.from_numpy(m.W).to(dev), m.W.size)
+    x = xdev(inputs.make_x(1, 4096, True, seed=1000))
+    y = torch.empty((1, 4096), device=dev)
+    n = len(Ws)
+    plain = _graph_time_us(torch, [lambda i=i: qmv.matvec(2, 1, 4096, 4096, Ws[i % n], x, y) for i in range(2 * n)], cap)
+    ov = _graph_time_us(torch, [lambda i=i: qmv.matvec_grouped(2, 1, [(4096, 4096, Ws[i % n], x, y)], overlap=True)
+                                for i in range(2 * n)], cap)
+    res["q4_4096_f16_b1"] = {"us_per_product": round(plain, 3), "weight_gbs": round(m.W.size / plain / 1e3, 1),
+                             "frac_hbm": round(m.W.size / plain / 1e3 / peak_hbm, 4),
+                             "overlapped_us_per_product": round(ov, 3),
+                             "overlapped_weight_gbs": round(m.W.size / ov / 1e3, 1),
+                             "overlapped_frac_hbm": round(m.W.size / ov / 1e3 / peak_hbm, 4)}
+    del Ws
+
+    # mixed q8_mask = 2 model: Q4_0 body of one dim-1024 layer (f32 scales) + Q8_0 classifier
+    wl = inputs.WORKLOADS["mixed_qwen"]
+    mats, nbytes = [], 0
+    for i, spec in enumerate(wl.matrices):
+        wt = qmv.matrix_wtype(wl.file_wtype, wl.q8_mask, spec.cls)
+        mm = inputs.make_matrix(wt, spec.scale_f16, spec.rows, spec.cols, seed=inputs.matrix_seed("mixed_qwen", i))
+        mats.append((spec, wt, torch.from_numpy(mm.W).to(dev)))
+        nbytes += mm.W.size
+    ncopy = max(2, -(-4 * l2 // nbytes) + 1)
+    sets = [[(s, wt, W if c == 0 else W.clone()) for s, wt, W in mats] for c in range(ncopy)]
+    body_groups = [["wq", "wk", "wv"], ["wo"], ["w1", "w3"], ["w2"]]
+    for batch in wl.batches:
+        for xbf16 in (True, False):
+            xs = [xdev(inputs.make_x(batch, s.cols, xbf16, seed=inputs.x_seed("mixed_qwen", i)))
+                  for i, (s, _, _) in enumerate(mats)]
+            ys = [torch.empty((batch, s.rows), device=dev) for s, _, _ in mats]
+            idx = {s.name: i for i, (s, _, _) in enumerate(mats)}
+
+            def step(c):
+                for grp in body_groups:
+                    probs = [(sets[c][idx[n]][0].rows, sets[c][idx[n]][0].cols, sets[c][idx[n]][2], xs[idx[n]],
+                              ys[idx[n]]) for n in grp]
+                    qmv.matvec_grouped(2, 0, probs, overlap=True)
+                s, wt, W = sets[c][idx["wcls"]]
+                qmv.matvec_grouped(wt, 0, [(s.rows, s.cols, W, xs[idx["wcls"]], ys[idx["wcls"]])], overlap=True)
+            us = _graph_time_us(torch, [lambda c=c: step(c) for c in range(ncopy)] * 2, cap)
+            s, wt, W = sets[0][idx["wcls"]]
+            cls_us = _graph_time_us(torch, [lambda c=c: qmv.matvec(wt, 0, s.rows, s.cols, sets[c][idx["wcls"]][2],
+                                                                   xs[idx["wcls"]], ys[idx["wcls"]])
+                                            for c in range(ncopy)] * 2, cap)
+            cls_bytes = inputs.array_offsets(wt, 0, s.rows, s.cols)
+            cls_bytes = cls_bytes[1] + cls_bytes[2]
+            res[f"mixed_qwen_b{batch}_{'bf16' if xbf16 else 'f32'}x"] = {
+                "us_per_model_step": round(us, 3), "weight_gbs": round(nbytes / us / 1e3, 1),
+                "frac_hbm": round(nbytes / us / 1e3 / peak_hbm, 4), "tokens_per_s": round(batch / (us * 1e-6), 1),
+                "classifier_us": round(cls_us, 3), "classifier_gbs": round(cls_bytes / cls_us / 1e3, 1),
+                "classifier_frac_hbm": round(cls_bytes / cls_us / 1e3 / peak_hbm, 4)}
+    del sets, mats
+
+    # prefill: Q4_0 f16, W 14336 x 4096 and 4096 x 14336, X bf16 of 16, 64, 128 tokens
+    for i, spec in enumerate(inputs.WORKLOADS["prefill"].matrices):
+        mm = inputs.make_matrix(2, 1, spec.rows, spec.cols, seed=i)
+        Ws = copies_for(torch.from_numpy(mm.W).to(dev), mm.W.size)
+        n = len(Ws)
+        for batch in inputs.WORKLOADS["prefill"].batches:
+            x = xdev(inputs.make_x(batch, spec.cols, True, seed=1000 + i))
+            y = torch.empty((batch, spec.rows), device=dev)
+            us = _graph_time_us(torch, [lambda j=j: qmv.matvec(2, 1, spec.rows, spec.cols, Ws[j % n], x, y)
+                                        for j in range(2 * n)], cap)
+            flops = 2.0 * spec.rows * spec.cols * batch
+            res[f"prefill_{spec.rows}x{spec.cols}_b{batch}"] = {
+                "us": round(us, 3), "tflops": round(flops / us / 1e6, 1),
+                "frac_bf16_tensor_peak": round(flops / us / 1e6 / peak_tf, 4),
+                "weight_gbs": round(mm.W.size / us / 1e3, 1), "frac_hbm": round(mm.W.size / us / 1e3 / peak_hbm, 4)}
+        del Ws
+    return res
 
 # ------------------------------------------------------------------ GPU arm
 def run_ours(args, world, rank, local):
@@ -333,13 +476,18 @@ def run_ours(args, world, rank, local):
     e2e = {"value": lb * world / e2e_s / 1e9, "unit": UNIT, "h2d_bytes_per_step": int(xh.numel() * 2),
            "d2h_bytes_per_step": int(yd.numel() * 4), "ms_per_step": e2e_s * 1e3}
 
-    peak, peak_src = measured_peaks()
+    peak, peak_tf, peak_src = measured_peaks()
     achieved = lb / (ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": None, "peak_source": peak_src,
+                "frac": round(achieved / peak, 4),
+                "traffic": recorded_traffic("llama7b_decode_layer_q4_0_f16_batch1"), "peak_source": peak_src,
                 "kernel": "matvec_mma_kernel<Q4_0, f16 scales, bf16 x>",
                 "bytes_per_launch": round(lb / len(LAYER_GROUPS)),
                 "avg_launch_us": round(ms * 1e3 / len(LAYER_GROUPS), 3)}
+
+    others = None
+    if not args.no_other_configs:
+        others = other_workloads(torch, qmv, dev, l2, cap, peak, peak_tf)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -357,7 +505,7 @@ def run_ours(args, world, rank, local):
                                        f"({l2 / 1e6:.0f} MB)",
                           "step": "one CUDA graph of 4 grouped libqmv launches: {wq,wk,wv} {wo} {w1,w3} {w2}"},
                "tokens_per_s_per_layer": round(tokens_per_s * world, 1),
-               "per_matrix": per_matrix, "e2e": e2e, "roofline": roofline, "cpu_baseline": cpu,
+               "per_matrix": per_matrix, "other_workloads": others, "e2e": e2e, "roofline": roofline, "cpu_baseline": cpu,
                "clocks": clk, "gpu_launches": len(LAYER_GROUPS) * args.steps}
         print(json.dumps(out), flush=True)
 
