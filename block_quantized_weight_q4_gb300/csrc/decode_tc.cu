@@ -1,0 +1,85 @@
+// decode_tc.cu -- entry of the tensor-memory decode product (kernels in decode_tc.cuh) and
+// the per-stream workspace its split tiles use.
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "decode_tc.cuh"
+
+namespace qmv {
+
+bool decode_tc_supported(const MatrixRef& m) {
+  return m.cols % dtc::kKS == 0 && m.rows < (1LL << 31) - dtc::kTileRows && m.cols < (1LL << 30);
+}
+
+int decode_tc_max_problems() { return dtc::kMaxProblems; }
+
+// counters first, then the partial sums, 256-byte aligned
+size_t workspace_counter_bytes(int max_ctas) { return ((size_t)max_ctas * sizeof(unsigned) + 255) / 256 * 256; }
+
+size_t workspace_bytes(int max_ctas) {
+  return workspace_counter_bytes(max_ctas) + (size_t)2 * max_ctas * dtc::kMaxBatch * dtc::kTileRows * sizeof(float);
+}
+
+void workspace_carve(void* base, int max_ctas, Workspace* ws) {
+  ws->counters = static_cast<unsigned*>(base);
+  ws->partials = reinterpret_cast<float*>(static_cast<uint8_t*>(base) + workspace_counter_bytes(max_ctas));
+  ws->max_ctas = max_ctas;
+}
+
+namespace {
+std::mutex g_ws_mu;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+}  // namespace
+
+cudaError_t stream_workspace(const DeviceInfo& dev, cudaStream_t stream, Workspace* ws) {
+  auto& cache = g_ws;
+  constexpr size_t kMaxEntries = 64;
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  const auto key = std::make_pair(dev.device, stream);
+  auto it = cache.find(key);
+  if (it != cache.end()) {
+    *ws = it->second;
+    return cudaSuccess;
+  }
+  if (cache.size() >= kMaxEntries) return cudaErrorMemoryAllocation;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t err = cudaStreamIsCapturing(stream, &cs);
+  if (err != cudaSuccess) return err;
+  if (cs != cudaStreamCaptureStatusNone) return cudaErrorNotReady;  // no allocation while capturing
+  void* base = nullptr;
+  const int max_ctas = dev.sm_count;
+  err = cudaMalloc(&base, workspace_bytes(max_ctas));
+  if (err != cudaSuccess) return err;
+  err = cudaMemsetAsync(base, 0, workspace_counter_bytes(max_ctas), stream);
+  if (err != cudaSuccess) {
+    cudaFree(base);
+    return err;
+  }
+  Workspace w;
+  workspace_carve(base, max_ctas, &w);
+  cache.emplace(key, w);
+  *ws = w;
+  return cudaSuccess;
+}
+
+cudaError_t reset_workspaces() {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  for (auto& kv : g_ws) {
+    if (kv.first.first != dev) continue;
+    err = cudaMemset(kv.second.counters, 0, workspace_counter_bytes(kv.second.max_ctas));
+    if (err != cudaSuccess) return err;
+  }
+  return cudaDeviceSynchronize();
+}
+
+cudaError_t launch_decode_tc(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, int batch, bool pdl,
+                             const DeviceInfo& dev, const Workspace& ws, cudaStream_t stream) {
+  if (ms[0].wtype == QMV_Q4_0) return dtc::launch_q4(ms, xs, ys, n, batch, pdl, dev, ws, stream);
+  return dtc::launch_q8(ms, xs, ys, n, batch, pdl, dev, ws, stream);
+}
+
+}  // namespace qmv

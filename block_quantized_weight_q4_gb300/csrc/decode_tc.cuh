@@ -1,0 +1,599 @@
+// decode_tc.cuh -- the decode product (1..8 bfloat16 activation vectors per pass) on the
+// 5th-generation tensor core, with the quantized weights unpacked into tensor memory.
+//
+// What is computed (Krafla ".mlb model format v1", "Q8_0", "Q4_0", "Body"):
+//   y[n][r] = sum_k d[r][k] * sum_{j<32} level[r][32k+j] * x[n][32k+j]
+// level = nibble - 8 (Q4_0) or the int8 quant (Q8_0), exact in bfloat16.  The tensor core
+// forms each block's dot product in float32; the rows' threads scale it (float32 FFMA) and
+// add the blocks in column order.
+//
+// Work.  Units of 256 rows x 256 columns (a tile and a chunk), ordered problem, tile, chunk.
+// One persistent CTA per SM takes an equal contiguous share of the units (stream-K), so a
+// tile may be split between consecutive CTAs.  A CTA that holds a whole tile stores y; the
+// parts of a split tile are written to a workspace, and the CTA that finishes its part last
+// (an arrival counter per split tile) adds the parts in CTA order and stores y, so the result
+// does not depend on timing; it also sets the counter back to zero for the next launch.
+//
+// Roles (352 threads):
+//   warp 0     TMA producer: per unit, the q box(es) (256 rows x 128 bytes, 128-byte
+//              swizzle), the d box (256 rows x 8 scales) and the activation box (16 vectors
+//              x 256 bf16 in four 64-wide boxes, 128-byte swizzle; vectors past the batch
+//              are zero-filled) into a ring slot.  The activation box is the MMA's B operand.
+//   warps 1-2  MMA issuers, one per warpgroup (warp 1 also allocates the 512 tensor-memory
+//              columns): per unit and half (blocks 0-3, 4-7), 8 tcgen05.mma (M 128, N 16,
+//              K 16, A from tensor memory, B from shared memory); block k of the unit
+//              accumulates into columns 16k .. 16k+15.
+//   warps 3-10 two warpgroups of 128 rows; thread = row.  Per unit: load the row's quant
+//              bytes and scales from the ring slot and release it; then, per half, read the
+//              previous unit's block sums of that half from tensor memory and add d * sum
+//              into the row's accumulators, and unpack this unit's quants of that half to
+//              bf16 levels stored to tensor memory (tcgen05.st) as the next MMA's A operand.
+//              A half's MMAs run while the rows work on the other half.
+// Tensor memory, warpgroup w: A in columns 256w .. 256w+127 (row r of the warpgroup in lane
+// r, two K elements per column), block sums in columns 256w+128 .. 256w+255.
+// Every wait is bounded; a wait that runs out records QMV_E_TIMEOUT and the roles unwind.
+#pragma once
+
+#include <cstring>
+
+#include "qmv_common.cuh"
+#include "qmv_internal.h"
+#include "tcgen05.cuh"
+
+namespace qmv {
+namespace dtc {
+
+constexpr int kWG = 2;                  // row warpgroups per CTA
+constexpr int kM = 128;                 // rows per warpgroup = MMA M = tensor-memory lanes
+constexpr int kTileRows = kWG * kM;     // rows per unit
+constexpr int kKS = 256;                // columns per unit
+constexpr int kBlk = kKS / 32;          // blocks per unit
+constexpr int kN = 16;                  // MMA N: activation vectors, zero-padded
+constexpr int kMaxBatch = 8;
+constexpr int kMaxProblems = 8;
+constexpr int kRowWarps = 4 * kWG;
+constexpr int kFirstRowWarp = 1 + kWG;  // after the producer and the MMA issuers
+constexpr int kThreads = 32 * (kFirstRowWarp + kRowWarps);
+constexpr int kHalfBlk = kBlk / 2;      // blocks per half unit
+constexpr int kTmemCols = 512;
+constexpr int kWGCols = 256;            // tensor-memory columns per warpgroup: A, then block sums
+constexpr int kXBox = 64;               // activation box width (one 128-byte swizzle span of bf16)
+constexpr int kXBoxBytes = kN * 128;
+
+template <int WT, bool F16>
+struct Cfg {
+  static constexpr int QROW = WT == QMV_Q4_0 ? 128 : 256;  // q bytes per row per unit
+  static constexpr int NQBOX = QROW / 128;
+  static constexpr int QWORDS = QROW / 4;
+  static constexpr int Q_BOX = kTileRows * 128;
+  static constexpr int Q_STAGE = NQBOX * Q_BOX;
+  static constexpr int DROW = kBlk * (F16 ? 2 : 4);         // scale bytes per row per unit
+  static constexpr int DWORDS = DROW / 4;
+  static constexpr int D_STAGE = kTileRows * DROW;
+  static constexpr int X_STAGE = (kKS / kXBox) * kXBoxBytes;
+  static constexpr int OFF_D = Q_STAGE;                      // within a slot
+  static constexpr int OFF_X = Q_STAGE + D_STAGE;            // 1024-aligned
+  static constexpr int STAGE = Q_STAGE + D_STAGE + X_STAGE;  // multiple of 1024
+  static constexpr int S = WT == QMV_Q4_0 ? 4 : 2;           // ring depth
+  static constexpr int OFF_BAR = S * STAGE;
+  // full[S], empty[S], afull[kWG][2], dfull[kWG][2], flush_bar, flush_done, mma_idle[kWG]
+  static constexpr int NBARS = 2 * S + 4 * kWG + 2 + kWG;
+  static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;       // tensor-memory base, failed, last
+  static constexpr int SMEM = 1024 + OFF_MISC + 16;
+};
+
+struct Problem {
+  float* y;
+  int rows;
+  int nchunks;     // cols / 256
+  int ntiles;      // ceil(rows / 256)
+  long long unit0; // first unit of this problem
+};
+
+struct Params {
+  int nprob;
+  int batch;
+  int grid;
+  long long units;
+  int* status;
+  float* partials;              // [2 * grid][kMaxBatch][kTileRows]
+  unsigned* counters;           // [grid] arrivals, zero between launches
+  Problem pr[kMaxProblems];
+};
+
+struct Maps {
+  CUtensorMap q[kMaxProblems];
+  CUtensorMap d[kMaxProblems];
+  CUtensorMap x[kMaxProblems];
+};
+
+struct Unit {
+  int prob, tile, chunk;
+};
+
+__device__ __forceinline__ void unit_at(const Params& p, long long u, Unit& w) {
+  int pr = 0;
+  while (pr + 1 < p.nprob && u >= p.pr[pr + 1].unit0) ++pr;
+  const long long local = u - p.pr[pr].unit0;
+  w.prob = pr;
+  w.tile = (int)(local / p.pr[pr].nchunks);
+  w.chunk = (int)(local - (long long)w.tile * p.pr[pr].nchunks);
+}
+
+__device__ __forceinline__ void unit_next(const Params& p, Unit& w) {
+  if (++w.chunk == p.pr[w.prob].nchunks) {
+    w.chunk = 0;
+    if (++w.tile == p.pr[w.prob].ntiles) {
+      w.tile = 0;
+      ++w.prob;
+    }
+  }
+}
+
+// first unit of CTA c, and the CTA whose share holds unit u
+__device__ __forceinline__ long long cta_first_unit(const Params& p, long long c) { return c * p.units / p.grid; }
+__device__ __forceinline__ int cta_of_unit(const Params& p, long long u) {
+  return (int)(((u + 1) * p.grid + p.units - 1) / p.units - 1);
+}
+
+// Bounded wait that gives up at once when another role has already failed.
+__device__ __forceinline__ bool twait(uint64_t* bar, uint32_t parity, volatile int* failed, int* status) {
+  if (*failed) return false;
+  if (mbar_wait_bounded(bar, parity)) return true;
+  record_status(status, QMV_E_TIMEOUT);
+  *failed = 1;
+  return false;
+}
+
+__device__ __forceinline__ void lds128(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr) : "memory");
+}
+
+// One Q4_0 block (16 quant bytes in w[0..3]) to 32 exact bf16 levels in K order, two per
+// 32-bit column: out[j] = (e[2j], e[2j+1]); elements 0..15 are the low nibbles of bytes
+// 0..15, elements 16..31 the high nibbles.  0x4300 | n is the bfloat16 of 128 + n.
+__device__ __forceinline__ void q4_block_levels(const uint32_t* w, uint32_t (&out)[16]) {
+  constexpr uint32_t kMask = 0x000F000Fu, kMagic = 0x43004300u, kOffset = 0x43084308u;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const uint32_t b01 = prmt(w[m], 0u, 0x4140);  // bytes 4m, 4m+1 in the low bytes of the two halves
+    const uint32_t b23 = prmt(w[m], 0u, 0x4342);
+    out[2 * m] = bf16x2_sub(lop_and_or(b01, kMask, kMagic), kOffset);
+    out[2 * m + 1] = bf16x2_sub(lop_and_or(b23, kMask, kMagic), kOffset);
+    out[8 + 2 * m] = bf16x2_sub(lop_and_or(b01 >> 4, kMask, kMagic), kOffset);
+    out[9 + 2 * m] = bf16x2_sub(lop_and_or(b23 >> 4, kMask, kMagic), kOffset);
+  }
+}
+
+// One Q8_0 block (32 int8 quants in w[0..7]) to 32 exact bf16 levels in K order.  In a
+// 16-bit lane holding quant byte b (m = b & 0x7F, s its sign bit, q = m - 128 s):
+// 0x4300 | m is the bfloat16 of 128 + m, 0x4300 | (b & 0x80) that of 128 or 256.
+__device__ __forceinline__ void q8_block_levels(const uint32_t* w, uint32_t (&out)[16]) {
+  constexpr uint32_t kLow7 = 0x007F007Fu, kSign = 0x00800080u, kMagic = 0x43004300u;
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const uint32_t b01 = prmt(w[m], 0u, 0x4140);
+    const uint32_t b23 = prmt(w[m], 0u, 0x4342);
+    out[2 * m] = bf16x2_sub(lop_and_or(b01, kLow7, kMagic), lop_and_or(b01, kSign, kMagic));
+    out[2 * m + 1] = bf16x2_sub(lop_and_or(b23, kLow7, kMagic), lop_and_or(b23, kSign, kMagic));
+  }
+}
+
+// acc[n] += d[k] * S[k][n] over blocks k = k0 .. k0+3 in order, S read from the block-sum
+// columns (block k at column 16k).
+template <int NV>
+__device__ __forceinline__ void add_block_sums(uint32_t tsum, int k0, const float (&dk)[kBlk], float (&acc)[NV]) {
+  constexpr int G = NV <= 4 ? kHalfBlk : 2;  // blocks per tensor-memory read batch
+#pragma unroll
+  for (int kb = 0; kb < kHalfBlk; kb += G) {
+    uint32_t v[G][NV];
+#pragma unroll
+    for (int k = 0; k < G; ++k) {
+      const uint32_t a = tsum + (uint32_t)(16 * (k0 + kb + k));
+      if constexpr (NV == 1) tmem_ld1(a, v[k]);
+      else if constexpr (NV == 2) tmem_ld2(a, v[k]);
+      else if constexpr (NV == 4) tmem_ld4(a, v[k]);
+      else tmem_ld8(a, v[k]);
+    }
+    tmem_ld_wait();
+#pragma unroll
+    for (int k = 0; k < G; ++k)
+#pragma unroll
+      for (int n = 0; n < NV; ++n) acc[n] = fmaf(dk[k0 + kb + k], __uint_as_float(v[k][n]), acc[n]);
+  }
+}
+
+template <int WT, bool F16, int NV>
+__global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_constant__ Maps maps,
+                                                                const __grid_constant__ Params p) {
+  using C = Cfg<WT, F16>;
+  constexpr int S = C::S;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);  // 1024-aligned: swizzle atoms
+  const uint32_t sbase = smem_u32(smem);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + S;
+  uint64_t* afull = bars + 2 * S;    // [wg][half]
+  uint64_t* dfull = afull + 2 * kWG;  // [wg][half]
+  uint64_t* flush_bar = dfull + 2 * kWG;
+  uint64_t* flush_done = flush_bar + 1;
+  uint64_t* mma_idle = flush_done + 1;  // [wg]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* failed = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
+
+  const long long u0 = cta_first_unit(p, blockIdx.x);
+  const long long u1 = cta_first_unit(p, (long long)blockIdx.x + 1);
+  const int nunits = (int)(u1 - u0);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kRowWarps + kWG);  // every row warp has read the slot; the MMAs are done
+    }
+    for (int i = 0; i < 2 * kWG; ++i) {
+      mbar_init(&afull[i], 4);
+      mbar_init(&dfull[i], 1);
+    }
+    mbar_init(flush_bar, kRowWarps);
+    mbar_init(flush_done, 1);
+    for (int w = 0; w < kWG; ++w) mbar_init(&mma_idle[w], 1);
+    *failed = 0;
+    *last_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_first();
+      Unit w;
+      unit_at(p, u0, w);
+      Unit deferred[S];
+      int issued = 0;
+      bool waited = false;
+      auto load_x = [&](int s, const Unit& wx) {
+        uint8_t* xs = smem + s * C::STAGE + C::OFF_X;
+#pragma unroll
+        for (int j = 0; j < kKS / kXBox; ++j)
+          tma_load_2d_keep(xs + j * kXBoxBytes, &maps.x[wx.prob], wx.chunk * kKS + j * kXBox, 0, &full[s]);
+      };
+      for (int i = 0; i < nunits; ++i) {
+        const int s = i % S;
+        if (i >= S && !twait(&empty[s], (uint32_t)((i / S - 1) & 1), failed, p.status)) break;
+        mbar_arrive_expect_tx(&full[s], (uint32_t)C::STAGE);
+        uint8_t* slot = smem + s * C::STAGE;
+#pragma unroll
+        for (int b = 0; b < C::NQBOX; ++b)
+          tma_load_2d(slot + b * C::Q_BOX, &maps.q[w.prob], w.chunk * C::QROW + b * 128, w.tile * kTileRows,
+                      &full[s], pol);
+        tma_load_2d(slot + C::OFF_D, &maps.d[w.prob], w.chunk * C::DROW, w.tile * kTileRows, &full[s], pol);
+        if (waited) {
+          load_x(s, w);
+        } else {
+          deferred[i] = w;
+        }
+        issued = i + 1;
+        if (!waited && (i == S - 1 || i == nunits - 1)) {
+          // weights of the first stages are in flight; activations only once the preceding
+          // kernel has finished
+          griddep_wait();
+          griddep_launch_dependents();
+          waited = true;
+          for (int j = 0; j <= i; ++j) load_x(j, deferred[j]);
+        }
+        unit_next(p, w);
+      }
+      if (!waited) {
+        griddep_wait();
+        griddep_launch_dependents();
+      }
+      if (*failed) {
+        // let the copies still in flight land before the shared memory is released
+        for (int s = 0; s < S && s < issued; ++s) {
+          const int last = issued - 1 - ((issued - 1 - s) % S);  // last stage issued into slot s
+          mbar_wait_bounded(&full[last % S], (uint32_t)((last / S) & 1), 400000000LL);
+        }
+      }
+    }
+  } else if (warp < kFirstRowWarp) {
+    // ------------------------------------------------------------------ MMA issuers
+    const int wg = warp - 1;
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kM, kN);
+      const uint32_t ta = tmem + (uint32_t)(wg * kWGCols);
+      bool any = false;
+      for (int i = 0; i < nunits; ++i) {
+        const int s = i % S;
+        if (!twait(&full[s], (uint32_t)((i / S) & 1), failed, p.status)) break;
+        const uint32_t xb = sbase + s * C::STAGE + C::OFF_X;
+        bool ok = true;
+        for (int h = 0; h < 2; ++h) {
+          if (!twait(&afull[2 * wg + h], (uint32_t)(i & 1), failed, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int k = h * kHalfBlk; k < (h + 1) * kHalfBlk; ++k) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int kk = 32 * k + 16 * e;  // first K element of this MMA
+              const uint32_t b = xb + (uint32_t)((kk / kXBox) * kXBoxBytes + (kk % kXBox) * 2);
+              tc_mma_f16_ts(ta + 128 + 16 * k, ta + 16 * k + 8 * e, smem_desc_sw128(b), idesc, e != 0);
+            }
+          }
+          tc_commit(smem_u32(&dfull[2 * wg + h]));
+          any = true;
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(&empty[s]));
+      }
+      if (any) {
+        // every MMA issued above has completed before the tensor memory is released
+        tc_commit(smem_u32(&mma_idle[wg]));
+        mbar_wait_bounded(&mma_idle[wg], 0u, 400000000LL);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ rows
+    const int wg = (warp - kFirstRowWarp) >> 2;
+    const int quarter = warp & 3;  // the tensor-memory lane quarter this warp may access
+    const int rt = wg * kM + quarter * 32 + lane;  // row within the unit
+    const int sw = rt & 7;
+    const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(wg * kWGCols);
+    const uint32_t ta = tl;        // A columns
+    const uint32_t tsum = tl + 128;  // block-sum columns
+
+    float acc[NV];
+#pragma unroll
+    for (int n = 0; n < NV; ++n) acc[n] = 0.f;
+    uint32_t dprev[C::DWORDS];
+    Unit cur, prev;
+    unit_at(p, u0, cur);
+    prev = cur;
+    long long seg0 = u0;  // first unit of the open segment
+    int flushes = 0;
+
+    // the open segment [seg0, ue] of tile (pw.prob, pw.tile) is complete in acc: store it
+    auto flush = [&](const Unit& pw, long long ue) {
+      griddep_wait();  // y and the workspace are written only after the preceding kernel
+      const Problem& P = p.pr[pw.prob];
+      const long long t0 = P.unit0 + (long long)pw.tile * P.nchunks;  // the tile's first unit
+      const int grow = pw.tile * kTileRows + rt;
+      if (seg0 == t0 && ue == t0 + P.nchunks - 1) {
+        if (grow < P.rows) {
+#pragma unroll
+          for (int n = 0; n < NV; ++n)
+            if (n < p.batch) P.y[(size_t)n * P.rows + grow] = acc[n];
+        }
+        return;
+      }
+      const int me = (int)blockIdx.x;
+      const int cfirst = cta_of_unit(p, t0);
+      const int clast = cta_of_unit(p, t0 + P.nchunks - 1);
+      const int myslot = 2 * me + (t0 <= u0 ? 0 : 1);
+      float* mine = p.partials + (size_t)myslot * (kMaxBatch * kTileRows);
+#pragma unroll
+      for (int n = 0; n < NV; ++n) mine[n * kTileRows + rt] = acc[n];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(flush_bar);
+      if (threadIdx.x == 32 * kFirstRowWarp) {
+        // the CTA's parts are all written (the barrier orders them before this thread's
+        // device-scope fence, which publishes them with the arrival): count this CTA's
+        // arrival at the tile
+        bool last = false;
+        if (twait(flush_bar, (uint32_t)(flushes & 1), failed, p.status)) {
+          __threadfence();
+          const unsigned before = atomicAdd(p.counters + cfirst, 1u);
+          last = (int)before + 1 == clast - cfirst + 1;
+          if (last) {
+            p.counters[cfirst] = 0u;  // every part has arrived: ready for the next launch
+            __threadfence();          // the other CTAs' parts are visible to this CTA's rows
+          }
+        }
+        *last_flag = last ? 1 : 0;
+        mbar_arrive(flush_done);
+      }
+      const bool ok = twait(flush_done, (uint32_t)(flushes & 1), failed, p.status);
+      ++flushes;
+      if (!ok || !*last_flag) return;
+      // the last part of the tile: add all parts in CTA order
+      float sum[NV];
+#pragma unroll
+      for (int n = 0; n < NV; ++n) sum[n] = 0.f;
+      for (int c = cfirst; c <= clast; ++c) {
+        const int slot = 2 * c + (t0 <= cta_first_unit(p, c) ? 0 : 1);
+        const float* part = p.partials + (size_t)slot * (kMaxBatch * kTileRows);
+#pragma unroll
+        for (int n = 0; n < NV; ++n) sum[n] += __ldcg(part + n * kTileRows + rt);
+      }
+      if (grow < P.rows) {
+#pragma unroll
+        for (int n = 0; n < NV; ++n)
+          if (n < p.batch) P.y[(size_t)n * P.rows + grow] = sum[n];
+      }
+    };
+    auto scales = [&](const uint32_t (&dw)[C::DWORDS], float (&dk)[kBlk]) {
+#pragma unroll
+      for (int k = 0; k < kBlk; ++k) {
+        if (F16) {
+          const uint32_t v = dw[k >> 1];
+          dk[k] = f16_bits_to_f32((uint16_t)((k & 1) ? (v >> 16) : (v & 0xFFFFu)));
+        } else {
+          dk[k] = __uint_as_float(dw[k]);
+        }
+      }
+    };
+
+    // unit i's levels of half h into tensor memory: the next A operand of that half
+    auto unpack_half = [&](const uint32_t* w, int h) {
+#pragma unroll
+      for (int k = h * kHalfBlk; k < (h + 1) * kHalfBlk; ++k) {
+        uint32_t lv[16];
+        if (WT == QMV_Q4_0) {
+          q4_block_levels(&w[4 * k], lv);
+        } else {
+          q8_block_levels(&w[8 * k], lv);
+        }
+        tmem_st16(ta + (uint32_t)(16 * k), lv);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&afull[2 * wg + h]);
+    };
+    // block sums of half h of the previous unit (unit j) into acc
+    auto take_half = [&](int j, int h, const float (&dk)[kBlk]) -> bool {
+      if (!twait(&dfull[2 * wg + h], (uint32_t)(j & 1), failed, p.status)) return false;
+      tc_fence_after();
+      add_block_sums<NV>(tsum, h * kHalfBlk, dk, acc);
+      return true;
+    };
+
+    int done = 0;  // units whose A has been handed to the MMA
+    for (int i = 0; i < nunits; ++i) {
+      const int s = i % S;
+      if (!twait(&full[s], (uint32_t)((i / S) & 1), failed, p.status)) break;
+      // this row's quant bytes and scales of unit i
+      uint32_t w[C::QWORDS];
+      uint32_t dcur[C::DWORDS];
+      const uint32_t qrow = sbase + s * C::STAGE + rt * 128;
+#pragma unroll
+      for (int b = 0; b < C::NQBOX; ++b)
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          lds128(qrow + b * C::Q_BOX + ((c ^ sw) << 4), w[32 * b + 4 * c], w[32 * b + 4 * c + 1],
+                 w[32 * b + 4 * c + 2], w[32 * b + 4 * c + 3]);
+      const uint32_t drow = sbase + s * C::STAGE + C::OFF_D + rt * C::DROW;
+#pragma unroll
+      for (int j = 0; j < C::DWORDS; j += 4) lds128(drow + 4 * j, dcur[j], dcur[j + 1], dcur[j + 2], dcur[j + 3]);
+      float dk[kBlk];
+      if (i > 0) scales(dprev, dk);
+      // half 0: the previous unit's first-half sums free A and sums of half 0 (the shared
+      // memory loads above complete meanwhile; the slot is released once all are consumed)
+      if (i > 0 && !take_half(i - 1, 0, dk)) break;
+      unpack_half(w, 0);
+      if (i > 0) {
+        if (!take_half(i - 1, 1, dk)) break;
+        const long long ue = u0 + i - 1;
+        if (prev.chunk == p.pr[prev.prob].nchunks - 1) {  // unit i-1 ends its tile
+          flush(prev, ue);
+          if (*failed) break;
+#pragma unroll
+          for (int n = 0; n < NV; ++n) acc[n] = 0.f;
+          seg0 = ue + 1;
+        }
+      }
+      unpack_half(w, 1);
+      if (lane == 0) mbar_arrive(&empty[s]);  // every lane's loads of the slot are consumed
+      ++done;
+#pragma unroll
+      for (int j = 0; j < C::DWORDS; ++j) dprev[j] = dcur[j];
+      prev = cur;
+      unit_next(p, cur);
+    }
+    if (done == nunits && nunits > 0 && !*failed) {
+      float dk[kBlk];
+      scales(dprev, dk);
+      if (take_half(nunits - 1, 0, dk) && take_half(nunits - 1, 1, dk)) flush(prev, u1 - 1);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int WT, bool F16, int NV>
+cudaError_t launch_typed(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, int batch, bool pdl,
+                         const DeviceInfo& dev, const Workspace& ws, cudaStream_t stream) {
+  using C = Cfg<WT, F16>;
+  auto kern = decode_tc_kernel<WT, F16, NV>;
+  static bool ready[64] = {};
+  if (dev.device < 0 || dev.device >= 64 || n < 1 || n > kMaxProblems || batch < 1 || batch > NV)
+    return cudaErrorInvalidValue;
+  if (!ready[dev.device]) {
+    const cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (err != cudaSuccess) return err;
+    ready[dev.device] = true;
+  }
+  Params p{};
+  p.nprob = n;
+  p.batch = batch;
+  p.status = dev.status;
+  p.partials = ws.partials;
+  p.counters = ws.counters;
+  long long units = 0;
+  for (int i = 0; i < n; ++i) {
+    p.pr[i].y = ys[i];
+    p.pr[i].rows = (int)ms[i].rows;
+    p.pr[i].nchunks = (int)(ms[i].cols / kKS);
+    p.pr[i].ntiles = (int)((ms[i].rows + kTileRows - 1) / kTileRows);
+    p.pr[i].unit0 = units;
+    units += (long long)p.pr[i].ntiles * p.pr[i].nchunks;
+  }
+  int grid = dev.sm_count < ws.max_ctas ? dev.sm_count : ws.max_ctas;
+  if ((long long)grid > units) grid = (int)units;
+  if (grid < 1) return cudaErrorInvalidValue;
+  p.units = units;
+  p.grid = grid;
+
+  Maps maps;
+  memset(&maps, 0, sizeof(maps));
+  for (int i = 0; i < n; ++i) {
+    const MatrixRef& m = ms[i];
+    const uint64_t qrow = (WT == QMV_Q4_0) ? (uint64_t)m.cols / 2 : (uint64_t)m.cols;
+    const uint64_t drow = (uint64_t)(m.cols / 32) * (F16 ? 2 : 4);
+    cudaError_t err = encode_tmap_2d(&maps.q[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, m.q, qrow, (uint64_t)m.rows, qrow,
+                                     128, kTileRows, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (err != cudaSuccess) return err;
+    err = encode_tmap_2d(&maps.d[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, m.d, drow, (uint64_t)m.rows, drow, C::DROW,
+                         kTileRows, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (err != cudaSuccess) return err;
+    err = encode_tmap_2d(&maps.x[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xs[i], (uint64_t)m.cols, (uint64_t)batch,
+                         (uint64_t)m.cols * 2, kXBox, kN, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (err != cudaSuccess) return err;
+  }
+
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, maps, p);
+}
+
+template <int WT, bool F16>
+cudaError_t launch_wtype(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, int batch, bool pdl,
+                         const DeviceInfo& dev, const Workspace& ws, cudaStream_t stream) {
+  if (batch <= 1) return launch_typed<WT, F16, 1>(ms, xs, ys, n, batch, pdl, dev, ws, stream);
+  if (batch <= 2) return launch_typed<WT, F16, 2>(ms, xs, ys, n, batch, pdl, dev, ws, stream);
+  if (batch <= 4) return launch_typed<WT, F16, 4>(ms, xs, ys, n, batch, pdl, dev, ws, stream);
+  return launch_typed<WT, F16, 8>(ms, xs, ys, n, batch, pdl, dev, ws, stream);
+}
+
+cudaError_t launch_q4(const MatrixRef*, const void* const*, float* const*, int, int, bool, const DeviceInfo&,
+                      const Workspace&, cudaStream_t);
+cudaError_t launch_q8(const MatrixRef*, const void* const*, float* const*, int, int, bool, const DeviceInfo&,
+                      const Workspace&, cudaStream_t);
+
+}  // namespace dtc
+}  // namespace qmv

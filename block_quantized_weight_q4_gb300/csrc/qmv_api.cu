@@ -18,6 +18,8 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kPrefillMinBatch = 16;  // from here on the tensor-memory kernel takes bf16 batches
+constexpr int kTcMinBatch = 5;        // decode passes of this many bf16 vectors go to decode_tc
+constexpr long long kTcMinQ8Weights = 64LL << 20;  // and Q8_0 launches of this many weights
 std::mutex g_dev_mutex;
 DeviceInfo g_dev[kMaxDevices];
 bool g_dev_ready[kMaxDevices] = {};
@@ -176,7 +178,20 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
         return QMV_E_CUDA;
       }
     }
-    if (nf > 0 && launch_matvec_mma(fast, fx, fy, nf, xb, nb, pdl, dev, stream) != cudaSuccess) return QMV_E_CUDA;
+    if (nf == 0) continue;
+    // bf16 activations: the tensor-memory kernel for passes of 5 or more vectors, and for
+    // Q8_0 launches of 64M weights or more (where it measured faster), when this stream has
+    // its workspace (created on the stream's first such call, never while it is captured)
+    long long nweights = 0;
+    for (int i = 0; i < nf; ++i) nweights += fast[i].rows * fast[i].cols;
+    bool tc = xb && (nb >= kTcMinBatch || (wtype == QMV_Q8_0 && nweights >= kTcMinQ8Weights));
+    for (int i = 0; i < nf && tc; ++i) tc = decode_tc_supported(fast[i]);
+    Workspace ws;
+    if (tc && stream_workspace(dev, stream, &ws) == cudaSuccess) {
+      if (launch_decode_tc(fast, fx, fy, nf, nb, pdl, dev, ws, stream) != cudaSuccess) return QMV_E_CUDA;
+    } else if (launch_matvec_mma(fast, fx, fy, nf, xb, nb, pdl, dev, stream) != cudaSuccess) {
+      return QMV_E_CUDA;
+    }
   }
   return QMV_OK;
 }
@@ -221,6 +236,8 @@ int qmv_check_device(void) {
   if (v != 0) {
     const int zero = 0;
     if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return QMV_E_CUDA;
+    // a kernel that gave up may have left a split tile's arrival counter part-way
+    if (reset_workspaces() != cudaSuccess) return QMV_E_CUDA;
   }
   return v;
 }

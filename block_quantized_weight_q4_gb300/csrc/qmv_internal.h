@@ -58,4 +58,30 @@ int prefill_max_batch();
 cudaError_t launch_prefill(const MatrixRef& m, const void* x, float* y, int batch, const DeviceInfo& dev,
                            cudaStream_t stream);
 
+// Scratch of the tensor-memory decode product: arrival counters and the partial sums of
+// tiles split between CTAs.  One per stream (calls on one stream never overlap).  The
+// counters are zero between launches (the last arrival at a tile resets its counter).
+struct Workspace {
+  float* partials;     // [2 * max_ctas][8 vectors][256 rows]
+  unsigned* counters;  // [max_ctas] arrivals
+  int max_ctas;        // CTAs a launch may use
+};
+size_t workspace_bytes(int max_ctas);
+size_t workspace_counter_bytes(int max_ctas);
+void workspace_carve(void* base, int max_ctas, Workspace* ws);
+// The workspace of (current device, stream), allocated and zeroed on first use; returns
+// cudaErrorNotReady when there is none yet and the stream is being captured.
+cudaError_t stream_workspace(const DeviceInfo& dev, cudaStream_t stream, Workspace* ws);
+// Zero the counters of every workspace of the current device (after a kernel gave up on a
+// bounded wait, a counter may have been left part-way); synchronous.
+cudaError_t reset_workspaces();
+
+// Decode product on the 5th-generation tensor core with the weights unpacked into tensor
+// memory: bf16 activations, cols % 256 == 0, 1..8 vectors, 1..decode_tc_max_problems()
+// problems of the same wtype and scale type per launch.
+bool decode_tc_supported(const MatrixRef& m);
+int decode_tc_max_problems();
+cudaError_t launch_decode_tc(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, int batch, bool pdl,
+                             const DeviceInfo& dev, const Workspace& ws, cudaStream_t stream);
+
 }  // namespace qmv

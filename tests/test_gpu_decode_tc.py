@@ -1,0 +1,147 @@
+"""The tensor-memory decode kernel (bf16 activations, passes of 5..8 vectors, and Q8_0
+launches of 64M weights or more) vs the oracle.
+
+That kernel splits the work into units of 256 rows x 256 columns shared out evenly between
+one CTA per SM, so a tile's columns may be summed by several CTAs; the parts meet in a
+per-stream workspace and the last CTA to arrive adds them in CTA order.  These tests aim at
+that machinery: tiles split between many CTAs, tiles that end where a problem of a grouped
+launch ends, repeated calls (the arrival counters must be back at zero after every call),
+and the result's independence from timing (bit-identical across calls and graph replays).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from block_quantized_weight_q4_gb300 import inputs
+from helpers import assert_bits_equal, check_product, dev_u8, dev_x
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-3
+TYPES = [(1, 0), (1, 1), (2, 0), (2, 1)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def qmv():
+    import torch
+    from block_quantized_weight_q4_gb300.build import build
+    import block_quantized_weight_q4_gb300 as q
+    assert torch.cuda.is_available()
+    build()
+    q.load_library()
+    yield q
+    assert q.last_error() == 0
+
+
+def run(q, m, x, y=None):
+    import torch
+    y = q.matvec(m.wtype, m.scale_f16, m.rows, m.cols, dev_u8(m.W), dev_x(x), y)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+@pytest.mark.parametrize("wt,sf", TYPES)
+@pytest.mark.parametrize("rows,cols", [(256, 256), (512, 4096), (300, 2048), (2000, 1024), (4096, 4096)])
+@pytest.mark.parametrize("batch", [5, 6, 8])
+def test_tc_decode_matches_oracle(qmv, wt, sf, rows, cols, batch):
+    # 512 x 4096: 32 units on 32 CTAs, each of the two tiles split 16 ways
+    m = inputs.make_matrix(wt, sf, rows, cols, seed=rows * 7 + cols + batch)
+    x = inputs.make_x(batch, cols, True, seed=batch + rows)
+    y_ref, absref = oracle.matvec(m.W, wt, sf, rows, cols, x)
+    check_product(run(qmv, m, x), y_ref, absref, TOL, f"tc {wt},{sf} {rows}x{cols} b{batch}")
+
+
+@pytest.mark.parametrize("wt,sf", [(1, 0), (2, 1)])
+def test_tc_exact_pow2(qmv, wt, sf):
+    # power-of-two scales, integer activations: every partial sum is exact, in any split
+    rows, cols, batch = 600, 4096, 8
+    rng = np.random.default_rng(11 + wt)
+    m = inputs.make_matrix(wt, sf, rows, cols, seed=12)
+    codes = inputs.pow2_scales(rng, rows * cols // 32, sf)
+    W = inputs.assemble(wt, sf, rows, cols, m.q, codes)
+    x = inputs.make_int_x(batch, cols, True, seed=13)
+    y_ref, _ = oracle.matvec(W, wt, sf, rows, cols, x)
+    m2 = inputs.Matrix(wt, sf, rows, cols, W, m.q, codes)
+    assert np.array_equal(run(qmv, m2, x).astype(np.float64), y_ref)
+
+
+def test_tc_zero_rows_exact(qmv):
+    rows, cols, batch = 700, 2048, 6
+    m = inputs.make_matrix(2, 1, rows, cols, seed=14)
+    q = m.q.copy().reshape(rows, -1)
+    q[::7] = 0x88  # every level 0
+    W = inputs.assemble(2, 1, rows, cols, q.reshape(-1), m.d_codes)
+    m2 = inputs.Matrix(2, 1, rows, cols, W, q.reshape(-1), m.d_codes)
+    x = inputs.make_x(batch, cols, True, seed=14)
+    y_ref, absref = oracle.matvec(W, 2, 1, rows, cols, x)
+    y = run(qmv, m2, x)
+    assert np.all(y[:, ::7] == 0.0)
+    check_product(y, y_ref, absref, TOL, "tc zero rows")
+
+
+@pytest.mark.parametrize("wt,sf", [(2, 1), (1, 0)])
+def test_tc_repeated_calls_bit_identical(qmv, wt, sf):
+    # the split tiles' counters are reset by each call: later calls give the same bits
+    rows, cols, batch = 1536, 4096, 8
+    m = inputs.make_matrix(wt, sf, rows, cols, seed=15)
+    x = inputs.make_x(batch, cols, True, seed=15)
+    first = run(qmv, m, x)
+    y_ref, absref = oracle.matvec(m.W, wt, sf, rows, cols, x)
+    check_product(first, y_ref, absref, TOL, "tc first call")
+    for _ in range(3):
+        assert_bits_equal(run(qmv, m, x), first, "tc repeated call")
+
+
+def test_tc_grouped_problems(qmv):
+    # a grouped launch: units of all problems in one list, tiles ending at problem ends
+    import torch
+    shapes = [(300, 4096), (1024, 1024), (257, 2048), (4096, 256)]
+    batch = 7
+    probs, refs = [], []
+    for i, (rows, cols) in enumerate(shapes):
+        m = inputs.make_matrix(2, 1, rows, cols, seed=70 + i)
+        x = inputs.make_x(batch, cols, True, seed=80 + i)
+        y = torch.full((batch, rows), 3.0, device="cuda")
+        probs.append((rows, cols, dev_u8(m.W), dev_x(x), y))
+        refs.append(oracle.matvec(m.W, 2, 1, rows, cols, x))
+    for overlap in (False, True):
+        qmv.matvec_grouped(2, 1, probs, overlap=overlap)
+        torch.cuda.synchronize()
+        for (rows, cols, _, _, y), (y_ref, absref) in zip(probs, refs):
+            check_product(y.cpu().numpy(), y_ref, absref, TOL, f"tc grouped {rows}x{cols} overlap={overlap}")
+
+
+def test_tc_graph_replay_bit_identical(qmv):
+    # captured after an eager call on the same stream (which creates its workspace)
+    import torch
+    rows, cols, batch = 2048, 4096, 8
+    m = inputs.make_matrix(2, 1, rows, cols, seed=16)
+    W = dev_u8(m.W)
+    x = dev_x(inputs.make_x(batch, cols, True, seed=16))
+    s = torch.cuda.Stream()
+    y = torch.empty((batch, rows), device="cuda")
+    with torch.cuda.stream(s):
+        qmv.matvec(2, 1, rows, cols, W, x, y)
+    torch.cuda.synchronize()
+    eager = y.cpu().numpy().copy()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(3):
+            qmv.matvec(2, 1, rows, cols, W, x, y)
+    y.fill_(0.0)
+    for _ in range(4):
+        g.replay()
+    torch.cuda.synchronize()
+    assert_bits_equal(y.cpu().numpy(), eager, "graph replay")
+
+
+def test_tc_q8_large_launch_batch1(qmv):
+    # a Q8_0 launch of 64M weights or more takes the kernel at batch 1 too; sampled rows
+    import torch
+    rows, cols = 65536, 1024
+    m = inputs.make_matrix(1, 0, rows, cols, seed=17)
+    x = inputs.make_x(1, cols, True, seed=17)
+    y = run(qmv, m, x)
+    ids = np.arange(0, rows, 97)
+    y_ref, absref = oracle.matvec_rows(m.W, 1, 0, rows, cols, x, ids)
+    check_product(y[:, ids], y_ref, absref, TOL, "q8 large b1")
