@@ -61,6 +61,7 @@ def load_library():
     lib.qmv_matvec.argtypes = [i32, i32, i64, i64, vp, vp, i32, vp, i32, vp]
     lib.qmv_matvec_grouped.restype = i32
     lib.qmv_matvec_grouped.argtypes = [i32, i32, i32, i32, vp, i32, ctypes.c_uint, vp]
+    lib.qmv_matvec_grouped_noalloc.argtypes = [i32, i32, i32, i32, vp, i32, ctypes.c_uint, vp]
     lib.qmv_dequant.restype = i32
     lib.qmv_dequant.argtypes = [i32, i32, i64, i64, vp, vp, vp]
     lib.qmv_validate.restype = i32
@@ -140,13 +141,10 @@ class Problem(ctypes.Structure):
 
 FLAG_OVERLAP = 1
 MAX_GROUP = 8
+NOALLOC_MAX_BATCH = 8
 
 
-def matvec_grouped(wtype: int, scale_dtype: int, problems, overlap: bool = False, stream=None):
-    """Several products in one launch.  problems: list of (rows, cols, W, x, y) with W a
-    uint8 CUDA tensor, x (batch, cols) and y (batch, rows) CUDA tensors; all share wtype,
-    scale_dtype, the x dtype and batch.  overlap: QMV_FLAG_OVERLAP (the weights must not be
-    written by the preceding kernel on the stream)."""
+def _problem_array(problems):
     n = len(problems)
     if not 1 <= n <= MAX_GROUP:
         raise ValueError("1..8 problems per group")
@@ -159,9 +157,28 @@ def matvec_grouped(wtype: int, scale_dtype: int, problems, overlap: bool = False
         if not (x.is_contiguous() and y.is_contiguous()):
             raise ValueError("x and y must be contiguous")
         arr[i] = Problem(rows, cols, W.data_ptr(), x.data_ptr(), y.data_ptr())
+    return arr, n, batch, xdt
+
+
+def matvec_grouped(wtype: int, scale_dtype: int, problems, overlap: bool = False, stream=None):
+    """Several products in one launch.  problems: list of (rows, cols, W, x, y) with W a
+    uint8 CUDA tensor, x (batch, cols) and y (batch, rows) CUDA tensors; all share wtype,
+    scale_dtype, the x dtype and batch.  overlap: QMV_FLAG_OVERLAP (the weights must not be
+    written by the preceding kernel on the stream)."""
+    arr, n, batch, xdt = _problem_array(problems)
     st = load_library().qmv_matvec_grouped(wtype, scale_dtype, xdt, batch, ctypes.addressof(arr), n,
                                            FLAG_OVERLAP if overlap else 0, _stream(stream))
     _check(st, "qmv_matvec_grouped")
+
+
+def matvec_grouped_noalloc(wtype: int, scale_dtype: int, problems, overlap: bool = False, stream=None):
+    """matvec_grouped that allocates no device memory (qmv_matvec_grouped_noalloc): bfloat16
+    x, at most NOALLOC_MAX_BATCH vectors, cols % 256 == 0; its scratch is one fixed array
+    in the library, so calls that may overlap in time must be ordered on one stream."""
+    arr, n, batch, xdt = _problem_array(problems)
+    st = load_library().qmv_matvec_grouped_noalloc(wtype, scale_dtype, xdt, batch, ctypes.addressof(arr), n,
+                                                   FLAG_OVERLAP if overlap else 0, _stream(stream))
+    _check(st, "qmv_matvec_grouped_noalloc")
 
 
 def dequant(wtype: int, scale_dtype: int, rows: int, cols: int, W, out=None, stream=None):

@@ -90,6 +90,29 @@ cudaError_t current_device_info(DeviceInfo* info) {
 
 using namespace qmv;
 
+// Scratch of qmv_matvec_grouped_noalloc: split-tile arrival counters and partial sums of
+// the tensor-memory decode kernel for up to QMV_NOALLOC_MAX_CTAS CTAs, in the layout of a
+// per-stream workspace.  Zero-initialized when the module loads; every call clears the
+// counters again before its launch.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[QMV_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch on `device` (the current device), looked up once.
+static cudaError_t noalloc_scratch(int device, void** base) {
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[device] == nullptr) {
+    if (workspace_bytes(QMV_NOALLOC_MAX_CTAS) > sizeof(g_noalloc_scratch)) return cudaErrorInvalidValue;
+    void* p = nullptr;
+    const cudaError_t err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (err != cudaSuccess) return err;
+    addr[device] = p;
+  }
+  *base = addr[device];
+  return cudaSuccess;
+}
+
 extern "C" {
 
 size_t qmv_weight_bytes(int wtype, int scale_dtype, int64_t rows, int64_t cols) {
@@ -194,6 +217,39 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
     }
   }
   return QMV_OK;
+}
+
+int qmv_matvec_grouped_noalloc(int wtype, int scale_dtype, int x_dtype, int batch, const qmv_problem* problems,
+                               int n, unsigned flags, cudaStream_t stream) {
+  if (problems == nullptr || n < 1 || n > QMV_MAX_GROUP) return QMV_E_ARG;
+  if (x_dtype != QMV_X_F32 && x_dtype != QMV_X_BF16) return QMV_E_FORMAT;
+  if (batch < 0 || batch > QMV_NOALLOC_MAX_BATCH) return QMV_E_ARG;
+  if ((flags & ~QMV_FLAG_OVERLAP) != 0) return QMV_E_ARG;
+  MatrixRef ms[QMV_MAX_GROUP];
+  const void* xs[QMV_MAX_GROUP];
+  float* ys[QMV_MAX_GROUP];
+  for (int i = 0; i < n; ++i) {
+    const qmv_problem& pr = problems[i];
+    const int st = make_ref(wtype, scale_dtype, pr.rows, pr.cols, pr.W, &ms[i]);
+    if (st != QMV_OK) return st;
+    if (!decode_tc_supported(ms[i])) return QMV_E_SHAPE;
+    xs[i] = pr.x;
+    ys[i] = pr.y;
+    if (batch == 0) continue;
+    if (pr.x == nullptr || pr.y == nullptr) return QMV_E_ARG;
+    if (!aligned(pr.x, 16) || !aligned(pr.y, 4)) return QMV_E_ALIGN;
+  }
+  if (x_dtype != QMV_X_BF16) return QMV_E_FORMAT;  // the tensor-memory kernel reads bf16 only
+  if (batch == 0) return QMV_OK;
+  DeviceInfo dev;
+  if (current_device_info(&dev) != cudaSuccess) return QMV_E_CUDA;
+  void* base = nullptr;
+  if (noalloc_scratch(dev.device, &base) != cudaSuccess) return QMV_E_CUDA;
+  Workspace ws;
+  workspace_carve(base, dev.sm_count < QMV_NOALLOC_MAX_CTAS ? dev.sm_count : QMV_NOALLOC_MAX_CTAS, &ws);
+  if (cudaMemsetAsync(ws.counters, 0, workspace_counter_bytes(ws.max_ctas), stream) != cudaSuccess) return QMV_E_CUDA;
+  const bool pdl = (flags & QMV_FLAG_OVERLAP) != 0;
+  return launch_decode_tc(ms, xs, ys, n, batch, pdl, dev, ws, stream) == cudaSuccess ? QMV_OK : QMV_E_CUDA;
 }
 
 int qmv_matvec(int wtype, int scale_dtype, int64_t rows, int64_t cols, const void* W, const void* x,

@@ -140,6 +140,44 @@ typedef struct qmv_problem {
 int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const qmv_problem *problems, int n,
                        unsigned flags, cudaStream_t stream);
 
+/* Limits of qmv_matvec_grouped_noalloc. */
+#define QMV_NOALLOC_MAX_BATCH 8   /* activation vectors per call */
+#define QMV_NOALLOC_MAX_CTAS 160  /* CTAs its scratch array holds partial sums for */
+#define QMV_NOALLOC_SCRATCH_BYTES 2622208 /* size of that array (2.5 MiB + 768 bytes) */
+
+/* Allocation-free variant of qmv_matvec_grouped (the Krafla page has no counterpart: this
+ * is a property of this library's runtime, not of the format).  For callers that cannot
+ * let a library allocate device memory after start-up: an inference server that hands all
+ * free device memory to its own pool at start-up (a later cudaMalloc would fail, or eat
+ * into that pool), or a latency-critical path that cannot take cudaMalloc's implicit
+ * device synchronization.
+ *
+ * It runs the tensor-memory decode kernel (bf16 activations, weights unpacked into tensor
+ * memory, tcgen05 MMA), whose tiles may be split between CTAs; the split tiles' partial
+ * sums and arrival counters live in one fixed array inside the library
+ * (QMV_NOALLOC_SCRATCH_BYTES of device memory per device, allocated when the library is
+ * loaded) instead of the per-stream workspace that qmv_matvec_grouped allocates on a
+ * stream's first such call.  Nothing is allocated, freed or resized by this call.
+ *
+ * Same arguments and results as qmv_matvec_grouped, restricted to what that kernel takes:
+ *   x_dtype must be QMV_X_BF16, else QMV_E_FORMAT;
+ *   0 <= batch <= QMV_NOALLOC_MAX_BATCH, else QMV_E_ARG (larger batches: call once per
+ *     group of at most 8 vectors);
+ *   cols % 256 == 0 and rows < 2^31 - 256 for every problem, else QMV_E_SHAPE.
+ * All checks happen before any launch.  The kernel uses at most QMV_NOALLOC_MAX_CTAS CTAs
+ * (fewer on a device with fewer SMs).
+ *
+ * The arrival counters in the array must be zero when the kernel starts: every call first
+ * clears them on `stream` (cudaMemsetAsync of 768 bytes, not an allocation), and a call that
+ * completes leaves them at zero.  The array is shared by all calls on a device, so calls
+ * that may overlap in time (on different streams, or from different host threads without
+ * ordering) race on it and give wrong results: order them on one stream.  The first call
+ * on each device looks up the array's address (cudaGetSymbolAddress, with that device
+ * current) and sets the kernel's shared-memory limit; make that first call before
+ * capturing the stream, if the stream is to be captured. */
+int qmv_matvec_grouped_noalloc(int wtype, int scale_dtype, int x_dtype, int batch, const qmv_problem *problems,
+                               int n, unsigned flags, cudaStream_t stream);
+
 /* out[r][c] = level * d as float32, with one float32 multiplication rounded to nearest
  * even (Krafla page, "Q8_0" and "Q4_0"; f16 scales are first converted exactly to
  * float32, "The runtime converts f16 scales to f32 exactly").  No flush of subnormals;
