@@ -14,18 +14,20 @@ bool decode_tc_supported(const MatrixRef& m) {
 
 int decode_tc_max_problems() { return dtc::kMaxProblems; }
 
-// counters first, then the partial sums, 256-byte aligned
-size_t workspace_counter_bytes(int max_ctas) { return ((size_t)max_ctas * sizeof(unsigned) + 255) / 256 * 256; }
+size_t workspace_counter_bytes(int n) { return ((size_t)n * sizeof(unsigned) + 255) / 256 * 256; }
 
-size_t workspace_bytes(int max_ctas) {
-  return workspace_counter_bytes(max_ctas) + (size_t)2 * max_ctas * dtc::kMaxBatch * dtc::kTileRows * sizeof(float);
-}
-
-void workspace_carve(void* base, int max_ctas, Workspace* ws) {
+void workspace_carve(void* base, size_t bytes, int n, Workspace* ws) {
+  const size_t cb = workspace_counter_bytes(n);
   ws->counters = static_cast<unsigned*>(base);
-  ws->partials = reinterpret_cast<float*>(static_cast<uint8_t*>(base) + workspace_counter_bytes(max_ctas));
-  ws->max_ctas = max_ctas;
+  ws->max_counters = n;
+  ws->partials = reinterpret_cast<float*>(static_cast<uint8_t*>(base) + cb);
+  ws->max_partial_floats = bytes > cb ? (bytes - cb) / sizeof(float) : 0;
 }
+
+// a stream's workspace: counters for up to 1024 CTAs, then the parts (2 per CTA of 256
+// rows x 8 vectors); the kernel sizes its grid to fit
+constexpr int kStreamCounters = 1024;
+constexpr size_t kStreamWorkspaceBytes = (size_t)4 << 20;
 
 namespace {
 std::mutex g_ws_mu;
@@ -48,16 +50,15 @@ cudaError_t stream_workspace(const DeviceInfo& dev, cudaStream_t stream, Workspa
   if (err != cudaSuccess) return err;
   if (cs != cudaStreamCaptureStatusNone) return cudaErrorNotReady;  // no allocation while capturing
   void* base = nullptr;
-  const int max_ctas = dev.sm_count;
-  err = cudaMalloc(&base, workspace_bytes(max_ctas));
+  err = cudaMalloc(&base, kStreamWorkspaceBytes);
   if (err != cudaSuccess) return err;
-  err = cudaMemsetAsync(base, 0, workspace_counter_bytes(max_ctas), stream);
+  err = cudaMemsetAsync(base, 0, workspace_counter_bytes(kStreamCounters), stream);
   if (err != cudaSuccess) {
     cudaFree(base);
     return err;
   }
   Workspace w;
-  workspace_carve(base, max_ctas, &w);
+  workspace_carve(base, kStreamWorkspaceBytes, kStreamCounters, &w);
   cache.emplace(key, w);
   *ws = w;
   return cudaSuccess;
@@ -70,7 +71,7 @@ cudaError_t reset_workspaces() {
   std::lock_guard<std::mutex> lock(g_ws_mu);
   for (auto& kv : g_ws) {
     if (kv.first.first != dev) continue;
-    err = cudaMemset(kv.second.counters, 0, workspace_counter_bytes(kv.second.max_ctas));
+    err = cudaMemset(kv.second.counters, 0, workspace_counter_bytes(kv.second.max_counters));
     if (err != cudaSuccess) return err;
   }
   return cudaDeviceSynchronize();

@@ -7,30 +7,31 @@
 // forms each block's dot product in float32; the rows' threads scale it (float32 FFMA) and
 // add the blocks in column order.
 //
-// Work.  Units of 256 rows x 256 columns (a tile and a chunk), ordered problem, tile, chunk.
-// One persistent CTA per SM takes an equal contiguous share of the units (stream-K), so a
+// Work.  Units of 128 rows x 256 columns (a tile and a chunk), ordered problem, tile, chunk.
+// The persistent CTAs (two per SM) take equal contiguous shares of the units (stream-K), so a
 // tile may be split between consecutive CTAs.  A CTA that holds a whole tile stores y; the
 // parts of a split tile are written to a workspace, and the CTA that finishes its part last
 // (an arrival counter per split tile) adds the parts in CTA order and stores y, so the result
 // does not depend on timing; it also sets the counter back to zero for the next launch.
 //
-// Roles (352 threads):
-//   warp 0     TMA producer: per unit, the q box(es) (256 rows x 128 bytes, 128-byte
-//              swizzle), the d box (256 rows x 8 scales) and the activation box (16 vectors
+// Roles (224 threads; two CTAs per SM):
+//   warp 0     TMA producer: per unit, the q box(es) (128 rows x 128 bytes, 128-byte
+//              swizzle), the d box (128 rows x 8 scales) and the activation box (16 vectors
 //              x 256 bf16 in four 64-wide boxes, 128-byte swizzle; vectors past the batch
 //              are zero-filled) into a ring slot.  The activation box is the MMA's B operand.
-//   warps 1-2  MMA issuers, one per warpgroup (warp 1 also allocates the 512 tensor-memory
-//              columns): per unit and half (blocks 0-3, 4-7), 8 tcgen05.mma (M 128, N 16,
-//              K 16, A from tensor memory, B from shared memory); block k of the unit
-//              accumulates into columns 16k .. 16k+15.
-//   warps 3-10 two warpgroups of 128 rows; thread = row.  Per unit: load the row's quant
-//              bytes and scales from the ring slot and release it; then, per half, read the
-//              previous unit's block sums of that half from tensor memory and add d * sum
-//              into the row's accumulators, and unpack this unit's quants of that half to
-//              bf16 levels stored to tensor memory (tcgen05.st) as the next MMA's A operand.
-//              A half's MMAs run while the rows work on the other half.
-// Tensor memory, warpgroup w: A in columns 256w .. 256w+127 (row r of the warpgroup in lane
-// r, two K elements per column), block sums in columns 256w+128 .. 256w+255.
+//   warps 1-2  MMA issuers (warp 1 also allocates the 256 tensor-memory columns): warp 1+h
+//              issues, per unit, the 8 tcgen05.mma (M 128, N 16, K 16, A from tensor memory,
+//              B from shared memory) of half h (blocks 4h .. 4h+3), block k accumulating into
+//              columns 128+16k .. 128+16k+15.  One thread issues about one MMA per 90 cycles,
+//              so the SM's four issuing warps (two CTAs) keep four streams of MMAs going.
+//   warps 3-6  128 rows, thread = row.  Per unit and half (blocks 0-3, 4-7): load the row's
+//              quant bytes of that half from the ring slot, read the previous unit's block
+//              sums of that half from tensor memory and add d * sum into the row's
+//              accumulators, unpack the quants to bf16 levels and store them to tensor memory
+//              (tcgen05.st) as the next MMA's A operand.  A half's MMAs run while the rows
+//              work on the other half.
+// Tensor memory: A in columns 0..127 (row r in lane r, two K elements per column), block sums
+// in columns 128..255.
 // Every wait is bounded; a wait that runs out records QMV_E_TIMEOUT and the roles unwind.
 #pragma once
 
@@ -43,28 +44,30 @@
 namespace qmv {
 namespace dtc {
 
-constexpr int kWG = 2;                  // row warpgroups per CTA
-constexpr int kM = 128;                 // rows per warpgroup = MMA M = tensor-memory lanes
-constexpr int kTileRows = kWG * kM;     // rows per unit
+constexpr int kM = 128;                 // rows per CTA tile = MMA M = tensor-memory lanes
+constexpr int kTileRows = kM;           // rows per unit
 constexpr int kKS = 256;                // columns per unit
 constexpr int kBlk = kKS / 32;          // blocks per unit
 constexpr int kN = 16;                  // MMA N: activation vectors, zero-padded
 constexpr int kMaxBatch = 8;
 constexpr int kMaxProblems = 8;
-constexpr int kRowWarps = 4 * kWG;
-constexpr int kFirstRowWarp = 1 + kWG;  // after the producer and the MMA issuers
+constexpr int kIssuers = 2;             // MMA-issuing warps, one per half unit
+constexpr int kRowWarps = 4;
+constexpr int kFirstRowWarp = 1 + kIssuers;  // after the producer and the MMA issuers
 constexpr int kThreads = 32 * (kFirstRowWarp + kRowWarps);
 constexpr int kHalfBlk = kBlk / 2;      // blocks per half unit
-constexpr int kTmemCols = 512;
-constexpr int kWGCols = 256;            // tensor-memory columns per warpgroup: A, then block sums
+constexpr int kTmemCols = 256;          // A, then block sums
+constexpr int kSumCol = 128;            // first block-sum column
 constexpr int kXBox = 64;               // activation box width (one 128-byte swizzle span of bf16)
 constexpr int kXBoxBytes = kN * 128;
+constexpr int kPart = kMaxBatch * kTileRows;  // floats of one part of a split tile
 
 template <int WT, bool F16>
 struct Cfg {
   static constexpr int QROW = WT == QMV_Q4_0 ? 128 : 256;  // q bytes per row per unit
   static constexpr int NQBOX = QROW / 128;
   static constexpr int QWORDS = QROW / 4;
+  static constexpr int QHALF = QWORDS / 2;                   // quant words per row per half
   static constexpr int Q_BOX = kTileRows * 128;
   static constexpr int Q_STAGE = NQBOX * Q_BOX;
   static constexpr int DROW = kBlk * (F16 ? 2 : 4);         // scale bytes per row per unit
@@ -74,10 +77,12 @@ struct Cfg {
   static constexpr int OFF_D = Q_STAGE;                      // within a slot
   static constexpr int OFF_X = Q_STAGE + D_STAGE;            // 1024-aligned
   static constexpr int STAGE = Q_STAGE + D_STAGE + X_STAGE;  // multiple of 1024
-  static constexpr int S = WT == QMV_Q4_0 ? 4 : 2;           // ring depth
+  // ring depth: two CTAs per SM within 228 KB of shared memory (and 120 registers per
+  // thread, so that two CTAs fit the register file)
+  static constexpr int S = WT == QMV_Q4_0 ? (F16 ? 4 : 3) : 2;
   static constexpr int OFF_BAR = S * STAGE;
-  // full[S], empty[S], afull[kWG][2], dfull[kWG][2], flush_bar, flush_done, mma_idle[kWG]
-  static constexpr int NBARS = 2 * S + 4 * kWG + 2 + kWG;
+  // full[S], empty[S], afull[2], dfull[2], flush_bar, flush_done, mma_idle[kIssuers]
+  static constexpr int NBARS = 2 * S + 4 + 2 + kIssuers;
   static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;       // tensor-memory base, failed, last
   static constexpr int SMEM = 1024 + OFF_MISC + 16;
 };
@@ -86,7 +91,7 @@ struct Problem {
   float* y;
   int rows;
   int nchunks;     // cols / 256
-  int ntiles;      // ceil(rows / 256)
+  int ntiles;      // ceil(rows / 128)
   long long unit0; // first unit of this problem
 };
 
@@ -96,7 +101,7 @@ struct Params {
   int grid;
   long long units;
   int* status;
-  float* partials;              // [2 * grid][kMaxBatch][kTileRows]
+  float* partials;              // [2 * grid][kMaxBatch][kTileRows] parts of split tiles
   unsigned* counters;           // [grid] arrivals, zero between launches
   Problem pr[kMaxProblems];
 };
@@ -134,6 +139,12 @@ __device__ __forceinline__ void unit_next(const Params& p, Unit& w) {
 __device__ __forceinline__ long long cta_first_unit(const Params& p, long long c) { return c * p.units / p.grid; }
 __device__ __forceinline__ int cta_of_unit(const Params& p, long long u) {
   return (int)(((u + 1) * p.grid + p.units - 1) / p.units - 1);
+}
+
+__device__ __forceinline__ unsigned atomic_add_acq_rel(unsigned* addr, unsigned v) {
+  unsigned old;
+  asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+  return old;
 }
 
 // Bounded wait that gives up at once when another role has already failed.
@@ -204,7 +215,7 @@ __device__ __forceinline__ void add_block_sums(uint32_t tsum, int k0, const floa
 }
 
 template <int WT, bool F16, int NV>
-__global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_constant__ Maps maps,
+__global__ void __maxnreg__(120) decode_tc_kernel(const __grid_constant__ Maps maps,
                                                                 const __grid_constant__ Params p) {
   using C = Cfg<WT, F16>;
   constexpr int S = C::S;
@@ -218,11 +229,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
-  uint64_t* afull = bars + 2 * S;    // [wg][half]
-  uint64_t* dfull = afull + 2 * kWG;  // [wg][half]
-  uint64_t* flush_bar = dfull + 2 * kWG;
+  uint64_t* afull = bars + 2 * S;  // [half]
+  uint64_t* dfull = afull + 2;     // [half]
+  uint64_t* flush_bar = dfull + 2;
   uint64_t* flush_done = flush_bar + 1;
-  uint64_t* mma_idle = flush_done + 1;  // [wg]
+  uint64_t* mma_idle = flush_done + 1;  // [issuer]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* failed = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
@@ -234,15 +245,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kRowWarps + kWG);  // every row warp has read the slot; the MMAs are done
+      mbar_init(&empty[i], kRowWarps + kIssuers);  // every row warp has read the slot; its MMAs are done
     }
-    for (int i = 0; i < 2 * kWG; ++i) {
-      mbar_init(&afull[i], 4);
-      mbar_init(&dfull[i], 1);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&afull[h], kRowWarps);
+      mbar_init(&dfull[h], 1);  // the issuer of that half
     }
     mbar_init(flush_bar, kRowWarps);
     mbar_init(flush_done, 1);
-    for (int w = 0; w < kWG; ++w) mbar_init(&mma_idle[w], 1);
+    for (int j = 0; j < kIssuers; ++j) mbar_init(&mma_idle[j], 1);
     *failed = 0;
     *last_flag = 0;
     fence_mbar_init();
@@ -308,52 +319,44 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     }
   } else if (warp < kFirstRowWarp) {
     // ------------------------------------------------------------------ MMA issuers
-    const int wg = warp - 1;
+    const int j = warp - 1;  // issuer j: half h = j of every unit
+    const int h = j;
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(kM, kN);
-      const uint32_t ta = tmem + (uint32_t)(wg * kWGCols);
       bool any = false;
       for (int i = 0; i < nunits; ++i) {
         const int s = i % S;
         if (!twait(&full[s], (uint32_t)((i / S) & 1), failed, p.status)) break;
+        if (!twait(&afull[h], (uint32_t)(i & 1), failed, p.status)) break;
+        tc_fence_after();
         const uint32_t xb = sbase + s * C::STAGE + C::OFF_X;
-        bool ok = true;
-        for (int h = 0; h < 2; ++h) {
-          if (!twait(&afull[2 * wg + h], (uint32_t)(i & 1), failed, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
 #pragma unroll
-          for (int k = h * kHalfBlk; k < (h + 1) * kHalfBlk; ++k) {
+        for (int k = h * kHalfBlk; k < (h + 1) * kHalfBlk; ++k) {
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int kk = 32 * k + 16 * e;  // first K element of this MMA
-              const uint32_t b = xb + (uint32_t)((kk / kXBox) * kXBoxBytes + (kk % kXBox) * 2);
-              tc_mma_f16_ts(ta + 128 + 16 * k, ta + 16 * k + 8 * e, smem_desc_sw128(b), idesc, e != 0);
-            }
+          for (int e = 0; e < 2; ++e) {
+            const int kk = 32 * k + 16 * e;  // first K element of this MMA
+            const uint32_t b = xb + (uint32_t)((kk / kXBox) * kXBoxBytes + (kk % kXBox) * 2);
+            tc_mma_f16_ts(tmem + kSumCol + 16 * k, tmem + 16 * k + 8 * e, smem_desc_sw128(b), idesc, e != 0);
           }
-          tc_commit(smem_u32(&dfull[2 * wg + h]));
-          any = true;
         }
-        if (!ok) break;
+        tc_commit(smem_u32(&dfull[h]));
         tc_commit(smem_u32(&empty[s]));
+        any = true;
       }
       if (any) {
         // every MMA issued above has completed before the tensor memory is released
-        tc_commit(smem_u32(&mma_idle[wg]));
-        mbar_wait_bounded(&mma_idle[wg], 0u, 400000000LL);
+        tc_commit(smem_u32(&mma_idle[j]));
+        mbar_wait_bounded(&mma_idle[j], 0u, 400000000LL);
       }
     }
   } else {
     // ------------------------------------------------------------------ rows
-    const int wg = (warp - kFirstRowWarp) >> 2;
     const int quarter = warp & 3;  // the tensor-memory lane quarter this warp may access
-    const int rt = wg * kM + quarter * 32 + lane;  // row within the unit
+    const int rt = quarter * 32 + lane;  // row within the unit
     const int sw = rt & 7;
-    const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(wg * kWGCols);
-    const uint32_t ta = tl;        // A columns
-    const uint32_t tsum = tl + 128;  // block-sum columns
+    const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t ta = tl;             // A columns
+    const uint32_t tsum = tl + kSumCol;  // block-sum columns
 
     float acc[NV];
 #pragma unroll
@@ -382,25 +385,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       const int me = (int)blockIdx.x;
       const int cfirst = cta_of_unit(p, t0);
       const int clast = cta_of_unit(p, t0 + P.nchunks - 1);
+      // the tile is this CTA's first segment when it starts at or before the first unit
       const int myslot = 2 * me + (t0 <= u0 ? 0 : 1);
-      float* mine = p.partials + (size_t)myslot * (kMaxBatch * kTileRows);
+      float* mine = p.partials + (size_t)myslot * kPart;
 #pragma unroll
       for (int n = 0; n < NV; ++n) mine[n * kTileRows + rt] = acc[n];
       __syncwarp();
       if (lane == 0) mbar_arrive(flush_bar);
       if (threadIdx.x == 32 * kFirstRowWarp) {
         // the CTA's parts are all written (the barrier orders them before this thread's
-        // device-scope fence, which publishes them with the arrival): count this CTA's
-        // arrival at the tile
+        // release): count this CTA's arrival at the tile
         bool last = false;
         if (twait(flush_bar, (uint32_t)(flushes & 1), failed, p.status)) {
-          __threadfence();
-          const unsigned before = atomicAdd(p.counters + cfirst, 1u);
+          const unsigned before = atomic_add_acq_rel(p.counters + cfirst, 1u);
           last = (int)before + 1 == clast - cfirst + 1;
-          if (last) {
-            p.counters[cfirst] = 0u;  // every part has arrived: ready for the next launch
-            __threadfence();          // the other CTAs' parts are visible to this CTA's rows
-          }
+          if (last) p.counters[cfirst] = 0u;  // every part has arrived: ready for the next launch
         }
         *last_flag = last ? 1 : 0;
         mbar_arrive(flush_done);
@@ -408,15 +407,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       const bool ok = twait(flush_done, (uint32_t)(flushes & 1), failed, p.status);
       ++flushes;
       if (!ok || !*last_flag) return;
-      // the last part of the tile: add all parts in CTA order
+      // the last part of the tile: add all parts in CTA order, four in flight at a time
       float sum[NV];
 #pragma unroll
       for (int n = 0; n < NV; ++n) sum[n] = 0.f;
-      for (int c = cfirst; c <= clast; ++c) {
-        const int slot = 2 * c + (t0 <= cta_first_unit(p, c) ? 0 : 1);
-        const float* part = p.partials + (size_t)slot * (kMaxBatch * kTileRows);
+      for (int c = cfirst; c <= clast; c += 4) {
+        float v[4][NV];
 #pragma unroll
-        for (int n = 0; n < NV; ++n) sum[n] += __ldcg(part + n * kTileRows + rt);
+        for (int q = 0; q < 4; ++q) {
+          const int cc = c + q;
+          const int slot = 2 * cc + (t0 * p.grid <= (long long)cc * p.units ? 0 : 1);
+          const float* part = p.partials + (size_t)slot * kPart;
+#pragma unroll
+          for (int n = 0; n < NV; ++n) v[q][n] = cc <= clast ? __ldcg(part + n * kTileRows + rt) : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int n = 0; n < NV; ++n) sum[n] += v[q][n];
       }
       if (grow < P.rows) {
 #pragma unroll
@@ -435,27 +443,37 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         }
       }
     };
-
-    // unit i's levels of half h into tensor memory: the next A operand of that half
-    auto unpack_half = [&](const uint32_t* w, int h) {
+    // this row's quant words of half h of the unit in slot s
+    auto load_half = [&](int s, int h, uint32_t (&w)[C::QHALF]) {
+      const uint32_t qrow = sbase + s * C::STAGE + rt * 128;
+      constexpr int CH = C::QHALF / 4;  // 16-byte chunks per half
 #pragma unroll
-      for (int k = h * kHalfBlk; k < (h + 1) * kHalfBlk; ++k) {
+      for (int c = 0; c < CH; ++c) {
+        const int chunk = h * CH + c;            // chunk of the row's unit bytes
+        const int box = chunk / 8, cb = chunk % 8;  // 128-byte box and chunk within it
+        lds128(qrow + box * C::Q_BOX + ((cb ^ sw) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+      }
+    };
+    // the levels of half h into tensor memory: the next A operand of that half
+    auto unpack_half = [&](const uint32_t (&w)[C::QHALF], int h) {
+#pragma unroll
+      for (int k = 0; k < kHalfBlk; ++k) {
         uint32_t lv[16];
         if (WT == QMV_Q4_0) {
           q4_block_levels(&w[4 * k], lv);
         } else {
           q8_block_levels(&w[8 * k], lv);
         }
-        tmem_st16(ta + (uint32_t)(16 * k), lv);
+        tmem_st16(ta + (uint32_t)(16 * (h * kHalfBlk + k)), lv);
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&afull[2 * wg + h]);
+      if (lane == 0) mbar_arrive(&afull[h]);
     };
-    // block sums of half h of the previous unit (unit j) into acc
+    // block sums of half h of unit j into acc
     auto take_half = [&](int j, int h, const float (&dk)[kBlk]) -> bool {
-      if (!twait(&dfull[2 * wg + h], (uint32_t)(j & 1), failed, p.status)) return false;
+      if (!twait(&dfull[h], (uint32_t)(j & 1), failed, p.status)) return false;
       tc_fence_after();
       add_block_sums<NV>(tsum, h * kHalfBlk, dk, acc);
       return true;
@@ -465,25 +483,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     for (int i = 0; i < nunits; ++i) {
       const int s = i % S;
       if (!twait(&full[s], (uint32_t)((i / S) & 1), failed, p.status)) break;
-      // this row's quant bytes and scales of unit i
-      uint32_t w[C::QWORDS];
+      uint32_t w[C::QHALF];
       uint32_t dcur[C::DWORDS];
-      const uint32_t qrow = sbase + s * C::STAGE + rt * 128;
-#pragma unroll
-      for (int b = 0; b < C::NQBOX; ++b)
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          lds128(qrow + b * C::Q_BOX + ((c ^ sw) << 4), w[32 * b + 4 * c], w[32 * b + 4 * c + 1],
-                 w[32 * b + 4 * c + 2], w[32 * b + 4 * c + 3]);
+      load_half(s, 0, w);
       const uint32_t drow = sbase + s * C::STAGE + C::OFF_D + rt * C::DROW;
 #pragma unroll
-      for (int j = 0; j < C::DWORDS; j += 4) lds128(drow + 4 * j, dcur[j], dcur[j + 1], dcur[j + 2], dcur[j + 3]);
+      for (int k = 0; k < C::DWORDS; k += 4) lds128(drow + 4 * k, dcur[k], dcur[k + 1], dcur[k + 2], dcur[k + 3]);
       float dk[kBlk];
       if (i > 0) scales(dprev, dk);
-      // half 0: the previous unit's first-half sums free A and sums of half 0 (the shared
-      // memory loads above complete meanwhile; the slot is released once all are consumed)
+      // half 0: the previous unit's first-half sums free A and sums of half 0
       if (i > 0 && !take_half(i - 1, 0, dk)) break;
       unpack_half(w, 0);
+      load_half(s, 1, w);
       if (i > 0) {
         if (!take_half(i - 1, 1, dk)) break;
         const long long ue = u0 + i - 1;
@@ -499,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       if (lane == 0) mbar_arrive(&empty[s]);  // every lane's loads of the slot are consumed
       ++done;
 #pragma unroll
-      for (int j = 0; j < C::DWORDS; ++j) dprev[j] = dcur[j];
+      for (int k = 0; k < C::DWORDS; ++k) dprev[k] = dcur[k];
       prev = cur;
       unit_next(p, cur);
     }
@@ -526,7 +537,10 @@ cudaError_t launch_typed(const MatrixRef* ms, const void* const* xs, float* cons
   if (dev.device < 0 || dev.device >= 64 || n < 1 || n > kMaxProblems || batch < 1 || batch > NV)
     return cudaErrorInvalidValue;
   if (!ready[dev.device]) {
-    const cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (err != cudaSuccess) return err;
+    // the whole carve-out for shared memory, so that two CTAs fit on an SM
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (err != cudaSuccess) return err;
     ready[dev.device] = true;
   }
@@ -545,9 +559,18 @@ cudaError_t launch_typed(const MatrixRef* ms, const void* const* xs, float* cons
     p.pr[i].unit0 = units;
     units += (long long)p.pr[i].ntiles * p.pr[i].nchunks;
   }
-  int grid = dev.sm_count < ws.max_ctas ? dev.sm_count : ws.max_ctas;
-  if ((long long)grid > units) grid = (int)units;
-  if (grid < 1) return cudaErrorInvalidValue;
+  // two CTAs per SM: shared memory (<= 113 KB each), registers (120 x 224 each) and tensor
+  // memory (256 columns each) hold two.  (The occupancy query reports one CTA per SM for any
+  // kernel that allocates tensor memory, so it is not used here.)  Within the workspace's
+  // counters and parts, and no more CTAs than units.
+  static_assert(2 * (C::SMEM + 1024) <= 233472, "two CTAs per SM by shared memory");
+  static_assert(2 * kTmemCols <= 512, "two CTAs per SM by tensor memory");
+  long long cap = 2LL * dev.sm_count;
+  if (cap > ws.max_counters) cap = ws.max_counters;
+  const long long by_parts = (long long)(ws.max_partial_floats / ((size_t)2 * kPart));
+  if (cap > by_parts) cap = by_parts;
+  if (cap > units) cap = units;
+  const int grid = (int)cap;
   p.units = units;
   p.grid = grid;
 

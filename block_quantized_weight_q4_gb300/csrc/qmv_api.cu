@@ -18,7 +18,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kPrefillMinBatch = 16;  // from here on the tensor-memory kernel takes bf16 batches
-constexpr int kTcMinBatch = 5;        // decode passes of this many bf16 vectors go to decode_tc
+constexpr int kTcMinBatch = 4;        // decode passes of this many bf16 vectors go to decode_tc
 constexpr long long kTcMinQ8Weights = 64LL << 20;  // and Q8_0 launches of this many weights
 std::mutex g_dev_mutex;
 DeviceInfo g_dev[kMaxDevices];
@@ -103,7 +103,6 @@ static cudaError_t noalloc_scratch(int device, void** base) {
   if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
   if (addr[device] == nullptr) {
-    if (workspace_bytes(QMV_NOALLOC_MAX_CTAS) > sizeof(g_noalloc_scratch)) return cudaErrorInvalidValue;
     void* p = nullptr;
     const cudaError_t err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (err != cudaSuccess) return err;
@@ -202,9 +201,10 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
       }
     }
     if (nf == 0) continue;
-    // bf16 activations: the tensor-memory kernel for passes of 5 or more vectors, and for
+    // bf16 activations: the tensor-memory kernel for passes of 4 or more vectors, and for
     // Q8_0 launches of 64M weights or more (where it measured faster), when this stream has
-    // its workspace (created on the stream's first such call, never while it is captured)
+    // its workspace (created on the stream's first such call, never while it is captured);
+    // else the mma.sync kernel
     long long nweights = 0;
     for (int i = 0; i < nf; ++i) nweights += fast[i].rows * fast[i].cols;
     bool tc = xb && (nb >= kTcMinBatch || (wtype == QMV_Q8_0 && nweights >= kTcMinQ8Weights));
@@ -246,8 +246,9 @@ int qmv_matvec_grouped_noalloc(int wtype, int scale_dtype, int x_dtype, int batc
   void* base = nullptr;
   if (noalloc_scratch(dev.device, &base) != cudaSuccess) return QMV_E_CUDA;
   Workspace ws;
-  workspace_carve(base, dev.sm_count < QMV_NOALLOC_MAX_CTAS ? dev.sm_count : QMV_NOALLOC_MAX_CTAS, &ws);
-  if (cudaMemsetAsync(ws.counters, 0, workspace_counter_bytes(ws.max_ctas), stream) != cudaSuccess) return QMV_E_CUDA;
+  workspace_carve(base, sizeof(g_noalloc_scratch), QMV_NOALLOC_MAX_CTAS, &ws);
+  if (cudaMemsetAsync(ws.counters, 0, workspace_counter_bytes(ws.max_counters), stream) != cudaSuccess)
+    return QMV_E_CUDA;
   const bool pdl = (flags & QMV_FLAG_OVERLAP) != 0;
   return launch_decode_tc(ms, xs, ys, n, batch, pdl, dev, ws, stream) == cudaSuccess ? QMV_OK : QMV_E_CUDA;
 }

@@ -25,6 +25,26 @@ struct DeviceInfo {
   int* status;  // device address of this device's status word
 };
 
+// Scratch of the tensor-memory decode kernel: arrival counters and the parts of tiles split
+// between CTAs.  One per stream (calls on one stream never overlap).  The counters are zero
+// between launches (the last arrival at a tile resets its counter).
+struct Workspace {
+  unsigned* counters;         // arrival counters
+  int max_counters;
+  float* partials;            // parts of split tiles
+  size_t max_partial_floats;
+};
+// Bytes of the counter region for n counters (a multiple of 256); carve `bytes` at `base`
+// into n counters followed by the parts.
+size_t workspace_counter_bytes(int n);
+void workspace_carve(void* base, size_t bytes, int n, Workspace* ws);
+// The workspace of (current device, stream), allocated and zeroed on first use; returns
+// cudaErrorNotReady when there is none yet and the stream is being captured.
+cudaError_t stream_workspace(const DeviceInfo& dev, cudaStream_t stream, Workspace* ws);
+// Zero the counters of every workspace of the current device (after a kernel gave up on a
+// bounded wait, a counter may have been left part-way); synchronous.
+cudaError_t reset_workspaces();
+
 // 2-D tiled tensor map over a row-major array: inner_elems elements of `dtype`
 // (a CUtensorMapDataType) per row, `outer` rows, rows row_stride_bytes apart; box of
 // box_inner x box_outer elements; swizzle is a CUtensorMapSwizzle; out-of-range reads
@@ -57,24 +77,6 @@ bool prefill_supported(const MatrixRef& m, bool x_bf16);
 int prefill_max_batch();
 cudaError_t launch_prefill(const MatrixRef& m, const void* x, float* y, int batch, const DeviceInfo& dev,
                            cudaStream_t stream);
-
-// Scratch of the tensor-memory decode product: arrival counters and the partial sums of
-// tiles split between CTAs.  One per stream (calls on one stream never overlap).  The
-// counters are zero between launches (the last arrival at a tile resets its counter).
-struct Workspace {
-  float* partials;     // [2 * max_ctas][8 vectors][256 rows]
-  unsigned* counters;  // [max_ctas] arrivals
-  int max_ctas;        // CTAs a launch may use
-};
-size_t workspace_bytes(int max_ctas);
-size_t workspace_counter_bytes(int max_ctas);
-void workspace_carve(void* base, int max_ctas, Workspace* ws);
-// The workspace of (current device, stream), allocated and zeroed on first use; returns
-// cudaErrorNotReady when there is none yet and the stream is being captured.
-cudaError_t stream_workspace(const DeviceInfo& dev, cudaStream_t stream, Workspace* ws);
-// Zero the counters of every workspace of the current device (after a kernel gave up on a
-// bounded wait, a counter may have been left part-way); synchronous.
-cudaError_t reset_workspaces();
 
 // Decode product on the 5th-generation tensor core with the weights unpacked into tensor
 // memory: bf16 activations, cols % 256 == 0, 1..8 vectors, 1..decode_tc_max_problems()

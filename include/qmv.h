@@ -99,10 +99,16 @@ int qmv_matrix_wtype(int file_wtype, uint32_t q8_mask, int class_bit, int shared
  *   batch : number of activation vectors, >= 0; 0 launches nothing and returns QMV_OK.
  * Each block contributes d * sum_j level_j * x_j; sums are kept in float32.  Batches
  * below 16 (and float32 activations) run in passes of up to 8 vectors through the decode
- * kernels (weights decoded in registers to exact bfloat16 levels, tensor-core mma, f32
- * scale and accumulate).  bfloat16 batches of 16 and more (cols % 256 == 0) run in passes
- * of up to 128 through the prefill kernel (each weight dequantized as qmv_dequant does and
- * rounded to bfloat16 in shared memory, tcgen05 MMA into tensor memory, f32 accumulate).
+ * kernels (weights decoded to exact bfloat16 levels, one tensor-core dot product per block,
+ * f32 scale and accumulate): passes of 4 or more bf16 vectors, and Q8_0 launches of 64M
+ * weights or more, take the tensor-memory kernel (levels stored to tensor memory, tcgen05
+ * MMA), the rest the mma.sync kernel.  The tensor-memory kernel splits tiles between CTAs;
+ * their parts meet in a workspace of the calling stream (4 MiB of device memory, allocated
+ * on the stream's first such call and kept; while a stream without one is being captured,
+ * the call takes the mma.sync kernel instead).  Results do not depend on timing.
+ * bfloat16 batches of 16 and more (cols % 256 == 0) run in passes of up to 128 through the
+ * prefill kernel (each weight dequantized as qmv_dequant does and rounded to bfloat16 in
+ * shared memory, tcgen05 MMA into tensor memory, f32 accumulate).
  * Products agree with an
  * exact evaluation to within 1e-3 * sum_c |W[r][c] x[c]| per output.  A Q8_0 byte of
  * -128 is not rejected here: it decodes as -128 * d (see qmv_validate).
@@ -142,8 +148,8 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
 
 /* Limits of qmv_matvec_grouped_noalloc. */
 #define QMV_NOALLOC_MAX_BATCH 8   /* activation vectors per call */
-#define QMV_NOALLOC_MAX_CTAS 160  /* CTAs its scratch array holds partial sums for */
-#define QMV_NOALLOC_SCRATCH_BYTES 2622208 /* size of that array (2.5 MiB + 768 bytes) */
+#define QMV_NOALLOC_MAX_CTAS 320  /* CTAs its scratch array holds partial sums for */
+#define QMV_NOALLOC_SCRATCH_BYTES 2622976 /* size of that array (2.5 MiB + 1536 bytes) */
 
 /* Allocation-free variant of qmv_matvec_grouped (the Krafla page has no counterpart: this
  * is a property of this library's runtime, not of the format).  For callers that cannot
@@ -168,7 +174,7 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
  * (fewer on a device with fewer SMs).
  *
  * The arrival counters in the array must be zero when the kernel starts: every call first
- * clears them on `stream` (cudaMemsetAsync of 768 bytes, not an allocation), and a call that
+ * clears them on `stream` (cudaMemsetAsync of 1536 bytes, not an allocation), and a call that
  * completes leaves them at zero.  The array is shared by all calls on a device, so calls
  * that may overlap in time (on different streams, or from different host threads without
  * ordering) race on it and give wrong results: order them on one stream.  The first call
