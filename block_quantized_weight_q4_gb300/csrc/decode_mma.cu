@@ -7,9 +7,10 @@
 // How:
 //   * Work.  A warp owns tiles of 16*MT rows (MT = 2 for Q4_0, 1 for Q8_0: one or two 16-row
 //     MMA tiles sharing the activation fragments); the columns are cut into chunks of 256
-//     weights (8 blocks).  A CTA of 4 warps takes items of (4/ks) tiles x ks column slices
-//     and walks its items persistently (item = blockIdx.x, + gridDim.x, ...); each warp sees
-//     one continuous stream of stages across its items.
+//     weights (8 blocks).  A CTA of NW warps (4, or 8 or 16 for launches with few tiles) takes items
+//     of (NW/ks) tiles x ks column slices and walks its items persistently (item =
+//     blockIdx.x, + gridDim.x, ...); each warp sees one continuous stream of stages across
+//     its items.
 //   * Streams.  Each warp has its own ring of S shared-memory stages.  Lane 0 fills a stage
 //     with 2-D TMA loads: the (16*MT)-row x 128-byte q box (128-byte swizzle; two boxes for
 //     Q8_0), the (16*MT)-row x 8-scale d box, and the batch x 256 activation box.  Rows past
@@ -37,6 +38,7 @@
 // f32 activations are split x = hi + lo (two bfloat16s, hi = RN(x)) and take two MMAs each,
 // which keeps 16 significant bits of x.
 #include <cstring>
+#include <mutex>
 
 #include "qmv_common.cuh"
 #include "qmv_internal.h"
@@ -45,7 +47,7 @@ namespace qmv {
 
 namespace {
 
-constexpr int kWarps = 4;            // warps per CTA
+constexpr int kMaxWarps = 16;        // warps per CTA: 4, or 8 or 16 for launches with few tiles
 constexpr int kTK = 256;             // weights per stage and row
 constexpr int kBlocksPerStage = kTK / 32;
 constexpr int kRows = 16;            // rows per MMA tile
@@ -53,8 +55,9 @@ constexpr int kBox = 128;            // q box inner extent in bytes (the 128-byt
 constexpr int kMaxBatch = 8;         // activation vectors per pass (the MMA's N)
 constexpr int kMaxProblems = 8;      // problems per grouped launch
 
-template <int WT, bool F16, bool XBF16>
+template <int WT, bool F16, bool XBF16, int NW>
 struct Cfg {
+  static constexpr int kWarps = NW;
   static constexpr int MT = (WT == QMV_Q4_0) ? 2 : 1;           // 16-row MMA tiles per warp tile
   static constexpr int WROWS = MT * kRows;                        // rows per warp tile
   static constexpr int NQBOX = (WT == QMV_Q4_0) ? 1 : 2;        // q boxes per stage
@@ -64,7 +67,7 @@ struct Cfg {
   static constexpr int DROW = kBlocksPerStage * (F16 ? 2 : 4);    // scale bytes per row per stage
   static constexpr int D_STAGE = WROWS * DROW;                     // multiple of 128
   static constexpr int XROW = kTK * (XBF16 ? 2 : 4);              // activation bytes per vector per stage
-  static constexpr int S = 3;                                      // ring depth
+  static constexpr int S = NW >= 16 ? 2 : 3;                       // ring depth (16 warps: 2, to fit)
   static constexpr int Q_WARP = S * Q_STAGE;
   static constexpr int D_WARP = S * D_STAGE;
   static constexpr int RED_FLOATS = kWarps * WROWS * 8;
@@ -91,7 +94,7 @@ struct Problem {
 struct Params {
   int nprob;
   int batch;    // 1..8
-  int ks;       // column slices per tile (1, 2, 4); at most every problem's nchunks
+  int ks;       // column slices per tile (1, 2, 4, 8, 16); at most every problem's nchunks
   int nitems;
   int* status;
   Problem pr[kMaxProblems];
@@ -117,16 +120,17 @@ __device__ __forceinline__ void cursor_load(Cursor& c, const Params& p, int tile
   c.prob = pr;
   c.tile = (c.item - p.pr[pr].item0) * tiles_per_item + tile_local;
   const int nch = p.pr[pr].nchunks;
-  const int lg = p.ks == 1 ? 0 : (p.ks == 2 ? 1 : 2);  // ks is 1, 2 or 4
+  const int lg = 31 - __clz(p.ks);  // ks is a power of two
   c.c0 = (kslice * nch) >> lg;
   c.n = (((kslice + 1) * nch) >> lg) - c.c0;
   c.j = 0;
 }
 
-template <int WT, bool F16, bool XBF16>
-__global__ void __launch_bounds__(kWarps * 32) matvec_mma_kernel(const __grid_constant__ Maps maps,
-                                                                 const __grid_constant__ Params p) {
-  using C = Cfg<WT, F16, XBF16>;
+template <int WT, bool F16, bool XBF16, int NW>
+__global__ void __launch_bounds__(NW * 32) matvec_mma_kernel(const __grid_constant__ Maps maps,
+                                                             const __grid_constant__ Params p) {
+  using C = Cfg<WT, F16, XBF16, NW>;
+  constexpr int kWarps = NW;
   constexpr int MT = C::MT;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -402,52 +406,58 @@ __global__ void __launch_bounds__(kWarps * 32) matvec_mma_kernel(const __grid_co
   }
 }
 
-template <int WT, bool F16, bool XBF16>
-cudaError_t launch_typed(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, int batch,
-                         bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
-  using C = Cfg<WT, F16, XBF16>;
-  auto kern = matvec_mma_kernel<WT, F16, XBF16>;
-  // per device and batch: shared-memory limit raised and occupancy known
+// One warps-per-CTA choice's plan for a launch: column split, item count, grid, and the
+// estimated stages on the critical path (the stages of an even share of all items plus one
+// item's stages for the tail, plus half a stage per item for the CTA-wide reduction that a
+// split needs).
+struct Plan {
+  int ks = 1, nitems = 0, grid = 0, smem = 0;
+  long cost = -1;
+};
+
+template <int WT, bool F16, bool XBF16, int NW>
+cudaError_t plan_typed(const MatrixRef* ms, int n, int batch, const DeviceInfo& dev, Plan* out) {
+  using C = Cfg<WT, F16, XBF16, NW>;
+  auto kern = matvec_mma_kernel<WT, F16, XBF16, NW>;
+  // per device: the shared-memory limit raised as far as the batches seen need; per device
+  // and batch: occupancy known (0 = this warps-per-CTA choice does not fit)
+  static std::mutex mu;
+  static int attr_smem[64] = {};
   static bool ready[64][kMaxBatch + 1] = {};
   static int ctas_per_sm[64][kMaxBatch + 1] = {};
   if (dev.device < 0 || dev.device >= 64 || batch < 1 || batch > kMaxBatch || n < 1 || n > kMaxProblems)
     return cudaErrorInvalidValue;
   const int smem = C::smem_bytes(batch);
-  if (!ready[dev.device][batch]) {
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::smem_bytes(kMaxBatch));
-    if (err != cudaSuccess) return err;
-    int k = 0;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&k, kern, kWarps * 32, smem);
-    if (err != cudaSuccess) return err;
-    ctas_per_sm[dev.device][batch] = k > 0 ? k : 1;
-    ready[dev.device][batch] = true;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ready[dev.device][batch]) {
+      int k = 0;
+      if ((size_t)smem <= dev.smem_optin) {
+        if (smem > attr_smem[dev.device]) {
+          const cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+          if (err != cudaSuccess) return err;
+          attr_smem[dev.device] = smem;
+        }
+        const cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&k, kern, NW * 32, smem);
+        if (err != cudaSuccess) return err;
+      }
+      ctas_per_sm[dev.device][batch] = k;
+      ready[dev.device][batch] = true;
+    }
   }
+  *out = Plan{};
+  if (ctas_per_sm[dev.device][batch] == 0) return cudaSuccess;  // does not fit: cost stays -1
   const long slots = (long)ctas_per_sm[dev.device][batch] * dev.sm_count;
-
-  Params p{};
-  p.nprob = n;
-  p.batch = batch;
-  p.status = dev.status;
-  int min_chunks = 1 << 30;
-  for (int i = 0; i < n; ++i) {
-    p.pr[i].y = ys[i];
-    p.pr[i].rows = (int)ms[i].rows;
-    p.pr[i].cols = (int)ms[i].cols;
-    p.pr[i].ntiles = (int)((ms[i].rows + C::WROWS - 1) / C::WROWS);
-    p.pr[i].nchunks = (int)(ms[i].cols / kTK);
-    if (p.pr[i].nchunks < min_chunks) min_chunks = p.pr[i].nchunks;
-  }
-  // column split: fewest stages on the critical path, estimated as the stages of an even
-  // share of all items plus one item's stages (the tail), plus half a stage per item for the
-  // CTA-wide reduction that a split needs; ties go to fewer slices
-  int best_ks = 1;
-  long best_cost = -1;
-  for (int ks = 1; ks <= kWarps && ks <= min_chunks; ks *= 2) {
-    const int tpi = kWarps / ks;
+  long min_chunks = 1L << 30;
+  for (int i = 0; i < n; ++i)
+    if (ms[i].cols / kTK < min_chunks) min_chunks = ms[i].cols / kTK;
+  Plan best;
+  for (int ks = 1; ks <= NW && ks <= min_chunks; ks *= 2) {
+    const int tpi = NW / ks;
     long items = 0, units = 0, longest = 0;
     for (int i = 0; i < n; ++i) {
-      const long it = (p.pr[i].ntiles + tpi - 1) / tpi;
-      const long st = (p.pr[i].nchunks + ks - 1) / ks;
+      const long it = ((ms[i].rows + C::WROWS - 1) / C::WROWS + tpi - 1) / tpi;
+      const long st = (ms[i].cols / kTK + ks - 1) / ks;
       items += it;
       units += it * st;
       if (st > longest) longest = st;
@@ -455,20 +465,40 @@ cudaError_t launch_typed(const MatrixRef* ms, const void* const* xs, float* cons
     const long grid = items < slots ? items : slots;
     const long per_cta = (items + grid - 1) / grid;
     const long cost = 2 * ((units + grid - 1) / grid + longest) + (ks > 1 ? per_cta : 0);
-    if (best_cost < 0 || cost < best_cost) {
-      best_cost = cost;
-      best_ks = ks;
+    if (best.cost < 0 || cost < best.cost) {
+      best.cost = cost;
+      best.ks = ks;
+      best.nitems = (int)items;
+      best.grid = (int)grid;
     }
   }
-  p.ks = best_ks;
-  const int tpi = kWarps / best_ks;
+  best.smem = smem;
+  *out = best;
+  return cudaSuccess;
+}
+
+template <int WT, bool F16, bool XBF16, int NW>
+cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* const* xs, float* const* ys, int n,
+                         int batch, bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
+  using C = Cfg<WT, F16, XBF16, NW>;
+  Params p{};
+  p.nprob = n;
+  p.batch = batch;
+  p.status = dev.status;
+  p.ks = plan.ks;
+  const int tpi = NW / plan.ks;
   int items = 0;
   for (int i = 0; i < n; ++i) {
+    p.pr[i].y = ys[i];
+    p.pr[i].rows = (int)ms[i].rows;
+    p.pr[i].cols = (int)ms[i].cols;
+    p.pr[i].ntiles = (int)((ms[i].rows + C::WROWS - 1) / C::WROWS);
+    p.pr[i].nchunks = (int)(ms[i].cols / kTK);
     p.pr[i].item0 = items;
     items += (p.pr[i].ntiles + tpi - 1) / tpi;
   }
+  if (items != plan.nitems) return cudaErrorInvalidValue;
   p.nitems = items;
-  const int grid = (int)(items < slots ? items : slots);
 
   Maps maps;
   memset(&maps, 0, sizeof(maps));
@@ -489,16 +519,39 @@ cudaError_t launch_typed(const MatrixRef* ms, const void* const* xs, float* cons
   }
 
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kWarps * 32);
-  cfg.dynamicSmemBytes = smem;
+  cfg.gridDim = dim3(plan.grid);
+  cfg.blockDim = dim3(NW * 32);
+  cfg.dynamicSmemBytes = plan.smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, maps, p);
+  return cudaLaunchKernelEx(&cfg, matvec_mma_kernel<WT, F16, XBF16, NW>, maps, p);
+}
+
+// 4 warps per CTA; when that leaves SMs without a CTA (a launch with few tiles), 8 or 16
+// warps per CTA instead if the plan estimates them shorter (ties to fewer warps).  With
+// every SM busy, more warps per CTA measured slower (they share the SM's issue slots).
+template <int WT, bool F16, bool XBF16>
+cudaError_t launch_best(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, int batch, bool pdl,
+                        const DeviceInfo& dev, cudaStream_t stream) {
+  Plan p4, p8, p16;
+  cudaError_t err = plan_typed<WT, F16, XBF16, 4>(ms, n, batch, dev, &p4);
+  if (err != cudaSuccess) return err;
+  if (p4.cost >= 0 && p4.grid > dev.sm_count)
+    return launch_typed<WT, F16, XBF16, 4>(p4, ms, xs, ys, n, batch, pdl, dev, stream);
+  err = plan_typed<WT, F16, XBF16, 8>(ms, n, batch, dev, &p8);
+  if (err != cudaSuccess) return err;
+  err = plan_typed<WT, F16, XBF16, 16>(ms, n, batch, dev, &p16);
+  if (err != cudaSuccess) return err;
+  auto better = [](const Plan& a, const Plan& b) { return a.cost >= 0 && (b.cost < 0 || a.cost < b.cost); };
+  if (better(p16, p8) && better(p16, p4))
+    return launch_typed<WT, F16, XBF16, 16>(p16, ms, xs, ys, n, batch, pdl, dev, stream);
+  if (better(p8, p4)) return launch_typed<WT, F16, XBF16, 8>(p8, ms, xs, ys, n, batch, pdl, dev, stream);
+  if (p4.cost < 0) return cudaErrorInvalidConfiguration;
+  return launch_typed<WT, F16, XBF16, 4>(p4, ms, xs, ys, n, batch, pdl, dev, stream);
 }
 
 }  // namespace
@@ -513,15 +566,15 @@ cudaError_t launch_matvec_mma(const MatrixRef* ms, const void* const* xs, float*
                               int batch, bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
   const MatrixRef& m = ms[0];
   if (m.wtype == QMV_Q4_0) {
-    if (m.scale_f16) return x_bf16 ? launch_typed<QMV_Q4_0, true, true>(ms, xs, ys, n, batch, pdl, dev, stream)
-                                   : launch_typed<QMV_Q4_0, true, false>(ms, xs, ys, n, batch, pdl, dev, stream);
-    return x_bf16 ? launch_typed<QMV_Q4_0, false, true>(ms, xs, ys, n, batch, pdl, dev, stream)
-                  : launch_typed<QMV_Q4_0, false, false>(ms, xs, ys, n, batch, pdl, dev, stream);
+    if (m.scale_f16) return x_bf16 ? launch_best<QMV_Q4_0, true, true>(ms, xs, ys, n, batch, pdl, dev, stream)
+                                   : launch_best<QMV_Q4_0, true, false>(ms, xs, ys, n, batch, pdl, dev, stream);
+    return x_bf16 ? launch_best<QMV_Q4_0, false, true>(ms, xs, ys, n, batch, pdl, dev, stream)
+                  : launch_best<QMV_Q4_0, false, false>(ms, xs, ys, n, batch, pdl, dev, stream);
   }
-  if (m.scale_f16) return x_bf16 ? launch_typed<QMV_Q8_0, true, true>(ms, xs, ys, n, batch, pdl, dev, stream)
-                                 : launch_typed<QMV_Q8_0, true, false>(ms, xs, ys, n, batch, pdl, dev, stream);
-  return x_bf16 ? launch_typed<QMV_Q8_0, false, true>(ms, xs, ys, n, batch, pdl, dev, stream)
-                : launch_typed<QMV_Q8_0, false, false>(ms, xs, ys, n, batch, pdl, dev, stream);
+  if (m.scale_f16) return x_bf16 ? launch_best<QMV_Q8_0, true, true>(ms, xs, ys, n, batch, pdl, dev, stream)
+                                 : launch_best<QMV_Q8_0, true, false>(ms, xs, ys, n, batch, pdl, dev, stream);
+  return x_bf16 ? launch_best<QMV_Q8_0, false, true>(ms, xs, ys, n, batch, pdl, dev, stream)
+                : launch_best<QMV_Q8_0, false, false>(ms, xs, ys, n, batch, pdl, dev, stream);
 }
 
 }  // namespace qmv
