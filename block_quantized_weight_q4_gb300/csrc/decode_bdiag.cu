@@ -1,0 +1,539 @@
+// decode_bdiag.cu -- the decode product for one bfloat16 activation vector, cols % 256 == 0.
+//
+// What is computed (Krafla ".mlb model format v1", "Q8_0", "Q4_0", "Body"):
+//   y[r] = sum_k d[r][k] * sum_{j<32} level[r][32k+j] * x[32k+j]
+// with level = nibble - 8 (Q4_0) or the int8 quant (Q8_0), d the block's scale.
+//
+// The stream of stages, the work split (warp tiles of 16*MT rows, 256-column chunks, items
+// of NW/ks tiles x ks column slices walked persistently), the per-warp TMA rings and the
+// overlap with the preceding kernel are those of the general decode kernel
+// (decode_mma.cu).  What changes with a single vector:
+//   * Block-diagonal activations.  The 8 columns of an m16n8k16 MMA are spent on the 8
+//     weight blocks of a stage instead of on 8 vectors: the MMA of block j multiplies 16
+//     rows' levels of block j by an activation fragment whose column j holds x of block j
+//     and whose other columns are zero.  After the stage's 16 MMAs (8 blocks x 2 halves)
+//     column j of the accumulator is each row's block-j dot product, and the thread holding
+//     it (g, t with j = 2t or 2t+1) applies that row's block-j scale: 4 FFMA per 16 rows and
+//     stage instead of 32.  Lanes g = j hold x of block j in the fragment of block j; each
+//     lane writes its 16 activation bytes to a slot of its own and reads, for block j, that
+//     slot (j = g) or a shared zero line (j != g).  At the end of an item the four lanes t
+//     that share rows g, g+8 add their blocks' sums (two xor shuffles).
+//   * Half-precision operands.  When every activation of the stage converts exactly to IEEE
+//     half (zero, and bfloat16 values with 2^-17 <= |x| <= 65280; tested by converting back),
+//     levels and activations enter the MMA as f16, whose 10-bit mantissa holds a whole quant
+//     byte (0x6400 | b is 1024 + b): Q4_0 levels then cost 2 integer and 2 half operations
+//     per byte pair instead of 4 and 2 (see q4_word_to_f16_levels).  The products are the
+//     same exact products as with bfloat16 operands.  A stage whose activations are not all
+//     exact halves (larger, tinier, NaN) uses bfloat16 operands, as the general kernel does.
+#include <cstring>
+#include <mutex>
+
+#include "qmv_common.cuh"
+#include "qmv_internal.h"
+
+namespace qmv {
+
+namespace {
+
+constexpr int kTK = 256;             // weights per stage and row
+constexpr int kBlocksPerStage = kTK / 32;
+constexpr int kRows = 16;            // rows per MMA tile
+constexpr int kBox = 128;            // q box inner extent in bytes (the 128-byte swizzle span)
+constexpr int kMaxProblems = 8;      // problems per grouped launch
+constexpr int kXStage = kTK * 2;     // bfloat16 activations of one stage, bytes
+
+template <int WT, bool F16, int NW>
+struct Cfg {
+  static constexpr int MT = (WT == QMV_Q4_0) ? 2 : 1;           // 16-row MMA tiles per warp tile
+  static constexpr int WROWS = MT * kRows;                        // rows per warp tile
+  static constexpr int NQBOX = (WT == QMV_Q4_0) ? 1 : 2;        // q boxes per stage
+  static constexpr int Q_BOX_BYTES = WROWS * kBox;
+  static constexpr int Q_STAGE = NQBOX * Q_BOX_BYTES;             // 4096 bytes, multiple of 1024
+  static constexpr int QROW = NQBOX * kBox;                        // q bytes per row per stage
+  static constexpr int DROW = kBlocksPerStage * (F16 ? 2 : 4);    // scale bytes per row per stage
+  static constexpr int D_STAGE = WROWS * DROW;                     // multiple of 256
+  static constexpr int S = NW >= 16 ? 2 : 3;                       // ring depth
+  static constexpr int Q_WARP = S * Q_STAGE;
+  static constexpr int D_WARP = S * D_STAGE;
+  static constexpr int X_WARP = S * kXStage;
+  // q rings, d rings, activation rings, activation slots (32 lanes x 16 bytes per warp),
+  // zero line, reduction buffer (split-K), barriers
+  static constexpr int OFF_D = NW * Q_WARP;
+  static constexpr int OFF_X = OFF_D + NW * D_WARP;
+  static constexpr int OFF_SLOT = OFF_X + NW * X_WARP;
+  static constexpr int OFF_ZERO = OFF_SLOT + NW * 512;
+  static constexpr int OFF_RED = OFF_ZERO + 128;
+  static constexpr int OFF_BAR = OFF_RED + ((NW * WROWS * 4 + 127) / 128) * 128;
+  static constexpr int SMEM = 1024 + OFF_BAR + ((NW * S * 8 + 127) / 128) * 128;
+};
+
+struct Problem {
+  float* y;
+  int rows;
+  int ntiles;   // warp tiles (16*MT rows)
+  int nchunks;  // cols / 256
+  int item0;    // first item of this problem in the group's item list
+};
+
+struct Params {
+  int nprob;
+  int ks;       // column slices per tile (1, 2, 4, 8, 16); at most every problem's nchunks
+  int nitems;
+  int* status;
+  Problem pr[kMaxProblems];
+};
+
+struct Maps {  // per problem: q (128-byte swizzle), d, and activation tensor maps
+  CUtensorMap q[kMaxProblems];
+  CUtensorMap d[kMaxProblems];
+  CUtensorMap x[kMaxProblems];
+};
+
+// Position of a warp in its stream of stages (as in the general decode kernel).
+struct Cursor {
+  int item, prob, tile, c0, n, j;
+};
+
+__device__ __forceinline__ void cursor_load(Cursor& c, const Params& p, int tiles_per_item, int tile_local,
+                                            int kslice) {
+  if (c.item >= p.nitems) return;
+  int pr = 0;
+  while (pr + 1 < p.nprob && c.item >= p.pr[pr + 1].item0) ++pr;
+  c.prob = pr;
+  c.tile = (c.item - p.pr[pr].item0) * tiles_per_item + tile_local;
+  const int nch = p.pr[pr].nchunks;
+  const int lg = 31 - __clz(p.ks);  // ks is a power of two
+  c.c0 = (kslice * nch) >> lg;
+  c.n = (((kslice + 1) * nch) >> lg) - c.c0;
+  c.j = 0;
+}
+
+// One stage of one warp: the 16*MT x 256 weights at qs (q, swizzled) and ds (scales), x
+// block j read through bsrc[j]; adds each row's scaled block sums of blocks 2t, 2t+1 to acc.
+template <int WT, bool F16, int NW, bool HALF>
+__device__ __forceinline__ void stage_math(float (&acc)[Cfg<WT, F16, NW>::MT][2], uint32_t qs, const uint8_t* ds,
+                                           const uint32_t (&bsrc)[kBlocksPerStage], int lrow, int lsub, int sw,
+                                           int g, int t) {
+  using C = Cfg<WT, F16, NW>;
+  constexpr int MT = C::MT;
+  float da[MT][4], db[MT][4];  // block sums of elements 0..15 and 16..31, column j = block j
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) da[mt][i] = db[mt][i] = 0.f;
+#pragma unroll
+  for (int bp = 0; bp < kBlocksPerStage / 2; ++bp) {
+    uint32_t w[MT][4];  // Q4_0: [tile][row g blk 2bp, row g+8 blk 2bp, row g blk 2bp+1, row g+8 blk 2bp+1]
+    if (WT == QMV_Q4_0) {
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+        ldmatrix_x4(w[mt][0], w[mt][1], w[mt][2], w[mt][3],
+                    qs + (16 * mt + lrow) * kBox + (((2 * bp + lsub) ^ sw) << 4));
+    }
+#pragma unroll
+    for (int hb = 0; hb < 2; ++hb) {
+      const int k = 2 * bp + hb;
+      uint32_t b[4];  // elements (4t, 4t+1), (4t+2, 4t+3), (16+4t, ..), (18+4t, ..) of block k, or zeros
+      lds_u32x4(bsrc[k], b);
+      if (WT == QMV_Q4_0) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          uint32_t g01, g23, gh01, gh23, h01, h23, hh01, hh23;
+          if (HALF) {
+            q4_word_to_f16_levels(w[mt][2 * hb], g01, g23, gh01, gh23);      // row g
+            q4_word_to_f16_levels(w[mt][2 * hb + 1], h01, h23, hh01, hh23);  // row g + 8
+            mma_f16_16816(da[mt], g01, h01, g23, h23, b[0], b[1], da[mt]);
+            mma_f16_16816(db[mt], gh01, hh01, gh23, hh23, b[2], b[3], db[mt]);
+          } else {
+            q4_word_to_bf16_levels(w[mt][2 * hb], g01, g23, gh01, gh23);
+            q4_word_to_bf16_levels(w[mt][2 * hb + 1], h01, h23, hh01, hh23);
+            mma_bf16_16816(da[mt], g01, h01, g23, h23, b[0], b[1], da[mt]);
+            mma_bf16_16816(db[mt], gh01, hh01, gh23, hh23, b[2], b[3], db[mt]);
+          }
+        }
+      } else {
+        // Q8_0: block k = chunks 2k, 2k+1 of the stage (box k / 4)
+        uint32_t q[4];  // row g half 0, row g+8 half 0, row g half 1, row g+8 half 1
+        const int chunk = 2 * (k & 3) + lsub;
+        ldmatrix_x4(q[0], q[1], q[2], q[3], qs + (k >> 2) * C::Q_BOX_BYTES + lrow * kBox + ((chunk ^ sw) << 4));
+        uint32_t g0a, g0b, h0a, h0b, g1a, g1b, h1a, h1b;
+        if (HALF) {
+          q8_word_to_f16_levels(q[0], g0a, g0b);
+          q8_word_to_f16_levels(q[1], h0a, h0b);
+          q8_word_to_f16_levels(q[2], g1a, g1b);
+          q8_word_to_f16_levels(q[3], h1a, h1b);
+          mma_f16_16816(da[0], g0a, h0a, g0b, h0b, b[0], b[1], da[0]);
+          mma_f16_16816(db[0], g1a, h1a, g1b, h1b, b[2], b[3], db[0]);
+        } else {
+          q8_word_to_bf16_levels(q[0], g0a, g0b);
+          q8_word_to_bf16_levels(q[1], h0a, h0b);
+          q8_word_to_bf16_levels(q[2], g1a, g1b);
+          q8_word_to_bf16_levels(q[3], h1a, h1b);
+          mma_bf16_16816(da[0], g0a, h0a, g0b, h0b, b[0], b[1], da[0]);
+          mma_bf16_16816(db[0], g1a, h1a, g1b, h1b, b[2], b[3], db[0]);
+        }
+      }
+    }
+  }
+  // columns 2t, 2t+1 = blocks 2t, 2t+1; fragment entries [2h], [2h+1] are row g + 8h
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint8_t* dr = ds + (16 * mt + 8 * h + g) * C::DROW;
+      float d0, d1;
+      if (F16) {
+        const uint32_t v = *reinterpret_cast<const uint32_t*>(dr + 4 * t);
+        d0 = f16_bits_to_f32((uint16_t)(v & 0xFFFF));
+        d1 = f16_bits_to_f32((uint16_t)(v >> 16));
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(dr + 8 * t);
+        d0 = v.x;
+        d1 = v.y;
+      }
+      const float s0 = da[mt][2 * h] + db[mt][2 * h];
+      const float s1 = da[mt][2 * h + 1] + db[mt][2 * h + 1];
+      acc[mt][h] = fmaf(d1, s1, fmaf(d0, s0, acc[mt][h]));
+    }
+  }
+}
+
+template <int WT, bool F16, int NW>
+__global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_constant__ Maps maps,
+                                                               const __grid_constant__ Params p) {
+  using C = Cfg<WT, F16, NW>;
+  constexpr int MT = C::MT;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);  // 1024-aligned: swizzle atoms
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2;
+  const int t = lane & 3;
+
+  uint8_t* qring = smem + warp * C::Q_WARP;
+  uint8_t* dring = smem + C::OFF_D + warp * C::D_WARP;
+  uint8_t* xring = smem + C::OFF_X + warp * C::X_WARP;
+  const uint32_t slot = smem_u32(smem + C::OFF_SLOT + warp * 512 + lane * 16);
+  const uint32_t zline = smem_u32(smem + C::OFF_ZERO);
+  float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + warp * C::S;
+
+  const int tiles_per_item = NW / p.ks;
+  const int tile_local = warp / p.ks;
+  const int kslice = warp % p.ks;
+  constexpr uint32_t stage_tx = (uint32_t)(C::Q_STAGE + C::D_STAGE + kXStage);
+
+  if (threadIdx.x < 32) reinterpret_cast<uint32_t*>(smem + C::OFF_ZERO)[threadIdx.x] = 0u;
+  if (lane == 0) {
+    for (int s = 0; s < C::S; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();  // zero line and barriers visible
+  const uint64_t pol_stream = l2_policy_evict_first();
+
+  // producer cursor: runs S-1 stages ahead of the consumer cursor
+  Cursor pc;
+  pc.item = (int)blockIdx.x;
+  cursor_load(pc, p, tiles_per_item, tile_local, kslice);
+  int ps = 0;
+  int issued = 0;
+  // fill ring slot ps from the producer cursor; with_x = false defers the activation box
+  auto issue = [&](bool with_x) {
+    if (lane == 0) {
+      const Problem& P = p.pr[pc.prob];
+      if (pc.tile < P.ntiles) {
+        const int c = pc.c0 + pc.j;
+        mbar_arrive_expect_tx(&bars[ps], stage_tx);
+        fence_proxy_async_smem();
+#pragma unroll
+        for (int b = 0; b < C::NQBOX; ++b)
+          tma_load_2d(qring + ps * C::Q_STAGE + b * C::Q_BOX_BYTES, &maps.q[pc.prob], c * C::QROW + b * kBox,
+                      pc.tile * C::WROWS, &bars[ps], pol_stream);
+        tma_load_2d(dring + ps * C::D_STAGE, &maps.d[pc.prob], c * C::DROW, pc.tile * C::WROWS, &bars[ps],
+                    pol_stream);
+        if (with_x) tma_load_2d_keep(xring + ps * kXStage, &maps.x[pc.prob], c * kTK, 0, &bars[ps]);
+      } else {
+        mbar_arrive(&bars[ps]);  // a tile past the end of its problem: complete the phase, no data
+      }
+    }
+  };
+  auto advance = [&](Cursor& c) {
+    if (++c.j == c.n) {
+      c.item += (int)gridDim.x;
+      cursor_load(c, p, tiles_per_item, tile_local, kslice);
+    }
+  };
+
+  // prologue: weight boxes of the first S-1 stages may be requested before the preceding
+  // kernel has finished; activations only after griddepcontrol.wait
+  int pre_c[C::S], pre_prob[C::S];
+  bool pre_valid[C::S];
+  int pre = 0;
+  while (pre < C::S - 1 && pc.item < p.nitems) {
+    pre_c[pre] = pc.c0 + pc.j;
+    pre_prob[pre] = pc.prob;
+    pre_valid[pre] = pc.tile < p.pr[pc.prob].ntiles;
+    issue(false);
+    ps = (ps + 1 == C::S) ? 0 : ps + 1;
+    advance(pc);
+    ++pre;
+  }
+  issued = pre;
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  if (lane == 0) {
+    for (int i = 0; i < pre; ++i)
+      if (pre_valid[i]) tma_load_2d_keep(xring + i * kXStage, &maps.x[pre_prob[i]], pre_c[i] * kTK, 0, &bars[i]);
+  }
+
+  // ldmatrix: lane supplies row (lane & 7) + 8 * (matrix & 1), 16-byte chunk (matrix >> 1)
+  const int lm = lane >> 3;
+  const int lrow = (lane & 7) + ((lm & 1) << 3);
+  const int lsub = lm >> 1;
+  const int sw = lrow & 7;  // 128-byte swizzle: physical chunk = logical chunk ^ (row & 7)
+  // activation fragment source of block j: this lane's slot for j = g, else the zero line
+  uint32_t bsrc[kBlocksPerStage];
+#pragma unroll
+  for (int j = 0; j < kBlocksPerStage; ++j) bsrc[j] = (j == g) ? slot : zline;
+
+  float acc[MT][2];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = 0.f;
+  bool failed = false;
+  int cs = 0;          // consumer ring slot
+  uint32_t phase = 0;  // its parity
+  int consumed = 0;
+  Cursor cc;
+  cc.item = (int)blockIdx.x;
+  cursor_load(cc, p, tiles_per_item, tile_local, kslice);
+  while (cc.item < p.nitems) {
+    const Problem& P = p.pr[cc.prob];
+    const bool valid = cc.tile < P.ntiles;
+    if (!failed) {
+      if (pc.item < p.nitems) {
+        issue(true);
+        ps = (ps + 1 == C::S) ? 0 : ps + 1;
+        advance(pc);
+        ++issued;
+      }
+      if (!mbar_wait_bounded(&bars[cs], phase)) {
+        record_status(p.status, QMV_E_TIMEOUT);
+        failed = true;
+      } else {
+        ++consumed;
+        if (valid) {
+          const uint32_t qs = smem_u32(qring + cs * C::Q_STAGE);
+          const uint8_t* ds = dring + cs * C::D_STAGE;
+          // this lane's activations: block g, elements 4t..4t+3 and 16+4t..16+4t+3
+          const uint8_t* xl = xring + cs * kXStage + g * 64 + t * 8;
+          const uint2 xa = *reinterpret_cast<const uint2*>(xl);
+          const uint2 xb = *reinterpret_cast<const uint2*>(xl + 32);
+          bool exact = true;
+          const uint32_t h0 = bf16x2_to_f16x2(xa.x, exact);
+          const uint32_t h1 = bf16x2_to_f16x2(xa.y, exact);
+          const uint32_t h2 = bf16x2_to_f16x2(xb.x, exact);
+          const uint32_t h3 = bf16x2_to_f16x2(xb.y, exact);
+          if (__all_sync(0xffffffffu, exact)) {
+            sts_u32x4(slot, h0, h1, h2, h3);
+            stage_math<WT, F16, NW, true>(acc, qs, ds, bsrc, lrow, lsub, sw, g, t);
+          } else {
+            sts_u32x4(slot, xa.x, xa.y, xb.x, xb.y);
+            stage_math<WT, F16, NW, false>(acc, qs, ds, bsrc, lrow, lsub, sw, g, t);
+          }
+        }
+      }
+      __syncwarp();
+    }
+
+    if (cc.j == cc.n - 1) {  // end of an item: add the lanes' blocks and the column slices, store y
+      const int row0 = cc.tile * C::WROWS;
+      // row sums over the four lanes t that share rows g, g + 8 (the same value in all four)
+      float v[MT][2];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float s = acc[mt][h];
+          s += __shfl_xor_sync(0xffffffffu, s, 1);
+          s += __shfl_xor_sync(0xffffffffu, s, 2);
+          v[mt][h] = s;
+        }
+      // lane t keeps row g + 8 (t & 1) of MMA tile t >> 1 (t < 2 * MT)
+      float mine = (t & 1) ? v[0][1] : v[0][0];
+      if (MT == 2 && t >= 2) mine = (t & 1) ? v[MT - 1][1] : v[MT - 1][0];
+      const int r = 16 * (t >> 1) + 8 * (t & 1) + g;
+      const bool holder = t < 2 * MT;
+      if (p.ks == 1) {
+        if (valid && !failed && holder && row0 + r < P.rows) P.y[row0 + r] = mine;
+      } else {
+        if (holder) red[warp * C::WROWS + r] = mine;
+        __syncthreads();
+        if (kslice == 0 && valid && !failed && lane < C::WROWS && row0 + lane < P.rows) {
+          float sum = 0.f;
+          for (int k = 0; k < p.ks; ++k) sum += red[(warp + k) * C::WROWS + lane];
+          P.y[row0 + lane] = sum;
+        }
+        __syncthreads();
+      }
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = 0.f;
+    }
+    cs = (cs + 1 == C::S) ? 0 : cs + 1;
+    if (cs == 0) phase ^= 1u;
+    advance(cc);
+  }
+  if (failed) {
+    // let this warp's copies still in flight land before the CTA's shared memory is released
+    for (int j = consumed; j < issued; ++j)
+      mbar_wait_bounded(&bars[j % C::S], (uint32_t)(j / C::S) & 1u, 400000000LL);
+  }
+}
+
+// One warps-per-CTA choice's plan for a launch (the same estimate as the general kernel's:
+// stages on the critical path, plus half a stage per item for a split's CTA-wide reduction).
+struct Plan {
+  int ks = 1, nitems = 0, grid = 0, smem = 0;
+  long cost = -1;
+};
+
+template <int WT, bool F16, int NW>
+cudaError_t plan_typed(const MatrixRef* ms, int n, const DeviceInfo& dev, Plan* out) {
+  using C = Cfg<WT, F16, NW>;
+  auto kern = matvec_bdiag_kernel<WT, F16, NW>;
+  // per device: the shared-memory attribute set and the occupancy known (0 = does not fit)
+  static std::mutex mu;
+  static bool ready[64] = {};
+  static int ctas_per_sm[64] = {};
+  if (dev.device < 0 || dev.device >= 64 || n < 1 || n > kMaxProblems) return cudaErrorInvalidValue;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ready[dev.device]) {
+      int k = 0;
+      if ((size_t)C::SMEM <= dev.smem_optin) {
+        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (err != cudaSuccess) return err;
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&k, kern, NW * 32, C::SMEM);
+        if (err != cudaSuccess) return err;
+      }
+      ctas_per_sm[dev.device] = k;
+      ready[dev.device] = true;
+    }
+  }
+  *out = Plan{};
+  if (ctas_per_sm[dev.device] == 0) return cudaSuccess;  // does not fit: cost stays -1
+  const long slots = (long)ctas_per_sm[dev.device] * dev.sm_count;
+  long min_chunks = 1L << 30;
+  for (int i = 0; i < n; ++i)
+    if (ms[i].cols / kTK < min_chunks) min_chunks = ms[i].cols / kTK;
+  Plan best;
+  for (int ks = 1; ks <= NW && ks <= min_chunks; ks *= 2) {
+    const int tpi = NW / ks;
+    long items = 0, units = 0, longest = 0;
+    for (int i = 0; i < n; ++i) {
+      const long it = ((ms[i].rows + C::WROWS - 1) / C::WROWS + tpi - 1) / tpi;
+      const long st = (ms[i].cols / kTK + ks - 1) / ks;
+      items += it;
+      units += it * st;
+      if (st > longest) longest = st;
+    }
+    const long grid = items < slots ? items : slots;
+    const long per_cta = (items + grid - 1) / grid;
+    const long cost = 2 * ((units + grid - 1) / grid + longest) + (ks > 1 ? per_cta : 0);
+    if (best.cost < 0 || cost < best.cost) {
+      best.cost = cost;
+      best.ks = ks;
+      best.nitems = (int)items;
+      best.grid = (int)grid;
+    }
+  }
+  best.smem = C::SMEM;
+  *out = best;
+  return cudaSuccess;
+}
+
+template <int WT, bool F16, int NW>
+cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* const* xs, float* const* ys, int n,
+                         bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
+  using C = Cfg<WT, F16, NW>;
+  Params p{};
+  p.nprob = n;
+  p.status = dev.status;
+  p.ks = plan.ks;
+  const int tpi = NW / plan.ks;
+  int items = 0;
+  for (int i = 0; i < n; ++i) {
+    p.pr[i].y = ys[i];
+    p.pr[i].rows = (int)ms[i].rows;
+    p.pr[i].ntiles = (int)((ms[i].rows + C::WROWS - 1) / C::WROWS);
+    p.pr[i].nchunks = (int)(ms[i].cols / kTK);
+    p.pr[i].item0 = items;
+    items += (p.pr[i].ntiles + tpi - 1) / tpi;
+  }
+  if (items != plan.nitems) return cudaErrorInvalidValue;
+  p.nitems = items;
+
+  Maps maps;
+  memset(&maps, 0, sizeof(maps));
+  for (int i = 0; i < n; ++i) {
+    const MatrixRef& m = ms[i];
+    const uint64_t qrow = (WT == QMV_Q4_0) ? (uint64_t)m.cols / 2 : (uint64_t)m.cols;
+    const uint64_t drow = (uint64_t)(m.cols / 32) * (F16 ? 2 : 4);
+    cudaError_t err = encode_tmap_2d(&maps.q[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, m.q, qrow, (uint64_t)m.rows, qrow,
+                                     kBox, C::WROWS, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (err != cudaSuccess) return err;
+    err = encode_tmap_2d(&maps.d[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, m.d, drow, (uint64_t)m.rows, drow, C::DROW,
+                         C::WROWS, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (err != cudaSuccess) return err;
+    err = encode_tmap_2d(&maps.x[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xs[i], (uint64_t)m.cols, 1,
+                         (uint64_t)m.cols * 2, kTK, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (err != cudaSuccess) return err;
+  }
+
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(plan.grid);
+  cfg.blockDim = dim3(NW * 32);
+  cfg.dynamicSmemBytes = plan.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, matvec_bdiag_kernel<WT, F16, NW>, maps, p);
+}
+
+// 4 warps per CTA; when that leaves SMs without a CTA (a launch with few tiles), 8 or 16
+// warps per CTA instead if the plan estimates them shorter (ties to fewer warps).
+template <int WT, bool F16>
+cudaError_t launch_best(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
+                        const DeviceInfo& dev, cudaStream_t stream) {
+  Plan p4, p8, p16;
+  cudaError_t err = plan_typed<WT, F16, 4>(ms, n, dev, &p4);
+  if (err != cudaSuccess) return err;
+  if (p4.cost >= 0 && p4.grid > dev.sm_count) return launch_typed<WT, F16, 4>(p4, ms, xs, ys, n, pdl, dev, stream);
+  err = plan_typed<WT, F16, 8>(ms, n, dev, &p8);
+  if (err != cudaSuccess) return err;
+  err = plan_typed<WT, F16, 16>(ms, n, dev, &p16);
+  if (err != cudaSuccess) return err;
+  auto better = [](const Plan& a, const Plan& b) { return a.cost >= 0 && (b.cost < 0 || a.cost < b.cost); };
+  if (better(p16, p8) && better(p16, p4)) return launch_typed<WT, F16, 16>(p16, ms, xs, ys, n, pdl, dev, stream);
+  if (better(p8, p4)) return launch_typed<WT, F16, 8>(p8, ms, xs, ys, n, pdl, dev, stream);
+  if (p4.cost < 0) return cudaErrorInvalidConfiguration;
+  return launch_typed<WT, F16, 4>(p4, ms, xs, ys, n, pdl, dev, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_matvec_bdiag(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
+                                const DeviceInfo& dev, cudaStream_t stream) {
+  const MatrixRef& m = ms[0];
+  if (m.wtype == QMV_Q4_0)
+    return m.scale_f16 ? launch_best<QMV_Q4_0, true>(ms, xs, ys, n, pdl, dev, stream)
+                       : launch_best<QMV_Q4_0, false>(ms, xs, ys, n, pdl, dev, stream);
+  return m.scale_f16 ? launch_best<QMV_Q8_0, true>(ms, xs, ys, n, pdl, dev, stream)
+                     : launch_best<QMV_Q8_0, false>(ms, xs, ys, n, pdl, dev, stream);
+}
+
+}  // namespace qmv

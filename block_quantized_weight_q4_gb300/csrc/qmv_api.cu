@@ -19,7 +19,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int kPrefillMinBatch = 16;  // from here on the tensor-memory kernel takes bf16 batches
 constexpr int kTcMinBatch = 4;        // decode passes of this many bf16 vectors go to decode_tc
-constexpr long long kTcMinQ8Weights = 64LL << 20;  // and Q8_0 launches of this many weights
+constexpr long long kTcMinQ8Weights = 64LL << 20;  // and Q8_0 passes of 2-3 vectors over this many weights
 std::mutex g_dev_mutex;
 DeviceInfo g_dev[kMaxDevices];
 bool g_dev_ready[kMaxDevices] = {};
@@ -202,16 +202,19 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
     }
     if (nf == 0) continue;
     // bf16 activations: the tensor-memory kernel for passes of 4 or more vectors, and for
-    // Q8_0 launches of 64M weights or more (where it measured faster), when this stream has
-    // its workspace (created on the stream's first such call, never while it is captured);
-    // else the mma.sync kernel
+    // Q8_0 passes of 2 or 3 vectors over 64M weights or more (where it measured faster),
+    // when this stream has its workspace (created on the stream's first such call, never
+    // while it is captured); one bf16 vector: the block-diagonal kernel; else the mma.sync
+    // kernel
     long long nweights = 0;
     for (int i = 0; i < nf; ++i) nweights += fast[i].rows * fast[i].cols;
-    bool tc = xb && (nb >= kTcMinBatch || (wtype == QMV_Q8_0 && nweights >= kTcMinQ8Weights));
+    bool tc = xb && (nb >= kTcMinBatch || (wtype == QMV_Q8_0 && nb > 1 && nweights >= kTcMinQ8Weights));
     for (int i = 0; i < nf && tc; ++i) tc = decode_tc_supported(fast[i]);
     Workspace ws;
     if (tc && stream_workspace(dev, stream, &ws) == cudaSuccess) {
       if (launch_decode_tc(fast, fx, fy, nf, nb, pdl, dev, ws, stream) != cudaSuccess) return QMV_E_CUDA;
+    } else if (xb && nb == 1) {
+      if (launch_matvec_bdiag(fast, fx, fy, nf, pdl, dev, stream) != cudaSuccess) return QMV_E_CUDA;
     } else if (launch_matvec_mma(fast, fx, fy, nf, xb, nb, pdl, dev, stream) != cudaSuccess) {
       return QMV_E_CUDA;
     }

@@ -218,4 +218,80 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// ---------------------------------------------------------------------------- half precision
+// IEEE half pair arithmetic on packed registers (all uses below are exact).
+__device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t f16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+
+// A bfloat16 pair (low half first) as an IEEE half pair; `exact` is cleared unless both
+// values convert exactly (checked by converting back: zero, and bfloat16 values with
+// 2^-17 <= |x| <= 65280, pass; larger and tinier values and NaN do not).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t p, bool& exact) {
+  const float lo = __uint_as_float(p << 16);
+  const float hi = __uint_as_float(p & 0xFFFF0000u);
+  uint32_t h;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(hi), "f"(lo));
+  const float blo = __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xFFFFu)));
+  const float bhi = __half2float(__ushort_as_half(static_cast<unsigned short>(h >> 16)));
+  exact = exact & (blo == lo) & (bhi == hi);
+  return h;
+}
+
+// Four Q4_0 quant bytes (as for q4_word_to_bf16_levels) to exact IEEE half levels in natural
+// pairs.  prmt puts byte b under the half exponent of 1024 (0x6400 | b is 1024 + b: the
+// 10-bit mantissa takes the whole byte); H = 1024 + 16 hi + 8 (the low nibble replaced by 8);
+// then (1024 + b) - H = lo - 8 and H / 16 - 72.5 = hi - 8, both exact.
+__device__ __forceinline__ void q4_word_to_f16_levels(uint32_t w, uint32_t& lo01, uint32_t& lo23, uint32_t& hi01,
+                                                      uint32_t& hi23) {
+  constexpr uint32_t kExp = 0x64646464u;       // 0x64: the high byte of half 1024
+  constexpr uint32_t kSixteenth = 0x2C002C00u;  // half 1/16
+  constexpr uint32_t kOff = 0xD488D488u;        // half -72.5
+  const uint32_t p01 = prmt(w, kExp, 0x4140);   // 1024 + b0, 1024 + b1
+  const uint32_t p23 = prmt(w, kExp, 0x4342);   // 1024 + b2, 1024 + b3
+  const uint32_t h01 = lop_and_or(p01, 0xFFF0FFF0u, 0x00080008u);
+  const uint32_t h23 = lop_and_or(p23, 0xFFF0FFF0u, 0x00080008u);
+  lo01 = f16x2_sub(p01, h01);
+  lo23 = f16x2_sub(p23, h23);
+  hi01 = f16x2_fma(h01, kSixteenth, kOff);
+  hi23 = f16x2_fma(h23, kSixteenth, kOff);
+}
+
+// Four Q8_0 quant bytes q0..q3 to exact IEEE half levels q01 = (q0, q1), q23 = (q2, q3):
+// with u = q + 128, 0x6400 | u is 1024 + u, and (1024 + u) - 1152 = q.
+__device__ __forceinline__ void q8_word_to_f16_levels(uint32_t w, uint32_t& q01, uint32_t& q23) {
+  constexpr uint32_t kExp = 0x64646464u;
+  constexpr uint32_t kBias = 0x64806480u;  // half 1152
+  const uint32_t u = w ^ 0x80808080u;
+  q01 = f16x2_sub(prmt(u, kExp, 0x4140), kBias);
+  q23 = f16x2_sub(prmt(u, kExp, 0x4342), kBias);
+}
+
+// D = A(16x16 f16, row) * B(16x8 f16, col) + C, f32 accumulate.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1, const float (&c)[4]) {
+  asm(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%10, %11, %12, %13};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
+}
+
+__device__ __forceinline__ void lds_u32x4(uint32_t addr, uint32_t (&v)[4]) {
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]) : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void sts_u32x4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
 }  // namespace qmv

@@ -70,6 +70,12 @@ int matvec_mma_max_problems();
 cudaError_t launch_matvec_mma(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool x_bf16,
                               int batch, bool pdl, const DeviceInfo& dev, cudaStream_t stream);
 
+// The same problems with one bfloat16 activation vector (batch 1), block-diagonal
+// activation fragments and half-precision operands where exact (decode_bdiag.cu); takes
+// every problem matvec_mma_supported() accepts.
+cudaError_t launch_matvec_bdiag(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
+                                const DeviceInfo& dev, cudaStream_t stream);
+
 // Batched product on the 5th-generation tensor core (weights dequantized to bf16 in shared
 // memory, tcgen05 MMA into tensor memory): bf16 activations, cols % 256 == 0, 1..128
 // vectors per launch (meant for 16 and more).

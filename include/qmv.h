@@ -99,10 +99,13 @@ int qmv_matrix_wtype(int file_wtype, uint32_t q8_mask, int class_bit, int shared
  *   batch : number of activation vectors, >= 0; 0 launches nothing and returns QMV_OK.
  * Each block contributes d * sum_j level_j * x_j; sums are kept in float32.  Batches
  * below 16 (and float32 activations) run in passes of up to 8 vectors through the decode
- * kernels (weights decoded to exact bfloat16 levels, one tensor-core dot product per block,
- * f32 scale and accumulate): passes of 4 or more bf16 vectors, and Q8_0 launches of 64M
- * weights or more, take the tensor-memory kernel (levels stored to tensor memory, tcgen05
- * MMA), the rest the mma.sync kernel.  The tensor-memory kernel splits tiles between CTAs;
+ * kernels (weights decoded to exact levels, one tensor-core dot product per block, f32
+ * scale and accumulate): passes of 4 or more bf16 vectors, and Q8_0 passes of 2 or 3 bf16
+ * vectors over 64M weights or more, take the tensor-memory kernel (levels stored to tensor
+ * memory, tcgen05 MMA); a pass of one bf16 vector takes the block-diagonal kernel (one MMA
+ * column per weight block; IEEE-half operands for the 256-column stages whose activations
+ * are exact halves, bfloat16 otherwise); the rest the mma.sync kernel.  The
+ * tensor-memory kernel splits tiles between CTAs;
  * their parts meet in a workspace of the calling stream (4 MiB of device memory, allocated
  * on the stream's first such call and kept; while a stream without one is being captured,
  * the call takes the mma.sync kernel instead).  Results do not depend on timing.
