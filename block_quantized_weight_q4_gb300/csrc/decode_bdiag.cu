@@ -7,7 +7,11 @@
 // The stream of stages, the work split (warp tiles of 16*MT rows, 256-column chunks, items
 // of NW/ks tiles x ks column slices walked persistently), the per-warp TMA rings and the
 // overlap with the preceding kernel are those of the general decode kernel
-// (decode_mma.cu).  What changes with a single vector:
+// (decode_mma.cu), with two changes to the split: the ks warps of a tile take interleaved
+// chunks (warp k: chunks k, k + ks, k + 2 ks, ...), so that they read neighbouring 128-byte
+// pieces of the same rows at a time (DRAM pages are reused: one warp walking a row alone
+// measured 20% slower); and ks is chosen by an estimate that counts waves of items (see
+// plan_typed).  What changes with a single vector:
 //   * Block-diagonal activations.  The 8 columns of an m16n8k16 MMA are spent on the 8
 //     weight blocks of a stage instead of on 8 vectors: the MMA of block j multiplies 16
 //     rows' levels of block j by an activation fragment whose column j holds x of block j
@@ -78,6 +82,7 @@ struct Problem {
 struct Params {
   int nprob;
   int ks;       // column slices per tile (1, 2, 4, 8, 16); at most every problem's nchunks
+  int lgks;     // log2(ks)
   int nitems;
   int* status;
   Problem pr[kMaxProblems];
@@ -89,7 +94,8 @@ struct Maps {  // per problem: q (128-byte swizzle), d, and activation tensor ma
   CUtensorMap x[kMaxProblems];
 };
 
-// Position of a warp in its stream of stages (as in the general decode kernel).
+// Position of a warp in its stream of stages: item (global index), its problem and warp
+// tile, this warp's first chunk and chunk count in the item (chunk c0 + j * ks is the j-th).
 struct Cursor {
   int item, prob, tile, c0, n, j;
 };
@@ -101,10 +107,9 @@ __device__ __forceinline__ void cursor_load(Cursor& c, const Params& p, int tile
   while (pr + 1 < p.nprob && c.item >= p.pr[pr + 1].item0) ++pr;
   c.prob = pr;
   c.tile = (c.item - p.pr[pr].item0) * tiles_per_item + tile_local;
-  const int nch = p.pr[pr].nchunks;
-  const int lg = 31 - __clz(p.ks);  // ks is a power of two
-  c.c0 = (kslice * nch) >> lg;
-  c.n = (((kslice + 1) * nch) >> lg) - c.c0;
+  // chunks kslice, kslice + ks, ... (ks <= nchunks: at least one)
+  c.c0 = kslice;
+  c.n = (p.pr[pr].nchunks - kslice + p.ks - 1) >> p.lgks;
   c.j = 0;
 }
 
@@ -244,7 +249,7 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
     if (lane == 0) {
       const Problem& P = p.pr[pc.prob];
       if (pc.tile < P.ntiles) {
-        const int c = pc.c0 + pc.j;
+        const int c = pc.c0 + (pc.j << p.lgks);
         mbar_arrive_expect_tx(&bars[ps], stage_tx);
         fence_proxy_async_smem();
 #pragma unroll
@@ -272,7 +277,7 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
   bool pre_valid[C::S];
   int pre = 0;
   while (pre < C::S - 1 && pc.item < p.nitems) {
-    pre_c[pre] = pc.c0 + pc.j;
+    pre_c[pre] = pc.c0 + (pc.j << p.lgks);
     pre_prob[pre] = pc.prob;
     pre_valid[pre] = pc.tile < p.pr[pc.prob].ntiles;
     issue(false);
@@ -391,11 +396,14 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
   }
 }
 
-// One warps-per-CTA choice's plan for a launch (the same estimate as the general kernel's:
-// stages on the critical path, plus half a stage per item for a split's CTA-wide reduction).
+// One warps-per-CTA choice's plan for a launch: the column split ks with the smallest
+// estimate of the launch's duration, in 1/40 stage.  A launch with more items than resident
+// CTAs runs in waves of `grid` items (the last one partly filled), each as long as one item:
+// ceil(nchunks / ks) stages plus, for ks > 1, a CTA-wide reduction (about a quarter stage);
+// with ks = 1 a warp walks a row alone, which measured about 10% slower per stage.
 struct Plan {
   int ks = 1, nitems = 0, grid = 0, smem = 0;
-  long cost = -1;
+  long long cost = -1;
 };
 
 template <int WT, bool F16, int NW>
@@ -423,25 +431,23 @@ cudaError_t plan_typed(const MatrixRef* ms, int n, const DeviceInfo& dev, Plan* 
   }
   *out = Plan{};
   if (ctas_per_sm[dev.device] == 0) return cudaSuccess;  // does not fit: cost stays -1
-  const long slots = (long)ctas_per_sm[dev.device] * dev.sm_count;
-  long min_chunks = 1L << 30;
+  const long long slots = (long long)ctas_per_sm[dev.device] * dev.sm_count;
+  long long min_chunks = 1LL << 30;
   for (int i = 0; i < n; ++i)
     if (ms[i].cols / kTK < min_chunks) min_chunks = ms[i].cols / kTK;
   Plan best;
   for (int ks = 1; ks <= NW && ks <= min_chunks; ks *= 2) {
     const int tpi = NW / ks;
-    long items = 0, units = 0, longest = 0;
+    long long items = 0, longest = 0;
     for (int i = 0; i < n; ++i) {
-      const long it = ((ms[i].rows + C::WROWS - 1) / C::WROWS + tpi - 1) / tpi;
-      const long st = (ms[i].cols / kTK + ks - 1) / ks;
-      items += it;
-      units += it * st;
+      items += ((ms[i].rows + C::WROWS - 1) / C::WROWS + tpi - 1) / tpi;
+      const long long st = (ms[i].cols / kTK + ks - 1) / ks;
       if (st > longest) longest = st;
     }
-    const long grid = items < slots ? items : slots;
-    const long per_cta = (items + grid - 1) / grid;
-    const long cost = 2 * ((units + grid - 1) / grid + longest) + (ks > 1 ? per_cta : 0);
-    if (best.cost < 0 || cost < best.cost) {
+    const long long grid = items < slots ? items : slots;
+    const long long waves = (items + grid - 1) / grid;
+    const long long cost = waves * (longest * (ks == 1 ? 44 : 40) + (ks > 1 ? 10 : 0));
+    if (best.cost < 0 || cost < best.cost || (cost == best.cost && grid < best.grid)) {
       best.cost = cost;
       best.ks = ks;
       best.nitems = (int)items;
@@ -461,6 +467,7 @@ cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* cons
   p.nprob = n;
   p.status = dev.status;
   p.ks = plan.ks;
+  p.lgks = 31 - __builtin_clz((unsigned)plan.ks);
   const int tpi = NW / plan.ks;
   int items = 0;
   for (int i = 0; i < n; ++i) {
@@ -505,7 +512,9 @@ cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* cons
 }
 
 // 4 warps per CTA; when that leaves SMs without a CTA (a launch with few tiles), 8 or 16
-// warps per CTA instead if the plan estimates them shorter (ties to fewer warps).
+// warps per CTA instead if their estimate is smaller (ties to fewer warps).  With every SM
+// busy, more warps per CTA measured slower (they share the SM's issue slots, and 16-warp CTAs
+// hold 2 stages per warp instead of 3).
 template <int WT, bool F16>
 cudaError_t launch_best(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
                         const DeviceInfo& dev, cudaStream_t stream) {
