@@ -56,7 +56,9 @@ struct Cfg {
   static constexpr int QROW = NQBOX * kBox;                        // q bytes per row per stage
   static constexpr int DROW = kBlocksPerStage * (F16 ? 2 : 4);    // scale bytes per row per stage
   static constexpr int D_STAGE = WROWS * DROW;                     // multiple of 256
-  static constexpr int S = NW >= 16 ? 2 : 3;                       // ring depth
+  // ring depth: Q4_0 2 (five 4-warp CTAs per SM, measured faster than three with 3 stages),
+  // Q8_0 3 (its stages cost fewer instructions; deeper rings measured faster)
+  static constexpr int S = (WT == QMV_Q4_0 || NW >= 16) ? 2 : 3;
   static constexpr int Q_WARP = S * Q_STAGE;
   static constexpr int D_WARP = S * D_STAGE;
   static constexpr int X_WARP = S * kXStage;
@@ -121,11 +123,11 @@ __device__ __forceinline__ void stage_math(float (&acc)[Cfg<WT, F16, NW>::MT][2]
                                            int g, int t) {
   using C = Cfg<WT, F16, NW>;
   constexpr int MT = C::MT;
-  float da[MT][4], db[MT][4];  // block sums of elements 0..15 and 16..31, column j = block j
+  float da[MT][4];  // block sums (both halves of a block), column j = block j
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) da[mt][i] = db[mt][i] = 0.f;
+    for (int i = 0; i < 4; ++i) da[mt][i] = 0.f;
 #pragma unroll
   for (int bp = 0; bp < kBlocksPerStage / 2; ++bp) {
     uint32_t w[MT][4];  // Q4_0: [tile][row g blk 2bp, row g+8 blk 2bp, row g blk 2bp+1, row g+8 blk 2bp+1]
@@ -148,12 +150,12 @@ __device__ __forceinline__ void stage_math(float (&acc)[Cfg<WT, F16, NW>::MT][2]
             q4_word_to_f16_levels(w[mt][2 * hb], g01, g23, gh01, gh23);      // row g
             q4_word_to_f16_levels(w[mt][2 * hb + 1], h01, h23, hh01, hh23);  // row g + 8
             mma_f16_16816(da[mt], g01, h01, g23, h23, b[0], b[1], da[mt]);
-            mma_f16_16816(db[mt], gh01, hh01, gh23, hh23, b[2], b[3], db[mt]);
+            mma_f16_16816(da[mt], gh01, hh01, gh23, hh23, b[2], b[3], da[mt]);
           } else {
             q4_word_to_bf16_levels(w[mt][2 * hb], g01, g23, gh01, gh23);
             q4_word_to_bf16_levels(w[mt][2 * hb + 1], h01, h23, hh01, hh23);
             mma_bf16_16816(da[mt], g01, h01, g23, h23, b[0], b[1], da[mt]);
-            mma_bf16_16816(db[mt], gh01, hh01, gh23, hh23, b[2], b[3], db[mt]);
+            mma_bf16_16816(da[mt], gh01, hh01, gh23, hh23, b[2], b[3], da[mt]);
           }
         }
       } else {
@@ -168,14 +170,14 @@ __device__ __forceinline__ void stage_math(float (&acc)[Cfg<WT, F16, NW>::MT][2]
           q8_word_to_f16_levels(q[2], g1a, g1b);
           q8_word_to_f16_levels(q[3], h1a, h1b);
           mma_f16_16816(da[0], g0a, h0a, g0b, h0b, b[0], b[1], da[0]);
-          mma_f16_16816(db[0], g1a, h1a, g1b, h1b, b[2], b[3], db[0]);
+          mma_f16_16816(da[0], g1a, h1a, g1b, h1b, b[2], b[3], da[0]);
         } else {
           q8_word_to_bf16_levels(q[0], g0a, g0b);
           q8_word_to_bf16_levels(q[1], h0a, h0b);
           q8_word_to_bf16_levels(q[2], g1a, g1b);
           q8_word_to_bf16_levels(q[3], h1a, h1b);
           mma_bf16_16816(da[0], g0a, h0a, g0b, h0b, b[0], b[1], da[0]);
-          mma_bf16_16816(db[0], g1a, h1a, g1b, h1b, b[2], b[3], db[0]);
+          mma_bf16_16816(da[0], g1a, h1a, g1b, h1b, b[2], b[3], da[0]);
         }
       }
     }
@@ -196,8 +198,8 @@ __device__ __forceinline__ void stage_math(float (&acc)[Cfg<WT, F16, NW>::MT][2]
         d0 = v.x;
         d1 = v.y;
       }
-      const float s0 = da[mt][2 * h] + db[mt][2 * h];
-      const float s1 = da[mt][2 * h + 1] + db[mt][2 * h + 1];
+      const float s0 = da[mt][2 * h];
+      const float s1 = da[mt][2 * h + 1];
       acc[mt][h] = fmaf(d1, s1, fmaf(d0, s0, acc[mt][h]));
     }
   }
