@@ -4,21 +4,23 @@
 //   y[r] = sum_k d[r][k] * sum_{j<32} level[r][32k+j] * x[32k+j]
 // with level = nibble - 8 (Q4_0) or the int8 quant (Q8_0), d the block's scale.
 //
-// The stream of stages, the work split (warp tiles of 16*MT rows, 256-column chunks, items
-// of NW/ks tiles x ks column slices walked persistently), the per-warp TMA rings and the
-// overlap with the preceding kernel are those of the general decode kernel
-// (decode_mma.cu), with two changes to the split: the ks warps of a tile take interleaved
-// chunks (warp k: chunks k, k + ks, k + 2 ks, ...), so that they read neighbouring 128-byte
+// The stream of stages, the work split (warp tiles of 16*MT rows, items of NW/ks tiles x ks
+// column slices walked persistently), the per-warp TMA rings and the overlap with the
+// preceding kernel are those of the general decode kernel (decode_mma.cu), with three
+// changes: a stage is two 256-column chunks (one TMA issue of each kind, one wait and one
+// activation check per 512 columns: the per-stage bookkeeping and the many 16-byte rows of
+// the scale box measured as costly as a third of the stage's work); the ks warps of a tile
+// take interleaved stages (warp k: stages k, k + ks, ...), so that they read neighbouring
 // pieces of the same rows at a time (DRAM pages are reused: one warp walking a row alone
 // measured 20% slower); and ks is chosen by an estimate that counts waves of items (see
 // plan_typed).  What changes with a single vector:
 //   * Block-diagonal activations.  The 8 columns of an m16n8k16 MMA are spent on the 8
-//     weight blocks of a stage instead of on 8 vectors: the MMA of block j multiplies 16
+//     weight blocks of a chunk instead of on 8 vectors: the MMA of block j multiplies 16
 //     rows' levels of block j by an activation fragment whose column j holds x of block j
-//     and whose other columns are zero.  After the stage's 16 MMAs (8 blocks x 2 halves)
+//     and whose other columns are zero.  After the chunk's 16 MMAs (8 blocks x 2 halves)
 //     column j of the accumulator is each row's block-j dot product, and the thread holding
 //     it (g, t with j = 2t or 2t+1) applies that row's block-j scale: 4 FFMA per 16 rows and
-//     stage instead of 32.  Lanes g = j hold x of block j in the fragment of block j; each
+//     chunk instead of 32.  Lanes g = j hold x of block j in the fragment of block j; each
 //     lane writes its 16 activation bytes to a slot of its own and reads, for block j, that
 //     slot (j = g) or a shared zero line (j != g).  At the end of an item the four lanes t
 //     that share rows g, g+8 add their blocks' sums (two xor shuffles).
@@ -39,36 +41,38 @@ namespace qmv {
 
 namespace {
 
-constexpr int kTK = 256;             // weights per stage and row
-constexpr int kBlocksPerStage = kTK / 32;
+constexpr int kTK = 256;             // weights per chunk and row
+constexpr int kBlocksPerStage = kTK / 32;  // blocks per chunk (the MMA's 8 columns)
 constexpr int kRows = 16;            // rows per MMA tile
 constexpr int kBox = 128;            // q box inner extent in bytes (the 128-byte swizzle span)
 constexpr int kMaxProblems = 8;      // problems per grouped launch
-constexpr int kXStage = kTK * 2;     // bfloat16 activations of one stage, bytes
 
-template <int WT, bool F16, int NW>
+template <int WT, bool F16, int NW, int CH>
 struct Cfg {
+  static constexpr int kCH = CH;                                   // chunks per stage
+  static constexpr int X_STAGE = CH * kTK * 2;                    // bfloat16 activations of one stage
   static constexpr int MT = (WT == QMV_Q4_0) ? 2 : 1;           // 16-row MMA tiles per warp tile
   static constexpr int WROWS = MT * kRows;                        // rows per warp tile
-  static constexpr int NQBOX = (WT == QMV_Q4_0) ? 1 : 2;        // q boxes per stage
+  static constexpr int CBOX = (WT == QMV_Q4_0) ? 1 : 2;         // q boxes per chunk
+  static constexpr int NQBOX = CBOX * CH;                        // q boxes per stage
   static constexpr int Q_BOX_BYTES = WROWS * kBox;
-  static constexpr int Q_STAGE = NQBOX * Q_BOX_BYTES;             // 4096 bytes, multiple of 1024
-  static constexpr int QROW = NQBOX * kBox;                        // q bytes per row per stage
-  static constexpr int DROW = kBlocksPerStage * (F16 ? 2 : 4);    // scale bytes per row per stage
-  static constexpr int D_STAGE = WROWS * DROW;                     // multiple of 256
-  // ring depth: Q4_0 2 (five 4-warp CTAs per SM, measured faster than three with 3 stages),
-  // Q8_0 3 (its stages cost fewer instructions; deeper rings measured faster)
-  static constexpr int S = (WT == QMV_Q4_0 || NW >= 16) ? 2 : 3;
+  static constexpr int Q_CHUNK = CBOX * Q_BOX_BYTES;              // 4096 bytes, multiple of 1024
+  static constexpr int Q_STAGE = CH * Q_CHUNK;
+  static constexpr int QROW = CBOX * kBox;                         // q bytes per row per chunk
+  static constexpr int DCHUNK = kBlocksPerStage * (F16 ? 2 : 4);  // scale bytes per row per chunk
+  static constexpr int DROW = CH * DCHUNK;                        // scale bytes per row per stage
+  static constexpr int D_STAGE = WROWS * DROW;                     // multiple of 512
+  static constexpr int S = 2;  // ring depth
   static constexpr int Q_WARP = S * Q_STAGE;
   static constexpr int D_WARP = S * D_STAGE;
-  static constexpr int X_WARP = S * kXStage;
-  // q rings, d rings, activation rings, activation slots (32 lanes x 16 bytes per warp),
-  // zero line, reduction buffer (split-K), barriers
+  static constexpr int X_WARP = S * X_STAGE;
+  // q rings, d rings, activation rings, activation slots (per chunk: 32 lanes x 16 bytes),
+  // zero area (a zero line CH-1 slot areas long), reduction buffer (split-K), barriers
   static constexpr int OFF_D = NW * Q_WARP;
   static constexpr int OFF_X = OFF_D + NW * D_WARP;
   static constexpr int OFF_SLOT = OFF_X + NW * X_WARP;
-  static constexpr int OFF_ZERO = OFF_SLOT + NW * 512;
-  static constexpr int OFF_RED = OFF_ZERO + 128;
+  static constexpr int OFF_ZERO = OFF_SLOT + NW * CH * 512;
+  static constexpr int OFF_RED = OFF_ZERO + CH * 512;
   static constexpr int OFF_BAR = OFF_RED + ((NW * WROWS * 4 + 127) / 128) * 128;
   static constexpr int SMEM = 1024 + OFF_BAR + ((NW * S * 8 + 127) / 128) * 128;
 };
@@ -77,27 +81,28 @@ struct Problem {
   float* y;
   int rows;
   int ntiles;   // warp tiles (16*MT rows)
-  int nchunks;  // cols / 256
+  int nst;      // stages per tile row: ceil(cols / 256 / CH) (chunks past the end read zeros)
   int item0;    // first item of this problem in the group's item list
 };
 
 struct Params {
   int nprob;
-  int ks;       // column slices per tile (1, 2, 4, 8, 16); at most every problem's nchunks
+  int ks;       // column slices per tile (1, 2, 4, 8); at most every problem's nst
   int lgks;     // log2(ks)
   int nitems;
   int* status;
   Problem pr[kMaxProblems];
 };
 
-struct Maps {  // per problem: q (128-byte swizzle), d, and activation tensor maps
+struct Maps {  // per problem: q (128-byte swizzle), d, and activation (viewed as [cols/256][256]) tensor maps
   CUtensorMap q[kMaxProblems];
   CUtensorMap d[kMaxProblems];
   CUtensorMap x[kMaxProblems];
 };
 
 // Position of a warp in its stream of stages: item (global index), its problem and warp
-// tile, this warp's first chunk and chunk count in the item (chunk c0 + j * ks is the j-th).
+// tile, this warp's first stage and stage count in the item (stage c0 + j * ks is the j-th;
+// stage c covers chunks CH c .. CH c + CH - 1).
 struct Cursor {
   int item, prob, tile, c0, n, j;
 };
@@ -109,19 +114,20 @@ __device__ __forceinline__ void cursor_load(Cursor& c, const Params& p, int tile
   while (pr + 1 < p.nprob && c.item >= p.pr[pr + 1].item0) ++pr;
   c.prob = pr;
   c.tile = (c.item - p.pr[pr].item0) * tiles_per_item + tile_local;
-  // chunks kslice, kslice + ks, ... (ks <= nchunks: at least one)
+  // stages kslice, kslice + ks, ... (ks <= nst: at least one)
   c.c0 = kslice;
-  c.n = (p.pr[pr].nchunks - kslice + p.ks - 1) >> p.lgks;
+  c.n = (p.pr[pr].nst - kslice + p.ks - 1) >> p.lgks;
   c.j = 0;
 }
 
-// One stage of one warp: the 16*MT x 256 weights at qs (q, swizzled) and ds (scales), x
-// block j read through bsrc[j]; adds each row's scaled block sums of blocks 2t, 2t+1 to acc.
-template <int WT, bool F16, int NW, bool HALF>
-__device__ __forceinline__ void stage_math(float (&acc)[Cfg<WT, F16, NW>::MT][2], uint32_t qs, const uint8_t* ds,
-                                           const uint32_t (&bsrc)[kBlocksPerStage], int lrow, int lsub, int sw,
-                                           int g, int t) {
-  using C = Cfg<WT, F16, NW>;
+// One chunk of a stage of one warp: the 16*MT x 256 weights at qs (q, swizzled) and ds
+// (the chunk's first scale in each DROW-byte row), x block j read at bsrc[j] + boff; adds each
+// row's scaled block sums of blocks 2t, 2t+1 to acc.
+template <int WT, bool F16, int NW, int CH, bool HALF>
+__device__ __forceinline__ void chunk_math(float (&acc)[Cfg<WT, F16, NW, CH>::MT][2], uint32_t qs, const uint8_t* ds,
+                                           const uint32_t (&bsrc)[kBlocksPerStage], uint32_t boff, int lrow,
+                                           int lsub, int sw, int g, int t) {
+  using C = Cfg<WT, F16, NW, CH>;
   constexpr int MT = C::MT;
   float da[MT][4];  // block sums (both halves of a block), column j = block j
 #pragma unroll
@@ -141,7 +147,7 @@ __device__ __forceinline__ void stage_math(float (&acc)[Cfg<WT, F16, NW>::MT][2]
     for (int hb = 0; hb < 2; ++hb) {
       const int k = 2 * bp + hb;
       uint32_t b[4];  // elements (4t, 4t+1), (4t+2, 4t+3), (16+4t, ..), (18+4t, ..) of block k, or zeros
-      lds_u32x4(bsrc[k], b);
+      lds_u32x4(bsrc[k] + boff, b);
       if (WT == QMV_Q4_0) {
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
@@ -205,10 +211,10 @@ __device__ __forceinline__ void stage_math(float (&acc)[Cfg<WT, F16, NW>::MT][2]
   }
 }
 
-template <int WT, bool F16, int NW>
+template <int WT, bool F16, int NW, int CH>
 __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_constant__ Maps maps,
                                                                const __grid_constant__ Params p) {
-  using C = Cfg<WT, F16, NW>;
+  using C = Cfg<WT, F16, NW, CH>;
   constexpr int MT = C::MT;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -222,7 +228,7 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
   uint8_t* qring = smem + warp * C::Q_WARP;
   uint8_t* dring = smem + C::OFF_D + warp * C::D_WARP;
   uint8_t* xring = smem + C::OFF_X + warp * C::X_WARP;
-  const uint32_t slot = smem_u32(smem + C::OFF_SLOT + warp * 512 + lane * 16);
+  const uint32_t slot = smem_u32(smem + C::OFF_SLOT + warp * (C::kCH * 512) + lane * 16);
   const uint32_t zline = smem_u32(smem + C::OFF_ZERO);
   float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + warp * C::S;
@@ -230,9 +236,9 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
   const int tiles_per_item = NW / p.ks;
   const int tile_local = warp / p.ks;
   const int kslice = warp % p.ks;
-  constexpr uint32_t stage_tx = (uint32_t)(C::Q_STAGE + C::D_STAGE + kXStage);
+  constexpr uint32_t stage_tx = (uint32_t)(C::Q_STAGE + C::D_STAGE + C::X_STAGE);
 
-  if (threadIdx.x < 32) reinterpret_cast<uint32_t*>(smem + C::OFF_ZERO)[threadIdx.x] = 0u;
+  for (int i = threadIdx.x; i < C::kCH * 128; i += NW * 32) reinterpret_cast<uint32_t*>(smem + C::OFF_ZERO)[i] = 0u;
   if (lane == 0) {
     for (int s = 0; s < C::S; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
@@ -251,16 +257,16 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
     if (lane == 0) {
       const Problem& P = p.pr[pc.prob];
       if (pc.tile < P.ntiles) {
-        const int c = pc.c0 + (pc.j << p.lgks);
+        const int c = pc.c0 + (pc.j << p.lgks);  // stage: chunks CH c ..
         mbar_arrive_expect_tx(&bars[ps], stage_tx);
         fence_proxy_async_smem();
 #pragma unroll
         for (int b = 0; b < C::NQBOX; ++b)
-          tma_load_2d(qring + ps * C::Q_STAGE + b * C::Q_BOX_BYTES, &maps.q[pc.prob], c * C::QROW + b * kBox,
+          tma_load_2d(qring + ps * C::Q_STAGE + b * C::Q_BOX_BYTES, &maps.q[pc.prob], c * (C::kCH * C::QROW) + b * kBox,
                       pc.tile * C::WROWS, &bars[ps], pol_stream);
         tma_load_2d(dring + ps * C::D_STAGE, &maps.d[pc.prob], c * C::DROW, pc.tile * C::WROWS, &bars[ps],
                     pol_stream);
-        if (with_x) tma_load_2d_keep(xring + ps * kXStage, &maps.x[pc.prob], c * kTK, 0, &bars[ps]);
+        if (with_x) tma_load_2d_keep(xring + ps * C::X_STAGE, &maps.x[pc.prob], 0, c * C::kCH, &bars[ps]);
       } else {
         mbar_arrive(&bars[ps]);  // a tile past the end of its problem: complete the phase, no data
       }
@@ -292,7 +298,7 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
   if (threadIdx.x == 0) griddep_launch_dependents();
   if (lane == 0) {
     for (int i = 0; i < pre; ++i)
-      if (pre_valid[i]) tma_load_2d_keep(xring + i * kXStage, &maps.x[pre_prob[i]], pre_c[i] * kTK, 0, &bars[i]);
+      if (pre_valid[i]) tma_load_2d_keep(xring + i * C::X_STAGE, &maps.x[pre_prob[i]], 0, pre_c[i] * C::kCH, &bars[i]);
   }
 
   // ldmatrix: lane supplies row (lane & 7) + 8 * (matrix & 1), 16-byte chunk (matrix >> 1)
@@ -333,21 +339,35 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
         if (valid) {
           const uint32_t qs = smem_u32(qring + cs * C::Q_STAGE);
           const uint8_t* ds = dring + cs * C::D_STAGE;
-          // this lane's activations: block g, elements 4t..4t+3 and 16+4t..16+4t+3
-          const uint8_t* xl = xring + cs * kXStage + g * 64 + t * 8;
-          const uint2 xa = *reinterpret_cast<const uint2*>(xl);
-          const uint2 xb = *reinterpret_cast<const uint2*>(xl + 32);
+          // this lane's activations of each chunk h: block g, elements 4t..4t+3 and
+          // 16+4t..16+4t+3; its slot for chunk h is 512 bytes after the one for chunk h-1
+          uint2 xa[C::kCH], xb[C::kCH];
+          uint32_t hx[C::kCH][4];
           bool exact = true;
-          const uint32_t h0 = bf16x2_to_f16x2(xa.x, exact);
-          const uint32_t h1 = bf16x2_to_f16x2(xa.y, exact);
-          const uint32_t h2 = bf16x2_to_f16x2(xb.x, exact);
-          const uint32_t h3 = bf16x2_to_f16x2(xb.y, exact);
+#pragma unroll
+          for (int h = 0; h < C::kCH; ++h) {
+            const uint8_t* xl = xring + cs * C::X_STAGE + h * (kTK * 2) + g * 64 + t * 8;
+            xa[h] = *reinterpret_cast<const uint2*>(xl);
+            xb[h] = *reinterpret_cast<const uint2*>(xl + 32);
+            hx[h][0] = bf16x2_to_f16x2(xa[h].x, exact);
+            hx[h][1] = bf16x2_to_f16x2(xa[h].y, exact);
+            hx[h][2] = bf16x2_to_f16x2(xb[h].x, exact);
+            hx[h][3] = bf16x2_to_f16x2(xb[h].y, exact);
+          }
           if (__all_sync(0xffffffffu, exact)) {
-            sts_u32x4(slot, h0, h1, h2, h3);
-            stage_math<WT, F16, NW, true>(acc, qs, ds, bsrc, lrow, lsub, sw, g, t);
+#pragma unroll
+            for (int h = 0; h < C::kCH; ++h) sts_u32x4(slot + h * 512, hx[h][0], hx[h][1], hx[h][2], hx[h][3]);
+#pragma unroll
+            for (int h = 0; h < C::kCH; ++h)
+              chunk_math<WT, F16, NW, CH, true>(acc, qs + h * C::Q_CHUNK, ds + h * C::DCHUNK, bsrc, h * 512u, lrow,
+                                            lsub, sw, g, t);
           } else {
-            sts_u32x4(slot, xa.x, xa.y, xb.x, xb.y);
-            stage_math<WT, F16, NW, false>(acc, qs, ds, bsrc, lrow, lsub, sw, g, t);
+#pragma unroll
+            for (int h = 0; h < C::kCH; ++h) sts_u32x4(slot + h * 512, xa[h].x, xa[h].y, xb[h].x, xb[h].y);
+#pragma unroll
+            for (int h = 0; h < C::kCH; ++h)
+              chunk_math<WT, F16, NW, CH, false>(acc, qs + h * C::Q_CHUNK, ds + h * C::DCHUNK, bsrc, h * 512u, lrow,
+                                             lsub, sw, g, t);
           }
         }
       }
@@ -401,17 +421,17 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
 // One warps-per-CTA choice's plan for a launch: the column split ks with the smallest
 // estimate of the launch's duration, in 1/40 stage.  A launch with more items than resident
 // CTAs runs in waves of `grid` items (the last one partly filled), each as long as one item:
-// ceil(nchunks / ks) stages plus, for ks > 1, a CTA-wide reduction (about a quarter stage);
+// ceil(nst / ks) stages plus, for ks > 1, a CTA-wide reduction (about a quarter stage);
 // with ks = 1 a warp walks a row alone, which measured about 10% slower per stage.
 struct Plan {
   int ks = 1, nitems = 0, grid = 0, smem = 0;
   long long cost = -1;
 };
 
-template <int WT, bool F16, int NW>
+template <int WT, bool F16, int NW, int CH>
 cudaError_t plan_typed(const MatrixRef* ms, int n, const DeviceInfo& dev, Plan* out) {
-  using C = Cfg<WT, F16, NW>;
-  auto kern = matvec_bdiag_kernel<WT, F16, NW>;
+  using C = Cfg<WT, F16, NW, CH>;
+  auto kern = matvec_bdiag_kernel<WT, F16, NW, CH>;
   // per device: the shared-memory attribute set and the occupancy known (0 = does not fit)
   static std::mutex mu;
   static bool ready[64] = {};
@@ -434,16 +454,18 @@ cudaError_t plan_typed(const MatrixRef* ms, int n, const DeviceInfo& dev, Plan* 
   *out = Plan{};
   if (ctas_per_sm[dev.device] == 0) return cudaSuccess;  // does not fit: cost stays -1
   const long long slots = (long long)ctas_per_sm[dev.device] * dev.sm_count;
-  long long min_chunks = 1LL << 30;
-  for (int i = 0; i < n; ++i)
-    if (ms[i].cols / kTK < min_chunks) min_chunks = ms[i].cols / kTK;
+  long long min_stages = 1LL << 30;
+  for (int i = 0; i < n; ++i) {
+    const long long nst = (ms[i].cols / kTK + C::kCH - 1) / C::kCH;
+    if (nst < min_stages) min_stages = nst;
+  }
   Plan best;
-  for (int ks = 1; ks <= NW && ks <= min_chunks; ks *= 2) {
+  for (int ks = 1; ks <= NW && ks <= min_stages; ks *= 2) {
     const int tpi = NW / ks;
     long long items = 0, longest = 0;
     for (int i = 0; i < n; ++i) {
       items += ((ms[i].rows + C::WROWS - 1) / C::WROWS + tpi - 1) / tpi;
-      const long long st = (ms[i].cols / kTK + ks - 1) / ks;
+      const long long st = ((ms[i].cols / kTK + C::kCH - 1) / C::kCH + ks - 1) / ks;
       if (st > longest) longest = st;
     }
     const long long grid = items < slots ? items : slots;
@@ -461,10 +483,10 @@ cudaError_t plan_typed(const MatrixRef* ms, int n, const DeviceInfo& dev, Plan* 
   return cudaSuccess;
 }
 
-template <int WT, bool F16, int NW>
+template <int WT, bool F16, int NW, int CH>
 cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* const* xs, float* const* ys, int n,
                          bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
-  using C = Cfg<WT, F16, NW>;
+  using C = Cfg<WT, F16, NW, CH>;
   Params p{};
   p.nprob = n;
   p.status = dev.status;
@@ -476,7 +498,7 @@ cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* cons
     p.pr[i].y = ys[i];
     p.pr[i].rows = (int)ms[i].rows;
     p.pr[i].ntiles = (int)((ms[i].rows + C::WROWS - 1) / C::WROWS);
-    p.pr[i].nchunks = (int)(ms[i].cols / kTK);
+    p.pr[i].nst = (int)((ms[i].cols / kTK + C::kCH - 1) / C::kCH);
     p.pr[i].item0 = items;
     items += (p.pr[i].ntiles + tpi - 1) / tpi;
   }
@@ -495,8 +517,8 @@ cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* cons
     err = encode_tmap_2d(&maps.d[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, m.d, drow, (uint64_t)m.rows, drow, C::DROW,
                          C::WROWS, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (err != cudaSuccess) return err;
-    err = encode_tmap_2d(&maps.x[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xs[i], (uint64_t)m.cols, 1,
-                         (uint64_t)m.cols * 2, kTK, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
+    err = encode_tmap_2d(&maps.x[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xs[i], kTK, (uint64_t)(m.cols / kTK), kTK * 2,
+                         kTK, C::kCH, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (err != cudaSuccess) return err;
   }
 
@@ -510,29 +532,25 @@ cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* cons
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, matvec_bdiag_kernel<WT, F16, NW>, maps, p);
+  return cudaLaunchKernelEx(&cfg, matvec_bdiag_kernel<WT, F16, NW, CH>, maps, p);
 }
 
-// 4 warps per CTA; when that leaves SMs without a CTA (a launch with few tiles), 8 or 16
-// warps per CTA instead if their estimate is smaller (ties to fewer warps).  With every SM
-// busy, more warps per CTA measured slower (they share the SM's issue slots, and 16-warp CTAs
-// hold 2 stages per warp instead of 3).
+// Stages of two chunks (one-chunk stages fit more warps per SM and measured faster on large
+// Q4_0 launches alone, but slower on the Llama-7B layer step, the Q4_0 4096 x 4096 product and
+// Q8_0), in 4-warp CTAs; when that leaves SMs without a CTA (a launch with few tiles), 8-warp
+// CTAs instead if their estimate is smaller.
 template <int WT, bool F16>
 cudaError_t launch_best(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
                         const DeviceInfo& dev, cudaStream_t stream) {
-  Plan p4, p8, p16;
-  cudaError_t err = plan_typed<WT, F16, 4>(ms, n, dev, &p4);
+  Plan p4, p8;
+  cudaError_t err = plan_typed<WT, F16, 4, 2>(ms, n, dev, &p4);
   if (err != cudaSuccess) return err;
-  if (p4.cost >= 0 && p4.grid > dev.sm_count) return launch_typed<WT, F16, 4>(p4, ms, xs, ys, n, pdl, dev, stream);
-  err = plan_typed<WT, F16, 8>(ms, n, dev, &p8);
+  if (p4.cost >= 0 && p4.grid > dev.sm_count) return launch_typed<WT, F16, 4, 2>(p4, ms, xs, ys, n, pdl, dev, stream);
+  err = plan_typed<WT, F16, 8, 2>(ms, n, dev, &p8);
   if (err != cudaSuccess) return err;
-  err = plan_typed<WT, F16, 16>(ms, n, dev, &p16);
-  if (err != cudaSuccess) return err;
-  auto better = [](const Plan& a, const Plan& b) { return a.cost >= 0 && (b.cost < 0 || a.cost < b.cost); };
-  if (better(p16, p8) && better(p16, p4)) return launch_typed<WT, F16, 16>(p16, ms, xs, ys, n, pdl, dev, stream);
-  if (better(p8, p4)) return launch_typed<WT, F16, 8>(p8, ms, xs, ys, n, pdl, dev, stream);
+  if (p8.cost >= 0 && (p4.cost < 0 || p8.cost < p4.cost)) return launch_typed<WT, F16, 8, 2>(p8, ms, xs, ys, n, pdl, dev, stream);
   if (p4.cost < 0) return cudaErrorInvalidConfiguration;
-  return launch_typed<WT, F16, 4>(p4, ms, xs, ys, n, pdl, dev, stream);
+  return launch_typed<WT, F16, 4, 2>(p4, ms, xs, ys, n, pdl, dev, stream);
 }
 
 }  // namespace
