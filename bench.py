@@ -236,9 +236,11 @@ def run_reference(args, world, rank):
 
 # ------------------------------------------------------------------ other workloads
 def _graph_time_us(torch, launches, cap, replays=5):
-    """Per-launch GPU time of a list of launch closures, replayed as one CUDA graph."""
-    for f in launches[:2]:
-        f()
+    """Per-launch GPU time of a list of launch closures, replayed as one CUDA graph (warmed up
+    on the capture stream, whose first calls create its workspaces)."""
+    with torch.cuda.stream(cap):
+        for f in launches[:2]:
+            f()
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=cap):

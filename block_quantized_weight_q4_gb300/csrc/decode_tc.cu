@@ -29,13 +29,18 @@ void workspace_carve(void* base, size_t bytes, int n, Workspace* ws) {
 constexpr int kStreamCounters = 1024;
 constexpr size_t kStreamWorkspaceBytes = (size_t)4 << 20;
 
+// a stream's prefill workspace: counters for 4096 tiles, then the parts of split tiles
+// (ksplit x 128 rows x up to 128 vectors per tile; the launch picks ksplit to fit)
+constexpr int kPrefillCounters = 4096;
+constexpr size_t kPrefillWorkspaceBytes = (size_t)32 << 20;
+
 namespace {
 std::mutex g_ws_mu;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
-}  // namespace
+std::map<std::pair<int, cudaStream_t>, Workspace> g_pws;
 
-cudaError_t stream_workspace(const DeviceInfo& dev, cudaStream_t stream, Workspace* ws) {
-  auto& cache = g_ws;
+cudaError_t cached_workspace(std::map<std::pair<int, cudaStream_t>, Workspace>& cache, const DeviceInfo& dev,
+                             cudaStream_t stream, size_t bytes, int counters, Workspace* ws) {
   constexpr size_t kMaxEntries = 64;
   std::lock_guard<std::mutex> lock(g_ws_mu);
   const auto key = std::make_pair(dev.device, stream);
@@ -50,18 +55,27 @@ cudaError_t stream_workspace(const DeviceInfo& dev, cudaStream_t stream, Workspa
   if (err != cudaSuccess) return err;
   if (cs != cudaStreamCaptureStatusNone) return cudaErrorNotReady;  // no allocation while capturing
   void* base = nullptr;
-  err = cudaMalloc(&base, kStreamWorkspaceBytes);
+  err = cudaMalloc(&base, bytes);
   if (err != cudaSuccess) return err;
-  err = cudaMemsetAsync(base, 0, workspace_counter_bytes(kStreamCounters), stream);
+  err = cudaMemsetAsync(base, 0, workspace_counter_bytes(counters), stream);
   if (err != cudaSuccess) {
     cudaFree(base);
     return err;
   }
   Workspace w;
-  workspace_carve(base, kStreamWorkspaceBytes, kStreamCounters, &w);
+  workspace_carve(base, bytes, counters, &w);
   cache.emplace(key, w);
   *ws = w;
   return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t stream_workspace(const DeviceInfo& dev, cudaStream_t stream, Workspace* ws) {
+  return cached_workspace(g_ws, dev, stream, kStreamWorkspaceBytes, kStreamCounters, ws);
+}
+
+cudaError_t stream_prefill_workspace(const DeviceInfo& dev, cudaStream_t stream, Workspace* ws) {
+  return cached_workspace(g_pws, dev, stream, kPrefillWorkspaceBytes, kPrefillCounters, ws);
 }
 
 cudaError_t reset_workspaces() {
@@ -69,10 +83,12 @@ cudaError_t reset_workspaces() {
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   std::lock_guard<std::mutex> lock(g_ws_mu);
-  for (auto& kv : g_ws) {
-    if (kv.first.first != dev) continue;
-    err = cudaMemset(kv.second.counters, 0, workspace_counter_bytes(kv.second.max_counters));
-    if (err != cudaSuccess) return err;
+  for (auto* cache : {&g_ws, &g_pws}) {
+    for (auto& kv : *cache) {
+      if (kv.first.first != dev) continue;
+      err = cudaMemset(kv.second.counters, 0, workspace_counter_bytes(kv.second.max_counters));
+      if (err != cudaSuccess) return err;
+    }
   }
   return cudaDeviceSynchronize();
 }

@@ -6,8 +6,12 @@
 // exactly as qmv_dequant does (fl32(level * d)) and then rounded to bfloat16; products and
 // sums are formed by the tensor core in float32.
 //
-// One CTA owns 128 rows (the MMA's M) over all columns; the activation vectors are the MMA's
-// N (their count rounded up to 16).  Roles:
+// One CTA owns 128 rows (the MMA's M) over all columns, or, when the matrix has fewer
+// 128-row tiles than the GPU has SMs, over one of ksplit ranges of its columns (split-K: the
+// ksplit CTAs of a tile each write their 128 x N partial product to the stream's prefill
+// workspace and count their arrival on the tile's counter; the last to arrive adds the parts
+// in split order, stores y and resets the counter, so the result does not depend on timing).
+// The activation vectors are the MMA's N (their count rounded up to 16).  Roles:
 //   warp 0     TMA producer: raw stages (128 rows x 256 weights of q, 128 x 8 scales) and
 //              X stages (N x 64 bf16, 128-byte swizzle), each filling a ring slot and
 //              completing on its mbarrier.
@@ -65,27 +69,59 @@ struct PParams {
   int batch;  // vectors in this pass (1..128)
   int npad;   // batch rounded up to 16
   int* status;
+  int ksplit;          // column ranges per tile (1: no workspace used)
+  unsigned* counters;  // per tile arrival counters, zero between launches
+  float* parts;        // per (tile, split): 128 rows x npad partial sums, row-major
 };
 
-// float32 of (nibble - 8): 0x4B000000 | n is 2^23 + n exactly.
-__device__ __forceinline__ float q4_level(uint32_t w, int shift) {
-  return __fsub_rn(__uint_as_float(lop_and_or(w >> shift, 0xFu, 0x4B000000u)), 8388616.0f);
+__device__ __forceinline__ unsigned atomic_add_acq_rel_u32(unsigned* addr, unsigned v) {
+  unsigned old;
+  asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void epilogue_barrier() {  // the 8 dequantize/epilogue warps
+  asm volatile("bar.sync 1, %0;" ::"r"(32 * kDeqWarps) : "memory");
+}
+
+// fl32(a * d) and fl32(b * d) (one packed float32 multiply) rounded to a bfloat16 pair,
+// a in the low half.
+__device__ __forceinline__ uint32_t scale2_bf16(float a, float b, float d) {
+  float ra, rb;
+  asm("{\n\t.reg .b64 va, vd, vr;\n\t"
+      "mov.b64 va, {%2, %3};\n\t"
+      "mov.b64 vd, {%4, %4};\n\t"
+      "mul.rn.f32x2 vr, va, vd;\n\t"
+      "mov.b64 {%0, %1}, vr;\n\t}"
+      : "=f"(ra), "=f"(rb)
+      : "f"(a), "f"(b), "f"(d));
+  return pack_bf16x2(ra, rb);
+}
+
+// An IEEE-half level pair (exact small integers) times d, as bfloat16: RN(fl32(level * d)).
+__device__ __forceinline__ uint32_t scale_half_levels(uint32_t h2, float d) {
+  return scale2_bf16(__half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu))),
+                     __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16))), d);
 }
 
 // One Q4_0 block (quant bytes in w[0..3], byte j = word j/4 bits 8(j%4)) to 32 bf16 weights
 // RN(fl32(level * d)) in element order: out[0..7] elements 0..15 (low nibbles of bytes
-// 0..15), out[8..15] elements 16..31 (high nibbles).
+// 0..15), out[8..15] elements 16..31 (high nibbles).  The levels are formed as exact halves
+// (q4_word_to_f16_levels) and widened to float32 exactly.
 __device__ __forceinline__ void q4_block_to_bf16(const uint32_t (&w)[4], float d, uint32_t (&out)[16]) {
 #pragma unroll
-  for (int j = 0; j < 16; j += 2) {
-    const uint32_t wi = w[j >> 2];
-    const int sh = 8 * (j & 3);
-    out[j >> 1] = pack_bf16x2(__fmul_rn(q4_level(wi, sh), d), __fmul_rn(q4_level(wi, sh + 8), d));
-    out[8 + (j >> 1)] = pack_bf16x2(__fmul_rn(q4_level(wi, sh + 4), d), __fmul_rn(q4_level(wi, sh + 12), d));
+  for (int i = 0; i < 4; ++i) {
+    uint32_t lo01, lo23, hi01, hi23;
+    q4_word_to_f16_levels(w[i], lo01, lo23, hi01, hi23);
+    out[2 * i] = scale_half_levels(lo01, d);          // elements 4i, 4i+1
+    out[2 * i + 1] = scale_half_levels(lo23, d);      // 4i+2, 4i+3
+    out[8 + 2 * i] = scale_half_levels(hi01, d);      // 16+4i, 16+4i+1
+    out[8 + 2 * i + 1] = scale_half_levels(hi23, d);  // 16+4i+2, 16+4i+3
   }
 }
 
-// One Q8_0 block (32 int8 quants in w[0..7]) to 32 bf16 weights RN(fl32(q * d)), in order.
+// One Q8_0 block (32 int8 quants in w[0..7]) to 32 bf16 weights RN(fl32(q * d)), in order:
+// 0x4B000000 | (q + 128) is 2^23 + q + 128, minus 2^23 + 128 gives q exactly (packed pairs).
 __device__ __forceinline__ void q8_block_to_bf16(const uint32_t (&w)[8], float d, uint32_t (&out)[16]) {
   const float bias = 8388736.0f;  // 2^23 + 128
 #pragma unroll
@@ -95,8 +131,8 @@ __device__ __forceinline__ void q8_block_to_bf16(const uint32_t (&w)[8], float d
     const float f1 = __fsub_rn(__uint_as_float(prmt(u, 0x4B000000u, 0x7441)), bias);
     const float f2 = __fsub_rn(__uint_as_float(prmt(u, 0x4B000000u, 0x7442)), bias);
     const float f3 = __fsub_rn(__uint_as_float(prmt(u, 0x4B000000u, 0x7443)), bias);
-    out[2 * i] = pack_bf16x2(__fmul_rn(f0, d), __fmul_rn(f1, d));
-    out[2 * i + 1] = pack_bf16x2(__fmul_rn(f2, d), __fmul_rn(f3, d));
+    out[2 * i] = scale2_bf16(f0, f1, d);
+    out[2 * i + 1] = scale2_bf16(f2, f3, d);
   }
 }
 
@@ -139,9 +175,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   uint64_t* acc_full = empty + kKS;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* failed = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
 
-  const int row0 = (int)blockIdx.x * kPM;
-  const int nkb = p.cols / kKB;
+  // this CTA's tile and column range: raw stages [q0, q1) = 64-column stages kb0 + [0, nkb)
+  const int tile = (int)blockIdx.x / p.ksplit;
+  const int split = (int)blockIdx.x - tile * p.ksplit;
+  const int row0 = tile * kPM;
+  const int nq = p.cols / kRawK;
+  const int q0 = split * nq / p.ksplit;
+  const int q1 = (split + 1) * nq / p.ksplit;
+  const int kb0 = 4 * q0;
+  const int nkb = 4 * (q1 - q0);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRS; ++i) {
@@ -178,15 +222,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           mbar_arrive_expect_tx(&raw_full[r], C::Q_RAW + C::D_RAW);
 #pragma unroll
           for (int b = 0; b < C::NQBOX; ++b)
-            tma_load_2d(smem + C::OFF_Q + r * C::Q_RAW + b * (kPM * 128), &tq, q * C::QRAW_ROW + b * 128, row0,
-                        &raw_full[r], pol);
-          tma_load_2d(smem + C::OFF_D + r * C::D_RAW, &td, q * C::DROW, row0, &raw_full[r], pol);
+            tma_load_2d(smem + C::OFF_Q + r * C::Q_RAW + b * (kPM * 128), &tq, (q0 + q) * C::QRAW_ROW + b * 128,
+                        row0, &raw_full[r], pol);
+          tma_load_2d(smem + C::OFF_D + r * C::D_RAW, &td, (q0 + q) * C::DROW, row0, &raw_full[r], pol);
           raw_issued = q + 1;
         }
         const int s = kb % kKS;
         if (kb >= kKS && !pwait(&empty[s], (uint32_t)((kb / kKS - 1) & 1), failed, p.status)) break;
         mbar_arrive_expect_tx(&x_full[s], (uint32_t)(p.npad * 128));
-        tma_load_2d_keep(smem + C::OFF_X + s * C::X_STAGE, &tx, kb * kKB, 0, &x_full[s]);
+        tma_load_2d_keep(smem + C::OFF_X + s * C::X_STAGE, &tx, (kb0 + kb) * kKB, 0, &x_full[s]);
         x_issued = kb + 1;
       }
       if (*failed) {
@@ -271,18 +315,78 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       *failed = 1;
     }
     tc_fence_after();
-    if (ok && !*failed) {
-      const int quarter = warp & 3;
-      const int half = (warp - 2) >> 2;
-      const int grow = row0 + quarter * 32 + lane;
-      for (int c = half * 16; c < p.npad; c += 32) {
-        uint32_t v[16];
-        tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c, v);
-        tmem_ld_wait();
-        if (grow < p.rows) {
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int trow = quarter * 32 + lane;  // row within the tile
+    const int grow = row0 + trow;
+    if (p.ksplit == 1) {
+      if (ok && !*failed) {
+        for (int c = half * 16; c < p.npad; c += 32) {
+          uint32_t v[16];
+          tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c, v);
+          tmem_ld_wait();
+          if (grow < p.rows) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (c + i < p.batch) p.y[(size_t)(c + i) * p.rows + grow] = __uint_as_float(v[i]);
+          }
+        }
+      }
+    } else {
+      // this split's part (row-major: row trow's npad values contiguous); then the last CTA
+      // of the tile to arrive adds the parts in split order
+      float* part = p.parts + ((size_t)blockIdx.x * kPM + trow) * p.npad;
+      if (ok && !*failed) {
+        for (int c = half * 16; c < p.npad; c += 32) {
+          uint32_t v[16];
+          tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; i += 4)
+            *reinterpret_cast<uint4*>(part + c + i) = make_uint4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        }
+      }
+      epilogue_barrier();  // every part of this CTA is written before the release below
+      if (dt == 0) {
+        const unsigned before = atomic_add_acq_rel_u32(p.counters + tile, 1u);
+        const bool last = before + 1 == (unsigned)p.ksplit;
+        if (last) p.counters[tile] = 0u;  // every part has arrived: ready for the next launch
+        *last_flag = last ? 1 : 0;
+      }
+      epilogue_barrier();  // the acquire above is ordered before the loads below
+      if (*last_flag && !*failed && grow < p.rows) {
+        // this thread's columns: chunks half*16 + 32k (k < 4), 16 values each; every split's
+        // values of up to 4 chunks are loaded at once (16-byte loads) and added in split order
+        const float* rpart = p.parts + ((size_t)tile * p.ksplit * kPM + trow) * p.npad;
+        const size_t sstride = (size_t)kPM * p.npad;  // floats between splits of the tile
+        float sum[4][16];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int i = 0; i < 16; ++i) sum[k][i] = 0.f;
+        for (int sp = 0; sp < p.ksplit; ++sp) {
+          const float* src = rpart + sp * sstride;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int c = half * 16 + 32 * k;
+            if (c < p.npad) {
+#pragma unroll
+              for (int i = 0; i < 16; i += 4) {
+                const float4 q = __ldcg(reinterpret_cast<const float4*>(src + c + i));
+                sum[k][i] += q.x;
+                sum[k][i + 1] += q.y;
+                sum[k][i + 2] += q.z;
+                sum[k][i + 3] += q.w;
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int c = half * 16 + 32 * k;
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            if (c + i < p.batch) p.y[(size_t)(c + i) * p.rows + grow] = __uint_as_float(v[i]);
+            if (c + i < p.batch) p.y[(size_t)(c + i) * p.rows + grow] = sum[k][i];
         }
       }
     }
@@ -303,9 +407,22 @@ bool prefill_supported(const MatrixRef& m, bool x_bf16) {
 
 int prefill_max_batch() { return kMaxN; }
 
+// Column ranges per tile: enough to give every SM a CTA when the matrix has fewer tiles than
+// SMs (at least two raw stages per range), within the workspace; 1 without one.
+static int prefill_ksplit(const MatrixRef& m, int npad, const DeviceInfo& dev, const Workspace* ws) {
+  const long long tiles = (m.rows + kPM - 1) / kPM;
+  const long long nq = m.cols / kRawK;
+  if (ws == nullptr || tiles >= dev.sm_count || tiles > ws->max_counters) return 1;
+  long long k = dev.sm_count / tiles;
+  if (k > nq / 2) k = nq / 2;
+  if (k > 16) k = 16;
+  while (k > 1 && (size_t)(tiles * k * npad * kPM) > ws->max_partial_floats) --k;
+  return k < 1 ? 1 : (int)k;
+}
+
 template <int WT, bool F16>
 static cudaError_t launch_prefill_typed(const MatrixRef& m, const void* x, float* y, int batch, const DeviceInfo& dev,
-                                        cudaStream_t stream) {
+                                        const Workspace* ws, cudaStream_t stream) {
   using C = PCfg<WT, F16>;
   auto kern = prefill_kernel<WT, F16>;
   static bool ready[64] = {};
@@ -322,6 +439,9 @@ static cudaError_t launch_prefill_typed(const MatrixRef& m, const void* x, float
   p.batch = batch;
   p.npad = (batch + 15) / 16 * 16;
   p.status = dev.status;
+  p.ksplit = prefill_ksplit(m, p.npad, dev, ws);
+  p.counters = p.ksplit > 1 ? ws->counters : nullptr;
+  p.parts = p.ksplit > 1 ? ws->partials : nullptr;
   CUtensorMap tq, td, tx;
   const uint64_t qrow = (WT == QMV_Q4_0) ? (uint64_t)m.cols / 2 : (uint64_t)m.cols;
   const uint64_t drow = (uint64_t)(m.cols / 32) * C::ESZ;
@@ -334,20 +454,20 @@ static cudaError_t launch_prefill_typed(const MatrixRef& m, const void* x, float
   err = encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)m.cols, (uint64_t)batch,
                        (uint64_t)m.cols * 2, kKB, p.npad, CU_TENSOR_MAP_SWIZZLE_128B);
   if (err != cudaSuccess) return err;
-  const int grid = (int)((m.rows + kPM - 1) / kPM);
+  const int grid = (int)((m.rows + kPM - 1) / kPM) * p.ksplit;
   kern<<<grid, kThreads, C::SMEM, stream>>>(tq, td, tx, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_prefill(const MatrixRef& m, const void* x, float* y, int batch, const DeviceInfo& dev,
-                           cudaStream_t stream) {
+                           const Workspace* ws, cudaStream_t stream) {
   if (batch < 1 || batch > kMaxN) return cudaErrorInvalidValue;
   if (m.wtype == QMV_Q4_0) {
-    return m.scale_f16 ? launch_prefill_typed<QMV_Q4_0, true>(m, x, y, batch, dev, stream)
-                       : launch_prefill_typed<QMV_Q4_0, false>(m, x, y, batch, dev, stream);
+    return m.scale_f16 ? launch_prefill_typed<QMV_Q4_0, true>(m, x, y, batch, dev, ws, stream)
+                       : launch_prefill_typed<QMV_Q4_0, false>(m, x, y, batch, dev, ws, stream);
   }
-  return m.scale_f16 ? launch_prefill_typed<QMV_Q8_0, true>(m, x, y, batch, dev, stream)
-                     : launch_prefill_typed<QMV_Q8_0, false>(m, x, y, batch, dev, stream);
+  return m.scale_f16 ? launch_prefill_typed<QMV_Q8_0, true>(m, x, y, batch, dev, ws, stream)
+                     : launch_prefill_typed<QMV_Q8_0, false>(m, x, y, batch, dev, ws, stream);
 }
 
 }  // namespace qmv

@@ -167,12 +167,16 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
   for (int i = 0; i < n; ++i) {
     use_prefill[i] = batch >= kPrefillMinBatch && prefill_supported(ms[i], xb);
     if (use_prefill[i]) {
+      // split tiles between CTAs when the stream has its prefill workspace (created on the
+      // stream's first prefill call, never while it is captured)
+      Workspace pws;
+      const Workspace* pw = stream_prefill_workspace(dev, stream, &pws) == cudaSuccess ? &pws : nullptr;
       const int pmax = prefill_max_batch();
       for (int b0 = 0; b0 < batch; b0 += pmax) {
         const int nb = (batch - b0) < pmax ? (batch - b0) : pmax;
         const void* xp = static_cast<const uint8_t*>(problems[i].x) + (size_t)b0 * (size_t)ms[i].cols * xsz;
         float* yp = problems[i].y + (size_t)b0 * (size_t)ms[i].rows;
-        if (launch_prefill(ms[i], xp, yp, nb, dev, stream) != cudaSuccess) return QMV_E_CUDA;
+        if (launch_prefill(ms[i], xp, yp, nb, dev, pw, stream) != cudaSuccess) return QMV_E_CUDA;
       }
     } else {
       any_decode = true;

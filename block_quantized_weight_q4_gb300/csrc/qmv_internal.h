@@ -41,7 +41,9 @@ void workspace_carve(void* base, size_t bytes, int n, Workspace* ws);
 // The workspace of (current device, stream), allocated and zeroed on first use; returns
 // cudaErrorNotReady when there is none yet and the stream is being captured.
 cudaError_t stream_workspace(const DeviceInfo& dev, cudaStream_t stream, Workspace* ws);
-// Zero the counters of every workspace of the current device (after a kernel gave up on a
+// The same for the prefill kernel's split tiles (a separate, larger workspace per stream).
+cudaError_t stream_prefill_workspace(const DeviceInfo& dev, cudaStream_t stream, Workspace* ws);
+// Zero the counters of every workspace (decode and prefill) of the current device (after a kernel gave up on a
 // bounded wait, a counter may have been left part-way); synchronous.
 cudaError_t reset_workspaces();
 
@@ -78,11 +80,12 @@ cudaError_t launch_matvec_bdiag(const MatrixRef* ms, const void* const* xs, floa
 
 // Batched product on the 5th-generation tensor core (weights dequantized to bf16 in shared
 // memory, tcgen05 MMA into tensor memory): bf16 activations, cols % 256 == 0, 1..128
-// vectors per launch (meant for 16 and more).
+// vectors per launch (meant for 16 and more).  ws: the stream's prefill workspace, or null
+// (then no tile is split between CTAs).
 bool prefill_supported(const MatrixRef& m, bool x_bf16);
 int prefill_max_batch();
 cudaError_t launch_prefill(const MatrixRef& m, const void* x, float* y, int batch, const DeviceInfo& dev,
-                           cudaStream_t stream);
+                           const Workspace* ws, cudaStream_t stream);
 
 // Decode product on the 5th-generation tensor core with the weights unpacked into tensor
 // memory: bf16 activations, cols % 256 == 0, 1..8 vectors, 1..decode_tc_max_problems()

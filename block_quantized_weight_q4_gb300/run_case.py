@@ -42,11 +42,14 @@ def main(argv=None):
     x = inputs.make_x(a.batch, a.cols, not a.x_f32, seed=2)
     xd = torch.from_numpy(x).cuda() if a.x_f32 else torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
     y = torch.empty((a.batch, a.rows), device="cuda")
-    for i in range(a.iters):
-        qmv.matvec(a.wtype, a.scale_f16, a.rows, a.cols, Ws[i % a.copies], xd, y)
+    # eager calls on the stream that is captured below: a stream's first call creates the
+    # workspace its split tiles use (never while it is being captured)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for i in range(a.iters):
+            qmv.matvec(a.wtype, a.scale_f16, a.rows, a.cols, Ws[i % a.copies], xd, y)
     torch.cuda.synchronize()
     if a.graph_calls > 0:
-        s = torch.cuda.Stream()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
             for i in range(a.graph_calls):

@@ -111,7 +111,10 @@ int qmv_matrix_wtype(int file_wtype, uint32_t q8_mask, int class_bit, int shared
  * the call takes the mma.sync kernel instead).  Results do not depend on timing.
  * bfloat16 batches of 16 and more (cols % 256 == 0) run in passes of up to 128 through the
  * prefill kernel (each weight dequantized as qmv_dequant does and rounded to bfloat16 in
- * shared memory, tcgen05 MMA into tensor memory, f32 accumulate).
+ * shared memory, tcgen05 MMA into tensor memory, f32 accumulate); a matrix with fewer
+ * 128-row tiles than the GPU has SMs has its columns split between CTAs, whose parts meet in
+ * a second workspace of the calling stream (32 MiB, allocated like the first; without it the
+ * call does not split).
  * Products agree with an
  * exact evaluation to within 1e-3 * sum_c |W[r][c] x[c]| per output.  A Q8_0 byte of
  * -128 is not rejected here: it decodes as -128 * d (see qmv_validate).

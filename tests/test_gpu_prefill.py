@@ -134,3 +134,52 @@ def test_prefill_output_guards(qmv):
     torch.cuda.synchronize()
     b = buf.cpu().numpy()
     assert np.all(b[:128] == 4321.0) and np.all(b[128 + batch * rows:] == 4321.0)
+
+
+@pytest.mark.parametrize("wt,sf", [(2, 1), (1, 0)])
+def test_prefill_split_tiles_repeat_and_graph_bit_identical(qmv, wt, sf):
+    # 3 row tiles of 128 over 56 raw stages: each tile's columns are split between 16 CTAs,
+    # whose parts the last of them adds in split order; the counters must be back at zero after
+    # every call (repeated calls and graph replays give the same bits)
+    import torch
+    from helpers import assert_bits_equal
+    rows, cols, batch = 300, 14336, 64
+    m = inputs.make_matrix(wt, sf, rows, cols, seed=31)
+    x = inputs.make_x(batch, cols, True, seed=32)
+    y_ref, absref = oracle.matvec(m.W, wt, sf, rows, cols, x)
+    W, xd = dev_u8(m.W), dev_x(x)
+    s = torch.cuda.Stream()
+    y = torch.empty((batch, rows), device="cuda")
+    with torch.cuda.stream(s):
+        qmv.matvec(wt, sf, rows, cols, W, xd, y)
+    torch.cuda.synchronize()
+    first = y.cpu().numpy().copy()
+    check_product(first, y_ref, absref, TOL, f"prefill split {wt},{sf}")
+    for _ in range(3):
+        with torch.cuda.stream(s):
+            qmv.matvec(wt, sf, rows, cols, W, xd, y)
+        torch.cuda.synchronize()
+        assert_bits_equal(y.cpu().numpy(), first, "repeated split-tile prefill")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(2):
+            qmv.matvec(wt, sf, rows, cols, W, xd, y)
+    y.fill_(0.0)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert_bits_equal(y.cpu().numpy(), first, "split-tile prefill graph replay")
+
+
+def test_prefill_split_tiles_exact_pow2(qmv):
+    # exact case over split tiles: power-of-two scales, integer x; any order of the parts'
+    # addition gives the oracle's value
+    rows, cols, batch = 256, 8192, 32
+    rng = np.random.default_rng(33)
+    m = inputs.make_matrix(2, 1, rows, cols, seed=34)
+    codes = inputs.pow2_scales(rng, rows * cols // 32, 1)
+    W = inputs.assemble(2, 1, rows, cols, m.q, codes)
+    m2 = inputs.Matrix(2, 1, rows, cols, W, m.q, codes)
+    x = inputs.make_int_x(batch, cols, True, seed=35)
+    y_ref, _ = oracle.matvec(W, 2, 1, rows, cols, x)
+    assert np.array_equal(run(qmv, m2, x).astype(np.float64), y_ref)
