@@ -12,15 +12,19 @@
 // workspace and count their arrival on the tile's counter; the last to arrive adds the parts
 // in split order, stores y and resets the counter, so the result does not depend on timing).
 // The activation vectors are the MMA's N (their count rounded up to 16).  Roles:
-//   warp 0     TMA producer: raw stages (128 rows x 256 weights of q, 128 x 8 scales) and
-//              X stages (N x 64 bf16, 128-byte swizzle), each filling a ring slot and
-//              completing on its mbarrier.
+//   warp 0     TMA producer of the raw stages (128 rows x 256 weights of q, 128 x 8 scales).
+//   warp 10    TMA producer of the X stages (N x 64 bf16, 128-byte swizzle); a stage's slot is
+//              free once the MMAs that read it complete, and the weight loads must not wait
+//              for that, hence a producer of their own.
 //   warp 1     allocates tensor memory (128 lanes x 128 f32 columns); lane 0 issues, per
 //              64-column stage, four tcgen05.mma (M 128, N, K 16, bf16 in, f32 accumulate)
 //              from the bf16 weight stage and the X stage, then commits to the stage's
 //              "empty" barrier; after the last stage it commits to "accumulator full".
-//   warps 2-9  dequantize: thread (row, half) turns one 32-weight block of its row into 32
-//              bf16 weights written in the MMA's K-major 128-byte-swizzled layout; then they
+//   warps 2-9  dequantize two 64-column stages at a time: thread (row, half) turns one
+//              32-weight block of its row per stage into 32 bf16 weights written in the MMA's
+//              K-major 128-byte-swizzled layout (one proxy fence and one pass of waits per
+//              pair of stages: the per-stage synchronisation, not the arithmetic, set the
+//              pace when every stage had its own); then they
 //              read the accumulator from tensor memory (each warp its 32-lane quarter, half
 //              of the columns) and store y.
 // Every wait is bounded; a wait that runs out records QMV_E_TIMEOUT and the roles unwind.
@@ -36,9 +40,11 @@ constexpr int kPM = 128;      // rows of W per CTA tile = MMA M = tensor-memory 
 constexpr int kKB = 64;       // columns per MMA stage: one 128-byte swizzle span of bf16
 constexpr int kRawK = 256;    // columns per raw (quantized) stage
 constexpr int kKS = 4;        // ring depth of the bf16-weight and X stages
-constexpr int kRS = 2;        // ring depth of the raw stages
+constexpr int kRS = 2;        // ring depth of the raw stages (deeper measured no faster)
+static_assert(kKS % 2 == 0, "the dequantize warps fill the weight ring two stages at a time");
 constexpr int kDeqWarps = 8;  // dequantize, then drain the accumulator
-constexpr int kThreads = 32 * (2 + kDeqWarps);
+constexpr int kXWarp = 2 + kDeqWarps;  // the X-stage producer
+constexpr int kThreads = 32 * (3 + kDeqWarps);
 constexpr int kMaxN = 128;    // activation vectors per pass
 constexpr int kTmemCols = 128;
 
@@ -60,6 +66,7 @@ struct PCfg {
   static constexpr int NBARS = 2 * kRS + 3 * kKS + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;  // tensor-memory base, failure flag
   static constexpr int SMEM = 1024 + OFF_MISC + 16;
+  static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
 };
 
 struct PParams {
@@ -144,8 +151,10 @@ __device__ __forceinline__ void lds128(uint32_t addr, uint32_t& a, uint32_t& b, 
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr) : "memory");
 }
 
-// Bounded wait that gives up at once when another role has already failed.
+// Bounded wait that gives up at once when another role has already failed (a phase that has
+// already completed returns without reading the failure flag).
 __device__ __forceinline__ bool pwait(uint64_t* bar, uint32_t parity, volatile int* failed, int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
   if (*failed) return false;
   if (mbar_wait_bounded(bar, parity)) return true;
   record_status(status, QMV_E_TIMEOUT);
@@ -211,27 +220,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- TMA producer
+    // ---------------------------------------------------------------- raw-stage producer
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
-      int raw_issued = 0, x_issued = 0;
-      for (int kb = 0; kb < nkb && !*failed; ++kb) {
-        if (kb % 4 == 0) {
-          const int q = kb / 4, r = q % kRS;
-          if (q >= kRS && !pwait(&raw_empty[r], (uint32_t)((q / kRS - 1) & 1), failed, p.status)) break;
-          mbar_arrive_expect_tx(&raw_full[r], C::Q_RAW + C::D_RAW);
+      const int nqs = q1 - q0;
+      int raw_issued = 0;
+      for (int q = 0; q < nqs && !*failed; ++q) {
+        const int r = q % kRS;
+        if (q >= kRS && !pwait(&raw_empty[r], (uint32_t)((q / kRS - 1) & 1), failed, p.status)) break;
+        mbar_arrive_expect_tx(&raw_full[r], C::Q_RAW + C::D_RAW);
 #pragma unroll
-          for (int b = 0; b < C::NQBOX; ++b)
-            tma_load_2d(smem + C::OFF_Q + r * C::Q_RAW + b * (kPM * 128), &tq, (q0 + q) * C::QRAW_ROW + b * 128,
-                        row0, &raw_full[r], pol);
-          tma_load_2d(smem + C::OFF_D + r * C::D_RAW, &td, (q0 + q) * C::DROW, row0, &raw_full[r], pol);
-          raw_issued = q + 1;
-        }
-        const int s = kb % kKS;
-        if (kb >= kKS && !pwait(&empty[s], (uint32_t)((kb / kKS - 1) & 1), failed, p.status)) break;
-        mbar_arrive_expect_tx(&x_full[s], (uint32_t)(p.npad * 128));
-        tma_load_2d_keep(smem + C::OFF_X + s * C::X_STAGE, &tx, (kb0 + kb) * kKB, 0, &x_full[s]);
-        x_issued = kb + 1;
+        for (int b = 0; b < C::NQBOX; ++b)
+          tma_load_2d(smem + C::OFF_Q + r * C::Q_RAW + b * (kPM * 128), &tq, (q0 + q) * C::QRAW_ROW + b * 128, row0,
+                      &raw_full[r], pol);
+        tma_load_2d(smem + C::OFF_D + r * C::D_RAW, &td, (q0 + q) * C::DROW, row0, &raw_full[r], pol);
+        raw_issued = q + 1;
       }
       if (*failed) {
         // let the copies still in flight land before the shared memory is released
@@ -239,6 +242,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           const int last = raw_issued - 1 - ((raw_issued - 1 - r) % kRS);  // last raw stage in slot r
           mbar_wait_bounded(&raw_full[last % kRS], (uint32_t)((last / kRS) & 1), 400000000LL);
         }
+      }
+    }
+  } else if (warp == kXWarp) {
+    // ---------------------------------------------------------------- X-stage producer
+    if (lane == 0) {
+      int x_issued = 0;
+      for (int kb = 0; kb < nkb && !*failed; ++kb) {
+        const int s = kb % kKS;
+        if (kb >= kKS && !pwait(&empty[s], (uint32_t)((kb / kKS - 1) & 1), failed, p.status)) break;
+        mbar_arrive_expect_tx(&x_full[s], (uint32_t)(p.npad * 128));
+        tma_load_2d_keep(smem + C::OFF_X + s * C::X_STAGE, &tx, (kb0 + kb) * kKB, 0, &x_full[s]);
+        x_issued = kb + 1;
+      }
+      if (*failed) {
         for (int s = 0; s < kKS && s < x_issued; ++s) {
           const int last = x_issued - 1 - ((x_issued - 1 - s) % kKS);
           mbar_wait_bounded(&x_full[last % kKS], (uint32_t)((last / kKS) & 1), 400000000LL);
@@ -270,41 +287,58 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const int h = dt >> 7;  // which block of each 64-column stage
     const int sw = row & 7;
     const uint32_t a_row = (uint32_t)((row >> 3) * 1024 + sw * 128);
-    for (int kb = 0; kb < nkb; ++kb) {
+    // stages kb and kb + 1 (slots s and s + 1 of the weight ring, blocks blk and blk + 2 of
+    // the raw stage)
+    for (int kb = 0; kb < nkb; kb += 2) {
       const int q = kb / 4, r = q % kRS;
       if (kb % 4 == 0 && !pwait(&raw_full[r], (uint32_t)((q / kRS) & 1), failed, p.status)) break;
       const int s = kb % kKS;
-      if (kb >= kKS && !pwait(&empty[s], (uint32_t)((kb / kKS - 1) & 1), failed, p.status)) break;
-      const int blk = 2 * (kb & 3) + h;  // block of the raw stage
-      float d;
+      if (kb >= kKS && (!pwait(&empty[s], (uint32_t)((kb / kKS - 1) & 1), failed, p.status) ||
+                        !pwait(&empty[s + 1], (uint32_t)(((kb + 1) / kKS - 1) & 1), failed, p.status)))
+        break;
+      const int blk = 2 * (kb & 3) + h;
+      float d0, d1;
       if (F16) {
-        d = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(smem + C::OFF_D + r * C::D_RAW + row * C::DROW + 2 * blk));
+        const uint16_t* ds = reinterpret_cast<const uint16_t*>(smem + C::OFF_D + r * C::D_RAW + row * C::DROW);
+        d0 = f16_bits_to_f32(ds[blk]);
+        d1 = f16_bits_to_f32(ds[blk + 2]);
       } else {
-        d = *reinterpret_cast<const float*>(smem + C::OFF_D + r * C::D_RAW + row * C::DROW + 4 * blk);
+        const float* ds = reinterpret_cast<const float*>(smem + C::OFF_D + r * C::D_RAW + row * C::DROW);
+        d0 = ds[blk];
+        d1 = ds[blk + 2];
       }
-      uint32_t out[16];
+      uint32_t out0[16], out1[16];
       const uint32_t qrow = sbase + C::OFF_Q + r * C::Q_RAW + row * 128;
       if (WT == QMV_Q4_0) {
-        uint32_t w[4];
-        lds128(qrow + ((blk ^ sw) << 4), w[0], w[1], w[2], w[3]);
-        q4_block_to_bf16(w, d, out);
+        uint32_t w0[4], w1[4];
+        lds128(qrow + ((blk ^ sw) << 4), w0[0], w0[1], w0[2], w0[3]);
+        lds128(qrow + (((blk + 2) ^ sw) << 4), w1[0], w1[1], w1[2], w1[3]);
+        q4_block_to_bf16(w0, d0, out0);
+        q4_block_to_bf16(w1, d1, out1);
       } else {
-        uint32_t w[8];
+        uint32_t w0[8], w1[8];
         const uint32_t box = qrow + (blk >> 2) * (kPM * 128);
-        const int c0 = 2 * (blk & 3);
-        lds128(box + ((c0 ^ sw) << 4), w[0], w[1], w[2], w[3]);
-        lds128(box + (((c0 + 1) ^ sw) << 4), w[4], w[5], w[6], w[7]);
-        q8_block_to_bf16(w, d, out);
+        const int c0 = 2 * (blk & 3);  // blk + 2 lies in the same 128-byte box (blk & 3 < 2)
+        lds128(box + ((c0 ^ sw) << 4), w0[0], w0[1], w0[2], w0[3]);
+        lds128(box + (((c0 + 1) ^ sw) << 4), w0[4], w0[5], w0[6], w0[7]);
+        lds128(box + (((c0 + 4) ^ sw) << 4), w1[0], w1[1], w1[2], w1[3]);
+        lds128(box + (((c0 + 5) ^ sw) << 4), w1[4], w1[5], w1[6], w1[7]);
+        q8_block_to_bf16(w0, d0, out0);
+        q8_block_to_bf16(w1, d1, out1);
       }
       const uint32_t arow = sbase + s * C::A_STAGE + a_row;
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        sts128(arow + (((4 * h + j) ^ sw) << 4), out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
+      for (int j = 0; j < 4; ++j) {
+        sts128(arow + (((4 * h + j) ^ sw) << 4), out0[4 * j], out0[4 * j + 1], out0[4 * j + 2], out0[4 * j + 3]);
+        sts128(arow + C::A_STAGE + (((4 * h + j) ^ sw) << 4), out1[4 * j], out1[4 * j + 1], out1[4 * j + 2],
+               out1[4 * j + 3]);
+      }
       fence_proxy_async_smem();  // the tensor core reads these stores through the async proxy
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&a_full[s]);
-        if ((kb & 3) == 3) mbar_arrive(&raw_empty[r]);
+        mbar_arrive(&a_full[s + 1]);
+        if ((kb & 3) == 2) mbar_arrive(&raw_empty[r]);
       }
     }
     // drain the accumulator: warp w reads tensor-memory lanes 32*(w%4) .. +31 (its rows) and
