@@ -13,20 +13,25 @@
 // in split order, stores y and resets the counter, so the result does not depend on timing).
 // The activation vectors are the MMA's N (their count rounded up to 16).  Roles:
 //   warp 0     TMA producer of the raw stages (128 rows x 256 weights of q, 128 x 8 scales).
-//   warp 10    TMA producer of the X stages (N x 64 bf16, 128-byte swizzle); a stage's slot is
+//   warp 18    TMA producer of the X stages (N x 64 bf16, 128-byte swizzle); a stage's slot is
 //              free once the MMAs that read it complete, and the weight loads must not wait
 //              for that, hence a producer of their own.
-//   warp 1     allocates tensor memory (128 lanes x 128 f32 columns); lane 0 issues, per
-//              64-column stage, four tcgen05.mma (M 128, N, K 16, bf16 in, f32 accumulate)
-//              from the bf16 weight stage and the X stage, then commits to the stage's
-//              "empty" barrier; after the last stage it commits to "accumulator full".
-//   warps 2-9  dequantize two 64-column stages at a time: thread (row, half) turns one
+//   warp 1     allocates tensor memory (128 lanes x 256 f32 columns: two accumulators).
+//   warps 1, 19  lane 0 issues, per 64-column stage (warp 1 the even ones into accumulator 0,
+//              warp 19 the odd ones into accumulator 1), four tcgen05.mma (M 128, N, K 16,
+//              bf16 in, f32 accumulate) from the bf16 weight stage and the X stage, then
+//              commits to the stage's "empty" barrier; after its last stage, to
+//              "accumulator full".  One issuing thread could not keep up: each instruction
+//              costs it tens of cycles while the tensor core finishes a stage in fewer.
+//   warps 2-17 dequantize, in two groups of eight (warps 2-9 and 10-17) that take turns
+//              with the pairs of 64-column stages: thread (row, half) of a group turns one
 //              32-weight block of its row per stage into 32 bf16 weights written in the MMA's
 //              K-major 128-byte-swizzled layout (one proxy fence and one pass of waits per
 //              pair of stages: the per-stage synchronisation, not the arithmetic, set the
-//              pace when every stage had its own); then they
-//              read the accumulator from tensor memory (each warp its 32-lane quarter, half
-//              of the columns) and store y.
+//              pace when every stage had its own; two groups keep four warps per scheduler
+//              busy).  Then they read the accumulators from tensor memory (each warp its
+//              32-lane quarter and a quarter of the columns) and store y, or, for a split
+//              tile, the CTA's part (vector-major) for the last CTA to add.
 // Every wait is bounded; a wait that runs out records QMV_E_TIMEOUT and the roles unwind.
 #include "qmv_common.cuh"
 #include "qmv_internal.h"
@@ -39,14 +44,14 @@ namespace {
 constexpr int kPM = 128;      // rows of W per CTA tile = MMA M = tensor-memory lanes
 constexpr int kKB = 64;       // columns per MMA stage: one 128-byte swizzle span of bf16
 constexpr int kRawK = 256;    // columns per raw (quantized) stage
-constexpr int kKS = 4;        // ring depth of the bf16-weight and X stages
+constexpr int kMaxXS = 16;    // deepest X ring (its depth is set per launch by the batch)
 constexpr int kRS = 2;        // ring depth of the raw stages (deeper measured no faster)
-static_assert(kKS % 2 == 0, "the dequantize warps fill the weight ring two stages at a time");
-constexpr int kDeqWarps = 8;  // dequantize, then drain the accumulator
+constexpr int kDeqWarps = 16;  // dequantize (two groups of 8); the first group drains the accumulators
 constexpr int kXWarp = 2 + kDeqWarps;  // the X-stage producer
-constexpr int kThreads = 32 * (3 + kDeqWarps);
+constexpr int kMmaWarp2 = 3 + kDeqWarps;  // the second MMA issuer (odd stages)
+constexpr int kThreads = 32 * (4 + kDeqWarps);
 constexpr int kMaxN = 128;    // activation vectors per pass
-constexpr int kTmemCols = 128;
+constexpr int kTmemCols = 256;  // two accumulators of 128 columns (even and odd stages)
 
 template <int WT, bool F16>
 struct PCfg {
@@ -57,16 +62,22 @@ struct PCfg {
   static constexpr int DROW = (kRawK / 32) * ESZ;                        // scale bytes per row per raw stage
   static constexpr int D_RAW = kPM * DROW;
   static constexpr int A_STAGE = kPM * 128;                              // 128 rows x 64 bf16
-  static constexpr int X_STAGE = kMaxN * 128;                            // up to 128 vectors x 64 bf16
-  static constexpr int OFF_X = kKS * A_STAGE;
-  static constexpr int OFF_Q = OFF_X + kKS * X_STAGE;
+  // ring depth of the bf16-weight stages: deep enough that each dequantize group can fill one
+  // pair of stages while the MMAs of its previous pair are still in flight, within the
+  // shared memory that the raw ring and at least two 128-vector X stages leave
+  static constexpr int KS = (WT == QMV_Q4_0) ? 8 : 6;
+  static_assert(KS % 2 == 0, "the dequantize warps fill the weight ring two stages at a time");
+  static constexpr int OFF_Q = KS * A_STAGE;
   static constexpr int OFF_D = OFF_Q + kRS * Q_RAW;
   static constexpr int OFF_BAR = OFF_D + kRS * D_RAW;
-  // barriers: raw_full[kRS], raw_empty[kRS], x_full[kKS], a_full[kKS], empty[kKS], acc_full
-  static constexpr int NBARS = 2 * kRS + 3 * kKS + 1;
-  static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;  // tensor-memory base, failure flag
-  static constexpr int SMEM = 1024 + OFF_MISC + 16;
-  static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
+  // barriers: raw_full[kRS], raw_empty[kRS], a_full[KS], empty[KS], x_full[kMaxXS],
+  // x_empty[kMaxXS], acc_full
+  static constexpr int NBARS = 2 * kRS + 2 * KS + 2 * kMaxXS + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;  // tensor-memory base, failure and last flags
+  static constexpr int OFF_X = (OFF_MISC + 16 + 1023) / 1024 * 1024;  // X ring (1024-aligned stages)
+  // shared memory of a launch with an X ring of xs stages of npad vectors (npad x 128 bytes)
+  static constexpr int smem_bytes(int xs, int npad) { return 1024 + OFF_X + xs * npad * 128; }
+  static_assert(smem_bytes(2, kMaxN) <= 227 * 1024, "shared memory of one CTA");
 };
 
 struct PParams {
@@ -76,9 +87,10 @@ struct PParams {
   int batch;  // vectors in this pass (1..128)
   int npad;   // batch rounded up to 16
   int* status;
+  int xs;              // X ring depth (2..kMaxXS)
   int ksplit;          // column ranges per tile (1: no workspace used)
   unsigned* counters;  // per tile arrival counters, zero between launches
-  float* parts;        // per (tile, split): 128 rows x npad partial sums, row-major
+  float* parts;        // per (tile, split): npad x 128 partial sums, vector-major
 };
 
 __device__ __forceinline__ unsigned atomic_add_acq_rel_u32(unsigned* addr, unsigned v) {
@@ -87,7 +99,7 @@ __device__ __forceinline__ unsigned atomic_add_acq_rel_u32(unsigned* addr, unsig
   return old;
 }
 
-__device__ __forceinline__ void epilogue_barrier() {  // the 8 dequantize/epilogue warps
+__device__ __forceinline__ void epilogue_barrier() {  // the dequantize warps
   asm volatile("bar.sync 1, %0;" ::"r"(32 * kDeqWarps) : "memory");
 }
 
@@ -151,6 +163,16 @@ __device__ __forceinline__ void lds128(uint32_t addr, uint32_t& a, uint32_t& b, 
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr) : "memory");
 }
 
+// 16 columns of accumulator 0 plus the same columns of accumulator 1 (128 columns on).
+__device__ __forceinline__ void acc_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  uint32_t u[16];
+  tmem_ld16(taddr, v);
+  tmem_ld16(taddr + 128u, u);
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(u[i]));
+}
+
 // Bounded wait that gives up at once when another role has already failed (a phase that has
 // already completed returns without reading the failure flag).
 __device__ __forceinline__ bool pwait(uint64_t* bar, uint32_t parity, volatile int* failed, int* status) {
@@ -178,10 +200,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* raw_full = bars;
   uint64_t* raw_empty = bars + kRS;
-  uint64_t* x_full = bars + 2 * kRS;
-  uint64_t* a_full = x_full + kKS;
-  uint64_t* empty = a_full + kKS;
-  uint64_t* acc_full = empty + kKS;
+  uint64_t* a_full = bars + 2 * kRS;
+  uint64_t* empty = a_full + C::KS;
+  uint64_t* x_full = empty + C::KS;
+  uint64_t* x_empty = x_full + kMaxXS;
+  uint64_t* acc_full = x_empty + kMaxXS;
+  const uint32_t xstage = (uint32_t)p.npad * 128;  // bytes of one X stage
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* failed = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
@@ -199,14 +223,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRS; ++i) {
       mbar_init(&raw_full[i], 1);
-      mbar_init(&raw_empty[i], kDeqWarps);
+      mbar_init(&raw_empty[i], kDeqWarps);  // both groups read every raw stage
     }
-    for (int i = 0; i < kKS; ++i) {
+    for (int i = 0; i < kMaxXS; ++i) {
       mbar_init(&x_full[i], 1);
-      mbar_init(&a_full[i], kDeqWarps);
+      mbar_init(&x_empty[i], 1);
+    }
+    for (int i = 0; i < C::KS; ++i) {
+      mbar_init(&a_full[i], 8);
       mbar_init(&empty[i], 1);
     }
-    mbar_init(acc_full, 1);
+    mbar_init(acc_full, 2);
     *failed = 0;
     fence_mbar_init();
     prefetch_tmap(&tq);
@@ -248,53 +275,73 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     // ---------------------------------------------------------------- X-stage producer
     if (lane == 0) {
       int x_issued = 0;
+      int xs = 0;         // slot of stage kb in the X ring (kb % p.xs)
+      uint32_t xph = 0;   // its phase ((kb / p.xs) & 1)
       for (int kb = 0; kb < nkb && !*failed; ++kb) {
-        const int s = kb % kKS;
-        if (kb >= kKS && !pwait(&empty[s], (uint32_t)((kb / kKS - 1) & 1), failed, p.status)) break;
-        mbar_arrive_expect_tx(&x_full[s], (uint32_t)(p.npad * 128));
-        tma_load_2d_keep(smem + C::OFF_X + s * C::X_STAGE, &tx, (kb0 + kb) * kKB, 0, &x_full[s]);
+        if (kb >= p.xs && !pwait(&x_empty[xs], xph ^ 1u, failed, p.status)) break;
+        mbar_arrive_expect_tx(&x_full[xs], xstage);
+        tma_load_2d_keep(smem + C::OFF_X + xs * xstage, &tx, (kb0 + kb) * kKB, 0, &x_full[xs]);
         x_issued = kb + 1;
+        if (++xs == p.xs) {
+          xs = 0;
+          xph ^= 1u;
+        }
       }
       if (*failed) {
-        for (int s = 0; s < kKS && s < x_issued; ++s) {
-          const int last = x_issued - 1 - ((x_issued - 1 - s) % kKS);
-          mbar_wait_bounded(&x_full[last % kKS], (uint32_t)((last / kKS) & 1), 400000000LL);
+        for (int s = 0; s < p.xs && s < x_issued; ++s) {
+          const int last = x_issued - 1 - ((x_issued - 1 - s) % p.xs);
+          mbar_wait_bounded(&x_full[last % p.xs], (uint32_t)((last / p.xs) & 1), 400000000LL);
         }
       }
     }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
+  } else if (warp == 1 || warp == kMmaWarp2) {
+    // ---------------------------------------------------------------- MMA issuers
+    // Warp 1 issues the even stages into accumulator 0 (columns 0..127), the other warp the
+    // odd ones into accumulator 1 (columns 128..255): a single issuing thread, not the
+    // tensor core, set the pace with one.
     if (lane == 0) {
+      const int m = warp == 1 ? 0 : 1;
+      const uint32_t acc = tmem + (uint32_t)(m * 128);
       const uint32_t idesc = idesc_bf16_f32(kPM, p.npad);
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % kKS;
-        const uint32_t ph = (uint32_t)((kb / kKS) & 1);
-        if (!pwait(&x_full[s], ph, failed, p.status) || !pwait(&a_full[s], ph, failed, p.status)) break;
+      int xs = m;        // slot of stage kb in the X ring (kb % p.xs; p.xs >= 2)
+      uint32_t xph = 0;  // its phase
+      for (int kb = m; kb < nkb; kb += 2) {
+        const int s = kb % C::KS;
+        if (!pwait(&x_full[xs], xph, failed, p.status) ||
+            !pwait(&a_full[s], (uint32_t)((kb / C::KS) & 1), failed, p.status))
+          break;
         tc_fence_after();
         const uint32_t a0 = sbase + s * C::A_STAGE;
-        const uint32_t b0 = sbase + C::OFF_X + s * C::X_STAGE;
+        const uint32_t b0 = sbase + C::OFF_X + xs * xstage;
 #pragma unroll
         for (int k = 0; k < kKB / 16; ++k)
-          tc_mma_f16(tmem, smem_desc_sw128(a0 + 32 * k), smem_desc_sw128(b0 + 32 * k), idesc, (kb | k) != 0);
-        tc_commit(smem_u32(&empty[s]));
+          tc_mma_f16(acc, smem_desc_sw128(a0 + 32 * k), smem_desc_sw128(b0 + 32 * k), idesc, ((kb - m) | k) != 0);
+        tc_commit(smem_u32(&empty[s]));     // the weight stage is free once these MMAs complete
+        tc_commit(smem_u32(&x_empty[xs]));  // and so is the X stage
+        xs += 2;
+        if (xs >= p.xs) {
+          xs -= p.xs;
+          xph ^= 1u;
+        }
       }
-      tc_commit(smem_u32(acc_full));  // arrives once every MMA issued above has completed
+      tc_commit(smem_u32(acc_full));  // arrives once every MMA this thread issued has completed
     }
   } else {
     // ---------------------------------------------------------------- dequantize, then drain
-    const int dt = threadIdx.x - 64;
+    const int grp = (warp - 2) >> 3;
+    const int dt = threadIdx.x - 64 - 256 * grp;
     const int row = dt & (kPM - 1);
     const int h = dt >> 7;  // which block of each 64-column stage
     const int sw = row & 7;
     const uint32_t a_row = (uint32_t)((row >> 3) * 1024 + sw * 128);
     // stages kb and kb + 1 (slots s and s + 1 of the weight ring, blocks blk and blk + 2 of
     // the raw stage)
-    for (int kb = 0; kb < nkb; kb += 2) {
+    for (int kb = 2 * grp; kb < nkb; kb += 4) {
       const int q = kb / 4, r = q % kRS;
-      if (kb % 4 == 0 && !pwait(&raw_full[r], (uint32_t)((q / kRS) & 1), failed, p.status)) break;
-      const int s = kb % kKS;
-      if (kb >= kKS && (!pwait(&empty[s], (uint32_t)((kb / kKS - 1) & 1), failed, p.status) ||
-                        !pwait(&empty[s + 1], (uint32_t)(((kb + 1) / kKS - 1) & 1), failed, p.status)))
+      if (!pwait(&raw_full[r], (uint32_t)((q / kRS) & 1), failed, p.status)) break;
+      const int s = kb % C::KS;
+      if (kb >= C::KS && (!pwait(&empty[s], (uint32_t)((kb / C::KS - 1) & 1), failed, p.status) ||
+                        !pwait(&empty[s + 1], (uint32_t)(((kb + 1) / C::KS - 1) & 1), failed, p.status)))
         break;
       const int blk = 2 * (kb & 3) + h;
       float d0, d1;
@@ -338,11 +385,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       if (lane == 0) {
         mbar_arrive(&a_full[s]);
         mbar_arrive(&a_full[s + 1]);
-        if ((kb & 3) == 2) mbar_arrive(&raw_empty[r]);
+        mbar_arrive(&raw_empty[r]);
       }
     }
-    // drain the accumulator: warp w reads tensor-memory lanes 32*(w%4) .. +31 (its rows) and
-    // every other 16-column chunk
+    // drain the accumulators and store y (all dequantize warps): warp w reads tensor-memory
+    // lanes 32*(w%4) .. +31 (its rows) and the 16-column chunks (w-2)/4 + 4k of both
+    // accumulators, and adds them (even stages + odd stages)
     const bool ok = mbar_wait_bounded(acc_full, 0u);
     if (!ok) {
       record_status(p.status, QMV_E_TIMEOUT);
@@ -350,15 +398,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     }
     tc_fence_after();
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int cg = (warp - 2) >> 2;  // which 16-column chunks: cg, cg + 4, ...
     const int trow = quarter * 32 + lane;  // row within the tile
     const int grow = row0 + trow;
+    const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
     if (p.ksplit == 1) {
       if (ok && !*failed) {
-        for (int c = half * 16; c < p.npad; c += 32) {
+        for (int c = cg * 16; c < p.npad; c += 64) {
           uint32_t v[16];
-          tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c, v);
-          tmem_ld_wait();
+          acc_ld16(tl + (uint32_t)c, v);
           if (grow < p.rows) {
 #pragma unroll
             for (int i = 0; i < 16; ++i)
@@ -367,60 +415,77 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         }
       }
     } else {
-      // this split's part (row-major: row trow's npad values contiguous); then the last CTA
-      // of the tile to arrive adds the parts in split order
-      float* part = p.parts + ((size_t)blockIdx.x * kPM + trow) * p.npad;
+      // this split's part, vector-major (the 128 sums of vector n contiguous) so that its
+      // stores here and the loads of the last CTA below are coalesced; then the last CTA of
+      // the tile to arrive adds the parts in split order
+      float* part = p.parts + (size_t)blockIdx.x * kPM * p.npad;
       if (ok && !*failed) {
-        for (int c = half * 16; c < p.npad; c += 32) {
+        for (int c = cg * 16; c < p.npad; c += 64) {
           uint32_t v[16];
-          tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c, v);
-          tmem_ld_wait();
+          acc_ld16(tl + (uint32_t)c, v);
 #pragma unroll
-          for (int i = 0; i < 16; i += 4)
-            *reinterpret_cast<uint4*>(part + c + i) = make_uint4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+          for (int i = 0; i < 16; ++i) part[(size_t)(c + i) * kPM + trow] = __uint_as_float(v[i]);
         }
       }
       epilogue_barrier();  // every part of this CTA is written before the release below
-      if (dt == 0) {
+      if (threadIdx.x == 64) {
         const unsigned before = atomic_add_acq_rel_u32(p.counters + tile, 1u);
         const bool last = before + 1 == (unsigned)p.ksplit;
         if (last) p.counters[tile] = 0u;  // every part has arrived: ready for the next launch
         *last_flag = last ? 1 : 0;
       }
       epilogue_barrier();  // the acquire above is ordered before the loads below
-      if (*last_flag && !*failed && grow < p.rows) {
-        // this thread's columns: chunks half*16 + 32k (k < 4), 16 values each; every split's
-        // values of up to 4 chunks are loaded at once (16-byte loads) and added in split order
-        const float* rpart = p.parts + ((size_t)tile * p.ksplit * kPM + trow) * p.npad;
-        const size_t sstride = (size_t)kPM * p.npad;  // floats between splits of the tile
-        float sum[4][16];
+      if (*last_flag && !*failed) {
+        // units of 4 consecutive rows of one vector; each thread takes kUnits of them at a
+        // time and loads every split's values (4 splits at a time) before adding them in order
+        constexpr int kUnits = 2;
+        constexpr int kEpi = 32 * kDeqWarps;  // threads
+        const float* tpart = p.parts + (size_t)tile * p.ksplit * kPM * p.npad;
+        const size_t sstride = (size_t)kPM * p.npad;  // floats between the splits of the tile
+        const int units = p.npad * (kPM / 4);
+        const int et = threadIdx.x - 64;
+        for (int u0 = et; u0 < units; u0 += kUnits * kEpi) {
+          float4 acc[kUnits];
+          for (int sp0 = 0; sp0 < p.ksplit; sp0 += 4) {
+            float4 q[kUnits][4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
+            for (int j = 0; j < kUnits; ++j)
 #pragma unroll
-          for (int i = 0; i < 16; ++i) sum[k][i] = 0.f;
-        for (int sp = 0; sp < p.ksplit; ++sp) {
-          const float* src = rpart + sp * sstride;
+              for (int e = 0; e < 4; ++e)
+                if (u0 + j * kEpi < units && sp0 + e < p.ksplit)
+                  q[j][e] = __ldcg(reinterpret_cast<const float4*>(tpart + (sp0 + e) * sstride) + u0 + j * kEpi);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int c = half * 16 + 32 * k;
-            if (c < p.npad) {
+            for (int j = 0; j < kUnits; ++j)
 #pragma unroll
-              for (int i = 0; i < 16; i += 4) {
-                const float4 q = __ldcg(reinterpret_cast<const float4*>(src + c + i));
-                sum[k][i] += q.x;
-                sum[k][i + 1] += q.y;
-                sum[k][i + 2] += q.z;
-                sum[k][i + 3] += q.w;
+              for (int e = 0; e < 4; ++e)
+                if (u0 + j * kEpi < units && sp0 + e < p.ksplit) {
+                  if (sp0 + e == 0) {
+                    acc[j] = q[j][e];
+                  } else {
+                    acc[j].x += q[j][e].x;
+                    acc[j].y += q[j][e].y;
+                    acc[j].z += q[j][e].z;
+                    acc[j].w += q[j][e].w;
+                  }
+                }
+          }
+#pragma unroll
+          for (int j = 0; j < kUnits; ++j) {
+            const int u = u0 + j * kEpi;
+            const int n = u / (kPM / 4);
+            const int r = row0 + (u % (kPM / 4)) * 4;
+            if (u < units && n < p.batch) {
+              float* dst = p.y + (size_t)n * p.rows + r;
+              if (r + 3 < p.rows && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {  // y is 4-byte aligned
+                *reinterpret_cast<float4*>(dst) = acc[j];
+              } else {
+                if (r < p.rows) dst[0] = acc[j].x;
+                if (r + 1 < p.rows) dst[1] = acc[j].y;
+                if (r + 2 < p.rows) dst[2] = acc[j].z;
+                if (r + 3 < p.rows) dst[3] = acc[j].w;
               }
             }
           }
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int c = half * 16 + 32 * k;
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (c + i < p.batch) p.y[(size_t)(c + i) * p.rows + grow] = sum[k][i];
         }
       }
     }
@@ -462,7 +527,7 @@ static cudaError_t launch_prefill_typed(const MatrixRef& m, const void* x, float
   static bool ready[64] = {};
   if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
   if (!ready[dev.device]) {
-    const cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    const cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dev.smem_optin);
     if (err != cudaSuccess) return err;
     ready[dev.device] = true;
   }
@@ -473,6 +538,10 @@ static cudaError_t launch_prefill_typed(const MatrixRef& m, const void* x, float
   p.batch = batch;
   p.npad = (batch + 15) / 16 * 16;
   p.status = dev.status;
+  // as many X stages as the shared memory left by the other rings holds
+  p.xs = ((int)dev.smem_optin - C::smem_bytes(0, p.npad)) / (p.npad * 128);
+  if (p.xs > kMaxXS) p.xs = kMaxXS;
+  if (p.xs < 2) return cudaErrorInvalidConfiguration;
   p.ksplit = prefill_ksplit(m, p.npad, dev, ws);
   p.counters = p.ksplit > 1 ? ws->counters : nullptr;
   p.parts = p.ksplit > 1 ? ws->partials : nullptr;
@@ -489,7 +558,7 @@ static cudaError_t launch_prefill_typed(const MatrixRef& m, const void* x, float
                        (uint64_t)m.cols * 2, kKB, p.npad, CU_TENSOR_MAP_SWIZZLE_128B);
   if (err != cudaSuccess) return err;
   const int grid = (int)((m.rows + kPM - 1) / kPM) * p.ksplit;
-  kern<<<grid, kThreads, C::SMEM, stream>>>(tq, td, tx, p);
+  kern<<<grid, kThreads, C::smem_bytes(p.xs, p.npad), stream>>>(tq, td, tx, p);
   return cudaGetLastError();
 }
 

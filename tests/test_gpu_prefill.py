@@ -183,3 +183,22 @@ def test_prefill_split_tiles_exact_pow2(qmv):
     x = inputs.make_int_x(batch, cols, True, seed=35)
     y_ref, _ = oracle.matvec(W, 2, 1, rows, cols, x)
     assert np.array_equal(run(qmv, m2, x).astype(np.float64), y_ref)
+
+
+@pytest.mark.parametrize("offset,batch", [(1, 48), (2, 40), (4, 40)])
+def test_prefill_split_tiles_unaligned_y_and_guards(qmv, offset, batch):
+    # split tiles (2 row tiles over 16 raw stages) whose last CTA stores 4 consecutive rows
+    # of y at a time: y only 4-byte aligned (offset 1 or 2 floats), or 16-byte aligned with
+    # a batch that is not a multiple of 16; nothing outside y is written
+    import torch
+    rows, cols = 256, 4096
+    m = inputs.make_matrix(2, 1, rows, cols, seed=40 + offset)
+    x = inputs.make_x(batch, cols, True, seed=41 + offset)
+    y_ref, absref = oracle.matvec(m.W, 2, 1, rows, cols, x)
+    buf = torch.full((batch * rows + 64,), 4321.0, device="cuda")
+    y = buf[offset:offset + batch * rows].view(batch, rows)
+    qmv.matvec(2, 1, rows, cols, dev_u8(m.W), dev_x(x), y)
+    torch.cuda.synchronize()
+    b = buf.cpu().numpy()
+    assert np.all(b[:offset] == 4321.0) and np.all(b[offset + batch * rows:] == 4321.0)
+    check_product(b[offset:offset + batch * rows].reshape(batch, rows), y_ref, absref, TOL, f"unaligned y {offset}")
