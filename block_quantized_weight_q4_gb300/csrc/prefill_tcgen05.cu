@@ -62,22 +62,21 @@ struct PCfg {
   static constexpr int DROW = (kRawK / 32) * ESZ;                        // scale bytes per row per raw stage
   static constexpr int D_RAW = kPM * DROW;
   static constexpr int A_STAGE = kPM * 128;                              // 128 rows x 64 bf16
-  // ring depth of the bf16-weight stages: deep enough that each dequantize group can fill one
-  // pair of stages while the MMAs of its previous pair are still in flight, within the
-  // shared memory that the raw ring and at least two 128-vector X stages leave
-  static constexpr int KS = (WT == QMV_Q4_0) ? 8 : 6;
-  static_assert(KS % 2 == 0, "the dequantize warps fill the weight ring two stages at a time");
-  static constexpr int OFF_Q = KS * A_STAGE;
+  // deepest ring of bf16-weight stages: each dequantize group can then fill one pair of
+  // stages while the MMAs of its previous pair are in flight.  A launch takes the deepest
+  // (even) depth up to this that leaves room for four X stages of its batch.
+  static constexpr int MAXKS = (WT == QMV_Q4_0) ? 8 : 6;
+  static constexpr int OFF_Q = 0;  // raw ring, then scales, barriers, flags; then the bf16-weight and X rings
   static constexpr int OFF_D = OFF_Q + kRS * Q_RAW;
   static constexpr int OFF_BAR = OFF_D + kRS * D_RAW;
-  // barriers: raw_full[kRS], raw_empty[kRS], a_full[KS], empty[KS], x_full[kMaxXS],
+  // barriers: raw_full[kRS], raw_empty[kRS], a_full[MAXKS], empty[MAXKS], x_full[kMaxXS],
   // x_empty[kMaxXS], acc_full
-  static constexpr int NBARS = 2 * kRS + 2 * KS + 2 * kMaxXS + 1;
+  static constexpr int NBARS = 2 * kRS + 2 * MAXKS + 2 * kMaxXS + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;  // tensor-memory base, failure and last flags
-  static constexpr int OFF_X = (OFF_MISC + 16 + 1023) / 1024 * 1024;  // X ring (1024-aligned stages)
-  // shared memory of a launch with an X ring of xs stages of npad vectors (npad x 128 bytes)
-  static constexpr int smem_bytes(int xs, int npad) { return 1024 + OFF_X + xs * npad * 128; }
-  static_assert(smem_bytes(2, kMaxN) <= 227 * 1024, "shared memory of one CTA");
+  static constexpr int OFF_A = (OFF_MISC + 16 + 1023) / 1024 * 1024;  // weight ring (1024-aligned stages)
+  // shared memory of a launch with ks weight stages and xs X stages of npad vectors
+  static constexpr int smem_bytes(int ks, int xs, int npad) { return 1024 + OFF_A + ks * A_STAGE + xs * npad * 128; }
+  static_assert(smem_bytes(4, 2, kMaxN) <= 227 * 1024, "shared memory of one CTA");
 };
 
 struct PParams {
@@ -87,7 +86,8 @@ struct PParams {
   int batch;  // vectors in this pass (1..128)
   int npad;   // batch rounded up to 16
   int* status;
-  int xs;              // X ring depth (2..kMaxXS)
+  int ks;              // weight ring depth (4..MAXKS, even)
+  int xs;              // X ring depth (2..kMaxXS, even)
   int ksplit;          // column ranges per tile (1: no workspace used)
   unsigned* counters;  // per tile arrival counters, zero between launches
   float* parts;        // per (tile, split): npad x 128 partial sums, vector-major
@@ -201,11 +201,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   uint64_t* raw_full = bars;
   uint64_t* raw_empty = bars + kRS;
   uint64_t* a_full = bars + 2 * kRS;
-  uint64_t* empty = a_full + C::KS;
-  uint64_t* x_full = empty + C::KS;
+  uint64_t* empty = a_full + C::MAXKS;
+  uint64_t* x_full = empty + C::MAXKS;
   uint64_t* x_empty = x_full + kMaxXS;
   uint64_t* acc_full = x_empty + kMaxXS;
   const uint32_t xstage = (uint32_t)p.npad * 128;  // bytes of one X stage
+  const uint32_t off_x = C::OFF_A + p.ks * C::A_STAGE;  // the X ring follows the weight ring
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* failed = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
@@ -229,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       mbar_init(&x_full[i], 1);
       mbar_init(&x_empty[i], 1);
     }
-    for (int i = 0; i < C::KS; ++i) {
+    for (int i = 0; i < C::MAXKS; ++i) {
       mbar_init(&a_full[i], 8);
       mbar_init(&empty[i], 1);
     }
@@ -280,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       for (int kb = 0; kb < nkb && !*failed; ++kb) {
         if (kb >= p.xs && !pwait(&x_empty[xs], xph ^ 1u, failed, p.status)) break;
         mbar_arrive_expect_tx(&x_full[xs], xstage);
-        tma_load_2d_keep(smem + C::OFF_X + xs * xstage, &tx, (kb0 + kb) * kKB, 0, &x_full[xs]);
+        tma_load_2d_keep(smem + off_x + xs * xstage, &tx, (kb0 + kb) * kKB, 0, &x_full[xs]);
         x_issued = kb + 1;
         if (++xs == p.xs) {
           xs = 0;
@@ -303,16 +304,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const int m = warp == 1 ? 0 : 1;
       const uint32_t acc = tmem + (uint32_t)(m * 128);
       const uint32_t idesc = idesc_bf16_f32(kPM, p.npad);
-      int xs = m;        // slot of stage kb in the X ring (kb % p.xs; p.xs >= 2)
+      int xs = m;        // slot of stage kb in the X ring (kb % p.xs; p.xs even)
       uint32_t xph = 0;  // its phase
+      int s = m;         // slot of stage kb in the weight ring (kb % p.ks; p.ks even)
+      uint32_t aph = 0;  // its phase
       for (int kb = m; kb < nkb; kb += 2) {
-        const int s = kb % C::KS;
-        if (!pwait(&x_full[xs], xph, failed, p.status) ||
-            !pwait(&a_full[s], (uint32_t)((kb / C::KS) & 1), failed, p.status))
-          break;
+        if (!pwait(&x_full[xs], xph, failed, p.status) || !pwait(&a_full[s], aph, failed, p.status)) break;
         tc_fence_after();
-        const uint32_t a0 = sbase + s * C::A_STAGE;
-        const uint32_t b0 = sbase + C::OFF_X + xs * xstage;
+        const uint32_t a0 = sbase + C::OFF_A + s * C::A_STAGE;
+        const uint32_t b0 = sbase + off_x + xs * xstage;
 #pragma unroll
         for (int k = 0; k < kKB / 16; ++k)
           tc_mma_f16(acc, smem_desc_sw128(a0 + 32 * k), smem_desc_sw128(b0 + 32 * k), idesc, ((kb - m) | k) != 0);
@@ -322,6 +322,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         if (xs >= p.xs) {
           xs -= p.xs;
           xph ^= 1u;
+        }
+        s += 2;
+        if (s >= p.ks) {
+          s -= p.ks;
+          aph ^= 1u;
         }
       }
       tc_commit(smem_u32(acc_full));  // arrives once every MMA this thread issued has completed
@@ -336,12 +341,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const uint32_t a_row = (uint32_t)((row >> 3) * 1024 + sw * 128);
     // stages kb and kb + 1 (slots s and s + 1 of the weight ring, blocks blk and blk + 2 of
     // the raw stage)
+    int s = 2 * grp;   // slot of stage kb in the weight ring (kb % p.ks; stage kb + 1 takes s + 1)
+    uint32_t ph = 0;   // its phase
     for (int kb = 2 * grp; kb < nkb; kb += 4) {
       const int q = kb / 4, r = q % kRS;
       if (!pwait(&raw_full[r], (uint32_t)((q / kRS) & 1), failed, p.status)) break;
-      const int s = kb % C::KS;
-      if (kb >= C::KS && (!pwait(&empty[s], (uint32_t)((kb / C::KS - 1) & 1), failed, p.status) ||
-                        !pwait(&empty[s + 1], (uint32_t)(((kb + 1) / C::KS - 1) & 1), failed, p.status)))
+      if (kb >= p.ks && (!pwait(&empty[s], ph ^ 1u, failed, p.status) || !pwait(&empty[s + 1], ph ^ 1u, failed, p.status)))
         break;
       const int blk = 2 * (kb & 3) + h;
       float d0, d1;
@@ -373,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         q8_block_to_bf16(w0, d0, out0);
         q8_block_to_bf16(w1, d1, out1);
       }
-      const uint32_t arow = sbase + s * C::A_STAGE + a_row;
+      const uint32_t arow = sbase + C::OFF_A + s * C::A_STAGE + a_row;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         sts128(arow + (((4 * h + j) ^ sw) << 4), out0[4 * j], out0[4 * j + 1], out0[4 * j + 2], out0[4 * j + 3]);
@@ -386,6 +391,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         mbar_arrive(&a_full[s]);
         mbar_arrive(&a_full[s + 1]);
         mbar_arrive(&raw_empty[r]);
+      }
+      s += 4;
+      if (s >= p.ks) {
+        s -= p.ks;
+        ph ^= 1u;
       }
     }
     // drain the accumulators and store y (all dequantize warps): warp w reads tensor-memory
@@ -538,9 +548,22 @@ static cudaError_t launch_prefill_typed(const MatrixRef& m, const void* x, float
   p.batch = batch;
   p.npad = (batch + 15) / 16 * 16;
   p.status = dev.status;
-  // as many X stages as the shared memory left by the other rings holds
-  p.xs = ((int)dev.smem_optin - C::smem_bytes(0, p.npad)) / (p.npad * 128);
-  if (p.xs > kMaxXS) p.xs = kMaxXS;
+  // ring depths: X stages are taken in even numbers (the two MMA warps take alternate stages,
+  // so with an even depth each slot always serves the same warp and no warp can wait for a
+  // phase two ahead of the slot's barrier, which a parity wait would take as done); the
+  // weight ring is the deepest (even) one that leaves room for four X stages, else 4
+  const auto x_depth = [&](int ks) {
+    int xs = ((int)dev.smem_optin - C::smem_bytes(ks, 0, p.npad)) / (p.npad * 128);
+    if (xs > kMaxXS) xs = kMaxXS;
+    return xs & ~1;
+  };
+  p.ks = 4;
+  for (int ks = C::MAXKS; ks > 4; ks -= 2)
+    if (x_depth(ks) >= 4) {
+      p.ks = ks;
+      break;
+    }
+  p.xs = x_depth(p.ks);
   if (p.xs < 2) return cudaErrorInvalidConfiguration;
   p.ksplit = prefill_ksplit(m, p.npad, dev, ws);
   p.counters = p.ksplit > 1 ? ws->counters : nullptr;
@@ -558,7 +581,7 @@ static cudaError_t launch_prefill_typed(const MatrixRef& m, const void* x, float
                        (uint64_t)m.cols * 2, kKB, p.npad, CU_TENSOR_MAP_SWIZZLE_128B);
   if (err != cudaSuccess) return err;
   const int grid = (int)((m.rows + kPM - 1) / kPM) * p.ksplit;
-  kern<<<grid, kThreads, C::smem_bytes(p.xs, p.npad), stream>>>(tq, td, tx, p);
+  kern<<<grid, kThreads, C::smem_bytes(p.ks, p.xs, p.npad), stream>>>(tq, td, tx, p);
   return cudaGetLastError();
 }
 
