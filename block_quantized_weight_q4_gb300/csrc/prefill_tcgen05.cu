@@ -16,20 +16,23 @@
 //   warp 18    TMA producer of the X stages (N x 64 bf16, 128-byte swizzle); a stage's slot is
 //              free once the MMAs that read it complete, and the weight loads must not wait
 //              for that, hence a producer of their own.
-//   warp 1     allocates tensor memory (128 lanes x 256 f32 columns: two accumulators).
+//   warp 1     allocates tensor memory (128 lanes x 512 columns: two f32 accumulators of 128
+//              columns, then a ring of 8 bf16-weight stages of 32 columns).
 //   warps 1, 19  lane 0 issues, per 64-column stage (warp 1 the even ones into accumulator 0,
 //              warp 19 the odd ones into accumulator 1), four tcgen05.mma (M 128, N, K 16,
-//              bf16 in, f32 accumulate) from the bf16 weight stage and the X stage, then
-//              commits to the stage's "empty" barrier; after its last stage, to
-//              "accumulator full".  One issuing thread could not keep up: each instruction
-//              costs it tens of cycles while the tensor core finishes a stage in fewer.
+//              bf16 in, f32 accumulate), A from the weight stage in tensor memory and B from
+//              the X stage in shared memory, then commits to the stage's "empty" barriers;
+//              after its last stage, to "accumulator full".  One issuing thread could not
+//              keep up: each instruction costs it tens of cycles while the tensor core
+//              finishes a stage in fewer.
 //   warps 2-17 dequantize, in two groups of eight (warps 2-9 and 10-17) that take turns
 //              with the pairs of 64-column stages: thread (row, half) of a group turns one
-//              32-weight block of its row per stage into 32 bf16 weights written in the MMA's
-//              K-major 128-byte-swizzled layout (one proxy fence and one pass of waits per
-//              pair of stages: the per-stage synchronisation, not the arithmetic, set the
-//              pace when every stage had its own; two groups keep four warps per scheduler
-//              busy).  Then they read the accumulators from tensor memory (each warp its
+//              32-weight block of its row per stage into 32 bf16 weights and stores them
+//              (tcgen05.st) to its row's tensor-memory lane, where the MMA reads them, so the
+//              weights cross shared memory only in their quantized form.  One pass of waits
+//              per pair of stages (per-stage synchronisation, not the arithmetic, set the
+//              pace when every stage had its own); two groups keep four warps per scheduler
+//              busy.  Then they read the accumulators from tensor memory (each warp its
 //              32-lane quarter and a quarter of the columns) and store y, or, for a split
 //              tile, the CTA's part (vector-major) for the last CTA to add.
 // Every wait is bounded; a wait that runs out records QMV_E_TIMEOUT and the roles unwind.
@@ -45,13 +48,17 @@ constexpr int kPM = 128;      // rows of W per CTA tile = MMA M = tensor-memory 
 constexpr int kKB = 64;       // columns per MMA stage: one 128-byte swizzle span of bf16
 constexpr int kRawK = 256;    // columns per raw (quantized) stage
 constexpr int kMaxXS = 16;    // deepest X ring (its depth is set per launch by the batch)
-constexpr int kRS = 2;        // ring depth of the raw stages (deeper measured no faster)
+constexpr int kRS = 4;        // ring depth of the raw stages
 constexpr int kDeqWarps = 16;  // dequantize (two groups of 8); the first group drains the accumulators
 constexpr int kXWarp = 2 + kDeqWarps;  // the X-stage producer
 constexpr int kMmaWarp2 = 3 + kDeqWarps;  // the second MMA issuer (odd stages)
 constexpr int kThreads = 32 * (4 + kDeqWarps);
 constexpr int kMaxN = 128;    // activation vectors per pass
-constexpr int kTmemCols = 256;  // two accumulators of 128 columns (even and odd stages)
+constexpr int kKS = 8;        // ring depth of the bf16-weight stages (in tensor memory)
+constexpr int kAccCol = 0;    // accumulators: columns 0..127 (even stages), 128..255 (odd stages)
+constexpr int kACol = 256;    // weight ring: stage s at columns 256 + 32 s (128 lanes x 64 bf16)
+constexpr int kTmemCols = 512;
+static_assert(kACol + 32 * kKS <= kTmemCols, "tensor memory");
 
 template <int WT, bool F16>
 struct PCfg {
@@ -61,22 +68,17 @@ struct PCfg {
   static constexpr int ESZ = F16 ? 2 : 4;
   static constexpr int DROW = (kRawK / 32) * ESZ;                        // scale bytes per row per raw stage
   static constexpr int D_RAW = kPM * DROW;
-  static constexpr int A_STAGE = kPM * 128;                              // 128 rows x 64 bf16
-  // deepest ring of bf16-weight stages: each dequantize group can then fill one pair of
-  // stages while the MMAs of its previous pair are in flight.  A launch takes the deepest
-  // (even) depth up to this that leaves room for four X stages of its batch.
-  static constexpr int MAXKS = (WT == QMV_Q4_0) ? 8 : 6;
-  static constexpr int OFF_Q = 0;  // raw ring, then scales, barriers, flags; then the bf16-weight and X rings
+  static constexpr int OFF_Q = 0;  // raw ring, then scales, barriers, flags, then the X ring
   static constexpr int OFF_D = OFF_Q + kRS * Q_RAW;
   static constexpr int OFF_BAR = OFF_D + kRS * D_RAW;
-  // barriers: raw_full[kRS], raw_empty[kRS], a_full[MAXKS], empty[MAXKS], x_full[kMaxXS],
+  // barriers: raw_full[kRS], raw_empty[kRS], a_full[kKS], empty[kKS], x_full[kMaxXS],
   // x_empty[kMaxXS], acc_full
-  static constexpr int NBARS = 2 * kRS + 2 * MAXKS + 2 * kMaxXS + 1;
+  static constexpr int NBARS = 2 * kRS + 2 * kKS + 2 * kMaxXS + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;  // tensor-memory base, failure and last flags
-  static constexpr int OFF_A = (OFF_MISC + 16 + 1023) / 1024 * 1024;  // weight ring (1024-aligned stages)
-  // shared memory of a launch with ks weight stages and xs X stages of npad vectors
-  static constexpr int smem_bytes(int ks, int xs, int npad) { return 1024 + OFF_A + ks * A_STAGE + xs * npad * 128; }
-  static_assert(smem_bytes(4, 2, kMaxN) <= 227 * 1024, "shared memory of one CTA");
+  static constexpr int OFF_X = (OFF_MISC + 16 + 1023) / 1024 * 1024;  // X ring (1024-aligned stages)
+  // shared memory of a launch with xs X stages of npad vectors
+  static constexpr int smem_bytes(int xs, int npad) { return 1024 + OFF_X + xs * npad * 128; }
+  static_assert(smem_bytes(4, kMaxN) <= 227 * 1024, "shared memory of one CTA");
 };
 
 struct PParams {
@@ -86,7 +88,6 @@ struct PParams {
   int batch;  // vectors in this pass (1..128)
   int npad;   // batch rounded up to 16
   int* status;
-  int ks;              // weight ring depth (4..MAXKS, even)
   int xs;              // X ring depth (2..kMaxXS, even)
   int ksplit;          // column ranges per tile (1: no workspace used)
   unsigned* counters;  // per tile arrival counters, zero between launches
@@ -136,6 +137,51 @@ __device__ __forceinline__ void q4_block_to_bf16(const uint32_t (&w)[4], float d
     out[2 * i + 1] = scale_half_levels(lo23, d);      // 4i+2, 4i+3
     out[8 + 2 * i] = scale_half_levels(hi01, d);      // 16+4i, 16+4i+1
     out[8 + 2 * i + 1] = scale_half_levels(hi23, d);  // 16+4i+2, 16+4i+3
+  }
+}
+
+// An IEEE-half scale d (as float32) as two bfloat16 parts, each in both halves of a word:
+// hi = RN_bf16(d) and lo = d - hi.  d has at most 11 significant bits, so lo has at most 3
+// and is itself a bfloat16 (exact).  A scale that is not finite keeps lo = 0.
+__device__ __forceinline__ void split_half_scale(float d, uint32_t& hi2, uint32_t& lo2) {
+  hi2 = pack_bf16x2(d, d);
+  const float lo = isfinite(d) ? d - __uint_as_float(hi2 << 16) : 0.0f;
+  lo2 = pack_bf16x2(lo, lo);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_mul_rn(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_fma_rn(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+
+// A bfloat16 level pair (exact integers, |level| <= 8) times the split scale: level * lo has
+// at most 3 + 3 significant bits, so it is exact in bfloat16, and the fused multiply-add
+// rounds level * hi + level * lo = level * d once: RN_bf16(level * d), which equals
+// RN_bf16(fl32(level * d)) since level * d (at most 4 + 11 bits) is exact in float32.
+__device__ __forceinline__ uint32_t scale_bf16_levels(uint32_t l2, uint32_t hi2, uint32_t lo2) {
+  return bf16x2_fma_rn(l2, hi2, bf16x2_mul_rn(l2, lo2));
+}
+
+// One Q4_0 block with an IEEE-half scale (split by split_half_scale) to the same 32 bfloat16
+// weights as q4_block_to_bf16, from exact bfloat16 levels (q4_word_to_bf16_levels) in two
+// packed bfloat16 operations per pair instead of two widenings, a multiply and a narrowing.
+__device__ __forceinline__ void q4_block_to_bf16_split(const uint32_t (&w)[4], uint32_t hi2, uint32_t lo2,
+                                                       uint32_t (&out)[16]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t lo01, lo23, hi01, hi23;
+    q4_word_to_bf16_levels(w[i], lo01, lo23, hi01, hi23);
+    out[2 * i] = scale_bf16_levels(lo01, hi2, lo2);
+    out[2 * i + 1] = scale_bf16_levels(lo23, hi2, lo2);
+    out[8 + 2 * i] = scale_bf16_levels(hi01, hi2, lo2);
+    out[8 + 2 * i + 1] = scale_bf16_levels(hi23, hi2, lo2);
   }
 }
 
@@ -201,12 +247,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   uint64_t* raw_full = bars;
   uint64_t* raw_empty = bars + kRS;
   uint64_t* a_full = bars + 2 * kRS;
-  uint64_t* empty = a_full + C::MAXKS;
-  uint64_t* x_full = empty + C::MAXKS;
+  uint64_t* empty = a_full + kKS;
+  uint64_t* x_full = empty + kKS;
   uint64_t* x_empty = x_full + kMaxXS;
   uint64_t* acc_full = x_empty + kMaxXS;
   const uint32_t xstage = (uint32_t)p.npad * 128;  // bytes of one X stage
-  const uint32_t off_x = C::OFF_A + p.ks * C::A_STAGE;  // the X ring follows the weight ring
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* failed = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
@@ -230,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       mbar_init(&x_full[i], 1);
       mbar_init(&x_empty[i], 1);
     }
-    for (int i = 0; i < C::MAXKS; ++i) {
+    for (int i = 0; i < kKS; ++i) {
       mbar_init(&a_full[i], 8);
       mbar_init(&empty[i], 1);
     }
@@ -281,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       for (int kb = 0; kb < nkb && !*failed; ++kb) {
         if (kb >= p.xs && !pwait(&x_empty[xs], xph ^ 1u, failed, p.status)) break;
         mbar_arrive_expect_tx(&x_full[xs], xstage);
-        tma_load_2d_keep(smem + off_x + xs * xstage, &tx, (kb0 + kb) * kKB, 0, &x_full[xs]);
+        tma_load_2d_keep(smem + C::OFF_X + xs * xstage, &tx, (kb0 + kb) * kKB, 0, &x_full[xs]);
         x_issued = kb + 1;
         if (++xs == p.xs) {
           xs = 0;
@@ -302,20 +347,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     // tensor core, set the pace with one.
     if (lane == 0) {
       const int m = warp == 1 ? 0 : 1;
-      const uint32_t acc = tmem + (uint32_t)(m * 128);
+      const uint32_t acc = tmem + (uint32_t)(kAccCol + m * 128);
       const uint32_t idesc = idesc_bf16_f32(kPM, p.npad);
       int xs = m;        // slot of stage kb in the X ring (kb % p.xs; p.xs even)
       uint32_t xph = 0;  // its phase
-      int s = m;         // slot of stage kb in the weight ring (kb % p.ks; p.ks even)
+      int s = m;         // slot of stage kb in the weight ring (kb % kKS)
       uint32_t aph = 0;  // its phase
       for (int kb = m; kb < nkb; kb += 2) {
         if (!pwait(&x_full[xs], xph, failed, p.status) || !pwait(&a_full[s], aph, failed, p.status)) break;
         tc_fence_after();
-        const uint32_t a0 = sbase + C::OFF_A + s * C::A_STAGE;
-        const uint32_t b0 = sbase + off_x + xs * xstage;
+        const uint32_t a0 = tmem + (uint32_t)(kACol + 32 * s);  // A: 128 lanes x 32 columns (two bf16 each)
+        const uint32_t b0 = sbase + C::OFF_X + xs * xstage;
 #pragma unroll
         for (int k = 0; k < kKB / 16; ++k)
-          tc_mma_f16(acc, smem_desc_sw128(a0 + 32 * k), smem_desc_sw128(b0 + 32 * k), idesc, ((kb - m) | k) != 0);
+          tc_mma_f16_ts(acc, a0 + 8 * k, smem_desc_sw128(b0 + 32 * k), idesc, ((kb - m) | k) != 0);
         tc_commit(smem_u32(&empty[s]));     // the weight stage is free once these MMAs complete
         tc_commit(smem_u32(&x_empty[xs]));  // and so is the X stage
         xs += 2;
@@ -324,8 +369,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           xph ^= 1u;
         }
         s += 2;
-        if (s >= p.ks) {
-          s -= p.ks;
+        if (s >= kKS) {
+          s -= kKS;
           aph ^= 1u;
         }
       }
@@ -333,21 +378,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     }
   } else {
     // ---------------------------------------------------------------- dequantize, then drain
+    // thread (row, h): a warp may write only its own 32-lane quarter of tensor memory, so
+    // the row is 32 (warp % 4) + lane; the group's first four warps take block 0 of each
+    // stage, the others block 1
     const int grp = (warp - 2) >> 3;
     const int dt = threadIdx.x - 64 - 256 * grp;
-    const int row = dt & (kPM - 1);
-    const int h = dt >> 7;  // which block of each 64-column stage
+    const int row = 32 * (warp & 3) + lane;
+    const int h = (dt >> 7) & 1;  // which block of each 64-column stage
     const int sw = row & 7;
-    const uint32_t a_row = (uint32_t)((row >> 3) * 1024 + sw * 128);
+    const uint32_t a_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(kACol + 16 * h);
     // stages kb and kb + 1 (slots s and s + 1 of the weight ring, blocks blk and blk + 2 of
     // the raw stage)
-    int s = 2 * grp;   // slot of stage kb in the weight ring (kb % p.ks; stage kb + 1 takes s + 1)
+    int s = 2 * grp;   // slot of stage kb in the weight ring (kb % kKS; stage kb + 1 takes s + 1)
     uint32_t ph = 0;   // its phase
     for (int kb = 2 * grp; kb < nkb; kb += 4) {
       const int q = kb / 4, r = q % kRS;
-      if (!pwait(&raw_full[r], (uint32_t)((q / kRS) & 1), failed, p.status)) break;
-      if (kb >= p.ks && (!pwait(&empty[s], ph ^ 1u, failed, p.status) || !pwait(&empty[s + 1], ph ^ 1u, failed, p.status)))
-        break;
+      const bool ok = pwait(&raw_full[r], (uint32_t)((q / kRS) & 1), failed, p.status) &&
+                      (kb < kKS || (pwait(&empty[s], ph ^ 1u, failed, p.status) &&
+                                    pwait(&empty[s + 1], ph ^ 1u, failed, p.status)));
+      // the tensor-memory stores below are warp-wide: the warp leaves together
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();  // the MMAs that read these stages' tensor memory are complete
       const int blk = 2 * (kb & 3) + h;
       float d0, d1;
       if (F16) {
@@ -365,8 +416,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         uint32_t w0[4], w1[4];
         lds128(qrow + ((blk ^ sw) << 4), w0[0], w0[1], w0[2], w0[3]);
         lds128(qrow + (((blk + 2) ^ sw) << 4), w1[0], w1[1], w1[2], w1[3]);
-        q4_block_to_bf16(w0, d0, out0);
-        q4_block_to_bf16(w1, d1, out1);
+        if (F16) {
+          uint32_t h0, l0, h1, l1;
+          split_half_scale(d0, h0, l0);
+          split_half_scale(d1, h1, l1);
+          q4_block_to_bf16_split(w0, h0, l0, out0);
+          q4_block_to_bf16_split(w1, h1, l1, out1);
+        } else {
+          q4_block_to_bf16(w0, d0, out0);
+          q4_block_to_bf16(w1, d1, out1);
+        }
       } else {
         uint32_t w0[8], w1[8];
         const uint32_t box = qrow + (blk >> 2) * (kPM * 128);
@@ -378,14 +437,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         q8_block_to_bf16(w0, d0, out0);
         q8_block_to_bf16(w1, d1, out1);
       }
-      const uint32_t arow = sbase + C::OFF_A + s * C::A_STAGE + a_row;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        sts128(arow + (((4 * h + j) ^ sw) << 4), out0[4 * j], out0[4 * j + 1], out0[4 * j + 2], out0[4 * j + 3]);
-        sts128(arow + C::A_STAGE + (((4 * h + j) ^ sw) << 4), out1[4 * j], out1[4 * j + 1], out1[4 * j + 2],
-               out1[4 * j + 3]);
-      }
-      fence_proxy_async_smem();  // the tensor core reads these stores through the async proxy
+      // the block's 32 bf16 weights (pairs in element order) into 16 columns of this row's lane
+      tmem_st16(a_lane + (uint32_t)(32 * s), out0);
+      tmem_st16(a_lane + (uint32_t)(32 * (s + 1)), out1);
+      tmem_st_wait();
+      tc_fence_before();  // the stores are complete before the arrivals below
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&a_full[s]);
@@ -393,8 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         mbar_arrive(&raw_empty[r]);
       }
       s += 4;
-      if (s >= p.ks) {
-        s -= p.ks;
+      if (s >= kKS) {
+        s -= kKS;
         ph ^= 1u;
       }
     }
@@ -548,22 +604,13 @@ static cudaError_t launch_prefill_typed(const MatrixRef& m, const void* x, float
   p.batch = batch;
   p.npad = (batch + 15) / 16 * 16;
   p.status = dev.status;
-  // ring depths: X stages are taken in even numbers (the two MMA warps take alternate stages,
-  // so with an even depth each slot always serves the same warp and no warp can wait for a
-  // phase two ahead of the slot's barrier, which a parity wait would take as done); the
-  // weight ring is the deepest (even) one that leaves room for four X stages, else 4
-  const auto x_depth = [&](int ks) {
-    int xs = ((int)dev.smem_optin - C::smem_bytes(ks, 0, p.npad)) / (p.npad * 128);
-    if (xs > kMaxXS) xs = kMaxXS;
-    return xs & ~1;
-  };
-  p.ks = 4;
-  for (int ks = C::MAXKS; ks > 4; ks -= 2)
-    if (x_depth(ks) >= 4) {
-      p.ks = ks;
-      break;
-    }
-  p.xs = x_depth(p.ks);
+  // X ring: as many stages as the shared memory left by the raw ring holds, in an even
+  // number (the two MMA warps take alternate stages, so with an even depth each slot always
+  // serves the same warp and no warp can wait for a phase two ahead of the slot's barrier,
+  // which a parity wait would take as done)
+  p.xs = ((int)dev.smem_optin - C::smem_bytes(0, p.npad)) / (p.npad * 128);
+  if (p.xs > kMaxXS) p.xs = kMaxXS;
+  p.xs &= ~1;
   if (p.xs < 2) return cudaErrorInvalidConfiguration;
   p.ksplit = prefill_ksplit(m, p.npad, dev, ws);
   p.counters = p.ksplit > 1 ? ws->counters : nullptr;
@@ -581,7 +628,7 @@ static cudaError_t launch_prefill_typed(const MatrixRef& m, const void* x, float
                        (uint64_t)m.cols * 2, kKB, p.npad, CU_TENSOR_MAP_SWIZZLE_128B);
   if (err != cudaSuccess) return err;
   const int grid = (int)((m.rows + kPM - 1) / kPM) * p.ksplit;
-  kern<<<grid, kThreads, C::smem_bytes(p.ks, p.xs, p.npad), stream>>>(tq, td, tx, p);
+  kern<<<grid, kThreads, C::smem_bytes(p.xs, p.npad), stream>>>(tq, td, tx, p);
   return cudaGetLastError();
 }
 

@@ -109,6 +109,24 @@ def test_prefill_one_hot_pow2_is_dequant(qmv):
     assert np.array_equal(y, deq[:, picks].T)
 
 
+@pytest.mark.parametrize("wt,sf", TYPES)
+def test_prefill_one_hot_general_scales_is_bf16_of_dequant(qmv, wt, sf):
+    # one-hot activations with the workload's scale distribution (not powers of two): each
+    # output is one weight as the tensor core saw it, which must be the bfloat16 (ties to
+    # even) of the exact dequantized weight, bit for bit, whichever way the kernel forms it
+    rows, cols, batch = 300, 1024, 48
+    rng = np.random.default_rng(18 + wt + sf)
+    m = inputs.make_matrix(wt, sf, rows, cols, seed=18 + wt + sf)
+    picks = rng.integers(0, cols, batch)
+    x = np.zeros((batch, cols), np.float32)
+    x[np.arange(batch), picks] = 1.0
+    deq = oracle.dequant(m.W, wt, sf, rows, cols)
+    wb = (inputs.bf16_codes(deq).astype(np.uint32) << 16).view(np.float32)
+    y = run(qmv, m, inputs.bf16_codes(x))
+    expect = wb[:, picks].T
+    assert np.array_equal(y, expect), f"{np.count_nonzero(y != expect)} weights differ"
+
+
 def test_prefill_zero_rows_exact(qmv):
     rows, cols, batch = 140, 512, 24
     m = inputs.make_matrix(2, 1, rows, cols, seed=9)
