@@ -282,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     mbar_init(acc_full, 2);
     *failed = 0;
     fence_mbar_init();
+    griddep_launch_dependents();  // the next kernel may be scheduled (it waits for this one before its activations)
     prefetch_tmap(&tq);
     prefetch_tmap(&td);
     prefetch_tmap(&tx);
@@ -320,6 +321,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   } else if (warp == kXWarp) {
     // ---------------------------------------------------------------- X-stage producer
     if (lane == 0) {
+      // the activations (and, after them, the y and workspace writes) wait for the preceding
+      // kernel to complete when this launch overlaps it; the weights do not
+      griddep_wait();
       int x_issued = 0;
       int xs = 0;         // slot of stage kb in the X ring (kb % p.xs)
       uint32_t xph = 0;   // its phase ((kb / p.xs) & 1)
@@ -587,7 +591,7 @@ static int prefill_ksplit(const MatrixRef& m, int npad, const DeviceInfo& dev, c
 
 template <int WT, bool F16>
 static cudaError_t launch_prefill_typed(const MatrixRef& m, const void* x, float* y, int batch, const DeviceInfo& dev,
-                                        const Workspace* ws, cudaStream_t stream) {
+                                        const Workspace* ws, bool pdl, cudaStream_t stream) {
   using C = PCfg<WT, F16>;
   auto kern = prefill_kernel<WT, F16>;
   static bool ready[64] = {};
@@ -628,19 +632,28 @@ static cudaError_t launch_prefill_typed(const MatrixRef& m, const void* x, float
                        (uint64_t)m.cols * 2, kKB, p.npad, CU_TENSOR_MAP_SWIZZLE_128B);
   if (err != cudaSuccess) return err;
   const int grid = (int)((m.rows + kPM - 1) / kPM) * p.ksplit;
-  kern<<<grid, kThreads, C::smem_bytes(p.xs, p.npad), stream>>>(tq, td, tx, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::smem_bytes(p.xs, p.npad);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, tq, td, tx, p);
 }
 
 cudaError_t launch_prefill(const MatrixRef& m, const void* x, float* y, int batch, const DeviceInfo& dev,
-                           const Workspace* ws, cudaStream_t stream) {
+                           const Workspace* ws, bool pdl, cudaStream_t stream) {
   if (batch < 1 || batch > kMaxN) return cudaErrorInvalidValue;
   if (m.wtype == QMV_Q4_0) {
-    return m.scale_f16 ? launch_prefill_typed<QMV_Q4_0, true>(m, x, y, batch, dev, ws, stream)
-                       : launch_prefill_typed<QMV_Q4_0, false>(m, x, y, batch, dev, ws, stream);
+    return m.scale_f16 ? launch_prefill_typed<QMV_Q4_0, true>(m, x, y, batch, dev, ws, pdl, stream)
+                       : launch_prefill_typed<QMV_Q4_0, false>(m, x, y, batch, dev, ws, pdl, stream);
   }
-  return m.scale_f16 ? launch_prefill_typed<QMV_Q8_0, true>(m, x, y, batch, dev, ws, stream)
-                     : launch_prefill_typed<QMV_Q8_0, false>(m, x, y, batch, dev, ws, stream);
+  return m.scale_f16 ? launch_prefill_typed<QMV_Q8_0, true>(m, x, y, batch, dev, ws, pdl, stream)
+                     : launch_prefill_typed<QMV_Q8_0, false>(m, x, y, batch, dev, ws, pdl, stream);
 }
 
 }  // namespace qmv

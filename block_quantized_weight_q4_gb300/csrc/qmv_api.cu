@@ -176,7 +176,7 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
         const int nb = (batch - b0) < pmax ? (batch - b0) : pmax;
         const void* xp = static_cast<const uint8_t*>(problems[i].x) + (size_t)b0 * (size_t)ms[i].cols * xsz;
         float* yp = problems[i].y + (size_t)b0 * (size_t)ms[i].rows;
-        if (launch_prefill(ms[i], xp, yp, nb, dev, pw, stream) != cudaSuccess) return QMV_E_CUDA;
+        if (launch_prefill(ms[i], xp, yp, nb, dev, pw, pdl, stream) != cudaSuccess) return QMV_E_CUDA;
       }
     } else {
       any_decode = true;

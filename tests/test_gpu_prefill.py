@@ -254,3 +254,45 @@ def test_prefill_full_size_graph_replays_stable(qmv, wt, sf, batch):
         torch.cuda.synchronize()
         assert_bits_equal(y.cpu().numpy(), first, "full-size prefill graph replay")
     assert qmv.last_error() == 0
+
+
+def test_prefill_overlap_waits_for_the_preceding_kernel(qmv):
+    # y1 = W1 x (prefill); x2 = bf16(y1) by a torch kernel; y2 = W2 x2 launched with the
+    # overlap flag: its weight loads may start early, but it must read x2 only after the
+    # conversion kernel has finished (eager and in a graph, repeated)
+    import torch
+    from helpers import assert_bits_equal
+    batch, rows1, cols1, rows2 = 48, 1024, 2048, 384
+    m1 = inputs.make_matrix(2, 1, rows1, cols1, seed=61)
+    m2 = inputs.make_matrix(2, 1, rows2, rows1, seed=62)
+    x = inputs.make_x(batch, cols1, True, seed=63)
+    W1, W2, xd = dev_u8(m1.W), dev_u8(m2.W), dev_x(x)
+    y1 = torch.empty((batch, rows1), device="cuda")
+    y2 = torch.empty((batch, rows2), device="cuda")
+    x2 = torch.empty((batch, rows1), device="cuda", dtype=torch.bfloat16)
+    s = torch.cuda.Stream()
+
+    def step():
+        qmv.matvec_grouped(2, 1, [(rows1, cols1, W1, xd, y1)], overlap=True)
+        x2.copy_(y1)  # float32 -> bfloat16, ties to even
+        qmv.matvec_grouped(2, 1, [(rows2, rows1, W2, x2, y2)], overlap=True)
+
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.synchronize()
+    x2_codes = x2.view(torch.int16).cpu().numpy().view(np.uint16)
+    y_ref, absref = oracle.matvec(m2.W, 2, 1, rows2, rows1, x2_codes)
+    first = y2.cpu().numpy().copy()
+    check_product(first, y_ref, absref, TOL, "overlapped chain")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(3):
+            step()
+    for _ in range(4):
+        y1.fill_(0.0)
+        x2.fill_(0.0)
+        y2.fill_(0.0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert_bits_equal(y2.cpu().numpy(), first, "overlapped chain graph replay")
+    assert qmv.last_error() == 0
