@@ -34,10 +34,15 @@ constexpr size_t kStreamWorkspaceBytes = (size_t)4 << 20;
 constexpr int kPrefillCounters = 4096;
 constexpr size_t kPrefillWorkspaceBytes = (size_t)32 << 20;
 
+// a stream's buffer for float32 activations split into bfloat16 pairs (16 rows of cols
+// bf16 per problem: up to 65,536 columns over the problems of one launch)
+constexpr size_t kSplitBytes = (size_t)2 << 20;
+
 namespace {
 std::mutex g_ws_mu;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_pws;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_xws;
 
 cudaError_t cached_workspace(std::map<std::pair<int, cudaStream_t>, Workspace>& cache, const DeviceInfo& dev,
                              cudaStream_t stream, size_t bytes, int counters, Workspace* ws) {
@@ -78,6 +83,99 @@ cudaError_t stream_prefill_workspace(const DeviceInfo& dev, cudaStream_t stream,
   return cached_workspace(g_pws, dev, stream, kPrefillWorkspaceBytes, kPrefillCounters, ws);
 }
 
+namespace {
+
+struct SplitArgs {
+  const float* x[dtc::kMaxProblems];
+  uint16_t* out[dtc::kMaxProblems];
+  int cols[dtc::kMaxProblems];
+  int batch;
+};
+
+// bfloat16 bits of v rounded to nearest (ties to even); finite v beyond the bfloat16 range
+// (which would round to infinity) are truncated instead, so that hi + lo stays finite.
+__device__ __forceinline__ uint16_t bf16_bits_rn_finite(float v) {
+  const uint32_t r = pack_bf16x2(v, v) & 0xFFFFu;
+  const float back = __uint_as_float(r << 16);
+  if (isfinite(v) && !isfinite(back)) return static_cast<uint16_t>(__float_as_uint(v) >> 16);
+  return static_cast<uint16_t>(r);
+}
+
+// x (batch float32 vectors of cols) as 16 rows of bfloat16: row n < 8 the hi part of vector
+// n, row 8 + n its lo part, hi = RN_bf16(x) and lo = RN_bf16(x - hi) (x - hi is exact in
+// float32); rows of vectors past the batch are zero, and so is lo of a value that is not
+// finite.  One thread per column of one problem (blockIdx.y).
+__global__ void __launch_bounds__(256) split_x_kernel(const __grid_constant__ SplitArgs a) {
+  griddep_wait();  // the activations may be the preceding kernel's output
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  const int i = blockIdx.y;
+  const int cols = a.cols[i];
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= cols) return;
+  const float* x = a.x[i];
+  uint16_t* out = a.out[i];
+#pragma unroll
+  for (int n = 0; n < 8; ++n) {
+    uint16_t hi = 0, lo = 0;
+    if (n < a.batch) {
+      const float v = x[(size_t)n * cols + c];
+      hi = bf16_bits_rn_finite(v);
+      const float h = __uint_as_float((uint32_t)hi << 16);
+      lo = isfinite(v) ? bf16_bits_rn_finite(v - h) : 0;
+    }
+    out[(size_t)n * cols + c] = hi;
+    out[(size_t)(8 + n) * cols + c] = lo;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode_tc_f32(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, int batch,
+                                 bool pdl, const DeviceInfo& dev, const Workspace& ws, cudaStream_t stream) {
+  if (n < 1 || n > dtc::kMaxProblems || batch < 1 || batch > dtc::kMaxBatch) return cudaErrorInvalidValue;
+  size_t need = 0;
+  int maxcols = 0;
+  for (int i = 0; i < n; ++i) {
+    need += (size_t)dtc::kN * (size_t)ms[i].cols * 2;
+    if (ms[i].cols > maxcols) maxcols = (int)ms[i].cols;
+  }
+  if (need > kSplitBytes) return cudaErrorInvalidValue;
+  Workspace xw;
+  cudaError_t err = cached_workspace(g_xws, dev, stream, kSplitBytes, 0, &xw);
+  if (err != cudaSuccess) return err;
+  SplitArgs a{};
+  const void* sx[dtc::kMaxProblems];
+  uint8_t* base = reinterpret_cast<uint8_t*>(xw.partials);
+  for (int i = 0; i < n; ++i) {
+    a.x[i] = static_cast<const float*>(xs[i]);
+    a.out[i] = reinterpret_cast<uint16_t*>(base);
+    a.cols[i] = (int)ms[i].cols;
+    sx[i] = base;
+    base += (size_t)dtc::kN * (size_t)ms[i].cols * 2;  // cols % 256 == 0: every buffer 16-byte aligned
+  }
+  a.batch = batch;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)((maxcols + 255) / 256), (unsigned)n);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  err = cudaLaunchKernelEx(&cfg, split_x_kernel, a);
+  if (err != cudaSuccess) return err;
+  // the product launches as a programmatic dependent of the split: its weight loads overlap it
+  if (ms[0].wtype == QMV_Q4_0) return dtc::launch_q4(ms, sx, ys, n, batch, true, true, dev, ws, stream);
+  return dtc::launch_q8(ms, sx, ys, n, batch, true, true, dev, ws, stream);
+}
+
+bool decode_tc_f32_fits(const MatrixRef* ms, int n) {
+  size_t need = 0;
+  for (int i = 0; i < n; ++i) need += (size_t)dtc::kN * (size_t)ms[i].cols * 2;
+  return need <= kSplitBytes;
+}
+
 cudaError_t reset_workspaces() {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -95,8 +193,8 @@ cudaError_t reset_workspaces() {
 
 cudaError_t launch_decode_tc(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, int batch, bool pdl,
                              const DeviceInfo& dev, const Workspace& ws, cudaStream_t stream) {
-  if (ms[0].wtype == QMV_Q4_0) return dtc::launch_q4(ms, xs, ys, n, batch, pdl, dev, ws, stream);
-  return dtc::launch_q8(ms, xs, ys, n, batch, pdl, dev, ws, stream);
+  if (ms[0].wtype == QMV_Q4_0) return dtc::launch_q4(ms, xs, ys, n, batch, false, pdl, dev, ws, stream);
+  return dtc::launch_q8(ms, xs, ys, n, batch, false, pdl, dev, ws, stream);
 }
 
 }  // namespace qmv

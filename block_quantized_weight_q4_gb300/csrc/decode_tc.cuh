@@ -98,6 +98,7 @@ struct Problem {
 struct Params {
   int nprob;
   int batch;
+  int xsplit;  // 1: x[i] is 16 rows of bfloat16, hi parts of the vectors in rows 0..7, lo in 8..15
   int grid;
   long long units;
   int* status;
@@ -211,6 +212,42 @@ __device__ __forceinline__ void add_block_sums(uint32_t tsum, int k0, const floa
     for (int k = 0; k < G; ++k)
 #pragma unroll
       for (int n = 0; n < NV; ++n) acc[n] = fmaf(dk[k0 + kb + k], __uint_as_float(v[k][n]), acc[n]);
+  }
+}
+
+// The same with float32 activations given as bfloat16 pairs x = hi + lo: the MMA's B rows
+// 0..7 hold the vectors' hi parts and rows 8..15 their lo parts, so vector n's block sum is
+// S[k][n] + S[k][8 + n].
+template <int NV>
+__device__ __forceinline__ void add_block_sums_split(uint32_t tsum, int k0, const float (&dk)[kBlk],
+                                                     float (&acc)[NV]) {
+  constexpr int G = NV <= 4 ? kHalfBlk : 1;  // blocks per tensor-memory read batch
+#pragma unroll
+  for (int kb = 0; kb < kHalfBlk; kb += G) {
+    uint32_t hi[G][NV], lo[G][NV];
+#pragma unroll
+    for (int k = 0; k < G; ++k) {
+      const uint32_t a = tsum + (uint32_t)(16 * (k0 + kb + k));
+      if constexpr (NV == 1) {
+        tmem_ld1(a, hi[k]);
+        tmem_ld1(a + 8, lo[k]);
+      } else if constexpr (NV == 2) {
+        tmem_ld2(a, hi[k]);
+        tmem_ld2(a + 8, lo[k]);
+      } else if constexpr (NV == 4) {
+        tmem_ld4(a, hi[k]);
+        tmem_ld4(a + 8, lo[k]);
+      } else {
+        tmem_ld8(a, hi[k]);
+        tmem_ld8(a + 8, lo[k]);
+      }
+    }
+    tmem_ld_wait();
+#pragma unroll
+    for (int k = 0; k < G; ++k)
+#pragma unroll
+      for (int n = 0; n < NV; ++n)
+        acc[n] = fmaf(dk[k0 + kb + k], __uint_as_float(hi[k][n]) + __uint_as_float(lo[k][n]), acc[n]);
   }
 }
 
@@ -475,7 +512,11 @@ __global__ void __maxnreg__(120) decode_tc_kernel(const __grid_constant__ Maps m
     auto take_half = [&](int j, int h, const float (&dk)[kBlk]) -> bool {
       if (!twait(&dfull[h], (uint32_t)(j & 1), failed, p.status)) return false;
       tc_fence_after();
-      add_block_sums<NV>(tsum, h * kHalfBlk, dk, acc);
+      if (p.xsplit) {
+        add_block_sums_split<NV>(tsum, h * kHalfBlk, dk, acc);
+      } else {
+        add_block_sums<NV>(tsum, h * kHalfBlk, dk, acc);
+      }
       return true;
     };
 
@@ -529,7 +570,8 @@ __global__ void __maxnreg__(120) decode_tc_kernel(const __grid_constant__ Maps m
 }
 
 template <int WT, bool F16, int NV>
-cudaError_t launch_typed(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, int batch, bool pdl,
+cudaError_t launch_typed(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, int batch, bool xsplit,
+                         bool pdl,
                          const DeviceInfo& dev, const Workspace& ws, cudaStream_t stream) {
   using C = Cfg<WT, F16>;
   auto kern = decode_tc_kernel<WT, F16, NV>;
@@ -547,6 +589,7 @@ cudaError_t launch_typed(const MatrixRef* ms, const void* const* xs, float* cons
   Params p{};
   p.nprob = n;
   p.batch = batch;
+  p.xsplit = xsplit ? 1 : 0;
   p.status = dev.status;
   p.partials = ws.partials;
   p.counters = ws.counters;
@@ -586,7 +629,8 @@ cudaError_t launch_typed(const MatrixRef* ms, const void* const* xs, float* cons
     err = encode_tmap_2d(&maps.d[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, m.d, drow, (uint64_t)m.rows, drow, C::DROW,
                          kTileRows, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (err != cudaSuccess) return err;
-    err = encode_tmap_2d(&maps.x[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xs[i], (uint64_t)m.cols, (uint64_t)batch,
+    err = encode_tmap_2d(&maps.x[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xs[i], (uint64_t)m.cols,
+                         (uint64_t)(xsplit ? kN : batch),
                          (uint64_t)m.cols * 2, kXBox, kN, CU_TENSOR_MAP_SWIZZLE_128B);
     if (err != cudaSuccess) return err;
   }
@@ -605,17 +649,17 @@ cudaError_t launch_typed(const MatrixRef* ms, const void* const* xs, float* cons
 }
 
 template <int WT, bool F16>
-cudaError_t launch_wtype(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, int batch, bool pdl,
-                         const DeviceInfo& dev, const Workspace& ws, cudaStream_t stream) {
-  if (batch <= 1) return launch_typed<WT, F16, 1>(ms, xs, ys, n, batch, pdl, dev, ws, stream);
-  if (batch <= 2) return launch_typed<WT, F16, 2>(ms, xs, ys, n, batch, pdl, dev, ws, stream);
-  if (batch <= 4) return launch_typed<WT, F16, 4>(ms, xs, ys, n, batch, pdl, dev, ws, stream);
-  return launch_typed<WT, F16, 8>(ms, xs, ys, n, batch, pdl, dev, ws, stream);
+cudaError_t launch_wtype(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, int batch, bool xsplit,
+                         bool pdl, const DeviceInfo& dev, const Workspace& ws, cudaStream_t stream) {
+  if (batch <= 1) return launch_typed<WT, F16, 1>(ms, xs, ys, n, batch, xsplit, pdl, dev, ws, stream);
+  if (batch <= 2) return launch_typed<WT, F16, 2>(ms, xs, ys, n, batch, xsplit, pdl, dev, ws, stream);
+  if (batch <= 4) return launch_typed<WT, F16, 4>(ms, xs, ys, n, batch, xsplit, pdl, dev, ws, stream);
+  return launch_typed<WT, F16, 8>(ms, xs, ys, n, batch, xsplit, pdl, dev, ws, stream);
 }
 
-cudaError_t launch_q4(const MatrixRef*, const void* const*, float* const*, int, int, bool, const DeviceInfo&,
+cudaError_t launch_q4(const MatrixRef*, const void* const*, float* const*, int, int, bool, bool, const DeviceInfo&,
                       const Workspace&, cudaStream_t);
-cudaError_t launch_q8(const MatrixRef*, const void* const*, float* const*, int, int, bool, const DeviceInfo&,
+cudaError_t launch_q8(const MatrixRef*, const void* const*, float* const*, int, int, bool, bool, const DeviceInfo&,
                       const Workspace&, cudaStream_t);
 
 }  // namespace dtc

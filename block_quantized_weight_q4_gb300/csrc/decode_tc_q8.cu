@@ -4,10 +4,10 @@
 namespace qmv {
 namespace dtc {
 
-cudaError_t launch_q8(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, int batch, bool pdl,
+cudaError_t launch_q8(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, int batch, bool xsplit, bool pdl,
                       const DeviceInfo& dev, const Workspace& ws, cudaStream_t stream) {
-  return ms[0].scale_f16 ? launch_wtype<QMV_Q8_0, true>(ms, xs, ys, n, batch, pdl, dev, ws, stream)
-                         : launch_wtype<QMV_Q8_0, false>(ms, xs, ys, n, batch, pdl, dev, ws, stream);
+  return ms[0].scale_f16 ? launch_wtype<QMV_Q8_0, true>(ms, xs, ys, n, batch, xsplit, pdl, dev, ws, stream)
+                         : launch_wtype<QMV_Q8_0, false>(ms, xs, ys, n, batch, xsplit, pdl, dev, ws, stream);
 }
 
 }  // namespace dtc

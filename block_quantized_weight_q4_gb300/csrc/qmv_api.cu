@@ -214,9 +214,16 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
     for (int i = 0; i < nf; ++i) nweights += fast[i].rows * fast[i].cols;
     bool tc = xb && (nb >= kTcMinBatch || (wtype == QMV_Q8_0 && nb > 1 && nweights >= kTcMinQ8Weights));
     for (int i = 0; i < nf && tc; ++i) tc = decode_tc_supported(fast[i]);
+    // float32 activations, 2..8 vectors: the tensor-memory kernel on the bf16 pairs hi + lo
+    // (its 16 MMA columns hold both parts of up to 8 vectors)
+    bool tc32 = !xb && nb >= 2 && decode_tc_f32_fits(fast, nf);
+    for (int i = 0; i < nf && tc32; ++i) tc32 = decode_tc_supported(fast[i]);
     Workspace ws;
     if (tc && stream_workspace(dev, stream, &ws) == cudaSuccess) {
       if (launch_decode_tc(fast, fx, fy, nf, nb, pdl, dev, ws, stream) != cudaSuccess) return QMV_E_CUDA;
+    } else if (tc32 && stream_workspace(dev, stream, &ws) == cudaSuccess &&
+               launch_decode_tc_f32(fast, fx, fy, nf, nb, pdl, dev, ws, stream) == cudaSuccess) {
+      // done (a stream being captured without its split buffer yet falls through to mma.sync)
     } else if (xb && nb == 1) {
       if (launch_matvec_bdiag(fast, fx, fy, nf, pdl, dev, stream) != cudaSuccess) return QMV_E_CUDA;
     } else if (launch_matvec_mma(fast, fx, fy, nf, xb, nb, pdl, dev, stream) != cudaSuccess) {

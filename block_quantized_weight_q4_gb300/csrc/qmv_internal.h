@@ -96,4 +96,13 @@ int decode_tc_max_problems();
 cudaError_t launch_decode_tc(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, int batch, bool pdl,
                              const DeviceInfo& dev, const Workspace& ws, cudaStream_t stream);
 
+// The same product for float32 activations: x is first split into bfloat16 pairs hi + lo
+// (hi = RN_bf16(x), lo = RN_bf16(x - hi)) in a buffer of the stream, 16 rows per problem
+// (hi of the vectors in rows 0..7, lo in 8..15), which the kernel takes as its 16 MMA
+// columns and adds per vector.  Needs decode_tc_f32_fits (the buffer holds 65,536 columns
+// over the problems) and a stream that is not being captured when it has no buffer yet.
+bool decode_tc_f32_fits(const MatrixRef* ms, int n);
+cudaError_t launch_decode_tc_f32(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, int batch,
+                                 bool pdl, const DeviceInfo& dev, const Workspace& ws, cudaStream_t stream);
+
 }  // namespace qmv

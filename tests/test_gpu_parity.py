@@ -291,3 +291,53 @@ def test_grouped_in_graph_with_overlap(qmv):
         got = yf[i].cpu().numpy()
         check_product(got, y_ref, absref, TOL, f"chain {i}")
         x = inputs.bf16_codes(got.astype(np.float32))
+
+
+@pytest.mark.parametrize("wt,sf", TYPES)
+@pytest.mark.parametrize("batch", [2, 5, 8])
+def test_f32_activations_needing_the_lo_part_exact(qmv, wt, sf, batch):
+    # float32 x = k * 2^-6 with |k| < 2^10: up to 10 significant bits, more than bfloat16
+    # holds, so a product that kept only the bfloat16 of x would be off; split as hi + lo
+    # (both bfloat16) x is exact.  With |level| <= 8 (Q8_0 quants drawn in [-7, 7]) and
+    # d = 2^e (e in [-2, 0]) every term is a multiple of 2^-8 below 2^7 and every partial sum
+    # over 512 columns stays below 2^16: exact in float32 in any order, so the product must
+    # equal the oracle bit for bit.
+    rows, cols = 300, 512
+    rng = np.random.default_rng(70 + wt + sf + batch)
+    m = inputs.make_matrix(wt, sf, rows, cols, seed=71 + batch)
+    q = m.q if wt == 2 else rng.integers(-7, 8, size=m.q.size).astype(np.int8).view(np.uint8)
+    codes = inputs.pow2_scales(rng, rows * cols // 32, sf, -2, 0)
+    W = inputs.assemble(wt, sf, rows, cols, q, codes)
+    m2 = inputs.Matrix(wt, sf, rows, cols, W, q, codes)
+    x = np.ldexp(rng.integers(-1023, 1024, size=(batch, cols)).astype(np.float32), -6)
+    assert np.any(inputs.bf16_codes(x).astype(np.uint32) << 16 != x.view(np.uint32))
+    y_ref, _ = oracle.matvec(W, wt, sf, rows, cols, x)
+    y = gpu_matvec(qmv, m2, x)
+    assert np.array_equal(y.astype(np.float64), y_ref)
+
+
+def test_f32_activations_batch8_graph_replay_bit_identical(qmv):
+    # float32 activations, 8 vectors: the split kernel and the tensor-memory product, eager
+    # on a stream (which creates its buffers) and then replayed in a graph on it
+    import torch
+    rows, cols, batch = 1100, 2048, 8
+    m = inputs.make_matrix(1, 0, rows, cols, seed=81)
+    x = inputs.make_x(batch, cols, False, seed=82)
+    y_ref, absref = oracle.matvec(m.W, 1, 0, rows, cols, x)
+    W, xd = dev_u8(m.W), dev_x(x)
+    y = torch.empty((batch, rows), device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        qmv.matvec(1, 0, rows, cols, W, xd, y)
+    torch.cuda.synchronize()
+    first = y.cpu().numpy().copy()
+    check_product(first, y_ref, absref, TOL, "f32 x batch 8")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(3):
+            qmv.matvec(1, 0, rows, cols, W, xd, y)
+    for _ in range(3):
+        y.fill_(0.0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert_bits_equal(y.cpu().numpy(), first, "f32 x graph replay")
