@@ -47,10 +47,14 @@ constexpr int kRows = 16;            // rows per MMA tile
 constexpr int kBox = 128;            // q box inner extent in bytes (the 128-byte swizzle span)
 constexpr int kMaxProblems = 8;      // problems per grouped launch
 
-template <int WT, bool F16, int NW, int CH>
+// XS: float32 activations given as two bfloat16 vectors hi + lo (x = hi + lo); each stage
+// then carries both and every block's MMAs run once with each, into the same sums.
+template <int WT, bool F16, int NW, int CH, bool XS = false>
 struct Cfg {
   static constexpr int kCH = CH;                                   // chunks per stage
-  static constexpr int X_STAGE = CH * kTK * 2;                    // bfloat16 activations of one stage
+  static constexpr int XPARTS = XS ? 2 : 1;                        // activation vectors per stage
+  static constexpr int X_PART = CH * kTK * 2;                      // bfloat16 activations of one vector
+  static constexpr int X_STAGE = XPARTS * X_PART;                  // activations of one stage
   static constexpr int MT = (WT == QMV_Q4_0) ? 2 : 1;           // 16-row MMA tiles per warp tile
   static constexpr int WROWS = MT * kRows;                        // rows per warp tile
   static constexpr int CBOX = (WT == QMV_Q4_0) ? 1 : 2;         // q boxes per chunk
@@ -66,13 +70,15 @@ struct Cfg {
   static constexpr int Q_WARP = S * Q_STAGE;
   static constexpr int D_WARP = S * D_STAGE;
   static constexpr int X_WARP = S * X_STAGE;
-  // q rings, d rings, activation rings, activation slots (per chunk: 32 lanes x 16 bytes),
-  // zero area (a zero line CH-1 slot areas long), reduction buffer (split-K), barriers
+  // q rings, d rings, activation rings, activation slots (per chunk and vector: 32 lanes x
+  // 16 bytes), zero area (a zero line as long as a warp's slots), reduction buffer (split-K),
+  // barriers
   static constexpr int OFF_D = NW * Q_WARP;
   static constexpr int OFF_X = OFF_D + NW * D_WARP;
   static constexpr int OFF_SLOT = OFF_X + NW * X_WARP;
-  static constexpr int OFF_ZERO = OFF_SLOT + NW * CH * 512;
-  static constexpr int OFF_RED = OFF_ZERO + CH * 512;
+  static constexpr int SLOT_WARP = XPARTS * CH * 512;             // a warp's slots: [vector][chunk][lane]
+  static constexpr int OFF_ZERO = OFF_SLOT + NW * SLOT_WARP;
+  static constexpr int OFF_RED = OFF_ZERO + SLOT_WARP;
   static constexpr int OFF_BAR = OFF_RED + ((NW * WROWS * 4 + 127) / 128) * 128;
   static constexpr int SMEM = 1024 + OFF_BAR + ((NW * S * 8 + 127) / 128) * 128;
 };
@@ -98,6 +104,7 @@ struct Maps {  // per problem: q (128-byte swizzle), d, and activation (viewed a
   CUtensorMap q[kMaxProblems];
   CUtensorMap d[kMaxProblems];
   CUtensorMap x[kMaxProblems];
+  CUtensorMap xl[kMaxProblems];  // the lo vectors (XS)
 };
 
 // Position of a warp in its stream of stages: item (global index), its problem and warp
@@ -123,7 +130,7 @@ __device__ __forceinline__ void cursor_load(Cursor& c, const Params& p, int tile
 // One chunk of a stage of one warp: the 16*MT x 256 weights at qs (q, swizzled) and ds
 // (the chunk's first scale in each DROW-byte row), x block j read at bsrc[j] + boff; adds each
 // row's scaled block sums of blocks 2t, 2t+1 to acc.
-template <int WT, bool F16, int NW, int CH, bool HALF>
+template <int WT, bool F16, int NW, int CH, bool HALF, bool XS = false>
 __device__ __forceinline__ void chunk_math(float (&acc)[Cfg<WT, F16, NW, CH>::MT][2], uint32_t qs, const uint8_t* ds,
                                            const uint32_t (&bsrc)[kBlocksPerStage], uint32_t boff, int lrow,
                                            int lsub, int sw, int g, int t) {
@@ -148,6 +155,8 @@ __device__ __forceinline__ void chunk_math(float (&acc)[Cfg<WT, F16, NW, CH>::MT
       const int k = 2 * bp + hb;
       uint32_t b[4];  // elements (4t, 4t+1), (4t+2, 4t+3), (16+4t, ..), (18+4t, ..) of block k, or zeros
       lds_u32x4(bsrc[k] + boff, b);
+      uint32_t bl[4];  // the same of the lo vector (XS: its slots follow the hi ones)
+      if (XS) lds_u32x4(bsrc[k] + boff + (uint32_t)(CH * 512), bl);
       if (WT == QMV_Q4_0) {
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
@@ -157,11 +166,19 @@ __device__ __forceinline__ void chunk_math(float (&acc)[Cfg<WT, F16, NW, CH>::MT
             q4_word_to_f16_levels(w[mt][2 * hb + 1], h01, h23, hh01, hh23);  // row g + 8
             mma_f16_16816(da[mt], g01, h01, g23, h23, b[0], b[1], da[mt]);
             mma_f16_16816(da[mt], gh01, hh01, gh23, hh23, b[2], b[3], da[mt]);
+            if (XS) {
+              mma_f16_16816(da[mt], g01, h01, g23, h23, bl[0], bl[1], da[mt]);
+              mma_f16_16816(da[mt], gh01, hh01, gh23, hh23, bl[2], bl[3], da[mt]);
+            }
           } else {
             q4_word_to_bf16_levels(w[mt][2 * hb], g01, g23, gh01, gh23);
             q4_word_to_bf16_levels(w[mt][2 * hb + 1], h01, h23, hh01, hh23);
             mma_bf16_16816(da[mt], g01, h01, g23, h23, b[0], b[1], da[mt]);
             mma_bf16_16816(da[mt], gh01, hh01, gh23, hh23, b[2], b[3], da[mt]);
+            if (XS) {
+              mma_bf16_16816(da[mt], g01, h01, g23, h23, bl[0], bl[1], da[mt]);
+              mma_bf16_16816(da[mt], gh01, hh01, gh23, hh23, bl[2], bl[3], da[mt]);
+            }
           }
         }
       } else {
@@ -177,6 +194,10 @@ __device__ __forceinline__ void chunk_math(float (&acc)[Cfg<WT, F16, NW, CH>::MT
           q8_word_to_f16_levels(q[3], h1a, h1b);
           mma_f16_16816(da[0], g0a, h0a, g0b, h0b, b[0], b[1], da[0]);
           mma_f16_16816(da[0], g1a, h1a, g1b, h1b, b[2], b[3], da[0]);
+          if (XS) {
+            mma_f16_16816(da[0], g0a, h0a, g0b, h0b, bl[0], bl[1], da[0]);
+            mma_f16_16816(da[0], g1a, h1a, g1b, h1b, bl[2], bl[3], da[0]);
+          }
         } else {
           q8_word_to_bf16_levels(q[0], g0a, g0b);
           q8_word_to_bf16_levels(q[1], h0a, h0b);
@@ -184,6 +205,10 @@ __device__ __forceinline__ void chunk_math(float (&acc)[Cfg<WT, F16, NW, CH>::MT
           q8_word_to_bf16_levels(q[3], h1a, h1b);
           mma_bf16_16816(da[0], g0a, h0a, g0b, h0b, b[0], b[1], da[0]);
           mma_bf16_16816(da[0], g1a, h1a, g1b, h1b, b[2], b[3], da[0]);
+          if (XS) {
+            mma_bf16_16816(da[0], g0a, h0a, g0b, h0b, bl[0], bl[1], da[0]);
+            mma_bf16_16816(da[0], g1a, h1a, g1b, h1b, bl[2], bl[3], da[0]);
+          }
         }
       }
     }
@@ -211,10 +236,10 @@ __device__ __forceinline__ void chunk_math(float (&acc)[Cfg<WT, F16, NW, CH>::MT
   }
 }
 
-template <int WT, bool F16, int NW, int CH>
+template <int WT, bool F16, int NW, int CH, bool XS>
 __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_constant__ Maps maps,
                                                                const __grid_constant__ Params p) {
-  using C = Cfg<WT, F16, NW, CH>;
+  using C = Cfg<WT, F16, NW, CH, XS>;
   constexpr int MT = C::MT;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -228,7 +253,7 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
   uint8_t* qring = smem + warp * C::Q_WARP;
   uint8_t* dring = smem + C::OFF_D + warp * C::D_WARP;
   uint8_t* xring = smem + C::OFF_X + warp * C::X_WARP;
-  const uint32_t slot = smem_u32(smem + C::OFF_SLOT + warp * (C::kCH * 512) + lane * 16);
+  const uint32_t slot = smem_u32(smem + C::OFF_SLOT + warp * C::SLOT_WARP + lane * 16);
   const uint32_t zline = smem_u32(smem + C::OFF_ZERO);
   float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + warp * C::S;
@@ -238,7 +263,7 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
   const int kslice = warp % p.ks;
   constexpr uint32_t stage_tx = (uint32_t)(C::Q_STAGE + C::D_STAGE + C::X_STAGE);
 
-  for (int i = threadIdx.x; i < C::kCH * 128; i += NW * 32) reinterpret_cast<uint32_t*>(smem + C::OFF_ZERO)[i] = 0u;
+  for (int i = threadIdx.x; i < C::SLOT_WARP / 4; i += NW * 32) reinterpret_cast<uint32_t*>(smem + C::OFF_ZERO)[i] = 0u;
   if (lane == 0) {
     for (int s = 0; s < C::S; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
@@ -266,7 +291,10 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
                       pc.tile * C::WROWS, &bars[ps], pol_stream);
         tma_load_2d(dring + ps * C::D_STAGE, &maps.d[pc.prob], c * C::DROW, pc.tile * C::WROWS, &bars[ps],
                     pol_stream);
-        if (with_x) tma_load_2d_keep(xring + ps * C::X_STAGE, &maps.x[pc.prob], 0, c * C::kCH, &bars[ps]);
+        if (with_x) {
+          tma_load_2d_keep(xring + ps * C::X_STAGE, &maps.x[pc.prob], 0, c * C::kCH, &bars[ps]);
+          if (XS) tma_load_2d_keep(xring + ps * C::X_STAGE + C::X_PART, &maps.xl[pc.prob], 0, c * C::kCH, &bars[ps]);
+        }
       } else {
         mbar_arrive(&bars[ps]);  // a tile past the end of its problem: complete the phase, no data
       }
@@ -298,7 +326,11 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
   if (threadIdx.x == 0) griddep_launch_dependents();
   if (lane == 0) {
     for (int i = 0; i < pre; ++i)
-      if (pre_valid[i]) tma_load_2d_keep(xring + i * C::X_STAGE, &maps.x[pre_prob[i]], 0, pre_c[i] * C::kCH, &bars[i]);
+      if (pre_valid[i]) {
+        tma_load_2d_keep(xring + i * C::X_STAGE, &maps.x[pre_prob[i]], 0, pre_c[i] * C::kCH, &bars[i]);
+        if (XS)
+          tma_load_2d_keep(xring + i * C::X_STAGE + C::X_PART, &maps.xl[pre_prob[i]], 0, pre_c[i] * C::kCH, &bars[i]);
+      }
   }
 
   // ldmatrix: lane supplies row (lane & 7) + 8 * (matrix & 1), 16-byte chunk (matrix >> 1)
@@ -341,33 +373,35 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
           const uint8_t* ds = dring + cs * C::D_STAGE;
           // this lane's activations of each chunk h: block g, elements 4t..4t+3 and
           // 16+4t..16+4t+3; its slot for chunk h is 512 bytes after the one for chunk h-1
-          uint2 xa[C::kCH], xb[C::kCH];
-          uint32_t hx[C::kCH][4];
+          // (XS: the same of the lo vector, whose slots follow the hi ones: chunk h at CH + h)
+          constexpr int NX = C::XPARTS * C::kCH;
+          uint2 xa[NX], xb[NX];
+          uint32_t hx[NX][4];
           bool exact = true;
 #pragma unroll
-          for (int h = 0; h < C::kCH; ++h) {
-            const uint8_t* xl = xring + cs * C::X_STAGE + h * (kTK * 2) + g * 64 + t * 8;
-            xa[h] = *reinterpret_cast<const uint2*>(xl);
-            xb[h] = *reinterpret_cast<const uint2*>(xl + 32);
-            hx[h][0] = bf16x2_to_f16x2(xa[h].x, exact);
-            hx[h][1] = bf16x2_to_f16x2(xa[h].y, exact);
-            hx[h][2] = bf16x2_to_f16x2(xb[h].x, exact);
-            hx[h][3] = bf16x2_to_f16x2(xb[h].y, exact);
+          for (int e = 0; e < NX; ++e) {
+            const uint8_t* xl = xring + cs * C::X_STAGE + e * (kTK * 2) + g * 64 + t * 8;
+            xa[e] = *reinterpret_cast<const uint2*>(xl);
+            xb[e] = *reinterpret_cast<const uint2*>(xl + 32);
+            hx[e][0] = bf16x2_to_f16x2(xa[e].x, exact);
+            hx[e][1] = bf16x2_to_f16x2(xa[e].y, exact);
+            hx[e][2] = bf16x2_to_f16x2(xb[e].x, exact);
+            hx[e][3] = bf16x2_to_f16x2(xb[e].y, exact);
           }
           if (__all_sync(0xffffffffu, exact)) {
 #pragma unroll
-            for (int h = 0; h < C::kCH; ++h) sts_u32x4(slot + h * 512, hx[h][0], hx[h][1], hx[h][2], hx[h][3]);
+            for (int e = 0; e < NX; ++e) sts_u32x4(slot + e * 512, hx[e][0], hx[e][1], hx[e][2], hx[e][3]);
 #pragma unroll
             for (int h = 0; h < C::kCH; ++h)
-              chunk_math<WT, F16, NW, CH, true>(acc, qs + h * C::Q_CHUNK, ds + h * C::DCHUNK, bsrc, h * 512u, lrow,
-                                            lsub, sw, g, t);
+              chunk_math<WT, F16, NW, CH, true, XS>(acc, qs + h * C::Q_CHUNK, ds + h * C::DCHUNK, bsrc, h * 512u,
+                                                    lrow, lsub, sw, g, t);
           } else {
 #pragma unroll
-            for (int h = 0; h < C::kCH; ++h) sts_u32x4(slot + h * 512, xa[h].x, xa[h].y, xb[h].x, xb[h].y);
+            for (int e = 0; e < NX; ++e) sts_u32x4(slot + e * 512, xa[e].x, xa[e].y, xb[e].x, xb[e].y);
 #pragma unroll
             for (int h = 0; h < C::kCH; ++h)
-              chunk_math<WT, F16, NW, CH, false>(acc, qs + h * C::Q_CHUNK, ds + h * C::DCHUNK, bsrc, h * 512u, lrow,
-                                             lsub, sw, g, t);
+              chunk_math<WT, F16, NW, CH, false, XS>(acc, qs + h * C::Q_CHUNK, ds + h * C::DCHUNK, bsrc, h * 512u,
+                                                     lrow, lsub, sw, g, t);
           }
         }
       }
@@ -428,10 +462,10 @@ struct Plan {
   long long cost = -1;
 };
 
-template <int WT, bool F16, int NW, int CH>
+template <int WT, bool F16, int NW, int CH, bool XS>
 cudaError_t plan_typed(const MatrixRef* ms, int n, const DeviceInfo& dev, Plan* out) {
-  using C = Cfg<WT, F16, NW, CH>;
-  auto kern = matvec_bdiag_kernel<WT, F16, NW, CH>;
+  using C = Cfg<WT, F16, NW, CH, XS>;
+  auto kern = matvec_bdiag_kernel<WT, F16, NW, CH, XS>;
   // per device: the shared-memory attribute set and the occupancy known (0 = does not fit)
   static std::mutex mu;
   static bool ready[64] = {};
@@ -483,10 +517,10 @@ cudaError_t plan_typed(const MatrixRef* ms, int n, const DeviceInfo& dev, Plan* 
   return cudaSuccess;
 }
 
-template <int WT, bool F16, int NW, int CH>
+template <int WT, bool F16, int NW, int CH, bool XS>
 cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* const* xs, float* const* ys, int n,
                          bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
-  using C = Cfg<WT, F16, NW, CH>;
+  using C = Cfg<WT, F16, NW, CH, XS>;
   Params p{};
   p.nprob = n;
   p.status = dev.status;
@@ -520,6 +554,12 @@ cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* cons
     err = encode_tmap_2d(&maps.x[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xs[i], kTK, (uint64_t)(m.cols / kTK), kTK * 2,
                          kTK, C::kCH, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (err != cudaSuccess) return err;
+    if (XS) {  // the lo vector follows the hi one
+      const void* lo = static_cast<const uint8_t*>(xs[i]) + (size_t)m.cols * 2;
+      err = encode_tmap_2d(&maps.xl[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, lo, kTK, (uint64_t)(m.cols / kTK), kTK * 2,
+                           kTK, C::kCH, CU_TENSOR_MAP_SWIZZLE_NONE);
+      if (err != cudaSuccess) return err;
+    }
   }
 
   cudaLaunchConfig_t cfg{};
@@ -532,37 +572,50 @@ cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* cons
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, matvec_bdiag_kernel<WT, F16, NW, CH>, maps, p);
+  return cudaLaunchKernelEx(&cfg, matvec_bdiag_kernel<WT, F16, NW, CH, XS>, maps, p);
 }
 
 // Stages of two chunks (one-chunk stages fit more warps per SM and measured faster on large
 // Q4_0 launches alone, but slower on the Llama-7B layer step, the Q4_0 4096 x 4096 product and
 // Q8_0), in 4-warp CTAs; when that leaves SMs without a CTA (a launch with few tiles), 8-warp
 // CTAs instead if their estimate is smaller.
-template <int WT, bool F16>
+template <int WT, bool F16, bool XS>
 cudaError_t launch_best(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
                         const DeviceInfo& dev, cudaStream_t stream) {
   Plan p4, p8;
-  cudaError_t err = plan_typed<WT, F16, 4, 2>(ms, n, dev, &p4);
+  cudaError_t err = plan_typed<WT, F16, 4, 2, XS>(ms, n, dev, &p4);
   if (err != cudaSuccess) return err;
-  if (p4.cost >= 0 && p4.grid > dev.sm_count) return launch_typed<WT, F16, 4, 2>(p4, ms, xs, ys, n, pdl, dev, stream);
-  err = plan_typed<WT, F16, 8, 2>(ms, n, dev, &p8);
+  if (p4.cost >= 0 && p4.grid > dev.sm_count)
+    return launch_typed<WT, F16, 4, 2, XS>(p4, ms, xs, ys, n, pdl, dev, stream);
+  err = plan_typed<WT, F16, 8, 2, XS>(ms, n, dev, &p8);
   if (err != cudaSuccess) return err;
-  if (p8.cost >= 0 && (p4.cost < 0 || p8.cost < p4.cost)) return launch_typed<WT, F16, 8, 2>(p8, ms, xs, ys, n, pdl, dev, stream);
+  if (p8.cost >= 0 && (p4.cost < 0 || p8.cost < p4.cost))
+    return launch_typed<WT, F16, 8, 2, XS>(p8, ms, xs, ys, n, pdl, dev, stream);
   if (p4.cost < 0) return cudaErrorInvalidConfiguration;
-  return launch_typed<WT, F16, 4, 2>(p4, ms, xs, ys, n, pdl, dev, stream);
+  return launch_typed<WT, F16, 4, 2, XS>(p4, ms, xs, ys, n, pdl, dev, stream);
+}
+
+template <bool XS>
+cudaError_t launch_any(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
+                       const DeviceInfo& dev, cudaStream_t stream) {
+  const MatrixRef& m = ms[0];
+  if (m.wtype == QMV_Q4_0)
+    return m.scale_f16 ? launch_best<QMV_Q4_0, true, XS>(ms, xs, ys, n, pdl, dev, stream)
+                       : launch_best<QMV_Q4_0, false, XS>(ms, xs, ys, n, pdl, dev, stream);
+  return m.scale_f16 ? launch_best<QMV_Q8_0, true, XS>(ms, xs, ys, n, pdl, dev, stream)
+                     : launch_best<QMV_Q8_0, false, XS>(ms, xs, ys, n, pdl, dev, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_matvec_bdiag(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
                                 const DeviceInfo& dev, cudaStream_t stream) {
-  const MatrixRef& m = ms[0];
-  if (m.wtype == QMV_Q4_0)
-    return m.scale_f16 ? launch_best<QMV_Q4_0, true>(ms, xs, ys, n, pdl, dev, stream)
-                       : launch_best<QMV_Q4_0, false>(ms, xs, ys, n, pdl, dev, stream);
-  return m.scale_f16 ? launch_best<QMV_Q8_0, true>(ms, xs, ys, n, pdl, dev, stream)
-                     : launch_best<QMV_Q8_0, false>(ms, xs, ys, n, pdl, dev, stream);
+  return launch_any<false>(ms, xs, ys, n, pdl, dev, stream);
+}
+
+cudaError_t launch_matvec_bdiag_split(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
+                                      const DeviceInfo& dev, cudaStream_t stream) {
+  return launch_any<true>(ms, xs, ys, n, pdl, dev, stream);
 }
 
 }  // namespace qmv

@@ -90,6 +90,8 @@ struct SplitArgs {
   uint16_t* out[dtc::kMaxProblems];
   int cols[dtc::kMaxProblems];
   int batch;
+  int nvec;    // hi rows written (the lo rows too): batch rounded up to the consumer's width
+  int lo_row;  // row of vector 0's lo part
 };
 
 // bfloat16 bits of v rounded to nearest (ties to even); finite v beyond the bfloat16 range
@@ -101,9 +103,9 @@ __device__ __forceinline__ uint16_t bf16_bits_rn_finite(float v) {
   return static_cast<uint16_t>(r);
 }
 
-// x (batch float32 vectors of cols) as 16 rows of bfloat16: row n < 8 the hi part of vector
-// n, row 8 + n its lo part, hi = RN_bf16(x) and lo = RN_bf16(x - hi) (x - hi is exact in
-// float32); rows of vectors past the batch are zero, and so is lo of a value that is not
+// x (batch float32 vectors of cols) as rows of bfloat16: row n < nvec the hi part of vector
+// n, row lo_row + n its lo part, hi = RN_bf16(x) and lo = RN_bf16(x - hi) (x - hi is exact
+// in float32); rows of vectors past the batch are zero, and so is lo of a value that is not
 // finite.  One thread per column of one problem (blockIdx.y).
 __global__ void __launch_bounds__(256) split_x_kernel(const __grid_constant__ SplitArgs a) {
   griddep_wait();  // the activations may be the preceding kernel's output
@@ -114,8 +116,7 @@ __global__ void __launch_bounds__(256) split_x_kernel(const __grid_constant__ Sp
   if (c >= cols) return;
   const float* x = a.x[i];
   uint16_t* out = a.out[i];
-#pragma unroll
-  for (int n = 0; n < 8; ++n) {
+  for (int n = 0; n < a.nvec; ++n) {
     uint16_t hi = 0, lo = 0;
     if (n < a.batch) {
       const float v = x[(size_t)n * cols + c];
@@ -124,19 +125,24 @@ __global__ void __launch_bounds__(256) split_x_kernel(const __grid_constant__ Sp
       lo = isfinite(v) ? bf16_bits_rn_finite(v - h) : 0;
     }
     out[(size_t)n * cols + c] = hi;
-    out[(size_t)(8 + n) * cols + c] = lo;
+    out[(size_t)(a.lo_row + n) * cols + c] = lo;
   }
 }
 
 }  // namespace
 
-cudaError_t launch_decode_tc_f32(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, int batch,
-                                 bool pdl, const DeviceInfo& dev, const Workspace& ws, cudaStream_t stream) {
-  if (n < 1 || n > dtc::kMaxProblems || batch < 1 || batch > dtc::kMaxBatch) return cudaErrorInvalidValue;
+// Split the float32 activations of n problems (batch vectors each) into rows of bfloat16 in
+// the stream's split buffer: per problem lo_row + nvec rows of cols, laid out one problem
+// after the other; sx[i] receives problem i's rows.  pdl: the split waits for the preceding
+// kernel before reading x.
+static cudaError_t split_activations(const MatrixRef* ms, const void* const* xs, int n, int batch, int nvec, int lo_row,
+                                     bool pdl, const DeviceInfo& dev, cudaStream_t stream, const void** sx) {
+  if (n < 1 || n > dtc::kMaxProblems || batch < 1 || batch > nvec) return cudaErrorInvalidValue;
+  const int rows = lo_row + nvec;
   size_t need = 0;
   int maxcols = 0;
   for (int i = 0; i < n; ++i) {
-    need += (size_t)dtc::kN * (size_t)ms[i].cols * 2;
+    need += (size_t)rows * (size_t)ms[i].cols * 2;
     if (ms[i].cols > maxcols) maxcols = (int)ms[i].cols;
   }
   if (need > kSplitBytes) return cudaErrorInvalidValue;
@@ -144,16 +150,17 @@ cudaError_t launch_decode_tc_f32(const MatrixRef* ms, const void* const* xs, flo
   cudaError_t err = cached_workspace(g_xws, dev, stream, kSplitBytes, 0, &xw);
   if (err != cudaSuccess) return err;
   SplitArgs a{};
-  const void* sx[dtc::kMaxProblems];
   uint8_t* base = reinterpret_cast<uint8_t*>(xw.partials);
   for (int i = 0; i < n; ++i) {
     a.x[i] = static_cast<const float*>(xs[i]);
     a.out[i] = reinterpret_cast<uint16_t*>(base);
     a.cols[i] = (int)ms[i].cols;
     sx[i] = base;
-    base += (size_t)dtc::kN * (size_t)ms[i].cols * 2;  // cols % 256 == 0: every buffer 16-byte aligned
+    base += (size_t)rows * (size_t)ms[i].cols * 2;  // cols % 256 == 0: every row 512-byte aligned
   }
   a.batch = batch;
+  a.nvec = nvec;
+  a.lo_row = lo_row;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)((maxcols + 255) / 256), (unsigned)n);
   cfg.blockDim = dim3(256);
@@ -163,7 +170,14 @@ cudaError_t launch_decode_tc_f32(const MatrixRef* ms, const void* const* xs, flo
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  err = cudaLaunchKernelEx(&cfg, split_x_kernel, a);
+  return cudaLaunchKernelEx(&cfg, split_x_kernel, a);
+}
+
+cudaError_t launch_decode_tc_f32(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, int batch,
+                                 bool pdl, const DeviceInfo& dev, const Workspace& ws, cudaStream_t stream) {
+  const void* sx[dtc::kMaxProblems];
+  // 16 MMA columns: the hi parts of up to 8 vectors, then their lo parts
+  cudaError_t err = split_activations(ms, xs, n, batch, dtc::kMaxBatch, dtc::kMaxBatch, pdl, dev, stream, sx);
   if (err != cudaSuccess) return err;
   // the product launches as a programmatic dependent of the split: its weight loads overlap it
   if (ms[0].wtype == QMV_Q4_0) return dtc::launch_q4(ms, sx, ys, n, batch, true, true, dev, ws, stream);
@@ -174,6 +188,17 @@ bool decode_tc_f32_fits(const MatrixRef* ms, int n) {
   size_t need = 0;
   for (int i = 0; i < n; ++i) need += (size_t)dtc::kN * (size_t)ms[i].cols * 2;
   return need <= kSplitBytes;
+}
+
+cudaError_t launch_matvec_bdiag_f32(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
+                                    const DeviceInfo& dev, cudaStream_t stream) {
+  size_t need = 0;
+  for (int i = 0; i < n; ++i) need += (size_t)2 * (size_t)ms[i].cols * 2;
+  if (need > kSplitBytes) return cudaErrorInvalidValue;
+  const void* sx[dtc::kMaxProblems];
+  cudaError_t err = split_activations(ms, xs, n, 1, 1, 1, pdl, dev, stream, sx);  // rows: hi, lo
+  if (err != cudaSuccess) return err;
+  return launch_matvec_bdiag_split(ms, sx, ys, n, true, dev, stream);
 }
 
 cudaError_t reset_workspaces() {

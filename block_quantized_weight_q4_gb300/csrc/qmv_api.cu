@@ -226,6 +226,8 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
       // done (a stream being captured without its split buffer yet falls through to mma.sync)
     } else if (xb && nb == 1) {
       if (launch_matvec_bdiag(fast, fx, fy, nf, pdl, dev, stream) != cudaSuccess) return QMV_E_CUDA;
+    } else if (!xb && nb == 1 && launch_matvec_bdiag_f32(fast, fx, fy, nf, pdl, dev, stream) == cudaSuccess) {
+      // one float32 vector: the block-diagonal kernel on its bf16 hi + lo parts
     } else if (launch_matvec_mma(fast, fx, fy, nf, xb, nb, pdl, dev, stream) != cudaSuccess) {
       return QMV_E_CUDA;
     }

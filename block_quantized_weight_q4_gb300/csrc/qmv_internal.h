@@ -77,6 +77,16 @@ cudaError_t launch_matvec_mma(const MatrixRef* ms, const void* const* xs, float*
 // every problem matvec_mma_supported() accepts.
 cudaError_t launch_matvec_bdiag(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
                                 const DeviceInfo& dev, cudaStream_t stream);
+// The same with each activation vector given as two bfloat16 vectors hi and lo (x = hi + lo,
+// lo in the cols following hi): every block's MMAs run once with each into the same sums.
+cudaError_t launch_matvec_bdiag_split(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
+                                      const DeviceInfo& dev, cudaStream_t stream);
+// One float32 activation vector per problem: split into hi + lo bfloat16 in the stream's
+// split buffer (2 rows per problem, up to 524,288 columns over the problems), then the above.
+// Fails (nothing launched) when the buffer would not hold them, or cannot be created while
+// the stream is being captured.
+cudaError_t launch_matvec_bdiag_f32(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
+                                    const DeviceInfo& dev, cudaStream_t stream);
 
 // Batched product on the 5th-generation tensor core (weights dequantized to bf16 in tensor
 // memory, tcgen05 MMA, f32 accumulators in tensor memory): bf16 activations, cols % 256 == 0,

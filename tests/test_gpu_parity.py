@@ -294,7 +294,7 @@ def test_grouped_in_graph_with_overlap(qmv):
 
 
 @pytest.mark.parametrize("wt,sf", TYPES)
-@pytest.mark.parametrize("batch", [2, 5, 8])
+@pytest.mark.parametrize("batch", [1, 2, 5, 8])
 def test_f32_activations_needing_the_lo_part_exact(qmv, wt, sf, batch):
     # float32 x = k * 2^-6 with |k| < 2^10: up to 10 significant bits, more than bfloat16
     # holds, so a product that kept only the bfloat16 of x would be off; split as hi + lo
