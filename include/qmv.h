@@ -104,8 +104,13 @@ int qmv_matrix_wtype(int file_wtype, uint32_t q8_mask, int class_bit, int shared
  * vectors over 64M weights or more, take the tensor-memory kernel (levels stored to tensor
  * memory, tcgen05 MMA); a pass of one bf16 vector takes the block-diagonal kernel (one MMA
  * column per weight block; IEEE-half operands for the 256-column stages whose activations
- * are exact halves, bfloat16 otherwise); the rest the mma.sync kernel.  The
- * tensor-memory kernel splits tiles between CTAs;
+ * are exact halves, bfloat16 otherwise).  float32 activations are first split into
+ * bfloat16 pairs hi + lo (hi = RN_bf16(x), lo = RN_bf16(x - hi): 16 bits of x kept) in a
+ * 2 MiB buffer of the calling stream (allocated on its first such call; without it, and
+ * while the stream is captured before it exists, the mma.sync kernel takes them): passes
+ * of 2..8 vectors then take the tensor-memory kernel (hi and lo as its 16 MMA columns) and
+ * one vector the block-diagonal kernel (each block's MMAs once with hi, once with lo).  The
+ * rest take the mma.sync kernel.  The tensor-memory kernel splits tiles between CTAs;
  * their parts meet in a workspace of the calling stream (4 MiB of device memory, allocated
  * on the stream's first such call and kept; while a stream without one is being captured,
  * the call takes the mma.sync kernel instead).  Results do not depend on timing.
