@@ -358,6 +358,27 @@ def other_workloads(torch, qmv, dev, l2, cap, peak_hbm, peak_tf):
                 "overlapped_us": round(ov_us, 3), "overlapped_tflops": round(flops / ov_us / 1e6, 1),
                 "overlapped_frac_bf16_tensor_peak": round(flops / ov_us / 1e6 / peak_tf, 4)}
         del Ws
+
+    # the writer rules on the device: float32 14336 x 4096 (235 MB, past L2) into Q4_0 with
+    # f16 scales and Q8_0 with f32 scales; bytes = float32 read + quantized bytes written
+    lib = qmv.load_library()
+    rows, cols = 14336, 4096
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    src = torch.randn((rows, cols), device=dev, generator=gen, dtype=torch.float32)
+    first = torch.empty(1, dtype=torch.int64, device=dev)
+    for wt, sf, name in ((2, 1, "q4_0_f16"), (1, 0, "q8_0_f32")):
+        nbytes = qmv.weight_bytes(wt, sf, rows, cols)
+        W = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        call = lambda wt=wt, sf=sf, W=W: lib.qmv_quantize(wt, sf, rows, cols, src.data_ptr(), W.data_ptr(),
+                                                        first.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        us = _graph_time_us(torch, [call] * 8, cap)
+        moved = 4 * rows * cols + nbytes
+        res[f"quantize_{rows}x{cols}_{name}"] = {
+            "us": round(us, 3), "gbs": round(moved / us / 1e3, 1), "frac_hbm": round(moved / us / 1e3 / peak_hbm, 4),
+            "bytes": moved}
+        del W
+    del src
     return res
 
 # ------------------------------------------------------------------ GPU arm

@@ -66,6 +66,8 @@ def load_library():
     lib.qmv_dequant.argtypes = [i32, i32, i64, i64, vp, vp, vp]
     lib.qmv_validate.restype = i32
     lib.qmv_validate.argtypes = [i32, i32, i64, i64, vp, vp, vp]
+    lib.qmv_quantize.restype = i32
+    lib.qmv_quantize.argtypes = [i32, i32, i64, i64, vp, vp, vp, vp]
     lib.qmv_check_device.restype = i32
     lib.qmv_check_device.argtypes = []
     lib.qmv_strerror.restype = ctypes.c_char_p
@@ -199,6 +201,22 @@ def validate(wtype: int, scale_dtype: int, rows: int, cols: int, W, stream=None)
                                      _stream(stream))
     _check(st, "qmv_validate")
     return int(first.item())
+
+
+def quantize(wtype: int, scale_dtype: int, src, W=None, stream=None):
+    """Matrix bytes (uint8 CUDA tensor of weight_bytes()) from float32 (rows, cols) by the
+    writer rules.  Returns (W, first refused block index or -1); waits for the stream."""
+    import torch
+    rows, cols = src.shape
+    if src.dtype != torch.float32 or not src.is_contiguous():
+        raise ValueError("src must be a contiguous float32 (rows, cols) tensor")
+    if W is None:
+        W = torch.empty(weight_bytes(wtype, scale_dtype, rows, cols), dtype=torch.uint8, device=src.device)
+    first = torch.empty(1, dtype=torch.int64, device=src.device)
+    st = load_library().qmv_quantize(wtype, scale_dtype, rows, cols, src.data_ptr(), W.data_ptr(), first.data_ptr(),
+                                     _stream(stream))
+    _check(st, "qmv_quantize")
+    return W, int(first.item())
 
 
 def last_error() -> int:

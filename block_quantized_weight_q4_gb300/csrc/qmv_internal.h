@@ -58,6 +58,10 @@ cudaError_t encode_tmap_2d(CUtensorMap* map, int dtype, const void* base, uint64
 cudaError_t current_device_info(DeviceInfo* info);
 
 cudaError_t launch_dequant(const MatrixRef& m, float* out, cudaStream_t stream);
+// The writer rules into W (q at W, d at W + d_off; zeros between q_bytes and d_off).
+cudaError_t launch_quantize(int wtype, bool scale_f16, int64_t rows, int64_t cols, const float* src, uint8_t* W,
+                            int64_t d_off, int64_t q_bytes, int64_t* first_bad, const DeviceInfo& dev,
+                            cudaStream_t stream);
 cudaError_t launch_validate(const MatrixRef& m, int64_t* first_bad, cudaStream_t stream);
 
 // Any shape with cols % 32 == 0; batch 1..8 per call.

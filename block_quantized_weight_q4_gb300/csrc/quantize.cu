@@ -1,0 +1,253 @@
+// quantize.cu -- the writer rules on the device: float32 rows x cols into the two-array
+// layout (Krafla ".mlb model format v1", "Quantization rule" and "Body").
+//
+//   Q8_0 (per block of 32): amax = max |x|.  amax < 1e-30: d = 0 and every quant 0.
+//     f32 scale: d = amax / 127, q = trunc(x * (127 / amax) + copysign(0.5, x)).
+//     f16 scale: d = the f16 nearest amax / 127 (ties to even; a d beyond the f16 range is
+//     refused), q = trunc(x * (1 / d) + copysign(0.5, x)) against that d (d rounding to
+//     f16 zero gives the zero block).  q clamped to +-127.
+//   Q4_0, the "round" rule: d = (element of largest magnitude, the first of equals) / -8,
+//     rounded to the nearest f16 first with f16 scales (refused beyond the f16 range);
+//     nibble = min(15, trunc(x * (1 / d) + 8.5)), kept at or above 0; 1 / d taken as 0
+//     for d = 0.  Element j's nibble is the low half of byte j, element j + 16's the high.
+// Every product, quotient and sum is one IEEE float32 operation rounded to nearest even
+// (written with the _rn intrinsics, so nothing is contracted), so the bytes equal the
+// writer rules' bytes.  Inputs are meant to be finite; what a NaN or infinity produces is
+// not specified.
+#include <mutex>
+
+#include "qmv_common.cuh"
+#include "qmv_internal.h"
+
+namespace qmv {
+
+namespace {
+
+// The rules for one block, held whole by one lane (x[e] = element e).
+template <int WT, bool F16>
+__device__ __forceinline__ void quantize_block(const float (&x)[32], long long blk, uint8_t* __restrict__ q,
+                                               uint8_t* __restrict__ d, unsigned long long* first_bad) {
+  uint32_t dbits = 0;
+  bool bad = false;
+  if (WT == QMV_Q8_0) {
+    float amax = 0.f;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const float a = fabsf(x[e]);
+      if (a > amax) amax = a;
+    }
+    float inv = 0.f;  // 0: the zero block
+    if (!(amax < 1e-30f)) {
+      if (F16) {
+        const unsigned short h = __half_as_ushort(__float2half_rn(__fdiv_rn(amax, 127.0f)));
+        if ((h & 0x7fffu) >= 0x7c00u) {
+          bad = true;  // refused: written as the zero block
+        } else {
+          const float dv = __half2float(__ushort_as_half(h));
+          if (dv != 0.f) {
+            inv = __fdiv_rn(1.0f, dv);
+            dbits = h;
+          }
+        }
+      } else {
+        inv = __fdiv_rn(127.0f, amax);
+        dbits = __float_as_uint(__fdiv_rn(amax, 127.0f));
+      }
+    }
+    uint32_t w[8];
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      uint32_t packed = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        // inv = 0 (the zero block) gives trunc(+-0.5) = 0 with no branch; the conversion
+        // truncates, and clamping its integer equals clamping the truncated float
+        const float xe = x[4 * g + k];
+        int v = (int)__fadd_rn(__fmul_rn(xe, inv), copysignf(0.5f, xe));
+        v = v > 127 ? 127 : (v < -127 ? -127 : v);
+        packed |= (uint32_t)(v & 0xFF) << (8 * k);
+      }
+      w[g] = packed;
+    }
+    uint4* dst = reinterpret_cast<uint4*>(q + blk * 32);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  } else {
+    // element of largest magnitude, the first of equals (strict > in element order)
+    float best = fabsf(x[0]), bval = x[0];
+#pragma unroll
+    for (int e = 1; e < 32; ++e)
+      if (fabsf(x[e]) > best) {
+        best = fabsf(x[e]);
+        bval = x[e];
+      }
+    float dv = __fdiv_rn(bval, -8.0f);
+    if (F16) {
+      const unsigned short h = __half_as_ushort(__float2half_rn(dv));
+      if ((h & 0x7fffu) >= 0x7c00u) {
+        bad = true;  // refused: written as d = 0, every nibble 8
+        dv = 0.f;
+      } else {
+        dv = __half2float(__ushort_as_half(h));
+        dbits = h;
+      }
+    } else {
+      dbits = __float_as_uint(dv);
+    }
+    const float id = (dv != 0.f) ? __fdiv_rn(1.0f, dv) : 0.f;
+    uint32_t nib[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int n = (int)__fadd_rn(__fmul_rn(x[e], id), 8.5f);  // the conversion truncates
+      nib[e] = (uint32_t)(n > 15 ? 15 : (n < 0 ? 0 : n));
+    }
+    // byte j = nibble of element j | nibble of element j + 16 << 4
+    uint32_t w[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      uint32_t packed = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) packed |= (nib[4 * g + k] | (nib[4 * g + k + 16] << 4)) << (8 * k);
+      w[g] = packed;
+    }
+    *reinterpret_cast<uint4*>(q + blk * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  if (F16) {
+    reinterpret_cast<uint16_t*>(d)[blk] = (uint16_t)dbits;
+  } else {
+    reinterpret_cast<uint32_t*>(d)[blk] = dbits;
+  }
+  if (bad) atomicMin(first_bad, (unsigned long long)blk);
+}
+
+// A warp takes a chunk of 32 consecutive blocks (4 KB of float32) at a time, lane i the
+// chunk's block i.  The chunk comes into shared memory by cp.async, coalesced (the warp's
+// 16-byte copies cover 512 contiguous bytes each); block i lands in a slot of 36 floats, so
+// that the lanes' 16-byte reads of their own blocks hit distinct banks in every phase.  Each
+// warp keeps its own ring of kQStages chunks: kQStages - 1 are in flight while it works on
+// one, and cp.async.wait_group (a hardware wait) orders them; nothing spins.
+constexpr int kQWarps = 8;
+constexpr int kQStages = 2;
+constexpr int kQSlot = 36;
+constexpr int kQStageFloats = 32 * kQSlot;
+constexpr int kQSmem = kQWarps * kQStages * kQStageFloats * 4;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <int WT, bool F16>
+__global__ void __launch_bounds__(kQWarps * 32) quantize_kernel(const float* __restrict__ src,
+                                                                uint8_t* __restrict__ q, uint8_t* __restrict__ d,
+                                                                long long nblk, unsigned long long* first_bad) {
+  extern __shared__ __align__(16) float qsm[];
+  const int lane = threadIdx.x & 31;
+  const int wid = threadIdx.x >> 5;
+  const uint32_t ring = smem_u32(qsm) + (uint32_t)(wid * kQStages * kQStageFloats * 4);
+  const long long chunks = (nblk + 31) / 32;
+  const long long W = (long long)gridDim.x * kQWarps;
+  const long long gw = (long long)blockIdx.x * kQWarps + wid;
+
+  // copy chunk c (if there is one) into stage st; one commit group either way
+  auto issue = [&](long long c, int st) {
+    if (c < chunks) {
+      const long long b0 = c * 32;
+      const long long left = nblk - b0;
+      const int nb = left < 32 ? (int)left : 32;
+      const float* g = src + b0 * 32;
+      const uint32_t base = ring + (uint32_t)(st * kQStageFloats * 4);
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int j = 32 * t + lane;  // 16-byte piece j of the chunk: block j / 8, quarter j % 8
+        if (j < nb * 8) cp_async16(base + (uint32_t)(((j >> 3) * kQSlot + 4 * (j & 7)) * 4), g + 4 * j);
+      }
+    }
+    cp_async_commit();
+  };
+
+#pragma unroll
+  for (int st = 0; st < kQStages - 1; ++st) issue(gw + st * W, st);
+  long long k = 0;
+  for (long long c = gw; c < chunks; c += W, ++k) {
+    // the stage refilled here was read in the previous pass, which every lane has left
+    issue(c + (kQStages - 1) * W, (int)((k + kQStages - 1) % kQStages));
+    cp_async_wait<kQStages - 1>();  // this lane's copies of chunk c have landed
+    __syncwarp();                   // ... and every other lane's are visible
+    const uint32_t slot = ring + (uint32_t)(((int)(k % kQStages) * kQStageFloats + lane * kQSlot) * 4);
+    float x[32];
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+      float f[4];
+      lds_f32x4(slot + 16 * v, f);
+      x[4 * v] = f[0];
+      x[4 * v + 1] = f[1];
+      x[4 * v + 2] = f[2];
+      x[4 * v + 3] = f[3];
+    }
+    const long long blk = c * 32 + lane;
+    if (blk < nblk) quantize_block<WT, F16>(x, blk, q, d, first_bad);
+    __syncwarp();
+  }
+  cp_async_wait<0>();
+}
+
+// Grid: every CTA resident at once (the occupancy of this instance times the SMs), and no
+// more warps than chunks.
+template <int WT, bool F16>
+cudaError_t launch_typed(const float* src, uint8_t* q, uint8_t* d, long long nblk, unsigned long long* fb,
+                         const DeviceInfo& dev, cudaStream_t stream) {
+  auto kern = quantize_kernel<WT, F16>;
+  static std::mutex mu;
+  static int ctas_per_sm[64] = {};  // 0 = not yet known
+  if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidValue;
+  if ((size_t)kQSmem > dev.smem_optin) return cudaErrorInvalidConfiguration;
+  int per_sm;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (ctas_per_sm[dev.device] == 0) {
+      cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem);
+      if (err != cudaSuccess) return err;
+      int k = 0;
+      err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&k, kern, kQWarps * 32, kQSmem);
+      if (err != cudaSuccess) return err;
+      ctas_per_sm[dev.device] = k > 0 ? k : 1;
+    }
+    per_sm = ctas_per_sm[dev.device];
+  }
+  const long long chunks = (nblk + 31) / 32;
+  long long grid = (chunks + kQWarps - 1) / kQWarps;
+  const long long cap = (long long)dev.sm_count * per_sm;
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  kern<<<(unsigned)grid, kQWarps * 32, kQSmem, stream>>>(src, q, d, nblk, fb);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(int wtype, bool scale_f16, int64_t rows, int64_t cols, const float* src, uint8_t* W,
+                            int64_t d_off, int64_t q_bytes, int64_t* first_bad, const DeviceInfo& dev,
+                            cudaStream_t stream) {
+  const long long nblk = rows * (cols / 32);
+  cudaError_t err = cudaMemsetAsync(first_bad, 0xFF, sizeof(int64_t), stream);  // -1: none refused
+  if (err != cudaSuccess) return err;
+  if (d_off > q_bytes) {
+    err = cudaMemsetAsync(W + q_bytes, 0, (size_t)(d_off - q_bytes), stream);  // the padding between the arrays
+    if (err != cudaSuccess) return err;
+  }
+  unsigned long long* fb = reinterpret_cast<unsigned long long*>(first_bad);
+  uint8_t* d = W + d_off;
+  if (wtype == QMV_Q8_0) {
+    return scale_f16 ? launch_typed<QMV_Q8_0, true>(src, W, d, nblk, fb, dev, stream)
+                     : launch_typed<QMV_Q8_0, false>(src, W, d, nblk, fb, dev, stream);
+  }
+  return scale_f16 ? launch_typed<QMV_Q4_0, true>(src, W, d, nblk, fb, dev, stream)
+                   : launch_typed<QMV_Q4_0, false>(src, W, d, nblk, fb, dev, stream);
+}
+
+}  // namespace qmv

@@ -213,6 +213,26 @@ int qmv_dequant(int wtype, int scale_dtype, int64_t rows, int64_t cols, const vo
 int qmv_validate(int wtype, int scale_dtype, int64_t rows, int64_t cols, const void *W,
                  int64_t *first_bad, cudaStream_t stream);
 
+/* The writer rules on the device (Krafla page, "Quantization rule"): float32 rows x cols
+ * (src, device, row-major, 16-byte aligned) into the two-array layout at W (device, 16-byte
+ * aligned, qmv_weight_bytes() bytes; the padding between the arrays is written as zeros).
+ *   Q8_0, per block of 32: amax = max |x|; amax < 1e-30 gives d = 0 and zero quants;
+ *     f32 scale: d = amax / 127, q = trunc(x * (127 / amax) + copysign(0.5, x));
+ *     f16 scale: d = the f16 nearest amax / 127, q = trunc(x * (1 / d) + copysign(0.5, x))
+ *     (a d that rounds to f16 zero gives the zero block); q clamped to +-127.
+ *   Q4_0 ("round" rule): d = (element of largest magnitude, the first of equals) / -8,
+ *     rounded to the nearest f16 first with f16 scales; nibble = trunc(x * (1 / d) + 8.5)
+ *     kept in 0..15, with 1 / d = 0 for d = 0.
+ * Each operation is one float32 operation rounded to nearest even, so the bytes equal those
+ * of the rules evaluated in that order.  src is meant to be finite (what a NaN or an
+ * infinity gives is not specified).  A block whose f16 scale would lie beyond the f16 range
+ * is refused: it is written as d = 0 (Q8_0: zero quants, Q4_0: nibbles 8), and *first_bad
+ * (device, 8-byte aligned) receives the smallest such block index (row * cols / 32 +
+ * column block), or -1 when there is none.  Asynchronous.  Returns as qmv_dequant, and
+ * QMV_E_ARG for a null first_bad. */
+int qmv_quantize(int wtype, int scale_dtype, int64_t rows, int64_t cols, const float *src, void *W,
+                 int64_t *first_bad, cudaStream_t stream);
+
 /* Synchronizes the current device, then returns and clears the status word that the
  * kernels set when a bounded wait runs out (QMV_E_TIMEOUT); QMV_OK when none was set,
  * QMV_E_CUDA when the device reports a CUDA error. */

@@ -94,6 +94,14 @@ def test_dequant_and_validate_argument_errors(lib):
     assert lib.qmv_validate(1, 0, 64, 64, FAKE, 0, None) == binding.E_ARG
     assert lib.qmv_validate(1, 0, 64, 64, FAKE, FAKE + 4, None) == binding.E_ALIGN
     assert lib.qmv_validate(1, 0, 0, 64, FAKE, FAKE, None) == binding.E_SHAPE
+    # qmv_quantize: shape, format, null and alignment checks before any launch
+    assert lib.qmv_quantize(2, 1, 64, 48, FAKE, FAKE, FAKE, None) == binding.E_SHAPE
+    assert lib.qmv_quantize(3, 1, 64, 64, FAKE, FAKE, FAKE, None) == binding.E_FORMAT
+    assert lib.qmv_quantize(2, 1, 64, 64, 0, FAKE, FAKE, None) == binding.E_ARG
+    assert lib.qmv_quantize(2, 1, 64, 64, FAKE, FAKE, 0, None) == binding.E_ARG
+    assert lib.qmv_quantize(2, 1, 64, 64, FAKE + 4, FAKE, FAKE, None) == binding.E_ALIGN
+    assert lib.qmv_quantize(2, 1, 64, 64, FAKE, FAKE + 8, FAKE, None) == binding.E_ALIGN
+    assert lib.qmv_quantize(2, 1, 64, 64, FAKE, FAKE, FAKE + 4, None) == binding.E_ALIGN
 
 
 def test_strerror_never_null(lib):
