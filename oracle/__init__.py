@@ -80,6 +80,10 @@ def _load():
     lib.oracle_quant_q4_round_block.argtypes = [vp, i32, vp, vp]
     lib.oracle_quantize.restype = i32
     lib.oracle_quantize.argtypes = [i32, i32, i64, i64, vp, vp]
+    lib.oracle_quantize_x.restype = i32
+    lib.oracle_quantize_x.argtypes = [i32, i64, i64, vp, vp]
+    lib.oracle_matvec_qx.restype = i32
+    lib.oracle_matvec_qx.argtypes = [i32, i32, i64, i64, vp, vp, i32, vp, vp]
     _lib = lib
     return lib
 
@@ -199,3 +203,31 @@ def quantize(src: np.ndarray, wtype: int, scale_f16: int) -> np.ndarray:
     if st != OK:
         raise ValueError(f"oracle_quantize status {st}")
     return W
+
+
+def quantize_x(x: np.ndarray) -> np.ndarray:
+    """Activations (batch x cols, float32 or uint16 bfloat16 codes) by the Q8_0 rule into the
+    Q8_0 / f32-scale two-array image of a batch x cols matrix (uint8)."""
+    x = np.ascontiguousarray(x)
+    batch, cols = x.shape
+    n = weight_bytes(Q8_0, 0, batch, cols)
+    if n < 0:
+        raise ValueError("bad shape")
+    xq = np.zeros(n, dtype=np.uint8)
+    st = _load().oracle_quantize_x(_x_args(x), batch, cols, _ptr(x), _ptr(xq))
+    if st != OK:
+        raise ValueError(f"oracle_quantize_x status {st}")
+    return xq
+
+
+def matvec_qx(W: np.ndarray, wtype: int, scale_f16: int, rows: int, cols: int, xq: np.ndarray, batch: int):
+    """Activation-quantized product: y (batch x rows, float64) = per block d_w d_x times the exact
+    integer dot of weight levels and activation quants, and absref (same shape)."""
+    xq = np.ascontiguousarray(xq, dtype=np.uint8)
+    assert xq.size >= weight_bytes(Q8_0, 0, batch, cols)
+    y = np.empty((batch, rows), dtype=np.float64)
+    a = np.empty((batch, rows), dtype=np.float64)
+    st = _load().oracle_matvec_qx(wtype, scale_f16, rows, cols, _ptr(W), _ptr(xq), batch, _ptr(y), _ptr(a))
+    if st != OK:
+        raise ValueError(f"oracle_matvec_qx status {st}")
+    return y, a

@@ -24,6 +24,11 @@
  *   oracle_validate                           : pinned (hand-built -128 byte)
  *   oracle_quant_q8_block                     : pinned (invariants of the rule)
  *   oracle_quant_q4_round_block               : pinned (invariants of the rule)
+ *   oracle_quantize_x                         : pinned (exactly representable activations
+ *                                               give back their integers and power-of-two scale)
+ *   oracle_matvec_qx                          : pinned (equals the plain product on exactly
+ *                                               representable activations; equals the product
+ *                                               with the dequantized activations; a hand block)
  *   corner readings of the writers (f16 scale that rounds to 0, all-zero Q4 block,
  *   ties of the largest magnitude) : parity unpinned (writer-only, not on the product path)
  */
@@ -431,6 +436,80 @@ int oracle_quantize(int wtype, int scale_f16, int64_t rows, int64_t cols, const 
             } else {
                 for (int i = 0; i < 4; i++) W[off + 4 * idx + i] = (uint8_t)((bits >> (8 * i)) & 0xff);
             }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* ---------------------------------------------------------------------------
+ * The runtime's activation-quantized product.  Krafla page, "Quantization rule": the
+ * runtime's activation quantizer uses the same float32 operations as the Q8_0 writer
+ * (f32 scale); the minfer "02 - GGUF load" page (why weights stay raw until run time):
+ * activations are held in float32 and turned into Q8_0 blocks by the CPU at each product,
+ * whose kernels then work on the two sets of integers.  Reading: the pages do not spell
+ * out the float steps of that dot, so
+ * it is taken as its definition, block by block: the integer dot product of the weight
+ * levels and the activation quants (exact), times d_w * d_x, summed over the blocks.
+ * ------------------------------------------------------------------------- */
+
+/* Activations (batch x cols, float32 or bfloat16 codes with x_bf16 = 1; bfloat16 is
+ * widened to float32 exactly) into xq, the Q8_0 / f32-scale two-array image of a
+ * batch x cols matrix, block by block with the Q8_0 rule.  xq must hold
+ * oracle_weight_bytes(Q8_0, 0, batch, cols) bytes; its padding is written as zeros. */
+int oracle_quantize_x(int x_bf16, int64_t batch, int64_t cols, const void *x, uint8_t *xq)
+{
+    int64_t q, off, dsz;
+    int st = layout(ORACLE_Q8_0, 0, batch, cols, &q, &off, &dsz);
+    if (st != ORACLE_OK) return st;
+    memset(xq, 0, (size_t)(off + dsz));
+    int64_t nblk = cols / 32;
+    for (int64_t b = 0; b < batch; b++) {
+        for (int64_t k = 0; k < nblk; k++) {
+            float xb[32];
+            for (int j = 0; j < 32; j++) xb[j] = (float)x_value(x, x_bf16, cols, b, 32 * k + j);
+            uint32_t bits = 0;
+            st = oracle_quant_q8_block(xb, 0, (int8_t *)(xq + b * cols + 32 * k), &bits);
+            if (st != ORACLE_OK) return st;
+            int64_t idx = b * nblk + k;
+            for (int i = 0; i < 4; i++) xq[off + 4 * idx + i] = (uint8_t)((bits >> (8 * i)) & 0xff);
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* y[b][r] = sum over blocks k of d_w(r, k) * d_x(b, k) * sum_j level_w(r, 32k + j) * q_x(b, 32k + j)
+ * for W (wtype, scale_f16, rows x cols) and xq as oracle_quantize_x writes it (batch x
+ * cols).  The inner sum is an exact integer; d_w * d_x is exact in double (24-bit
+ * significands); the blocks are summed in double in column order.  absref[b][r] = sum over
+ * blocks |d_w d_x| * sum_j |level_w q_x|, the scale of the tolerance. */
+int oracle_matvec_qx(int wtype, int scale_f16, int64_t rows, int64_t cols, const uint8_t *W,
+                     const uint8_t *xq, int batch, double *y, double *absref)
+{
+    int64_t q, off, dsz;
+    int st = layout(wtype, scale_f16, rows, cols, &q, &off, &dsz);
+    if (st != ORACLE_OK) return st;
+    if (batch < 1) return ORACLE_E_SHAPE;
+    st = layout(ORACLE_Q8_0, 0, batch, cols, &q, &off, &dsz);
+    if (st != ORACLE_OK) return st;
+    int64_t nblk = cols / 32;
+    for (int b = 0; b < batch; b++) {
+        for (int64_t r = 0; r < rows; r++) {
+            double acc = 0.0, acc_abs = 0.0;
+            for (int64_t k = 0; k < nblk; k++) {
+                int64_t isum = 0, iabs = 0;
+                for (int j = 0; j < 32; j++) {
+                    int64_t t = (int64_t)oracle_level(W, wtype, cols, r, 32 * k + j) *
+                                (int64_t)oracle_level(xq, ORACLE_Q8_0, cols, b, 32 * k + j);
+                    isum += t;
+                    iabs += t < 0 ? -t : t;
+                }
+                double s = (double)oracle_scale(W, wtype, scale_f16, rows, cols, r, k) *
+                           (double)oracle_scale(xq, ORACLE_Q8_0, 0, batch, cols, b, k);
+                acc += s * (double)isum;
+                acc_abs += fabs(s) * (double)iabs;
+            }
+            y[(int64_t)b * rows + r] = acc;
+            absref[(int64_t)b * rows + r] = acc_abs;
         }
     }
     return ORACLE_OK;

@@ -2,6 +2,7 @@
 
 Each case copies oracle/qmv_oracle.c, plants one mistake by text substitution (a swapped
 nibble half, a dropped level offset, a transposed index, wrong padding, a lost sign...),
+each of which keeps every write inside its buffer (the copies run in this process),
 builds the copy with gcc into a temporary directory and runs the page-derived pin checks
 against it.  At least one check must fail for every mutant, and all checks must pass for
 the unmodified copy.  Everything happens on the CPU; the real oracle is not touched.
@@ -39,6 +40,14 @@ MUTANTS = {
     "f16_scale_size": ("int64_t dsz = nscales * (scale_f16 ? 2 : 4);", "int64_t dsz = nscales * 4;"),
     "f16_scale_read_as_f32": ("if (scale_f16) {\n        const uint8_t *p = W + off + 2 * idx;",
                               "if (0) {\n        const uint8_t *p = W + off + 2 * idx;"),
+    "qx_x_scale_of_vector_0": ("oracle_scale(xq, ORACLE_Q8_0, 0, batch, cols, b, k)",
+                               "oracle_scale(xq, ORACLE_Q8_0, 0, batch, cols, 0, k)"),
+    "qx_x_quants_of_vector_0": ("oracle_level(xq, ORACLE_Q8_0, cols, b, 32 * k + j)",
+                                "oracle_level(xq, ORACLE_Q8_0, cols, 0, 32 * k + j)"),
+    "qx_block_scale_dropped": ("acc += s * (double)isum;", "acc += (double)isum;"),
+    "qx_x_scale_byte_order": ("xq[off + 4 * idx + i] = (uint8_t)((bits >> (8 * i)) & 0xff);",
+                              "xq[off + 4 * idx + i] = (uint8_t)((bits >> (8 * (3 - i))) & 0xff);"),
+    "q8_rule_without_half": ("float u = t + copysignf(0.5f, x[j]);", "float u = t;"),
 }
 
 
@@ -58,6 +67,10 @@ class Orc:
         lib.oracle_matvec.argtypes = [i32, i32, i64, i64, vp, vp, i32, i32, vp, vp]
         lib.oracle_validate.restype = i32
         lib.oracle_validate.argtypes = [i32, i32, i64, i64, vp]
+        lib.oracle_quantize_x.restype = i32
+        lib.oracle_quantize_x.argtypes = [i32, i64, i64, vp, vp]
+        lib.oracle_matvec_qx.restype = i32
+        lib.oracle_matvec_qx.argtypes = [i32, i32, i64, i64, vp, vp, i32, vp, vp]
         self.lib = lib
 
     def dequant(self, W, wt, sf, rows, cols):
@@ -71,6 +84,20 @@ class Orc:
         a = np.empty_like(y)
         assert self.lib.oracle_matvec(wt, sf, rows, cols, W.ctypes.data, x.ctypes.data,
                                       int(x.dtype == np.uint16), x.shape[0], y.ctypes.data, a.ctypes.data) == 0
+        return y, a
+
+    def quantize_x(self, x):
+        batch, cols = x.shape
+        # room for whatever layout a mutant computes (a mutated size may undercount)
+        xq = np.zeros(4 * batch * cols + 1024, np.uint8)
+        assert self.lib.oracle_quantize_x(0, batch, cols, x.ctypes.data, xq.ctypes.data) == 0
+        return xq
+
+    def matvec_qx(self, W, wt, sf, rows, cols, xq, batch):
+        y = np.empty((batch, rows))
+        a = np.empty_like(y)
+        assert self.lib.oracle_matvec_qx(wt, sf, rows, cols, W.ctypes.data, xq.ctypes.data, batch,
+                                         y.ctypes.data, a.ctypes.data) == 0
         return y, a
 
 
@@ -112,6 +139,25 @@ def pin_checks(o):
     W[77] = 0x80
     yield "validate", o.lib.oracle_validate(1, 0, 4, 64, W.ctypes.data) == 2 and \
         o.lib.oracle_validate(1, 0, 4, 64, m.W.ctypes.data) == 0
+    # activation-quantized product: activations k * 2^e (one element of each block at +-127)
+    # quantize to k and 2^e exactly, so the product equals the plain one (exact sums)
+    rng = np.random.default_rng(5)
+    batch, cols = 2, 96
+    k = rng.integers(-127, 128, size=(batch, 3, 32))
+    k[:, :, 7] = 127
+    x = (k * np.exp2(rng.integers(-3, 1, size=(batch, 3)))[:, :, None]).reshape(batch, cols).astype(np.float32)
+    xq = o.quantize_x(x)
+    yield "qx_quants", bool(np.array_equal(xq[:batch * cols].view(np.int8), k.reshape(-1).astype(np.int8)))
+    for wt in (1, 2):
+        m = inputs.make_matrix(wt, 1, 4, cols, seed=8 + wt)
+        yq, _ = o.matvec_qx(m.W, wt, 1, 4, cols, xq, batch)
+        y, _ = o.matvec(m.W, wt, 1, 4, cols, x)
+        yield "qx_exact", bool(np.array_equal(yq, y))
+    # a hand block: levels +1, d_w = 0.5, x = [127, -63.5, 0...] -> q_x = [127, -64], y = 31.5
+    W = inputs.assemble(2, 0, 1, 32, np.full(16, 0x99, np.uint8), np.array([0.5], np.float32).view(np.uint32))
+    xh = np.zeros((1, 32), np.float32)
+    xh[0, 0], xh[0, 1] = 127.0, -63.5
+    yield "qx_hand", o.matvec_qx(W, 2, 0, 1, 32, o.quantize_x(xh), 1)[0][0, 0] == 31.5
 
 
 def build_variant(tmp, name, text):

@@ -378,3 +378,108 @@ def test_quantize_matrix_round_trip_q8():
     W2 = oracle.quantize(deq, 1, 0)
     q_bytes = 4 * 64
     assert np.array_equal(W2[:q_bytes], W[:q_bytes])
+
+
+# ----------------------------------------------------- activation-quantized product
+def _exact_activations(rng, batch, cols, e_lo=-6, e_hi=3):
+    """x = k * 2^e per block: integers |k| <= 127 with one element of each block at +-127,
+    and a power-of-two step 2^e per block.  The Q8_0 rule must give back k and d = 2^e
+    exactly: amax = 127 * 2^e, 127 / amax = 2^-e, x * 2^-e = k, k +- 0.5 truncates to k."""
+    nb = cols // 32
+    k = rng.integers(-127, 128, size=(batch, nb, 32))
+    pos = rng.integers(0, 32, size=(batch, nb))
+    sign = np.where(rng.random((batch, nb)) < 0.5, -1, 1)
+    for b in range(batch):
+        for blk in range(nb):
+            k[b, blk, pos[b, blk]] = 127 * sign[b, blk]
+    e = rng.integers(e_lo, e_hi + 1, size=(batch, nb))
+    x = (k * np.exp2(e)[:, :, None]).reshape(batch, cols).astype(np.float32)
+    return x, k.reshape(batch, cols).astype(np.int8), np.exp2(e).astype(np.float32).reshape(-1)
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_quantize_x_gives_back_exact_activations(bf16):
+    rng = np.random.default_rng(51)
+    batch, cols = 3, 128
+    x, k, step = _exact_activations(rng, batch, cols)
+    xin = inputs.bf16_codes(x) if bf16 else x   # k * 2^e has at most 8 significant bits
+    if bf16:
+        assert np.array_equal((xin.astype(np.uint32) << 16).view(np.float32), x)
+    xq = oracle.quantize_x(xin)
+    off = oracle.scale_offset(1, 0, batch, cols)
+    assert np.array_equal(xq[:batch * cols].view(np.int8), k.reshape(-1))
+    assert np.array_equal(xq[off:off + 4 * step.size].view(np.float32), step)
+    assert not xq[batch * cols:off].any()
+
+
+def test_quantize_x_is_the_q8_writer_rule():
+    # the runtime's activation quantizer and the writer share the rule ("Quantization rule")
+    rng = np.random.default_rng(52)
+    x = (rng.standard_normal((4, 96)) * np.exp(rng.uniform(-5, 5, (4, 1)))).astype(np.float32)
+    assert np.array_equal(oracle.quantize_x(x), oracle.quantize(x, 1, 0))
+    xb = inputs.bf16_codes(x)
+    assert np.array_equal(oracle.quantize_x(xb), oracle.quantize((xb.astype(np.uint32) << 16).view(np.float32), 1, 0))
+
+
+@pytest.mark.parametrize("wt", [1, 2])
+def test_matvec_qx_equals_plain_product_on_exact_activations(wt):
+    # activations that the rule represents exactly leave the product unchanged: with f16
+    # weight scales every term level * d_w * k * 2^e has <= 26 significant bits and the
+    # whole sum stays within double's 53, so both evaluations are exact
+    rng = np.random.default_rng(53 + wt)
+    rows, cols, batch = 6, 256, 3
+    m = inputs.make_matrix(wt, 1, rows, cols, seed=54 + wt)
+    x, _, _ = _exact_activations(rng, batch, cols, e_lo=-3, e_hi=0)
+    yq, aq = oracle.matvec_qx(m.W, wt, 1, rows, cols, oracle.quantize_x(x), batch)
+    y, a = oracle.matvec(m.W, wt, 1, rows, cols, x)
+    assert np.array_equal(yq, y)
+    assert np.array_equal(aq, a)
+
+
+@pytest.mark.parametrize("wt,sf", [(1, 0), (1, 1), (2, 0), (2, 1)])
+def test_matvec_qx_equals_product_with_dequantized_activations(wt, sf):
+    # sum_k d_w d_x sum_j level q_x = sum_c w_c * (q_x d_x)_c: the product against the
+    # dequantized activations; the f32 dequant rounds each q_x * d_x once (<= 2^-24 relative)
+    rows, cols, batch = 5, 320, 2
+    m = inputs.make_matrix(wt, sf, rows, cols, seed=60 + 2 * wt + sf)
+    x = inputs.make_x(batch, cols, False, seed=61)
+    xq = oracle.quantize_x(x)
+    xhat = oracle.dequant(xq, 1, 0, batch, cols)
+    yq, aq = oracle.matvec_qx(m.W, wt, sf, rows, cols, xq, batch)
+    y, a = oracle.matvec(m.W, wt, sf, rows, cols, xhat)
+    assert np.all(np.abs(yq - y) <= 2.0 ** -22 * a)
+    assert np.allclose(aq, a, rtol=2.0 ** -22, atol=0)
+    # and it differs from the product with the unquantized activations by about one step
+    y0, a0 = oracle.matvec(m.W, wt, sf, rows, cols, x)
+    assert np.all(np.abs(yq - y0) <= 0.01 * a0)
+
+
+def test_matvec_qx_hand_block():
+    # Q4_0, one block, every byte 0x99 (levels +1), d_w = 0.5.  x = [127, -63.5, 0, ...]:
+    # amax = 127, d_x = 1, 127 / amax = 1; q_0 = trunc(127 + 0.5) = 127, q_1 = trunc(-63.5 - 0.5)
+    # = -64 (rounded away from zero); isum = 127 - 64 = 63, y = 0.5 * 1 * 63 = 31.5 (the float
+    # product would be 0.5 * 63.5 = 31.75); absref = 0.5 * (127 + 64) = 95.5.
+    W = inputs.assemble(2, 0, 1, 32, np.full(16, 0x99, np.uint8), np.array([0.5], np.float32).view(np.uint32))
+    x = np.zeros((1, 32), np.float32)
+    x[0, 0], x[0, 1] = 127.0, -63.5
+    y, a = oracle.matvec_qx(W, 2, 0, 1, 32, oracle.quantize_x(x), 1)
+    assert y[0, 0] == 31.5 and a[0, 0] == 95.5
+    # Q8_0: quants [2, -3, 0, ...], d_w = 0.25; x = [127, 1.5, 0, ...] gives q_x = [127, 2]
+    # (1.5 + 0.5 = 2): isum = 254 - 6 = 248, y = 62
+    q = np.zeros(32, np.int8)
+    q[0], q[1] = 2, -3
+    W = inputs.assemble(1, 0, 1, 32, q.view(np.uint8), np.array([0.25], np.float32).view(np.uint32))
+    x = np.zeros((1, 32), np.float32)
+    x[0, 0], x[0, 1] = 127.0, 1.5
+    y, a = oracle.matvec_qx(W, 1, 0, 1, 32, oracle.quantize_x(x), 1)
+    assert y[0, 0] == 62.0 and a[0, 0] == 0.25 * 260
+
+
+def test_matvec_qx_batch_rows_are_independent():
+    rows, cols = 4, 128
+    m = inputs.make_matrix(2, 1, rows, cols, seed=70)
+    x = inputs.make_x(3, cols, False, seed=71)
+    y, _ = oracle.matvec_qx(m.W, 2, 1, rows, cols, oracle.quantize_x(x), 3)
+    for b in range(3):
+        yb, _ = oracle.matvec_qx(m.W, 2, 1, rows, cols, oracle.quantize_x(x[b:b + 1]), 1)
+        assert np.array_equal(y[b], yb[0])
