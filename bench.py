@@ -379,6 +379,49 @@ def other_workloads(torch, qmv, dev, l2, cap, peak_hbm, peak_tf):
             "bytes": moved}
         del W
     del src
+
+    # the activation-quantized product (activations to Q8_0 blocks by qmv_quantize_x, then exact
+    # int8 block dot products by qmv_matvec_qx): Q4_0 65536 x 4096 alone, batch 1 and 8, and
+    # the Llama-7B layer step with one quantized activation vector per dependency group
+    m = inputs.make_matrix(2, 1, 65536, 4096, seed=0)
+    Ws = copies_for(torch.from_numpy(m.W).to(dev), m.W.size)
+    n = len(Ws)
+    for batch in (1, 8):
+        x = xdev(inputs.make_x(batch, 4096, True, seed=1000))
+        xq = qmv.quantize_x(x)
+        y = torch.empty((batch, 65536), device=dev)
+        us = _graph_time_us(torch, [lambda i=i: qmv.matvec_qx(2, 1, 65536, 4096, Ws[i % n], xq, batch, y=y)
+                                    for i in range(2 * n)], cap)
+        qus = _graph_time_us(torch, [lambda: qmv.quantize_x(x, xq=xq)] * 64, cap)
+        res[f"qx_q4_65536x4096_f16_b{batch}"] = {
+            "us_per_product": round(us, 3), "weight_gbs": round(m.W.size / us / 1e3, 1),
+            "frac_hbm": round(m.W.size / us / 1e3 / peak_hbm, 4), "quantize_x_us": round(qus, 3)}
+    del Ws
+    specs = layer_specs()
+    lb = layer_bytes(specs)
+    ncopy = max(2, -(-4 * l2 // lb) + 1)
+    mats = [torch.from_numpy(inputs.make_matrix(s.wtype, s.scale_f16, s.rows, s.cols,
+                                                seed=inputs.matrix_seed(WORKLOAD, i)).W).to(dev)
+            for i, s in enumerate(specs)]
+    copies = [[w if c == 0 else w.clone() for w in mats] for c in range(ncopy)]
+    names = [s.name for s in specs]
+    groups = [[names.index(nm) for nm in grp] for grp in LAYER_GROUPS]
+    gx = [xdev(inputs.make_x(1, specs[grp[0]].cols, True, seed=inputs.x_seed(WORKLOAD, grp[0]))) for grp in groups]
+    gxq = [qmv.quantize_x(x) for x in gx]
+    ys = [torch.empty((1, s.rows), device=dev) for s in specs]
+
+    def qx_step(c):
+        for g, grp in enumerate(groups):
+            qmv.quantize_x(gx[g], xq=gxq[g])
+            for i in grp:
+                s = specs[i]
+                qmv.matvec_qx(s.wtype, s.scale_f16, s.rows, s.cols, copies[c][i], gxq[g], 1, y=ys[i])
+
+    us = _graph_time_us(torch, [lambda c=c: qx_step(c) for c in range(ncopy)] * 2, cap)
+    res["qx_llama7b_layer_b1"] = {"us_per_step": round(us, 3), "weight_gbs": round(lb / us / 1e3, 1),
+                                  "frac_hbm": round(lb / us / 1e3 / peak_hbm, 4),
+                                  "launches_per_step": len(groups) + len(specs)}
+    del copies, mats
     return res
 
 # ------------------------------------------------------------------ GPU arm

@@ -68,6 +68,10 @@ def load_library():
     lib.qmv_validate.argtypes = [i32, i32, i64, i64, vp, vp, vp]
     lib.qmv_quantize.restype = i32
     lib.qmv_quantize.argtypes = [i32, i32, i64, i64, vp, vp, vp, vp]
+    lib.qmv_quantize_x.restype = i32
+    lib.qmv_quantize_x.argtypes = [i32, i64, i64, vp, vp, vp]
+    lib.qmv_matvec_qx.restype = i32
+    lib.qmv_matvec_qx.argtypes = [i32, i32, i64, i64, vp, vp, vp, i32, vp]
     lib.qmv_check_device.restype = i32
     lib.qmv_check_device.argtypes = []
     lib.qmv_strerror.restype = ctypes.c_char_p
@@ -217,6 +221,37 @@ def quantize(wtype: int, scale_dtype: int, src, W=None, stream=None):
                                      _stream(stream))
     _check(st, "qmv_quantize")
     return W, int(first.item())
+
+
+def quantize_x(x, xq=None, stream=None):
+    """The runtime's activation quantizer: x (batch, cols) float32/bfloat16 CUDA tensor into
+    xq, the Q8_0 / f32-scale image of the batch x cols matrix (uint8 CUDA tensor of
+    weight_bytes(Q8_0, SCALE_F32, batch, cols)).  Returns xq."""
+    import torch
+    if x.dim() == 1:
+        x = x.unsqueeze(0)
+    batch, cols = x.shape
+    if not x.is_contiguous():
+        raise ValueError("x must be a contiguous (batch, cols) tensor")
+    if xq is None:
+        xq = torch.empty(max(weight_bytes(Q8_0, SCALE_F32, batch, cols), 0), dtype=torch.uint8, device=x.device)
+    st = load_library().qmv_quantize_x(_x_dtype(x), batch, cols, x.data_ptr(), xq.data_ptr(), _stream(stream))
+    _check(st, "qmv_quantize_x")
+    return xq
+
+
+def matvec_qx(wtype: int, scale_dtype: int, rows: int, cols: int, W, xq, batch: int, y=None, stream=None):
+    """Activation-quantized product: y[v][r] = sum_b d_w d_x (exact integer block dot) for the
+    quantized activations xq (as quantize_x returns them, batch vectors).  Returns y."""
+    import torch
+    if y is None:
+        y = torch.empty((batch, rows), dtype=torch.float32, device=xq.device)
+    if y.dtype != torch.float32 or tuple(y.shape) != (batch, rows) or not y.is_contiguous():
+        raise ValueError("y must be a contiguous float32 (batch, rows) tensor")
+    st = load_library().qmv_matvec_qx(wtype, scale_dtype, rows, cols, W.data_ptr(), xq.data_ptr(), y.data_ptr(),
+                                      batch, _stream(stream))
+    _check(st, "qmv_matvec_qx")
+    return y
 
 
 def last_error() -> int:

@@ -315,6 +315,41 @@ int qmv_quantize(int wtype, int scale_dtype, int64_t rows, int64_t cols, const f
              : QMV_E_CUDA;
 }
 
+int qmv_quantize_x(int x_dtype, int64_t batch, int64_t cols, const void* x, void* xq, cudaStream_t stream) {
+  if (x_dtype != QMV_X_F32 && x_dtype != QMV_X_BF16) return QMV_E_FORMAT;
+  if (batch < 0) return QMV_E_ARG;
+  if (cols <= 0 || cols % 32 != 0) return QMV_E_SHAPE;
+  if (batch == 0) return QMV_OK;
+  Layout L;
+  const int st = make_layout(QMV_Q8_0, QMV_SCALE_F32, batch, cols, &L);
+  if (st != QMV_OK) return st;
+  if (x == nullptr || xq == nullptr) return QMV_E_ARG;
+  if (!aligned(x, 16) || !aligned(xq, 16)) return QMV_E_ALIGN;
+  return launch_quantize_x(x_dtype == QMV_X_BF16, batch, cols, x, static_cast<uint8_t*>(xq), L.d_off, L.q_bytes,
+                           stream) == cudaSuccess
+             ? QMV_OK
+             : QMV_E_CUDA;
+}
+
+int qmv_matvec_qx(int wtype, int scale_dtype, int64_t rows, int64_t cols, const void* W, const void* xq,
+                  float* y, int batch, cudaStream_t stream) {
+  MatrixRef m;
+  int st = make_ref(wtype, scale_dtype, rows, cols, W, &m);
+  if (st != QMV_OK) return st;
+  if (batch < 0) return QMV_E_ARG;
+  if (batch == 0) return QMV_OK;
+  Layout LX;
+  st = make_layout(QMV_Q8_0, QMV_SCALE_F32, batch, cols, &LX);
+  if (st != QMV_OK) return st;
+  if (xq == nullptr || y == nullptr) return QMV_E_ARG;
+  if (!aligned(xq, 16) || !aligned(y, 4)) return QMV_E_ALIGN;
+  DeviceInfo dev;
+  if (current_device_info(&dev) != cudaSuccess) return QMV_E_CUDA;
+  const int8_t* xqq = static_cast<const int8_t*>(xq);
+  const float* xd = reinterpret_cast<const float*>(static_cast<const uint8_t*>(xq) + LX.d_off);
+  return launch_matvec_qx(m, xqq, xd, batch, y, dev, stream) == cudaSuccess ? QMV_OK : QMV_E_CUDA;
+}
+
 int qmv_check_device(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return QMV_E_CUDA;
   DeviceInfo dev;

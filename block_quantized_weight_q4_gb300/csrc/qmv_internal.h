@@ -63,6 +63,13 @@ cudaError_t launch_quantize(int wtype, bool scale_f16, int64_t rows, int64_t col
                             int64_t d_off, int64_t q_bytes, int64_t* first_bad, const DeviceInfo& dev,
                             cudaStream_t stream);
 cudaError_t launch_validate(const MatrixRef& m, int64_t* first_bad, cudaStream_t stream);
+// The activation quantizer (Q8_0 rule, f32 scale) into xq (q at xq, d at xq + d_off).
+cudaError_t launch_quantize_x(bool x_bf16, int64_t batch, int64_t cols, const void* x, uint8_t* xq, int64_t d_off,
+                              int64_t q_bytes, cudaStream_t stream);
+// The activation-quantized product y[v][r] = sum_b d_w d_x (integer dot of levels and quants);
+// xq / xd: the quants and scales of the batch x cols Q8_0 / f32 activation image.
+cudaError_t launch_matvec_qx(const MatrixRef& m, const int8_t* xq, const float* xd, int batch, float* y,
+                             const DeviceInfo& dev, cudaStream_t stream);
 
 // Any shape with cols % 32 == 0; batch 1..8 per call.
 cudaError_t launch_matvec_simple(const MatrixRef& m, const void* x, bool x_bf16, float* y, int batch,

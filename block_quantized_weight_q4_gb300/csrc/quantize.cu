@@ -228,7 +228,58 @@ cudaError_t launch_typed(const float* src, uint8_t* q, uint8_t* d, long long nbl
   return cudaGetLastError();
 }
 
+// The runtime's activation quantizer: the Q8_0 rule with an f32 scale, one thread per block
+// of 32 activations (float32, or bfloat16 widened exactly).  Activations are a few KB to a
+// few MB, so this is launch-latency bound; the block rule is the writer's.
+template <bool BF16>
+__global__ void __launch_bounds__(128) quantize_x_kernel(const void* __restrict__ x, uint8_t* __restrict__ q,
+                                                         uint8_t* __restrict__ d, long long nblk) {
+  const long long blk = (long long)blockIdx.x * 128 + threadIdx.x;
+  if (blk >= nblk) return;
+  float v[32];
+  if (BF16) {
+    const uint4* p = reinterpret_cast<const uint4*>(x) + blk * 4;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 u = __ldg(p + i);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        v[8 * i + 2 * k] = __uint_as_float(w[k] << 16);  // element 2k: the low half
+        v[8 * i + 2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+      }
+    }
+  } else {
+    const float4* p = reinterpret_cast<const float4*>(x) + blk * 8;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 f = __ldg(p + i);
+      v[4 * i] = f.x;
+      v[4 * i + 1] = f.y;
+      v[4 * i + 2] = f.z;
+      v[4 * i + 3] = f.w;
+    }
+  }
+  quantize_block<QMV_Q8_0, false>(v, blk, q, d, nullptr);  // an f32 scale is never refused
+}
+
 }  // namespace
+
+cudaError_t launch_quantize_x(bool x_bf16, int64_t batch, int64_t cols, const void* x, uint8_t* xq, int64_t d_off,
+                              int64_t q_bytes, cudaStream_t stream) {
+  const long long nblk = batch * (cols / 32);
+  if (d_off > q_bytes) {
+    const cudaError_t err = cudaMemsetAsync(xq + q_bytes, 0, (size_t)(d_off - q_bytes), stream);
+    if (err != cudaSuccess) return err;
+  }
+  const unsigned grid = (unsigned)((nblk + 127) / 128);
+  if (x_bf16) {
+    quantize_x_kernel<true><<<grid, 128, 0, stream>>>(x, xq, xq + d_off, nblk);
+  } else {
+    quantize_x_kernel<false><<<grid, 128, 0, stream>>>(x, xq, xq + d_off, nblk);
+  }
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quantize(int wtype, bool scale_f16, int64_t rows, int64_t cols, const float* src, uint8_t* W,
                             int64_t d_off, int64_t q_bytes, int64_t* first_bad, const DeviceInfo& dev,

@@ -233,6 +233,31 @@ int qmv_validate(int wtype, int scale_dtype, int64_t rows, int64_t cols, const v
 int qmv_quantize(int wtype, int scale_dtype, int64_t rows, int64_t cols, const float *src, void *W,
                  int64_t *first_bad, cudaStream_t stream);
 
+/* The runtime's activation quantizer (Krafla page, "Quantization rule": the writer's Q8_0
+ * operations, applied by the runtime to its activations; f32 scale): x (device, batch x cols,
+ * x_dtype QMV_X_F32 or QMV_X_BF16, row-major, 16-byte aligned; bfloat16 is widened to float32
+ * exactly) into xq (device, 16-byte aligned, qmv_weight_bytes(QMV_Q8_0, QMV_SCALE_F32, batch,
+ * cols) bytes): the two-array Q8_0 / f32-scale image of the batch x cols matrix, the padding
+ * between its arrays written as zeros.  For float32 x the bytes equal those of
+ * qmv_quantize(QMV_Q8_0, QMV_SCALE_F32, batch, cols, x, ...).  batch 0 writes nothing.
+ * Asynchronous.  Returns QMV_OK, QMV_E_FORMAT (x_dtype), QMV_E_SHAPE (cols not a positive
+ * multiple of 32, or a size that overflows), QMV_E_ARG (batch < 0, null pointer),
+ * QMV_E_ALIGN, or QMV_E_CUDA. */
+int qmv_quantize_x(int x_dtype, int64_t batch, int64_t cols, const void *x, void *xq, cudaStream_t stream);
+
+/* The activation-quantized product (the runtime's CPU path, which multiplies in quantized
+ * space; minfer "02 - GGUF load" page): W as for qmv_matvec; xq the Q8_0 / f32-scale image of
+ * batch x cols activations as qmv_quantize_x writes it (device, 16-byte aligned).  For each
+ * vector v, row r and block b:
+ *   isum = sum_j level_w[r][32b + j] * q_x[v][32b + j]   (exact integer),
+ *   y[v][r] = sum_b (d_w[r][b] * d_x[v][b]) * isum        (float32 products and sums),
+ * y device, batch x rows float32, row-major, 4-byte aligned, fully overwritten.  Results agree
+ * with an exact evaluation to within 1e-3 * sum_b |d_w d_x| sum_j |level_w q_x| per output and
+ * do not depend on timing.  Runs in passes of up to 8 vectors (dp4a integer dot products, one
+ * warp per 1, 2 or 4 rows).  batch 0 launches nothing.  Asynchronous.  Returns as qmv_matvec. */
+int qmv_matvec_qx(int wtype, int scale_dtype, int64_t rows, int64_t cols, const void *W, const void *xq,
+                  float *y, int batch, cudaStream_t stream);
+
 /* Synchronizes the current device, then returns and clears the status word that the
  * kernels set when a bounded wait runs out (QMV_E_TIMEOUT); QMV_OK when none was set,
  * QMV_E_CUDA when the device reports a CUDA error. */

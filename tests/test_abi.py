@@ -102,6 +102,27 @@ def test_dequant_and_validate_argument_errors(lib):
     assert lib.qmv_quantize(2, 1, 64, 64, FAKE + 4, FAKE, FAKE, None) == binding.E_ALIGN
     assert lib.qmv_quantize(2, 1, 64, 64, FAKE, FAKE + 8, FAKE, None) == binding.E_ALIGN
     assert lib.qmv_quantize(2, 1, 64, 64, FAKE, FAKE, FAKE + 4, None) == binding.E_ALIGN
+    # qmv_quantize_x: dtype, shape, batch, null and alignment checks before any launch
+    assert lib.qmv_quantize_x(2, 1, 64, FAKE, FAKE, None) == binding.E_FORMAT
+    assert lib.qmv_quantize_x(0, 1, 48, FAKE, FAKE, None) == binding.E_SHAPE
+    assert lib.qmv_quantize_x(0, 1, 0, FAKE, FAKE, None) == binding.E_SHAPE
+    assert lib.qmv_quantize_x(0, -1, 64, FAKE, FAKE, None) == binding.E_ARG
+    assert lib.qmv_quantize_x(1, 0, 64, 0, 0, None) == binding.OK          # batch 0: nothing to do
+    assert lib.qmv_quantize_x(0, 2, 64, 0, FAKE, None) == binding.E_ARG
+    assert lib.qmv_quantize_x(1, 2, 64, FAKE, 0, None) == binding.E_ARG
+    assert lib.qmv_quantize_x(0, 2, 64, FAKE + 8, FAKE, None) == binding.E_ALIGN
+    assert lib.qmv_quantize_x(0, 2, 64, FAKE, FAKE + 4, None) == binding.E_ALIGN
+    # qmv_matvec_qx: the matrix checks of qmv_matvec, then the activation image and y
+    assert lib.qmv_matvec_qx(3, 0, 64, 64, FAKE, FAKE, FAKE, 1, None) == binding.E_FORMAT
+    assert lib.qmv_matvec_qx(2, 1, 64, 48, FAKE, FAKE, FAKE, 1, None) == binding.E_SHAPE
+    assert lib.qmv_matvec_qx(2, 1, 64, 64, 0, FAKE, FAKE, 1, None) == binding.E_ARG
+    assert lib.qmv_matvec_qx(2, 1, 64, 64, FAKE + 8, FAKE, FAKE, 1, None) == binding.E_ALIGN
+    assert lib.qmv_matvec_qx(2, 1, 64, 64, FAKE, FAKE, FAKE, -1, None) == binding.E_ARG
+    assert lib.qmv_matvec_qx(2, 1, 64, 64, FAKE, 0, 0, 0, None) == binding.OK   # batch 0
+    assert lib.qmv_matvec_qx(2, 1, 64, 64, FAKE, 0, FAKE, 1, None) == binding.E_ARG
+    assert lib.qmv_matvec_qx(1, 0, 64, 64, FAKE, FAKE, 0, 1, None) == binding.E_ARG
+    assert lib.qmv_matvec_qx(2, 1, 64, 64, FAKE, FAKE + 8, FAKE, 1, None) == binding.E_ALIGN
+    assert lib.qmv_matvec_qx(2, 1, 64, 64, FAKE, FAKE, FAKE + 2, 1, None) == binding.E_ALIGN
 
 
 def test_strerror_never_null(lib):

@@ -1,0 +1,181 @@
+"""The activation-quantized product on the device vs the oracle.
+
+qmv_quantize_x must give the oracle's activation image byte for byte (the Q8_0 rule decides
+integers, and both sides take it in float32 round-to-nearest operations); qmv_matvec_qx must
+agree with the oracle's exact evaluation to within the product's tolerance, and exactly
+where every float32 step is exact.  Shapes cover one, two and four rows per warp, rows that
+do not fill the last warp, block counts that do not fill the lanes, passes of 1, 2, 4 and 8
+vectors and batches that take two passes; full-size matrices are checked on sampled rows.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from block_quantized_weight_q4_gb300 import inputs
+from helpers import assert_bits_equal, check_product, dev_u8, dev_x
+
+pytestmark = pytest.mark.gpu
+
+TYPES = [(1, 0), (1, 1), (2, 0), (2, 1)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def qmv():
+    import torch
+    from block_quantized_weight_q4_gb300.build import build
+    import block_quantized_weight_q4_gb300 as q
+    assert torch.cuda.is_available()
+    build()
+    q.load_library()
+    yield q
+    assert q.last_error() == 0
+
+
+def gpu_quantize_x(q, x):
+    import torch
+    xq = q.quantize_x(dev_x(x))
+    torch.cuda.synchronize()
+    return xq
+
+
+def gpu_qx(q, m, xq_dev, batch):
+    import torch
+    y = q.matvec_qx(m.wtype, m.scale_f16, m.rows, m.cols, dev_u8(m.W), xq_dev, batch)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+def sub_matrix(m, ids):
+    """The byte image of the listed rows of m (for checking full-size results row by row)."""
+    ids = np.asarray(ids)
+    qb = m.cols if m.wtype == 1 else m.cols // 2
+    q = m.q.reshape(m.rows, qb)[ids]
+    return inputs.assemble(m.wtype, m.scale_f16, ids.size, m.cols, q, m.d_codes[ids])
+
+
+def activations(rng, batch, cols):
+    # N(0, 1) with a per-block magnitude spread, plus blocks that probe the rule: all zero,
+    # amax below the 1e-30 floor, and halves (rounded away from zero)
+    x = (rng.standard_normal((batch, cols)) * np.exp(rng.uniform(-4, 4, (batch, cols // 32))).repeat(32, 1))
+    x = x.astype(np.float32)
+    nb = cols // 32
+    if nb >= 4:
+        x[0, 0:32] = 0.0
+        x[-1, 32:64] = rng.standard_normal(32) * 1e-31
+        x[0, 64:96] = np.arange(-16, 16) + 0.5
+    return x
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+@pytest.mark.parametrize("batch,cols", [(1, 32), (3, 96), (8, 4096), (5, 11008), (2, 14336)])
+def test_quantize_x_matches_oracle(qmv, bf16, batch, cols):
+    rng = np.random.default_rng(batch * 31 + cols + bf16)
+    x = activations(rng, batch, cols)
+    xin = inputs.bf16_codes(x) if bf16 else x
+    got = gpu_quantize_x(qmv, xin).cpu().numpy()
+    want = oracle.quantize_x(xin)
+    assert got.shape == want.shape
+    bad = np.flatnonzero(got != want)
+    assert bad.size == 0, f"{bad.size} bytes differ, first at {bad[:8]}"
+
+
+@pytest.mark.parametrize("wt,sf", TYPES)
+@pytest.mark.parametrize("rows,cols,batch", [(1, 32, 1), (5, 96, 2), (37, 1024, 3), (100, 4128, 4),
+                                             (300, 4096, 8), (70, 2048, 11)])
+def test_matvec_qx_matches_oracle(qmv, wt, sf, rows, cols, batch):
+    rng = np.random.default_rng(rows + cols + batch + 10 * wt + sf)
+    m = inputs.make_matrix(wt, sf, rows, cols, seed=rows * 3 + cols)
+    x = activations(rng, batch, cols)
+    xq_host = oracle.quantize_x(x)
+    y = gpu_qx(qmv, m, dev_u8(xq_host), batch)
+    y_ref, absref = oracle.matvec_qx(m.W, wt, sf, rows, cols, xq_host, batch)
+    check_product(y, y_ref, absref, what=f"qx {wt},{sf} {rows}x{cols} b{batch}")
+    check_product(y, y_ref, absref, tol=1e-4, what=f"qx tight {wt},{sf} {rows}x{cols} b{batch}")
+
+
+@pytest.mark.parametrize("wt", [1, 2])
+@pytest.mark.parametrize("batch", [1, 2, 3, 8])
+def test_matvec_qx_exact_case(qmv, wt, batch):
+    # power-of-two weight scales and activations k * 2^e (one element per block at +-127):
+    # every block term (d_w d_x) * isum is an integer times 2^-10 below 2^24 units, and so is
+    # every partial sum, so the float32 result is exact in any order
+    rows, cols = 9, 128
+    rng = np.random.default_rng(80 + wt + batch)
+    if wt == 1:
+        q = rng.integers(-127, 128, rows * cols).astype(np.int8).view(np.uint8)
+    else:
+        q = rng.integers(0, 256, rows * cols // 2).astype(np.uint8)
+    d = np.full(rows * cols // 32, 2.0 ** -6, np.float32).view(np.uint32)
+    W = inputs.assemble(wt, 0, rows, cols, q, d)
+    m = inputs.Matrix(wt, 0, rows, cols, W, q, d.reshape(rows, cols // 32))
+    k = rng.integers(-127, 128, (batch, cols // 32, 32))
+    k[:, :, 3] = 127
+    x = (k * 2.0 ** -4).reshape(batch, cols).astype(np.float32)
+    xq_host = oracle.quantize_x(x)
+    y = gpu_qx(qmv, m, dev_u8(xq_host), batch)
+    y_ref, _ = oracle.matvec_qx(W, wt, 0, rows, cols, xq_host, batch)
+    assert_bits_equal(y, y_ref.astype(np.float32), f"exact qx {wt} b{batch}")
+    assert np.array_equal(y.astype(np.float64), y_ref)
+
+
+@pytest.mark.parametrize("wt,sf,rows,cols,batch", [
+    (2, 1, 65536, 4096, 1),    # four rows per warp
+    (2, 1, 65536, 4096, 2),
+    (2, 1, 14336, 4096, 3),    # two rows per warp, a pass of 4 with one repeated vector
+    (1, 0, 11008, 4096, 8),    # Q8_0, two rows per warp
+    (2, 0, 4096, 11008, 1),    # one row per warp, 344 blocks per row
+    (1, 1, 151936, 1024, 1),   # the Q8_0 classifier shape
+])
+def test_matvec_qx_full_size_sampled_rows(qmv, wt, sf, rows, cols, batch):
+    import torch
+    rng = np.random.default_rng(rows + batch)
+    m = inputs.make_matrix(wt, sf, rows, cols, seed=rows + cols + wt)
+    x = activations(rng, batch, cols)
+    xq = qmv.quantize_x(dev_x(x))
+    y = qmv.matvec_qx(wt, sf, rows, cols, dev_u8(m.W), xq, batch)
+    torch.cuda.synchronize()
+    y = y.cpu().numpy()
+    xq_host = xq.cpu().numpy()
+    assert np.array_equal(xq_host, oracle.quantize_x(x))
+    ids = np.unique(np.concatenate([np.arange(8), rows - 1 - np.arange(8), rng.integers(0, rows, 48)]))
+    y_ref, absref = oracle.matvec_qx(sub_matrix(m, ids), wt, sf, ids.size, cols, xq_host, batch)
+    check_product(y[:, ids], y_ref, absref, what=f"full {wt},{sf} {rows}x{cols} b{batch}")
+    check_product(y[:, ids], y_ref, absref, tol=1e-4, what=f"full tight {wt},{sf} {rows}x{cols} b{batch}")
+
+
+def test_matvec_qx_repeat_and_graph_are_bit_identical(qmv):
+    import torch
+    rows, cols, batch = 14336, 4096, 2
+    m = inputs.make_matrix(2, 1, rows, cols, seed=5)
+    x = activations(np.random.default_rng(6), batch, cols)
+    W = dev_u8(m.W)
+    xd = dev_x(x)
+    xq = qmv.quantize_x(xd)
+    y1 = qmv.matvec_qx(2, 1, rows, cols, W, xq, batch).clone()
+    y2 = torch.empty_like(y1)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        qmv.quantize_x(xd, xq=xq, stream=s)
+        qmv.matvec_qx(2, 1, rows, cols, W, xq, batch, y=y2, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    y3 = torch.empty_like(y1)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        qmv.quantize_x(xd, xq=xq)
+        qmv.matvec_qx(2, 1, rows, cols, W, xq, batch, y=y3)
+    for _ in range(3):
+        y3.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    assert_bits_equal(y1.cpu().numpy(), y2.cpu().numpy(), "stream")
+    assert_bits_equal(y1.cpu().numpy(), y3.cpu().numpy(), "graph replay")
+
+
+def test_matvec_qx_empty_batch_and_y_untouched(qmv):
+    import torch
+    m = inputs.make_matrix(2, 1, 64, 64, seed=1)
+    y = torch.full((0, 64), 7.0, device="cuda")
+    out = qmv.matvec_qx(2, 1, 64, 64, dev_u8(m.W), torch.empty(0, dtype=torch.uint8, device="cuda"), 0, y=y)
+    torch.cuda.synchronize()
+    assert out.shape == (0, 64)
