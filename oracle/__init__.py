@@ -84,6 +84,10 @@ def _load():
     lib.oracle_quantize_x.argtypes = [i32, i64, i64, vp, vp]
     lib.oracle_matvec_qx.restype = i32
     lib.oracle_matvec_qx.argtypes = [i32, i32, i64, i64, vp, vp, i32, vp, vp]
+    lib.oracle_gguf_bytes.restype = i64
+    lib.oracle_gguf_bytes.argtypes = [i32, i64, i64]
+    lib.oracle_gguf_to_mlb.restype = i32
+    lib.oracle_gguf_to_mlb.argtypes = [i32, i64, i64, vp, vp]
     _lib = lib
     return lib
 
@@ -231,3 +235,19 @@ def matvec_qx(W: np.ndarray, wtype: int, scale_f16: int, rows: int, cols: int, x
     if st != OK:
         raise ValueError(f"oracle_matvec_qx status {st}")
     return y, a
+
+
+def gguf_bytes(wtype: int, rows: int, cols: int) -> int:
+    """Bytes of a rows x cols tensor in GGUF interleaved blocks (18 / 34 bytes per block)."""
+    return int(_load().oracle_gguf_bytes(wtype, rows, cols))
+
+
+def gguf_to_mlb(gguf: np.ndarray, wtype: int, rows: int, cols: int) -> np.ndarray:
+    """The two-array image (f16 scales) of a tensor given in GGUF interleaved blocks."""
+    gguf = np.ascontiguousarray(gguf, dtype=np.uint8)
+    assert gguf.size >= gguf_bytes(wtype, rows, cols)
+    W = np.zeros(weight_bytes(wtype, 1, rows, cols), dtype=np.uint8)
+    st = _load().oracle_gguf_to_mlb(wtype, rows, cols, _ptr(gguf), _ptr(W))
+    if st != OK:
+        raise ValueError(f"oracle_gguf_to_mlb status {st}")
+    return W

@@ -29,6 +29,8 @@
  *   oracle_matvec_qx                          : pinned (equals the plain product on exactly
  *                                               representable activations; equals the product
  *                                               with the dequantized activations; a hand block)
+ *   oracle_gguf_bytes                         : pinned (the minfer page's GGUF tensor sizes)
+ *   oracle_gguf_to_mlb                        : pinned (hand blocks written as GGUF records)
  *   corner readings of the writers (f16 scale that rounds to 0, all-zero Q4 block,
  *   ties of the largest magnitude) : parity unpinned (writer-only, not on the product path)
  */
@@ -510,6 +512,49 @@ int oracle_matvec_qx(int wtype, int scale_f16, int64_t rows, int64_t cols, const
             }
             y[(int64_t)b * rows + r] = acc;
             absref[(int64_t)b * rows + r] = acc_abs;
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* ---------------------------------------------------------------------------
+ * GGUF interleaved blocks (minfer "02 - GGUF load" page, §2.3-2.4): a Q4_0 block is an f16
+ * scale d followed by 16 bytes of nibbles (18 bytes), a Q8_0 block d followed by 32 int8
+ * quants (34 bytes); a row of cols values is cols/32 consecutive blocks (row stride
+ * (cols/32) * block bytes), rows follow one another with no padding.  Reading: the nibble
+ * order inside qs is the Krafla page's Q4_0 order (byte j: element j low, element j + 16
+ * high); the pages do not restate it for GGUF.
+ * ------------------------------------------------------------------------- */
+
+/* Bytes of a rows x cols tensor in GGUF blocks; -1 for invalid arguments. */
+int64_t oracle_gguf_bytes(int wtype, int64_t rows, int64_t cols)
+{
+    int64_t q, off, dsz;
+    if (layout(wtype, 1, rows, cols, &q, &off, &dsz) != ORACLE_OK) return -1;
+    int64_t block_bytes = (wtype == ORACLE_Q8_0) ? 34 : 18;
+    return rows * (cols / 32) * block_bytes;
+}
+
+/* The same matrix in the two-array layout with f16 scales (W must hold
+ * oracle_weight_bytes(wtype, 1, rows, cols) bytes; its padding is written as zeros): block
+ * k of row r is the GGUF record at (r * (cols/32) + k) * block bytes; its first two bytes
+ * are d (little-endian f16 code), the rest its quants, copied unchanged. */
+int oracle_gguf_to_mlb(int wtype, int64_t rows, int64_t cols, const uint8_t *gguf, uint8_t *W)
+{
+    int64_t q, off, dsz;
+    int st = layout(wtype, 1, rows, cols, &q, &off, &dsz);
+    if (st != ORACLE_OK) return st;
+    memset(W, 0, (size_t)(off + dsz));
+    int64_t nblk = cols / 32;
+    int64_t qb = (wtype == ORACLE_Q8_0) ? 32 : 16;
+    int64_t block_bytes = 2 + qb;
+    for (int64_t r = 0; r < rows; r++) {
+        for (int64_t k = 0; k < nblk; k++) {
+            const uint8_t *rec = gguf + (r * nblk + k) * block_bytes;
+            int64_t idx = r * nblk + k;
+            W[off + 2 * idx] = rec[0];
+            W[off + 2 * idx + 1] = rec[1];
+            for (int64_t j = 0; j < qb; j++) W[idx * qb + j] = rec[2 + j];
         }
     }
     return ORACLE_OK;

@@ -48,6 +48,12 @@ MUTANTS = {
     "qx_x_scale_byte_order": ("xq[off + 4 * idx + i] = (uint8_t)((bits >> (8 * i)) & 0xff);",
                               "xq[off + 4 * idx + i] = (uint8_t)((bits >> (8 * (3 - i))) & 0xff);"),
     "q8_rule_without_half": ("float u = t + copysignf(0.5f, x[j]);", "float u = t;"),
+    "gguf_record_without_d": ("int64_t block_bytes = 2 + qb;", "int64_t block_bytes = qb;"),
+    "gguf_d_bytes_swapped": ("W[off + 2 * idx] = rec[0];\n            W[off + 2 * idx + 1] = rec[1];",
+                             "W[off + 2 * idx] = rec[1];\n            W[off + 2 * idx + 1] = rec[0];"),
+    "gguf_quants_at_record_start": ("W[idx * qb + j] = rec[2 + j];", "W[idx * qb + j] = rec[j];"),
+    "gguf_q8_block_32": ("int64_t block_bytes = (wtype == ORACLE_Q8_0) ? 34 : 18;",
+                         "int64_t block_bytes = (wtype == ORACLE_Q8_0) ? 32 : 18;"),
 }
 
 
@@ -71,6 +77,10 @@ class Orc:
         lib.oracle_quantize_x.argtypes = [i32, i64, i64, vp, vp]
         lib.oracle_matvec_qx.restype = i32
         lib.oracle_matvec_qx.argtypes = [i32, i32, i64, i64, vp, vp, i32, vp, vp]
+        lib.oracle_gguf_bytes.restype = i64
+        lib.oracle_gguf_bytes.argtypes = [i32, i64, i64]
+        lib.oracle_gguf_to_mlb.restype = i32
+        lib.oracle_gguf_to_mlb.argtypes = [i32, i64, i64, vp, vp]
         self.lib = lib
 
     def dequant(self, W, wt, sf, rows, cols):
@@ -158,6 +168,21 @@ def pin_checks(o):
     xh = np.zeros((1, 32), np.float32)
     xh[0, 0], xh[0, 1] = 127.0, -63.5
     yield "qx_hand", o.matvec_qx(W, 2, 0, 1, 32, o.quantize_x(xh), 1)[0][0, 0] == 31.5
+    # GGUF: the page's tensor sizes, and records with d = 2^(3r + k), levels +1
+    for wt, rows, cols, expect, *_ in read_rows("gguf_sizes.txt"):
+        yield "gguf_size", o.lib.oracle_gguf_bytes(int(wt), int(rows), int(cols)) == int(expect)
+    for wt in (1, 2):
+        qb = 32 if wt == 1 else 16
+        recs = []
+        for r in range(3):
+            for k in range(3):
+                code = int(np.array([2.0 ** (3 * r + k)], np.float16).view(np.uint16)[0])
+                recs += [code & 0xFF, code >> 8] + [1 if wt == 1 else 0x99] * qb
+        g = np.array(recs + [0] * 256, np.uint8)       # slack: a mutated record size stays in bounds
+        Wg = np.zeros(4096, np.uint8)
+        assert o.lib.oracle_gguf_to_mlb(wt, 3, 96, g.ctypes.data, Wg.ctypes.data) == 0
+        exp = np.array([[2.0 ** (3 * r + c // 32) for c in range(96)] for r in range(3)], np.float32)
+        yield "gguf_records", bool(np.array_equal(o.dequant(Wg, wt, 1, 3, 96), exp))
 
 
 def build_variant(tmp, name, text):

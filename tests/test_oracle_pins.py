@@ -483,3 +483,43 @@ def test_matvec_qx_batch_rows_are_independent():
     for b in range(3):
         yb, _ = oracle.matvec_qx(m.W, 2, 1, rows, cols, oracle.quantize_x(x[b:b + 1]), 1)
         assert np.array_equal(y[b], yb[0])
+
+
+# ----------------------------------------------------------- GGUF interleaved blocks
+def test_gguf_sizes_match_the_page():
+    for wt, rows, cols, expect, *src in read_rows("gguf_sizes.txt"):
+        assert oracle.gguf_bytes(int(wt), int(rows), int(cols)) == int(expect), " ".join(src)
+
+
+@pytest.mark.parametrize("case", [c for c in read_cases("hand_blocks.txt") if c["scale_f16"][0] == "1"],
+                         ids=lambda c: c["name"])
+def test_gguf_hand_blocks(case):
+    # the hand blocks with f16 scales, written as one GGUF record each: d (little-endian f16
+    # code) then the quant bytes; converted, they must hold the weights worked out by hand
+    wt = int(case["wtype"][0])
+    code = int(case["scale_code"][0], 16)
+    qb = [int(b, 16) for b in case["bytes"]]
+    rec = np.array([code & 0xFF, code >> 8] + qb, np.uint8)
+    assert rec.size == oracle.gguf_bytes(wt, 1, 32)
+    W = oracle.gguf_to_mlb(rec, wt, 1, 32)
+    expect = np.array([float(v) for v in case["weights"]], np.float32)
+    assert np.array_equal(oracle.dequant(W, wt, 1, 1, 32)[0], expect)
+
+
+@pytest.mark.parametrize("wt", [1, 2])
+def test_gguf_record_addressing(wt):
+    # record (r, k) of a 3 x 96 tensor: d = 2^(3r + k), every weight level +1 (Q4_0 byte 0x99,
+    # Q8_0 byte 1), so w[r][c] = 2^(3r + c // 32): checks the record stride, row stride and
+    # the place of d in the record
+    rows, cols = 3, 96
+    qb = 32 if wt == 1 else 16
+    recs = []
+    for r in range(rows):
+        for k in range(cols // 32):
+            code = int(np.array([2.0 ** (3 * r + k)], np.float16).view(np.uint16)[0])
+            recs += [code & 0xFF, code >> 8] + [1 if wt == 1 else 0x99] * qb
+    g = np.array(recs, np.uint8)
+    assert g.size == oracle.gguf_bytes(wt, rows, cols)
+    W = oracle.gguf_to_mlb(g, wt, rows, cols)
+    expect = np.array([[2.0 ** (3 * r + c // 32) for c in range(cols)] for r in range(rows)], np.float32)
+    assert np.array_equal(oracle.dequant(W, wt, 1, rows, cols), expect)
