@@ -380,6 +380,23 @@ def other_workloads(torch, qmv, dev, l2, cap, peak_hbm, peak_tf):
         del W
     del src
 
+    # GGUF interleaved blocks into the two-array layout: the page's 151,936 x 896 tensors
+    # (Q8_0 output.weight, Q4_0 token_embd.weight); bytes = the tensor read + the same written;
+    # source / destination pairs rotate past 4x L2
+    rows, cols = 151936, 896
+    for wt, name in ((1, "q8_0"), (2, "q4_0")):
+        gb = qmv.gguf_bytes(wt, rows, cols)
+        moved = gb + qmv.weight_bytes(wt, 1, rows, cols)
+        npair = max(2, -(-4 * l2 // moved) + 1)
+        gs = [torch.randint(0, 256, (gb,), dtype=torch.uint8, device=dev) for _ in range(npair)]
+        Wd = [torch.empty(qmv.weight_bytes(wt, 1, rows, cols), dtype=torch.uint8, device=dev) for _ in range(npair)]
+        us = _graph_time_us(torch, [lambda wt=wt, i=i: qmv.gguf_to_mlb(wt, rows, cols, gs[i % npair], W=Wd[i % npair])
+                                    for i in range(2 * npair)], cap)
+        res[f"gguf_to_mlb_{rows}x{cols}_{name}"] = {
+            "us": round(us, 3), "gbs": round(moved / us / 1e3, 1), "frac_hbm": round(moved / us / 1e3 / peak_hbm, 4),
+            "bytes": moved}
+        del gs, Wd
+
     # the activation-quantized product (activations to Q8_0 blocks by qmv_quantize_x, then exact
     # int8 block dot products by qmv_matvec_qx): Q4_0 65536 x 4096 alone, batch 1 and 8, and
     # the Llama-7B layer step with one quantized activation vector per dependency group

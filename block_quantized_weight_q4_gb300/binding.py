@@ -68,6 +68,10 @@ def load_library():
     lib.qmv_validate.argtypes = [i32, i32, i64, i64, vp, vp, vp]
     lib.qmv_quantize.restype = i32
     lib.qmv_quantize.argtypes = [i32, i32, i64, i64, vp, vp, vp, vp]
+    lib.qmv_gguf_bytes.restype = ctypes.c_size_t
+    lib.qmv_gguf_bytes.argtypes = [i32, i64, i64]
+    lib.qmv_gguf_to_mlb.restype = i32
+    lib.qmv_gguf_to_mlb.argtypes = [i32, i64, i64, vp, vp, vp]
     lib.qmv_quantize_x.restype = i32
     lib.qmv_quantize_x.argtypes = [i32, i64, i64, vp, vp, vp]
     lib.qmv_matvec_qx.restype = i32
@@ -221,6 +225,22 @@ def quantize(wtype: int, scale_dtype: int, src, W=None, stream=None):
                                      _stream(stream))
     _check(st, "qmv_quantize")
     return W, int(first.item())
+
+
+def gguf_bytes(wtype: int, rows: int, cols: int) -> int:
+    """Bytes of a rows x cols tensor in GGUF interleaved blocks (0 when invalid)."""
+    return int(load_library().qmv_gguf_bytes(wtype, rows, cols))
+
+
+def gguf_to_mlb(wtype: int, rows: int, cols: int, src, W=None, stream=None):
+    """A tensor in GGUF interleaved blocks (uint8 CUDA tensor) into the two-array layout with
+    f16 scales (uint8 CUDA tensor of weight_bytes(wtype, SCALE_F16, rows, cols)).  Returns W."""
+    import torch
+    if W is None:
+        W = torch.empty(max(weight_bytes(wtype, SCALE_F16, rows, cols), 0), dtype=torch.uint8, device=src.device)
+    st = load_library().qmv_gguf_to_mlb(wtype, rows, cols, src.data_ptr(), W.data_ptr(), _stream(stream))
+    _check(st, "qmv_gguf_to_mlb")
+    return W
 
 
 def quantize_x(x, xq=None, stream=None):

@@ -315,6 +315,30 @@ int qmv_quantize(int wtype, int scale_dtype, int64_t rows, int64_t cols, const f
              : QMV_E_CUDA;
 }
 
+size_t qmv_gguf_bytes(int wtype, int64_t rows, int64_t cols) {
+  Layout L;
+  if (make_layout(wtype, QMV_SCALE_F16, rows, cols, &L) != QMV_OK) return 0;
+  const int64_t nrec = rows * (cols / 32);
+  const int64_t rec = wtype == QMV_Q8_0 ? 34 : 18;
+  if (nrec > INT64_MAX / rec) return 0;
+  return (size_t)(nrec * rec);
+}
+
+int qmv_gguf_to_mlb(int wtype, int64_t rows, int64_t cols, const void* src, void* W, cudaStream_t stream) {
+  Layout L;
+  const int st = make_layout(wtype, QMV_SCALE_F16, rows, cols, &L);
+  if (st != QMV_OK) return st;
+  if (qmv_gguf_bytes(wtype, rows, cols) == 0) return QMV_E_SHAPE;
+  if (src == nullptr || W == nullptr) return QMV_E_ARG;
+  if (!aligned(src, 16) || !aligned(W, 16)) return QMV_E_ALIGN;
+  DeviceInfo dev;
+  if (current_device_info(&dev) != cudaSuccess) return QMV_E_CUDA;
+  return launch_gguf_to_mlb(wtype, rows, cols, src, static_cast<uint8_t*>(W), L.d_off, L.q_bytes, dev, stream) ==
+                 cudaSuccess
+             ? QMV_OK
+             : QMV_E_CUDA;
+}
+
 int qmv_quantize_x(int x_dtype, int64_t batch, int64_t cols, const void* x, void* xq, cudaStream_t stream) {
   if (x_dtype != QMV_X_F32 && x_dtype != QMV_X_BF16) return QMV_E_FORMAT;
   if (batch < 0) return QMV_E_ARG;

@@ -233,6 +233,23 @@ int qmv_validate(int wtype, int scale_dtype, int64_t rows, int64_t cols, const v
 int qmv_quantize(int wtype, int scale_dtype, int64_t rows, int64_t cols, const float *src, void *W,
                  int64_t *first_bad, cudaStream_t stream);
 
+/* Size in bytes of a rows x cols tensor stored as GGUF interleaved blocks (minfer "02 - GGUF
+ * load" page, §2.3-2.4): rows * cols/32 records of 18 bytes (Q4_0: f16 d, then 16 bytes of
+ * nibbles) or 34 bytes (Q8_0: f16 d, then 32 int8 quants), a row being cols/32 consecutive
+ * records.  0 for invalid arguments. */
+size_t qmv_gguf_bytes(int wtype, int64_t rows, int64_t cols);
+
+/* A tensor in GGUF interleaved blocks (src, device, 16-byte aligned, qmv_gguf_bytes() bytes)
+ * into the two-array layout with f16 scales at W (device, 16-byte aligned,
+ * qmv_weight_bytes(wtype, QMV_SCALE_F16, rows, cols) bytes; the padding between the arrays is
+ * written as zeros), the layout every product entry point reads.  Bytes are moved, not decoded:
+ * record k of row r gives q block r*cols/32 + k (its quants, unchanged; for Q4_0 the nibble
+ * order is the Krafla page's: byte j holds element j low, element j + 16 high) and that
+ * block's scale (its f16 code, unchanged).  src and W must not overlap.  Asynchronous.
+ * Returns QMV_OK, QMV_E_FORMAT (wtype), QMV_E_SHAPE, QMV_E_ARG (null pointer), QMV_E_ALIGN, or
+ * QMV_E_CUDA. */
+int qmv_gguf_to_mlb(int wtype, int64_t rows, int64_t cols, const void *src, void *W, cudaStream_t stream);
+
 /* The runtime's activation quantizer (Krafla page, "Quantization rule": the writer's Q8_0
  * operations, applied by the runtime to its activations; f32 scale): x (device, batch x cols,
  * x_dtype QMV_X_F32 or QMV_X_BF16, row-major, 16-byte aligned; bfloat16 is widened to float32

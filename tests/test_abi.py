@@ -102,6 +102,18 @@ def test_dequant_and_validate_argument_errors(lib):
     assert lib.qmv_quantize(2, 1, 64, 64, FAKE + 4, FAKE, FAKE, None) == binding.E_ALIGN
     assert lib.qmv_quantize(2, 1, 64, 64, FAKE, FAKE + 8, FAKE, None) == binding.E_ALIGN
     assert lib.qmv_quantize(2, 1, 64, 64, FAKE, FAKE, FAKE + 4, None) == binding.E_ALIGN
+    # qmv_gguf_bytes / qmv_gguf_to_mlb: sizes, then shape, format, null and alignment checks
+    assert lib.qmv_gguf_bytes(1, 151936, 896) == 144643072
+    assert lib.qmv_gguf_bytes(2, 151936, 896) == 76575744
+    assert lib.qmv_gguf_bytes(2, 1, 896) == 504
+    assert lib.qmv_gguf_bytes(2, 1, 48) == 0 and lib.qmv_gguf_bytes(3, 1, 32) == 0
+    assert lib.qmv_gguf_to_mlb(3, 4, 64, FAKE, FAKE, None) == binding.E_FORMAT
+    assert lib.qmv_gguf_to_mlb(2, 4, 48, FAKE, FAKE, None) == binding.E_SHAPE
+    assert lib.qmv_gguf_to_mlb(2, 0, 64, FAKE, FAKE, None) == binding.E_SHAPE
+    assert lib.qmv_gguf_to_mlb(2, 4, 64, 0, FAKE, None) == binding.E_ARG
+    assert lib.qmv_gguf_to_mlb(1, 4, 64, FAKE, 0, None) == binding.E_ARG
+    assert lib.qmv_gguf_to_mlb(2, 4, 64, FAKE + 2, FAKE, None) == binding.E_ALIGN
+    assert lib.qmv_gguf_to_mlb(2, 4, 64, FAKE, FAKE + 8, None) == binding.E_ALIGN
     # qmv_quantize_x: dtype, shape, batch, null and alignment checks before any launch
     assert lib.qmv_quantize_x(2, 1, 64, FAKE, FAKE, None) == binding.E_FORMAT
     assert lib.qmv_quantize_x(0, 1, 48, FAKE, FAKE, None) == binding.E_SHAPE
