@@ -68,6 +68,12 @@ def load_library():
     lib.qmv_validate.argtypes = [i32, i32, i64, i64, vp, vp, vp]
     lib.qmv_quantize.restype = i32
     lib.qmv_quantize.argtypes = [i32, i32, i64, i64, vp, vp, vp, vp]
+    lib.qmv_step_create.restype = i32
+    lib.qmv_step_create.argtypes = [vp, i32, vp, i32, vp, i32, ctypes.POINTER(vp)]
+    lib.qmv_step_run.restype = i32
+    lib.qmv_step_run.argtypes = [vp, vp]
+    lib.qmv_step_destroy.restype = i32
+    lib.qmv_step_destroy.argtypes = [vp]
     lib.qmv_gguf_bytes.restype = ctypes.c_size_t
     lib.qmv_gguf_bytes.argtypes = [i32, i64, i64]
     lib.qmv_gguf_to_mlb.restype = i32
@@ -189,6 +195,66 @@ def matvec_grouped_noalloc(wtype: int, scale_dtype: int, problems, overlap: bool
     st = load_library().qmv_matvec_grouped_noalloc(wtype, scale_dtype, xdt, batch, ctypes.addressof(arr), n,
                                                    FLAG_OVERLAP if overlap else 0, _stream(stream))
     _check(st, "qmv_matvec_grouped_noalloc")
+
+
+class Copy(ctypes.Structure):
+    """qmv_copy of include/qmv.h."""
+    _fields_ = [("dst", ctypes.c_void_p), ("src", ctypes.c_void_p), ("bytes", ctypes.c_size_t)]
+
+
+class Group(ctypes.Structure):
+    """qmv_group of include/qmv.h."""
+    _fields_ = [("wtype", ctypes.c_int), ("scale_dtype", ctypes.c_int), ("x_dtype", ctypes.c_int),
+                ("batch", ctypes.c_int), ("problems", ctypes.c_void_p), ("n", ctypes.c_int),
+                ("flags", ctypes.c_uint)]
+
+
+def _copies(pairs):
+    arr = (Copy * max(len(pairs), 1))()
+    for i, (dst, src) in enumerate(pairs):
+        nbytes = src.numel() * src.element_size()
+        if dst.numel() * dst.element_size() != nbytes or not (dst.is_contiguous() and src.is_contiguous()):
+            raise ValueError("a copy needs contiguous tensors of equal size")
+        arr[i] = Copy(dst.data_ptr(), src.data_ptr(), nbytes)
+    return arr
+
+
+class Step:
+    """A compiled step (qmv_step_create): `before` copies, product groups, `after` copies,
+    recorded once as a CUDA graph; run() enqueues it with one library call.
+
+    before / after: lists of (dst, src) tensors (device or pinned host); groups: list of
+    (wtype, scale_dtype, problems, overlap) with problems as for matvec_grouped.  Creating the
+    step runs it once.  The tensors are kept alive with the step; a run reads and writes the
+    same buffers.  Runs of one step must not overlap in time."""
+
+    def __init__(self, groups, before=(), after=()):
+        keep = [list(before), list(after)]
+        garr = (Group * max(len(groups), 1))()
+        for i, (wtype, scale_dtype, problems, overlap) in enumerate(groups):
+            parr, n, batch, xdt = _problem_array(problems)
+            keep.append((parr, problems))
+            garr[i] = Group(wtype, scale_dtype, xdt, batch, ctypes.addressof(parr), n,
+                            FLAG_OVERLAP if overlap else 0)
+        b, a = _copies(list(before)), _copies(list(after))
+        handle = ctypes.c_void_p()
+        st = load_library().qmv_step_create(ctypes.addressof(b), len(before), ctypes.addressof(garr), len(groups),
+                                            ctypes.addressof(a), len(after), ctypes.byref(handle))
+        _check(st, "qmv_step_create")
+        self._handle = handle
+        self._keep = keep
+
+    def run(self, stream=None):
+        if self._handle is None:
+            raise ValueError("step destroyed")
+        _check(load_library().qmv_step_run(self._handle, _stream(stream)), "qmv_step_run")
+
+    def close(self):
+        if self._handle is not None:
+            st = load_library().qmv_step_destroy(self._handle)
+            self._handle = None
+            self._keep = None
+            _check(st, "qmv_step_destroy")
 
 
 def dequant(wtype: int, scale_dtype: int, rows: int, cols: int, W, out=None, stream=None):

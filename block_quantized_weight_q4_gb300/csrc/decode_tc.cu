@@ -216,6 +216,28 @@ cudaError_t reset_workspaces() {
   return cudaDeviceSynchronize();
 }
 
+cudaError_t prepare_stream_workspaces(const DeviceInfo& dev, cudaStream_t stream) {
+  Workspace w;
+  cudaError_t err = cached_workspace(g_ws, dev, stream, kStreamWorkspaceBytes, kStreamCounters, &w);
+  if (err != cudaSuccess) return err;
+  err = cached_workspace(g_pws, dev, stream, kPrefillWorkspaceBytes, kPrefillCounters, &w);
+  if (err != cudaSuccess) return err;
+  return cached_workspace(g_xws, dev, stream, kSplitBytes, 0, &w);
+}
+
+cudaError_t release_stream_workspaces(int device, cudaStream_t stream) {
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  cudaError_t first = cudaSuccess;
+  for (auto* cache : {&g_ws, &g_pws, &g_xws}) {
+    auto it = cache->find(std::make_pair(device, stream));
+    if (it == cache->end()) continue;
+    const cudaError_t err = cudaFree(it->second.counters);  // the allocation's base
+    if (err != cudaSuccess && first == cudaSuccess) first = err;
+    cache->erase(it);
+  }
+  return first;
+}
+
 cudaError_t launch_decode_tc(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, int batch, bool pdl,
                              const DeviceInfo& dev, const Workspace& ws, cudaStream_t stream) {
   if (ms[0].wtype == QMV_Q4_0) return dtc::launch_q4(ms, xs, ys, n, batch, false, pdl, dev, ws, stream);

@@ -63,6 +63,9 @@ cudaError_t launch_quantize(int wtype, bool scale_f16, int64_t rows, int64_t col
                             int64_t d_off, int64_t q_bytes, int64_t* first_bad, const DeviceInfo& dev,
                             cudaStream_t stream);
 cudaError_t launch_validate(const MatrixRef& m, int64_t* first_bad, cudaStream_t stream);
+// Create every per-stream workspace of `stream` now (not while it is captured), and free them.
+cudaError_t prepare_stream_workspaces(const DeviceInfo& dev, cudaStream_t stream);
+cudaError_t release_stream_workspaces(int device, cudaStream_t stream);
 // GGUF interleaved records (18-byte Q4_0, 34-byte Q8_0) into the two-array layout with f16
 // scales at W (q at W, d at W + d_off; zeros between q_bytes and d_off).
 cudaError_t launch_gguf_to_mlb(int wtype, int64_t rows, int64_t cols, const void* src, uint8_t* W, int64_t d_off,

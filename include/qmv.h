@@ -275,6 +275,50 @@ int qmv_quantize_x(int x_dtype, int64_t batch, int64_t cols, const void *x, void
 int qmv_matvec_qx(int wtype, int scale_dtype, int64_t rows, int64_t cols, const void *W, const void *xq,
                   float *y, int batch, cudaStream_t stream);
 
+/* A compiled step: copies and grouped products recorded once as a CUDA graph and replayed by
+ * one call (a decode step's host input, its products and its host output, launched together).
+ *   qmv_copy  : bytes from src to dst, any mix of device and pinned host pointers (the
+ *               direction follows from the addresses); pageable host memory is not allowed.
+ *   qmv_group : the arguments of one qmv_matvec_grouped call.
+ * qmv_step_create runs the step once, eagerly, on a private stream (the `before` copies in
+ * order, the groups in order, the `after` copies in order): that run sets up the kernels and
+ * the private stream's workspaces and checks every argument; it then records the same
+ * sequence as a graph.  The products take the kernels an eager call on that stream takes, so a
+ * run's results are bit-identical to the eager calls'.  Pointers are fixed at creation: a run
+ * reads and writes the same buffers (new inputs are new contents of the same buffers).
+ * Returns the status of the first call that failed (as qmv_matvec_grouped, QMV_E_CUDA for a
+ * copy), QMV_E_ARG for null arrays with a positive count or a null `step`; nothing is
+ * recorded then and *step is NULL. */
+typedef struct qmv_copy {
+  void *dst;
+  const void *src;
+  size_t bytes;
+} qmv_copy;
+
+typedef struct qmv_group {
+  int wtype;
+  int scale_dtype;
+  int x_dtype;
+  int batch;
+  const qmv_problem *problems;
+  int n;
+  unsigned flags;
+} qmv_group;
+
+typedef struct qmv_step qmv_step;
+
+int qmv_step_create(const qmv_copy *before, int n_before, const qmv_group *groups, int n_groups,
+                    const qmv_copy *after, int n_after, qmv_step **step);
+
+/* Enqueues one run of the step on `stream` (the graph's launch; asynchronous).  Runs of one
+ * step must not overlap each other (they share its workspaces): issue them on one stream, or
+ * order them.  Returns QMV_OK, QMV_E_ARG (null step) or QMV_E_CUDA. */
+int qmv_step_run(qmv_step *step, cudaStream_t stream);
+
+/* Waits for the device, then frees the step and its workspaces.  NULL is a no-op.  Returns
+ * QMV_OK or QMV_E_CUDA. */
+int qmv_step_destroy(qmv_step *step);
+
 /* Synchronizes the current device, then returns and clears the status word that the
  * kernels set when a bounded wait runs out (QMV_E_TIMEOUT); QMV_OK when none was set,
  * QMV_E_CUDA when the device reports a CUDA error. */

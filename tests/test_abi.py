@@ -102,6 +102,18 @@ def test_dequant_and_validate_argument_errors(lib):
     assert lib.qmv_quantize(2, 1, 64, 64, FAKE + 4, FAKE, FAKE, None) == binding.E_ALIGN
     assert lib.qmv_quantize(2, 1, 64, 64, FAKE, FAKE + 8, FAKE, None) == binding.E_ALIGN
     assert lib.qmv_quantize(2, 1, 64, 64, FAKE, FAKE, FAKE + 4, None) == binding.E_ALIGN
+    # qmv_step_create / run / destroy: argument checks before any CUDA call
+    out = ctypes.c_void_p(123)
+    assert lib.qmv_step_create(None, 0, None, 0, None, 0, None) == binding.E_ARG
+    assert lib.qmv_step_create(None, 1, None, 0, None, 0, ctypes.byref(out)) == binding.E_ARG
+    assert out.value is None                                  # *step is cleared on failure
+    assert lib.qmv_step_create(None, 0, None, -1, None, 0, ctypes.byref(out)) == binding.E_ARG
+    assert lib.qmv_step_create(None, 0, None, 2, None, 0, ctypes.byref(out)) == binding.E_ARG
+    assert lib.qmv_step_create(None, 0, None, 0, None, -1, ctypes.byref(out)) == binding.E_ARG
+    bad = (binding.Copy * 1)(binding.Copy(0, FAKE, 64))
+    assert lib.qmv_step_create(ctypes.addressof(bad), 1, None, 0, None, 0, ctypes.byref(out)) == binding.E_ARG
+    assert lib.qmv_step_run(None, None) == binding.E_ARG
+    assert lib.qmv_step_destroy(None) == binding.OK
     # qmv_gguf_bytes / qmv_gguf_to_mlb: sizes, then shape, format, null and alignment checks
     assert lib.qmv_gguf_bytes(1, 151936, 896) == 144643072
     assert lib.qmv_gguf_bytes(2, 151936, 896) == 76575744
