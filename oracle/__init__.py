@@ -84,6 +84,8 @@ def _load():
     lib.oracle_quantize_x.argtypes = [i32, i64, i64, vp, vp]
     lib.oracle_matvec_qx.restype = i32
     lib.oracle_matvec_qx.argtypes = [i32, i32, i64, i64, vp, vp, i32, vp, vp]
+    lib.oracle_matvec_glu.restype = i32
+    lib.oracle_matvec_glu.argtypes = [i32, i32, i64, i64, vp, i32, vp, vp, i32, vp, vp]
     lib.oracle_gguf_bytes.restype = i64
     lib.oracle_gguf_bytes.argtypes = [i32, i64, i64]
     lib.oracle_gguf_to_mlb.restype = i32
@@ -251,3 +253,20 @@ def gguf_to_mlb(gguf: np.ndarray, wtype: int, rows: int, cols: int) -> np.ndarra
     if st != OK:
         raise ValueError(f"oracle_gguf_to_mlb status {st}")
     return W
+
+
+def matvec_glu(W: np.ndarray, wtype: int, scale_f16: int, rows: int, cols: int, act: int,
+               gate: np.ndarray, up: np.ndarray):
+    """y = W (act(gate) * up) for batch x cols float32 gate and up (act 0 SiLU, 1 GELU-tanh),
+    float64 y and absref (batch x rows)."""
+    gate = np.ascontiguousarray(gate, dtype=np.float32)
+    up = np.ascontiguousarray(up, dtype=np.float32)
+    batch = gate.shape[0]
+    assert gate.shape == up.shape == (batch, cols)
+    y = np.empty((batch, rows), dtype=np.float64)
+    a = np.empty((batch, rows), dtype=np.float64)
+    st = _load().oracle_matvec_glu(wtype, scale_f16, rows, cols, _ptr(W), act, _ptr(gate), _ptr(up), batch,
+                                   _ptr(y), _ptr(a))
+    if st != OK:
+        raise ValueError(f"oracle_matvec_glu status {st}")
+    return y, a

@@ -31,6 +31,9 @@
  *                                               with the dequantized activations; a hand block)
  *   oracle_gguf_bytes                         : pinned (the minfer page's GGUF tensor sizes)
  *   oracle_gguf_to_mlb                        : pinned (hand blocks written as GGUF records)
+ *   oracle_matvec_glu                         : pinned (act(g) - act(-g) = g turns a pair of
+ *                                               gated products into the plain product; SiLU at
+ *                                               ln 3 and GELU where its tanh is 1/2 give 3g/4)
  *   corner readings of the writers (f16 scale that rounds to 0, all-zero Q4 block,
  *   ties of the largest magnitude) : parity unpinned (writer-only, not on the product path)
  */
@@ -555,6 +558,47 @@ int oracle_gguf_to_mlb(int wtype, int64_t rows, int64_t cols, const uint8_t *ggu
             W[off + 2 * idx] = rec[0];
             W[off + 2 * idx + 1] = rec[1];
             for (int64_t j = 0; j < qb; j++) W[idx * qb + j] = rec[2 + j];
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* ---------------------------------------------------------------------------
+ * The FFN's gated activation feeding the down projection (Krafla page, "Body": w1 is the gate
+ * and w3 the up projection, hidden_dim x dim, w2 the down projection, dim x hidden_dim; header
+ * field act: 0 = SiLU, 1 = GELU with the tanh approximation).  Reading: the down projection's
+ * input is h = act(w1 x) * (w3 x), element by element, and the product is y = w2 h.
+ *   SiLU(g) = g / (1 + e^-g);   GELU_tanh(g) = g/2 * (1 + tanh(sqrt(2/pi) * (g + 0.044715 g^3))).
+ * gate and up are batch x cols float32 (the products w1 x, w3 x); h is evaluated in double.
+ * ------------------------------------------------------------------------- */
+
+static double glu_act(int act, double g)
+{
+    if (act == 0) return g / (1.0 + exp(-g));
+    const double k = sqrt(2.0 / acos(-1.0));
+    return 0.5 * g * (1.0 + tanh(k * (g + 0.044715 * g * g * g)));
+}
+
+/* y[b][r] = sum_c W[r][c] * act(gate[b][c]) * up[b][c], absref = sum_c |W[r][c] * h[b][c]|. */
+int oracle_matvec_glu(int wtype, int scale_f16, int64_t rows, int64_t cols, const uint8_t *W, int act,
+                      const float *gate, const float *up, int batch, double *y, double *absref)
+{
+    int64_t q, off, dsz;
+    int st = layout(wtype, scale_f16, rows, cols, &q, &off, &dsz);
+    if (st != ORACLE_OK) return st;
+    if (act != 0 && act != 1) return ORACLE_E_FORMAT;
+    for (int b = 0; b < batch; b++) {
+        for (int64_t r = 0; r < rows; r++) {
+            double acc = 0.0, acc_abs = 0.0;
+            for (int64_t c = 0; c < cols; c++) {
+                double w = (double)oracle_level(W, wtype, cols, r, c) *
+                           (double)oracle_scale(W, wtype, scale_f16, rows, cols, r, c / 32);
+                double h = glu_act(act, (double)gate[(int64_t)b * cols + c]) * (double)up[(int64_t)b * cols + c];
+                acc += w * h;
+                acc_abs += fabs(w * h);
+            }
+            y[(int64_t)b * rows + r] = acc;
+            absref[(int64_t)b * rows + r] = acc_abs;
         }
     }
     return ORACLE_OK;

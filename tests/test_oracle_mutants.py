@@ -48,6 +48,10 @@ MUTANTS = {
     "qx_x_scale_byte_order": ("xq[off + 4 * idx + i] = (uint8_t)((bits >> (8 * i)) & 0xff);",
                               "xq[off + 4 * idx + i] = (uint8_t)((bits >> (8 * (3 - i))) & 0xff);"),
     "q8_rule_without_half": ("float u = t + copysignf(0.5f, x[j]);", "float u = t;"),
+    "glu_silu_sign": ("if (act == 0) return g / (1.0 + exp(-g));", "if (act == 0) return g / (1.0 + exp(g));"),
+    "glu_gelu_cubic": ("(g + 0.044715 * g * g * g)", "(g + 0.044715 * g * g)"),
+    "glu_up_dropped": ("glu_act(act, (double)gate[(int64_t)b * cols + c]) * (double)up[(int64_t)b * cols + c]",
+                       "glu_act(act, (double)gate[(int64_t)b * cols + c])"),
     "gguf_record_without_d": ("int64_t block_bytes = 2 + qb;", "int64_t block_bytes = qb;"),
     "gguf_d_bytes_swapped": ("W[off + 2 * idx] = rec[0];\n            W[off + 2 * idx + 1] = rec[1];",
                              "W[off + 2 * idx] = rec[1];\n            W[off + 2 * idx + 1] = rec[0];"),
@@ -79,6 +83,8 @@ class Orc:
         lib.oracle_matvec_qx.argtypes = [i32, i32, i64, i64, vp, vp, i32, vp, vp]
         lib.oracle_gguf_bytes.restype = i64
         lib.oracle_gguf_bytes.argtypes = [i32, i64, i64]
+        lib.oracle_matvec_glu.restype = i32
+        lib.oracle_matvec_glu.argtypes = [i32, i32, i64, i64, vp, i32, vp, vp, i32, vp, vp]
         lib.oracle_gguf_to_mlb.restype = i32
         lib.oracle_gguf_to_mlb.argtypes = [i32, i64, i64, vp, vp]
         self.lib = lib
@@ -183,6 +189,42 @@ def pin_checks(o):
         assert o.lib.oracle_gguf_to_mlb(wt, 3, 96, g.ctypes.data, Wg.ctypes.data) == 0
         exp = np.array([[2.0 ** (3 * r + c // 32) for c in range(96)] for r in range(3)], np.float32)
         yield "gguf_records", bool(np.array_equal(o.dequant(Wg, wt, 1, 3, 96), exp))
+    # gated activation: act(g) - act(-g) = g turns two gated products into the plain one, and a
+    # one-hot weight reads SiLU(ln 3) = 3/4 ln 3, GELU-tanh at a known point = 3g/4
+    m = inputs.make_matrix(2, 1, 4, 64, seed=12)
+    rng = np.random.default_rng(13)
+    g = np.ascontiguousarray((rng.integers(-6, 7, (1, 64)) / 4).astype(np.float32))
+    u = np.ascontiguousarray((rng.integers(-8, 9, (1, 64)) / 8).astype(np.float32))
+    ng = np.ascontiguousarray(-g)
+    for act in (0, 1):
+        yp, yn, a = (np.empty((1, 4)) for _ in range(3))
+        o.lib.oracle_matvec_glu(2, 1, 4, 64, m.W.ctypes.data, act, g.ctypes.data, u.ctypes.data, 1,
+                                yp.ctypes.data, a.ctypes.data)
+        o.lib.oracle_matvec_glu(2, 1, 4, 64, m.W.ctypes.data, act, ng.ctypes.data, u.ctypes.data, 1,
+                                yn.ctypes.data, a.ctypes.data)
+        y, a = o.matvec(m.W, 2, 1, 4, 64, np.ascontiguousarray((g * u).astype(np.float32)))
+        yield "glu_odd", bool(np.all(np.abs((yp - yn) - y) <= 1e-12 * a + 1e-300))
+    qh = np.full(16, 0x88, np.uint8)
+    qh[0] = 0x89
+    Wh = inputs.assemble(2, 0, 1, 32, qh, np.array([1.0], np.float32).view(np.uint32))
+    uh = np.zeros((1, 32), np.float32)
+    uh[0, 0] = 1.0
+    gh = np.zeros((1, 32), np.float32)
+    gh[0, 0] = np.float32(np.log(3.0))
+    yv, av = np.empty((1, 1)), np.empty((1, 1))
+    o.lib.oracle_matvec_glu(2, 0, 1, 32, Wh.ctypes.data, 0, gh.ctypes.data, uh.ctypes.data, 1, yv.ctypes.data,
+                            av.ctypes.data)
+    yield "glu_silu_ln3", abs(yv[0, 0] - 0.75 * float(gh[0, 0])) < 1e-7
+    # GELU-tanh where its tanh is 1/2 (the point found by bisection): GELU(g) = 3g/4
+    kk, target = np.sqrt(2 / np.pi), np.arctanh(0.5)
+    lo, hi = 0.0, 2.0
+    for _ in range(200):
+        mid = (lo + hi) / 2
+        lo, hi = (mid, hi) if kk * (mid + 0.044715 * mid ** 3) < target else (lo, mid)
+    gh[0, 0] = np.float32(lo)
+    o.lib.oracle_matvec_glu(2, 0, 1, 32, Wh.ctypes.data, 1, gh.ctypes.data, uh.ctypes.data, 1, yv.ctypes.data,
+                            av.ctypes.data)
+    yield "glu_gelu_value", abs(yv[0, 0] - 0.75 * float(gh[0, 0])) < 1e-6
 
 
 def build_variant(tmp, name, text):

@@ -523,3 +523,53 @@ def test_gguf_record_addressing(wt):
     W = oracle.gguf_to_mlb(g, wt, rows, cols)
     expect = np.array([[2.0 ** (3 * r + c // 32) for c in range(cols)] for r in range(rows)], np.float32)
     assert np.array_equal(oracle.dequant(W, wt, 1, rows, cols), expect)
+
+
+# ------------------------------------------------- gated activation (FFN down projection)
+@pytest.mark.parametrize("act", [0, 1])
+@pytest.mark.parametrize("wt,sf", [(1, 0), (2, 1)])
+def test_glu_odd_part_gives_the_plain_product(act, wt, sf):
+    # both activations satisfy act(g) - act(-g) = g (SiLU: g s(g) + g s(-g) = g since
+    # s(g) + s(-g) = 1; GELU-tanh: tanh is odd), so y(g, u) - y(-g, u) = W (g * u): the plain
+    # product, pinned separately, with x = g * u (exact in float32 for these small integers)
+    rows, cols, batch = 5, 96, 2
+    m = inputs.make_matrix(wt, sf, rows, cols, seed=110 + act)
+    rng = np.random.default_rng(111)
+    g = rng.integers(-6, 7, (batch, cols)).astype(np.float32) / 4
+    u = rng.integers(-8, 9, (batch, cols)).astype(np.float32) / 8
+    yp, _ = oracle.matvec_glu(m.W, wt, sf, rows, cols, act, g, u)
+    yn, _ = oracle.matvec_glu(m.W, wt, sf, rows, cols, act, -g, u)
+    y, a = oracle.matvec(m.W, wt, sf, rows, cols, (g * u).astype(np.float32))
+    assert np.all(np.abs((yp - yn) - y) <= 1e-12 * a)
+
+
+def test_glu_silu_and_gelu_values():
+    # one-hot weights pick h itself: W = one block, level +1 at column 0 only, d = 1
+    q = np.full(16, 0x88, np.uint8)
+    q[0] = 0x89                                         # element 0: nibble 9 (level +1)
+    W = inputs.assemble(2, 0, 1, 32, q, np.array([1.0], np.float32).view(np.uint32))
+    up = np.zeros((1, 32), np.float32)
+    up[0, 0] = 1.0
+    # SiLU at ln 3: the sigmoid is exactly 3/4, so SiLU(g) = 3g/4 (g rounded to float32)
+    g = np.zeros((1, 32), np.float32)
+    g[0, 0] = np.float32(np.log(3.0))
+    y, _ = oracle.matvec_glu(W, 2, 0, 1, 32, 0, g, up)
+    assert abs(y[0, 0] - 0.75 * float(g[0, 0])) < 1e-7
+    # GELU-tanh where its tanh is exactly 1/2: sqrt(2/pi)(g + 0.044715 g^3) = atanh(1/2), found
+    # by bisection here; then GELU(g) = g/2 * 3/2 = 3g/4
+    k, target = np.sqrt(2 / np.pi), np.arctanh(0.5)
+    lo, hi = 0.0, 2.0
+    for _ in range(200):
+        mid = (lo + hi) / 2
+        lo, hi = (mid, hi) if k * (mid + 0.044715 * mid ** 3) < target else (lo, mid)
+    g[0, 0] = np.float32(lo)
+    y, _ = oracle.matvec_glu(W, 2, 0, 1, 32, 1, g, up)
+    assert abs(y[0, 0] - 0.75 * float(g[0, 0])) < 1e-6
+    # zero up or zero gate give zero; a large gate passes through SiLU unchanged
+    y, a = oracle.matvec_glu(W, 2, 0, 1, 32, 0, g, np.zeros_like(up))
+    assert y[0, 0] == 0 and a[0, 0] == 0
+    y, _ = oracle.matvec_glu(W, 2, 0, 1, 32, 0, np.zeros_like(g), up)
+    assert y[0, 0] == 0
+    g[0, 0] = 40.0
+    y, _ = oracle.matvec_glu(W, 2, 0, 1, 32, 0, g, up)
+    assert abs(y[0, 0] - 40.0) < 1e-12
