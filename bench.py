@@ -438,6 +438,30 @@ def other_workloads(torch, qmv, dev, l2, cap, peak_hbm, peak_tf):
     res["qx_llama7b_layer_b1"] = {"us_per_step": round(us, 3), "weight_gbs": round(lb / us / 1e3, 1),
                                   "frac_hbm": round(lb / us / 1e3 / peak_hbm, 4),
                                   "launches_per_step": len(groups) + len(specs)}
+
+    # the layer step with the FFN's SwiGLU in the down projection's activation prep: w1 and w3
+    # write gate and up into one buffer, w2 takes SiLU(gate) * up as float32 activations
+    xs_b = [xdev(inputs.make_x(1, s.cols, True, seed=inputs.x_seed(WORKLOAD, i))) for i, s in enumerate(specs)]
+    i1, i3, i2 = names.index("w1"), names.index("w3"), names.index("w2")
+    gu = torch.empty((2, 1, specs[i1].rows), device=dev)
+    outs = {i: ys[i] for i in range(len(specs))}
+    outs[i1], outs[i3] = gu[0], gu[1]
+
+    def glu_step(c):
+        for grp in groups:
+            s0 = specs[grp[0]]
+            if grp == [i2]:
+                qmv.matvec_grouped(s0.wtype, s0.scale_f16, [(s0.rows, s0.cols, copies[c][i2], gu, ys[i2])],
+                                   overlap=True, act="silu")
+            else:
+                qmv.matvec_grouped(s0.wtype, s0.scale_f16,
+                                   [(specs[i].rows, specs[i].cols, copies[c][i], xs_b[i], outs[i]) for i in grp],
+                                   overlap=True)
+
+    us = _graph_time_us(torch, [lambda c=c: glu_step(c) for c in range(ncopy)] * 2, cap)
+    res["llama7b_layer_swiglu_b1"] = {"us_per_step": round(us, 3), "weight_gbs": round(lb / us / 1e3, 1),
+                                      "frac_hbm": round(lb / us / 1e3 / peak_hbm, 4),
+                                      "note": "w2 on SiLU(w1 x) * (w3 x) (float32 route: activation prep + hi/lo bf16)"}
     del copies, mats
     return res
 

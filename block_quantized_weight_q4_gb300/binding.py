@@ -157,18 +157,35 @@ class Problem(ctypes.Structure):
 
 FLAG_OVERLAP = 1
 MAX_GROUP = 8
+X_SILU_GLU_F32 = 2
+X_GELU_GLU_F32 = 3
+ACTS = {"silu": X_SILU_GLU_F32, "gelu": X_GELU_GLU_F32}
 NOALLOC_MAX_BATCH = 8
 
 
-def _problem_array(problems):
+def _problem_array(problems, act=None):
+    """act: None, or "silu" / "gelu" for gated activations (x of each problem: float32
+    (2, batch, cols), gate then up)."""
     n = len(problems)
     if not 1 <= n <= MAX_GROUP:
         raise ValueError("1..8 problems per group")
     arr = (Problem * n)()
-    batch = problems[0][3].shape[0]
-    xdt = _x_dtype(problems[0][3])
+    if act is not None:
+        import torch
+        if act not in ACTS:
+            raise ValueError("act must be 'silu' or 'gelu'")
+        batch = problems[0][3].shape[1]
+        for (rows, cols, W, x, y) in problems:
+            if x.dtype != torch.float32 or tuple(x.shape) != (2, batch, cols):
+                raise ValueError("gated activations need float32 x of shape (2, batch, cols)")
+        xdt = ACTS[act]
+    else:
+        batch = problems[0][3].shape[0]
+        xdt = _x_dtype(problems[0][3])
     for i, (rows, cols, W, x, y) in enumerate(problems):
-        if x.shape != (batch, cols) or tuple(y.shape) != (batch, rows) or _x_dtype(x) != xdt:
+        xshape = (2, batch, cols) if act is not None else (batch, cols)
+        xdt_i = xdt if act is not None else _x_dtype(x)
+        if tuple(x.shape) != xshape or tuple(y.shape) != (batch, rows) or xdt_i != xdt:
             raise ValueError("every problem needs x (batch, cols) of one dtype and y (batch, rows)")
         if not (x.is_contiguous() and y.is_contiguous()):
             raise ValueError("x and y must be contiguous")
@@ -176,12 +193,13 @@ def _problem_array(problems):
     return arr, n, batch, xdt
 
 
-def matvec_grouped(wtype: int, scale_dtype: int, problems, overlap: bool = False, stream=None):
+def matvec_grouped(wtype: int, scale_dtype: int, problems, overlap: bool = False, stream=None, act=None):
     """Several products in one launch.  problems: list of (rows, cols, W, x, y) with W a
     uint8 CUDA tensor, x (batch, cols) and y (batch, rows) CUDA tensors; all share wtype,
     scale_dtype, the x dtype and batch.  overlap: QMV_FLAG_OVERLAP (the weights must not be
-    written by the preceding kernel on the stream)."""
-    arr, n, batch, xdt = _problem_array(problems)
+    written by the preceding kernel on the stream).  act: "silu" / "gelu" for gated
+    activations, x then float32 (2, batch, cols): gate, up; the product takes act(gate) * up."""
+    arr, n, batch, xdt = _problem_array(problems, act)
     st = load_library().qmv_matvec_grouped(wtype, scale_dtype, xdt, batch, ctypes.addressof(arr), n,
                                            FLAG_OVERLAP if overlap else 0, _stream(stream))
     _check(st, "qmv_matvec_grouped")
@@ -224,15 +242,16 @@ class Step:
     recorded once as a CUDA graph; run() enqueues it with one library call.
 
     before / after: lists of (dst, src) tensors (device or pinned host); groups: list of
-    (wtype, scale_dtype, problems, overlap) with problems as for matvec_grouped.  Creating the
+    (wtype, scale_dtype, problems, overlap[, act]) with problems as for matvec_grouped.  Creating the
     step runs it once.  The tensors are kept alive with the step; a run reads and writes the
     same buffers.  Runs of one step must not overlap in time."""
 
     def __init__(self, groups, before=(), after=()):
         keep = [list(before), list(after)]
         garr = (Group * max(len(groups), 1))()
-        for i, (wtype, scale_dtype, problems, overlap) in enumerate(groups):
-            parr, n, batch, xdt = _problem_array(problems)
+        for i, grp in enumerate(groups):
+            wtype, scale_dtype, problems, overlap = grp[:4]
+            parr, n, batch, xdt = _problem_array(problems, grp[4] if len(grp) > 4 else None)
             keep.append((parr, problems))
             garr[i] = Group(wtype, scale_dtype, xdt, batch, ctypes.addressof(parr), n,
                             FLAG_OVERLAP if overlap else 0)

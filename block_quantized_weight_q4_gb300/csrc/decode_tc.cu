@@ -92,7 +92,23 @@ struct SplitArgs {
   int batch;
   int nvec;    // hi rows written (the lo rows too): batch rounded up to the consumer's width
   int lo_row;  // row of vector 0's lo part
+  int act;     // -1: x as given; 0 / 1: x is a gate and the activations are act(gate) * up
+  long long up_batch;  // gated activations: a problem's up array is up_batch * cols floats after its gate
 };
+
+// The FFN's gated activation: SiLU(g) = g / (1 + e^-g), GELU_tanh(g) = g/2 (1 + tanh(sqrt(2/pi)
+// (g + 0.044715 g^3))), times up; float32 operations with CUDA's expf and tanhf.
+__device__ __forceinline__ float glu(int act, float g, float u) {
+  float h;
+  if (act == 0) {
+    h = __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
+  } else {
+    const float k = 0.7978845608028654f;  // sqrt(2 / pi)
+    const float inner = __fmul_rn(k, __fadd_rn(g, __fmul_rn(0.044715f, __fmul_rn(g, __fmul_rn(g, g)))));
+    h = __fmul_rn(__fmul_rn(0.5f, g), __fadd_rn(1.0f, tanhf(inner)));
+  }
+  return __fmul_rn(h, u);
+}
 
 // bfloat16 bits of v rounded to nearest (ties to even); finite v beyond the bfloat16 range
 // (which would round to infinity) are truncated instead, so that hi + lo stays finite.
@@ -119,7 +135,8 @@ __global__ void __launch_bounds__(256) split_x_kernel(const __grid_constant__ Sp
   for (int n = 0; n < a.nvec; ++n) {
     uint16_t hi = 0, lo = 0;
     if (n < a.batch) {
-      const float v = x[(size_t)n * cols + c];
+      float v = x[(size_t)n * cols + c];
+      if (a.act >= 0) v = glu(a.act, v, x[(size_t)(a.up_batch + n) * cols + c]);
       hi = bf16_bits_rn_finite(v);
       const float h = __uint_as_float((uint32_t)hi << 16);
       lo = isfinite(v) ? bf16_bits_rn_finite(v - h) : 0;
@@ -136,7 +153,8 @@ __global__ void __launch_bounds__(256) split_x_kernel(const __grid_constant__ Sp
 // after the other; sx[i] receives problem i's rows.  pdl: the split waits for the preceding
 // kernel before reading x.
 static cudaError_t split_activations(const MatrixRef* ms, const void* const* xs, int n, int batch, int nvec, int lo_row,
-                                     bool pdl, const DeviceInfo& dev, cudaStream_t stream, const void** sx) {
+                                     int act, long long up_batch, bool pdl, const DeviceInfo& dev, cudaStream_t stream,
+                                     const void** sx) {
   if (n < 1 || n > dtc::kMaxProblems || batch < 1 || batch > nvec) return cudaErrorInvalidValue;
   const int rows = lo_row + nvec;
   size_t need = 0;
@@ -161,6 +179,8 @@ static cudaError_t split_activations(const MatrixRef* ms, const void* const* xs,
   a.batch = batch;
   a.nvec = nvec;
   a.lo_row = lo_row;
+  a.act = act;
+  a.up_batch = up_batch;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)((maxcols + 255) / 256), (unsigned)n);
   cfg.blockDim = dim3(256);
@@ -174,10 +194,12 @@ static cudaError_t split_activations(const MatrixRef* ms, const void* const* xs,
 }
 
 cudaError_t launch_decode_tc_f32(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, int batch,
-                                 bool pdl, const DeviceInfo& dev, const Workspace& ws, cudaStream_t stream) {
+                                 bool pdl, const DeviceInfo& dev, const Workspace& ws, cudaStream_t stream, int act,
+                                 long long up_batch) {
   const void* sx[dtc::kMaxProblems];
   // 16 MMA columns: the hi parts of up to 8 vectors, then their lo parts
-  cudaError_t err = split_activations(ms, xs, n, batch, dtc::kMaxBatch, dtc::kMaxBatch, pdl, dev, stream, sx);
+  cudaError_t err =
+      split_activations(ms, xs, n, batch, dtc::kMaxBatch, dtc::kMaxBatch, act, up_batch, pdl, dev, stream, sx);
   if (err != cudaSuccess) return err;
   // the product launches as a programmatic dependent of the split: its weight loads overlap it
   if (ms[0].wtype == QMV_Q4_0) return dtc::launch_q4(ms, sx, ys, n, batch, true, true, dev, ws, stream);
@@ -191,12 +213,12 @@ bool decode_tc_f32_fits(const MatrixRef* ms, int n) {
 }
 
 cudaError_t launch_matvec_bdiag_f32(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
-                                    const DeviceInfo& dev, cudaStream_t stream) {
+                                    const DeviceInfo& dev, cudaStream_t stream, int act, long long up_batch) {
   size_t need = 0;
   for (int i = 0; i < n; ++i) need += (size_t)2 * (size_t)ms[i].cols * 2;
   if (need > kSplitBytes) return cudaErrorInvalidValue;
   const void* sx[dtc::kMaxProblems];
-  cudaError_t err = split_activations(ms, xs, n, 1, 1, 1, pdl, dev, stream, sx);  // rows: hi, lo
+  cudaError_t err = split_activations(ms, xs, n, 1, 1, 1, act, up_batch, pdl, dev, stream, sx);  // rows: hi, lo
   if (err != cudaSuccess) return err;
   return launch_matvec_bdiag_split(ms, sx, ys, n, true, dev, stream);
 }

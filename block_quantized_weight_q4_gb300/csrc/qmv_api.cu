@@ -142,9 +142,15 @@ int qmv_matrix_wtype(int file_wtype, uint32_t q8_mask, int class_bit, int shared
 int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const qmv_problem* problems, int n,
                        unsigned flags, cudaStream_t stream) {
   if (problems == nullptr || n < 1 || n > QMV_MAX_GROUP) return QMV_E_ARG;
-  if (x_dtype != QMV_X_F32 && x_dtype != QMV_X_BF16) return QMV_E_FORMAT;
+  if (x_dtype != QMV_X_F32 && x_dtype != QMV_X_BF16 && x_dtype != QMV_X_SILU_GLU_F32 &&
+      x_dtype != QMV_X_GELU_GLU_F32)
+    return QMV_E_FORMAT;
   if (batch < 0) return QMV_E_ARG;
   if ((flags & ~QMV_FLAG_OVERLAP) != 0) return QMV_E_ARG;
+  // gated activations: x holds gate then up (batch x cols float32 each); act(gate) * up is
+  // formed in the activation prep of the float32 routes
+  const bool glu = x_dtype == QMV_X_SILU_GLU_F32 || x_dtype == QMV_X_GELU_GLU_F32;
+  const int act = x_dtype == QMV_X_SILU_GLU_F32 ? 0 : x_dtype == QMV_X_GELU_GLU_F32 ? 1 : -1;
   MatrixRef ms[QMV_MAX_GROUP];
   for (int i = 0; i < n; ++i) {
     const qmv_problem& pr = problems[i];
@@ -154,6 +160,7 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
     if (pr.x == nullptr || pr.y == nullptr) return QMV_E_ARG;
     if (!aligned(pr.x, 16) || !aligned(pr.y, 4)) return QMV_E_ALIGN;
     if (pr.rows > INT64_MAX / batch) return QMV_E_SHAPE;
+    if (glu && !matvec_mma_supported(ms[i])) return QMV_E_SHAPE;
   }
   if (batch == 0) return QMV_OK;
   DeviceInfo dev;
@@ -222,12 +229,16 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
     if (tc && stream_workspace(dev, stream, &ws) == cudaSuccess) {
       if (launch_decode_tc(fast, fx, fy, nf, nb, pdl, dev, ws, stream) != cudaSuccess) return QMV_E_CUDA;
     } else if (tc32 && stream_workspace(dev, stream, &ws) == cudaSuccess &&
-               launch_decode_tc_f32(fast, fx, fy, nf, nb, pdl, dev, ws, stream) == cudaSuccess) {
+               launch_decode_tc_f32(fast, fx, fy, nf, nb, pdl, dev, ws, stream, act, batch) ==
+                   cudaSuccess) {
       // done (a stream being captured without its split buffer yet falls through to mma.sync)
     } else if (xb && nb == 1) {
       if (launch_matvec_bdiag(fast, fx, fy, nf, pdl, dev, stream) != cudaSuccess) return QMV_E_CUDA;
-    } else if (!xb && nb == 1 && launch_matvec_bdiag_f32(fast, fx, fy, nf, pdl, dev, stream) == cudaSuccess) {
+    } else if (!xb && nb == 1 &&
+               launch_matvec_bdiag_f32(fast, fx, fy, nf, pdl, dev, stream, act, batch) == cudaSuccess) {
       // one float32 vector: the block-diagonal kernel on its bf16 hi + lo parts
+    } else if (glu) {
+      return QMV_E_ARG;  // gated activations need the stream's split buffer (see qmv.h)
     } else if (launch_matvec_mma(fast, fx, fy, nf, xb, nb, pdl, dev, stream) != cudaSuccess) {
       return QMV_E_CUDA;
     }

@@ -103,8 +103,9 @@ cudaError_t launch_matvec_bdiag_split(const MatrixRef* ms, const void* const* xs
 // split buffer (2 rows per problem, up to 524,288 columns over the problems), then the above.
 // Fails (nothing launched) when the buffer would not hold them, or cannot be created while
 // the stream is being captured.
+// act >= 0: xs are gates, the activations act(gate) * up with up at gate + up_batch * cols floats.
 cudaError_t launch_matvec_bdiag_f32(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
-                                    const DeviceInfo& dev, cudaStream_t stream);
+                                    const DeviceInfo& dev, cudaStream_t stream, int act = -1, long long up_batch = 0);
 
 // Batched product on the 5th-generation tensor core (weights dequantized to bf16 in tensor
 // memory, tcgen05 MMA, f32 accumulators in tensor memory): bf16 activations, cols % 256 == 0,
@@ -131,6 +132,7 @@ cudaError_t launch_decode_tc(const MatrixRef* ms, const void* const* xs, float* 
 // over the problems) and a stream that is not being captured when it has no buffer yet.
 bool decode_tc_f32_fits(const MatrixRef* ms, int n);
 cudaError_t launch_decode_tc_f32(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, int batch,
-                                 bool pdl, const DeviceInfo& dev, const Workspace& ws, cudaStream_t stream);
+                                 bool pdl, const DeviceInfo& dev, const Workspace& ws, cudaStream_t stream,
+                                 int act = -1, long long up_batch = 0);
 
 }  // namespace qmv

@@ -53,6 +53,19 @@ extern "C" {
 /* x_dtype: element type of the activations. */
 #define QMV_X_F32 0
 #define QMV_X_BF16 1
+/* Gated activations, the FFN down projection's input (Krafla page, "Body": w1 gate, w3 up,
+ * w2 down; header field act): x holds two batch x cols float32 arrays one after the other,
+ * gate (w1 x) then up (w3 x), and the product's activations are act(gate) * up, formed in
+ * float32 in the activation prep of the float32 routes (no launch of its own):
+ *   QMV_X_SILU_GLU_F32: act(g) = g / (1 + e^-g)
+ *   QMV_X_GELU_GLU_F32: act(g) = g/2 (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3)))
+ * with CUDA's expf / tanhf.  They need cols % 256 == 0 (QMV_E_SHAPE otherwise), at most
+ * 65,536 columns over a group's problems when batch >= 2, and the stream's split buffer (made
+ * on the stream's first float32 or gated call outside stream capture, or by qmv_step_create);
+ * QMV_E_ARG otherwise.  The tolerance of the product is taken against the exact
+ * act(gate) * up. */
+#define QMV_X_SILU_GLU_F32 2
+#define QMV_X_GELU_GLU_F32 3
 
 /* Status codes.  QMV_E_FORMAT and QMV_E_SHAPE mirror the loader's ML_E_FORMAT and
  * ML_E_SHAPE classes (Krafla page, "Validation done by the loader"): an unknown enum

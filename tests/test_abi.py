@@ -71,7 +71,11 @@ def call_matvec(lib, wt=2, sf=1, rows=64, cols=64, W=FAKE, x=FAKE, xd=1, y=FAKE,
 def test_matvec_argument_errors(lib):
     assert call_matvec(lib, wt=3) == binding.E_FORMAT
     assert call_matvec(lib, sf=2) == binding.E_FORMAT
-    assert call_matvec(lib, xd=2) == binding.E_FORMAT
+    assert call_matvec(lib, xd=4) == binding.E_FORMAT
+    assert call_matvec(lib, xd=-1) == binding.E_FORMAT
+    # gated activations (2: SiLU, 3: GELU-tanh) need cols % 256 == 0: checked before any launch
+    assert call_matvec(lib, xd=2, cols=64) == binding.E_SHAPE
+    assert call_matvec(lib, xd=3, cols=96) == binding.E_SHAPE
     assert call_matvec(lib, cols=48) == binding.E_SHAPE
     assert call_matvec(lib, rows=0) == binding.E_SHAPE
     assert call_matvec(lib, rows=2**40, cols=2**40) == binding.E_SHAPE
