@@ -66,8 +66,15 @@ struct WeightTile {
   }
 };
 
+// Passes of one vector: three CTAs per SM (24 warps, more loads in flight; the tile fits 80
+// registers); larger passes two.
+template <int R, int NV>
+struct MinCtas {
+  static constexpr int value = NV == 1 ? 3 : 2;
+};
+
 template <int WT, bool F16, int R, int NV>
-__global__ void __launch_bounds__(kWarps * 32, 2)
+__global__ void __launch_bounds__(kWarps * 32, MinCtas<R, NV>::value)
     matvec_qx_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ d, const int8_t* __restrict__ xq,
                      const float* __restrict__ xd, long long rows, long long nb, int nv, int ks,
                      float* __restrict__ y) {
