@@ -86,6 +86,10 @@ def _load():
     lib.oracle_matvec_qx.argtypes = [i32, i32, i64, i64, vp, vp, i32, vp, vp]
     lib.oracle_matvec_glu.restype = i32
     lib.oracle_matvec_glu.argtypes = [i32, i32, i64, i64, vp, i32, vp, vp, i32, vp, vp]
+    lib.oracle_quant_q4_fit_block.restype = i32
+    lib.oracle_quant_q4_fit_block.argtypes = [vp, i32, vp, vp]
+    lib.oracle_quantize_q4_fit.restype = i32
+    lib.oracle_quantize_q4_fit.argtypes = [i32, i64, i64, vp, vp]
     lib.oracle_gguf_bytes.restype = i64
     lib.oracle_gguf_bytes.argtypes = [i32, i64, i64]
     lib.oracle_gguf_to_mlb.restype = i32
@@ -270,3 +274,24 @@ def matvec_glu(W: np.ndarray, wtype: int, scale_f16: int, rows: int, cols: int, 
     if st != OK:
         raise ValueError(f"oracle_matvec_glu status {st}")
     return y, a
+
+
+def quant_q4_fit_block(x: np.ndarray, scale_f16: int):
+    """(status, 16 packed bytes, stored scale bits) for one block by the best-fit rule."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    assert x.size == 32
+    qs = np.zeros(16, dtype=np.uint8)
+    bits = ctypes.c_uint32(0)
+    st = _load().oracle_quant_q4_fit_block(_ptr(x), scale_f16, _ptr(qs), ctypes.addressof(bits))
+    return st, qs, int(bits.value)
+
+
+def quantize_q4_fit(src: np.ndarray, scale_f16: int) -> np.ndarray:
+    """Q4_0 matrix bytes (two-array layout) from float32 rows x cols by the best-fit rule."""
+    src = np.ascontiguousarray(src, dtype=np.float32)
+    rows, cols = src.shape
+    W = np.zeros(weight_bytes(Q4_0, scale_f16, rows, cols), dtype=np.uint8)
+    st = _load().oracle_quantize_q4_fit(scale_f16, rows, cols, _ptr(src), _ptr(W))
+    if st != OK:
+        raise ValueError(f"oracle_quantize_q4_fit status {st}")
+    return W

@@ -31,6 +31,11 @@
  *                                               with the dequantized activations; a hand block)
  *   oracle_gguf_bytes                         : pinned (the minfer page's GGUF tensor sizes)
  *   oracle_gguf_to_mlb                        : pinned (hand blocks written as GGUF records)
+ *   oracle_quant_q4_fit_block / _quantize_q4_fit : pinned by invariants only (exactly
+ *                                               representable blocks come back exactly; the
+ *                                               weighted error never exceeds the round rule's;
+ *                                               scaling a block scales d); the float order is a
+ *                                               reading: parity of the printed rule unpinned
  *   oracle_matvec_glu                         : pinned (act(g) - act(-g) = g turns a pair of
  *                                               gated products into the plain product; SiLU at
  *                                               ln 3 and GELU where its tanh is 1/2 give 3g/4)
@@ -599,6 +604,111 @@ int oracle_matvec_glu(int wtype, int scale_f16, int64_t rows, int64_t cols, cons
             }
             y[(int64_t)b * rows + r] = acc;
             absref[(int64_t)b * rows + r] = acc_abs;
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* ---------------------------------------------------------------------------
+ * The Q4_0 best-fit writer (Krafla page, "Quantization rule": the search tools/mlb.py runs
+ * per block).  The page fixes: the block's largest-magnitude element is mapped to each level
+ * from -6 to -8.4 in steps of 0.2 (levels clamped to [-8, 7]); for each candidate d is the
+ * least-squares fit to those levels with every element weighted by x^2; the candidate with
+ * the smallest weighted error wins; a block whose largest magnitude is below 1e-6 is scaled
+ * up to 1 for the fit and its d scaled back; d may be negative; with f16 scales the fitted d
+ * is rounded to the nearest f16.  Readings (parity pinned only by the invariants in the
+ * tests, not by printed values): every step is one float32 operation rounded to nearest even,
+ * in this order --
+ *   m = the element of largest magnitude (the first of equals), a = |m|;
+ *   a == 0: the zero block (d = 0, every level 0); a < 1e-6: x_j <- x_j / a, and d <- d * a
+ *   at the end;
+ *   candidate k = 0..12: L = (float)(-(60 + 2k)) / 10;  s = m / L;
+ *     l_j = clamp(rint(x_j / s), -8, 7)  (ties to even, as numpy rounds);
+ *     t_j = x_j * x_j;  num += (t_j * x_j) * l_j;  den += (t_j * l_j) * l_j  (j = 0..31 in order);
+ *     d = den == 0 ? 0 : num / den;
+ *     err += t_j * (e_j * e_j), e_j = x_j - d * l_j  (j in order);
+ *   the first candidate with the smallest err wins (strict <); nibble = l + 8.
+ * ------------------------------------------------------------------------- */
+
+/* One block; d_bits receives the stored scale bits.  ORACLE_E_FORMAT for an f16 d beyond
+ * 65504 (refused, as the other f16 rules). */
+int oracle_quant_q4_fit_block(const float *xin, int scale_f16, uint8_t *qs, uint32_t *d_bits)
+{
+    float x[32];
+    float m = xin[0], a = fabsf(xin[0]);
+    for (int j = 1; j < 32; j++)
+        if (fabsf(xin[j]) > a) {
+            a = fabsf(xin[j]);
+            m = xin[j];
+        }
+    int best_l[32];
+    float best_d = 0.0f;
+    if (a == 0.0f) {
+        for (int j = 0; j < 32; j++) best_l[j] = 0;
+    } else {
+        const int small = a < 1e-6f;
+        for (int j = 0; j < 32; j++) x[j] = small ? xin[j] / a : xin[j];
+        if (small) m = m / a;
+        float best_err = 0.0f;
+        for (int k = 0; k <= 12; k++) {
+            const float L = (float)(-(60 + 2 * k)) / 10.0f;
+            const float s = m / L;
+            int l[32];
+            float num = 0.0f, den = 0.0f;
+            for (int j = 0; j < 32; j++) {
+                float r = rintf(x[j] / s);
+                if (r < -8.0f) r = -8.0f;
+                if (r > 7.0f) r = 7.0f;
+                l[j] = (int)r;
+                const float t = x[j] * x[j];
+                num += (t * x[j]) * (float)l[j];
+                den += (t * (float)l[j]) * (float)l[j];
+            }
+            const float d = den == 0.0f ? 0.0f : num / den;
+            float err = 0.0f;
+            for (int j = 0; j < 32; j++) {
+                const float e = x[j] - d * (float)l[j];
+                err += (x[j] * x[j]) * (e * e);
+            }
+            if (k == 0 || err < best_err) {
+                best_err = err;
+                best_d = d;
+                for (int j = 0; j < 32; j++) best_l[j] = l[j];
+            }
+        }
+        if (small) best_d = best_d * a;
+    }
+    for (int j = 0; j < 16; j++) qs[j] = (uint8_t)((best_l[j] + 8) | ((best_l[j + 16] + 8) << 4));
+    if (scale_f16) {
+        uint16_t h = oracle_f16_bits_rne(best_d);
+        if ((h & 0x7fff) >= 0x7c00) return ORACLE_E_FORMAT;
+        *d_bits = h;
+    } else {
+        *d_bits = bits_from_f32(best_d);
+    }
+    return ORACLE_OK;
+}
+
+/* A whole matrix by the best-fit rule into the two-array layout (as oracle_quantize). */
+int oracle_quantize_q4_fit(int scale_f16, int64_t rows, int64_t cols, const float *src, uint8_t *W)
+{
+    int64_t q, off, dsz;
+    int st = layout(ORACLE_Q4_0, scale_f16, rows, cols, &q, &off, &dsz);
+    if (st != ORACLE_OK) return st;
+    memset(W, 0, (size_t)(off + dsz));
+    int64_t nblk = cols / 32;
+    for (int64_t r = 0; r < rows; r++) {
+        for (int64_t k = 0; k < nblk; k++) {
+            uint32_t bits = 0;
+            st = oracle_quant_q4_fit_block(src + r * cols + 32 * k, scale_f16, W + r * (cols / 2) + 16 * k, &bits);
+            if (st != ORACLE_OK) return st;
+            int64_t idx = r * nblk + k;
+            if (scale_f16) {
+                W[off + 2 * idx] = (uint8_t)(bits & 0xff);
+                W[off + 2 * idx + 1] = (uint8_t)((bits >> 8) & 0xff);
+            } else {
+                for (int i = 0; i < 4; i++) W[off + 4 * idx + i] = (uint8_t)((bits >> (8 * i)) & 0xff);
+            }
         }
     }
     return ORACLE_OK;

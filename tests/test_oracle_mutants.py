@@ -48,6 +48,10 @@ MUTANTS = {
     "qx_x_scale_byte_order": ("xq[off + 4 * idx + i] = (uint8_t)((bits >> (8 * i)) & 0xff);",
                               "xq[off + 4 * idx + i] = (uint8_t)((bits >> (8 * (3 - i))) & 0xff);"),
     "q8_rule_without_half": ("float u = t + copysignf(0.5f, x[j]);", "float u = t;"),
+    "fit_den_unweighted_level": ("den += (t * (float)l[j]) * (float)l[j];", "den += t * (float)l[j];"),
+    "fit_clamp_high_8": ("if (r > 7.0f) r = 7.0f;", "if (r > 8.0f) r = 8.0f;"),
+    "fit_candidates_from_minus_7": ("const float L = (float)(-(60 + 2 * k)) / 10.0f;",
+                                    "const float L = (float)(-(70 + 2 * k)) / 10.0f;"),
     "glu_silu_sign": ("if (act == 0) return g / (1.0 + exp(-g));", "if (act == 0) return g / (1.0 + exp(g));"),
     "glu_gelu_cubic": ("(g + 0.044715 * g * g * g)", "(g + 0.044715 * g * g)"),
     "glu_up_dropped": ("glu_act(act, (double)gate[(int64_t)b * cols + c]) * (double)up[(int64_t)b * cols + c]",
@@ -83,6 +87,10 @@ class Orc:
         lib.oracle_matvec_qx.argtypes = [i32, i32, i64, i64, vp, vp, i32, vp, vp]
         lib.oracle_gguf_bytes.restype = i64
         lib.oracle_gguf_bytes.argtypes = [i32, i64, i64]
+        lib.oracle_quantize_q4_fit.restype = i32
+        lib.oracle_quantize_q4_fit.argtypes = [i32, i64, i64, vp, vp]
+        lib.oracle_quantize.restype = i32
+        lib.oracle_quantize.argtypes = [i32, i32, i64, i64, vp, vp]
         lib.oracle_matvec_glu.restype = i32
         lib.oracle_matvec_glu.argtypes = [i32, i32, i64, i64, vp, i32, vp, vp, i32, vp, vp]
         lib.oracle_gguf_to_mlb.restype = i32
@@ -189,6 +197,29 @@ def pin_checks(o):
         assert o.lib.oracle_gguf_to_mlb(wt, 3, 96, g.ctypes.data, Wg.ctypes.data) == 0
         exp = np.array([[2.0 ** (3 * r + c // 32) for c in range(96)] for r in range(3)], np.float32)
         yield "gguf_records", bool(np.array_equal(o.dequant(Wg, wt, 1, 3, 96), exp))
+    # Q4_0 best fit: exact blocks come back exactly; never worse than the round rule (weighted)
+    rng = np.random.default_rng(14)
+    lv = rng.integers(-7, 8, (4, 3, 32))
+    lv[:, :, 5] = -8
+    cc = np.exp2(rng.integers(-6, 2, (4, 3))).astype(np.float32)
+    xe = np.ascontiguousarray((lv * cc[:, :, None]).reshape(4, 96).astype(np.float32))
+    Wf = np.zeros(4096, np.uint8)
+    o.lib.oracle_quantize_q4_fit(0, 4, 96, xe.ctypes.data, Wf.ctypes.data)
+    yield "fit_exact", bool(np.array_equal(o.dequant(Wf, 2, 0, 4, 96), xe))
+    lv6 = rng.integers(-5, 6, (4, 3, 32))
+    lv6[:, :, 9] = -6
+    x6 = np.ascontiguousarray((lv6 * cc[:, :, None]).reshape(4, 96).astype(np.float32))
+    o.lib.oracle_quantize_q4_fit(0, 4, 96, x6.ctypes.data, Wf.ctypes.data)
+    yield "fit_exact_at_minus_6", bool(np.array_equal(o.dequant(Wf, 2, 0, 4, 96), x6))
+    xr = np.ascontiguousarray((rng.standard_normal((8, 96)) * 3).astype(np.float32))
+    Wr = np.zeros(4096, np.uint8)
+    o.lib.oracle_quantize_q4_fit(0, 8, 96, xr.ctypes.data, Wf.ctypes.data)
+    o.lib.oracle_quantize(2, 0, 8, 96, xr.ctypes.data, Wr.ctypes.data)
+    df, dr = o.dequant(Wf, 2, 0, 8, 96).astype(np.float64), o.dequant(Wr, 2, 0, 8, 96).astype(np.float64)
+    xd = xr.astype(np.float64)
+    ef = (xd ** 2 * (xd - df) ** 2).reshape(8, 3, 32).sum(axis=2)
+    er = (xd ** 2 * (xd - dr) ** 2).reshape(8, 3, 32).sum(axis=2)
+    yield "fit_vs_round", bool(np.all(ef <= er * (1 + 1e-5) + 1e-30) and np.sum(ef < er * (1 - 1e-3)) > 12)
     # gated activation: act(g) - act(-g) = g turns two gated products into the plain one, and a
     # one-hot weight reads SiLU(ln 3) = 3/4 ln 3, GELU-tanh at a known point = 3g/4
     m = inputs.make_matrix(2, 1, 4, 64, seed=12)

@@ -573,3 +573,86 @@ def test_glu_silu_and_gelu_values():
     g[0, 0] = 40.0
     y, _ = oracle.matvec_glu(W, 2, 0, 1, 32, 0, g, up)
     assert abs(y[0, 0] - 40.0) < 1e-12
+
+
+# ------------------------------------------------------------- Q4_0 best-fit writer
+def _weighted_err(x, w):
+    x = x.astype(np.float64)
+    return float(np.sum(x * x * (x - w.astype(np.float64)) ** 2))
+
+
+@pytest.mark.parametrize("sf", [0, 1])
+def test_q4_fit_exact_blocks_come_back_exactly(sf):
+    # x = c * l with integer levels l in [-7, 7], one element at -8 (the unique largest
+    # magnitude) and c a power of two: the candidate that maps the largest element to -8 reproduces
+    # l, the weighted least-squares d is c itself, and the error is zero; so dequant gives x back
+    rng = np.random.default_rng(120 + sf)
+    rows, cols = 6, 128
+    lv = rng.integers(-7, 8, (rows, cols // 32, 32))
+    lv[:, :, 5] = -8
+    c = np.exp2(rng.integers(-10, 3, (rows, cols // 32))).astype(np.float32)
+    x = (lv * c[:, :, None]).reshape(rows, cols).astype(np.float32)
+    W = oracle.quantize_q4_fit(x, sf)
+    assert np.array_equal(oracle.dequant(W, 2, sf, rows, cols), x)
+
+
+def test_q4_fit_never_worse_than_the_round_rule():
+    # the candidate at -8 starts from the round rule's own scale, and a weighted least-squares d
+    # over the same levels cannot raise the weighted error; the winner is no worse than that
+    rng = np.random.default_rng(130)
+    rows, cols = 64, 256
+    x = (rng.standard_normal((rows, cols)) * np.exp(rng.uniform(-3, 3, (rows, 1)))).astype(np.float32)
+    fit = oracle.dequant(oracle.quantize_q4_fit(x, 0), 2, 0, rows, cols)
+    rnd = oracle.dequant(oracle.quantize(x, 2, 0), 2, 0, rows, cols)
+    better = 0
+    for r in range(rows):
+        for k in range(cols // 32):
+            sl = slice(32 * k, 32 * k + 32)
+            ef, er = _weighted_err(x[r, sl], fit[r, sl]), _weighted_err(x[r, sl], rnd[r, sl])
+            assert ef <= er * (1 + 1e-5) + 1e-30, (r, k, ef, er)
+            better += ef < er * (1 - 1e-3)
+    assert better > rows * cols // 32 // 2   # the search usually finds a strictly better fit
+
+
+def test_q4_fit_scales_with_the_block():
+    # every step scales exactly under a power-of-two factor (away from the 1e-6 threshold and
+    # float32's range ends): the nibbles stay, d scales by the factor
+    rng = np.random.default_rng(140)
+    for _ in range(20):
+        x = rng.standard_normal(32).astype(np.float32)
+        st, q1, d1 = oracle.quant_q4_fit_block(x, 0)
+        st2, q2, d2 = oracle.quant_q4_fit_block(x * np.float32(2.0 ** 7), 0)
+        assert st == st2 == 0 and np.array_equal(q1, q2)
+        assert np.array([d2], np.uint32).view(np.float32)[0] == np.array([d1], np.uint32).view(np.float32)[0] * 2.0 ** 7
+
+
+def test_q4_fit_small_and_zero_blocks():
+    # a block below 1e-6 is fitted at unit scale: the same nibbles as the block scaled up to a
+    # largest magnitude of 1, and d scaled back; the all-zero block is d = 0 with level 0
+    rng = np.random.default_rng(150)
+    y = rng.standard_normal(32).astype(np.float32)
+    y[7] = 1.0
+    y = np.clip(y, -0.99, 1.0).astype(np.float32)     # element 7 is the unique largest, exactly 1
+    a = np.float32(2.0 ** -30)
+    st, qs, ds = oracle.quant_q4_fit_block(y * a, 0)
+    st1, q1, d1 = oracle.quant_q4_fit_block(y, 0)
+    assert st == st1 == 0 and np.array_equal(qs, q1)
+    assert np.array([ds], np.uint32).view(np.float32)[0] == np.array([d1], np.uint32).view(np.float32)[0] * a
+    st, q0, d0 = oracle.quant_q4_fit_block(np.zeros(32, np.float32), 1)
+    assert st == 0 and d0 == 0 and np.all(q0 == 0x88)
+
+
+@pytest.mark.parametrize("top", [-6, -7, 6])
+def test_q4_fit_exact_blocks_at_other_levels(top):
+    # the candidates run from -6 to -8.4: a block that is exactly c * l with its largest element
+    # at level -6 or -7 (others strictly smaller) is reproduced only by the candidate that maps
+    # it there; a positive largest element maps to the same levels with d negative
+    rng = np.random.default_rng(160 + top)
+    rows, cols = 4, 96
+    lim = abs(top) - 1
+    lv = rng.integers(-lim, lim + 1, (rows, cols // 32, 32))
+    lv[:, :, 11] = top
+    c = np.exp2(rng.integers(-8, 2, (rows, cols // 32))).astype(np.float32)
+    x = (lv * c[:, :, None]).reshape(rows, cols).astype(np.float32)
+    W = oracle.quantize_q4_fit(x, 0)
+    assert np.array_equal(oracle.dequant(W, 2, 0, rows, cols), x)
