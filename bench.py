@@ -403,6 +403,17 @@ def other_workloads(torch, qmv, dev, l2, cap, peak_hbm, peak_tf):
             "us": round(us, 3), "gbs": round(moved / us / 1e3, 1), "frac_hbm": round(moved / us / 1e3 / peak_hbm, 4),
             "bytes": moved}
         del W
+    # the Q4_0 best-fit writer (13 candidate fits per block): compute-bound, reported in GB/s too
+    nbytes = qmv.weight_bytes(2, 1, rows, cols)
+    W = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    call = lambda: lib.qmv_quantize_q4_fit(1, rows, cols, src.data_ptr(), W.data_ptr(), first.data_ptr(),
+                                           torch.cuda.current_stream().cuda_stream)
+    us = _graph_time_us(torch, [call] * 4, cap)
+    moved = 4 * rows * cols + nbytes
+    res[f"quantize_q4_fit_{rows}x{cols}_f16"] = {
+        "us": round(us, 3), "gbs": round(moved / us / 1e3, 1), "frac_hbm": round(moved / us / 1e3 / peak_hbm, 4),
+        "bytes": moved}
+    del W
     del src
 
     # GGUF interleaved blocks into the two-array layout: the page's 151,936 x 896 tensors

@@ -78,6 +78,8 @@ def load_library():
     lib.qmv_gguf_bytes.argtypes = [i32, i64, i64]
     lib.qmv_gguf_to_mlb.restype = i32
     lib.qmv_gguf_to_mlb.argtypes = [i32, i64, i64, vp, vp, vp]
+    lib.qmv_quantize_q4_fit.restype = i32
+    lib.qmv_quantize_q4_fit.argtypes = [i32, i64, i64, vp, vp, vp, vp]
     lib.qmv_quantize_x.restype = i32
     lib.qmv_quantize_x.argtypes = [i32, i64, i64, vp, vp, vp]
     lib.qmv_matvec_qx.restype = i32
@@ -357,6 +359,22 @@ def matvec_qx(wtype: int, scale_dtype: int, rows: int, cols: int, W, xq, batch: 
                                       batch, _stream(stream))
     _check(st, "qmv_matvec_qx")
     return y
+
+
+def quantize_q4_fit(scale_dtype: int, src, W=None, stream=None):
+    """Q4_0 matrix bytes from float32 (rows, cols) by the best-fit rule (qmv_quantize_q4_fit).
+    Returns (W, first refused block index or -1); waits for the stream."""
+    import torch
+    rows, cols = src.shape
+    if src.dtype != torch.float32 or not src.is_contiguous():
+        raise ValueError("src must be a contiguous float32 (rows, cols) tensor")
+    if W is None:
+        W = torch.empty(weight_bytes(Q4_0, scale_dtype, rows, cols), dtype=torch.uint8, device=src.device)
+    first = torch.empty(1, dtype=torch.int64, device=src.device)
+    st = load_library().qmv_quantize_q4_fit(scale_dtype, rows, cols, src.data_ptr(), W.data_ptr(), first.data_ptr(),
+                                            _stream(stream))
+    _check(st, "qmv_quantize_q4_fit")
+    return W, int(first.item())
 
 
 def last_error() -> int:

@@ -385,6 +385,21 @@ int qmv_matvec_qx(int wtype, int scale_dtype, int64_t rows, int64_t cols, const 
   return launch_matvec_qx(m, xqq, xd, batch, y, dev, stream) == cudaSuccess ? QMV_OK : QMV_E_CUDA;
 }
 
+int qmv_quantize_q4_fit(int scale_dtype, int64_t rows, int64_t cols, const float* src, void* W, int64_t* first_bad,
+                        cudaStream_t stream) {
+  Layout L;
+  const int st = make_layout(QMV_Q4_0, scale_dtype, rows, cols, &L);
+  if (st != QMV_OK) return st;
+  if (src == nullptr || W == nullptr || first_bad == nullptr) return QMV_E_ARG;
+  if (!aligned(src, 16) || !aligned(W, 16) || !aligned(first_bad, 8)) return QMV_E_ALIGN;
+  DeviceInfo dev;
+  if (current_device_info(&dev) != cudaSuccess) return QMV_E_CUDA;
+  return launch_quantize(kQuantQ4Fit, scale_dtype == QMV_SCALE_F16, rows, cols, src, static_cast<uint8_t*>(W), L.d_off,
+                         L.q_bytes, first_bad, dev, stream) == cudaSuccess
+             ? QMV_OK
+             : QMV_E_CUDA;
+}
+
 int qmv_check_device(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return QMV_E_CUDA;
   DeviceInfo dev;

@@ -58,7 +58,9 @@ cudaError_t encode_tmap_2d(CUtensorMap* map, int dtype, const void* base, uint64
 cudaError_t current_device_info(DeviceInfo* info);
 
 cudaError_t launch_dequant(const MatrixRef& m, float* out, cudaStream_t stream);
-// The writer rules into W (q at W, d at W + d_off; zeros between q_bytes and d_off).
+// The writer rules into W (q at W, d at W + d_off; zeros between q_bytes and d_off).  wtype:
+// QMV_Q8_0, QMV_Q4_0 (the round rule) or kQuantQ4Fit (the Q4_0 best-fit rule).
+constexpr int kQuantQ4Fit = 3;
 cudaError_t launch_quantize(int wtype, bool scale_f16, int64_t rows, int64_t cols, const float* src, uint8_t* W,
                             int64_t d_off, int64_t q_bytes, int64_t* first_bad, const DeviceInfo& dev,
                             cudaStream_t stream);

@@ -23,6 +23,96 @@ namespace qmv {
 
 namespace {
 
+// Kernel code of the Q4_0 best-fit rule (its output is a Q4_0 matrix).
+constexpr int kQ4Fit = kQuantQ4Fit;
+
+// The Q4_0 best-fit rule for one block: the largest-magnitude element m (first of equals) is
+// mapped to each candidate level L = -(60 + 2k) / 10, k = 0..12 (-6 .. -8.4); levels
+// l_j = clamp(rint(x_j / s), -8, 7) with s = m / L; d = sum(x^3 l) / sum(x^2 l^2); the candidate
+// with the smallest sum(x^2 (x - d l)^2) wins (the first on ties).  A block below 1e-6 is
+// fitted at unit scale and d scaled back; the zero block is d = 0, level 0.  Every operation
+// is one float32 operation rounded to nearest (ties to even for rint), in element order.
+template <bool F16>
+__device__ __forceinline__ void quantize_block_fit(const float (&xin)[32], long long blk, uint8_t* __restrict__ q,
+                                                   uint8_t* __restrict__ d, unsigned long long* first_bad) {
+  float x[32];
+  float m = xin[0], a = fabsf(xin[0]);
+#pragma unroll
+  for (int j = 1; j < 32; ++j)
+    if (fabsf(xin[j]) > a) {
+      a = fabsf(xin[j]);
+      m = xin[j];
+    }
+  uint32_t best_w[4] = {0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u};  // level 0 everywhere
+  float best_d = 0.f;
+  if (a != 0.f) {
+    const bool small = a < 1e-6f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) x[j] = small ? __fdiv_rn(xin[j], a) : xin[j];
+    if (small) m = __fdiv_rn(m, a);
+    float best_err = 0.f;
+#pragma unroll 1
+    for (int k = 0; k <= 12; ++k) {
+      const float L = __fdiv_rn((float)(-(60 + 2 * k)), 10.0f);
+      const float s = __fdiv_rn(m, L);
+      float lv[32];
+      float num = 0.f, den = 0.f;
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        float r = rintf(__fdiv_rn(x[j], s));
+        r = fminf(fmaxf(r, -8.0f), 7.0f);
+        lv[j] = r;
+        const float t = __fmul_rn(x[j], x[j]);
+        num = __fadd_rn(num, __fmul_rn(__fmul_rn(t, x[j]), r));
+        den = __fadd_rn(den, __fmul_rn(__fmul_rn(t, r), r));
+        const uint32_t nib = (uint32_t)((int)r + 8);
+        if (j < 16) {
+          w[j >> 2] |= nib << (8 * (j & 3));
+        } else {
+          w[(j - 16) >> 2] |= nib << (8 * ((j - 16) & 3) + 4);
+        }
+      }
+      const float dk = den == 0.f ? 0.f : __fdiv_rn(num, den);
+      float err = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float e = __fsub_rn(x[j], __fmul_rn(dk, lv[j]));
+        err = __fadd_rn(err, __fmul_rn(__fmul_rn(x[j], x[j]), __fmul_rn(e, e)));
+      }
+      if (k == 0 || err < best_err) {
+        best_err = err;
+        best_d = dk;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) best_w[i] = w[i];
+      }
+    }
+    if (small) best_d = __fmul_rn(best_d, a);
+  }
+  uint32_t dbits;
+  bool bad = false;
+  if (F16) {
+    const unsigned short h = __half_as_ushort(__float2half_rn(best_d));
+    if ((h & 0x7fffu) >= 0x7c00u) {
+      bad = true;  // refused: written as d = 0, every nibble 8
+      dbits = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) best_w[i] = 0x88888888u;
+    } else {
+      dbits = h;
+    }
+  } else {
+    dbits = __float_as_uint(best_d);
+  }
+  *reinterpret_cast<uint4*>(q + blk * 16) = make_uint4(best_w[0], best_w[1], best_w[2], best_w[3]);
+  if (F16) {
+    reinterpret_cast<uint16_t*>(d)[blk] = (uint16_t)dbits;
+  } else {
+    reinterpret_cast<uint32_t*>(d)[blk] = dbits;
+  }
+  if (bad) atomicMin(first_bad, (unsigned long long)blk);
+}
+
 // The rules for one block, held whole by one lane (x[e] = element e).
 template <int WT, bool F16>
 __device__ __forceinline__ void quantize_block(const float (&x)[32], long long blk, uint8_t* __restrict__ q,
@@ -190,7 +280,13 @@ __global__ void __launch_bounds__(kQWarps * 32) quantize_kernel(const float* __r
       x[4 * v + 3] = f[3];
     }
     const long long blk = c * 32 + lane;
-    if (blk < nblk) quantize_block<WT, F16>(x, blk, q, d, first_bad);
+    if (blk < nblk) {
+      if constexpr (WT == kQ4Fit) {
+        quantize_block_fit<F16>(x, blk, q, d, first_bad);
+      } else {
+        quantize_block<WT, F16>(x, blk, q, d, first_bad);
+      }
+    }
     __syncwarp();
   }
   cp_async_wait<0>();
@@ -296,6 +392,10 @@ cudaError_t launch_quantize(int wtype, bool scale_f16, int64_t rows, int64_t col
   if (wtype == QMV_Q8_0) {
     return scale_f16 ? launch_typed<QMV_Q8_0, true>(src, W, d, nblk, fb, dev, stream)
                      : launch_typed<QMV_Q8_0, false>(src, W, d, nblk, fb, dev, stream);
+  }
+  if (wtype == kQ4Fit) {
+    return scale_f16 ? launch_typed<kQ4Fit, true>(src, W, d, nblk, fb, dev, stream)
+                     : launch_typed<kQ4Fit, false>(src, W, d, nblk, fb, dev, stream);
   }
   return scale_f16 ? launch_typed<QMV_Q4_0, true>(src, W, d, nblk, fb, dev, stream)
                    : launch_typed<QMV_Q4_0, false>(src, W, d, nblk, fb, dev, stream);

@@ -288,6 +288,19 @@ int qmv_quantize_x(int x_dtype, int64_t batch, int64_t cols, const void *x, void
 int qmv_matvec_qx(int wtype, int scale_dtype, int64_t rows, int64_t cols, const void *W, const void *xq,
                   float *y, int batch, cudaStream_t stream);
 
+/* The Q4_0 best-fit writer (Krafla page, "Quantization rule": the search tools/mlb.py runs
+ * per block), arguments, layout and refusal as qmv_quantize with wtype QMV_Q4_0.  Per block:
+ * m = the element of largest magnitude (the first of equals); for the candidate levels
+ * L = -(60 + 2k)/10, k = 0..12 (-6 .. -8.4): s = m / L, l_j = clamp(rint(x_j / s), -8, 7)
+ * (ties to even), d = sum(x^3 l) / sum(x^2 l^2) (0 when the denominator is 0), and the
+ * candidate with the smallest sum(x^2 (x - d l)^2) wins (the first on ties); a block whose
+ * largest magnitude is below 1e-6 is fitted divided by it and d multiplied back; the zero block
+ * is d = 0 with every level 0; with f16 scales the winning d is rounded to the nearest f16.
+ * Every step is one float32 operation rounded to nearest, sums in element order.  About 13x
+ * the round rule's arithmetic per block.  Returns as qmv_quantize. */
+int qmv_quantize_q4_fit(int scale_dtype, int64_t rows, int64_t cols, const float *src, void *W,
+                        int64_t *first_bad, cudaStream_t stream);
+
 /* A compiled step: copies and grouped products recorded once as a CUDA graph and replayed by
  * one call (a decode step's host input, its products and its host output, launched together).
  *   qmv_copy  : bytes from src to dst, any mix of device and pinned host pointers (the

@@ -130,6 +130,13 @@ def test_dequant_and_validate_argument_errors(lib):
     assert lib.qmv_gguf_to_mlb(1, 4, 64, FAKE, 0, None) == binding.E_ARG
     assert lib.qmv_gguf_to_mlb(2, 4, 64, FAKE + 2, FAKE, None) == binding.E_ALIGN
     assert lib.qmv_gguf_to_mlb(2, 4, 64, FAKE, FAKE + 8, None) == binding.E_ALIGN
+    # qmv_quantize_q4_fit: the checks of qmv_quantize
+    assert lib.qmv_quantize_q4_fit(2, 64, 64, FAKE, FAKE, FAKE, None) == binding.E_FORMAT
+    assert lib.qmv_quantize_q4_fit(1, 64, 48, FAKE, FAKE, FAKE, None) == binding.E_SHAPE
+    assert lib.qmv_quantize_q4_fit(1, 64, 64, 0, FAKE, FAKE, None) == binding.E_ARG
+    assert lib.qmv_quantize_q4_fit(0, 64, 64, FAKE, FAKE, 0, None) == binding.E_ARG
+    assert lib.qmv_quantize_q4_fit(1, 64, 64, FAKE + 4, FAKE, FAKE, None) == binding.E_ALIGN
+    assert lib.qmv_quantize_q4_fit(1, 64, 64, FAKE, FAKE, FAKE + 4, None) == binding.E_ALIGN
     # qmv_quantize_x: dtype, shape, batch, null and alignment checks before any launch
     assert lib.qmv_quantize_x(2, 1, 64, FAKE, FAKE, None) == binding.E_FORMAT
     assert lib.qmv_quantize_x(0, 1, 48, FAKE, FAKE, None) == binding.E_SHAPE

@@ -151,3 +151,70 @@ def test_quantize_then_dequant_is_the_rule(qmv):
         want = oracle.dequant(oracle.quantize(src, wt, sf), wt, sf, rows, cols)
         got = out.cpu().numpy()
         assert np.array_equal(got.view(np.uint32), np.asarray(want, np.float32).view(np.uint32))
+
+
+# ------------------------------------------------------------- Q4_0 best-fit writer
+def gpu_quantize_fit(q, sf, src):
+    import torch
+    W, first = q.quantize_q4_fit(sf, dev_x(np.ascontiguousarray(src, dtype=np.float32)))
+    torch.cuda.synchronize()
+    return W.cpu().numpy(), first
+
+
+@pytest.mark.parametrize("sf", [0, 1])
+@pytest.mark.parametrize("rows,cols", [(1, 32), (3, 96), (33, 256), (256, 4096), (5, 11008)])
+def test_quantize_q4_fit_matches_oracle(qmv, sf, rows, cols):
+    rng = np.random.default_rng(rows * 5 + cols + sf)
+    src = workload_like(rng, rows, cols)
+    W, first = gpu_quantize_fit(qmv, sf, src)
+    assert first == -1
+    assert_bytes_equal(W, oracle.quantize_q4_fit(src, sf), f"fit {sf} {rows}x{cols}")
+
+
+@pytest.mark.parametrize("sf", [0, 1])
+def test_quantize_q4_fit_special_blocks(qmv, sf):
+    rng = np.random.default_rng(31 + sf)
+    blocks = list(special_blocks(rng))
+    lv = rng.integers(-5, 6, 32).astype(np.float32)
+    lv[4] = -6
+    blocks.append(lv * np.float32(0.25))                 # exactly representable at level -6
+    blocks.append(rng.standard_normal(32).astype(np.float32) * np.float32(3e-7))   # below 1e-6
+    b = rng.standard_normal(32).astype(np.float32) * np.float32(1e-6)
+    b[0] = np.float32(1e-6)
+    blocks.append(b)                                     # the threshold itself (not scaled)
+    src = np.array(blocks, dtype=np.float32)
+    for s in (src, src.reshape(1, -1)):
+        W, first = gpu_quantize_fit(qmv, sf, s)
+        assert first == -1
+        assert_bytes_equal(W, oracle.quantize_q4_fit(s, sf), f"fit special {sf} {s.shape}")
+
+
+def test_quantize_q4_fit_refuses_f16_overflow(qmv):
+    rows, cols = 4, 128
+    rng = np.random.default_rng(41)
+    src = workload_like(rng, rows, cols)
+    src[1, 32:64] = rng.standard_normal(32) * 65504.0 * 40      # block 1 * 4 + 1 = 5
+    W, first = gpu_quantize_fit(qmv, 1, src)
+    assert first == 5
+    ok = src.copy()
+    ok[1, 32:64] = 0.0
+    want = oracle.quantize_q4_fit(ok, 1)
+    assert_bytes_equal(W, want, "fit with a refused block")       # refused: d = 0, nibbles 8
+
+
+def test_quantize_q4_fit_full_size_sampled_rows(qmv):
+    # the prefill workload's 14336 x 4096 matrix on the device; rows checked against the oracle
+    # on a sample (the rule is per block, so the oracle runs on those rows alone)
+    rows, cols = 14336, 4096
+    rng = np.random.default_rng(51)
+    src = workload_like(rng, rows, cols)
+    W, first = gpu_quantize_fit(qmv, 1, src)
+    assert first == -1
+    ids = np.unique(np.concatenate([np.arange(4), rows - 1 - np.arange(4), rng.integers(0, rows, 40)]))
+    want = oracle.quantize_q4_fit(src[ids], 1)
+    qb, d_off = cols // 2, oracle.scale_offset(2, 1, rows, cols)
+    wq = W[:rows * qb].reshape(rows, qb)[ids]
+    wd = W[d_off:d_off + rows * cols // 16].reshape(rows, cols // 16)[ids]
+    d_off_s = oracle.scale_offset(2, 1, ids.size, cols)
+    assert np.array_equal(wq.reshape(-1), want[:ids.size * qb])
+    assert np.array_equal(wd.reshape(-1), want[d_off_s:d_off_s + ids.size * cols // 16])
