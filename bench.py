@@ -315,6 +315,17 @@ def other_workloads(torch, qmv, dev, l2, cap, peak_hbm, peak_tf):
     plain = _graph_time_us(torch, [lambda i=i: qmv.matvec(2, 1, 4096, 4096, Ws[i % n], x, y) for i in range(2 * n)], cap)
     ov = _graph_time_us(torch, [lambda i=i: qmv.matvec_grouped(2, 1, [(4096, 4096, Ws[i % n], x, y)], overlap=True)
                                 for i in range(2 * n)], cap)
+    # Q4_0 65536 x 4096 (151 MB), f16 scales, bf16 x, batch 1: one large launch, rotating copies
+    ml = inputs.make_matrix(2, 1, 65536, 4096, seed=0)
+    Wl = copies_for(torch.from_numpy(ml.W).to(dev), ml.W.size)
+    xl = xdev(inputs.make_x(1, 4096, True, seed=1000))
+    yl = torch.empty((1, 65536), device=dev)
+    nl = len(Wl)
+    us_l = _graph_time_us(torch, [lambda i=i: qmv.matvec(2, 1, 65536, 4096, Wl[i % nl], xl, yl) for i in range(2 * nl)],
+                          cap)
+    res["q4_65536x4096_f16_b1"] = {"us_per_product": round(us_l, 3), "weight_gbs": round(ml.W.size / us_l / 1e3, 1),
+                                   "frac_hbm": round(ml.W.size / us_l / 1e3 / peak_hbm, 4)}
+    del Wl, ml
     res["q4_4096_f16_b1"] = {"us_per_product": round(plain, 3), "weight_gbs": round(m.W.size / plain / 1e3, 1),
                              "frac_hbm": round(m.W.size / plain / 1e3 / peak_hbm, 4),
                              "overlapped_us_per_product": round(ov, 3),

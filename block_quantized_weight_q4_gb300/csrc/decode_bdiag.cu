@@ -575,15 +575,30 @@ cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* cons
   return cudaLaunchKernelEx(&cfg, matvec_bdiag_kernel<WT, F16, NW, CH, XS>, maps, p);
 }
 
-// Stages of two chunks (one-chunk stages fit more warps per SM and measured faster on large
-// Q4_0 launches alone, but slower on the Llama-7B layer step, the Q4_0 4096 x 4096 product and
-// Q8_0), in 4-warp CTAs; when that leaves SMs without a CTA (a launch with few tiles), 8-warp
-// CTAs instead if their estimate is smaller.
+// Q4_0 launches of at least this many weight bytes take one-chunk stages.
+constexpr long long kOneChunkBytes = 32LL << 20;
+
+// Stages of two chunks in 4-warp CTAs; when that leaves SMs without a CTA (a launch with few
+// tiles), 8-warp CTAs instead if their estimate is smaller.  One-chunk stages fit more warps per
+// SM (five 4-warp CTAs instead of two): measured faster on large Q4_0 launches, slower on
+// launches of a few tens of MB (the Llama-7B layer's, the 4096 x 4096 product) and on Q8_0.
 template <int WT, bool F16, bool XS>
 cudaError_t launch_best(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
                         const DeviceInfo& dev, cudaStream_t stream) {
   Plan p4, p8;
-  cudaError_t err = plan_typed<WT, F16, 4, 2, XS>(ms, n, dev, &p4);
+  cudaError_t err;
+  if (WT == QMV_Q4_0 && !XS) {
+    long long bytes = 0;
+    for (int i = 0; i < n; ++i) bytes += ms[i].rows * ms[i].cols / 2;
+    if (bytes >= kOneChunkBytes) {
+      Plan p1;
+      err = plan_typed<WT, F16, 4, 1, XS>(ms, n, dev, &p1);
+      if (err != cudaSuccess) return err;
+      if (p1.cost >= 0 && p1.grid > dev.sm_count)
+        return launch_typed<WT, F16, 4, 1, XS>(p1, ms, xs, ys, n, pdl, dev, stream);
+    }
+  }
+  err = plan_typed<WT, F16, 4, 2, XS>(ms, n, dev, &p4);
   if (err != cudaSuccess) return err;
   if (p4.cost >= 0 && p4.grid > dev.sm_count)
     return launch_typed<WT, F16, 4, 2, XS>(p4, ms, xs, ys, n, pdl, dev, stream);
