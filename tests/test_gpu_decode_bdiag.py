@@ -191,3 +191,43 @@ def test_b1_grouped_and_graph_replay_bit_identical(qmv):
     torch.cuda.synchronize()
     for p, e in zip(probs, eager):
         assert_bits_equal(p[4].cpu().numpy(), e, "graph replay")
+
+
+@pytest.mark.parametrize("sf", [1, 0])
+def test_one_chunk_stages_large_q4(qmv, sf):
+    # Q4_0 launches of 32 MB or more take one-chunk stages (five 4-warp CTAs per SM): 65536 x 4096
+    # (151 / 168 MB) against the oracle on sampled rows, and exactly on an integer case
+    import torch
+    rows, cols = 65536, 4096
+    m = inputs.make_matrix(2, sf, rows, cols, seed=500 + sf)
+    x = inputs.make_x(1, cols, True, seed=501)
+    y = run(qmv, m, x)
+    rng = np.random.default_rng(502)
+    ids = np.unique(np.concatenate([np.arange(40), rows - 1 - np.arange(40), rng.integers(0, rows, 200)]))
+    y_ref, absref = oracle.matvec_rows(m.W, 2, sf, rows, cols, x, ids)
+    check_product(y[:, ids], y_ref, absref, tol=TOL, what=f"one-chunk 65536x4096 sf{sf}")
+    # integer activations with power-of-two scales: every partial sum exact, so bit-exact
+    me = with_pow2_scales(m, 503)
+    xe = inputs.make_int_x(1, cols, True, seed=504)
+    ye = run(qmv, me, xe)
+    ye_ref, _ = oracle.matvec_rows(me.W, 2, sf, rows, cols, xe, ids)
+    assert_bits_equal(ye[:, ids], ye_ref.astype(np.float32), f"one-chunk exact sf{sf}")
+    assert torch.cuda.is_available()
+
+
+def test_one_chunk_stages_grouped_ffn(qmv):
+    # the layer's {w1, w3} launch (2 x 11008 x 4096, 50.8 MB) in one grouped call, with overlap
+    import torch
+    dim, hidden = 4096, 11008
+    ms = [inputs.make_matrix(2, 1, hidden, dim, seed=510 + i) for i in range(2)]
+    x = inputs.make_x(1, dim, True, seed=512)
+    xd = dev_x(x)
+    ys = [torch.empty((1, hidden), device="cuda") for _ in ms]
+    for _ in range(2):
+        qmv.matvec_grouped(2, 1, [(hidden, dim, dev_u8(m.W), xd, y) for m, y in zip(ms, ys)], overlap=True)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(513)
+    ids = np.unique(np.concatenate([np.arange(20), hidden - 1 - np.arange(20), rng.integers(0, hidden, 100)]))
+    for m, y in zip(ms, ys):
+        y_ref, absref = oracle.matvec_rows(m.W, 2, 1, hidden, dim, x, ids)
+        check_product(y.cpu().numpy()[:, ids], y_ref, absref, tol=TOL, what="one-chunk grouped ffn")
