@@ -231,3 +231,22 @@ def test_one_chunk_stages_grouped_ffn(qmv):
     for m, y in zip(ms, ys):
         y_ref, absref = oracle.matvec_rows(m.W, 2, 1, hidden, dim, x, ids)
         check_product(y.cpu().numpy()[:, ids], y_ref, absref, tol=TOL, what="one-chunk grouped ffn")
+
+
+@pytest.mark.parametrize("sf", [1, 0])
+@pytest.mark.parametrize("rows,cols", [(4096, 4096), (4096, 11008), (2048, 4096)])
+def test_few_tile_q4_launches(qmv, sf, rows, cols):
+    # Q4_0 launches with fewer 32-row warp tiles than SMs (4096 rows: 128 tiles; the column split
+    # and 8-warp CTAs fill the GPU): sampled rows against the oracle, an exact integer case bit for bit
+    m = inputs.make_matrix(2, sf, rows, cols, seed=520 + rows + cols + sf)
+    x = inputs.make_x(1, cols, True, seed=521)
+    y = run(qmv, m, x)
+    rng = np.random.default_rng(522)
+    ids = np.unique(np.concatenate([np.arange(40), rows - 1 - np.arange(40), rng.integers(0, rows, 200)]))
+    y_ref, absref = oracle.matvec_rows(m.W, 2, sf, rows, cols, x, ids)
+    check_product(y[:, ids], y_ref, absref, tol=TOL, what=f"few tiles {rows}x{cols} sf{sf}")
+    me = with_pow2_scales(m, 523)
+    xe = inputs.make_int_x(1, cols, True, seed=524)
+    ye = run(qmv, me, xe)
+    ye_ref, _ = oracle.matvec_rows(me.W, 2, sf, rows, cols, xe, ids)
+    assert_bits_equal(ye[:, ids], ye_ref.astype(np.float32), f"few tiles exact {rows}x{cols} sf{sf}")
