@@ -246,7 +246,8 @@ class Step:
     before / after: lists of (dst, src) tensors (device or pinned host); groups: list of
     (wtype, scale_dtype, problems, overlap[, act]) with problems as for matvec_grouped.  Creating the
     step runs it once.  The tensors are kept alive with the step; a run reads and writes the
-    same buffers.  Runs of one step must not overlap in time."""
+    same buffers.  Runs of one step must not overlap in time.  close() (or leaving a `with`
+    block) waits for the device and frees the step."""
 
     def __init__(self, groups, before=(), after=()):
         keep = [list(before), list(after)]
@@ -276,6 +277,13 @@ class Step:
             self._handle = None
             self._keep = None
             _check(st, "qmv_step_destroy")
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+        return False
 
 
 def dequant(wtype: int, scale_dtype: int, rows: int, cols: int, W, out=None, stream=None):

@@ -101,11 +101,10 @@ def test_step_of_copies_only(qmv):
     src = torch.arange(4096, dtype=torch.float32).pin_memory()
     mid = torch.empty(4096, device="cuda")
     dst = torch.zeros(4096).pin_memory()
-    step = qmv.Step([], before=[(mid, src)], after=[(dst, mid)])
-    try:
+    with qmv.Step([], before=[(mid, src)], after=[(dst, mid)]) as step:
         src.mul_(2.0)
         step.run()
         torch.cuda.current_stream().synchronize()
         assert torch.equal(dst, src)
-    finally:
-        step.close()
+    with pytest.raises(ValueError):
+        step.run()                                   # closed on leaving the block
