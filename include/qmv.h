@@ -122,7 +122,8 @@ int qmv_matrix_wtype(int file_wtype, uint32_t q8_mask, int class_bit, int shared
  * 2 MiB buffer of the calling stream (allocated on its first such call; without it, and
  * while the stream is captured before it exists, the mma.sync kernel takes them): passes
  * of 2..8 vectors then take the tensor-memory kernel (hi and lo as its 16 MMA columns) and
- * one vector the block-diagonal kernel (each block's MMAs once with hi, once with lo).  The
+ * one vector the block-diagonal kernel (each block's MMAs once with hi, once with lo; launches
+ * under 256K weights take the mma.sync kernel, which splits x the same way, in one launch).  The
  * rest take the mma.sync kernel.  The tensor-memory kernel splits tiles between CTAs;
  * their parts meet in a workspace of the calling stream (4 MiB of device memory, allocated
  * on the stream's first such call and kept; while a stream without one is being captured,
