@@ -163,3 +163,18 @@ def test_dequant_and_validate_argument_errors(lib):
 def test_strerror_never_null(lib):
     for s in (0, 2, 3, 4, 5, 6, 7, 99, -1):
         assert isinstance(lib.qmv_strerror(s), bytes) and lib.qmv_strerror(s)
+
+
+def test_binding_prototypes_match_the_header(lib):
+    # every function the header declares has a ctypes prototype in the binding with the same
+    # number of parameters (a mismatch would pass garbage through the C ABI)
+    text = open(os.path.join(ROOT, "include", "qmv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    decls = re.findall(r"\b(qmv_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", text)
+    assert len(decls) >= 19
+    for name, params in decls:
+        params = params.strip()
+        n = 0 if params in ("", "void") else params.count(",") + 1
+        fn = getattr(lib, name)
+        assert fn.argtypes is not None, f"{name}: no prototype in the binding"
+        assert len(fn.argtypes) == n, f"{name}: header has {n} parameters, binding {len(fn.argtypes)}"
