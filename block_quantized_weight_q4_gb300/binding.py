@@ -158,6 +158,7 @@ class Problem(ctypes.Structure):
 
 
 FLAG_OVERLAP = 1
+FLAG_BF16_WEIGHTS = 2
 MAX_GROUP = 8
 X_SILU_GLU_F32 = 2
 X_GELU_GLU_F32 = 3
@@ -195,15 +196,21 @@ def _problem_array(problems, act=None):
     return arr, n, batch, xdt
 
 
-def matvec_grouped(wtype: int, scale_dtype: int, problems, overlap: bool = False, stream=None, act=None):
+def _flags(overlap: bool, bf16_weights: bool = False) -> int:
+    return (FLAG_OVERLAP if overlap else 0) | (FLAG_BF16_WEIGHTS if bf16_weights else 0)
+
+
+def matvec_grouped(wtype: int, scale_dtype: int, problems, overlap: bool = False, stream=None, act=None,
+                   bf16_weights: bool = False):
     """Several products in one launch.  problems: list of (rows, cols, W, x, y) with W a
     uint8 CUDA tensor, x (batch, cols) and y (batch, rows) CUDA tensors; all share wtype,
     scale_dtype, the x dtype and batch.  overlap: QMV_FLAG_OVERLAP (the weights must not be
     written by the preceding kernel on the stream).  act: "silu" / "gelu" for gated
-    activations, x then float32 (2, batch, cols): gate, up; the product takes act(gate) * up."""
+    activations, x then float32 (2, batch, cols): gate, up; the product takes act(gate) * up.
+    bf16_weights: QMV_FLAG_BF16_WEIGHTS (prefill passes round each weight once to bfloat16)."""
     arr, n, batch, xdt = _problem_array(problems, act)
     st = load_library().qmv_matvec_grouped(wtype, scale_dtype, xdt, batch, ctypes.addressof(arr), n,
-                                           FLAG_OVERLAP if overlap else 0, _stream(stream))
+                                           _flags(overlap, bf16_weights), _stream(stream))
     _check(st, "qmv_matvec_grouped")
 
 
@@ -244,7 +251,8 @@ class Step:
     recorded once as a CUDA graph; run() enqueues it with one library call.
 
     before / after: lists of (dst, src) tensors (device or pinned host); groups: list of
-    (wtype, scale_dtype, problems, overlap[, act]) with problems as for matvec_grouped.  Creating the
+    (wtype, scale_dtype, problems, overlap[, act[, bf16_weights]]) with problems as for
+    matvec_grouped.  Creating the
     step runs it once.  The tensors are kept alive with the step; a run reads and writes the
     same buffers.  Runs of one step must not overlap in time.  close() (or leaving a `with`
     block) waits for the device and frees the step."""
@@ -257,7 +265,7 @@ class Step:
             parr, n, batch, xdt = _problem_array(problems, grp[4] if len(grp) > 4 else None)
             keep.append((parr, problems))
             garr[i] = Group(wtype, scale_dtype, xdt, batch, ctypes.addressof(parr), n,
-                            FLAG_OVERLAP if overlap else 0)
+                            _flags(overlap, len(grp) > 5 and bool(grp[5])))
         b, a = _copies(list(before)), _copies(list(after))
         handle = ctypes.c_void_p()
         st = load_library().qmv_step_create(ctypes.addressof(b), len(before), ctypes.addressof(garr), len(groups),

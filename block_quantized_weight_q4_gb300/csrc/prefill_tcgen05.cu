@@ -2,9 +2,16 @@
 // on the 5th-generation tensor core.
 //
 // What is computed (Krafla ".mlb model format v1", "Q8_0", "Q4_0", "Body"): for each row r
-// and vector n, y[n][r] = sum_c w[r][c] * x[n][c], where each weight is first dequantized
-// exactly as qmv_dequant does (fl32(level * d)) and then rounded to bfloat16; products and
-// sums are formed by the tensor core in float32.
+// and vector n, y[n][r] = sum_c w[r][c] * x[n][c], where each weight w = fl32(level * d) is
+// the exact dequantized value (as qmv_dequant forms it).  The tensor core takes bfloat16
+// operands, so each weight enters it as two bfloat16 parts: hi = RN_bf16(w) and
+// lo = RN_bf16(w - hi), and every 16-column step issues two MMAs into the same float32
+// accumulator, one with hi and one with lo.  For Q4_0 with f16 scales hi + lo equals w
+// exactly (w has at most 15 significant bits, hi takes 8 and w - hi fits in the other 7); in
+// the other formats the part lost is below 2^-17 |w|.  A single bfloat16 rounding of w (the
+// "bf16 weights" variant, one MMA per step) loses up to 2^-9 |w| per term, which is more than
+// a 1e-3 * sum |w x| tolerance allows when one term dominates an output; that variant is kept
+// for callers that ask for it.
 //
 // One CTA owns 128 rows (the MMA's M) over all columns, or, when the matrix has fewer
 // 128-row tiles than the GPU has SMs, over one of ksplit ranges of its columns (split-K: the
@@ -17,24 +24,26 @@
 //              free once the MMAs that read it complete, and the weight loads must not wait
 //              for that, hence a producer of their own.
 //   warp 1     allocates tensor memory (128 lanes x 512 columns: two f32 accumulators of 128
-//              columns, then a ring of 8 bf16-weight stages of 32 columns).
+//              columns, then a ring of bf16-weight stages: 4 stages of 64 columns, hi then lo
+//              parts, or 8 stages of 32 columns with bf16 weights).
 //   warps 1, 19  lane 0 issues, per 64-column stage (warp 1 the even ones into accumulator 0,
 //              warp 19 the odd ones into accumulator 1), four tcgen05.mma (M 128, N, K 16,
-//              bf16 in, f32 accumulate), A from the weight stage in tensor memory and B from
-//              the X stage in shared memory, then commits to the stage's "empty" barriers;
-//              after its last stage, to "accumulator full".  One issuing thread could not
-//              keep up: each instruction costs it tens of cycles while the tensor core
-//              finishes a stage in fewer.
+//              bf16 in, f32 accumulate) with the hi parts and four with the lo parts (or four
+//              with bf16 weights), A from the weight stage in tensor memory and B from the X
+//              stage in shared memory, then commits to the stage's "empty" barriers; after its
+//              last stage, to "accumulator full".  One issuing thread could not keep up: each
+//              instruction costs it tens of cycles while the tensor core finishes a stage in
+//              fewer.
 //   warps 2-17 dequantize, in two groups of eight (warps 2-9 and 10-17) that take turns
 //              with the pairs of 64-column stages: thread (row, half) of a group turns one
-//              32-weight block of its row per stage into 32 bf16 weights and stores them
-//              (tcgen05.st) to its row's tensor-memory lane, where the MMA reads them, so the
-//              weights cross shared memory only in their quantized form.  One pass of waits
-//              per pair of stages (per-stage synchronisation, not the arithmetic, set the
-//              pace when every stage had its own); two groups keep four warps per scheduler
-//              busy.  Then they read the accumulators from tensor memory (each warp its
-//              32-lane quarter and a quarter of the columns) and store y, or, for a split
-//              tile, the CTA's part (vector-major) for the last CTA to add.
+//              32-weight block of its row per stage into 32 bf16 weights (or their hi and lo
+//              parts) and stores them (tcgen05.st) to its row's tensor-memory lane, where the
+//              MMA reads them, so the weights cross shared memory only in their quantized
+//              form.  One pass of waits per pair of stages (per-stage synchronisation, not the
+//              arithmetic, set the pace when every stage had its own); two groups keep four
+//              warps per scheduler busy.  Then they read the accumulators from tensor memory
+//              (each warp its 32-lane quarter and a quarter of the columns) and store y, or,
+//              for a split tile, the CTA's part (vector-major) for the last CTA to add.
 // Every wait is bounded; a wait that runs out records QMV_E_TIMEOUT and the roles unwind.
 #include "qmv_common.cuh"
 #include "qmv_internal.h"
@@ -54,11 +63,19 @@ constexpr int kXWarp = 2 + kDeqWarps;  // the X-stage producer
 constexpr int kMmaWarp2 = 3 + kDeqWarps;  // the second MMA issuer (odd stages)
 constexpr int kThreads = 32 * (4 + kDeqWarps);
 constexpr int kMaxN = 128;    // activation vectors per pass
-constexpr int kKS = 8;        // ring depth of the bf16-weight stages (in tensor memory)
+constexpr int kMaxKS = 8;     // deepest ring of weight stages in tensor memory
 constexpr int kAccCol = 0;    // accumulators: columns 0..127 (even stages), 128..255 (odd stages)
-constexpr int kACol = 256;    // weight ring: stage s at columns 256 + 32 s (128 lanes x 64 bf16)
+constexpr int kACol = 256;    // weight ring from column 256 (128 lanes x 64 bf16 per part of a stage)
 constexpr int kTmemCols = 512;
-static_assert(kACol + 32 * kKS <= kTmemCols, "tensor memory");
+// ring of weight stages in tensor memory: HILO (hi and lo parts, 64 columns per stage) 4
+// stages, bf16 weights (32 columns per stage) 8; a multiple of 4, since the two dequantize
+// groups take turns with pairs of stages
+template <bool HILO>
+struct Ring {
+  static constexpr int kStageCols = HILO ? 64 : 32;
+  static constexpr int kKS = HILO ? 4 : 8;
+  static_assert(kACol + kStageCols * kKS <= kTmemCols && kKS <= kMaxKS && kKS % 4 == 0, "tensor memory");
+};
 
 template <int WT, bool F16>
 struct PCfg {
@@ -71,9 +88,9 @@ struct PCfg {
   static constexpr int OFF_Q = 0;  // raw ring, then scales, barriers, flags, then the X ring
   static constexpr int OFF_D = OFF_Q + kRS * Q_RAW;
   static constexpr int OFF_BAR = OFF_D + kRS * D_RAW;
-  // barriers: raw_full[kRS], raw_empty[kRS], a_full[kKS], empty[kKS], x_full[kMaxXS],
+  // barriers: raw_full[kRS], raw_empty[kRS], a_full[kMaxKS], empty[kMaxKS], x_full[kMaxXS],
   // x_empty[kMaxXS], acc_full
-  static constexpr int NBARS = 2 * kRS + 2 * kKS + 2 * kMaxXS + 1;
+  static constexpr int NBARS = 2 * kRS + 2 * kMaxKS + 2 * kMaxXS + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;  // tensor-memory base, failure and last flags
   static constexpr int OFF_X = (OFF_MISC + 16 + 1023) / 1024 * 1024;  // X ring (1024-aligned stages)
   // shared memory of a launch with xs X stages of npad vectors
@@ -201,8 +218,111 @@ __device__ __forceinline__ void q8_block_to_bf16(const uint32_t (&w)[8], float d
   }
 }
 
-__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+// ---------------------------------------------------------------- hi and lo parts
+// hi = RN_bf16(v) with finite values beyond the bfloat16 range (and infinities) saturated to
+// the largest finite bfloat16, so that v - hi stays meaningful; lo = RN_bf16(v - hi).  v - hi is
+// exact in float32 (hi is v rounded to fewer bits, within a factor of two of v).  An infinite v
+// gives hi = +-max and lo = +-inf, a NaN gives NaN in both, so hi x + lo x follows v x.
+__device__ __forceinline__ void split2_bf16(float a, float b, uint32_t& hi, uint32_t& lo) {
+  asm("cvt.rn.satfinite.bf16x2.f32 %0, %1, %2;" : "=r"(hi) : "f"(b), "f"(a));
+  float ra, rb;
+  asm("{\n\t.reg .b64 va, vh, vr;\n\t"
+      "mov.b64 va, {%2, %3};\n\t"
+      "mov.b64 vh, {%4, %5};\n\t"
+      "sub.rn.f32x2 vr, va, vh;\n\t"
+      "mov.b64 {%0, %1}, vr;\n\t}"
+      : "=f"(ra), "=f"(rb)
+      : "f"(a), "f"(b), "f"(__uint_as_float(hi << 16)), "f"(__uint_as_float(hi & 0xFFFF0000u)));
+  lo = pack_bf16x2(ra, rb);
+}
+
+// fl32(a * d), fl32(b * d) (one packed float32 multiply) as hi and lo bfloat16 pairs.
+__device__ __forceinline__ void scale2_hilo(float a, float b, float d, uint32_t& hi, uint32_t& lo) {
+  float ra, rb;
+  asm("{\n\t.reg .b64 va, vd, vr;\n\t"
+      "mov.b64 va, {%2, %3};\n\t"
+      "mov.b64 vd, {%4, %4};\n\t"
+      "mul.rn.f32x2 vr, va, vd;\n\t"
+      "mov.b64 {%0, %1}, vr;\n\t}"
+      : "=f"(ra), "=f"(rb)
+      : "f"(a), "f"(b), "f"(d));
+  split2_bf16(ra, rb, hi, lo);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_add_rn(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// A bfloat16 level pair l (exact integers, |l| <= 8) times an IEEE-half scale d split as
+// d = dh + dl (dh = RN_bf16(d), dl exact with at most 3 significant bits; split_half_scale):
+//   m  = l * dl                (at most 7 bits: exact)
+//   hi = RN_bf16(l * dh + m)   = RN_bf16(l * d)
+//   t  = l * dh - hi           (exact: a multiple of ulp(dh) of magnitude below 16 ulp(dh))
+//   lo = t + m                 = l * d - hi (exact: w = l * d has at most 15 significant bits,
+//                               hi the leading 8, so w - hi fits in bfloat16's 8)
+// so hi + lo = l * d exactly.  Four packed bfloat16 operations per pair.
+__device__ __forceinline__ void scale_bf16_levels_hilo(uint32_t l2, uint32_t hi2, uint32_t lo2, uint32_t& h,
+                                                       uint32_t& l) {
+  const uint32_t m = bf16x2_mul_rn(l2, lo2);
+  h = bf16x2_fma_rn(l2, hi2, m);
+  const uint32_t t = bf16x2_fma_rn(l2, hi2, h ^ 0x80008000u);  // fma with -hi (sign bits flipped)
+  l = bf16x2_add_rn(t, m);
+}
+
+// One Q4_0 block with an IEEE-half scale (split by split_half_scale) to the hi and lo parts
+// of its 32 weights (hi + lo = level * d exactly; pairs in the order of q4_block_to_bf16).
+// A scale that is not finite gives lo = 0 (hi then carries the infinity or NaN).
+__device__ __forceinline__ void q4_block_to_hilo_split(const uint32_t (&w)[4], uint32_t hi2, uint32_t lo2,
+                                                       bool finite, uint32_t (&hi)[16], uint32_t (&lo)[16]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t lo01, lo23, hi01, hi23;
+    q4_word_to_bf16_levels(w[i], lo01, lo23, hi01, hi23);
+    scale_bf16_levels_hilo(lo01, hi2, lo2, hi[2 * i], lo[2 * i]);
+    scale_bf16_levels_hilo(lo23, hi2, lo2, hi[2 * i + 1], lo[2 * i + 1]);
+    scale_bf16_levels_hilo(hi01, hi2, lo2, hi[8 + 2 * i], lo[8 + 2 * i]);
+    scale_bf16_levels_hilo(hi23, hi2, lo2, hi[8 + 2 * i + 1], lo[8 + 2 * i + 1]);
+  }
+  if (!finite) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) lo[i] = 0u;
+  }
+}
+
+// One Q4_0 block with a float32 scale to the hi and lo parts of fl32(level * d).
+__device__ __forceinline__ void q4_block_to_hilo(const uint32_t (&w)[4], float d, uint32_t (&hi)[16],
+                                                 uint32_t (&lo)[16]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t lo01, lo23, hi01, hi23;
+    q4_word_to_f16_levels(w[i], lo01, lo23, hi01, hi23);
+#define QMV_HALF_PAIR(h2, k)                                                                                 \
+  scale2_hilo(__half2float(__ushort_as_half(static_cast<unsigned short>((h2) & 0xFFFFu))),                  \
+              __half2float(__ushort_as_half(static_cast<unsigned short>((h2) >> 16))), d, hi[k], lo[k])
+    QMV_HALF_PAIR(lo01, 2 * i);
+    QMV_HALF_PAIR(lo23, 2 * i + 1);
+    QMV_HALF_PAIR(hi01, 8 + 2 * i);
+    QMV_HALF_PAIR(hi23, 8 + 2 * i + 1);
+#undef QMV_HALF_PAIR
+  }
+}
+
+// One Q8_0 block (32 int8 quants in w[0..7]) to the hi and lo parts of fl32(q * d).
+__device__ __forceinline__ void q8_block_to_hilo(const uint32_t (&w)[8], float d, uint32_t (&hi)[16],
+                                                 uint32_t (&lo)[16]) {
+  const float bias = 8388736.0f;  // 2^23 + 128
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t u = w[i] ^ 0x80808080u;  // q + 128 per byte
+    const float f0 = __fsub_rn(__uint_as_float(prmt(u, 0x4B000000u, 0x7440)), bias);
+    const float f1 = __fsub_rn(__uint_as_float(prmt(u, 0x4B000000u, 0x7441)), bias);
+    const float f2 = __fsub_rn(__uint_as_float(prmt(u, 0x4B000000u, 0x7442)), bias);
+    const float f3 = __fsub_rn(__uint_as_float(prmt(u, 0x4B000000u, 0x7443)), bias);
+    scale2_hilo(f0, f1, d, hi[2 * i], lo[2 * i]);
+    scale2_hilo(f2, f3, d, hi[2 * i + 1], lo[2 * i + 1]);
+  }
 }
 
 __device__ __forceinline__ void lds128(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
@@ -230,12 +350,14 @@ __device__ __forceinline__ bool pwait(uint64_t* bar, uint32_t parity, volatile i
   return false;
 }
 
-template <int WT, bool F16>
+template <int WT, bool F16, bool HILO>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tq,
                                                               const __grid_constant__ CUtensorMap td,
                                                               const __grid_constant__ CUtensorMap tx,
                                                               const PParams p) {
   using C = PCfg<WT, F16>;
+  constexpr int kKS = Ring<HILO>::kKS;
+  constexpr int kSC = Ring<HILO>::kStageCols;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);  // 1024-aligned: swizzle atoms
@@ -247,8 +369,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   uint64_t* raw_full = bars;
   uint64_t* raw_empty = bars + kRS;
   uint64_t* a_full = bars + 2 * kRS;
-  uint64_t* empty = a_full + kKS;
-  uint64_t* x_full = empty + kKS;
+  uint64_t* empty = a_full + kMaxKS;
+  uint64_t* x_full = empty + kMaxKS;
   uint64_t* x_empty = x_full + kMaxXS;
   uint64_t* acc_full = x_empty + kMaxXS;
   const uint32_t xstage = (uint32_t)p.npad * 128;  // bytes of one X stage
@@ -360,11 +482,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       for (int kb = m; kb < nkb; kb += 2) {
         if (!pwait(&x_full[xs], xph, failed, p.status) || !pwait(&a_full[s], aph, failed, p.status)) break;
         tc_fence_after();
-        const uint32_t a0 = tmem + (uint32_t)(kACol + 32 * s);  // A: 128 lanes x 32 columns (two bf16 each)
+        // A: 128 lanes x 32 columns (two bf16 each) of hi parts (or bf16 weights), then as many
+        // of lo parts
+        const uint32_t a0 = tmem + (uint32_t)(kACol + kSC * s);
         const uint32_t b0 = sbase + C::OFF_X + xs * xstage;
 #pragma unroll
-        for (int k = 0; k < kKB / 16; ++k)
-          tc_mma_f16_ts(acc, a0 + 8 * k, smem_desc_sw128(b0 + 32 * k), idesc, ((kb - m) | k) != 0);
+        for (int k = 0; k < kKB / 16; ++k) {
+          const uint64_t bdesc = smem_desc_sw128(b0 + 32 * k);
+          tc_mma_f16_ts(acc, a0 + 8 * k, bdesc, idesc, ((kb - m) | k) != 0);
+          if (HILO) tc_mma_f16_ts(acc, a0 + 32 + 8 * k, bdesc, idesc, true);
+        }
         tc_commit(smem_u32(&empty[s]));     // the weight stage is free once these MMAs complete
         tc_commit(smem_u32(&x_empty[xs]));  // and so is the X stage
         xs += 2;
@@ -390,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const int row = 32 * (warp & 3) + lane;
     const int h = (dt >> 7) & 1;  // which block of each 64-column stage
     const int sw = row & 7;
-    const uint32_t a_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(kACol + 16 * h);
+    const uint32_t a_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(kACol + 16 * h);  // hi part
     // stages kb and kb + 1 (slots s and s + 1 of the weight ring, blocks blk and blk + 2 of
     // the raw stage)
     int s = 2 * grp;   // slot of stage kb in the weight ring (kb % kKS; stage kb + 1 takes s + 1)
@@ -414,7 +541,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         d0 = ds[blk];
         d1 = ds[blk + 2];
       }
-      uint32_t out0[16], out1[16];
+      uint32_t out0[16], out1[16];  // hi parts (or bf16 weights) of blocks blk and blk + 2
+      uint32_t lo0[16], lo1[16];    // lo parts (HILO)
       const uint32_t qrow = sbase + C::OFF_Q + r * C::Q_RAW + row * 128;
       if (WT == QMV_Q4_0) {
         uint32_t w0[4], w1[4];
@@ -424,8 +552,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           uint32_t h0, l0, h1, l1;
           split_half_scale(d0, h0, l0);
           split_half_scale(d1, h1, l1);
-          q4_block_to_bf16_split(w0, h0, l0, out0);
-          q4_block_to_bf16_split(w1, h1, l1, out1);
+          if (HILO) {
+            q4_block_to_hilo_split(w0, h0, l0, isfinite(d0), out0, lo0);
+            q4_block_to_hilo_split(w1, h1, l1, isfinite(d1), out1, lo1);
+          } else {
+            q4_block_to_bf16_split(w0, h0, l0, out0);
+            q4_block_to_bf16_split(w1, h1, l1, out1);
+          }
+        } else if (HILO) {
+          q4_block_to_hilo(w0, d0, out0, lo0);
+          q4_block_to_hilo(w1, d1, out1, lo1);
         } else {
           q4_block_to_bf16(w0, d0, out0);
           q4_block_to_bf16(w1, d1, out1);
@@ -438,12 +574,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         lds128(box + (((c0 + 1) ^ sw) << 4), w0[4], w0[5], w0[6], w0[7]);
         lds128(box + (((c0 + 4) ^ sw) << 4), w1[0], w1[1], w1[2], w1[3]);
         lds128(box + (((c0 + 5) ^ sw) << 4), w1[4], w1[5], w1[6], w1[7]);
-        q8_block_to_bf16(w0, d0, out0);
-        q8_block_to_bf16(w1, d1, out1);
+        if (HILO) {
+          q8_block_to_hilo(w0, d0, out0, lo0);
+          q8_block_to_hilo(w1, d1, out1, lo1);
+        } else {
+          q8_block_to_bf16(w0, d0, out0);
+          q8_block_to_bf16(w1, d1, out1);
+        }
       }
-      // the block's 32 bf16 weights (pairs in element order) into 16 columns of this row's lane
-      tmem_st16(a_lane + (uint32_t)(32 * s), out0);
-      tmem_st16(a_lane + (uint32_t)(32 * (s + 1)), out1);
+      // the block's 32 bf16 weights (pairs in element order) into 16 columns of this row's lane;
+      // the lo parts 32 columns further on
+      tmem_st16(a_lane + (uint32_t)(kSC * s), out0);
+      tmem_st16(a_lane + (uint32_t)(kSC * (s + 1)), out1);
+      if (HILO) {
+        tmem_st16(a_lane + (uint32_t)(kSC * s + 32), lo0);
+        tmem_st16(a_lane + (uint32_t)(kSC * (s + 1) + 32), lo1);
+      }
       tmem_st_wait();
       tc_fence_before();  // the stores are complete before the arrivals below
       __syncwarp();
@@ -589,11 +735,11 @@ static int prefill_ksplit(const MatrixRef& m, int npad, const DeviceInfo& dev, c
   return k < 1 ? 1 : (int)k;
 }
 
-template <int WT, bool F16>
+template <int WT, bool F16, bool HILO>
 static cudaError_t launch_prefill_typed(const MatrixRef& m, const void* x, float* y, int batch, const DeviceInfo& dev,
                                         const Workspace* ws, bool pdl, cudaStream_t stream) {
   using C = PCfg<WT, F16>;
-  auto kern = prefill_kernel<WT, F16>;
+  auto kern = prefill_kernel<WT, F16, HILO>;
   static bool ready[64] = {};
   if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
   if (!ready[dev.device]) {
@@ -645,15 +791,22 @@ static cudaError_t launch_prefill_typed(const MatrixRef& m, const void* x, float
   return cudaLaunchKernelEx(&cfg, kern, tq, td, tx, p);
 }
 
-cudaError_t launch_prefill(const MatrixRef& m, const void* x, float* y, int batch, const DeviceInfo& dev,
-                           const Workspace* ws, bool pdl, cudaStream_t stream) {
-  if (batch < 1 || batch > kMaxN) return cudaErrorInvalidValue;
+template <bool HILO>
+static cudaError_t launch_prefill_ring(const MatrixRef& m, const void* x, float* y, int batch, const DeviceInfo& dev,
+                                       const Workspace* ws, bool pdl, cudaStream_t stream) {
   if (m.wtype == QMV_Q4_0) {
-    return m.scale_f16 ? launch_prefill_typed<QMV_Q4_0, true>(m, x, y, batch, dev, ws, pdl, stream)
-                       : launch_prefill_typed<QMV_Q4_0, false>(m, x, y, batch, dev, ws, pdl, stream);
+    return m.scale_f16 ? launch_prefill_typed<QMV_Q4_0, true, HILO>(m, x, y, batch, dev, ws, pdl, stream)
+                       : launch_prefill_typed<QMV_Q4_0, false, HILO>(m, x, y, batch, dev, ws, pdl, stream);
   }
-  return m.scale_f16 ? launch_prefill_typed<QMV_Q8_0, true>(m, x, y, batch, dev, ws, pdl, stream)
-                     : launch_prefill_typed<QMV_Q8_0, false>(m, x, y, batch, dev, ws, pdl, stream);
+  return m.scale_f16 ? launch_prefill_typed<QMV_Q8_0, true, HILO>(m, x, y, batch, dev, ws, pdl, stream)
+                     : launch_prefill_typed<QMV_Q8_0, false, HILO>(m, x, y, batch, dev, ws, pdl, stream);
+}
+
+cudaError_t launch_prefill(const MatrixRef& m, const void* x, float* y, int batch, bool bf16_weights,
+                           const DeviceInfo& dev, const Workspace* ws, bool pdl, cudaStream_t stream) {
+  if (batch < 1 || batch > kMaxN) return cudaErrorInvalidValue;
+  return bf16_weights ? launch_prefill_ring<false>(m, x, y, batch, dev, ws, pdl, stream)
+                      : launch_prefill_ring<true>(m, x, y, batch, dev, ws, pdl, stream);
 }
 
 }  // namespace qmv

@@ -93,24 +93,40 @@ using namespace qmv;
 
 // Scratch of qmv_matvec_grouped_noalloc: split-tile arrival counters and partial sums of
 // the tensor-memory decode kernel for up to QMV_NOALLOC_MAX_CTAS CTAs, in the layout of a
-// per-stream workspace.  Zero-initialized when the module loads; every call clears the
-// counters again before its launch.
+// per-stream workspace.  Zero-initialized when this module is loaded onto a device (on the
+// library's first call that needs it there: modules load lazily).  A launch that completes
+// leaves the counters at zero (the last arrival at a split tile resets its counter); after a
+// kernel gave up on a bounded wait, qmv_check_device() clears them.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[QMV_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+}  // namespace
 
 // Device address of g_noalloc_scratch on `device` (the current device), looked up once.
 static cudaError_t noalloc_scratch(int device, void** base) {
-  static std::mutex mu;
-  static void* addr[kMaxDevices] = {};
   if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
-  if (addr[device] == nullptr) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_addr[device] == nullptr) {
     void* p = nullptr;
     const cudaError_t err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (err != cudaSuccess) return err;
-    addr[device] = p;
+    g_noalloc_addr[device] = p;
   }
-  *base = addr[device];
+  *base = g_noalloc_addr[device];
   return cudaSuccess;
+}
+
+// Zero the arrival counters of g_noalloc_scratch on `device` (the current device) if the
+// entry point has been used there; synchronous.
+static cudaError_t noalloc_reset(int device) {
+  if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_addr[device] == nullptr) return cudaSuccess;
+  Workspace ws;
+  workspace_carve(g_noalloc_addr[device], sizeof(g_noalloc_scratch), QMV_NOALLOC_MAX_CTAS, &ws);
+  return cudaMemset(ws.counters, 0, workspace_counter_bytes(ws.max_counters));
 }
 
 extern "C" {
@@ -147,7 +163,7 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
       x_dtype != QMV_X_GELU_GLU_F32)
     return QMV_E_FORMAT;
   if (batch < 0) return QMV_E_ARG;
-  if ((flags & ~QMV_FLAG_OVERLAP) != 0) return QMV_E_ARG;
+  if ((flags & ~(QMV_FLAG_OVERLAP | QMV_FLAG_BF16_WEIGHTS)) != 0) return QMV_E_ARG;
   // gated activations: x holds gate then up (batch x cols float32 each); act(gate) * up is
   // formed in the activation prep of the float32 routes
   const bool glu = x_dtype == QMV_X_SILU_GLU_F32 || x_dtype == QMV_X_GELU_GLU_F32;
@@ -184,7 +200,9 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
         const int nb = (batch - b0) < pmax ? (batch - b0) : pmax;
         const void* xp = static_cast<const uint8_t*>(problems[i].x) + (size_t)b0 * (size_t)ms[i].cols * xsz;
         float* yp = problems[i].y + (size_t)b0 * (size_t)ms[i].rows;
-        if (launch_prefill(ms[i], xp, yp, nb, dev, pw, pdl, stream) != cudaSuccess) return QMV_E_CUDA;
+        if (launch_prefill(ms[i], xp, yp, nb, (flags & QMV_FLAG_BF16_WEIGHTS) != 0, dev, pw, pdl, stream) !=
+            cudaSuccess)
+          return QMV_E_CUDA;
       }
     } else {
       any_decode = true;
@@ -252,7 +270,7 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
 int qmv_matvec_grouped_noalloc(int wtype, int scale_dtype, int x_dtype, int batch, const qmv_problem* problems,
                                int n, unsigned flags, cudaStream_t stream) {
   if (problems == nullptr || n < 1 || n > QMV_MAX_GROUP) return QMV_E_ARG;
-  if (x_dtype != QMV_X_F32 && x_dtype != QMV_X_BF16) return QMV_E_FORMAT;
+  if (x_dtype != QMV_X_BF16) return QMV_E_FORMAT;  // the tensor-memory kernel reads bf16 only
   if (batch < 0 || batch > QMV_NOALLOC_MAX_BATCH) return QMV_E_ARG;
   if ((flags & ~QMV_FLAG_OVERLAP) != 0) return QMV_E_ARG;
   MatrixRef ms[QMV_MAX_GROUP];
@@ -269,7 +287,6 @@ int qmv_matvec_grouped_noalloc(int wtype, int scale_dtype, int x_dtype, int batc
     if (pr.x == nullptr || pr.y == nullptr) return QMV_E_ARG;
     if (!aligned(pr.x, 16) || !aligned(pr.y, 4)) return QMV_E_ALIGN;
   }
-  if (x_dtype != QMV_X_BF16) return QMV_E_FORMAT;  // the tensor-memory kernel reads bf16 only
   if (batch == 0) return QMV_OK;
   DeviceInfo dev;
   if (current_device_info(&dev) != cudaSuccess) return QMV_E_CUDA;
@@ -277,8 +294,6 @@ int qmv_matvec_grouped_noalloc(int wtype, int scale_dtype, int x_dtype, int batc
   if (noalloc_scratch(dev.device, &base) != cudaSuccess) return QMV_E_CUDA;
   Workspace ws;
   workspace_carve(base, sizeof(g_noalloc_scratch), QMV_NOALLOC_MAX_CTAS, &ws);
-  if (cudaMemsetAsync(ws.counters, 0, workspace_counter_bytes(ws.max_counters), stream) != cudaSuccess)
-    return QMV_E_CUDA;
   const bool pdl = (flags & QMV_FLAG_OVERLAP) != 0;
   return launch_decode_tc(ms, xs, ys, n, batch, pdl, dev, ws, stream) == cudaSuccess ? QMV_OK : QMV_E_CUDA;
 }
@@ -414,6 +429,7 @@ int qmv_check_device(void) {
     if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return QMV_E_CUDA;
     // a kernel that gave up may have left a split tile's arrival counter part-way
     if (reset_workspaces() != cudaSuccess) return QMV_E_CUDA;
+    if (noalloc_reset(dev.device) != cudaSuccess) return QMV_E_CUDA;
   }
   return v;
 }

@@ -109,15 +109,16 @@ cudaError_t launch_matvec_bdiag_split(const MatrixRef* ms, const void* const* xs
 cudaError_t launch_matvec_bdiag_f32(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
                                     const DeviceInfo& dev, cudaStream_t stream, int act = -1, long long up_batch = 0);
 
-// Batched product on the 5th-generation tensor core (weights dequantized to bf16 in tensor
-// memory, tcgen05 MMA, f32 accumulators in tensor memory): bf16 activations, cols % 256 == 0,
-// 1..128 vectors per launch (meant for 16 and more).  ws: the stream's prefill workspace, or
-// null (then no tile is split between CTAs).  pdl: launch as a programmatic dependent of the
-// preceding kernel (weights are read before that kernel finishes).
+// Batched product on the 5th-generation tensor core (weights dequantized in tensor memory as
+// bf16 hi + lo parts, or rounded once to bf16 when bf16_weights; tcgen05 MMA, f32 accumulators
+// in tensor memory): bf16 activations, cols % 256 == 0, 1..128 vectors per launch (meant for
+// 16 and more).  ws: the stream's prefill workspace, or null (then no tile is split between
+// CTAs).  pdl: launch as a programmatic dependent of the preceding kernel (weights are read
+// before that kernel finishes).
 bool prefill_supported(const MatrixRef& m, bool x_bf16);
 int prefill_max_batch();
-cudaError_t launch_prefill(const MatrixRef& m, const void* x, float* y, int batch, const DeviceInfo& dev,
-                           const Workspace* ws, bool pdl, cudaStream_t stream);
+cudaError_t launch_prefill(const MatrixRef& m, const void* x, float* y, int batch, bool bf16_weights,
+                           const DeviceInfo& dev, const Workspace* ws, bool pdl, cudaStream_t stream);
 
 // Decode product on the 5th-generation tensor core with the weights unpacked into tensor
 // memory: bf16 activations, cols % 256 == 0, 1..8 vectors, 1..decode_tc_max_problems()

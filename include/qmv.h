@@ -129,13 +129,17 @@ int qmv_matrix_wtype(int file_wtype, uint32_t q8_mask, int class_bit, int shared
  * on the stream's first such call and kept; while a stream without one is being captured,
  * the call takes the mma.sync kernel instead).  Results do not depend on timing.
  * bfloat16 batches of 16 and more (cols % 256 == 0) run in passes of up to 128 through the
- * prefill kernel (each weight dequantized as qmv_dequant does and rounded to bfloat16 in
- * shared memory, tcgen05 MMA into tensor memory, f32 accumulate); a matrix with fewer
+ * prefill kernel: each weight w is dequantized as qmv_dequant does and enters the tensor core
+ * as two bfloat16 parts hi = RN_bf16(w) and lo = RN_bf16(w - hi) (for Q4_0 with f16 scales
+ * hi + lo = w exactly; otherwise within 2^-17 |w|, and within 2^-134 absolute for the
+ * weights below 2^-117 that only float32 scales under 2^-120 produce), stored to tensor
+ * memory; two tcgen05 MMAs per 16 columns (hi, then lo) accumulate in f32 in tensor memory.  A matrix with fewer
  * 128-row tiles than the GPU has SMs has its columns split between CTAs, whose parts meet in
  * a second workspace of the calling stream (32 MiB, allocated like the first; without it the
  * call does not split).
  * Products agree with an
- * exact evaluation to within 1e-3 * sum_c |W[r][c] x[c]| per output.  A Q8_0 byte of
+ * exact evaluation to within 1e-3 * sum_c |W[r][c] x[c]| per output (on the prefill route with
+ * float32 scales, for weights of magnitude 2^-124 or more).  A Q8_0 byte of
  * -128 is not rejected here: it decodes as -128 * d (see qmv_validate).
  * Returns QMV_OK, or QMV_E_FORMAT / QMV_E_SHAPE / QMV_E_ARG / QMV_E_ALIGN before any
  * launch, or QMV_E_CUDA. */
@@ -159,15 +163,24 @@ typedef struct qmv_problem {
  *   the stream, so that this launch's first weight tiles are fetched while that kernel
  *   finishes.  Activations are read, and y written, only after the preceding kernel has
  *   completed; the WEIGHTS however may be read earlier, so they must not be written by
- *   the immediately preceding kernel (true for model weights after loading). */
+ *   the immediately preceding kernel (true for model weights after loading).
+ * QMV_FLAG_BF16_WEIGHTS: for the problems that take the prefill kernel (16 or more bf16
+ *   vectors), round each dequantized weight once to bfloat16 instead of passing it as hi + lo
+ *   parts: one MMA per 16 columns instead of two.  Each term then carries a relative error of
+ *   up to 2^-9, so an output dominated by a few terms (short rows, concentrated activations)
+ *   can miss the 1e-3 * sum |W x| tolerance stated for qmv_matvec; with many comparable terms
+ *   the rounding errors largely cancel.  No effect on the other kernels, which use exact
+ *   levels. */
 #define QMV_FLAG_OVERLAP 1u
+#define QMV_FLAG_BF16_WEIGHTS 2u
 
 /* Several products in one launch (Krafla page, "Body": the projections of a layer, e.g.
  * wq, wk, wv reading the same normalized input, or w1 and w3).  All n problems share
  * wtype, scale_dtype, x_dtype and batch; each has its own rows, cols, W, x and y.  Same
- * results as n calls of qmv_matvec.  problems is a host array of n entries, read during
- * the call only; 1 <= n <= QMV_MAX_GROUP, else QMV_E_ARG.  Returns as qmv_matvec (the
- * first failing problem decides the code; nothing is launched then). */
+ * results as n calls of qmv_matvec (without QMV_FLAG_BF16_WEIGHTS).  problems is a host array
+ * of n entries, read during the call only; 1 <= n <= QMV_MAX_GROUP, else QMV_E_ARG; flags
+ * other than the QMV_FLAG_* above give QMV_E_ARG.  Returns as qmv_matvec (the first failing
+ * problem decides the code; nothing is launched then). */
 int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const qmv_problem *problems, int n,
                        unsigned flags, cudaStream_t stream);
 
@@ -186,26 +199,35 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
  * It runs the tensor-memory decode kernel (bf16 activations, weights unpacked into tensor
  * memory, tcgen05 MMA), whose tiles may be split between CTAs; the split tiles' partial
  * sums and arrival counters live in one fixed array inside the library
- * (QMV_NOALLOC_SCRATCH_BYTES of device memory per device, allocated when the library is
- * loaded) instead of the per-stream workspace that qmv_matvec_grouped allocates on a
- * stream's first such call.  Nothing is allocated, freed or resized by this call.
+ * (QMV_NOALLOC_SCRATCH_BYTES of device memory per device) instead of the per-stream workspace
+ * that qmv_matvec_grouped allocates on a stream's first such call.  Nothing is allocated,
+ * freed or resized by this call.
  *
- * Same arguments and results as qmv_matvec_grouped, restricted to what that kernel takes:
+ * Set-up on first use.  CUDA loads the library's device code lazily: the array, and the
+ * kernel it serves, come into existence on a device at the first call that needs them there,
+ * and the first call on each device also looks up the array's address (cudaGetSymbolAddress,
+ * with that device current) and sets the kernel's shared-memory limit.  That first call
+ * therefore takes device memory (the array and the kernel's code); make one call per device
+ * (any valid arguments) before handing the remaining device memory to a pool, and before
+ * capturing a stream if the calls are to be captured.  Later calls take no memory.
+ *
+ * Same arguments and results as qmv_matvec_grouped, restricted to what that kernel takes.
+ * The checks, all made before any launch, in this order:
+ *   problems non-null and 1 <= n <= QMV_MAX_GROUP, else QMV_E_ARG;
  *   x_dtype must be QMV_X_BF16, else QMV_E_FORMAT;
  *   0 <= batch <= QMV_NOALLOC_MAX_BATCH, else QMV_E_ARG (larger batches: call once per
  *     group of at most 8 vectors);
- *   cols % 256 == 0 and rows < 2^31 - 256 for every problem, else QMV_E_SHAPE.
- * All checks happen before any launch.  The kernel uses at most QMV_NOALLOC_MAX_CTAS CTAs
- * (fewer on a device with fewer SMs).
+ *   flags only QMV_FLAG_OVERLAP, else QMV_E_ARG;
+ *   per problem as qmv_matvec_grouped, and cols % 256 == 0 and rows < 2^31 - 256, else
+ *     QMV_E_SHAPE.
+ * The kernel uses at most QMV_NOALLOC_MAX_CTAS CTAs (fewer on a device with fewer SMs).
  *
- * The arrival counters in the array must be zero when the kernel starts: every call first
- * clears them on `stream` (cudaMemsetAsync of 1536 bytes, not an allocation), and a call that
- * completes leaves them at zero.  The array is shared by all calls on a device, so calls
- * that may overlap in time (on different streams, or from different host threads without
- * ordering) race on it and give wrong results: order them on one stream.  The first call
- * on each device looks up the array's address (cudaGetSymbolAddress, with that device
- * current) and sets the kernel's shared-memory limit; make that first call before
- * capturing the stream, if the stream is to be captured. */
+ * The arrival counters in the array must be zero when the kernel starts.  A call that
+ * completes leaves them at zero; a kernel that gave up on a bounded wait (QMV_E_TIMEOUT from
+ * qmv_check_device) may leave them part-way, and qmv_check_device() then clears them.  The
+ * array is shared by all calls on a device, so calls that may overlap in time (on different
+ * streams, or from different host threads without ordering) race on it and give wrong
+ * results: order them on one stream. */
 int qmv_matvec_grouped_noalloc(int wtype, int scale_dtype, int x_dtype, int batch, const qmv_problem *problems,
                                int n, unsigned flags, cudaStream_t stream);
 
@@ -348,7 +370,11 @@ int qmv_step_destroy(qmv_step *step);
 
 /* Synchronizes the current device, then returns and clears the status word that the
  * kernels set when a bounded wait runs out (QMV_E_TIMEOUT); QMV_OK when none was set,
- * QMV_E_CUDA when the device reports a CUDA error. */
+ * QMV_E_CUDA when the device reports a CUDA error.  When the word was set it also zeroes the
+ * split-tile arrival counters of every workspace on the device (the per-stream ones and the
+ * array of qmv_matvec_grouped_noalloc), which a kernel that gave up may have left part-way.
+ * This is the library's sticky device-error query: the errors a running kernel can meet are
+ * recorded here rather than in a per-thread "last error". */
 int qmv_check_device(void);
 
 /* Short English text for a status code; never NULL. */

@@ -50,12 +50,15 @@ def test_noalloc_matches_grouped_and_oracle(qmv, wt, sf, batch):
     qmv.matvec_grouped(wt, sf, probs)
     torch.cuda.synchronize()
     base = [p[4].cpu().numpy().copy() for p in probs]
-    # the allocation-free one, twice
+    # the allocation-free one, twice, on a stream no other entry point has used (so that no
+    # per-stream workspace exists that it could have fallen back on)
+    s = torch.cuda.Stream()
     outs = []
     for _ in range(2):
         for p in probs:
             p[4].fill_(5.0)
-        qmv.matvec_grouped_noalloc(wt, sf, probs)
+        torch.cuda.synchronize()
+        qmv.matvec_grouped_noalloc(wt, sf, probs, stream=s)
         torch.cuda.synchronize()
         outs.append([p[4].cpu().numpy().copy() for p in probs])
     for k, (p, (y_ref, absref)) in enumerate(zip(probs, refs)):
@@ -66,6 +69,28 @@ def test_noalloc_matches_grouped_and_oracle(qmv, wt, sf, batch):
         if batch >= 5:
             # the existing entry point runs the same kernel here: same splits, same bits
             assert_bits_equal(outs[0][k], base[k], what + " vs existing")
+
+
+def test_noalloc_takes_no_device_memory_after_first_call(qmv):
+    # after one call on the device (the library's device code and the scratch array are set up
+    # lazily), further calls on a new stream leave the free device memory unchanged, with and
+    # without the overlap flag, and match the oracle
+    import torch
+    wt, sf, batch = 2, 1, 8
+    shapes = [(2048, 4096), (512, 1024)]
+    mats, probs = _problems(wt, sf, shapes, batch, seed=400)
+    refs = [oracle.matvec(m.W, wt, sf, p[0], p[1], x) for (m, x), p in zip(mats, probs)]
+    s = torch.cuda.Stream()
+    qmv.matvec_grouped_noalloc(wt, sf, probs, stream=s)  # warm-up
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for overlap in (False, True, False, True):
+        qmv.matvec_grouped_noalloc(wt, sf, probs, overlap=overlap, stream=s)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0, "device memory taken by the allocation-free calls"
+    for p, (y_ref, absref) in zip(probs, refs):
+        check_product(p[4].cpu().numpy(), y_ref, absref, TOL, f"noalloc overlap {p[0]}x{p[1]}")
+    assert qmv.last_error() == 0
 
 
 def test_noalloc_rejects_what_it_cannot_run(qmv):
