@@ -84,6 +84,8 @@ def _load():
     lib.oracle_quantize_x.argtypes = [i32, i64, i64, vp, vp]
     lib.oracle_matvec_qx.restype = i32
     lib.oracle_matvec_qx.argtypes = [i32, i32, i64, i64, vp, vp, i32, vp, vp]
+    lib.oracle_glu.restype = i32
+    lib.oracle_glu.argtypes = [i32, i64, vp, vp, vp]
     lib.oracle_matvec_glu.restype = i32
     lib.oracle_matvec_glu.argtypes = [i32, i32, i64, i64, vp, i32, vp, vp, i32, vp, vp]
     lib.oracle_quant_q4_fit_block.restype = i32
@@ -274,6 +276,18 @@ def matvec_glu(W: np.ndarray, wtype: int, scale_f16: int, rows: int, cols: int, 
     if st != OK:
         raise ValueError(f"oracle_matvec_glu status {st}")
     return y, a
+
+
+def glu(act: int, gate: np.ndarray, up: np.ndarray) -> np.ndarray:
+    """h = act(gate) * up (act 0 SiLU, 1 GELU-tanh) for float64 arrays of one shape, in float64."""
+    gate = np.ascontiguousarray(gate, dtype=np.float64)
+    up = np.ascontiguousarray(up, dtype=np.float64)
+    assert gate.shape == up.shape
+    h = np.empty_like(gate)
+    st = _load().oracle_glu(act, gate.size, _ptr(gate), _ptr(up), _ptr(h))
+    if st != OK:
+        raise ValueError(f"oracle_glu status {st}")
+    return h
 
 
 def quant_q4_fit_block(x: np.ndarray, scale_f16: int):

@@ -39,6 +39,8 @@
  *   oracle_matvec_glu                         : pinned (act(g) - act(-g) = g turns a pair of
  *                                               gated products into the plain product; SiLU at
  *                                               ln 3 and GELU where its tanh is 1/2 give 3g/4)
+ *   oracle_glu                                : pinned (the same identities value by value, and
+ *                                               act(0) = 0, large |g|: act(g) -> max(g, 0))
  *   corner readings of the writers (f16 scale that rounds to 0, all-zero Q4 block,
  *   ties of the largest magnitude) : parity unpinned (writer-only, not on the product path)
  */
@@ -582,6 +584,16 @@ static double glu_act(int act, double g)
     if (act == 0) return g / (1.0 + exp(-g));
     const double k = sqrt(2.0 / acos(-1.0));
     return 0.5 * g * (1.0 + tanh(k * (g + 0.044715 * g * g * g)));
+}
+
+/* h[i] = act(gate[i]) * up[i] for n values given in double (the exact products w1 x and w3 x of
+ * a layer, as the oracle's matvec returns them), evaluated in double. */
+int oracle_glu(int act, int64_t n, const double *gate, const double *up, double *h)
+{
+    if (act != 0 && act != 1) return ORACLE_E_FORMAT;
+    if (n < 0) return ORACLE_E_SHAPE;
+    for (int64_t i = 0; i < n; i++) h[i] = glu_act(act, gate[i]) * up[i];
+    return ORACLE_OK;
 }
 
 /* y[b][r] = sum_c W[r][c] * act(gate[b][c]) * up[b][c], absref = sum_c |W[r][c] * h[b][c]|. */

@@ -60,6 +60,10 @@ MUTANTS = {
     "gguf_d_bytes_swapped": ("W[off + 2 * idx] = rec[0];\n            W[off + 2 * idx + 1] = rec[1];",
                              "W[off + 2 * idx] = rec[1];\n            W[off + 2 * idx + 1] = rec[0];"),
     "gguf_quants_at_record_start": ("W[idx * qb + j] = rec[2 + j];", "W[idx * qb + j] = rec[j];"),
+    "glu_values_up_dropped": ("for (int64_t i = 0; i < n; i++) h[i] = glu_act(act, gate[i]) * up[i];",
+                              "for (int64_t i = 0; i < n; i++) h[i] = glu_act(act, gate[i]);"),
+    "glu_values_gate_for_up": ("for (int64_t i = 0; i < n; i++) h[i] = glu_act(act, gate[i]) * up[i];",
+                               "for (int64_t i = 0; i < n; i++) h[i] = glu_act(act, gate[i]) * gate[i];"),
     "gguf_q8_block_32": ("int64_t block_bytes = (wtype == ORACLE_Q8_0) ? 34 : 18;",
                          "int64_t block_bytes = (wtype == ORACLE_Q8_0) ? 32 : 18;"),
 }
@@ -93,6 +97,8 @@ class Orc:
         lib.oracle_quantize.argtypes = [i32, i32, i64, i64, vp, vp]
         lib.oracle_matvec_glu.restype = i32
         lib.oracle_matvec_glu.argtypes = [i32, i32, i64, i64, vp, i32, vp, vp, i32, vp, vp]
+        lib.oracle_glu.restype = i32
+        lib.oracle_glu.argtypes = [i32, i64, vp, vp, vp]
         lib.oracle_gguf_to_mlb.restype = i32
         lib.oracle_gguf_to_mlb.argtypes = [i32, i64, i64, vp, vp]
         self.lib = lib
@@ -256,6 +262,15 @@ def pin_checks(o):
     o.lib.oracle_matvec_glu(2, 0, 1, 32, Wh.ctypes.data, 1, gh.ctypes.data, uh.ctypes.data, 1, yv.ctypes.data,
                             av.ctypes.data)
     yield "glu_gelu_value", abs(yv[0, 0] - 0.75 * float(gh[0, 0])) < 1e-6
+    # h = act(g) * u value by value: the odd part gives g * u
+    gv = np.ascontiguousarray(rng.standard_normal(50) * 3)
+    uv = np.ascontiguousarray(rng.standard_normal(50))
+    for act in (0, 1):
+        hp, hn = np.empty(50), np.empty(50)
+        o.lib.oracle_glu(act, 50, gv.ctypes.data, uv.ctypes.data, hp.ctypes.data)
+        ngv = np.ascontiguousarray(-gv)
+        o.lib.oracle_glu(act, 50, ngv.ctypes.data, uv.ctypes.data, hn.ctypes.data)
+        yield "glu_values_odd", bool(np.all(np.abs((hp - hn) - gv * uv) <= 1e-14 * (np.abs(gv * uv) + 1)))
 
 
 def build_variant(tmp, name, text):

@@ -575,6 +575,34 @@ def test_glu_silu_and_gelu_values():
     assert abs(y[0, 0] - 40.0) < 1e-12
 
 
+@pytest.mark.parametrize("act", [0, 1])
+def test_glu_values_odd_part_and_limits(act):
+    # h = act(g) * u value by value: the odd part act(g) - act(-g) = g (both activations), act(0)
+    # = 0, and for large |g| the activation tends to max(g, 0)
+    rng = np.random.default_rng(120 + act)
+    g = rng.standard_normal(200) * 3
+    u = rng.standard_normal(200)
+    hp, hn = oracle.glu(act, g, u), oracle.glu(act, -g, u)
+    assert np.all(np.abs((hp - hn) - g * u) <= 1e-14 * (np.abs(g * u) + 1))
+    assert np.all(oracle.glu(act, np.zeros(3), np.ones(3)) == 0)
+    big = np.array([40.0, -40.0])
+    h = oracle.glu(act, big, np.ones(2))
+    assert abs(h[0] - 40.0) < 1e-12 and abs(h[1]) < 1e-12
+
+
+def test_glu_silu_and_gelu_three_quarters():
+    # SiLU at ln 3 (sigmoid exactly 3/4) and GELU-tanh where its tanh is exactly 1/2 both give
+    # 3g/4, times u
+    g = np.array([np.log(3.0)])
+    assert abs(oracle.glu(0, g, np.array([2.0]))[0] - 1.5 * g[0]) < 1e-15
+    k, target = np.sqrt(2 / np.pi), np.arctanh(0.5)
+    lo, hi = 0.0, 2.0
+    for _ in range(200):
+        mid = (lo + hi) / 2
+        lo, hi = (mid, hi) if k * (mid + 0.044715 * mid ** 3) < target else (lo, mid)
+    assert abs(oracle.glu(1, np.array([lo]), np.array([-1.0]))[0] + 0.75 * lo) < 1e-14
+
+
 # ------------------------------------------------------------- Q4_0 best-fit writer
 def _weighted_err(x, w):
     x = x.astype(np.float64)
