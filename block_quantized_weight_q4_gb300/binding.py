@@ -62,6 +62,8 @@ def load_library():
     lib.qmv_matvec_grouped.restype = i32
     lib.qmv_matvec_grouped.argtypes = [i32, i32, i32, i32, vp, i32, ctypes.c_uint, vp]
     lib.qmv_matvec_grouped_noalloc.argtypes = [i32, i32, i32, i32, vp, i32, ctypes.c_uint, vp]
+    lib.qmv_matvec_glu.restype = i32
+    lib.qmv_matvec_glu.argtypes = [i32, i32, i64, i64, vp, vp, vp, i32, i32, vp, ctypes.c_uint, vp]
     lib.qmv_dequant.restype = i32
     lib.qmv_dequant.argtypes = [i32, i32, i64, i64, vp, vp, vp]
     lib.qmv_validate.restype = i32
@@ -162,17 +164,31 @@ FLAG_BF16_WEIGHTS = 2
 MAX_GROUP = 8
 X_SILU_GLU_F32 = 2
 X_GELU_GLU_F32 = 3
+X_BF16_PAIR = 4
 ACTS = {"silu": X_SILU_GLU_F32, "gelu": X_GELU_GLU_F32}
+ACT_SILU = 0
+ACT_GELU_TANH = 1
+ACT_CODES = {"silu": ACT_SILU, "gelu": ACT_GELU_TANH}
 NOALLOC_MAX_BATCH = 8
 
 
-def _problem_array(problems, act=None):
+def _problem_array(problems, act=None, pair=False):
     """act: None, or "silu" / "gelu" for gated activations (x of each problem: float32
-    (2, batch, cols), gate then up)."""
+    (2, batch, cols), gate then up).  pair: one vector given as bfloat16 (2, cols), hi parts
+    then lo parts (the layout matvec_glu writes)."""
     n = len(problems)
     if not 1 <= n <= MAX_GROUP:
         raise ValueError("1..8 problems per group")
     arr = (Problem * n)()
+    if pair:
+        import torch
+        for i, (rows, cols, W, x, y) in enumerate(problems):
+            if x.dtype != torch.bfloat16 or tuple(x.shape) != (2, cols) or not x.is_contiguous():
+                raise ValueError("a pair x is a contiguous bfloat16 (2, cols) tensor: hi, lo")
+            if tuple(y.shape) != (1, rows) or not y.is_contiguous():
+                raise ValueError("y must be a contiguous (1, rows) tensor")
+            arr[i] = Problem(rows, cols, W.data_ptr(), x.data_ptr(), y.data_ptr())
+        return arr, n, 1, X_BF16_PAIR
     if act is not None:
         import torch
         if act not in ACTS:
@@ -201,17 +217,40 @@ def _flags(overlap: bool, bf16_weights: bool = False) -> int:
 
 
 def matvec_grouped(wtype: int, scale_dtype: int, problems, overlap: bool = False, stream=None, act=None,
-                   bf16_weights: bool = False):
+                   bf16_weights: bool = False, pair: bool = False):
     """Several products in one launch.  problems: list of (rows, cols, W, x, y) with W a
     uint8 CUDA tensor, x (batch, cols) and y (batch, rows) CUDA tensors; all share wtype,
     scale_dtype, the x dtype and batch.  overlap: QMV_FLAG_OVERLAP (the weights must not be
     written by the preceding kernel on the stream).  act: "silu" / "gelu" for gated
     activations, x then float32 (2, batch, cols): gate, up; the product takes act(gate) * up.
-    bf16_weights: QMV_FLAG_BF16_WEIGHTS (prefill passes round each weight once to bfloat16)."""
-    arr, n, batch, xdt = _problem_array(problems, act)
+    bf16_weights: QMV_FLAG_BF16_WEIGHTS (prefill passes round each weight once to bfloat16).
+    pair: each x is one vector as a bfloat16 (2, cols) pair (QMV_X_BF16_PAIR), y (1, rows)."""
+    arr, n, batch, xdt = _problem_array(problems, act, pair)
     st = load_library().qmv_matvec_grouped(wtype, scale_dtype, xdt, batch, ctypes.addressof(arr), n,
                                            _flags(overlap, bf16_weights), _stream(stream))
     _check(st, "qmv_matvec_grouped")
+
+
+def matvec_glu(wtype: int, scale_dtype: int, rows: int, cols: int, W1, W3, x, act: str = "silu", h=None,
+               overlap: bool = False, stream=None):
+    """The FFN's gate and up projections with the gated activation as their epilogue
+    (qmv_matvec_glu): x a bfloat16 (cols,) or (1, cols) CUDA tensor; returns h, a bfloat16 (2, rows)
+    CUDA tensor holding act(W1 x) * (W3 x) as hi and lo parts (the pair layout matvec_grouped
+    takes with pair=True)."""
+    import torch
+    if act not in ACT_CODES:
+        raise ValueError("act must be 'silu' or 'gelu'")
+    if x.dtype != torch.bfloat16 or x.numel() != cols or not x.is_contiguous():
+        raise ValueError("x must be one contiguous bfloat16 vector of cols values")
+    if h is None:
+        h = torch.empty((2, rows), dtype=torch.bfloat16, device=x.device)
+    if h.dtype != torch.bfloat16 or tuple(h.shape) != (2, rows) or not h.is_contiguous():
+        raise ValueError("h must be a contiguous bfloat16 (2, rows) tensor")
+    st = load_library().qmv_matvec_glu(wtype, scale_dtype, rows, cols, W1.data_ptr(), W3.data_ptr(), x.data_ptr(),
+                                       X_BF16, ACT_CODES[act], h.data_ptr(), FLAG_OVERLAP if overlap else 0,
+                                       _stream(stream))
+    _check(st, "qmv_matvec_glu")
+    return h
 
 
 def matvec_grouped_noalloc(wtype: int, scale_dtype: int, problems, overlap: bool = False, stream=None):

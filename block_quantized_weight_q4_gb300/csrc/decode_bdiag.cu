@@ -31,6 +31,13 @@
 //     per byte pair instead of 4 and 2 (see q4_word_to_f16_levels).  The products are the
 //     same exact products as with bfloat16 operands.  A stage whose activations are not all
 //     exact halves (larger, tinier, NaN) uses bfloat16 operands, as the general kernel does.
+//   * Gated pair (Q4_0).  For the FFN's w1 (gate) and w3 (up) projections of one x (Krafla
+//     page, "Body"), a warp tile's two 16-row MMA tiles are rows 16t..16t+15 of w1 and the
+//     same rows of w3 (two 16-row TMA boxes into the same 32-row swizzled stage), so that at
+//     the end of its item the warp holds gate and up of the same rows and writes
+//     h = act(gate) * up directly as the bfloat16 pair hi = RN_bf16(h), lo = RN_bf16(h - hi)
+//     that the down projection's float32 route takes (the same bits the split kernel writes
+//     from float32 gate and up).
 #include <cstring>
 #include <mutex>
 
@@ -97,6 +104,9 @@ struct Params {
   int lgks;     // log2(ks)
   int nitems;
   int* status;
+  // gated pair: problem 0 is the w1 / w3 pair (rows = w1's rows, 16 of each per warp tile)
+  int act;        // 0 SiLU, 1 GELU-tanh
+  uint16_t* h;    // the down projection's activations: hi parts at h[r], lo parts at h[rows + r]
   Problem pr[kMaxProblems];
 };
 
@@ -236,11 +246,13 @@ __device__ __forceinline__ void chunk_math(float (&acc)[Cfg<WT, F16, NW, CH>::MT
   }
 }
 
-template <int WT, bool F16, int NW, int CH, bool XS>
+template <int WT, bool F16, int NW, int CH, bool XS, bool GLU = false>
 __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_constant__ Maps maps,
                                                                const __grid_constant__ Params p) {
   using C = Cfg<WT, F16, NW, CH, XS>;
   constexpr int MT = C::MT;
+  static_assert(!GLU || (MT == 2 && !XS), "the gated pair takes two 16-row MMA tiles per warp tile");
+  constexpr int TROWS = GLU ? kRows : C::WROWS;  // rows of each matrix per warp tile
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);  // 1024-aligned: swizzle atoms
@@ -285,12 +297,26 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
         const int c = pc.c0 + (pc.j << p.lgks);  // stage: chunks CH c ..
         mbar_arrive_expect_tx(&bars[ps], stage_tx);
         fence_proxy_async_smem();
+        if (GLU) {
+          // rows 16t.. of w1 into the stage's first 16 rows, the same rows of w3 into the next 16
 #pragma unroll
-        for (int b = 0; b < C::NQBOX; ++b)
-          tma_load_2d(qring + ps * C::Q_STAGE + b * C::Q_BOX_BYTES, &maps.q[pc.prob], c * (C::kCH * C::QROW) + b * kBox,
-                      pc.tile * C::WROWS, &bars[ps], pol_stream);
-        tma_load_2d(dring + ps * C::D_STAGE, &maps.d[pc.prob], c * C::DROW, pc.tile * C::WROWS, &bars[ps],
-                    pol_stream);
+          for (int b = 0; b < C::NQBOX; ++b)
+#pragma unroll
+            for (int m = 0; m < 2; ++m)
+              tma_load_2d(qring + ps * C::Q_STAGE + b * C::Q_BOX_BYTES + m * kRows * kBox, &maps.q[m],
+                          c * (C::kCH * C::QROW) + b * kBox, pc.tile * TROWS, &bars[ps], pol_stream);
+#pragma unroll
+          for (int m = 0; m < 2; ++m)
+            tma_load_2d(dring + ps * C::D_STAGE + m * kRows * C::DROW, &maps.d[m], c * C::DROW, pc.tile * TROWS,
+                        &bars[ps], pol_stream);
+        } else {
+#pragma unroll
+          for (int b = 0; b < C::NQBOX; ++b)
+            tma_load_2d(qring + ps * C::Q_STAGE + b * C::Q_BOX_BYTES, &maps.q[pc.prob],
+                        c * (C::kCH * C::QROW) + b * kBox, pc.tile * C::WROWS, &bars[ps], pol_stream);
+          tma_load_2d(dring + ps * C::D_STAGE, &maps.d[pc.prob], c * C::DROW, pc.tile * C::WROWS, &bars[ps],
+                      pol_stream);
+        }
         if (with_x) {
           tma_load_2d_keep(xring + ps * C::X_STAGE, &maps.x[pc.prob], 0, c * C::kCH, &bars[ps]);
           if (XS) tma_load_2d_keep(xring + ps * C::X_STAGE + C::X_PART, &maps.xl[pc.prob], 0, c * C::kCH, &bars[ps]);
@@ -409,7 +435,7 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
     }
 
     if (cc.j == cc.n - 1) {  // end of an item: add the lanes' blocks and the column slices, store y
-      const int row0 = cc.tile * C::WROWS;
+      const int row0 = cc.tile * TROWS;
       // row sums over the four lanes t that share rows g, g + 8 (the same value in all four)
       float v[MT][2];
 #pragma unroll
@@ -426,7 +452,27 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
       if (MT == 2 && t >= 2) mine = (t & 1) ? v[MT - 1][1] : v[MT - 1][0];
       const int r = 16 * (t >> 1) + 8 * (t & 1) + g;
       const bool holder = t < 2 * MT;
-      if (p.ks == 1) {
+      if (GLU) {
+        // gate of row row0 + i in lane i of the tile's first warp, up in lane 16 + i (rows 16..31
+        // of the warp tile are w3's); h = act(gate) * up as the bf16 pair
+        float sum = 0.f;
+        if (p.ks == 1) {
+          sum = __shfl_sync(0xffffffffu, mine, ((lane & 15) << 2 & 28) | ((lane >> 4) << 1) | ((lane >> 3) & 1));
+        } else {
+          if (holder) red[warp * C::WROWS + r] = mine;
+          __syncthreads();
+          if (kslice == 0)
+            for (int k = 0; k < p.ks; ++k) sum += red[(warp + k) * C::WROWS + lane];
+        }
+        const float up = __shfl_down_sync(0xffffffffu, sum, 16);
+        if (kslice == 0 && valid && !failed && lane < kRows && row0 + lane < P.rows) {
+          uint16_t hi, lo;
+          split_bf16_pair(glu(p.act, sum, up), hi, lo);
+          p.h[row0 + lane] = hi;
+          p.h[P.rows + row0 + lane] = lo;
+        }
+        if (p.ks != 1) __syncthreads();
+      } else if (p.ks == 1) {
         if (valid && !failed && holder && row0 + r < P.rows) P.y[row0 + r] = mine;
       } else {
         if (holder) red[warp * C::WROWS + r] = mine;
@@ -462,10 +508,10 @@ struct Plan {
   long long cost = -1;
 };
 
-template <int WT, bool F16, int NW, int CH, bool XS>
+template <int WT, bool F16, int NW, int CH, bool XS, bool GLU = false>
 cudaError_t plan_typed(const MatrixRef* ms, int n, const DeviceInfo& dev, Plan* out) {
   using C = Cfg<WT, F16, NW, CH, XS>;
-  auto kern = matvec_bdiag_kernel<WT, F16, NW, CH, XS>;
+  auto kern = matvec_bdiag_kernel<WT, F16, NW, CH, XS, GLU>;
   // per device: the shared-memory attribute set and the occupancy known (0 = does not fit)
   static std::mutex mu;
   static bool ready[64] = {};
@@ -517,21 +563,28 @@ cudaError_t plan_typed(const MatrixRef* ms, int n, const DeviceInfo& dev, Plan* 
   return cudaSuccess;
 }
 
-template <int WT, bool F16, int NW, int CH, bool XS>
+// GLU: ms = {w1, w3} (same shape), one x (xs[0]); the pair is one problem whose warp tiles are
+// 16 rows of each; act and h as in Params.
+template <int WT, bool F16, int NW, int CH, bool XS, bool GLU = false>
 cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* const* xs, float* const* ys, int n,
-                         bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
+                         bool pdl, const DeviceInfo& dev, cudaStream_t stream, int act = -1, uint16_t* h = nullptr) {
   using C = Cfg<WT, F16, NW, CH, XS>;
+  constexpr int TROWS = GLU ? kRows : C::WROWS;  // rows of each matrix per warp tile
+  if (GLU && (n != 2 || ms[0].rows != ms[1].rows || ms[0].cols != ms[1].cols || h == nullptr))
+    return cudaErrorInvalidValue;
   Params p{};
-  p.nprob = n;
+  p.nprob = GLU ? 1 : n;
   p.status = dev.status;
   p.ks = plan.ks;
   p.lgks = 31 - __builtin_clz((unsigned)plan.ks);
+  p.act = act;
+  p.h = h;
   const int tpi = NW / plan.ks;
   int items = 0;
-  for (int i = 0; i < n; ++i) {
-    p.pr[i].y = ys[i];
+  for (int i = 0; i < p.nprob; ++i) {
+    p.pr[i].y = GLU ? nullptr : ys[i];
     p.pr[i].rows = (int)ms[i].rows;
-    p.pr[i].ntiles = (int)((ms[i].rows + C::WROWS - 1) / C::WROWS);
+    p.pr[i].ntiles = (int)((ms[i].rows + TROWS - 1) / TROWS);
     p.pr[i].nst = (int)((ms[i].cols / kTK + C::kCH - 1) / C::kCH);
     p.pr[i].item0 = items;
     items += (p.pr[i].ntiles + tpi - 1) / tpi;
@@ -546,11 +599,12 @@ cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* cons
     const uint64_t qrow = (WT == QMV_Q4_0) ? (uint64_t)m.cols / 2 : (uint64_t)m.cols;
     const uint64_t drow = (uint64_t)(m.cols / 32) * (F16 ? 2 : 4);
     cudaError_t err = encode_tmap_2d(&maps.q[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, m.q, qrow, (uint64_t)m.rows, qrow,
-                                     kBox, C::WROWS, CU_TENSOR_MAP_SWIZZLE_128B);
+                                     kBox, TROWS, CU_TENSOR_MAP_SWIZZLE_128B);
     if (err != cudaSuccess) return err;
     err = encode_tmap_2d(&maps.d[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, m.d, drow, (uint64_t)m.rows, drow, C::DROW,
-                         C::WROWS, CU_TENSOR_MAP_SWIZZLE_NONE);
+                         TROWS, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (err != cudaSuccess) return err;
+    if (GLU && i == 1) continue;  // one x for the pair
     err = encode_tmap_2d(&maps.x[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xs[i], kTK, (uint64_t)(m.cols / kTK), kTK * 2,
                          kTK, C::kCH, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (err != cudaSuccess) return err;
@@ -572,7 +626,7 @@ cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* cons
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, matvec_bdiag_kernel<WT, F16, NW, CH, XS>, maps, p);
+  return cudaLaunchKernelEx(&cfg, matvec_bdiag_kernel<WT, F16, NW, CH, XS, GLU>, maps, p);
 }
 
 // Q4_0 launches of at least this many weight bytes take one-chunk stages.
@@ -582,32 +636,43 @@ constexpr long long kOneChunkBytes = 32LL << 20;
 // tiles), 8-warp CTAs instead if their estimate is smaller.  One-chunk stages fit more warps per
 // SM (five 4-warp CTAs instead of two): measured faster on large Q4_0 launches, slower on
 // launches of a few tens of MB (the Llama-7B layer's, the 4096 x 4096 product) and on Q8_0.
-template <int WT, bool F16, bool XS>
+// GLU: ms = {w1, w3}, planned as one matrix of twice the rows (the same warp tiles: 16 rows of
+// each per tile); act and h as in launch_typed.
+template <int WT, bool F16, bool XS, bool GLU = false>
 cudaError_t launch_best(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
-                        const DeviceInfo& dev, cudaStream_t stream) {
+                        const DeviceInfo& dev, cudaStream_t stream, int act = -1, uint16_t* h = nullptr) {
+  MatrixRef pair[1];
+  const MatrixRef* pm = ms;
+  int pn = n;
+  if (GLU) {
+    pair[0] = ms[0];
+    pair[0].rows = 2 * ms[0].rows;
+    pm = pair;
+    pn = 1;
+  }
   Plan p4, p8;
   cudaError_t err;
   if (WT == QMV_Q4_0 && !XS) {
     long long bytes = 0;
-    for (int i = 0; i < n; ++i) bytes += ms[i].rows * ms[i].cols / 2;
+    for (int i = 0; i < pn; ++i) bytes += pm[i].rows * pm[i].cols / 2;
     if (bytes >= kOneChunkBytes) {
       Plan p1;
-      err = plan_typed<WT, F16, 4, 1, XS>(ms, n, dev, &p1);
+      err = plan_typed<WT, F16, 4, 1, XS, GLU>(pm, pn, dev, &p1);
       if (err != cudaSuccess) return err;
       if (p1.cost >= 0 && p1.grid > dev.sm_count)
-        return launch_typed<WT, F16, 4, 1, XS>(p1, ms, xs, ys, n, pdl, dev, stream);
+        return launch_typed<WT, F16, 4, 1, XS, GLU>(p1, ms, xs, ys, n, pdl, dev, stream, act, h);
     }
   }
-  err = plan_typed<WT, F16, 4, 2, XS>(ms, n, dev, &p4);
+  err = plan_typed<WT, F16, 4, 2, XS, GLU>(pm, pn, dev, &p4);
   if (err != cudaSuccess) return err;
   if (p4.cost >= 0 && p4.grid > dev.sm_count)
-    return launch_typed<WT, F16, 4, 2, XS>(p4, ms, xs, ys, n, pdl, dev, stream);
-  err = plan_typed<WT, F16, 8, 2, XS>(ms, n, dev, &p8);
+    return launch_typed<WT, F16, 4, 2, XS, GLU>(p4, ms, xs, ys, n, pdl, dev, stream, act, h);
+  err = plan_typed<WT, F16, 8, 2, XS, GLU>(pm, pn, dev, &p8);
   if (err != cudaSuccess) return err;
   if (p8.cost >= 0 && (p4.cost < 0 || p8.cost < p4.cost))
-    return launch_typed<WT, F16, 8, 2, XS>(p8, ms, xs, ys, n, pdl, dev, stream);
+    return launch_typed<WT, F16, 8, 2, XS, GLU>(p8, ms, xs, ys, n, pdl, dev, stream, act, h);
   if (p4.cost < 0) return cudaErrorInvalidConfiguration;
-  return launch_typed<WT, F16, 4, 2, XS>(p4, ms, xs, ys, n, pdl, dev, stream);
+  return launch_typed<WT, F16, 4, 2, XS, GLU>(p4, ms, xs, ys, n, pdl, dev, stream, act, h);
 }
 
 template <bool XS>
@@ -631,6 +696,21 @@ cudaError_t launch_matvec_bdiag(const MatrixRef* ms, const void* const* xs, floa
 cudaError_t launch_matvec_bdiag_split(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
                                       const DeviceInfo& dev, cudaStream_t stream) {
   return launch_any<true>(ms, xs, ys, n, pdl, dev, stream);
+}
+
+bool matvec_bdiag_glu_supported(const MatrixRef& w1, const MatrixRef& w3) {
+  return w1.wtype == QMV_Q4_0 && w3.wtype == QMV_Q4_0 && w1.scale_f16 == w3.scale_f16 && w1.rows == w3.rows &&
+         w1.cols == w3.cols && w1.cols % kTK == 0 && w1.rows < (1LL << 30);
+}
+
+cudaError_t launch_matvec_bdiag_glu(const MatrixRef& w1, const MatrixRef& w3, const void* x, int act, uint16_t* h,
+                                    bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
+  if (!matvec_bdiag_glu_supported(w1, w3) || (act != 0 && act != 1)) return cudaErrorInvalidValue;
+  const MatrixRef ms[2] = {w1, w3};
+  const void* xs[2] = {x, x};
+  float* ys[2] = {nullptr, nullptr};
+  return w1.scale_f16 ? launch_best<QMV_Q4_0, true, false, true>(ms, xs, ys, 2, pdl, dev, stream, act, h)
+                      : launch_best<QMV_Q4_0, false, false, true>(ms, xs, ys, 2, pdl, dev, stream, act, h);
 }
 
 }  // namespace qmv

@@ -96,29 +96,6 @@ struct SplitArgs {
   long long up_batch;  // gated activations: a problem's up array is up_batch * cols floats after its gate
 };
 
-// The FFN's gated activation: SiLU(g) = g / (1 + e^-g), GELU_tanh(g) = g/2 (1 + tanh(sqrt(2/pi)
-// (g + 0.044715 g^3))), times up; float32 operations with CUDA's expf and tanhf.
-__device__ __forceinline__ float glu(int act, float g, float u) {
-  float h;
-  if (act == 0) {
-    h = __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
-  } else {
-    const float k = 0.7978845608028654f;  // sqrt(2 / pi)
-    const float inner = __fmul_rn(k, __fadd_rn(g, __fmul_rn(0.044715f, __fmul_rn(g, __fmul_rn(g, g)))));
-    h = __fmul_rn(__fmul_rn(0.5f, g), __fadd_rn(1.0f, tanhf(inner)));
-  }
-  return __fmul_rn(h, u);
-}
-
-// bfloat16 bits of v rounded to nearest (ties to even); finite v beyond the bfloat16 range
-// (which would round to infinity) are truncated instead, so that hi + lo stays finite.
-__device__ __forceinline__ uint16_t bf16_bits_rn_finite(float v) {
-  const uint32_t r = pack_bf16x2(v, v) & 0xFFFFu;
-  const float back = __uint_as_float(r << 16);
-  if (isfinite(v) && !isfinite(back)) return static_cast<uint16_t>(__float_as_uint(v) >> 16);
-  return static_cast<uint16_t>(r);
-}
-
 // x (batch float32 vectors of cols) as rows of bfloat16: row n < nvec the hi part of vector
 // n, row lo_row + n its lo part, hi = RN_bf16(x) and lo = RN_bf16(x - hi) (x - hi is exact
 // in float32); rows of vectors past the batch are zero, and so is lo of a value that is not
@@ -137,9 +114,7 @@ __global__ void __launch_bounds__(256) split_x_kernel(const __grid_constant__ Sp
     if (n < a.batch) {
       float v = x[(size_t)n * cols + c];
       if (a.act >= 0) v = glu(a.act, v, x[(size_t)(a.up_batch + n) * cols + c]);
-      hi = bf16_bits_rn_finite(v);
-      const float h = __uint_as_float((uint32_t)hi << 16);
-      lo = isfinite(v) ? bf16_bits_rn_finite(v - h) : 0;
+      split_bf16_pair(v, hi, lo);
     }
     out[(size_t)n * cols + c] = hi;
     out[(size_t)(a.lo_row + n) * cols + c] = lo;

@@ -160,10 +160,12 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
                        unsigned flags, cudaStream_t stream) {
   if (problems == nullptr || n < 1 || n > QMV_MAX_GROUP) return QMV_E_ARG;
   if (x_dtype != QMV_X_F32 && x_dtype != QMV_X_BF16 && x_dtype != QMV_X_SILU_GLU_F32 &&
-      x_dtype != QMV_X_GELU_GLU_F32)
+      x_dtype != QMV_X_GELU_GLU_F32 && x_dtype != QMV_X_BF16_PAIR)
     return QMV_E_FORMAT;
   if (batch < 0) return QMV_E_ARG;
   if ((flags & ~(QMV_FLAG_OVERLAP | QMV_FLAG_BF16_WEIGHTS)) != 0) return QMV_E_ARG;
+  const bool pair = x_dtype == QMV_X_BF16_PAIR;
+  if (pair && batch > 1) return QMV_E_ARG;
   // gated activations: x holds gate then up (batch x cols float32 each); act(gate) * up is
   // formed in the activation prep of the float32 routes
   const bool glu = x_dtype == QMV_X_SILU_GLU_F32 || x_dtype == QMV_X_GELU_GLU_F32;
@@ -177,11 +179,24 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
     if (pr.x == nullptr || pr.y == nullptr) return QMV_E_ARG;
     if (!aligned(pr.x, 16) || !aligned(pr.y, 4)) return QMV_E_ALIGN;
     if (pr.rows > INT64_MAX / batch) return QMV_E_SHAPE;
-    if (glu && !matvec_mma_supported(ms[i])) return QMV_E_SHAPE;
+    if ((glu || pair) && !matvec_mma_supported(ms[i])) return QMV_E_SHAPE;
   }
   if (batch == 0) return QMV_OK;
   DeviceInfo dev;
   if (current_device_info(&dev) != cudaSuccess) return QMV_E_CUDA;
+  if (pair) {
+    // one vector given as its bfloat16 hi and lo parts: the block-diagonal kernel runs every
+    // block's MMAs once with each
+    const void* xs[QMV_MAX_GROUP];
+    float* ys[QMV_MAX_GROUP];
+    for (int i = 0; i < n; ++i) {
+      xs[i] = problems[i].x;
+      ys[i] = problems[i].y;
+    }
+    return launch_matvec_bdiag_split(ms, xs, ys, n, (flags & QMV_FLAG_OVERLAP) != 0, dev, stream) == cudaSuccess
+               ? QMV_OK
+               : QMV_E_CUDA;
+  }
   const bool xb = x_dtype == QMV_X_BF16;
   const size_t xsz = xb ? 2 : 4;
   const bool pdl = (flags & QMV_FLAG_OVERLAP) != 0;
@@ -296,6 +311,27 @@ int qmv_matvec_grouped_noalloc(int wtype, int scale_dtype, int x_dtype, int batc
   workspace_carve(base, sizeof(g_noalloc_scratch), QMV_NOALLOC_MAX_CTAS, &ws);
   const bool pdl = (flags & QMV_FLAG_OVERLAP) != 0;
   return launch_decode_tc(ms, xs, ys, n, batch, pdl, dev, ws, stream) == cudaSuccess ? QMV_OK : QMV_E_CUDA;
+}
+
+int qmv_matvec_glu(int wtype, int scale_dtype, int64_t rows, int64_t cols, const void* W1, const void* W3,
+                   const void* x, int x_dtype, int act, void* h, unsigned flags, cudaStream_t stream) {
+  MatrixRef w1, w3;
+  int st = make_ref(wtype, scale_dtype, rows, cols, W1, &w1);
+  if (st != QMV_OK) return st;
+  st = make_ref(wtype, scale_dtype, rows, cols, W3, &w3);
+  if (st != QMV_OK) return st;
+  if (wtype != QMV_Q4_0 || x_dtype != QMV_X_BF16) return QMV_E_FORMAT;
+  if (act != QMV_ACT_SILU && act != QMV_ACT_GELU_TANH) return QMV_E_FORMAT;
+  if ((flags & ~QMV_FLAG_OVERLAP) != 0) return QMV_E_ARG;
+  if (!matvec_bdiag_glu_supported(w1, w3)) return QMV_E_SHAPE;
+  if (x == nullptr || h == nullptr) return QMV_E_ARG;
+  if (!aligned(x, 16) || !aligned(h, 16)) return QMV_E_ALIGN;
+  DeviceInfo dev;
+  if (current_device_info(&dev) != cudaSuccess) return QMV_E_CUDA;
+  return launch_matvec_bdiag_glu(w1, w3, x, act, static_cast<uint16_t*>(h), (flags & QMV_FLAG_OVERLAP) != 0, dev,
+                                 stream) == cudaSuccess
+             ? QMV_OK
+             : QMV_E_CUDA;
 }
 
 int qmv_matvec(int wtype, int scale_dtype, int64_t rows, int64_t cols, const void* W, const void* x,

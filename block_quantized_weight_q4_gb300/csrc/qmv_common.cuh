@@ -294,4 +294,38 @@ __device__ __forceinline__ void sts_u32x4(uint32_t addr, uint32_t a, uint32_t b,
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+
+// ---------------------------------------------------------------------------- gated activation
+// The FFN's gated activation (Krafla page, "Body": w1 gate, w3 up, header field act):
+// SiLU(g) = g / (1 + e^-g) (act 0), GELU_tanh(g) = g/2 (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3)))
+// (act 1), times up; float32 operations with CUDA's expf and tanhf.
+__device__ __forceinline__ float glu(int act, float g, float u) {
+  float h;
+  if (act == 0) {
+    h = __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
+  } else {
+    const float k = 0.7978845608028654f;  // sqrt(2 / pi)
+    const float inner = __fmul_rn(k, __fadd_rn(g, __fmul_rn(0.044715f, __fmul_rn(g, __fmul_rn(g, g)))));
+    h = __fmul_rn(__fmul_rn(0.5f, g), __fadd_rn(1.0f, tanhf(inner)));
+  }
+  return __fmul_rn(h, u);
+}
+
+// bfloat16 bits of v rounded to nearest (ties to even); finite v beyond the bfloat16 range
+// (which would round to infinity) are truncated instead, so that hi + lo stays finite.
+__device__ __forceinline__ uint16_t bf16_bits_rn_finite(float v) {
+  const uint32_t r = pack_bf16x2(v, v) & 0xFFFFu;
+  const float back = __uint_as_float(r << 16);
+  if (isfinite(v) && !isfinite(back)) return static_cast<uint16_t>(__float_as_uint(v) >> 16);
+  return static_cast<uint16_t>(r);
+}
+
+// A float32 activation as a bfloat16 pair: hi = RN_bf16(v), lo = RN_bf16(v - hi) (v - hi is
+// exact in float32; lo = 0 for v that is not finite): 16 significant bits of v kept.
+__device__ __forceinline__ void split_bf16_pair(float v, uint16_t& hi, uint16_t& lo) {
+  hi = bf16_bits_rn_finite(v);
+  const float h = __uint_as_float((uint32_t)hi << 16);
+  lo = isfinite(v) ? bf16_bits_rn_finite(v - h) : 0;
+}
+
 }  // namespace qmv

@@ -101,6 +101,12 @@ cudaError_t launch_matvec_bdiag(const MatrixRef* ms, const void* const* xs, floa
 // lo in the cols following hi): every block's MMAs run once with each into the same sums.
 cudaError_t launch_matvec_bdiag_split(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
                                       const DeviceInfo& dev, cudaStream_t stream);
+// The FFN's gated pair (Q4_0, one bfloat16 vector x): w1 x and w3 x in one launch, written as
+// h = act(w1 x) * (w3 x) in the bfloat16 pair layout launch_matvec_bdiag_split reads (hi parts
+// at h[r], lo parts at h[rows + r]); act 0 SiLU, 1 GELU-tanh.
+bool matvec_bdiag_glu_supported(const MatrixRef& w1, const MatrixRef& w3);
+cudaError_t launch_matvec_bdiag_glu(const MatrixRef& w1, const MatrixRef& w3, const void* x, int act, uint16_t* h,
+                                    bool pdl, const DeviceInfo& dev, cudaStream_t stream);
 // One float32 activation vector per problem: split into hi + lo bfloat16 in the stream's
 // split buffer (2 rows per problem, up to 524,288 columns over the problems), then the above.
 // Fails (nothing launched) when the buffer would not hold them, or cannot be created while

@@ -66,6 +66,16 @@ extern "C" {
  * act(gate) * up. */
 #define QMV_X_SILU_GLU_F32 2
 #define QMV_X_GELU_GLU_F32 3
+/* One activation vector given as a bfloat16 pair (batch must be 1): x holds cols bfloat16 hi
+ * parts followed by cols bfloat16 lo parts, the activations being hi + lo; the product runs
+ * every block's dot products once with each part (16 significant bits of the activations
+ * kept).  This is the layout qmv_matvec_glu writes.  cols % 256 == 0 (QMV_E_SHAPE otherwise),
+ * batch other than 0 or 1 gives QMV_E_ARG. */
+#define QMV_X_BF16_PAIR 4
+
+/* act of qmv_matvec_glu (the .mlb header's act field): */
+#define QMV_ACT_SILU 0      /* SiLU(g) = g / (1 + e^-g) */
+#define QMV_ACT_GELU_TANH 1 /* GELU(g) = g/2 (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3))) */
 
 /* Status codes.  QMV_E_FORMAT and QMV_E_SHAPE mirror the loader's ML_E_FORMAT and
  * ML_E_SHAPE classes (Krafla page, "Validation done by the loader"): an unknown enum
@@ -230,6 +240,28 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
  * results: order them on one stream. */
 int qmv_matvec_grouped_noalloc(int wtype, int scale_dtype, int x_dtype, int batch, const qmv_problem *problems,
                                int n, unsigned flags, cudaStream_t stream);
+
+/* The FFN's gate and up projections with the gated activation as their epilogue (Krafla page,
+ * "Body": w1 gate, w3 up, both hidden_dim x dim; header field act): for one bfloat16 activation
+ * vector x (device, cols bfloat16, 16-byte aligned),
+ *   gate = W1 x,  up = W3 x  (each as qmv_matvec computes it, float32 sums),
+ *   h[r] = act(gate[r]) * up[r]  (float32 operations, CUDA's expf / tanhf),
+ * written to h (device, 2 * rows bfloat16, 16-byte aligned) as the pair hi[r] = RN_bf16(h[r]) at
+ * h[r] and lo[r] = RN_bf16(h[r] - hi[r]) at h[rows + r] (a finite h beyond the bfloat16 range
+ * keeps a truncated hi; lo = 0 for h that is not finite): the layout of QMV_X_BF16_PAIR, so the
+ * down projection takes it directly (qmv_matvec_grouped with x_dtype QMV_X_BF16_PAIR, batch 1).
+ * One launch: each warp tile holds 16 rows of W1 and the same 16 rows of W3, so gate and up
+ * meet in registers and neither is written to memory.  The result has the bits that the
+ * grouped product of {W1, W3} followed by the float32 gated route (QMV_X_SILU_GLU_F32 /
+ * QMV_X_GELU_GLU_F32) forms from the same sums.
+ *   wtype must be QMV_Q4_0 (QMV_E_FORMAT otherwise; other types: qmv_matvec_grouped on {W1, W3},
+ *   then the gated float32 route); x_dtype must be QMV_X_BF16 (QMV_E_FORMAT); act QMV_ACT_SILU
+ *   or QMV_ACT_GELU_TANH (QMV_E_FORMAT); cols % 256 == 0 (QMV_E_SHAPE); flags QMV_FLAG_OVERLAP
+ *   or 0 (QMV_E_ARG).
+ * W1 and W3 are matrix images as for qmv_matvec (same wtype, scale_dtype, rows and cols).
+ * Allocates nothing.  Asynchronous.  Returns as qmv_matvec. */
+int qmv_matvec_glu(int wtype, int scale_dtype, int64_t rows, int64_t cols, const void *W1, const void *W3,
+                   const void *x, int x_dtype, int act, void *h, unsigned flags, cudaStream_t stream);
 
 /* out[r][c] = level * d as float32, with one float32 multiplication rounded to nearest
  * even (Krafla page, "Q8_0" and "Q4_0"; f16 scales are first converted exactly to

@@ -71,8 +71,11 @@ def call_matvec(lib, wt=2, sf=1, rows=64, cols=64, W=FAKE, x=FAKE, xd=1, y=FAKE,
 def test_matvec_argument_errors(lib):
     assert call_matvec(lib, wt=3) == binding.E_FORMAT
     assert call_matvec(lib, sf=2) == binding.E_FORMAT
-    assert call_matvec(lib, xd=4) == binding.E_FORMAT
+    assert call_matvec(lib, xd=5) == binding.E_FORMAT
     assert call_matvec(lib, xd=-1) == binding.E_FORMAT
+    # a bfloat16 pair (4) is one vector with cols % 256 == 0
+    assert call_matvec(lib, xd=4, cols=64) == binding.E_SHAPE
+    assert call_matvec(lib, xd=4, cols=256, batch=2) == binding.E_ARG
     # gated activations (2: SiLU, 3: GELU-tanh) need cols % 256 == 0: checked before any launch
     assert call_matvec(lib, xd=2, cols=64) == binding.E_SHAPE
     assert call_matvec(lib, xd=3, cols=96) == binding.E_SHAPE
@@ -158,6 +161,23 @@ def test_dequant_and_validate_argument_errors(lib):
     assert lib.qmv_matvec_qx(1, 0, 64, 64, FAKE, FAKE, 0, 1, None) == binding.E_ARG
     assert lib.qmv_matvec_qx(2, 1, 64, 64, FAKE, FAKE + 8, FAKE, 1, None) == binding.E_ALIGN
     assert lib.qmv_matvec_qx(2, 1, 64, 64, FAKE, FAKE, FAKE + 2, 1, None) == binding.E_ALIGN
+
+
+def test_matvec_glu_argument_errors(lib):
+    def glu(wt=2, sf=1, rows=64, cols=256, W1=FAKE, W3=FAKE, x=FAKE, xd=1, act=0, h=FAKE, flags=0):
+        return lib.qmv_matvec_glu(wt, sf, rows, cols, W1, W3, x, xd, act, h, flags, None)
+    assert glu(wt=1) == binding.E_FORMAT          # the fused epilogue takes Q4_0
+    assert glu(wt=3) == binding.E_FORMAT
+    assert glu(xd=0) == binding.E_FORMAT          # one bfloat16 vector
+    assert glu(act=2) == binding.E_FORMAT
+    assert glu(flags=2) == binding.E_ARG
+    assert glu(cols=64) == binding.E_SHAPE        # cols % 256
+    assert glu(cols=48) == binding.E_SHAPE
+    assert glu(rows=0) == binding.E_SHAPE
+    assert glu(W1=0) == binding.E_ARG and glu(W3=0) == binding.E_ARG
+    assert glu(x=0) == binding.E_ARG and glu(h=0) == binding.E_ARG
+    assert glu(W3=FAKE + 8) == binding.E_ALIGN
+    assert glu(x=FAKE + 2) == binding.E_ALIGN and glu(h=FAKE + 4) == binding.E_ALIGN
 
 
 def test_strerror_never_null(lib):

@@ -113,3 +113,119 @@ def test_glu_refusals(qmv):
         qmv.matvec_grouped(2, 1, [(64, 96, dev_u8(m.W), x, y)], act="silu")
     with pytest.raises(ValueError):          # x not (2, batch, cols)
         qmv.matvec_grouped(2, 1, [(64, 96, dev_u8(m.W), x[0], y)], act="gelu")
+
+
+# ------------------------------------------------------- fused gate/up epilogue (qmv_matvec_glu)
+# |act'| <= 1.1 for SiLU and <= 1.13 for GELU-tanh; 1.2 bounds both
+ACT_LIPSCHITZ = 1.2
+
+
+def _pair_values(h):
+    """float64 hi + lo of a bfloat16 (2, rows) pair tensor."""
+    import torch
+    codes = h.view(torch.int16).cpu().numpy().view(np.uint16).astype(np.uint32)
+    v = (codes << 16).view(np.float32).astype(np.float64)
+    return v[0] + v[1], v
+
+
+def _check_h(h_gpu, gate, G, up, U, act_id, what):
+    # gate and up each meet the product bar (1e-3 of their sum |w x|); act changes by at most
+    # ACT_LIPSCHITZ times a change of its argument; the float32 evaluation and the hi + lo pair
+    # add a few parts in 2^17 of |h|
+    h_ref = oracle.glu(act_id, gate, up)
+    ag = np.abs(oracle.glu(act_id, gate, np.ones_like(gate)))
+    dg, du = 1e-3 * G, 1e-3 * U
+    bound = ACT_LIPSCHITZ * dg * (np.abs(up) + du) + ag * du + 2.0 ** -15 * np.abs(h_ref)
+    err = np.abs(h_gpu - h_ref)
+    assert np.all(err <= bound), f"{what}: {np.count_nonzero(err > bound)} values of h out of bound"
+    return h_ref
+
+
+@pytest.mark.parametrize("act,act_id", ACTS)
+@pytest.mark.parametrize("sf", [0, 1])
+@pytest.mark.parametrize("rows,cols", [(300, 2048), (64, 256), (1000, 4096)])
+def test_fused_glu_matches_oracle(qmv, act, act_id, sf, rows, cols):
+    import torch
+    from helpers import dev_x
+    m1 = inputs.make_matrix(2, sf, rows, cols, seed=500 + rows + sf)
+    m3 = inputs.make_matrix(2, sf, rows, cols, seed=501 + rows + sf)
+    x = inputs.make_x(1, cols, True, seed=502 + act_id)
+    h = qmv.matvec_glu(2, sf, rows, cols, dev_u8(m1.W), dev_u8(m3.W), dev_x(x)[0], act=act)
+    torch.cuda.synchronize()
+    h_gpu, parts = _pair_values(h)
+    gate, G = oracle.matvec(m1.W, 2, sf, rows, cols, x)
+    up, U = oracle.matvec(m3.W, 2, sf, rows, cols, x)
+    _check_h(h_gpu, gate[0], G[0], up[0], U[0], act_id, f"fused {act} {sf} {rows}x{cols}")
+    # lo is the rounding of h - hi: at most half a bfloat16 ulp of hi
+    hi, lo = parts
+    assert np.all(np.abs(lo) <= np.abs(hi) * 2.0 ** -8)
+
+
+@pytest.mark.parametrize("act,act_id", ACTS)
+def test_fused_glu_then_down_projection(qmv, act, act_id):
+    # the down projection reads the pair directly (x_dtype QMV_X_BF16_PAIR): against the oracle
+    # on the pair's values hi + lo (exact in float32), and against the chain's exact h
+    import torch
+    from helpers import dev_x
+    dim, hidden = 1024, 2816
+    m1 = inputs.make_matrix(2, 1, hidden, dim, seed=510)
+    m3 = inputs.make_matrix(2, 1, hidden, dim, seed=511)
+    m2 = inputs.make_matrix(2, 1, dim, hidden, seed=512)
+    x = inputs.make_x(1, dim, True, seed=513)
+    h = qmv.matvec_glu(2, 1, hidden, dim, dev_u8(m1.W), dev_u8(m3.W), dev_x(x)[0], act=act)
+    y = torch.empty((1, dim), device="cuda")
+    qmv.matvec_grouped(2, 1, [(dim, hidden, dev_u8(m2.W), h, y)], pair=True)
+    torch.cuda.synchronize()
+    h_gpu, _ = _pair_values(h)
+    y_ref, absref = oracle.matvec(m2.W, 2, 1, dim, hidden, h_gpu.astype(np.float32)[None, :])
+    check_product(y.cpu().numpy(), y_ref, absref, what=f"down projection on the pair ({act})")
+    check_product(y.cpu().numpy(), y_ref, absref, tol=1e-5, what=f"down projection tight ({act})")
+
+
+def test_pair_route_equals_float32_route_bits(qmv):
+    # a float32 vector x = hi + lo (hi, lo bfloat16, |lo| <= ulp(hi)/2) splits back into the same
+    # hi and lo, so the float32 route (split kernel + the same product) and the pair route give
+    # the same bits
+    import torch
+    from helpers import assert_bits_equal
+    rows, cols = 512, 1024
+    m = inputs.make_matrix(2, 1, rows, cols, seed=520)
+    rng = np.random.default_rng(521)
+    v = rng.standard_normal(cols).astype(np.float32)
+    hi = inputs.bf16_codes(v)
+    lo = inputs.bf16_codes(v - (hi.astype(np.uint32) << 16).view(np.float32))
+    pair = torch.from_numpy(np.stack([hi, lo]).view(np.int16)).cuda().view(torch.bfloat16)
+    xf = ((hi.astype(np.uint32) << 16).view(np.float32) + (lo.astype(np.uint32) << 16).view(np.float32))
+    W = dev_u8(m.W)
+    y1 = torch.empty((1, rows), device="cuda")
+    y2 = torch.empty((1, rows), device="cuda")
+    qmv.matvec_grouped(2, 1, [(rows, cols, W, pair, y1)], pair=True)
+    qmv.matvec_grouped(2, 1, [(rows, cols, W, torch.from_numpy(xf[None, :]).cuda(), y2)])
+    torch.cuda.synchronize()
+    assert_bits_equal(y1.cpu().numpy(), y2.cpu().numpy(), "pair route vs float32 route")
+    y_ref, absref = oracle.matvec(m.W, 2, 1, rows, cols, xf[None, :])
+    check_product(y1.cpu().numpy(), y_ref, absref, what="pair route")
+
+
+@pytest.mark.parametrize("act,act_id", ACTS)
+def test_fused_glu_full_size_llama7b(qmv, act, act_id):
+    # the Llama-7B FFN's w1 / w3 (11008 x 4096), every row against the oracle; the unfused path
+    # (grouped {w1, w3} into float32 gate and up, h formed from them) is held to the same bound
+    import torch
+    from helpers import dev_x
+    rows, cols = 11008, 4096
+    m1 = inputs.make_matrix(2, 1, rows, cols, seed=530)
+    m3 = inputs.make_matrix(2, 1, rows, cols, seed=531)
+    x = inputs.make_x(1, cols, True, seed=532)
+    W1, W3, xd = dev_u8(m1.W), dev_u8(m3.W), dev_x(x)
+    h = qmv.matvec_glu(2, 1, rows, cols, W1, W3, xd[0], act=act)
+    gu = torch.empty((2, 1, rows), device="cuda")
+    qmv.matvec_grouped(2, 1, [(rows, cols, W1, xd, gu[0]), (rows, cols, W3, xd, gu[1])])
+    torch.cuda.synchronize()
+    h_gpu, _ = _pair_values(h)
+    gate, G = oracle.matvec(m1.W, 2, 1, rows, cols, x)
+    up, U = oracle.matvec(m3.W, 2, 1, rows, cols, x)
+    _check_h(h_gpu, gate[0], G[0], up[0], U[0], act_id, f"full-size fused {act}")
+    g, u = gu[0, 0].cpu().numpy().astype(np.float64), gu[1, 0].cpu().numpy().astype(np.float64)
+    _check_h(oracle.glu(act_id, g, u), gate[0], G[0], up[0], U[0], act_id, f"full-size unfused {act}")
+    assert qmv.last_error() == 0
