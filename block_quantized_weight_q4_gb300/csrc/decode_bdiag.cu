@@ -147,10 +147,11 @@ __device__ __forceinline__ void chunk_math(float (&acc)[Cfg<WT, F16, NW, CH>::MT
   using C = Cfg<WT, F16, NW, CH>;
   constexpr int MT = C::MT;
   float da[MT][4];  // block sums (both halves of a block), column j = block j
+  float dl[MT][4];  // XS: the same for the lo vector (scaled by 2^9 in HALF stages)
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) da[mt][i] = 0.f;
+    for (int i = 0; i < 4; ++i) da[mt][i] = dl[mt][i] = 0.f;
 #pragma unroll
   for (int bp = 0; bp < kBlocksPerStage / 2; ++bp) {
     uint32_t w[MT][4];  // Q4_0: [tile][row g blk 2bp, row g+8 blk 2bp, row g blk 2bp+1, row g+8 blk 2bp+1]
@@ -177,8 +178,8 @@ __device__ __forceinline__ void chunk_math(float (&acc)[Cfg<WT, F16, NW, CH>::MT
             mma_f16_16816(da[mt], g01, h01, g23, h23, b[0], b[1], da[mt]);
             mma_f16_16816(da[mt], gh01, hh01, gh23, hh23, b[2], b[3], da[mt]);
             if (XS) {
-              mma_f16_16816(da[mt], g01, h01, g23, h23, bl[0], bl[1], da[mt]);
-              mma_f16_16816(da[mt], gh01, hh01, gh23, hh23, bl[2], bl[3], da[mt]);
+              mma_f16_16816(dl[mt], g01, h01, g23, h23, bl[0], bl[1], dl[mt]);
+              mma_f16_16816(dl[mt], gh01, hh01, gh23, hh23, bl[2], bl[3], dl[mt]);
             }
           } else {
             q4_word_to_bf16_levels(w[mt][2 * hb], g01, g23, gh01, gh23);
@@ -186,8 +187,8 @@ __device__ __forceinline__ void chunk_math(float (&acc)[Cfg<WT, F16, NW, CH>::MT
             mma_bf16_16816(da[mt], g01, h01, g23, h23, b[0], b[1], da[mt]);
             mma_bf16_16816(da[mt], gh01, hh01, gh23, hh23, b[2], b[3], da[mt]);
             if (XS) {
-              mma_bf16_16816(da[mt], g01, h01, g23, h23, bl[0], bl[1], da[mt]);
-              mma_bf16_16816(da[mt], gh01, hh01, gh23, hh23, bl[2], bl[3], da[mt]);
+              mma_bf16_16816(dl[mt], g01, h01, g23, h23, bl[0], bl[1], dl[mt]);
+              mma_bf16_16816(dl[mt], gh01, hh01, gh23, hh23, bl[2], bl[3], dl[mt]);
             }
           }
         }
@@ -205,8 +206,8 @@ __device__ __forceinline__ void chunk_math(float (&acc)[Cfg<WT, F16, NW, CH>::MT
           mma_f16_16816(da[0], g0a, h0a, g0b, h0b, b[0], b[1], da[0]);
           mma_f16_16816(da[0], g1a, h1a, g1b, h1b, b[2], b[3], da[0]);
           if (XS) {
-            mma_f16_16816(da[0], g0a, h0a, g0b, h0b, bl[0], bl[1], da[0]);
-            mma_f16_16816(da[0], g1a, h1a, g1b, h1b, bl[2], bl[3], da[0]);
+            mma_f16_16816(dl[0], g0a, h0a, g0b, h0b, bl[0], bl[1], dl[0]);
+            mma_f16_16816(dl[0], g1a, h1a, g1b, h1b, bl[2], bl[3], dl[0]);
           }
         } else {
           q8_word_to_bf16_levels(q[0], g0a, g0b);
@@ -216,8 +217,8 @@ __device__ __forceinline__ void chunk_math(float (&acc)[Cfg<WT, F16, NW, CH>::MT
           mma_bf16_16816(da[0], g0a, h0a, g0b, h0b, b[0], b[1], da[0]);
           mma_bf16_16816(da[0], g1a, h1a, g1b, h1b, b[2], b[3], da[0]);
           if (XS) {
-            mma_bf16_16816(da[0], g0a, h0a, g0b, h0b, bl[0], bl[1], da[0]);
-            mma_bf16_16816(da[0], g1a, h1a, g1b, h1b, bl[2], bl[3], da[0]);
+            mma_bf16_16816(dl[0], g0a, h0a, g0b, h0b, bl[0], bl[1], dl[0]);
+            mma_bf16_16816(dl[0], g1a, h1a, g1b, h1b, bl[2], bl[3], dl[0]);
           }
         }
       }
@@ -239,8 +240,10 @@ __device__ __forceinline__ void chunk_math(float (&acc)[Cfg<WT, F16, NW, CH>::MT
         d0 = v.x;
         d1 = v.y;
       }
-      const float s0 = da[mt][2 * h];
-      const float s1 = da[mt][2 * h + 1];
+      // XS: the lo vector's sums, scaled back (2^-9 is exact) in HALF stages
+      constexpr float kLoBack = HALF ? 0x1p-9f : 1.0f;
+      const float s0 = XS ? da[mt][2 * h] + dl[mt][2 * h] * kLoBack : da[mt][2 * h];
+      const float s1 = XS ? da[mt][2 * h + 1] + dl[mt][2 * h + 1] * kLoBack : da[mt][2 * h + 1];
       acc[mt][h] = fmaf(d1, s1, fmaf(d0, s0, acc[mt][h]));
     }
   }
@@ -409,10 +412,13 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
             const uint8_t* xl = xring + cs * C::X_STAGE + e * (kTK * 2) + g * 64 + t * 8;
             xa[e] = *reinterpret_cast<const uint2*>(xl);
             xb[e] = *reinterpret_cast<const uint2*>(xl + 32);
-            hx[e][0] = bf16x2_to_f16x2(xa[e].x, exact);
-            hx[e][1] = bf16x2_to_f16x2(xa[e].y, exact);
-            hx[e][2] = bf16x2_to_f16x2(xb[e].x, exact);
-            hx[e][3] = bf16x2_to_f16x2(xb[e].y, exact);
+            // XS: the lo vector (about 2^-9 of hi) scaled by 2^9, exactly, so that its values lie
+            // where IEEE half holds them exactly as often as hi's do
+            const float sc = (XS && e >= C::kCH) ? 512.0f : 1.0f;
+            hx[e][0] = bf16x2_to_f16x2_scaled(xa[e].x, sc, exact);
+            hx[e][1] = bf16x2_to_f16x2_scaled(xa[e].y, sc, exact);
+            hx[e][2] = bf16x2_to_f16x2_scaled(xb[e].x, sc, exact);
+            hx[e][3] = bf16x2_to_f16x2_scaled(xb[e].y, sc, exact);
           }
           if (__all_sync(0xffffffffu, exact)) {
 #pragma unroll

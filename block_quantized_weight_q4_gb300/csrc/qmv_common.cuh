@@ -246,6 +246,18 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t p, bool& exact) {
   return h;
 }
 
+// The same for a bfloat16 pair times a power of two `scale` (exact in float32).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t p, float scale, bool& exact) {
+  const float lo = __uint_as_float(p << 16) * scale;
+  const float hi = __uint_as_float(p & 0xFFFF0000u) * scale;
+  uint32_t h;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(hi), "f"(lo));
+  const float blo = __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xFFFFu)));
+  const float bhi = __half2float(__ushort_as_half(static_cast<unsigned short>(h >> 16)));
+  exact = exact & (blo == lo) & (bhi == hi);
+  return h;
+}
+
 // Four Q4_0 quant bytes (as for q4_word_to_bf16_levels) to exact IEEE half levels in natural
 // pairs.  prmt puts byte b under the half exponent of 1024 (0x6400 | b is 1024 + b: the
 // 10-bit mantissa takes the whole byte); H = 1024 + 16 hi + 8 (the low nibble replaced by 8);
@@ -326,6 +338,69 @@ __device__ __forceinline__ void split_bf16_pair(float v, uint16_t& hi, uint16_t&
   hi = bf16_bits_rn_finite(v);
   const float h = __uint_as_float((uint32_t)hi << 16);
   lo = isfinite(v) ? bf16_bits_rn_finite(v - h) : 0;
+}
+
+
+// ---------------------------------------------------------------------------- activation rule
+// The runtime's activation quantizer on one block of 32 values (Krafla page, "Quantization
+// rule", Q8_0 with a float32 scale): amax = max |x|; amax < 1e-30 gives the zero block (d = 0,
+// every quant 0); else d = amax / 127 and q = trunc(x * (127 / amax) + copysign(0.5, x)),
+// clamped to +-127; each step one float32 operation rounded to nearest.  w[g] holds quants
+// 4g..4g+3 (byte k = quant 4g + k); returns d.
+__device__ __forceinline__ float act_q8_block(const float (&x)[32], uint32_t (&w)[8]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    const float a = fabsf(x[e]);
+    if (a > amax) amax = a;
+  }
+  float inv = 0.f, d = 0.f;  // the zero block
+  if (!(amax < 1e-30f)) {
+    inv = __fdiv_rn(127.0f, amax);
+    d = __fdiv_rn(amax, 127.0f);
+  }
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    uint32_t packed = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      // inv = 0 gives trunc(+-0.5) = 0 with no branch; the conversion truncates
+      const float xe = x[4 * g + k];
+      int v = (int)__fadd_rn(__fmul_rn(xe, inv), copysignf(0.5f, xe));
+      v = v > 127 ? 127 : (v < -127 ? -127 : v);
+      packed |= (uint32_t)(v & 0xFF) << (8 * k);
+    }
+    w[g] = packed;
+  }
+  return d;
+}
+
+// 32 activations (float32, or bfloat16 widened exactly) starting at element `first` of x.
+template <bool BF16>
+__device__ __forceinline__ void load_act_block(const void* __restrict__ x, long long first, float (&v)[32]) {
+  if (BF16) {
+    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + first);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 u = __ldg(p + i);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        v[8 * i + 2 * k] = __uint_as_float(w[k] << 16);  // element 2k: the low half
+        v[8 * i + 2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+      }
+    }
+  } else {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(x) + first);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 f = __ldg(p + i);
+      v[4 * i] = f.x;
+      v[4 * i + 1] = f.y;
+      v[4 * i + 2] = f.z;
+      v[4 * i + 3] = f.w;
+    }
+  }
 }
 
 }  // namespace qmv
