@@ -465,9 +465,14 @@ def other_workloads(torch, qmv, dev, l2, cap, peak_hbm, peak_tf):
         us = _graph_time_us(torch, [lambda i=i: qmv.matvec_qx(2, 1, 65536, 4096, Ws[i % n], xq, batch, y=y)
                                     for i in range(2 * n)], cap)
         qus = _graph_time_us(torch, [lambda: qmv.quantize_x(x, xq=xq)] * 64, cap)
+        # the quantizer inside the product (qmv_matvec_qx_grouped): one launch
+        fus = _graph_time_us(torch, [lambda i=i: qmv.matvec_qx_grouped(2, 1, [(65536, 4096, Ws[i % n], x, y)])
+                                     for i in range(2 * n)], cap)
         res[f"qx_q4_65536x4096_f16_b{batch}"] = {
             "us_per_product": round(us, 3), "weight_gbs": round(m.W.size / us / 1e3, 1),
-            "frac_hbm": round(m.W.size / us / 1e3 / peak_hbm, 4), "quantize_x_us": round(qus, 3)}
+            "frac_hbm": round(m.W.size / us / 1e3 / peak_hbm, 4), "quantize_x_us": round(qus, 3),
+            "fused_us_per_product": round(fus, 3), "fused_weight_gbs": round(m.W.size / fus / 1e3, 1),
+            "fused_frac_hbm": round(m.W.size / fus / 1e3 / peak_hbm, 4)}
     del Ws
     specs = layer_specs()
     lb = layer_bytes(specs)
@@ -490,9 +495,21 @@ def other_workloads(torch, qmv, dev, l2, cap, peak_hbm, peak_tf):
                 qmv.matvec_qx(s.wtype, s.scale_f16, s.rows, s.cols, copies[c][i], gxq[g], 1, y=ys[i])
 
     us = _graph_time_us(torch, [lambda c=c: qx_step(c) for c in range(ncopy)] * 2, cap)
+    res["qx_llama7b_layer_unfused_b1"] = {"us_per_step": round(us, 3), "weight_gbs": round(lb / us / 1e3, 1),
+                                          "frac_hbm": round(lb / us / 1e3 / peak_hbm, 4),
+                                          "launches_per_step": len(groups) + len(specs),
+                                          "note": "qmv_quantize_x per group, then qmv_matvec_qx per matrix"}
+
+    def qx_fused_step(c):
+        for g, grp in enumerate(groups):
+            qmv.matvec_qx_grouped(2, 1, [(specs[i].rows, specs[i].cols, copies[c][i], gx[g], ys[i]) for i in grp],
+                                  overlap=True)
+
+    us = _graph_time_us(torch, [lambda c=c: qx_fused_step(c) for c in range(ncopy)] * 2, cap)
     res["qx_llama7b_layer_b1"] = {"us_per_step": round(us, 3), "weight_gbs": round(lb / us / 1e3, 1),
-                                  "frac_hbm": round(lb / us / 1e3 / peak_hbm, 4),
-                                  "launches_per_step": len(groups) + len(specs)}
+                                  "frac_hbm": round(lb / us / 1e3 / peak_hbm, 4), "launches_per_step": len(groups),
+                                  "note": "qmv_matvec_qx_grouped per group: activations quantized inside the "
+                                          "product, grouped problems, programmatic overlap"}
 
     # the layer step with the FFN's SwiGLU in the down projection's activation prep: w1 and w3
     # write gate and up into one buffer, w2 takes SiLU(gate) * up as float32 activations

@@ -84,6 +84,8 @@ def load_library():
     lib.qmv_quantize_q4_fit.argtypes = [i32, i64, i64, vp, vp, vp, vp]
     lib.qmv_quantize_x.restype = i32
     lib.qmv_quantize_x.argtypes = [i32, i64, i64, vp, vp, vp]
+    lib.qmv_matvec_qx_grouped.restype = i32
+    lib.qmv_matvec_qx_grouped.argtypes = [i32, i32, i32, i32, vp, i32, ctypes.c_uint, vp]
     lib.qmv_matvec_qx.restype = i32
     lib.qmv_matvec_qx.argtypes = [i32, i32, i64, i64, vp, vp, vp, i32, vp]
     lib.qmv_check_device.restype = i32
@@ -414,6 +416,16 @@ def matvec_qx(wtype: int, scale_dtype: int, rows: int, cols: int, W, xq, batch: 
                                       batch, _stream(stream))
     _check(st, "qmv_matvec_qx")
     return y
+
+
+def matvec_qx_grouped(wtype: int, scale_dtype: int, problems, overlap: bool = False, stream=None):
+    """The activation-quantized product with the activation quantizer inside the launch
+    (qmv_matvec_qx_grouped): problems as for matvec_grouped, x float32 or bfloat16 (batch, cols);
+    each y receives matvec_qx(W, quantize_x(x))."""
+    arr, n, batch, xdt = _problem_array(problems)
+    st = load_library().qmv_matvec_qx_grouped(wtype, scale_dtype, xdt, batch, ctypes.addressof(arr), n,
+                                              FLAG_OVERLAP if overlap else 0, _stream(stream))
+    _check(st, "qmv_matvec_qx_grouped")
 
 
 def quantize_q4_fit(scale_dtype: int, src, W=None, stream=None):

@@ -47,7 +47,6 @@ namespace qmv {
 
 namespace {
 
-constexpr int kMaxWarps = 16;        // warps per CTA: 4, or 8 or 16 for launches with few tiles
 constexpr int kTK = 256;             // weights per stage and row
 constexpr int kBlocksPerStage = kTK / 32;
 constexpr int kRows = 16;            // rows per MMA tile

@@ -1,0 +1,18 @@
+// matvec_qx_fused_q8.cu -- the activation-quantized product with in-kernel activation
+// quantization, Q8_0 weights (kernels in matvec_qx.cuh), and the entry that picks the type.
+#include "matvec_qx.cuh"
+
+namespace qmv {
+
+cudaError_t launch_matvec_qx_fused_q4(const MatrixRef* ms, const void* const* xs, float* const* ys, int n,
+                                      bool x_bf16, int batch, bool pdl, const DeviceInfo& dev, cudaStream_t stream);
+
+cudaError_t launch_matvec_qx_fused(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool x_bf16,
+                                   int batch, bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
+  if (n < 1 || n > qx::kMaxFused) return cudaErrorInvalidValue;
+  if (ms[0].wtype == QMV_Q4_0) return launch_matvec_qx_fused_q4(ms, xs, ys, n, x_bf16, batch, pdl, dev, stream);
+  return x_bf16 ? qx::launch_fused_wtype<QMV_Q8_0, true>(ms, xs, ys, n, batch, pdl, dev, stream)
+                : qx::launch_fused_wtype<QMV_Q8_0, false>(ms, xs, ys, n, batch, pdl, dev, stream);
+}
+
+}  // namespace qmv

@@ -439,6 +439,37 @@ int qmv_matvec_qx(int wtype, int scale_dtype, int64_t rows, int64_t cols, const 
   return launch_matvec_qx(m, xqq, xd, batch, y, dev, stream) == cudaSuccess ? QMV_OK : QMV_E_CUDA;
 }
 
+int qmv_matvec_qx_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const qmv_problem* problems, int n,
+                          unsigned flags, cudaStream_t stream) {
+  if (problems == nullptr || n < 1 || n > QMV_MAX_GROUP) return QMV_E_ARG;
+  if (x_dtype != QMV_X_F32 && x_dtype != QMV_X_BF16) return QMV_E_FORMAT;
+  if (batch < 0) return QMV_E_ARG;
+  if ((flags & ~QMV_FLAG_OVERLAP) != 0) return QMV_E_ARG;
+  MatrixRef ms[QMV_MAX_GROUP];
+  const void* xs[QMV_MAX_GROUP];
+  float* ys[QMV_MAX_GROUP];
+  const int64_t nv = batch < 8 ? batch : 8;
+  for (int i = 0; i < n; ++i) {
+    const qmv_problem& pr = problems[i];
+    const int st = make_ref(wtype, scale_dtype, pr.rows, pr.cols, pr.W, &ms[i]);
+    if (st != QMV_OK) return st;
+    if (nv * pr.cols > QMV_QX_MAX_VEC_COLS) return QMV_E_SHAPE;
+    xs[i] = pr.x;
+    ys[i] = pr.y;
+    if (batch == 0) continue;
+    if (pr.x == nullptr || pr.y == nullptr) return QMV_E_ARG;
+    if (!aligned(pr.x, 16) || !aligned(pr.y, 4)) return QMV_E_ALIGN;
+    if (pr.rows > INT64_MAX / batch) return QMV_E_SHAPE;
+  }
+  if (batch == 0) return QMV_OK;
+  DeviceInfo dev;
+  if (current_device_info(&dev) != cudaSuccess) return QMV_E_CUDA;
+  return launch_matvec_qx_fused(ms, xs, ys, n, x_dtype == QMV_X_BF16, batch, (flags & QMV_FLAG_OVERLAP) != 0, dev,
+                                stream) == cudaSuccess
+             ? QMV_OK
+             : QMV_E_CUDA;
+}
+
 int qmv_quantize_q4_fit(int scale_dtype, int64_t rows, int64_t cols, const float* src, void* W, int64_t* first_bad,
                         cudaStream_t stream) {
   Layout L;

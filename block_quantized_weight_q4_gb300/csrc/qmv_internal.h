@@ -79,6 +79,12 @@ cudaError_t launch_quantize_x(bool x_bf16, int64_t batch, int64_t cols, const vo
 // xq / xd: the quants and scales of the batch x cols Q8_0 / f32 activation image.
 cudaError_t launch_matvec_qx(const MatrixRef& m, const int8_t* xq, const float* xd, int batch, float* y,
                              const DeviceInfo& dev, cudaStream_t stream);
+// The same product for 1..8 problems of one weight type and scale type in one launch per pass
+// of 8 vectors, each with its float activations (batch x cols, bf16 or f32), which the kernel
+// quantizes itself (the bytes launch_quantize_x writes) into shared memory: needs
+// min(batch, 8) * cols * 9 / 8 bytes of shared memory for the largest cols of the group.
+cudaError_t launch_matvec_qx_fused(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool x_bf16,
+                                   int batch, bool pdl, const DeviceInfo& dev, cudaStream_t stream);
 
 // Any shape with cols % 32 == 0; batch 1..8 per call.
 cudaError_t launch_matvec_simple(const MatrixRef& m, const void* x, bool x_bf16, float* y, int batch,

@@ -333,30 +333,13 @@ __global__ void __launch_bounds__(128) quantize_x_kernel(const void* __restrict_
   const long long blk = (long long)blockIdx.x * 128 + threadIdx.x;
   if (blk >= nblk) return;
   float v[32];
-  if (BF16) {
-    const uint4* p = reinterpret_cast<const uint4*>(x) + blk * 4;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4 u = __ldg(p + i);
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        v[8 * i + 2 * k] = __uint_as_float(w[k] << 16);  // element 2k: the low half
-        v[8 * i + 2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
-      }
-    }
-  } else {
-    const float4* p = reinterpret_cast<const float4*>(x) + blk * 8;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float4 f = __ldg(p + i);
-      v[4 * i] = f.x;
-      v[4 * i + 1] = f.y;
-      v[4 * i + 2] = f.z;
-      v[4 * i + 3] = f.w;
-    }
-  }
-  quantize_block<QMV_Q8_0, false>(v, blk, q, d, nullptr);  // an f32 scale is never refused
+  load_act_block<BF16>(x, blk * 32, v);
+  uint32_t w[8];
+  const float dv = act_q8_block(v, w);
+  uint4* dst = reinterpret_cast<uint4*>(q + blk * 32);
+  dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  reinterpret_cast<float*>(d)[blk] = dv;
 }
 
 }  // namespace

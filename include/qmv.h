@@ -343,6 +343,25 @@ int qmv_quantize_x(int x_dtype, int64_t batch, int64_t cols, const void *x, void
 int qmv_matvec_qx(int wtype, int scale_dtype, int64_t rows, int64_t cols, const void *W, const void *xq,
                   float *y, int batch, cudaStream_t stream);
 
+/* The activation-quantized product with the activation quantizer inside it, for several
+ * products in one launch: for each problem, y = qmv_matvec_qx(W, qmv_quantize_x(x)) -- the same
+ * activation quants and scales (the runtime's Q8_0 / f32-scale rule), the same integer block dots
+ * and float32 steps -- without the separate quantizer launch or the intermediate image: each CTA
+ * quantizes its problem's activations into shared memory (a few KB per vector) and reads them
+ * from there.  All n problems share wtype, scale_dtype, x_dtype and batch; each has its own rows,
+ * cols, W, x and y (problems of one layer that read the same activations: pass the same x).
+ *   x_dtype : QMV_X_F32 or QMV_X_BF16 (QMV_E_FORMAT otherwise); x : device, batch x cols,
+ *             row-major, 16-byte aligned.  y : device, batch x rows float32, 4-byte aligned.
+ *   min(batch, 8) * (the largest cols of the group) <= QMV_QX_MAX_VEC_COLS, else QMV_E_SHAPE
+ *   (the shared memory of one pass); 1 <= n <= QMV_MAX_GROUP, flags 0 or QMV_FLAG_OVERLAP,
+ *   else QMV_E_ARG.
+ * Results agree with those of qmv_quantize_x followed by qmv_matvec_qx within the tolerance stated
+ * there (the column slices may be added in a different grouping) and do not depend on timing.
+ * Allocates nothing.  Asynchronous.  Returns as qmv_matvec_grouped. */
+#define QMV_QX_MAX_VEC_COLS 200704
+int qmv_matvec_qx_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const qmv_problem *problems, int n,
+                          unsigned flags, cudaStream_t stream);
+
 /* The Q4_0 best-fit writer (Krafla page, "Quantization rule": the search tools/mlb.py runs
  * per block), arguments, layout and refusal as qmv_quantize with wtype QMV_Q4_0.  Per block:
  * m = the element of largest magnitude (the first of equals); for the candidate levels

@@ -180,6 +180,26 @@ def test_matvec_glu_argument_errors(lib):
     assert glu(x=FAKE + 2) == binding.E_ALIGN and glu(h=FAKE + 4) == binding.E_ALIGN
 
 
+def test_matvec_qx_grouped_argument_errors(lib):
+    def call(wt=2, sf=1, xd=1, batch=1, rows=64, cols=64, W=FAKE, x=FAKE, y=FAKE, n=1, flags=0, null=False):
+        arr = (binding.Problem * 1)(binding.Problem(rows, cols, W, x, y))
+        return lib.qmv_matvec_qx_grouped(wt, sf, xd, batch, None if null else ctypes.addressof(arr), n, flags, None)
+    assert call(null=True) == binding.E_ARG
+    assert call(n=0) == binding.E_ARG and call(n=9) == binding.E_ARG
+    assert call(xd=2) == binding.E_FORMAT and call(xd=4) == binding.E_FORMAT
+    assert call(batch=-1) == binding.E_ARG
+    assert call(flags=2) == binding.E_ARG
+    assert call(wt=3) == binding.E_FORMAT and call(sf=2) == binding.E_FORMAT
+    assert call(cols=48) == binding.E_SHAPE and call(rows=0) == binding.E_SHAPE
+    # one pass of 8 vectors keeps 8 * cols quants in shared memory
+    assert call(batch=8, cols=25120 * 2) == binding.E_SHAPE
+    assert call(batch=1, cols=200704 + 32) == binding.E_SHAPE
+    assert call(W=0) == binding.E_ARG and call(x=0) == binding.E_ARG and call(y=0) == binding.E_ARG
+    assert call(W=FAKE + 8) == binding.E_ALIGN and call(x=FAKE + 8) == binding.E_ALIGN
+    assert call(y=FAKE + 2) == binding.E_ALIGN
+    assert call(batch=0, x=0, y=0) == binding.OK
+
+
 def test_strerror_never_null(lib):
     for s in (0, 2, 3, 4, 5, 6, 7, 99, -1):
         assert isinstance(lib.qmv_strerror(s), bytes) and lib.qmv_strerror(s)

@@ -179,3 +179,114 @@ def test_matvec_qx_empty_batch_and_y_untouched(qmv):
     out = qmv.matvec_qx(2, 1, 64, 64, dev_u8(m.W), torch.empty(0, dtype=torch.uint8, device="cuda"), 0, y=y)
     torch.cuda.synchronize()
     assert out.shape == (0, 64)
+
+
+# --------------------------------------------- quantizer inside the product (qmv_matvec_qx_grouped)
+def gpu_qx_grouped(q, wt, sf, mats, xs, bf16, overlap=False):
+    import torch
+    probs = []
+    for m, x in zip(mats, xs):
+        xin = inputs.bf16_codes(x) if bf16 else x
+        probs.append((m.rows, m.cols, dev_u8(m.W), dev_x(xin), torch.full((x.shape[0], m.rows), 9.0, device="cuda")))
+    q.matvec_qx_grouped(wt, sf, probs, overlap=overlap)
+    torch.cuda.synchronize()
+    return [p[4].cpu().numpy() for p in probs]
+
+
+def oracle_qx(m, x, bf16):
+    xin = inputs.bf16_codes(x) if bf16 else x
+    xq = oracle.quantize_x(xin)
+    return oracle.matvec_qx(m.W, m.wtype, m.scale_f16, m.rows, m.cols, xq, x.shape[0])
+
+
+@pytest.mark.parametrize("wt,sf", TYPES)
+@pytest.mark.parametrize("bf16", [False, True])
+@pytest.mark.parametrize("shapes,batch", [([(37, 1024), (100, 1024)], 1), ([(300, 4096), (64, 4096), (64, 4096)], 3),
+                                          ([(70, 2048), (40, 4128)], 8), ([(5, 96)], 11), ([(200, 512)], 2)])
+def test_matvec_qx_grouped_matches_oracle(qmv, wt, sf, bf16, shapes, batch):
+    rng = np.random.default_rng(sum(r for r, _ in shapes) + batch + 10 * wt + sf + bf16)
+    mats = [inputs.make_matrix(wt, sf, r, c, seed=r * 3 + c + i) for i, (r, c) in enumerate(shapes)]
+    xs = [activations(rng, batch, c) for _, c in shapes]
+    ys = gpu_qx_grouped(qmv, wt, sf, mats, xs, bf16)
+    for m, x, y in zip(mats, xs, ys):
+        y_ref, absref = oracle_qx(m, x, bf16)
+        what = f"qx grouped {wt},{sf} bf16={bf16} {m.rows}x{m.cols} b{batch}"
+        check_product(y, y_ref, absref, what=what)
+        check_product(y, y_ref, absref, tol=1e-4, what=what + " tight")
+
+
+@pytest.mark.parametrize("wt", [1, 2])
+@pytest.mark.parametrize("batch", [1, 3, 8])
+def test_matvec_qx_grouped_exact_case(qmv, wt, batch):
+    # the exact case of test_matvec_qx_exact_case for a group of two problems: bit-exact
+    rng = np.random.default_rng(90 + wt + batch)
+    mats, xs = [], []
+    for rows, cols in [(9, 128), (17, 256)]:
+        if wt == 1:
+            q = rng.integers(-127, 128, rows * cols).astype(np.int8).view(np.uint8)
+        else:
+            q = rng.integers(0, 256, rows * cols // 2).astype(np.uint8)
+        d = np.full(rows * cols // 32, 2.0 ** -6, np.float32).view(np.uint32)
+        W = inputs.assemble(wt, 0, rows, cols, q, d)
+        mats.append(inputs.Matrix(wt, 0, rows, cols, W, q, d.reshape(rows, cols // 32)))
+        k = rng.integers(-127, 128, (batch, cols // 32, 32))
+        k[:, :, 3] = 127
+        xs.append((k * 2.0 ** -4).reshape(batch, cols).astype(np.float32))
+    ys = gpu_qx_grouped(qmv, wt, 0, mats, xs, False)
+    for m, x, y in zip(mats, xs, ys):
+        y_ref, _ = oracle_qx(m, x, False)
+        assert np.array_equal(y.astype(np.float64), y_ref), f"exact grouped qx {wt} b{batch} {m.rows}x{m.cols}"
+
+
+@pytest.mark.parametrize("batch", [1, 8])
+def test_matvec_qx_grouped_llama7b_groups_sampled(qmv, batch):
+    # the layer's groups as the layer step runs them ({wq,wk,wv} on one x, {w1,w3} on one x,
+    # {w2} on 11008 columns): sampled rows of every matrix against the oracle
+    rng = np.random.default_rng(95 + batch)
+    spec = {s.name: s for s in inputs.WORKLOADS["llama7b"].matrices}
+    for grp in (["wq", "wk", "wv"], ["w1", "w3"], ["w2"]):
+        mats = [inputs.make_matrix(spec[n].wtype, spec[n].scale_f16, spec[n].rows, spec[n].cols, seed=300 + i)
+                for i, n in enumerate(grp)]
+        x = activations(rng, batch, mats[0].cols)
+        ys = gpu_qx_grouped(qmv, 2, 1, mats, [x] * len(mats), True)
+        xq = oracle.quantize_x(inputs.bf16_codes(x))
+        for m, y in zip(mats, ys):
+            ids = np.unique(np.concatenate([np.arange(8), m.rows - 1 - np.arange(8), rng.integers(0, m.rows, 32)]))
+            y_ref, absref = oracle.matvec_qx(sub_matrix(m, ids), 2, 1, ids.size, m.cols, xq, batch)
+            check_product(y[:, ids], y_ref, absref, tol=1e-4, what=f"layer group {grp} b{batch}")
+
+
+def test_matvec_qx_grouped_repeat_overlap_and_graph_bit_identical(qmv):
+    # the same launch eagerly, with the overlap flag after a kernel that writes x, and in graph
+    # replays: the same bits; and the same sums as the two-step path within the tolerance
+    import torch
+    rows, cols, batch = 14336, 4096, 2
+    m = inputs.make_matrix(2, 1, rows, cols, seed=7)
+    x = activations(np.random.default_rng(8), batch, cols)
+    W = dev_u8(m.W)
+    xd = dev_x(inputs.bf16_codes(x))
+    xsrc = xd.clone()
+    y1 = torch.empty((batch, rows), device="cuda")
+    qmv.matvec_qx_grouped(2, 1, [(rows, cols, W, xd, y1)])
+    torch.cuda.synchronize()
+    first = y1.cpu().numpy().copy()
+    y2 = torch.empty_like(y1)
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.graph(g, stream=s):
+        xd.copy_(xsrc)   # the activations come from the kernel just before the product
+        qmv.matvec_qx_grouped(2, 1, [(rows, cols, W, xd, y2)], overlap=True)
+    for _ in range(4):
+        xd.zero_()
+        y2.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert_bits_equal(y2.cpu().numpy(), first, "graph replay with overlap")
+    xq = qmv.quantize_x(xd)
+    y3 = qmv.matvec_qx(2, 1, rows, cols, W, xq, batch)
+    torch.cuda.synchronize()
+    ids = np.arange(0, rows, 97)
+    y_ref, absref = oracle.matvec_qx(sub_matrix(m, ids), 2, 1, ids.size, cols, xq.cpu().numpy(), batch)
+    check_product(first[:, ids], y_ref, absref, tol=1e-4, what="fused")
+    check_product(y3.cpu().numpy()[:, ids], y_ref, absref, tol=1e-4, what="two-step")
+    assert qmv.last_error() == 0
