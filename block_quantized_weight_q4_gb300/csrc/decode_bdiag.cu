@@ -249,12 +249,17 @@ __device__ __forceinline__ void chunk_math(float (&acc)[Cfg<WT, F16, NW, CH>::MT
   }
 }
 
-template <int WT, bool F16, int NW, int CH, bool XS, bool GLU = false>
+// XF (with XS): the activations arrive as float32 (one box of CH x 256 values per stage, the
+// bytes of the hi and lo boxes) and each lane splits its values into hi = RN_bf16(x) and
+// lo = RN_bf16(x - hi) in registers (split_bf16_pair, the split kernel's rule), so float32
+// activations take one launch.
+template <int WT, bool F16, int NW, int CH, bool XS, bool GLU = false, bool XF = false>
 __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_constant__ Maps maps,
                                                                const __grid_constant__ Params p) {
   using C = Cfg<WT, F16, NW, CH, XS>;
   constexpr int MT = C::MT;
   static_assert(!GLU || (MT == 2 && !XS), "the gated pair takes two 16-row MMA tiles per warp tile");
+  static_assert(!XF || XS, "float32 activations are split into the hi and lo parts");
   constexpr int TROWS = GLU ? kRows : C::WROWS;  // rows of each matrix per warp tile
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -322,7 +327,8 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
         }
         if (with_x) {
           tma_load_2d_keep(xring + ps * C::X_STAGE, &maps.x[pc.prob], 0, c * C::kCH, &bars[ps]);
-          if (XS) tma_load_2d_keep(xring + ps * C::X_STAGE + C::X_PART, &maps.xl[pc.prob], 0, c * C::kCH, &bars[ps]);
+          if (XS && !XF)
+            tma_load_2d_keep(xring + ps * C::X_STAGE + C::X_PART, &maps.xl[pc.prob], 0, c * C::kCH, &bars[ps]);
         }
       } else {
         mbar_arrive(&bars[ps]);  // a tile past the end of its problem: complete the phase, no data
@@ -357,7 +363,7 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
     for (int i = 0; i < pre; ++i)
       if (pre_valid[i]) {
         tma_load_2d_keep(xring + i * C::X_STAGE, &maps.x[pre_prob[i]], 0, pre_c[i] * C::kCH, &bars[i]);
-        if (XS)
+        if (XS && !XF)
           tma_load_2d_keep(xring + i * C::X_STAGE + C::X_PART, &maps.xl[pre_prob[i]], 0, pre_c[i] * C::kCH, &bars[i]);
       }
   }
@@ -407,11 +413,31 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
           uint2 xa[NX], xb[NX];
           uint32_t hx[NX][4];
           bool exact = true;
+          if (XF) {
+            // float32 activations: elements 4t..4t+3 and 16+4t..16+4t+3 of block g of each chunk,
+            // split into the bf16 hi (chunk h) and lo (chunk CH + h) parts
+#pragma unroll
+            for (int h = 0; h < C::kCH; ++h) {
+              const uint8_t* xf = xring + cs * C::X_STAGE + h * (kTK * 4) + g * 128 + t * 16;
+              const float4 fa = *reinterpret_cast<const float4*>(xf);
+              const float4 fb = *reinterpret_cast<const float4*>(xf + 64);
+              const float v[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
+              uint16_t hi[8], lo[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) split_bf16_pair(v[k], hi[k], lo[k]);
+              xa[h] = make_uint2(hi[0] | ((uint32_t)hi[1] << 16), hi[2] | ((uint32_t)hi[3] << 16));
+              xb[h] = make_uint2(hi[4] | ((uint32_t)hi[5] << 16), hi[6] | ((uint32_t)hi[7] << 16));
+              xa[C::kCH + h] = make_uint2(lo[0] | ((uint32_t)lo[1] << 16), lo[2] | ((uint32_t)lo[3] << 16));
+              xb[C::kCH + h] = make_uint2(lo[4] | ((uint32_t)lo[5] << 16), lo[6] | ((uint32_t)lo[7] << 16));
+            }
+          }
 #pragma unroll
           for (int e = 0; e < NX; ++e) {
-            const uint8_t* xl = xring + cs * C::X_STAGE + e * (kTK * 2) + g * 64 + t * 8;
-            xa[e] = *reinterpret_cast<const uint2*>(xl);
-            xb[e] = *reinterpret_cast<const uint2*>(xl + 32);
+            if (!XF) {
+              const uint8_t* xl = xring + cs * C::X_STAGE + e * (kTK * 2) + g * 64 + t * 8;
+              xa[e] = *reinterpret_cast<const uint2*>(xl);
+              xb[e] = *reinterpret_cast<const uint2*>(xl + 32);
+            }
             // XS: the lo vector (about 2^-9 of hi) scaled by 2^9, exactly, so that its values lie
             // where IEEE half holds them exactly as often as hi's do
             const float sc = (XS && e >= C::kCH) ? 512.0f : 1.0f;
@@ -514,10 +540,10 @@ struct Plan {
   long long cost = -1;
 };
 
-template <int WT, bool F16, int NW, int CH, bool XS, bool GLU = false>
+template <int WT, bool F16, int NW, int CH, bool XS, bool GLU = false, bool XF = false>
 cudaError_t plan_typed(const MatrixRef* ms, int n, const DeviceInfo& dev, Plan* out) {
   using C = Cfg<WT, F16, NW, CH, XS>;
-  auto kern = matvec_bdiag_kernel<WT, F16, NW, CH, XS, GLU>;
+  auto kern = matvec_bdiag_kernel<WT, F16, NW, CH, XS, GLU, XF>;
   // per device: the shared-memory attribute set and the occupancy known (0 = does not fit)
   static std::mutex mu;
   static bool ready[64] = {};
@@ -571,7 +597,7 @@ cudaError_t plan_typed(const MatrixRef* ms, int n, const DeviceInfo& dev, Plan* 
 
 // GLU: ms = {w1, w3} (same shape), one x (xs[0]); the pair is one problem whose warp tiles are
 // 16 rows of each; act and h as in Params.
-template <int WT, bool F16, int NW, int CH, bool XS, bool GLU = false>
+template <int WT, bool F16, int NW, int CH, bool XS, bool GLU = false, bool XF = false>
 cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* const* xs, float* const* ys, int n,
                          bool pdl, const DeviceInfo& dev, cudaStream_t stream, int act = -1, uint16_t* h = nullptr) {
   using C = Cfg<WT, F16, NW, CH, XS>;
@@ -611,6 +637,12 @@ cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* cons
                          TROWS, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (err != cudaSuccess) return err;
     if (GLU && i == 1) continue;  // one x for the pair
+    if (XF) {  // float32 activations, split in the kernel
+      err = encode_tmap_2d(&maps.x[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, xs[i], kTK, (uint64_t)(m.cols / kTK), kTK * 4,
+                           kTK, C::kCH, CU_TENSOR_MAP_SWIZZLE_NONE);
+      if (err != cudaSuccess) return err;
+      continue;
+    }
     err = encode_tmap_2d(&maps.x[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xs[i], kTK, (uint64_t)(m.cols / kTK), kTK * 2,
                          kTK, C::kCH, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (err != cudaSuccess) return err;
@@ -632,7 +664,7 @@ cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* cons
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, matvec_bdiag_kernel<WT, F16, NW, CH, XS, GLU>, maps, p);
+  return cudaLaunchKernelEx(&cfg, matvec_bdiag_kernel<WT, F16, NW, CH, XS, GLU, XF>, maps, p);
 }
 
 // Q4_0 launches of at least this many weight bytes take one-chunk stages.
@@ -644,7 +676,7 @@ constexpr long long kOneChunkBytes = 32LL << 20;
 // launches of a few tens of MB (the Llama-7B layer's, the 4096 x 4096 product) and on Q8_0.
 // GLU: ms = {w1, w3}, planned as one matrix of twice the rows (the same warp tiles: 16 rows of
 // each per tile); act and h as in launch_typed.
-template <int WT, bool F16, bool XS, bool GLU = false>
+template <int WT, bool F16, bool XS, bool GLU = false, bool XF = false>
 cudaError_t launch_best(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
                         const DeviceInfo& dev, cudaStream_t stream, int act = -1, uint16_t* h = nullptr) {
   MatrixRef pair[1];
@@ -663,33 +695,33 @@ cudaError_t launch_best(const MatrixRef* ms, const void* const* xs, float* const
     for (int i = 0; i < pn; ++i) bytes += pm[i].rows * pm[i].cols / 2;
     if (bytes >= kOneChunkBytes) {
       Plan p1;
-      err = plan_typed<WT, F16, 4, 1, XS, GLU>(pm, pn, dev, &p1);
+      err = plan_typed<WT, F16, 4, 1, XS, GLU, XF>(pm, pn, dev, &p1);
       if (err != cudaSuccess) return err;
       if (p1.cost >= 0 && p1.grid > dev.sm_count)
-        return launch_typed<WT, F16, 4, 1, XS, GLU>(p1, ms, xs, ys, n, pdl, dev, stream, act, h);
+        return launch_typed<WT, F16, 4, 1, XS, GLU, XF>(p1, ms, xs, ys, n, pdl, dev, stream, act, h);
     }
   }
-  err = plan_typed<WT, F16, 4, 2, XS, GLU>(pm, pn, dev, &p4);
+  err = plan_typed<WT, F16, 4, 2, XS, GLU, XF>(pm, pn, dev, &p4);
   if (err != cudaSuccess) return err;
   if (p4.cost >= 0 && p4.grid > dev.sm_count)
-    return launch_typed<WT, F16, 4, 2, XS, GLU>(p4, ms, xs, ys, n, pdl, dev, stream, act, h);
-  err = plan_typed<WT, F16, 8, 2, XS, GLU>(pm, pn, dev, &p8);
+    return launch_typed<WT, F16, 4, 2, XS, GLU, XF>(p4, ms, xs, ys, n, pdl, dev, stream, act, h);
+  err = plan_typed<WT, F16, 8, 2, XS, GLU, XF>(pm, pn, dev, &p8);
   if (err != cudaSuccess) return err;
   if (p8.cost >= 0 && (p4.cost < 0 || p8.cost < p4.cost))
-    return launch_typed<WT, F16, 8, 2, XS, GLU>(p8, ms, xs, ys, n, pdl, dev, stream, act, h);
+    return launch_typed<WT, F16, 8, 2, XS, GLU, XF>(p8, ms, xs, ys, n, pdl, dev, stream, act, h);
   if (p4.cost < 0) return cudaErrorInvalidConfiguration;
-  return launch_typed<WT, F16, 4, 2, XS, GLU>(p4, ms, xs, ys, n, pdl, dev, stream, act, h);
+  return launch_typed<WT, F16, 4, 2, XS, GLU, XF>(p4, ms, xs, ys, n, pdl, dev, stream, act, h);
 }
 
-template <bool XS>
+template <bool XS, bool XF = false>
 cudaError_t launch_any(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
                        const DeviceInfo& dev, cudaStream_t stream) {
   const MatrixRef& m = ms[0];
   if (m.wtype == QMV_Q4_0)
-    return m.scale_f16 ? launch_best<QMV_Q4_0, true, XS>(ms, xs, ys, n, pdl, dev, stream)
-                       : launch_best<QMV_Q4_0, false, XS>(ms, xs, ys, n, pdl, dev, stream);
-  return m.scale_f16 ? launch_best<QMV_Q8_0, true, XS>(ms, xs, ys, n, pdl, dev, stream)
-                     : launch_best<QMV_Q8_0, false, XS>(ms, xs, ys, n, pdl, dev, stream);
+    return m.scale_f16 ? launch_best<QMV_Q4_0, true, XS, false, XF>(ms, xs, ys, n, pdl, dev, stream)
+                       : launch_best<QMV_Q4_0, false, XS, false, XF>(ms, xs, ys, n, pdl, dev, stream);
+  return m.scale_f16 ? launch_best<QMV_Q8_0, true, XS, false, XF>(ms, xs, ys, n, pdl, dev, stream)
+                     : launch_best<QMV_Q8_0, false, XS, false, XF>(ms, xs, ys, n, pdl, dev, stream);
 }
 
 }  // namespace
@@ -702,6 +734,11 @@ cudaError_t launch_matvec_bdiag(const MatrixRef* ms, const void* const* xs, floa
 cudaError_t launch_matvec_bdiag_split(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
                                       const DeviceInfo& dev, cudaStream_t stream) {
   return launch_any<true>(ms, xs, ys, n, pdl, dev, stream);
+}
+
+cudaError_t launch_matvec_bdiag_f32in(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
+                                      const DeviceInfo& dev, cudaStream_t stream) {
+  return launch_any<true, true>(ms, xs, ys, n, pdl, dev, stream);
 }
 
 bool matvec_bdiag_glu_supported(const MatrixRef& w1, const MatrixRef& w3) {

@@ -21,6 +21,10 @@ constexpr int kPrefillMinBatch = 16;  // from here on the tensor-memory kernel t
 constexpr int kTcMinBatch = 4;        // decode passes of this many bf16 vectors go to decode_tc
 constexpr long long kTcMinQ8Weights = 64LL << 20;  // and Q8_0 passes of 2-3 vectors over this many weights
 constexpr long long kF32SplitMinWeights = 256LL << 10;  // one f32 vector: split hi/lo from this many weights
+// one f32 vector: split in the product's own activation stage (one launch) below this many
+// weight bytes; above it the split kernel runs once per column and the product reads its parts
+// (every row tile of a large launch redoing the split measured 25% more instructions per stage)
+constexpr long long kF32InKernelMaxBytes = 16LL << 20;
 std::mutex g_dev_mutex;
 DeviceInfo g_dev[kMaxDevices];
 bool g_dev_ready[kMaxDevices] = {};
@@ -268,11 +272,17 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
       // done (a stream being captured without its split buffer yet falls through to mma.sync)
     } else if (xb && nb == 1) {
       if (launch_matvec_bdiag(fast, fx, fy, nf, pdl, dev, stream) != cudaSuccess) return QMV_E_CUDA;
+    } else if (!xb && !glu && nb == 1 && nweights >= kF32SplitMinWeights &&
+               nweights * (wtype == QMV_Q8_0 ? 2 : 1) / 2 < kF32InKernelMaxBytes) {
+      // one float32 vector: the block-diagonal kernel splits it into bf16 hi + lo parts in its
+      // activation stage and runs every block's MMAs once with each (one launch; below a few
+      // hundred KB of weights the one mma.sync launch measured quicker)
+      if (launch_matvec_bdiag_f32in(fast, fx, fy, nf, pdl, dev, stream) != cudaSuccess) return QMV_E_CUDA;
     } else if (!xb && nb == 1 && (glu || nweights >= kF32SplitMinWeights) &&
                launch_matvec_bdiag_f32(fast, fx, fy, nf, pdl, dev, stream, act, batch) == cudaSuccess) {
-      // one float32 vector: the block-diagonal kernel on its bf16 hi + lo parts (below a few
-      // hundred KB of weights, the one mma.sync launch that reads f32 x directly is quicker
-      // than the split kernel and the product)
+      // one vector of large launches or of gated activations: x (or act(gate) * up) formed and
+      // split into bf16 hi + lo by the split kernel (once per column, not once per row tile),
+      // then the block-diagonal kernel on the parts
     } else if (glu) {
       return QMV_E_ARG;  // gated activations need the stream's split buffer (see qmv.h)
     } else if (launch_matvec_mma(fast, fx, fy, nf, xb, nb, pdl, dev, stream) != cudaSuccess) {

@@ -113,6 +113,10 @@ cudaError_t launch_matvec_bdiag_split(const MatrixRef* ms, const void* const* xs
 bool matvec_bdiag_glu_supported(const MatrixRef& w1, const MatrixRef& w3);
 cudaError_t launch_matvec_bdiag_glu(const MatrixRef& w1, const MatrixRef& w3, const void* x, int act, uint16_t* h,
                                     bool pdl, const DeviceInfo& dev, cudaStream_t stream);
+// One float32 activation vector per problem (16-byte aligned), split into bfloat16 hi + lo in
+// the kernel's activation stage (one launch; the same parts and results as below).
+cudaError_t launch_matvec_bdiag_f32in(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
+                                      const DeviceInfo& dev, cudaStream_t stream);
 // One float32 activation vector per problem: split into hi + lo bfloat16 in the stream's
 // split buffer (2 rows per problem, up to 524,288 columns over the problems), then the above.
 // Fails (nothing launched) when the buffer would not hold them, or cannot be created while

@@ -316,6 +316,38 @@ def test_f32_activations_needing_the_lo_part_exact(qmv, wt, sf, batch):
     assert np.array_equal(y.astype(np.float64), y_ref)
 
 
+@pytest.mark.parametrize("wt,sf", TYPES)
+@pytest.mark.parametrize("rows,cols", [(600, 512), (300, 2048), (77, 4096)])
+def test_f32_one_vector_split_in_the_product_exact(qmv, wt, sf, rows, cols):
+    # one float32 vector over 256K weights or more: the block-diagonal kernel splits x into bf16
+    # hi + lo in its activation stage (one launch); the exact case of the test above
+    rng = np.random.default_rng(90 + wt + sf + rows)
+    m = inputs.make_matrix(wt, sf, rows, cols, seed=91 + rows)
+    q = m.q if wt == 2 else rng.integers(-7, 8, size=m.q.size).astype(np.int8).view(np.uint8)
+    codes = inputs.pow2_scales(rng, rows * cols // 32, sf, -2, 0)
+    W = inputs.assemble(wt, sf, rows, cols, q, codes)
+    m2 = inputs.Matrix(wt, sf, rows, cols, W, q, codes)
+    x = np.ldexp(rng.integers(-1023, 1024, size=(1, cols)).astype(np.float32), -6)
+    y_ref, _ = oracle.matvec(W, wt, sf, rows, cols, x)
+    assert np.array_equal(gpu_matvec(qmv, m2, x).astype(np.float64), y_ref)
+
+
+@pytest.mark.parametrize("wt,sf", [(2, 1), (1, 0)])
+def test_f32_one_vector_wide_magnitudes(qmv, wt, sf):
+    # float32 activations over sixty decades (1e-30 .. 1e30, zeros, negative zeros), split in the
+    # product: within the tolerance of the oracle, tight
+    rows, cols = 512, 1024
+    rng = np.random.default_rng(95 + wt)
+    m = inputs.make_matrix(wt, sf, rows, cols, seed=96)
+    x = (rng.standard_normal((1, cols)) * 10.0 ** rng.uniform(-30, 30, (1, cols))).astype(np.float32)
+    x[0, ::37] = 0.0
+    x[0, 5::41] = -0.0
+    y_ref, absref = oracle.matvec(m.W, wt, sf, rows, cols, x)
+    y = gpu_matvec(qmv, m, x)
+    check_product(y, y_ref, absref, TOL, "wide f32 magnitudes")
+    check_product(y, y_ref, absref, 1e-5, "wide f32 magnitudes, tight")
+
+
 def test_f32_activations_batch8_graph_replay_bit_identical(qmv):
     # float32 activations, 8 vectors: the split kernel and the tensor-memory product, eager
     # on a stream (which creates its buffers) and then replayed in a graph on it
