@@ -56,7 +56,11 @@ constexpr int kMaxProblems = 8;      // problems per grouped launch
 
 // XS: float32 activations given as two bfloat16 vectors hi + lo (x = hi + lo); each stage
 // then carries both and every block's MMAs run once with each, into the same sums.
-template <int WT, bool F16, int NW, int CH, bool XS = false>
+// RD: ring depth (stages per warp in shared memory).  2: the next stage is requested before the
+// current one is used; 1: only for launches where every warp has a single stage (half the
+// shared memory, so twice the CTAs per SM), whose one stage is requested before the
+// dependency wait.
+template <int WT, bool F16, int NW, int CH, bool XS = false, int RD = 2>
 struct Cfg {
   static constexpr int kCH = CH;                                   // chunks per stage
   static constexpr int XPARTS = XS ? 2 : 1;                        // activation vectors per stage
@@ -73,7 +77,7 @@ struct Cfg {
   static constexpr int DCHUNK = kBlocksPerStage * (F16 ? 2 : 4);  // scale bytes per row per chunk
   static constexpr int DROW = CH * DCHUNK;                        // scale bytes per row per stage
   static constexpr int D_STAGE = WROWS * DROW;                     // multiple of 512
-  static constexpr int S = 2;  // ring depth
+  static constexpr int S = RD;  // ring depth
   static constexpr int Q_WARP = S * Q_STAGE;
   static constexpr int D_WARP = S * D_STAGE;
   static constexpr int X_WARP = S * X_STAGE;
@@ -253,10 +257,10 @@ __device__ __forceinline__ void chunk_math(float (&acc)[Cfg<WT, F16, NW, CH>::MT
 // bytes of the hi and lo boxes) and each lane splits its values into hi = RN_bf16(x) and
 // lo = RN_bf16(x - hi) in registers (split_bf16_pair, the split kernel's rule), so float32
 // activations take one launch.
-template <int WT, bool F16, int NW, int CH, bool XS, bool GLU = false, bool XF = false>
+template <int WT, bool F16, int NW, int CH, bool XS, bool GLU = false, bool XF = false, int RD = 2>
 __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_constant__ Maps maps,
                                                                const __grid_constant__ Params p) {
-  using C = Cfg<WT, F16, NW, CH, XS>;
+  using C = Cfg<WT, F16, NW, CH, XS, RD>;
   constexpr int MT = C::MT;
   static_assert(!GLU || (MT == 2 && !XS), "the gated pair takes two 16-row MMA tiles per warp tile");
   static_assert(!XF || XS, "float32 activations are split into the hi and lo parts");
@@ -342,12 +346,14 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
     }
   };
 
-  // prologue: weight boxes of the first S-1 stages may be requested before the preceding
-  // kernel has finished; activations only after griddepcontrol.wait
+  // prologue: weight boxes of the first S-1 stages (of the one stage with a ring of one) may be
+  // requested before the preceding kernel has finished; activations only after
+  // griddepcontrol.wait
+  constexpr int kPre = C::S > 1 ? C::S - 1 : 1;
   int pre_c[C::S], pre_prob[C::S];
   bool pre_valid[C::S];
   int pre = 0;
-  while (pre < C::S - 1 && pc.item < p.nitems) {
+  while (pre < kPre && pc.item < p.nitems) {
     pre_c[pre] = pc.c0 + (pc.j << p.lgks);
     pre_prob[pre] = pc.prob;
     pre_valid[pre] = pc.tile < p.pr[pc.prob].ntiles;
@@ -392,7 +398,7 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
     const Problem& P = p.pr[cc.prob];
     const bool valid = cc.tile < P.ntiles;
     if (!failed) {
-      if (pc.item < p.nitems) {
+      if (C::S > 1 && pc.item < p.nitems) {
         issue(true);
         ps = (ps + 1 == C::S) ? 0 : ps + 1;
         advance(pc);
@@ -464,6 +470,12 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
         }
       }
       __syncwarp();
+      // a ring of one: the slot is free only now (every lane has read it)
+      if (C::S == 1 && !failed && pc.item < p.nitems) {
+        issue(true);
+        advance(pc);
+        ++issued;
+      }
     }
 
     if (cc.j == cc.n - 1) {  // end of an item: add the lanes' blocks and the column slices, store y
@@ -538,12 +550,14 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
 struct Plan {
   int ks = 1, nitems = 0, grid = 0, smem = 0;
   long long cost = -1;
+  long long longest = 0;  // stages of the longest warp's item
+  long long waves = 0;
 };
 
-template <int WT, bool F16, int NW, int CH, bool XS, bool GLU = false, bool XF = false>
+template <int WT, bool F16, int NW, int CH, bool XS, bool GLU = false, bool XF = false, int RD = 2>
 cudaError_t plan_typed(const MatrixRef* ms, int n, const DeviceInfo& dev, Plan* out) {
-  using C = Cfg<WT, F16, NW, CH, XS>;
-  auto kern = matvec_bdiag_kernel<WT, F16, NW, CH, XS, GLU, XF>;
+  using C = Cfg<WT, F16, NW, CH, XS, RD>;
+  auto kern = matvec_bdiag_kernel<WT, F16, NW, CH, XS, GLU, XF, RD>;
   // per device: the shared-memory attribute set and the occupancy known (0 = does not fit)
   static std::mutex mu;
   static bool ready[64] = {};
@@ -588,6 +602,8 @@ cudaError_t plan_typed(const MatrixRef* ms, int n, const DeviceInfo& dev, Plan* 
       best.ks = ks;
       best.nitems = (int)items;
       best.grid = (int)grid;
+      best.longest = longest;
+      best.waves = waves;
     }
   }
   best.smem = C::SMEM;
@@ -597,10 +613,10 @@ cudaError_t plan_typed(const MatrixRef* ms, int n, const DeviceInfo& dev, Plan* 
 
 // GLU: ms = {w1, w3} (same shape), one x (xs[0]); the pair is one problem whose warp tiles are
 // 16 rows of each; act and h as in Params.
-template <int WT, bool F16, int NW, int CH, bool XS, bool GLU = false, bool XF = false>
+template <int WT, bool F16, int NW, int CH, bool XS, bool GLU = false, bool XF = false, int RD = 2>
 cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* const* xs, float* const* ys, int n,
                          bool pdl, const DeviceInfo& dev, cudaStream_t stream, int act = -1, uint16_t* h = nullptr) {
-  using C = Cfg<WT, F16, NW, CH, XS>;
+  using C = Cfg<WT, F16, NW, CH, XS, RD>;
   constexpr int TROWS = GLU ? kRows : C::WROWS;  // rows of each matrix per warp tile
   if (GLU && (n != 2 || ms[0].rows != ms[1].rows || ms[0].cols != ms[1].cols || h == nullptr))
     return cudaErrorInvalidValue;
@@ -664,7 +680,7 @@ cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* cons
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, matvec_bdiag_kernel<WT, F16, NW, CH, XS, GLU, XF>, maps, p);
+  return cudaLaunchKernelEx(&cfg, matvec_bdiag_kernel<WT, F16, NW, CH, XS, GLU, XF, RD>, maps, p);
 }
 
 // Q4_0 launches of at least this many weight bytes take one-chunk stages.
@@ -703,6 +719,17 @@ cudaError_t launch_best(const MatrixRef* ms, const void* const* xs, float* const
   }
   err = plan_typed<WT, F16, 4, 2, XS, GLU, XF>(pm, pn, dev, &p4);
   if (err != cudaSuccess) return err;
+  if constexpr (!XS && !GLU) {
+    if (p4.cost >= 0 && p4.longest > 1) {
+      // 8-warp CTAs with a ring of one: every warp one stage, in one wave, where 4-warp CTAs
+      // give each warp two or more stages one after the other
+      Plan p1;
+      err = plan_typed<WT, F16, 8, 2, XS, GLU, XF, 1>(pm, pn, dev, &p1);
+      if (err != cudaSuccess) return err;
+      if (p1.cost >= 0 && p1.longest == 1 && p1.waves == 1 && p1.grid > dev.sm_count)
+        return launch_typed<WT, F16, 8, 2, XS, GLU, XF, 1>(p1, ms, xs, ys, n, pdl, dev, stream, act, h);
+    }
+  }
   if (p4.cost >= 0 && p4.grid > dev.sm_count)
     return launch_typed<WT, F16, 4, 2, XS, GLU, XF>(p4, ms, xs, ys, n, pdl, dev, stream, act, h);
   err = plan_typed<WT, F16, 8, 2, XS, GLU, XF>(pm, pn, dev, &p8);
