@@ -55,7 +55,13 @@ constexpr int kBox = 128;            // q box inner extent in bytes (the 128-byt
 constexpr int kMaxProblems = 8;      // problems per grouped launch
 
 // XS: float32 activations given as two bfloat16 vectors hi + lo (x = hi + lo); each stage
-// then carries both and every block's MMAs run once with each, into the same sums.
+// then carries both.  A warp first forms x = hi + lo of its stage, scales it by the power of
+// two 2^s that brings the stage's largest magnitude into [2^14, 2^15) and rounds it once to
+// IEEE half: when every value is zero or a normal half after that (the stage's nonzero
+// magnitudes lie within 2^28 of one another and are finite), each block runs one MMA as for a
+// bfloat16 vector and its sums are multiplied by 2^-s (exact) before the scale; the rounding
+// errs by at most 2^-11 of each term.  Otherwise every block's MMAs run once with hi and once
+// with lo, into the same sums (16 significant bits of x).
 // RD: ring depth (stages per warp in shared memory).  2: the next stage is requested before the
 // current one is used; 1: only for launches where every warp has a single stage (half the
 // shared memory, so twice the CTAs per SM), whose one stage is requested before the
@@ -144,10 +150,12 @@ __device__ __forceinline__ void cursor_load(Cursor& c, const Params& p, int tile
 // One chunk of a stage of one warp: the 16*MT x 256 weights at qs (q, swizzled) and ds
 // (the chunk's first scale in each DROW-byte row), x block j read at bsrc[j] + boff; adds each
 // row's scaled block sums of blocks 2t, 2t+1 to acc.
-template <int WT, bool F16, int NW, int CH, bool HALF, bool XS = false>
+// SC: the activations were scaled by a power of two for the MMAs; xinv (its inverse) takes
+// each block sum back before the block's scale is applied (exact).
+template <int WT, bool F16, int NW, int CH, bool HALF, bool XS = false, bool SC = false>
 __device__ __forceinline__ void chunk_math(float (&acc)[Cfg<WT, F16, NW, CH>::MT][2], uint32_t qs, const uint8_t* ds,
                                            const uint32_t (&bsrc)[kBlocksPerStage], uint32_t boff, int lrow,
-                                           int lsub, int sw, int g, int t) {
+                                           int lsub, int sw, int g, int t, float xinv = 1.0f) {
   using C = Cfg<WT, F16, NW, CH>;
   constexpr int MT = C::MT;
   float da[MT][4];  // block sums (both halves of a block), column j = block j
@@ -246,17 +254,21 @@ __device__ __forceinline__ void chunk_math(float (&acc)[Cfg<WT, F16, NW, CH>::MT
       }
       // XS: the lo vector's sums, scaled back (2^-9 is exact) in HALF stages
       constexpr float kLoBack = HALF ? 0x1p-9f : 1.0f;
-      const float s0 = XS ? da[mt][2 * h] + dl[mt][2 * h] * kLoBack : da[mt][2 * h];
-      const float s1 = XS ? da[mt][2 * h + 1] + dl[mt][2 * h + 1] * kLoBack : da[mt][2 * h + 1];
+      float s0 = XS ? da[mt][2 * h] + dl[mt][2 * h] * kLoBack : da[mt][2 * h];
+      float s1 = XS ? da[mt][2 * h + 1] + dl[mt][2 * h + 1] * kLoBack : da[mt][2 * h + 1];
+      if (SC) {
+        s0 *= xinv;
+        s1 *= xinv;
+      }
       acc[mt][h] = fmaf(d1, s1, fmaf(d0, s0, acc[mt][h]));
     }
   }
 }
 
 // XF (with XS): the activations arrive as float32 (one box of CH x 256 values per stage, the
-// bytes of the hi and lo boxes) and each lane splits its values into hi = RN_bf16(x) and
-// lo = RN_bf16(x - hi) in registers (split_bf16_pair, the split kernel's rule), so float32
-// activations take one launch.
+// bytes of the hi and lo boxes); a stage that rounds to half as above takes them directly, the
+// others are split by each lane into hi = RN_bf16(x) and lo = RN_bf16(x - hi) in registers
+// (split_bf16_pair, the split kernel's rule), so float32 activations take one launch.
 template <int WT, bool F16, int NW, int CH, bool XS, bool GLU = false, bool XF = false, int RD = 2>
 __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_constant__ Maps maps,
                                                                const __grid_constant__ Params p) {
@@ -412,6 +424,66 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
         if (valid) {
           const uint32_t qs = smem_u32(qring + cs * C::Q_STAGE);
           const uint8_t* ds = dring + cs * C::D_STAGE;
+          bool rounded = false;
+          if constexpr (XS) {
+            // activations given as hi + lo (or float32): scaled by a power of two 2^s (from the
+            // stage's largest magnitude, so that it lies in [2^14, 2^15)) and rounded once to
+            // IEEE half (11 significant bits: at most 2^-11 relative error per term, under half
+            // the product's tolerance), one MMA per block as for bfloat16 activations, the block
+            // sums taken back by 2^-s; where some value of the stage would round to a subnormal
+            // half (a range over 2^28 within the stage) or is not finite, the exact two-part path
+            float v[C::kCH][8];
+            float amax = 0.f;
+#pragma unroll
+            for (int h = 0; h < C::kCH; ++h) {
+              if (XF) {
+                const uint8_t* xf = xring + cs * C::X_STAGE + h * (kTK * 4) + g * 128 + t * 16;
+                const float4 fa = *reinterpret_cast<const float4*>(xf);
+                const float4 fb = *reinterpret_cast<const float4*>(xf + 64);
+                v[h][0] = fa.x, v[h][1] = fa.y, v[h][2] = fa.z, v[h][3] = fa.w;
+                v[h][4] = fb.x, v[h][5] = fb.y, v[h][6] = fb.z, v[h][7] = fb.w;
+              } else {
+                const uint8_t* xh = xring + cs * C::X_STAGE + h * (kTK * 2) + g * 64 + t * 8;
+                const uint8_t* xl = xh + C::kCH * (kTK * 2);
+                const uint2 ha = *reinterpret_cast<const uint2*>(xh), hb = *reinterpret_cast<const uint2*>(xh + 32);
+                const uint2 la = *reinterpret_cast<const uint2*>(xl), lb = *reinterpret_cast<const uint2*>(xl + 32);
+                const uint32_t hw[4] = {ha.x, ha.y, hb.x, hb.y}, lw[4] = {la.x, la.y, lb.x, lb.y};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  // exact for a split x (lo under half an ulp of hi); one float32 rounding otherwise
+                  v[h][2 * i] = __uint_as_float(hw[i] << 16) + __uint_as_float(lw[i] << 16);
+                  v[h][2 * i + 1] = __uint_as_float(hw[i] & 0xFFFF0000u) + __uint_as_float(lw[i] & 0xFFFF0000u);
+                }
+              }
+#pragma unroll
+              for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(v[h][k]));  // a NaN is not taken
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            // 2^s with amax * 2^s in [2^14, 2^15): s = 141 - (biased exponent of amax); 1 for a stage
+            // of zeros
+            const int eb = (int)((__float_as_uint(amax) >> 23) & 0xFFu);
+            const bool scalable = amax == 0.f || (eb >= 15 && eb <= 254);
+            const int se = amax == 0.f ? 127 : 268 - eb;  // biased exponent of 2^s
+            const float xs = __uint_as_float((uint32_t)(scalable ? se : 127) << 23);
+            const float xinv = __uint_as_float((uint32_t)(scalable ? 254 - se : 127) << 23);
+            bool fits = scalable;
+            uint32_t rx[C::kCH][4];
+#pragma unroll
+            for (int h = 0; h < C::kCH; ++h)
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                rx[h][i] = f32x2_to_f16x2_normal(v[h][2 * i], v[h][2 * i + 1], xs, fits);
+            if (__all_sync(0xffffffffu, fits)) {
+              rounded = true;
+#pragma unroll
+              for (int h = 0; h < C::kCH; ++h) sts_u32x4(slot + h * 512, rx[h][0], rx[h][1], rx[h][2], rx[h][3]);
+#pragma unroll
+              for (int h = 0; h < C::kCH; ++h)
+                chunk_math<WT, F16, NW, CH, true, false, true>(acc, qs + h * C::Q_CHUNK, ds + h * C::DCHUNK, bsrc,
+                                                               h * 512u, lrow, lsub, sw, g, t, xinv);
+            }
+          }
           // this lane's activations of each chunk h: block g, elements 4t..4t+3 and
           // 16+4t..16+4t+3; its slot for chunk h is 512 bytes after the one for chunk h-1
           // (XS: the same of the lo vector, whose slots follow the hi ones: chunk h at CH + h)
@@ -419,6 +491,7 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
           uint2 xa[NX], xb[NX];
           uint32_t hx[NX][4];
           bool exact = true;
+          if (!rounded) {
           if (XF) {
             // float32 activations: elements 4t..4t+3 and 16+4t..16+4t+3 of block g of each chunk,
             // split into the bf16 hi (chunk h) and lo (chunk CH + h) parts
@@ -467,6 +540,7 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
               chunk_math<WT, F16, NW, CH, false, XS>(acc, qs + h * C::Q_CHUNK, ds + h * C::DCHUNK, bsrc, h * 512u,
                                                      lrow, lsub, sw, g, t);
           }
+          }  // !rounded
         }
       }
       __syncwarp();

@@ -274,9 +274,9 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
       if (launch_matvec_bdiag(fast, fx, fy, nf, pdl, dev, stream) != cudaSuccess) return QMV_E_CUDA;
     } else if (!xb && !glu && nb == 1 && nweights >= kF32SplitMinWeights &&
                nweights * (wtype == QMV_Q8_0 ? 2 : 1) / 2 < kF32InKernelMaxBytes) {
-      // one float32 vector: the block-diagonal kernel splits it into bf16 hi + lo parts in its
-      // activation stage and runs every block's MMAs once with each (one launch; below a few
-      // hundred KB of weights the one mma.sync launch measured quicker)
+      // one float32 vector: the block-diagonal kernel reads it as float32 and rounds each stage
+      // to half after a power-of-two scale, or splits it into bf16 hi + lo parts (one launch;
+      // below a few hundred KB of weights the one mma.sync launch measured quicker)
       if (launch_matvec_bdiag_f32in(fast, fx, fy, nf, pdl, dev, stream) != cudaSuccess) return QMV_E_CUDA;
     } else if (!xb && nb == 1 && (glu || nweights >= kF32SplitMinWeights) &&
                launch_matvec_bdiag_f32(fast, fx, fy, nf, pdl, dev, stream, act, batch) == cudaSuccess) {

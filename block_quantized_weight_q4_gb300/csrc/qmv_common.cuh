@@ -246,6 +246,21 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t p, bool& exact) {
   return h;
 }
 
+// Two float32 values times a power of two `scale` rounded to an IEEE half pair (to nearest
+// even); `fits` is cleared unless each value is zero or its result is a normal half (magnitude
+// 2^-14 .. 65504), where the rounding's relative error is at most 2^-11.  A product that left
+// the float32 normal range (so was not exact) gives a subnormal or zero half and clears `fits`.
+__device__ __forceinline__ uint32_t f32x2_to_f16x2_normal(float lo, float hi, float scale, bool& fits) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(hi * scale), "f"(lo * scale));
+  const float blo = fabsf(__half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xFFFFu))));
+  const float bhi = fabsf(__half2float(__ushort_as_half(static_cast<unsigned short>(h >> 16))));
+  const bool okl = (blo >= 0x1p-14f && blo <= 65504.0f) || lo == 0.0f;
+  const bool okh = (bhi >= 0x1p-14f && bhi <= 65504.0f) || hi == 0.0f;
+  fits = fits & okl & okh;
+  return h;
+}
+
 // The same for a bfloat16 pair times a power of two `scale` (exact in float32).
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t p, float scale, bool& exact) {
   const float lo = __uint_as_float(p << 16) * scale;

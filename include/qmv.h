@@ -67,10 +67,11 @@ extern "C" {
 #define QMV_X_SILU_GLU_F32 2
 #define QMV_X_GELU_GLU_F32 3
 /* One activation vector given as a bfloat16 pair (batch must be 1): x holds cols bfloat16 hi
- * parts followed by cols bfloat16 lo parts, the activations being hi + lo; the product runs
- * every block's dot products once with each part (16 significant bits of the activations
- * kept).  This is the layout qmv_matvec_glu writes.  cols % 256 == 0 (QMV_E_SHAPE otherwise),
- * batch other than 0 or 1 gives QMV_E_ARG. */
+ * parts followed by cols bfloat16 lo parts, the activations being hi + lo (formed in float32);
+ * the block-diagonal kernel takes them as it takes one float32 vector (each stage rounded once
+ * to half after a power-of-two scale, or both parts where that would not hold every value as a
+ * normal half).  This is the layout qmv_matvec_glu writes.  cols % 256 == 0 (QMV_E_SHAPE
+ * otherwise), batch other than 0 or 1 gives QMV_E_ARG. */
 #define QMV_X_BF16_PAIR 4
 
 /* act of qmv_matvec_glu (the .mlb header's act field): */
@@ -127,14 +128,20 @@ int qmv_matrix_wtype(int file_wtype, uint32_t q8_mask, int class_bit, int shared
  * vectors over 64M weights or more, take the tensor-memory kernel (levels stored to tensor
  * memory, tcgen05 MMA); a pass of one bf16 vector takes the block-diagonal kernel (one MMA
  * column per weight block; IEEE-half operands for the 256-column stages whose activations
- * are exact halves, bfloat16 otherwise).  float32 activations are first split into
- * bfloat16 pairs hi + lo (hi = RN_bf16(x), lo = RN_bf16(x - hi): 16 bits of x kept) in a
- * 2 MiB buffer of the calling stream (allocated on its first such call; without it, and
- * while the stream is captured before it exists, the mma.sync kernel takes them): passes
- * of 2..8 vectors then take the tensor-memory kernel (hi and lo as its 16 MMA columns) and
- * one vector the block-diagonal kernel (each block's MMAs once with hi, once with lo; launches
- * under 256K weights take the mma.sync kernel, which splits x the same way, in one launch).  The
- * rest take the mma.sync kernel.  The tensor-memory kernel splits tiles between CTAs;
+ * are exact halves, bfloat16 otherwise).  float32 activations, 2..8 vectors, are first split
+ * into bfloat16 pairs hi + lo (hi = RN_bf16(x), lo = RN_bf16(x - hi): 16 bits of x kept) in
+ * a 2 MiB buffer of the calling stream (allocated on its first such call; without it, and
+ * while the stream is captured before it exists, the mma.sync kernel takes them) and take the
+ * tensor-memory kernel (hi and lo as its 16 MMA columns).  One float32 vector takes the
+ * block-diagonal kernel (launches under 256K weights the mma.sync kernel, which splits x as
+ * above in one launch): under 16 MB of weights it reads x as float32, larger launches after
+ * the split into the buffer.  There each warp's stage of 256 or 512 columns is scaled by the
+ * power of two that brings its largest magnitude into [2^14, 2^15) and rounded once to IEEE
+ * half (at most 2^-11 relative error per term, one MMA per block, the sums scaled back
+ * exactly); a stage holding a nonzero value that would round to a subnormal half (nonzero
+ * magnitudes more than 2^28 apart) or a non-finite one runs each block's MMAs with hi and
+ * with lo instead.  The same holds for QMV_X_BF16_PAIR and for gated activations at batch 1.
+ * The rest take the mma.sync kernel.  The tensor-memory kernel splits tiles between CTAs;
  * their parts meet in a workspace of the calling stream (4 MiB of device memory, allocated
  * on the stream's first such call and kept; while a stream without one is being captured,
  * the call takes the mma.sync kernel instead).  Results do not depend on timing.

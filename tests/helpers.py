@@ -2,6 +2,12 @@
 import numpy as np
 
 
+# Batch-1 products on float32, bfloat16-pair or gated activations round each activation once to
+# IEEE half after a power-of-two scale of its stage: at most 2^-11 relative error per term, plus
+# the float32 sums (a few parts in 2^20 of sum |w x| at the sizes of the tests)
+HALF_TOL = 2.0 ** -11 + 2.0 ** -16
+
+
 def dev_u8(W):
     import torch
     return torch.from_numpy(np.ascontiguousarray(W)).cuda()

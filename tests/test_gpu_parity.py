@@ -9,7 +9,7 @@ import pytest
 
 import oracle
 from block_quantized_weight_q4_gb300 import inputs
-from helpers import assert_bits_equal, check_product, dev_u8, dev_x
+from helpers import HALF_TOL, assert_bits_equal, check_product, dev_u8, dev_x
 
 pytestmark = pytest.mark.gpu
 
@@ -335,7 +335,8 @@ def test_f32_one_vector_split_in_the_product_exact(qmv, wt, sf, rows, cols):
 @pytest.mark.parametrize("wt,sf", [(2, 1), (1, 0)])
 def test_f32_one_vector_wide_magnitudes(qmv, wt, sf):
     # float32 activations over sixty decades (1e-30 .. 1e30, zeros, negative zeros), split in the
-    # product: within the tolerance of the oracle, tight
+    # product: every stage spans far more than 2^28, so none is rounded to half and all keep
+    # hi + lo: within the tolerance of the oracle, tight
     rows, cols = 512, 1024
     rng = np.random.default_rng(95 + wt)
     m = inputs.make_matrix(wt, sf, rows, cols, seed=96)
@@ -373,3 +374,45 @@ def test_f32_activations_batch8_graph_replay_bit_identical(qmv):
         g.replay()
         torch.cuda.synchronize()
         assert_bits_equal(y.cpu().numpy(), first, "f32 x graph replay")
+
+
+@pytest.mark.parametrize("route", ["f32", "pair"])
+def test_one_vector_stages_rounded_to_half_and_exact(qmv, route):
+    # one vector x = 1 + 2^-12 everywhere (Q8_0 levels 1..7 and scales 2^-2..1: positive weights,
+    # so every error has one sign), except
+    # that columns 1024..1535 also hold 2^-40 at four places.  Stages of 256 or 512 columns with
+    # only 1 + 2^-12 are scaled into [2^14, 2^15) and rounded to half: 1 + 2^-12 becomes 1
+    # exactly.  The stages over columns 1024..1535 span 2^40 > 2^28, so they keep hi + lo and
+    # give x exactly.  The product must then equal the oracle's on x' (x with 1 outside columns
+    # 1024..1535) up to float32 sums, and differ from the oracle's on x by about 2^-12 of y
+    # (within HALF_TOL); the pair route (hi = 1, lo = 2^-12) and the float32 route agree
+    import torch
+    rows, cols = 256, 4096
+    rng = np.random.default_rng(97)
+    q = rng.integers(1, 8, size=rows * cols).astype(np.int8).view(np.uint8)
+    codes = inputs.pow2_scales(rng, rows * cols // 32, 1, -2, 0)
+    W = inputs.assemble(1, 1, rows, cols, q, codes)
+    x = np.full((1, cols), 1.0 + 2.0 ** -12, np.float32)
+    x[0, [1024 + 17, 1024 + 300, 1024 + 301, 1024 + 511]] = 2.0 ** -40
+    keep = np.zeros(cols, bool)
+    keep[1024:1536] = True
+    x_rounded = np.where(keep, x[0], np.float32(1.0))[None, :]
+    y_ref, absref = oracle.matvec(W, 1, 1, rows, cols, x)
+    y_exp, _ = oracle.matvec(W, 1, 1, rows, cols, x_rounded)
+    Wd = dev_u8(W)
+    y = torch.empty((1, rows), device="cuda")
+    if route == "f32":
+        qmv.matvec_grouped(1, 1, [(rows, cols, Wd, torch.from_numpy(x).cuda(), y)])
+    else:
+        hi = inputs.bf16_codes(x[0])
+        lo = inputs.bf16_codes(x[0] - (hi.astype(np.uint32) << 16).view(np.float32))
+        assert np.array_equal((hi.astype(np.uint32) << 16).view(np.float32)
+                              + (lo.astype(np.uint32) << 16).view(np.float32), x[0])
+        pair = torch.from_numpy(np.stack([hi, lo]).view(np.int16)).cuda().view(torch.bfloat16)
+        qmv.matvec_grouped(1, 1, [(rows, cols, Wd, pair, y)], pair=True)
+    torch.cuda.synchronize()
+    yg = y.cpu().numpy()
+    check_product(yg, y_ref, absref, HALF_TOL, f"{route}: against the oracle on x")
+    check_product(yg, y_exp, absref, 1e-6, f"{route}: rounded stages 1, exact stages x")
+    rel = (y_ref[0] - yg[0].astype(np.float64)) / absref[0]
+    assert np.all(rel > 2.0 ** -12 * 0.7) and np.all(rel < 2.0 ** -12), f"{route}: {rel.min()} .. {rel.max()}"
