@@ -24,10 +24,10 @@ void workspace_carve(void* base, size_t bytes, int n, Workspace* ws) {
   ws->max_partial_floats = bytes > cb ? (bytes - cb) / sizeof(float) : 0;
 }
 
-// a stream's workspace: counters for up to 1024 CTAs, then the parts (2 per CTA of 256
-// rows x 8 vectors); the kernel sizes its grid to fit
+// a stream's workspace: counters for up to 1024 CTAs, then the parts (2 per CTA of 128
+// rows x up to 16 vectors); the kernel sizes its grid to fit
 constexpr int kStreamCounters = 1024;
-constexpr size_t kStreamWorkspaceBytes = (size_t)4 << 20;
+constexpr size_t kStreamWorkspaceBytes = (size_t)8 << 20;
 
 // a stream's prefill workspace: counters for 4096 tiles, then the parts of split tiles
 // (ksplit x 128 rows x up to 128 vectors per tile; the launch picks ksplit to fit)

@@ -1,4 +1,4 @@
-// decode_tc.cuh -- the decode product (1..8 bfloat16 activation vectors per pass) on the
+// decode_tc.cuh -- the decode product (1..16 bfloat16 activation vectors per pass) on the
 // 5th-generation tensor core, with the quantized weights unpacked into tensor memory.
 //
 // What is computed (Krafla ".mlb model format v1", "Q8_0", "Q4_0", "Body"):
@@ -49,7 +49,8 @@ constexpr int kTileRows = kM;           // rows per unit
 constexpr int kKS = 256;                // columns per unit
 constexpr int kBlk = kKS / 32;          // blocks per unit
 constexpr int kN = 16;                  // MMA N: activation vectors, zero-padded
-constexpr int kMaxBatch = 8;
+constexpr int kMaxVec = kN;             // vectors per pass (bf16 activations)
+constexpr int kMaxBatch = 8;            // vectors per pass given as hi + lo pairs (16 MMA columns)
 constexpr int kMaxProblems = 8;
 constexpr int kIssuers = 2;             // MMA-issuing warps, one per half unit
 constexpr int kRowWarps = 4;
@@ -60,7 +61,6 @@ constexpr int kTmemCols = 256;          // A, then block sums
 constexpr int kSumCol = 128;            // first block-sum column
 constexpr int kXBox = 64;               // activation box width (one 128-byte swizzle span of bf16)
 constexpr int kXBoxBytes = kN * 128;
-constexpr int kPart = kMaxBatch * kTileRows;  // floats of one part of a split tile
 
 template <int WT, bool F16>
 struct Cfg {
@@ -102,7 +102,7 @@ struct Params {
   int grid;
   long long units;
   int* status;
-  float* partials;              // [2 * grid][kMaxBatch][kTileRows] parts of split tiles
+  float* partials;              // [2 * grid][NV][kTileRows] parts of split tiles (NV: the kernel's)
   unsigned* counters;           // [grid] arrivals, zero between launches
   Problem pr[kMaxProblems];
 };
@@ -195,7 +195,7 @@ __device__ __forceinline__ void q8_block_levels(const uint32_t* w, uint32_t (&ou
 // columns (block k at column 16k).
 template <int NV>
 __device__ __forceinline__ void add_block_sums(uint32_t tsum, int k0, const float (&dk)[kBlk], float (&acc)[NV]) {
-  constexpr int G = NV <= 4 ? kHalfBlk : 2;  // blocks per tensor-memory read batch
+  constexpr int G = NV <= 4 ? kHalfBlk : NV <= 8 ? 2 : 1;  // blocks per tensor-memory read batch
 #pragma unroll
   for (int kb = 0; kb < kHalfBlk; kb += G) {
     uint32_t v[G][NV];
@@ -205,7 +205,8 @@ __device__ __forceinline__ void add_block_sums(uint32_t tsum, int k0, const floa
       if constexpr (NV == 1) tmem_ld1(a, v[k]);
       else if constexpr (NV == 2) tmem_ld2(a, v[k]);
       else if constexpr (NV == 4) tmem_ld4(a, v[k]);
-      else tmem_ld8(a, v[k]);
+      else if constexpr (NV == 8) tmem_ld8(a, v[k]);
+      else tmem_ld16(a, v[k]);
     }
     tmem_ld_wait();
 #pragma unroll
@@ -252,10 +253,11 @@ __device__ __forceinline__ void add_block_sums_split(uint32_t tsum, int k0, cons
 }
 
 template <int WT, bool F16, int NV>
-__global__ void __maxnreg__(120) decode_tc_kernel(const __grid_constant__ Maps maps,
+__global__ void __maxnreg__(NV > 8 ? 144 : 120) decode_tc_kernel(const __grid_constant__ Maps maps,
                                                                 const __grid_constant__ Params p) {
   using C = Cfg<WT, F16>;
   constexpr int S = C::S;
+  constexpr int kPart = NV * kTileRows;  // floats of one part of a split tile
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);  // 1024-aligned: swizzle atoms
@@ -444,14 +446,15 @@ __global__ void __maxnreg__(120) decode_tc_kernel(const __grid_constant__ Maps m
       const bool ok = twait(flush_done, (uint32_t)(flushes & 1), failed, p.status);
       ++flushes;
       if (!ok || !*last_flag) return;
-      // the last part of the tile: add all parts in CTA order, four in flight at a time
+      // the last part of the tile: add all parts in CTA order, QF in flight at a time
       float sum[NV];
 #pragma unroll
       for (int n = 0; n < NV; ++n) sum[n] = 0.f;
-      for (int c = cfirst; c <= clast; c += 4) {
-        float v[4][NV];
+      constexpr int QF = NV <= 8 ? 4 : WT == QMV_Q4_0 ? 2 : 1;  // parts in flight (registers: QF x NV)
+      for (int c = cfirst; c <= clast; c += QF) {
+        float v[QF][NV];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < QF; ++q) {
           const int cc = c + q;
           const int slot = 2 * cc + (t0 * p.grid <= (long long)cc * p.units ? 0 : 1);
           const float* part = p.partials + (size_t)slot * kPart;
@@ -459,7 +462,7 @@ __global__ void __maxnreg__(120) decode_tc_kernel(const __grid_constant__ Maps m
           for (int n = 0; n < NV; ++n) v[q][n] = cc <= clast ? __ldcg(part + n * kTileRows + rt) : 0.f;
         }
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int q = 0; q < QF; ++q)
 #pragma unroll
           for (int n = 0; n < NV; ++n) sum[n] += v[q][n];
       }
@@ -512,11 +515,13 @@ __global__ void __maxnreg__(120) decode_tc_kernel(const __grid_constant__ Maps m
     auto take_half = [&](int j, int h, const float (&dk)[kBlk]) -> bool {
       if (!twait(&dfull[h], (uint32_t)(j & 1), failed, p.status)) return false;
       tc_fence_after();
-      if (p.xsplit) {
-        add_block_sums_split<NV>(tsum, h * kHalfBlk, dk, acc);
-      } else {
-        add_block_sums<NV>(tsum, h * kHalfBlk, dk, acc);
+      if constexpr (NV <= kMaxBatch) {
+        if (p.xsplit) {
+          add_block_sums_split<NV>(tsum, h * kHalfBlk, dk, acc);
+          return true;
+        }
       }
+      add_block_sums<NV>(tsum, h * kHalfBlk, dk, acc);
       return true;
     };
 
@@ -576,8 +581,10 @@ cudaError_t launch_typed(const MatrixRef* ms, const void* const* xs, float* cons
   using C = Cfg<WT, F16>;
   auto kern = decode_tc_kernel<WT, F16, NV>;
   static bool ready[64] = {};
-  if (dev.device < 0 || dev.device >= 64 || n < 1 || n > kMaxProblems || batch < 1 || batch > NV)
+  if (dev.device < 0 || dev.device >= 64 || n < 1 || n > kMaxProblems || batch < 1 || batch > NV ||
+      (xsplit && batch > kMaxBatch))
     return cudaErrorInvalidValue;
+  constexpr int kPart = NV * kTileRows;
   if (!ready[dev.device]) {
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (err != cudaSuccess) return err;
@@ -602,7 +609,7 @@ cudaError_t launch_typed(const MatrixRef* ms, const void* const* xs, float* cons
     p.pr[i].unit0 = units;
     units += (long long)p.pr[i].ntiles * p.pr[i].nchunks;
   }
-  // two CTAs per SM: shared memory (<= 113 KB each), registers (120 x 224 each) and tensor
+  // two CTAs per SM: shared memory (<= 113 KB each), registers (<= 144 x 224 each) and tensor
   // memory (256 columns each) hold two.  (The occupancy query reports one CTA per SM for any
   // kernel that allocates tensor memory, so it is not used here.)  Within the workspace's
   // counters and parts, and no more CTAs than units.
@@ -654,7 +661,8 @@ cudaError_t launch_wtype(const MatrixRef* ms, const void* const* xs, float* cons
   if (batch <= 1) return launch_typed<WT, F16, 1>(ms, xs, ys, n, batch, xsplit, pdl, dev, ws, stream);
   if (batch <= 2) return launch_typed<WT, F16, 2>(ms, xs, ys, n, batch, xsplit, pdl, dev, ws, stream);
   if (batch <= 4) return launch_typed<WT, F16, 4>(ms, xs, ys, n, batch, xsplit, pdl, dev, ws, stream);
-  return launch_typed<WT, F16, 8>(ms, xs, ys, n, batch, xsplit, pdl, dev, ws, stream);
+  if (batch <= 8) return launch_typed<WT, F16, 8>(ms, xs, ys, n, batch, xsplit, pdl, dev, ws, stream);
+  return launch_typed<WT, F16, 16>(ms, xs, ys, n, batch, xsplit, pdl, dev, ws, stream);
 }
 
 cudaError_t launch_q4(const MatrixRef*, const void* const*, float* const*, int, int, bool, bool, const DeviceInfo&,

@@ -17,9 +17,12 @@ __device__ int g_device_status = 0;
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kPrefillMinBatch = 16;  // from here on the tensor-memory kernel takes bf16 batches
-constexpr int kTcMinBatch = 4;        // decode passes of this many bf16 vectors go to decode_tc
+constexpr int kPrefillMinBatch = 17;  // from here on the prefill kernel takes bf16 batches
+constexpr int kTcMinBatch = 4;        // decode passes of this many bf16 vectors may go to decode_tc:
+constexpr long long kTcMinBytes = 40LL << 20;      // launches of this many weight bytes (below, mma.sync
+                                                   // measured faster at 4..8 vectors)
 constexpr long long kTcMinQ8Weights = 64LL << 20;  // and Q8_0 passes of 2-3 vectors over this many weights
+constexpr long long kTcWideMinBytes = 16LL << 20;  // passes of 9..16 vectors in one decode_tc launch
 constexpr long long kF32SplitMinWeights = 256LL << 10;  // one f32 vector: split hi/lo from this many weights
 // one f32 vector: split in the product's own activation stage (one launch) below this many
 // weight bytes; above it the split kernel runs once per column and the product reads its parts
@@ -204,11 +207,19 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
   const bool xb = x_dtype == QMV_X_BF16;
   const size_t xsz = xb ? 2 : 4;
   const bool pdl = (flags & QMV_FLAG_OVERLAP) != 0;
-  // 16 or more bf16 vectors: the tensor-memory kernel, per problem, in passes of up to 128
+  auto weight_bytes = [&](const MatrixRef& m) {
+    return m.rows * m.cols / 32 * ((wtype == QMV_Q4_0 ? 16 : 32) + (scale_dtype == QMV_SCALE_F16 ? 2 : 4));
+  };
+  long long group_bytes = 0;
+  for (int i = 0; i < n; ++i) group_bytes += weight_bytes(ms[i]);
+  // 17 or more bf16 vectors (16 in groups under 16 MB of weights, where it measured faster
+  // than one 16-vector pass of the tensor-memory decode kernel): the prefill kernel, per
+  // problem, in passes of up to 128
+  const bool prefill_batch = batch >= kPrefillMinBatch || (batch == 16 && group_bytes < kTcWideMinBytes);
   bool use_prefill[QMV_MAX_GROUP];
   bool any_decode = false;
   for (int i = 0; i < n; ++i) {
-    use_prefill[i] = batch >= kPrefillMinBatch && prefill_supported(ms[i], xb);
+    use_prefill[i] = prefill_batch && prefill_supported(ms[i], xb);
     if (use_prefill[i]) {
       // split tiles between CTAs when the stream has its prefill workspace (created on the
       // stream's first prefill call, never while it is captured)
@@ -229,12 +240,25 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
   }
   if (!any_decode) return QMV_OK;
   // problems the tensor-core kernel takes go in one launch per pass of 8 vectors; the rest
-  // run the general kernel one by one
+  // run the general kernel one by one.  bf16 batches of 9 or more whose problems the
+  // tensor-memory kernel takes all, 16 MB of weights or more, on a stream with its workspace:
+  // passes of 16 (that kernel's 16 MMA columns then all hold vectors)
+  long long decode_bytes = 0;
+  for (int i = 0; i < n; ++i)
+    if (!use_prefill[i]) decode_bytes += weight_bytes(ms[i]);
+  bool wide = xb && batch > 8 && decode_bytes >= kTcWideMinBytes;
+  for (int i = 0; i < n && wide; ++i)
+    wide = use_prefill[i] || (matvec_mma_supported(ms[i]) && decode_tc_supported(ms[i]));
+  if (wide) {
+    Workspace probe;
+    wide = stream_workspace(dev, stream, &probe) == cudaSuccess;
+  }
+  const int pass = wide ? 16 : 8;
   MatrixRef fast[QMV_MAX_GROUP];
   const void* fx[QMV_MAX_GROUP];
   float* fy[QMV_MAX_GROUP];
-  for (int b0 = 0; b0 < batch; b0 += 8) {
-    const int nb = (batch - b0) < 8 ? (batch - b0) : 8;
+  for (int b0 = 0; b0 < batch; b0 += pass) {
+    const int nb = (batch - b0) < pass ? (batch - b0) : pass;
     int nf = 0;
     for (int i = 0; i < n; ++i) {
       if (use_prefill[i]) continue;
@@ -250,14 +274,18 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
       }
     }
     if (nf == 0) continue;
-    // bf16 activations: the tensor-memory kernel for passes of 4 or more vectors, and for
-    // Q8_0 passes of 2 or 3 vectors over 64M weights or more (where it measured faster),
-    // when this stream has its workspace (created on the stream's first such call, never
-    // while it is captured); one bf16 vector: the block-diagonal kernel; else the mma.sync
-    // kernel
-    long long nweights = 0;
-    for (int i = 0; i < nf; ++i) nweights += fast[i].rows * fast[i].cols;
-    bool tc = xb && (nb >= kTcMinBatch || (wtype == QMV_Q8_0 && nb > 1 && nweights >= kTcMinQ8Weights));
+    // bf16 activations: the tensor-memory kernel for passes of 9..16 vectors, passes of 4..8
+    // over 40 MB of weights or more, and Q8_0 passes of 2 or 3 vectors over 64M weights or more
+    // (where it measured faster than the mma.sync kernel), when this stream has its workspace
+    // (created on the stream's first such call, never while it is captured); one bf16 vector:
+    // the block-diagonal kernel; else the mma.sync kernel
+    long long nweights = 0, nbytes = 0;
+    for (int i = 0; i < nf; ++i) {
+      nweights += fast[i].rows * fast[i].cols;
+      nbytes += weight_bytes(fast[i]);
+    }
+    bool tc = xb && (nb > 8 || (nb >= kTcMinBatch && nbytes >= kTcMinBytes) ||
+                     (wtype == QMV_Q8_0 && nb > 1 && nweights >= kTcMinQ8Weights));
     for (int i = 0; i < nf && tc; ++i) tc = decode_tc_supported(fast[i]);
     // float32 activations, 2..8 vectors: the tensor-memory kernel on the bf16 pairs hi + lo
     // (its 16 MMA columns hold both parts of up to 8 vectors)

@@ -122,11 +122,14 @@ int qmv_matrix_wtype(int file_wtype, uint32_t q8_mask, int class_bit, int shared
  *   y     : device, batch x rows float32, row-major; fully overwritten.
  *   batch : number of activation vectors, >= 0; 0 launches nothing and returns QMV_OK.
  * Each block contributes d * sum_j level_j * x_j; sums are kept in float32.  Batches
- * below 16 (and float32 activations) run in passes of up to 8 vectors through the decode
- * kernels (weights decoded to exact levels, one tensor-core dot product per block, f32
- * scale and accumulate): passes of 4 or more bf16 vectors, and Q8_0 passes of 2 or 3 bf16
- * vectors over 64M weights or more, take the tensor-memory kernel (levels stored to tensor
- * memory, tcgen05 MMA); a pass of one bf16 vector takes the block-diagonal kernel (one MMA
+ * below 16 (and 16 in groups of 16 MB of weights or more, and float32 activations) run
+ * through the decode kernels (weights decoded to exact levels, one tensor-core dot product
+ * per block, f32 scale and accumulate) in passes of up to 8 vectors, or of up to 16 for bf16
+ * batches of 9..16 in groups of 16 MB of weights or more: those 16-vector passes, bf16 passes
+ * of 4..8 vectors over 40 MB of weights or more, and Q8_0 passes of 2 or 3 bf16 vectors over
+ * 64M weights or more take the tensor-memory kernel (levels stored to tensor memory, tcgen05
+ * MMA; below those sizes the mma.sync kernel measured faster and takes the other passes of
+ * 2..8 vectors); a pass of one bf16 vector takes the block-diagonal kernel (one MMA
  * column per weight block; IEEE-half operands for the 256-column stages whose activations
  * are exact halves, bfloat16 otherwise).  float32 activations, 2..8 vectors, are first split
  * into bfloat16 pairs hi + lo (hi = RN_bf16(x), lo = RN_bf16(x - hi): 16 bits of x kept) in
@@ -142,11 +145,12 @@ int qmv_matrix_wtype(int file_wtype, uint32_t q8_mask, int class_bit, int shared
  * magnitudes more than 2^28 apart) or a non-finite one runs each block's MMAs with hi and
  * with lo instead.  The same holds for QMV_X_BF16_PAIR and for gated activations at batch 1.
  * The rest take the mma.sync kernel.  The tensor-memory kernel splits tiles between CTAs;
- * their parts meet in a workspace of the calling stream (4 MiB of device memory, allocated
+ * their parts meet in a workspace of the calling stream (8 MiB of device memory, allocated
  * on the stream's first such call and kept; while a stream without one is being captured,
  * the call takes the mma.sync kernel instead).  Results do not depend on timing.
- * bfloat16 batches of 16 and more (cols % 256 == 0) run in passes of up to 128 through the
- * prefill kernel: each weight w is dequantized as qmv_dequant does and enters the tensor core
+ * bfloat16 batches of 17 and more (and of 16 in groups under 16 MB of weights; cols % 256 ==
+ * 0) run in passes of up to 128 through the prefill kernel: each weight w is dequantized as
+ * qmv_dequant does and enters the tensor core
  * as two bfloat16 parts hi = RN_bf16(w) and lo = RN_bf16(w - hi) (for Q4_0 with f16 scales
  * hi + lo = w exactly; otherwise within 2^-17 |w|, and within 2^-134 absolute for the
  * weights below 2^-117 that only float32 scales under 2^-120 produce), stored to tensor

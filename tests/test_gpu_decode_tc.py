@@ -1,12 +1,14 @@
-"""The tensor-memory decode kernel (bf16 activations, passes of 4..8 vectors, and Q8_0
-launches of 64M weights or more) vs the oracle.
+"""The decode kernels for 2..16 bf16 vectors vs the oracle: the tensor-memory kernel (passes of
+4..8 vectors over 40 MB of weights, passes of 9..16 vectors over 16 MB, Q8_0 launches of 64M
+weights or more) and, on smaller launches, the mma.sync kernel (passes of up to 8).
 
-That kernel splits the work into units of 128 rows x 256 columns shared out evenly between
-two CTAs per SM, so a tile's columns may be summed by several CTAs; the parts meet in a
-per-stream workspace and the last CTA to arrive adds them in CTA order.  These tests aim at
-that machinery: tiles split between many CTAs, tiles that end where a problem of a grouped
-launch ends, repeated calls (the arrival counters must be back at zero after every call),
-and the result's independence from timing (bit-identical across calls and graph replays).
+The tensor-memory kernel splits the work into units of 128 rows x 256 columns shared out
+evenly between two CTAs per SM, so a tile's columns may be summed by several CTAs; the parts
+meet in a per-stream workspace and the last CTA to arrive adds them in CTA order.  The tests
+at its sizes aim at that machinery: tiles split between many CTAs, tiles that end where a
+problem of a grouped launch ends, repeated calls (the arrival counters must be back at zero
+after every call), and the result's independence from timing (bit-identical across calls and
+graph replays).  The small shapes check the mma.sync kernel the same way.
 """
 import numpy as np
 import pytest
@@ -19,6 +21,19 @@ pytestmark = pytest.mark.gpu
 
 TOL = 1e-3
 TYPES = [(1, 0), (1, 1), (2, 0), (2, 1)]
+# launch sizes from which the tensor-memory kernel takes the bf16 passes
+TC_MIN_BYTES = 40 << 20       # passes of 4..8 vectors
+TC_WIDE_MIN_BYTES = 16 << 20  # passes of 9..16 vectors, one launch each
+
+
+def weight_bytes(wt, sf, rows, cols):
+    return rows * cols // 32 * ((16 if wt == 2 else 32) + (2 if sf else 4))
+
+
+def sample_rows(rows, seed, n=160):
+    rng = np.random.default_rng(seed)
+    ids = np.unique(np.concatenate([rng.integers(0, rows, n), [0, 127, 128, rows - 1]]))
+    return ids
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -42,7 +57,7 @@ def run(q, m, x, y=None):
 
 @pytest.mark.parametrize("wt,sf", TYPES)
 @pytest.mark.parametrize("rows,cols", [(256, 256), (512, 4096), (300, 2048), (2000, 1024), (4096, 4096)])
-@pytest.mark.parametrize("batch", [4, 5, 8])
+@pytest.mark.parametrize("batch", [4, 5, 8, 9, 12, 15])
 def test_tc_decode_matches_oracle(qmv, wt, sf, rows, cols, batch):
     # 512 x 4096: 64 units on 64 CTAs, each of the four tiles split 16 ways
     m = inputs.make_matrix(wt, sf, rows, cols, seed=rows * 7 + cols + batch)
@@ -52,9 +67,10 @@ def test_tc_decode_matches_oracle(qmv, wt, sf, rows, cols, batch):
 
 
 @pytest.mark.parametrize("wt,sf", [(1, 0), (2, 1)])
-def test_tc_exact_pow2(qmv, wt, sf):
+@pytest.mark.parametrize("batch", [8, 13])
+def test_tc_exact_pow2(qmv, wt, sf, batch):
     # power-of-two scales, integer activations: every partial sum is exact, in any split
-    rows, cols, batch = 600, 4096, 8
+    rows, cols = 600, 4096
     rng = np.random.default_rng(11 + wt)
     m = inputs.make_matrix(wt, sf, rows, cols, seed=12)
     codes = inputs.pow2_scales(rng, rows * cols // 32, sf)
@@ -80,9 +96,10 @@ def test_tc_zero_rows_exact(qmv):
 
 
 @pytest.mark.parametrize("wt,sf", [(2, 1), (1, 0)])
-def test_tc_repeated_calls_bit_identical(qmv, wt, sf):
+@pytest.mark.parametrize("batch", [8, 14])
+def test_tc_repeated_calls_bit_identical(qmv, wt, sf, batch):
     # the split tiles' counters are reset by each call: later calls give the same bits
-    rows, cols, batch = 1536, 4096, 8
+    rows, cols = 1536, 4096
     m = inputs.make_matrix(wt, sf, rows, cols, seed=15)
     x = inputs.make_x(batch, cols, True, seed=15)
     first = run(qmv, m, x)
@@ -92,11 +109,11 @@ def test_tc_repeated_calls_bit_identical(qmv, wt, sf):
         assert_bits_equal(run(qmv, m, x), first, "tc repeated call")
 
 
-def test_tc_grouped_problems(qmv):
+@pytest.mark.parametrize("batch", [7, 11])
+def test_tc_grouped_problems(qmv, batch):
     # a grouped launch: units of all problems in one list, tiles ending at problem ends
     import torch
     shapes = [(300, 4096), (1024, 1024), (257, 2048), (4096, 256)]
-    batch = 7
     probs, refs = [], []
     for i, (rows, cols) in enumerate(shapes):
         m = inputs.make_matrix(2, 1, rows, cols, seed=70 + i)
@@ -145,3 +162,85 @@ def test_tc_q8_large_launch_batch1(qmv):
     ids = np.arange(0, rows, 97)
     y_ref, absref = oracle.matvec_rows(m.W, 1, 0, rows, cols, x, ids)
     check_product(y[:, ids], y_ref, absref, TOL, "q8 large b1")
+
+
+@pytest.mark.parametrize("wt,sf,rows,cols", [(1, 0, 20480, 2048), (2, 1, 36864, 2048)])
+@pytest.mark.parametrize("batch", [4, 7, 8])
+def test_tc_large_launch_sampled_rows(qmv, wt, sf, rows, cols, batch):
+    # 47 / 42 MB: the tensor-memory kernel at 4..8 vectors; rows sampled over every part of the
+    # matrix (tiles split between CTAs at every CTA boundary)
+    assert weight_bytes(wt, sf, rows, cols) >= TC_MIN_BYTES
+    m = inputs.make_matrix(wt, sf, rows, cols, seed=30 + batch)
+    x = inputs.make_x(batch, cols, True, seed=31 + batch)
+    y = run(qmv, m, x)
+    ids = sample_rows(rows, 32 + batch)
+    y_ref, absref = oracle.matvec_rows(m.W, wt, sf, rows, cols, x, ids)
+    check_product(y[:, ids], y_ref, absref, TOL, f"tc large {wt},{sf} b{batch}")
+
+
+@pytest.mark.parametrize("wt,sf,rows,cols", [(2, 1, 8192, 4096), (1, 1, 4096, 4096)])
+@pytest.mark.parametrize("batch", [9, 12, 16])
+def test_tc_sixteen_vector_pass(qmv, wt, sf, rows, cols, batch):
+    # 19 / 18 MB, 9..16 vectors: one pass of the tensor-memory kernel, all 16 MMA columns
+    # vectors (zeros past the batch); batch 16 takes it too at these sizes
+    assert weight_bytes(wt, sf, rows, cols) >= TC_WIDE_MIN_BYTES
+    m = inputs.make_matrix(wt, sf, rows, cols, seed=40 + batch)
+    x = inputs.make_x(batch, cols, True, seed=41 + batch)
+    y = run(qmv, m, x)
+    ids = sample_rows(rows, 42 + batch)
+    y_ref, absref = oracle.matvec_rows(m.W, wt, sf, rows, cols, x, ids)
+    check_product(y[:, ids], y_ref, absref, TOL, f"tc 16 {wt},{sf} b{batch}")
+    check_product(y[:, ids], y_ref, absref, 1e-5, f"tc 16 tight {wt},{sf} b{batch}")
+
+
+@pytest.mark.parametrize("batch", [10, 16])
+def test_tc_sixteen_vector_pass_exact_and_repeatable(qmv, batch):
+    # power-of-two scales and integer activations: every partial sum is exact in any split, so
+    # the sampled rows equal the oracle bit for bit; repeated calls and graph replays give the
+    # same bits (the arrival counters are back at zero after every launch)
+    import torch
+    wt, sf, rows, cols = 2, 1, 8192, 4096
+    rng = np.random.default_rng(50 + batch)
+    m = inputs.make_matrix(wt, sf, rows, cols, seed=51)
+    codes = inputs.pow2_scales(rng, rows * cols // 32, sf)
+    W = inputs.assemble(wt, sf, rows, cols, m.q, codes)
+    x = inputs.make_int_x(batch, cols, True, seed=52 + batch)
+    Wd, xd = dev_u8(W), dev_x(x)
+    s = torch.cuda.Stream()
+    y = torch.empty((batch, rows), device="cuda")
+    with torch.cuda.stream(s):
+        qmv.matvec(wt, sf, rows, cols, Wd, xd, y)
+    torch.cuda.synchronize()
+    first = y.cpu().numpy().copy()
+    ids = sample_rows(rows, 53)
+    y_ref, _ = oracle.matvec_rows(W, wt, sf, rows, cols, x, ids)
+    assert np.array_equal(first[:, ids].astype(np.float64), y_ref)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(3):
+            qmv.matvec(wt, sf, rows, cols, Wd, xd, y)
+    for _ in range(3):
+        y.fill_(0.0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert_bits_equal(y.cpu().numpy(), first, "tc 16 graph replay")
+
+
+@pytest.mark.parametrize("batch", [6, 11])
+def test_tc_grouped_large_launch(qmv, batch):
+    # a grouped launch of 45 MB (tiles of three problems in one unit list), with overlap
+    import torch
+    shapes = [(14336, 4096), (4096, 4096), (1000, 4096)]
+    assert sum(weight_bytes(2, 1, r, c) for r, c in shapes) >= TC_MIN_BYTES
+    probs, refs = [], []
+    for i, (rows, cols) in enumerate(shapes):
+        m = inputs.make_matrix(2, 1, rows, cols, seed=60 + i)
+        x = inputs.make_x(batch, cols, True, seed=70 + i)
+        y = torch.full((batch, rows), 3.0, device="cuda")
+        ids = sample_rows(rows, 80 + i)
+        probs.append((rows, cols, dev_u8(m.W), dev_x(x), y))
+        refs.append((ids, oracle.matvec_rows(m.W, 2, 1, rows, cols, x, ids)))
+    qmv.matvec_grouped(2, 1, probs, overlap=True)
+    torch.cuda.synchronize()
+    for (rows, cols, _, _, y), (ids, (y_ref, absref)) in zip(probs, refs):
+        check_product(y.cpu().numpy()[:, ids], y_ref, absref, TOL, f"tc grouped {rows}x{cols} b{batch}")

@@ -65,10 +65,31 @@ def test_noalloc_matches_grouped_and_oracle(qmv, wt, sf, batch):
         what = f"noalloc {wt},{sf} {p[0]}x{p[1]} b{batch}"
         check_product(outs[0][k], y_ref, absref, TOL, what)
         assert_bits_equal(outs[1][k], outs[0][k], what + " second call")
+        # (the existing entry point takes the mma.sync kernel at this size: other sums)
         check_product(base[k], y_ref, absref, TOL, what + " (existing entry point)")
-        if batch >= 5:
-            # the existing entry point runs the same kernel here: same splits, same bits
-            assert_bits_equal(outs[0][k], base[k], what + " vs existing")
+
+
+@pytest.mark.parametrize("batch", [5, 8])
+def test_noalloc_same_bits_as_grouped_at_tensor_memory_sizes(qmv, batch):
+    # 47 MB of Q8_0 weights, 5..8 vectors: qmv_matvec_grouped takes the tensor-memory kernel
+    # too, with the same grid and the same splits, so the two give the same bits (sampled rows
+    # against the oracle)
+    import torch
+    wt, sf, rows, cols = 1, 0, 20480, 2048
+    assert rows * cols // 32 * 36 >= 40 << 20
+    mats, probs = _problems(wt, sf, [(rows, cols)], batch, seed=350 + batch)
+    (m, x), = mats
+    qmv.matvec_grouped(wt, sf, probs)
+    torch.cuda.synchronize()
+    base = probs[0][4].cpu().numpy().copy()
+    probs[0][4].fill_(5.0)
+    qmv.matvec_grouped_noalloc(wt, sf, probs, stream=torch.cuda.Stream())
+    torch.cuda.synchronize()
+    out = probs[0][4].cpu().numpy()
+    ids = np.unique(np.random.default_rng(351).integers(0, rows, 128))
+    y_ref, absref = oracle.matvec_rows(m.W, wt, sf, rows, cols, x, ids)
+    check_product(out[:, ids], y_ref, absref, TOL, f"noalloc large b{batch}")
+    assert_bits_equal(out, base, f"noalloc large b{batch} vs existing")
 
 
 def test_noalloc_takes_no_device_memory_after_first_call(qmv):
