@@ -66,7 +66,10 @@ constexpr int kMaxProblems = 8;      // problems per grouped launch
 // current one is used; 1: only for launches where every warp has a single stage (half the
 // shared memory, so twice the CTAs per SM), whose one stage is requested before the
 // dependency wait.
-template <int WT, bool F16, int NW, int CH, bool XS = false, int RD = 2>
+// XH: the activations were rounded to half ahead of the product (per 256-column chunk, as above),
+// with the bfloat16 pair kept in device memory for the chunks that do not round: the stage holds
+// the half values (as a bfloat16 vector's), the slots room for both parts.
+template <int WT, bool F16, int NW, int CH, bool XS = false, int RD = 2, bool XH = false>
 struct Cfg {
   static constexpr int kCH = CH;                                   // chunks per stage
   static constexpr int XPARTS = XS ? 2 : 1;                        // activation vectors per stage
@@ -93,7 +96,7 @@ struct Cfg {
   static constexpr int OFF_D = NW * Q_WARP;
   static constexpr int OFF_X = OFF_D + NW * D_WARP;
   static constexpr int OFF_SLOT = OFF_X + NW * X_WARP;
-  static constexpr int SLOT_WARP = XPARTS * CH * 512;             // a warp's slots: [vector][chunk][lane]
+  static constexpr int SLOT_WARP = (XS || XH ? 2 : 1) * CH * 512;  // a warp's slots: [vector][chunk][lane]
   static constexpr int OFF_ZERO = OFF_SLOT + NW * SLOT_WARP;
   static constexpr int OFF_RED = OFF_ZERO + SLOT_WARP;
   static constexpr int OFF_BAR = OFF_RED + ((NW * WROWS * 4 + 127) / 128) * 128;
@@ -106,6 +109,9 @@ struct Problem {
   int ntiles;   // warp tiles (16*MT rows)
   int nst;      // stages per tile row: ceil(cols / 256 / CH) (chunks past the end read zeros)
   int item0;    // first item of this problem in the group's item list
+  int nchunks;  // cols / 256
+  const uint16_t* xg;  // XH: the bfloat16 hi parts (cols), then the lo parts (cols)
+  const float* xinv;   // XH: per chunk 2^-s of its half values, 0 for a chunk that keeps hi + lo
 };
 
 struct Params {
@@ -269,13 +275,15 @@ __device__ __forceinline__ void chunk_math(float (&acc)[Cfg<WT, F16, NW, CH>::MT
 // bytes of the hi and lo boxes); a stage that rounds to half as above takes them directly, the
 // others are split by each lane into hi = RN_bf16(x) and lo = RN_bf16(x - hi) in registers
 // (split_bf16_pair, the split kernel's rule), so float32 activations take one launch.
-template <int WT, bool F16, int NW, int CH, bool XS, bool GLU = false, bool XF = false, int RD = 2>
+template <int WT, bool F16, int NW, int CH, bool XS, bool GLU = false, bool XF = false, int RD = 2, bool XH = false>
 __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_constant__ Maps maps,
                                                                const __grid_constant__ Params p) {
-  using C = Cfg<WT, F16, NW, CH, XS, RD>;
+  using C = Cfg<WT, F16, NW, CH, XS, RD, XH>;
   constexpr int MT = C::MT;
   static_assert(!GLU || (MT == 2 && !XS), "the gated pair takes two 16-row MMA tiles per warp tile");
   static_assert(!XF || XS, "float32 activations are split into the hi and lo parts");
+  static_assert(!XH || (!XS && !XF && !GLU), "pre-rounded half activations are a route of their own");
+  constexpr bool XP = XS || XH;  // activations with hi and lo parts
   constexpr int TROWS = GLU ? kRows : C::WROWS;  // rows of each matrix per warp tile
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -460,14 +468,8 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            // 2^s with amax * 2^s in [2^14, 2^15): s = 141 - (biased exponent of amax); 1 for a stage
-            // of zeros
-            const int eb = (int)((__float_as_uint(amax) >> 23) & 0xFFu);
-            const bool scalable = amax == 0.f || (eb >= 15 && eb <= 254);
-            const int se = amax == 0.f ? 127 : 268 - eb;  // biased exponent of 2^s
-            const float xs = __uint_as_float((uint32_t)(scalable ? se : 127) << 23);
-            const float xinv = __uint_as_float((uint32_t)(scalable ? 254 - se : 127) << 23);
-            bool fits = scalable;
+            float xs, xinv;
+            bool fits = half_stage_scale(amax, xs, xinv);
             uint32_t rx[C::kCH][4];
 #pragma unroll
             for (int h = 0; h < C::kCH; ++h)
@@ -484,10 +486,37 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
                                                                h * 512u, lrow, lsub, sw, g, t, xinv);
             }
           }
+          const int stage = cc.c0 + (cc.j << p.lgks);  // chunks CH stage ..
+          if constexpr (XH) {
+            // half values rounded ahead: the stage's chunks all rounded (chunk scales from device
+            // memory, the same for every lane), one MMA per block, sums taken back by 2^-s
+            float xinv[C::kCH];
+            bool all = true;
+#pragma unroll
+            for (int h = 0; h < C::kCH; ++h) {
+              const int ch = stage * C::kCH + h;
+              xinv[h] = ch < P.nchunks ? __ldg(P.xinv + ch) : 1.0f;  // chunks past the end: zeros
+              all = all && xinv[h] != 0.f;
+            }
+            if (all) {
+              rounded = true;
+#pragma unroll
+              for (int h = 0; h < C::kCH; ++h) {
+                const uint8_t* xl = xring + cs * C::X_STAGE + h * (kTK * 2) + g * 64 + t * 8;
+                const uint2 a = *reinterpret_cast<const uint2*>(xl);
+                const uint2 b = *reinterpret_cast<const uint2*>(xl + 32);
+                sts_u32x4(slot + h * 512, a.x, a.y, b.x, b.y);
+              }
+#pragma unroll
+              for (int h = 0; h < C::kCH; ++h)
+                chunk_math<WT, F16, NW, CH, true, false, true>(acc, qs + h * C::Q_CHUNK, ds + h * C::DCHUNK, bsrc,
+                                                               h * 512u, lrow, lsub, sw, g, t, xinv[h]);
+            }
+          }
           // this lane's activations of each chunk h: block g, elements 4t..4t+3 and
           // 16+4t..16+4t+3; its slot for chunk h is 512 bytes after the one for chunk h-1
-          // (XS: the same of the lo vector, whose slots follow the hi ones: chunk h at CH + h)
-          constexpr int NX = C::XPARTS * C::kCH;
+          // (XS, XH: the same of the lo vector, whose slots follow the hi ones: chunk h at CH + h)
+          constexpr int NX = (XP ? 2 : 1) * C::kCH;
           uint2 xa[NX], xb[NX];
           uint32_t hx[NX][4];
           bool exact = true;
@@ -512,14 +541,24 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
           }
 #pragma unroll
           for (int e = 0; e < NX; ++e) {
-            if (!XF) {
+            if (XH) {
+              // the pair from device memory (hi row, then lo row), zeros past the end
+              const int ch = stage * C::kCH + (e % C::kCH);
+              xa[e] = xb[e] = make_uint2(0u, 0u);
+              if (ch < P.nchunks) {
+                const uint16_t* src = P.xg + (e >= C::kCH ? (size_t)P.nchunks * kTK : 0) + (size_t)ch * kTK +
+                                      g * 32 + t * 4;
+                xa[e] = __ldg(reinterpret_cast<const uint2*>(src));
+                xb[e] = __ldg(reinterpret_cast<const uint2*>(src + 16));
+              }
+            } else if (!XF) {
               const uint8_t* xl = xring + cs * C::X_STAGE + e * (kTK * 2) + g * 64 + t * 8;
               xa[e] = *reinterpret_cast<const uint2*>(xl);
               xb[e] = *reinterpret_cast<const uint2*>(xl + 32);
             }
-            // XS: the lo vector (about 2^-9 of hi) scaled by 2^9, exactly, so that its values lie
-            // where IEEE half holds them exactly as often as hi's do
-            const float sc = (XS && e >= C::kCH) ? 512.0f : 1.0f;
+            // XS, XH: the lo vector (about 2^-9 of hi) scaled by 2^9, exactly, so that its values
+            // lie where IEEE half holds them exactly as often as hi's do
+            const float sc = (XP && e >= C::kCH) ? 512.0f : 1.0f;
             hx[e][0] = bf16x2_to_f16x2_scaled(xa[e].x, sc, exact);
             hx[e][1] = bf16x2_to_f16x2_scaled(xa[e].y, sc, exact);
             hx[e][2] = bf16x2_to_f16x2_scaled(xb[e].x, sc, exact);
@@ -530,14 +569,14 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
             for (int e = 0; e < NX; ++e) sts_u32x4(slot + e * 512, hx[e][0], hx[e][1], hx[e][2], hx[e][3]);
 #pragma unroll
             for (int h = 0; h < C::kCH; ++h)
-              chunk_math<WT, F16, NW, CH, true, XS>(acc, qs + h * C::Q_CHUNK, ds + h * C::DCHUNK, bsrc, h * 512u,
+              chunk_math<WT, F16, NW, CH, true, XP>(acc, qs + h * C::Q_CHUNK, ds + h * C::DCHUNK, bsrc, h * 512u,
                                                     lrow, lsub, sw, g, t);
           } else {
 #pragma unroll
             for (int e = 0; e < NX; ++e) sts_u32x4(slot + e * 512, xa[e].x, xa[e].y, xb[e].x, xb[e].y);
 #pragma unroll
             for (int h = 0; h < C::kCH; ++h)
-              chunk_math<WT, F16, NW, CH, false, XS>(acc, qs + h * C::Q_CHUNK, ds + h * C::DCHUNK, bsrc, h * 512u,
+              chunk_math<WT, F16, NW, CH, false, XP>(acc, qs + h * C::Q_CHUNK, ds + h * C::DCHUNK, bsrc, h * 512u,
                                                      lrow, lsub, sw, g, t);
           }
           }  // !rounded
@@ -628,10 +667,10 @@ struct Plan {
   long long waves = 0;
 };
 
-template <int WT, bool F16, int NW, int CH, bool XS, bool GLU = false, bool XF = false, int RD = 2>
+template <int WT, bool F16, int NW, int CH, bool XS, bool GLU = false, bool XF = false, int RD = 2, bool XH = false>
 cudaError_t plan_typed(const MatrixRef* ms, int n, const DeviceInfo& dev, Plan* out) {
-  using C = Cfg<WT, F16, NW, CH, XS, RD>;
-  auto kern = matvec_bdiag_kernel<WT, F16, NW, CH, XS, GLU, XF, RD>;
+  using C = Cfg<WT, F16, NW, CH, XS, RD, XH>;
+  auto kern = matvec_bdiag_kernel<WT, F16, NW, CH, XS, GLU, XF, RD, XH>;
   // per device: the shared-memory attribute set and the occupancy known (0 = does not fit)
   static std::mutex mu;
   static bool ready[64] = {};
@@ -687,10 +726,12 @@ cudaError_t plan_typed(const MatrixRef* ms, int n, const DeviceInfo& dev, Plan* 
 
 // GLU: ms = {w1, w3} (same shape), one x (xs[0]); the pair is one problem whose warp tiles are
 // 16 rows of each; act and h as in Params.
-template <int WT, bool F16, int NW, int CH, bool XS, bool GLU = false, bool XF = false, int RD = 2>
+// XH: xs[i] is the problem's area of the half route's buffer: the bfloat16 hi row and lo row
+// (cols each), the half row, then the chunks' inverse scales (cols / 256 floats).
+template <int WT, bool F16, int NW, int CH, bool XS, bool GLU = false, bool XF = false, int RD = 2, bool XH = false>
 cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* const* xs, float* const* ys, int n,
                          bool pdl, const DeviceInfo& dev, cudaStream_t stream, int act = -1, uint16_t* h = nullptr) {
-  using C = Cfg<WT, F16, NW, CH, XS, RD>;
+  using C = Cfg<WT, F16, NW, CH, XS, RD, XH>;
   constexpr int TROWS = GLU ? kRows : C::WROWS;  // rows of each matrix per warp tile
   if (GLU && (n != 2 || ms[0].rows != ms[1].rows || ms[0].cols != ms[1].cols || h == nullptr))
     return cudaErrorInvalidValue;
@@ -709,6 +750,11 @@ cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* cons
     p.pr[i].ntiles = (int)((ms[i].rows + TROWS - 1) / TROWS);
     p.pr[i].nst = (int)((ms[i].cols / kTK + C::kCH - 1) / C::kCH);
     p.pr[i].item0 = items;
+    p.pr[i].nchunks = (int)(ms[i].cols / kTK);
+    if (XH) {
+      p.pr[i].xg = static_cast<const uint16_t*>(xs[i]);
+      p.pr[i].xinv = reinterpret_cast<const float*>(static_cast<const uint16_t*>(xs[i]) + 3 * ms[i].cols);
+    }
     items += (p.pr[i].ntiles + tpi - 1) / tpi;
   }
   if (items != plan.nitems) return cudaErrorInvalidValue;
@@ -733,7 +779,9 @@ cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* cons
       if (err != cudaSuccess) return err;
       continue;
     }
-    err = encode_tmap_2d(&maps.x[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xs[i], kTK, (uint64_t)(m.cols / kTK), kTK * 2,
+    // (XH: the half row; two-byte elements as a bfloat16 vector's)
+    const void* xb = XH ? static_cast<const void*>(static_cast<const uint16_t*>(xs[i]) + 2 * m.cols) : xs[i];
+    err = encode_tmap_2d(&maps.x[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xb, kTK, (uint64_t)(m.cols / kTK), kTK * 2,
                          kTK, C::kCH, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (err != cudaSuccess) return err;
     if (XS) {  // the lo vector follows the hi one
@@ -754,7 +802,7 @@ cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* cons
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, matvec_bdiag_kernel<WT, F16, NW, CH, XS, GLU, XF, RD>, maps, p);
+  return cudaLaunchKernelEx(&cfg, matvec_bdiag_kernel<WT, F16, NW, CH, XS, GLU, XF, RD, XH>, maps, p);
 }
 
 // Q4_0 launches of at least this many weight bytes take one-chunk stages.
@@ -766,7 +814,7 @@ constexpr long long kOneChunkBytes = 32LL << 20;
 // launches of a few tens of MB (the Llama-7B layer's, the 4096 x 4096 product) and on Q8_0.
 // GLU: ms = {w1, w3}, planned as one matrix of twice the rows (the same warp tiles: 16 rows of
 // each per tile); act and h as in launch_typed.
-template <int WT, bool F16, bool XS, bool GLU = false, bool XF = false>
+template <int WT, bool F16, bool XS, bool GLU = false, bool XF = false, bool XH = false>
 cudaError_t launch_best(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
                         const DeviceInfo& dev, cudaStream_t stream, int act = -1, uint16_t* h = nullptr) {
   MatrixRef pair[1];
@@ -785,44 +833,44 @@ cudaError_t launch_best(const MatrixRef* ms, const void* const* xs, float* const
     for (int i = 0; i < pn; ++i) bytes += pm[i].rows * pm[i].cols / 2;
     if (bytes >= kOneChunkBytes) {
       Plan p1;
-      err = plan_typed<WT, F16, 4, 1, XS, GLU, XF>(pm, pn, dev, &p1);
+      err = plan_typed<WT, F16, 4, 1, XS, GLU, XF, 2, XH>(pm, pn, dev, &p1);
       if (err != cudaSuccess) return err;
       if (p1.cost >= 0 && p1.grid > dev.sm_count)
-        return launch_typed<WT, F16, 4, 1, XS, GLU, XF>(p1, ms, xs, ys, n, pdl, dev, stream, act, h);
+        return launch_typed<WT, F16, 4, 1, XS, GLU, XF, 2, XH>(p1, ms, xs, ys, n, pdl, dev, stream, act, h);
     }
   }
-  err = plan_typed<WT, F16, 4, 2, XS, GLU, XF>(pm, pn, dev, &p4);
+  err = plan_typed<WT, F16, 4, 2, XS, GLU, XF, 2, XH>(pm, pn, dev, &p4);
   if (err != cudaSuccess) return err;
   if constexpr (!XS && !GLU) {
     if (p4.cost >= 0 && p4.longest > 1) {
       // 8-warp CTAs with a ring of one: every warp one stage, in one wave, where 4-warp CTAs
       // give each warp two or more stages one after the other
       Plan p1;
-      err = plan_typed<WT, F16, 8, 2, XS, GLU, XF, 1>(pm, pn, dev, &p1);
+      err = plan_typed<WT, F16, 8, 2, XS, GLU, XF, 1, XH>(pm, pn, dev, &p1);
       if (err != cudaSuccess) return err;
       if (p1.cost >= 0 && p1.longest == 1 && p1.waves == 1 && p1.grid > dev.sm_count)
-        return launch_typed<WT, F16, 8, 2, XS, GLU, XF, 1>(p1, ms, xs, ys, n, pdl, dev, stream, act, h);
+        return launch_typed<WT, F16, 8, 2, XS, GLU, XF, 1, XH>(p1, ms, xs, ys, n, pdl, dev, stream, act, h);
     }
   }
   if (p4.cost >= 0 && p4.grid > dev.sm_count)
-    return launch_typed<WT, F16, 4, 2, XS, GLU, XF>(p4, ms, xs, ys, n, pdl, dev, stream, act, h);
-  err = plan_typed<WT, F16, 8, 2, XS, GLU, XF>(pm, pn, dev, &p8);
+    return launch_typed<WT, F16, 4, 2, XS, GLU, XF, 2, XH>(p4, ms, xs, ys, n, pdl, dev, stream, act, h);
+  err = plan_typed<WT, F16, 8, 2, XS, GLU, XF, 2, XH>(pm, pn, dev, &p8);
   if (err != cudaSuccess) return err;
   if (p8.cost >= 0 && (p4.cost < 0 || p8.cost < p4.cost))
-    return launch_typed<WT, F16, 8, 2, XS, GLU, XF>(p8, ms, xs, ys, n, pdl, dev, stream, act, h);
+    return launch_typed<WT, F16, 8, 2, XS, GLU, XF, 2, XH>(p8, ms, xs, ys, n, pdl, dev, stream, act, h);
   if (p4.cost < 0) return cudaErrorInvalidConfiguration;
-  return launch_typed<WT, F16, 4, 2, XS, GLU, XF>(p4, ms, xs, ys, n, pdl, dev, stream, act, h);
+  return launch_typed<WT, F16, 4, 2, XS, GLU, XF, 2, XH>(p4, ms, xs, ys, n, pdl, dev, stream, act, h);
 }
 
-template <bool XS, bool XF = false>
+template <bool XS, bool XF = false, bool XH = false>
 cudaError_t launch_any(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
                        const DeviceInfo& dev, cudaStream_t stream) {
   const MatrixRef& m = ms[0];
   if (m.wtype == QMV_Q4_0)
-    return m.scale_f16 ? launch_best<QMV_Q4_0, true, XS, false, XF>(ms, xs, ys, n, pdl, dev, stream)
-                       : launch_best<QMV_Q4_0, false, XS, false, XF>(ms, xs, ys, n, pdl, dev, stream);
-  return m.scale_f16 ? launch_best<QMV_Q8_0, true, XS, false, XF>(ms, xs, ys, n, pdl, dev, stream)
-                     : launch_best<QMV_Q8_0, false, XS, false, XF>(ms, xs, ys, n, pdl, dev, stream);
+    return m.scale_f16 ? launch_best<QMV_Q4_0, true, XS, false, XF, XH>(ms, xs, ys, n, pdl, dev, stream)
+                       : launch_best<QMV_Q4_0, false, XS, false, XF, XH>(ms, xs, ys, n, pdl, dev, stream);
+  return m.scale_f16 ? launch_best<QMV_Q8_0, true, XS, false, XF, XH>(ms, xs, ys, n, pdl, dev, stream)
+                     : launch_best<QMV_Q8_0, false, XS, false, XF, XH>(ms, xs, ys, n, pdl, dev, stream);
 }
 
 }  // namespace
@@ -835,6 +883,11 @@ cudaError_t launch_matvec_bdiag(const MatrixRef* ms, const void* const* xs, floa
 cudaError_t launch_matvec_bdiag_split(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
                                       const DeviceInfo& dev, cudaStream_t stream) {
   return launch_any<true>(ms, xs, ys, n, pdl, dev, stream);
+}
+
+cudaError_t launch_matvec_bdiag_half(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
+                                     const DeviceInfo& dev, cudaStream_t stream) {
+  return launch_any<false, false, true>(ms, xs, ys, n, pdl, dev, stream);
 }
 
 cudaError_t launch_matvec_bdiag_f32in(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,

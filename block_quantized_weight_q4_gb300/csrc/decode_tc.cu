@@ -121,6 +121,63 @@ __global__ void __launch_bounds__(256) split_x_kernel(const __grid_constant__ Sp
   }
 }
 
+// The block-diagonal kernel's half route for one float32 vector per problem (or act(gate) * up):
+// per column the bfloat16 pair hi, lo (rows 0 and 1, split_x_kernel's rule) and, per 256-column
+// chunk, the power of two xs = 2^s that brings the chunk's largest magnitude into [2^14, 2^15)
+// (half_stage_scale): row 2 holds RN_half(x * xs) and, after the three rows, one float per chunk
+// holds 2^-s, or 0 when the chunk does not round (a value not finite, or a nonzero value with
+// |x * xs| under 2^-14, where half is not normal), whose products take hi and lo instead.  One
+// CTA of 256 threads per chunk (blockIdx.x) of a problem (blockIdx.y).
+struct HalfSplitArgs {
+  const float* x[dtc::kMaxProblems];
+  uint16_t* out[dtc::kMaxProblems];
+  int cols[dtc::kMaxProblems];
+  int act;             // -1: x as given; 0 / 1: x is a gate and the activations are act(gate) * up
+  long long up_batch;  // gated activations: a problem's up array is up_batch * cols floats after its gate
+};
+
+__global__ void __launch_bounds__(256) split_x_half_kernel(const __grid_constant__ HalfSplitArgs a) {
+  griddep_wait();  // the activations may be the preceding kernel's output
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  const int i = blockIdx.y;
+  const int cols = a.cols[i];
+  if ((int)blockIdx.x * 256 >= cols) return;  // the whole CTA: past this problem's chunks
+  const int c = blockIdx.x * 256 + threadIdx.x;
+  const float* x = a.x[i];
+  float v = x[c];
+  if (a.act >= 0) v = glu(a.act, v, x[(size_t)a.up_batch * cols + c]);
+  uint16_t hi, lo;
+  split_bf16_pair(v, hi, lo);
+  uint16_t* out = a.out[i];
+  out[c] = hi;
+  out[cols + c] = lo;
+  // the chunk's largest magnitude and smallest nonzero magnitude, as float32 bit patterns
+  // (unsigned order is magnitude order; a NaN lies above infinity)
+  const uint32_t m = __float_as_uint(v) & 0x7FFFFFFFu;
+  __shared__ uint32_t wmax[8], wmin[8];
+  uint32_t amax = __reduce_max_sync(0xffffffffu, m);
+  uint32_t amin = __reduce_min_sync(0xffffffffu, m == 0u ? 0xFFFFFFFFu : m);
+  if ((threadIdx.x & 31) == 0) {
+    wmax[threadIdx.x >> 5] = amax;
+    wmin[threadIdx.x >> 5] = amin;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    amax = wmax[w] > amax ? wmax[w] : amax;
+    amin = wmin[w] < amin ? wmin[w] : amin;
+  }
+  float xs, xinv;
+  bool fits = amax <= 0x7F7FFFFFu && half_stage_scale(__uint_as_float(amax), xs, xinv);
+  if (fits && amin != 0xFFFFFFFFu) fits = __uint_as_float(amin) * xs >= 0x1p-14f;
+  out[2 * cols + c] = __half_as_ushort(__float2half_rn(fits ? v * xs : 0.f));
+  if (threadIdx.x == 0) reinterpret_cast<float*>(out + 3 * (size_t)cols)[blockIdx.x] = fits ? xinv : 0.f;
+}
+
+// Bytes of one problem's area of the half route's buffer (three rows of cols two-byte values and
+// cols / 256 floats), rounded up to 512 so that every row of the next problem stays aligned.
+size_t half_area_bytes(int64_t cols) { return ((size_t)cols * 6 + (size_t)cols / 64 + 511) / 512 * 512; }
+
 }  // namespace
 
 // Split the float32 activations of n problems (batch vectors each) into rows of bfloat16 in
@@ -189,13 +246,43 @@ bool decode_tc_f32_fits(const MatrixRef* ms, int n) {
 
 cudaError_t launch_matvec_bdiag_f32(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
                                     const DeviceInfo& dev, cudaStream_t stream, int act, long long up_batch) {
+  if (n < 1 || n > dtc::kMaxProblems) return cudaErrorInvalidValue;
   size_t need = 0;
-  for (int i = 0; i < n; ++i) need += (size_t)2 * (size_t)ms[i].cols * 2;
+  int maxcols = 0;
+  for (int i = 0; i < n; ++i) {
+    if (ms[i].cols % dtc::kKS != 0) return cudaErrorInvalidValue;
+    need += half_area_bytes(ms[i].cols);
+    if (ms[i].cols > maxcols) maxcols = (int)ms[i].cols;
+  }
   if (need > kSplitBytes) return cudaErrorInvalidValue;
-  const void* sx[dtc::kMaxProblems];
-  cudaError_t err = split_activations(ms, xs, n, 1, 1, 1, act, up_batch, pdl, dev, stream, sx);  // rows: hi, lo
+  Workspace xw;
+  cudaError_t err = cached_workspace(g_xws, dev, stream, kSplitBytes, 0, &xw);
   if (err != cudaSuccess) return err;
-  return launch_matvec_bdiag_split(ms, sx, ys, n, true, dev, stream);
+  HalfSplitArgs a{};
+  const void* sx[dtc::kMaxProblems];
+  uint8_t* base = reinterpret_cast<uint8_t*>(xw.partials);
+  for (int i = 0; i < n; ++i) {
+    a.x[i] = static_cast<const float*>(xs[i]);
+    a.out[i] = reinterpret_cast<uint16_t*>(base);
+    a.cols[i] = (int)ms[i].cols;
+    sx[i] = base;
+    base += half_area_bytes(ms[i].cols);
+  }
+  a.act = act;
+  a.up_batch = up_batch;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)(maxcols / dtc::kKS), (unsigned)n);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  err = cudaLaunchKernelEx(&cfg, split_x_half_kernel, a);
+  if (err != cudaSuccess) return err;
+  // the product launches as a programmatic dependent of the split: its weight loads overlap it
+  return launch_matvec_bdiag_half(ms, sx, ys, n, true, dev, stream);
 }
 
 cudaError_t reset_workspaces() {

@@ -246,6 +246,19 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t p, bool& exact) {
   return h;
 }
 
+// The power of two xs = 2^s that brings a stage's largest magnitude amax into [2^14, 2^15)
+// (s = 141 - the biased exponent of amax), and xinv = 2^-s, both exact; amax == 0 gives
+// xs = xinv = 1.  False (xs = xinv = 1) when no such power is a normal float32: amax below
+// 2^-112, infinite or NaN.
+__device__ __forceinline__ bool half_stage_scale(float amax, float& xs, float& xinv) {
+  const int eb = (int)((__float_as_uint(amax) >> 23) & 0xFFu);
+  const bool ok = amax == 0.f || (eb >= 15 && eb <= 254);
+  const int se = (amax == 0.f || !ok) ? 127 : 268 - eb;  // biased exponent of 2^s
+  xs = __uint_as_float((uint32_t)se << 23);
+  xinv = __uint_as_float((uint32_t)(254 - se) << 23);
+  return ok;
+}
+
 // Two float32 values times a power of two `scale` rounded to an IEEE half pair (to nearest
 // even); `fits` is cleared unless each value is zero or its result is a normal half (magnitude
 // 2^-14 .. 65504), where the rounding's relative error is at most 2^-11.  A product that left

@@ -113,14 +113,20 @@ cudaError_t launch_matvec_bdiag_split(const MatrixRef* ms, const void* const* xs
 bool matvec_bdiag_glu_supported(const MatrixRef& w1, const MatrixRef& w3);
 cudaError_t launch_matvec_bdiag_glu(const MatrixRef& w1, const MatrixRef& w3, const void* x, int act, uint16_t* h,
                                     bool pdl, const DeviceInfo& dev, cudaStream_t stream);
+// The same problems with the activations rounded to half ahead of the product: xs[i] is the
+// problem's area written by the half route's split (launch_matvec_bdiag_f32): the bfloat16 hi and
+// lo rows, the half row and the chunks' inverse scales (0: that chunk takes hi and lo).
+cudaError_t launch_matvec_bdiag_half(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
+                                     const DeviceInfo& dev, cudaStream_t stream);
 // One float32 activation vector per problem (16-byte aligned), split into bfloat16 hi + lo in
 // the kernel's activation stage (one launch; the same parts and results as below).
 cudaError_t launch_matvec_bdiag_f32in(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
                                       const DeviceInfo& dev, cudaStream_t stream);
-// One float32 activation vector per problem: split into hi + lo bfloat16 in the stream's
-// split buffer (2 rows per problem, up to 524,288 columns over the problems), then the above.
-// Fails (nothing launched) when the buffer would not hold them, or cannot be created while
-// the stream is being captured.
+// One float32 activation vector per problem: split in the stream's split buffer into the hi + lo
+// bfloat16 rows and, per 256-column chunk, the values rounded to half after a power-of-two scale
+// (about 6 bytes per column: up to about 340,000 columns over the problems), then the half route
+// above.  Fails (nothing launched) when the buffer would not hold them, or cannot be created
+// while the stream is being captured.
 // act >= 0: xs are gates, the activations act(gate) * up with up at gate + up_batch * cols floats.
 cudaError_t launch_matvec_bdiag_f32(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
                                     const DeviceInfo& dev, cudaStream_t stream, int act = -1, long long up_batch = 0);

@@ -58,6 +58,24 @@ def test_glu_product_matches_oracle(qmv, act, act_id, wt, sf, batch):
     check_product(y.cpu().numpy(), y_ref, absref, tol=tight, what=f"glu tight {act} {wt},{sf} b{batch}")
 
 
+def test_glu_one_vector_chunk_with_a_wide_range(qmv):
+    # one vector: act(gate) * up is rounded to half per 256-column chunk ahead of the product;
+    # the chunk holding a value 2^-60 below the rest cannot be rounded (that value would not be
+    # a normal half) and keeps hi + lo, the others round: within HALF_TOL of the oracle
+    import torch
+    rows, cols = 512, 2048
+    m = inputs.make_matrix(2, 1, rows, cols, seed=440)
+    rng = np.random.default_rng(441)
+    g, u = gate_up(rng, 1, cols)
+    u[0, 700] = 2.0 ** -60
+    x = torch.from_numpy(np.stack([g, u])).cuda()
+    y = torch.empty((1, rows), device="cuda")
+    qmv.matvec_grouped(2, 1, [(rows, cols, dev_u8(m.W), x, y)], act="silu")
+    torch.cuda.synchronize()
+    y_ref, absref = oracle.matvec_glu(m.W, 2, 1, rows, cols, 0, g, u)
+    check_product(y.cpu().numpy(), y_ref, absref, tol=HALF_TOL, what="glu wide chunk")
+
+
 @pytest.mark.parametrize("batch", [1, 4])
 def test_glu_group_of_different_widths(qmv, batch):
     import torch

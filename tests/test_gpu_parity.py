@@ -376,7 +376,7 @@ def test_f32_activations_batch8_graph_replay_bit_identical(qmv):
         assert_bits_equal(y.cpu().numpy(), first, "f32 x graph replay")
 
 
-@pytest.mark.parametrize("route", ["f32", "pair"])
+@pytest.mark.parametrize("route", ["f32", "pair", "f32_split"])
 def test_one_vector_stages_rounded_to_half_and_exact(qmv, route):
     # one vector x = 1 + 2^-12 everywhere (Q8_0 levels 1..7 and scales 2^-2..1: positive weights,
     # so every error has one sign), except
@@ -385,9 +385,11 @@ def test_one_vector_stages_rounded_to_half_and_exact(qmv, route):
     # exactly.  The stages over columns 1024..1535 span 2^40 > 2^28, so they keep hi + lo and
     # give x exactly.  The product must then equal the oracle's on x' (x with 1 outside columns
     # 1024..1535) up to float32 sums, and differ from the oracle's on x by about 2^-12 of y
-    # (within HALF_TOL); the pair route (hi = 1, lo = 2^-12) and the float32 route agree
+    # (within HALF_TOL); the pair route (hi = 1, lo = 2^-12) and the float32 routes agree.  f32:
+    # 1 MB of weights, rounded in the product's stages; f32_split: 18 MB, rounded per 256-column
+    # chunk by the split kernel ahead of the product
     import torch
-    rows, cols = 256, 4096
+    rows, cols = (4096 if route == "f32_split" else 256), 4096
     rng = np.random.default_rng(97)
     q = rng.integers(1, 8, size=rows * cols).astype(np.int8).view(np.uint8)
     codes = inputs.pow2_scales(rng, rows * cols // 32, 1, -2, 0)
@@ -401,7 +403,7 @@ def test_one_vector_stages_rounded_to_half_and_exact(qmv, route):
     y_exp, _ = oracle.matvec(W, 1, 1, rows, cols, x_rounded)
     Wd = dev_u8(W)
     y = torch.empty((1, rows), device="cuda")
-    if route == "f32":
+    if route != "pair":
         qmv.matvec_grouped(1, 1, [(rows, cols, Wd, torch.from_numpy(x).cuda(), y)])
     else:
         hi = inputs.bf16_codes(x[0])
