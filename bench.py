@@ -395,9 +395,9 @@ def other_workloads(torch, qmv, dev, l2, cap, peak_hbm, peak_tf):
             ov_us = _graph_time_us(torch, [lambda j=j: qmv.matvec_grouped(
                 2, 1, [(spec.rows, spec.cols, Ws[j % n], x, y)], overlap=True) for j in range(2 * n)], cap)
             flops = 2.0 * spec.rows * spec.cols * batch
-            # batch 16 over 16 MB of weights takes one 16-vector pass of the tensor-memory decode
+            # batch 16 over 8 MB of weights takes one 16-vector pass of the tensor-memory decode
             # kernel (measured faster there than the prefill kernel)
-            kern = "decode_tc (16-vector pass)" if batch <= 16 and mm.W.size >= (16 << 20) else "prefill"
+            kern = "decode_tc (16-vector pass)" if batch <= 16 and mm.W.size >= (8 << 20) else "prefill"
             res[f"prefill_{spec.rows}x{spec.cols}_b{batch}"] = {
                 "kernel": kern, "us": round(us, 3), "tflops": round(flops / us / 1e6, 1),
                 "frac_bf16_tensor_peak": round(flops / us / 1e6 / peak_tf, 4),

@@ -253,7 +253,7 @@ __device__ __forceinline__ void add_block_sums_split(uint32_t tsum, int k0, cons
 }
 
 template <int WT, bool F16, int NV>
-__global__ void __maxnreg__(NV > 8 ? 144 : 120) decode_tc_kernel(const __grid_constant__ Maps maps,
+__global__ void __maxnreg__(NV > 8 ? 128 : 120) decode_tc_kernel(const __grid_constant__ Maps maps,
                                                                 const __grid_constant__ Params p) {
   using C = Cfg<WT, F16>;
   constexpr int S = C::S;
@@ -609,7 +609,8 @@ cudaError_t launch_typed(const MatrixRef* ms, const void* const* xs, float* cons
     p.pr[i].unit0 = units;
     units += (long long)p.pr[i].ntiles * p.pr[i].nchunks;
   }
-  // two CTAs per SM: shared memory (<= 113 KB each), registers (<= 144 x 224 each) and tensor
+  // two CTAs per SM: shared memory (<= 113 KB each), registers (at most 128 a thread: the 14
+  // warps put four on some sub-partition, whose 16K registers then hold 4 x 32 x 128) and tensor
   // memory (256 columns each) hold two.  (The occupancy query reports one CTA per SM for any
   // kernel that allocates tensor memory, so it is not used here.)  Within the workspace's
   // counters and parts, and no more CTAs than units.

@@ -22,7 +22,7 @@ constexpr int kTcMinBatch = 4;        // decode passes of this many bf16 vectors
 constexpr long long kTcMinBytes = 40LL << 20;      // launches of this many weight bytes (below, mma.sync
                                                    // measured faster at 4..8 vectors)
 constexpr long long kTcMinQ8Weights = 64LL << 20;  // and Q8_0 passes of 2-3 vectors over this many weights
-constexpr long long kTcWideMinBytes = 16LL << 20;  // passes of 9..16 vectors in one decode_tc launch
+constexpr long long kTcWideMinBytes = 8LL << 20;   // passes of 9..16 vectors in one decode_tc launch
 constexpr long long kF32SplitMinWeights = 256LL << 10;  // one f32 vector: split hi/lo from this many weights
 // one f32 vector: split in the product's own activation stage (one launch) below this many
 // weight bytes; above it the split kernel runs once per column and the product reads its parts
@@ -212,7 +212,7 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
   };
   long long group_bytes = 0;
   for (int i = 0; i < n; ++i) group_bytes += weight_bytes(ms[i]);
-  // 17 or more bf16 vectors (16 in groups under 16 MB of weights, where it measured faster
+  // 17 or more bf16 vectors (16 in groups under 8 MB of weights, where it measured faster
   // than one 16-vector pass of the tensor-memory decode kernel): the prefill kernel, per
   // problem, in passes of up to 128
   const bool prefill_batch = batch >= kPrefillMinBatch || (batch == 16 && group_bytes < kTcWideMinBytes);
@@ -241,7 +241,7 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
   if (!any_decode) return QMV_OK;
   // problems the tensor-core kernel takes go in one launch per pass of 8 vectors; the rest
   // run the general kernel one by one.  bf16 batches of 9 or more whose problems the
-  // tensor-memory kernel takes all, 16 MB of weights or more, on a stream with its workspace:
+  // tensor-memory kernel takes all, 8 MB of weights or more, on a stream with its workspace:
   // passes of 16 (that kernel's 16 MMA columns then all hold vectors)
   long long decode_bytes = 0;
   for (int i = 0; i < n; ++i)

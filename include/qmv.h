@@ -122,10 +122,10 @@ int qmv_matrix_wtype(int file_wtype, uint32_t q8_mask, int class_bit, int shared
  *   y     : device, batch x rows float32, row-major; fully overwritten.
  *   batch : number of activation vectors, >= 0; 0 launches nothing and returns QMV_OK.
  * Each block contributes d * sum_j level_j * x_j; sums are kept in float32.  Batches
- * below 16 (and 16 in groups of 16 MB of weights or more, and float32 activations) run
+ * below 16 (and 16 in groups of 8 MB of weights or more, and float32 activations) run
  * through the decode kernels (weights decoded to exact levels, one tensor-core dot product
  * per block, f32 scale and accumulate) in passes of up to 8 vectors, or of up to 16 for bf16
- * batches of 9..16 in groups of 16 MB of weights or more: those 16-vector passes, bf16 passes
+ * batches of 9..16 in groups of 8 MB of weights or more: those 16-vector passes, bf16 passes
  * of 4..8 vectors over 40 MB of weights or more, and Q8_0 passes of 2 or 3 bf16 vectors over
  * 64M weights or more take the tensor-memory kernel (levels stored to tensor memory, tcgen05
  * MMA; below those sizes the mma.sync kernel measured faster and takes the other passes of
@@ -148,7 +148,7 @@ int qmv_matrix_wtype(int file_wtype, uint32_t q8_mask, int class_bit, int shared
  * their parts meet in a workspace of the calling stream (8 MiB of device memory, allocated
  * on the stream's first such call and kept; while a stream without one is being captured,
  * the call takes the mma.sync kernel instead).  Results do not depend on timing.
- * bfloat16 batches of 17 and more (and of 16 in groups under 16 MB of weights; cols % 256 ==
+ * bfloat16 batches of 17 and more (and of 16 in groups under 8 MB of weights; cols % 256 ==
  * 0) run in passes of up to 128 through the prefill kernel: each weight w is dequantized as
  * qmv_dequant does and enters the tensor core
  * as two bfloat16 parts hi = RN_bf16(w) and lo = RN_bf16(w - hi) (for Q4_0 with f16 scales

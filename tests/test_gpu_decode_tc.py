@@ -1,5 +1,5 @@
 """The decode kernels for 2..16 bf16 vectors vs the oracle: the tensor-memory kernel (passes of
-4..8 vectors over 40 MB of weights, passes of 9..16 vectors over 16 MB, Q8_0 launches of 64M
+4..8 vectors over 40 MB of weights, passes of 9..16 vectors over 8 MB, Q8_0 launches of 64M
 weights or more) and, on smaller launches, the mma.sync kernel (passes of up to 8).
 
 The tensor-memory kernel splits the work into units of 128 rows x 256 columns shared out
@@ -23,7 +23,7 @@ TOL = 1e-3
 TYPES = [(1, 0), (1, 1), (2, 0), (2, 1)]
 # launch sizes from which the tensor-memory kernel takes the bf16 passes
 TC_MIN_BYTES = 40 << 20       # passes of 4..8 vectors
-TC_WIDE_MIN_BYTES = 16 << 20  # passes of 9..16 vectors, one launch each
+TC_WIDE_MIN_BYTES = 8 << 20   # passes of 9..16 vectors, one launch each
 
 
 def weight_bytes(wt, sf, rows, cols):
