@@ -69,12 +69,13 @@ constexpr int kMaxProblems = 8;      // problems per grouped launch
 // XH: the activations were rounded to half ahead of the product (per 256-column chunk, as above),
 // with the bfloat16 pair kept in device memory for the chunks that do not round: the stage holds
 // the half values (as a bfloat16 vector's), the slots room for both parts.
-template <int WT, bool F16, int NW, int CH, bool XS = false, int RD = 2, bool XH = false>
+// X4: the stage's activation box holds four bytes a value (float32 activations).
+template <int WT, bool F16, int NW, int CH, bool XS = false, int RD = 2, bool XH = false, bool X4 = false>
 struct Cfg {
   static constexpr int kCH = CH;                                   // chunks per stage
   static constexpr int XPARTS = XS ? 2 : 1;                        // activation vectors per stage
   static constexpr int X_PART = CH * kTK * 2;                      // bfloat16 activations of one vector
-  static constexpr int X_STAGE = XPARTS * X_PART;                  // activations of one stage
+  static constexpr int X_STAGE = (XS || X4 ? 2 : 1) * X_PART;       // activations of one stage
   static constexpr int MT = (WT == QMV_Q4_0) ? 2 : 1;           // 16-row MMA tiles per warp tile
   static constexpr int WROWS = MT * kRows;                        // rows per warp tile
   static constexpr int CBOX = (WT == QMV_Q4_0) ? 1 : 2;         // q boxes per chunk
@@ -158,10 +159,13 @@ __device__ __forceinline__ void cursor_load(Cursor& c, const Params& p, int tile
 // row's scaled block sums of blocks 2t, 2t+1 to acc.
 // SC: the activations were scaled by a power of two for the MMAs; xinv (its inverse) takes
 // each block sum back before the block's scale is applied (exact).
-template <int WT, bool F16, int NW, int CH, bool HALF, bool XS = false, bool SC = false>
+// QX: the activations are Q8_0 quants with a scale per block; dx0, dx1 are those of blocks 2t
+// and 2t+1, and each block's sum is scaled by the product d_w * d_x.
+template <int WT, bool F16, int NW, int CH, bool HALF, bool XS = false, bool SC = false, bool QX = false>
 __device__ __forceinline__ void chunk_math(float (&acc)[Cfg<WT, F16, NW, CH>::MT][2], uint32_t qs, const uint8_t* ds,
                                            const uint32_t (&bsrc)[kBlocksPerStage], uint32_t boff, int lrow,
-                                           int lsub, int sw, int g, int t, float xinv = 1.0f) {
+                                           int lsub, int sw, int g, int t, float xinv = 1.0f, float dx0 = 1.0f,
+                                           float dx1 = 1.0f) {
   using C = Cfg<WT, F16, NW, CH>;
   constexpr int MT = C::MT;
   float da[MT][4];  // block sums (both halves of a block), column j = block j
@@ -266,6 +270,10 @@ __device__ __forceinline__ void chunk_math(float (&acc)[Cfg<WT, F16, NW, CH>::MT
         s0 *= xinv;
         s1 *= xinv;
       }
+      if (QX) {
+        d0 *= dx0;
+        d1 *= dx1;
+      }
       acc[mt][h] = fmaf(d1, s1, fmaf(d0, s0, acc[mt][h]));
     }
   }
@@ -275,13 +283,19 @@ __device__ __forceinline__ void chunk_math(float (&acc)[Cfg<WT, F16, NW, CH>::MT
 // bytes of the hi and lo boxes); a stage that rounds to half as above takes them directly, the
 // others are split by each lane into hi = RN_bf16(x) and lo = RN_bf16(x - hi) in registers
 // (split_bf16_pair, the split kernel's rule), so float32 activations take one launch.
-template <int WT, bool F16, int NW, int CH, bool XS, bool GLU = false, bool XF = false, int RD = 2, bool XH = false>
+// XQ: the runtime's activation-quantized product: each stage's activations (bfloat16, or float32
+// with XF) are quantized by the Q8_0 activation rule in the stage (lanes 4g..4g+3 share block g of
+// a chunk: its largest magnitude by two shuffles), the quants enter the MMA as exact halves, so
+// each block's dot product is the exact integer sum, scaled by d_w * d_x.
+template <int WT, bool F16, int NW, int CH, bool XS, bool GLU = false, bool XF = false, int RD = 2, bool XH = false,
+          bool XQ = false>
 __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_constant__ Maps maps,
                                                                const __grid_constant__ Params p) {
-  using C = Cfg<WT, F16, NW, CH, XS, RD, XH>;
+  using C = Cfg<WT, F16, NW, CH, XS, RD, XH, XQ && XF>;
   constexpr int MT = C::MT;
   static_assert(!GLU || (MT == 2 && !XS), "the gated pair takes two 16-row MMA tiles per warp tile");
-  static_assert(!XF || XS, "float32 activations are split into the hi and lo parts");
+  static_assert(!XF || XS || XQ, "float32 activations are split into the hi and lo parts, or quantized");
+  static_assert(!XQ || (!XS && !XH && !GLU), "the activation-quantized product is a route of its own");
   static_assert(!XH || (!XS && !XF && !GLU), "pre-rounded half activations are a route of their own");
   constexpr bool XP = XS || XH;  // activations with hi and lo parts
   constexpr int TROWS = GLU ? kRows : C::WROWS;  // rows of each matrix per warp tile
@@ -486,6 +500,46 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
                                                                h * 512u, lrow, lsub, sw, g, t, xinv);
             }
           }
+          if constexpr (XQ) {
+            // this lane's 8 values of block g of each chunk (elements 4t..4t+3, 16+4t..16+4t+3),
+            // quantized with the block's scale; the quants as half pairs in the slot's order
+            uint32_t hq[C::kCH][4];
+            float dxb[C::kCH];  // the scale of block g of chunk h
+            float v[C::kCH][8];
+#pragma unroll
+            for (int h = 0; h < C::kCH; ++h) {
+              if (XF) {
+                const uint8_t* xf = xring + cs * C::X_STAGE + h * (kTK * 4) + g * 128 + t * 16;
+                const float4 fa = *reinterpret_cast<const float4*>(xf);
+                const float4 fb = *reinterpret_cast<const float4*>(xf + 64);
+                v[h][0] = fa.x, v[h][1] = fa.y, v[h][2] = fa.z, v[h][3] = fa.w;
+                v[h][4] = fb.x, v[h][5] = fb.y, v[h][6] = fb.z, v[h][7] = fb.w;
+              } else {
+                const uint8_t* xl = xring + cs * C::X_STAGE + h * (kTK * 2) + g * 64 + t * 8;
+                const uint2 a = *reinterpret_cast<const uint2*>(xl);
+                const uint2 b = *reinterpret_cast<const uint2*>(xl + 32);
+                const uint32_t w[4] = {a.x, a.y, b.x, b.y};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  v[h][2 * i] = __uint_as_float(w[i] << 16);
+                  v[h][2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+                }
+              }
+            }
+            act_q8_lane_quarters<C::kCH>(v, hq, dxb);
+#pragma unroll
+            for (int h = 0; h < C::kCH; ++h) sts_u32x4(slot + h * 512, hq[h][0], hq[h][1], hq[h][2], hq[h][3]);
+#pragma unroll
+            for (int h = 0; h < C::kCH; ++h) {
+              // the scales of blocks 2t and 2t+1 (computed by lanes 8t.. and 8t+4..)
+              const float dx0 = __shfl_sync(0xffffffffu, dxb[h], 8 * t);
+              const float dx1 = __shfl_sync(0xffffffffu, dxb[h], 8 * t + 4);
+              chunk_math<WT, F16, NW, CH, true, false, false, true>(acc, qs + h * C::Q_CHUNK, ds + h * C::DCHUNK,
+                                                                    bsrc, h * 512u, lrow, lsub, sw, g, t, 1.0f, dx0,
+                                                                    dx1);
+            }
+            rounded = true;
+          }
           const int stage = cc.c0 + (cc.j << p.lgks);  // chunks CH stage ..
           if constexpr (XH) {
             // half values rounded ahead: the stage's chunks all rounded (chunk scales from device
@@ -520,7 +574,7 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
           uint2 xa[NX], xb[NX];
           uint32_t hx[NX][4];
           bool exact = true;
-          if (!rounded) {
+          if (!XQ && !rounded) {
           if (XF) {
             // float32 activations: elements 4t..4t+3 and 16+4t..16+4t+3 of block g of each chunk,
             // split into the bf16 hi (chunk h) and lo (chunk CH + h) parts
@@ -667,10 +721,11 @@ struct Plan {
   long long waves = 0;
 };
 
-template <int WT, bool F16, int NW, int CH, bool XS, bool GLU = false, bool XF = false, int RD = 2, bool XH = false>
+template <int WT, bool F16, int NW, int CH, bool XS, bool GLU = false, bool XF = false, int RD = 2, bool XH = false,
+          bool XQ = false>
 cudaError_t plan_typed(const MatrixRef* ms, int n, const DeviceInfo& dev, Plan* out) {
-  using C = Cfg<WT, F16, NW, CH, XS, RD, XH>;
-  auto kern = matvec_bdiag_kernel<WT, F16, NW, CH, XS, GLU, XF, RD, XH>;
+  using C = Cfg<WT, F16, NW, CH, XS, RD, XH, XQ && XF>;
+  auto kern = matvec_bdiag_kernel<WT, F16, NW, CH, XS, GLU, XF, RD, XH, XQ>;
   // per device: the shared-memory attribute set and the occupancy known (0 = does not fit)
   static std::mutex mu;
   static bool ready[64] = {};
@@ -728,10 +783,11 @@ cudaError_t plan_typed(const MatrixRef* ms, int n, const DeviceInfo& dev, Plan* 
 // 16 rows of each; act and h as in Params.
 // XH: xs[i] is the problem's area of the half route's buffer: the bfloat16 hi row and lo row
 // (cols each), the half row, then the chunks' inverse scales (cols / 256 floats).
-template <int WT, bool F16, int NW, int CH, bool XS, bool GLU = false, bool XF = false, int RD = 2, bool XH = false>
+template <int WT, bool F16, int NW, int CH, bool XS, bool GLU = false, bool XF = false, int RD = 2, bool XH = false,
+          bool XQ = false>
 cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* const* xs, float* const* ys, int n,
                          bool pdl, const DeviceInfo& dev, cudaStream_t stream, int act = -1, uint16_t* h = nullptr) {
-  using C = Cfg<WT, F16, NW, CH, XS, RD, XH>;
+  using C = Cfg<WT, F16, NW, CH, XS, RD, XH, XQ && XF>;
   constexpr int TROWS = GLU ? kRows : C::WROWS;  // rows of each matrix per warp tile
   if (GLU && (n != 2 || ms[0].rows != ms[1].rows || ms[0].cols != ms[1].cols || h == nullptr))
     return cudaErrorInvalidValue;
@@ -802,7 +858,7 @@ cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* cons
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, matvec_bdiag_kernel<WT, F16, NW, CH, XS, GLU, XF, RD, XH>, maps, p);
+  return cudaLaunchKernelEx(&cfg, matvec_bdiag_kernel<WT, F16, NW, CH, XS, GLU, XF, RD, XH, XQ>, maps, p);
 }
 
 // Q4_0 launches of at least this many weight bytes take one-chunk stages.
@@ -814,7 +870,7 @@ constexpr long long kOneChunkBytes = 32LL << 20;
 // launches of a few tens of MB (the Llama-7B layer's, the 4096 x 4096 product) and on Q8_0.
 // GLU: ms = {w1, w3}, planned as one matrix of twice the rows (the same warp tiles: 16 rows of
 // each per tile); act and h as in launch_typed.
-template <int WT, bool F16, bool XS, bool GLU = false, bool XF = false, bool XH = false>
+template <int WT, bool F16, bool XS, bool GLU = false, bool XF = false, bool XH = false, bool XQ = false>
 cudaError_t launch_best(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
                         const DeviceInfo& dev, cudaStream_t stream, int act = -1, uint16_t* h = nullptr) {
   MatrixRef pair[1];
@@ -833,44 +889,44 @@ cudaError_t launch_best(const MatrixRef* ms, const void* const* xs, float* const
     for (int i = 0; i < pn; ++i) bytes += pm[i].rows * pm[i].cols / 2;
     if (bytes >= kOneChunkBytes) {
       Plan p1;
-      err = plan_typed<WT, F16, 4, 1, XS, GLU, XF, 2, XH>(pm, pn, dev, &p1);
+      err = plan_typed<WT, F16, 4, 1, XS, GLU, XF, 2, XH, XQ>(pm, pn, dev, &p1);
       if (err != cudaSuccess) return err;
       if (p1.cost >= 0 && p1.grid > dev.sm_count)
-        return launch_typed<WT, F16, 4, 1, XS, GLU, XF, 2, XH>(p1, ms, xs, ys, n, pdl, dev, stream, act, h);
+        return launch_typed<WT, F16, 4, 1, XS, GLU, XF, 2, XH, XQ>(p1, ms, xs, ys, n, pdl, dev, stream, act, h);
     }
   }
-  err = plan_typed<WT, F16, 4, 2, XS, GLU, XF, 2, XH>(pm, pn, dev, &p4);
+  err = plan_typed<WT, F16, 4, 2, XS, GLU, XF, 2, XH, XQ>(pm, pn, dev, &p4);
   if (err != cudaSuccess) return err;
   if constexpr (!XS && !GLU) {
     if (p4.cost >= 0 && p4.longest > 1) {
       // 8-warp CTAs with a ring of one: every warp one stage, in one wave, where 4-warp CTAs
       // give each warp two or more stages one after the other
       Plan p1;
-      err = plan_typed<WT, F16, 8, 2, XS, GLU, XF, 1, XH>(pm, pn, dev, &p1);
+      err = plan_typed<WT, F16, 8, 2, XS, GLU, XF, 1, XH, XQ>(pm, pn, dev, &p1);
       if (err != cudaSuccess) return err;
       if (p1.cost >= 0 && p1.longest == 1 && p1.waves == 1 && p1.grid > dev.sm_count)
-        return launch_typed<WT, F16, 8, 2, XS, GLU, XF, 1, XH>(p1, ms, xs, ys, n, pdl, dev, stream, act, h);
+        return launch_typed<WT, F16, 8, 2, XS, GLU, XF, 1, XH, XQ>(p1, ms, xs, ys, n, pdl, dev, stream, act, h);
     }
   }
   if (p4.cost >= 0 && p4.grid > dev.sm_count)
-    return launch_typed<WT, F16, 4, 2, XS, GLU, XF, 2, XH>(p4, ms, xs, ys, n, pdl, dev, stream, act, h);
-  err = plan_typed<WT, F16, 8, 2, XS, GLU, XF, 2, XH>(pm, pn, dev, &p8);
+    return launch_typed<WT, F16, 4, 2, XS, GLU, XF, 2, XH, XQ>(p4, ms, xs, ys, n, pdl, dev, stream, act, h);
+  err = plan_typed<WT, F16, 8, 2, XS, GLU, XF, 2, XH, XQ>(pm, pn, dev, &p8);
   if (err != cudaSuccess) return err;
   if (p8.cost >= 0 && (p4.cost < 0 || p8.cost < p4.cost))
-    return launch_typed<WT, F16, 8, 2, XS, GLU, XF, 2, XH>(p8, ms, xs, ys, n, pdl, dev, stream, act, h);
+    return launch_typed<WT, F16, 8, 2, XS, GLU, XF, 2, XH, XQ>(p8, ms, xs, ys, n, pdl, dev, stream, act, h);
   if (p4.cost < 0) return cudaErrorInvalidConfiguration;
-  return launch_typed<WT, F16, 4, 2, XS, GLU, XF, 2, XH>(p4, ms, xs, ys, n, pdl, dev, stream, act, h);
+  return launch_typed<WT, F16, 4, 2, XS, GLU, XF, 2, XH, XQ>(p4, ms, xs, ys, n, pdl, dev, stream, act, h);
 }
 
-template <bool XS, bool XF = false, bool XH = false>
+template <bool XS, bool XF = false, bool XH = false, bool XQ = false>
 cudaError_t launch_any(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
                        const DeviceInfo& dev, cudaStream_t stream) {
   const MatrixRef& m = ms[0];
   if (m.wtype == QMV_Q4_0)
-    return m.scale_f16 ? launch_best<QMV_Q4_0, true, XS, false, XF, XH>(ms, xs, ys, n, pdl, dev, stream)
-                       : launch_best<QMV_Q4_0, false, XS, false, XF, XH>(ms, xs, ys, n, pdl, dev, stream);
-  return m.scale_f16 ? launch_best<QMV_Q8_0, true, XS, false, XF, XH>(ms, xs, ys, n, pdl, dev, stream)
-                     : launch_best<QMV_Q8_0, false, XS, false, XF, XH>(ms, xs, ys, n, pdl, dev, stream);
+    return m.scale_f16 ? launch_best<QMV_Q4_0, true, XS, false, XF, XH, XQ>(ms, xs, ys, n, pdl, dev, stream)
+                       : launch_best<QMV_Q4_0, false, XS, false, XF, XH, XQ>(ms, xs, ys, n, pdl, dev, stream);
+  return m.scale_f16 ? launch_best<QMV_Q8_0, true, XS, false, XF, XH, XQ>(ms, xs, ys, n, pdl, dev, stream)
+                     : launch_best<QMV_Q8_0, false, XS, false, XF, XH, XQ>(ms, xs, ys, n, pdl, dev, stream);
 }
 
 }  // namespace
@@ -888,6 +944,12 @@ cudaError_t launch_matvec_bdiag_split(const MatrixRef* ms, const void* const* xs
 cudaError_t launch_matvec_bdiag_half(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,
                                      const DeviceInfo& dev, cudaStream_t stream) {
   return launch_any<false, false, true>(ms, xs, ys, n, pdl, dev, stream);
+}
+
+cudaError_t launch_matvec_bdiag_qx(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool x_bf16,
+                                   bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
+  return x_bf16 ? launch_any<false, false, false, true>(ms, xs, ys, n, pdl, dev, stream)
+                : launch_any<false, true, false, true>(ms, xs, ys, n, pdl, dev, stream);
 }
 
 cudaError_t launch_matvec_bdiag_f32in(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool pdl,

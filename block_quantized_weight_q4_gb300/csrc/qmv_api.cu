@@ -23,6 +23,8 @@ constexpr long long kTcMinBytes = 40LL << 20;      // launches of this many weig
                                                    // measured faster at 4..8 vectors)
 constexpr long long kTcMinQ8Weights = 64LL << 20;  // and Q8_0 passes of 2-3 vectors over this many weights
 constexpr long long kTcWideMinBytes = 8LL << 20;   // passes of 9..16 vectors in one decode_tc launch
+constexpr long long kQxBdiagMaxBytes = 96LL << 20;  // one-vector activation-quantized groups below this
+                                                    // size take the block-diagonal kernel
 constexpr long long kF32SplitMinWeights = 256LL << 10;  // one f32 vector: split hi/lo from this many weights
 // one f32 vector: split in the product's own activation stage (one launch) below this many
 // weight bytes; above it the split kernel runs once per column and the product reads its parts
@@ -502,6 +504,23 @@ int qmv_matvec_qx_grouped(int wtype, int scale_dtype, int x_dtype, int batch, co
   if (batch == 0) return QMV_OK;
   DeviceInfo dev;
   if (current_device_info(&dev) != cudaSuccess) return QMV_E_CUDA;
+  // one vector, every problem's cols a multiple of 256, under 96 MB of weights: the
+  // block-diagonal kernel quantizes the activations in its stages and takes the block dots on
+  // the tensor core (exact integer sums in half precision); else the fused dp4a kernel (whose
+  // quantizing prologue is paid once per CTA: on a 151 MB launch it measured 28.4 against
+  // 31.7 us, on the layer's launches of 9.4 to 51 MB 3 to 30% slower)
+  bool bdiag = batch == 1;
+  long long qx_bytes = 0;
+  for (int i = 0; i < n && bdiag; ++i) {
+    bdiag = matvec_mma_supported(ms[i]);
+    qx_bytes += ms[i].rows * ms[i].cols / 32 * ((wtype == QMV_Q4_0 ? 16 : 32) + (scale_dtype == QMV_SCALE_F16 ? 2 : 4));
+  }
+  if (qx_bytes >= kQxBdiagMaxBytes) bdiag = false;
+  if (bdiag)
+    return launch_matvec_bdiag_qx(ms, xs, ys, n, x_dtype == QMV_X_BF16, (flags & QMV_FLAG_OVERLAP) != 0, dev,
+                                  stream) == cudaSuccess
+               ? QMV_OK
+               : QMV_E_CUDA;
   return launch_matvec_qx_fused(ms, xs, ys, n, x_dtype == QMV_X_BF16, batch, (flags & QMV_FLAG_OVERLAP) != 0, dev,
                                 stream) == cudaSuccess
              ? QMV_OK

@@ -403,6 +403,59 @@ __device__ __forceinline__ float act_q8_block(const float (&x)[32], uint32_t (&w
   return d;
 }
 
+// The same rule on NCH blocks at once, each held by four lanes (lanes 4g .. 4g+3 of the warp hold
+// block g of chunk h, 8 values each, v[h]): each block's amax by two xor shuffles (the same
+// maximum as act_q8_block's); the divisions 127 / amax and amax / 127 of all NCH blocks in one
+// pass over the four lanes (lane 4g + 2h + r divides for chunk h, r = 0: d, r = 1: 1 / d), then
+// each value's quant by the same float32 steps, returned as IEEE half pairs (exact: |q| <= 127),
+// hq[h][i] = (q(v[h][2i]) low, q(v[h][2i+1]) high), and d[h] the block's scale.
+template <int NCH>
+__device__ __forceinline__ void act_q8_lane_quarters(const float (&v)[NCH][8], uint32_t (&hq)[NCH][4],
+                                                     float (&d)[NCH]) {
+  static_assert(NCH == 1 || NCH == 2, "one or two chunks");
+  const int lane = threadIdx.x & 31;
+  float amax[NCH];
+#pragma unroll
+  for (int h = 0; h < NCH; ++h) {
+    float m = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float a = fabsf(v[h][e]);
+      if (a > m) m = a;
+    }
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+      const float b = __shfl_xor_sync(0xffffffffu, m, o);
+      if (b > m) m = b;
+    }
+    amax[h] = m;
+  }
+  const int r = lane & 1;
+  const float am = (NCH == 2 && (lane & 2)) ? amax[NCH - 1] : amax[0];
+  // the zero block (amax below 1e-30) has d = 0 and 1 / d taken as 0
+  const float num = r ? 127.0f : am, den = r ? am : 127.0f;
+  const float quot = am < 1e-30f ? 0.f : __fdiv_rn(num, den);
+  const int base = lane & ~3;
+#pragma unroll
+  for (int h = 0; h < NCH; ++h) {
+    d[h] = __shfl_sync(0xffffffffu, quot, base + 2 * h);
+    const float inv = __shfl_sync(0xffffffffu, quot, base + 2 * h + 1);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float q[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        // the rule's clamp to +-127 never acts here: |x| <= amax gives |x * inv| <= 127 (1 + 2^-23)
+        // and a sum below 128 before the truncation; a value that is not finite gives NaN, whose
+        // conversion is 0, as in act_q8_block
+        const float xe = v[h][2 * i + j];
+        q[j] = (float)(int)__fadd_rn(__fmul_rn(xe, inv), copysignf(0.5f, xe));
+      }
+      asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(hq[h][i]) : "f"(q[1]), "f"(q[0]));
+    }
+  }
+}
+
 // 32 activations (float32, or bfloat16 widened exactly) starting at element `first` of x.
 template <bool BF16>
 __device__ __forceinline__ void load_act_block(const void* __restrict__ x, long long first, float (&v)[32]) {

@@ -113,6 +113,12 @@ cudaError_t launch_matvec_bdiag_split(const MatrixRef* ms, const void* const* xs
 bool matvec_bdiag_glu_supported(const MatrixRef& w1, const MatrixRef& w3);
 cudaError_t launch_matvec_bdiag_glu(const MatrixRef& w1, const MatrixRef& w3, const void* x, int act, uint16_t* h,
                                     bool pdl, const DeviceInfo& dev, cudaStream_t stream);
+// The runtime's activation-quantized product (the same quants, scales and float32 steps as
+// launch_matvec_qx after launch_quantize_x) for one activation vector per problem (bfloat16, or
+// float32 16-byte aligned), quantized in the kernel's activation stage; every problem
+// matvec_mma_supported().
+cudaError_t launch_matvec_bdiag_qx(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool x_bf16,
+                                   bool pdl, const DeviceInfo& dev, cudaStream_t stream);
 // The same problems with the activations rounded to half ahead of the product: xs[i] is the
 // problem's area written by the half route's split (launch_matvec_bdiag_f32): the bfloat16 hi and
 // lo rows, the half row and the chunks' inverse scales (0: that chunk takes hi and lo).

@@ -357,10 +357,15 @@ int qmv_matvec_qx(int wtype, int scale_dtype, int64_t rows, int64_t cols, const 
 /* The activation-quantized product with the activation quantizer inside it, for several
  * products in one launch: for each problem, y = qmv_matvec_qx(W, qmv_quantize_x(x)) -- the same
  * activation quants and scales (the runtime's Q8_0 / f32-scale rule), the same integer block dots
- * and float32 steps -- without the separate quantizer launch or the intermediate image: each CTA
- * quantizes its problem's activations into shared memory (a few KB per vector) and reads them
- * from there.  All n problems share wtype, scale_dtype, x_dtype and batch; each has its own rows,
- * cols, W, x and y (problems of one layer that read the same activations: pass the same x).
+ * and float32 steps -- without the separate quantizer launch or the intermediate image.  One
+ * vector (batch 1) in groups under 96 MB of weights with every problem's cols a multiple of 256
+ * runs the block-diagonal kernel: each warp quantizes the 256-column chunks it streams (four
+ * lanes to a block of 32), and the quants and the levels enter the tensor core as IEEE halves,
+ * whose block dot products are the exact integer sums.  Every other batch and group (the larger
+ * groups measured faster there) runs the dp4a kernel, whose CTAs each quantize their problem's
+ * activations into shared memory (a few KB per vector) and read them from there.  All n
+ * problems share wtype, scale_dtype, x_dtype and batch; each has its own rows, cols, W, x and y
+ * (problems of one layer that read the same activations: pass the same x).
  *   x_dtype : QMV_X_F32 or QMV_X_BF16 (QMV_E_FORMAT otherwise); x : device, batch x cols,
  *             row-major, 16-byte aligned.  y : device, batch x rows float32, 4-byte aligned.
  *   min(batch, 8) * (the largest cols of the group) <= QMV_QX_MAX_VEC_COLS, else QMV_E_SHAPE

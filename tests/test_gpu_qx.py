@@ -238,6 +238,32 @@ def test_matvec_qx_grouped_exact_case(qmv, wt, batch):
         assert np.array_equal(y.astype(np.float64), y_ref), f"exact grouped qx {wt} b{batch} {m.rows}x{m.cols}"
 
 
+@pytest.mark.parametrize("wt", [1, 2])
+@pytest.mark.parametrize("bf16", [False, True])
+def test_matvec_qx_grouped_one_vector_exact_case(qmv, wt, bf16):
+    # one vector, cols multiples of 256 (the block-diagonal kernel, quants in its stages): the
+    # exact case above (scales 2^-6 and 2^-4, integer block sums) must match bit for bit, with
+    # zero blocks and blocks whose largest magnitude sits in any of the four lanes
+    rng = np.random.default_rng(120 + wt + bf16)
+    mats, xs = [], []
+    for rows, cols in [(9, 256), (40, 512), (300, 512)]:  # block sums stay exact in float32
+        if wt == 1:
+            q = rng.integers(-127, 128, rows * cols).astype(np.int8).view(np.uint8)
+        else:
+            q = rng.integers(0, 256, rows * cols // 2).astype(np.uint8)
+        d = np.full(rows * cols // 32, 2.0 ** -6, np.float32).view(np.uint32)
+        W = inputs.assemble(wt, 0, rows, cols, q, d)
+        mats.append(inputs.Matrix(wt, 0, rows, cols, W, q, d.reshape(rows, cols // 32)))
+        k = rng.integers(-127, 128, (1, cols // 32, 32))
+        k[0, np.arange(cols // 32), rng.integers(0, 32, cols // 32)] = 127 * rng.choice([-1, 1], cols // 32)
+        k[0, ::7] = 0  # zero blocks
+        xs.append((k * 2.0 ** -4).reshape(1, cols).astype(np.float32))
+    ys = gpu_qx_grouped(qmv, wt, 0, mats, xs, bf16)
+    for m, x, y in zip(mats, xs, ys):
+        y_ref, _ = oracle_qx(m, x, bf16)
+        assert np.array_equal(y.astype(np.float64), y_ref), f"exact one-vector qx {wt} {m.rows}x{m.cols}"
+
+
 @pytest.mark.parametrize("batch", [1, 8])
 def test_matvec_qx_grouped_llama7b_groups_sampled(qmv, batch):
     # the layer's groups as the layer step runs them ({wq,wk,wv} on one x, {w1,w3} on one x,
