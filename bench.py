@@ -63,6 +63,7 @@ def parse():
                     help="time one product shape alone (WTYPE 1 = Q8_0, 2 = Q4_0) instead of the workload")
     ap.add_argument("--x-f32", action="store_true", help="--case: float32 activations (default bfloat16)")
     ap.add_argument("--bf16-weights", action="store_true", help="--case: the prefill kernel's bf16-weights variant")
+    ap.add_argument("--qx", action="store_true", help="--case: the activation-quantized product (qmv_matvec_qx_grouped)")
     ap.add_argument("--case-calls", type=int, default=20, help="--case: calls per timed CUDA graph")
     ap.add_argument("--case-copies", type=int, default=4, help="--case: rotating copies of the matrix")
     return ap.parse_args()
@@ -808,7 +809,10 @@ def run_case(args):
     y = torch.empty((batch, rows), device="cuda")
 
     def call(i):
-        qmv.matvec_grouped(wt, sf, [(rows, cols, Ws[i % ncopy], xd, y)], bf16_weights=args.bf16_weights)
+        if args.qx:
+            qmv.matvec_qx_grouped(wt, sf, [(rows, cols, Ws[i % ncopy], xd, y)])
+        else:
+            qmv.matvec_grouped(wt, sf, [(rows, cols, Ws[i % ncopy], xd, y)], bf16_weights=args.bf16_weights)
 
     # eager calls on the stream that is captured below: a stream's first call creates the
     # workspaces its kernels use (never while it is being captured)
@@ -819,6 +823,7 @@ def run_case(args):
     torch.cuda.synchronize()
     out = {"case": {"rows": rows, "cols": cols, "wtype": wt, "scale_f16": sf, "batch": batch,
                     "x_dtype": "f32" if args.x_f32 else "bf16", "bf16_weights": bool(args.bf16_weights),
+                    "activation_quantized": bool(args.qx),
                     "copies": ncopy}}
     if args.case_calls > 0:
         g = torch.cuda.CUDAGraph()
