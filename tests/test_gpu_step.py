@@ -108,3 +108,57 @@ def test_step_of_copies_only(qmv):
         assert torch.equal(dst, src)
     with pytest.raises(ValueError):
         step.run()                                   # closed on leaving the block
+
+
+def test_step_with_per_group_copies_and_a_chained_group(qmv):
+    # per-group copies, as a decode step hands each group its input and takes each result back:
+    # x0 and x2 come from the host, group 1 reads group 0's result y0 as float32 activations,
+    # and y0, y2, y1 go back to the host; every run must give the bits of the same calls made
+    # eagerly in order
+    import torch
+    cols = 4096
+    m0 = inputs.make_matrix(2, 1, 4096, cols, seed=230)
+    m1 = inputs.make_matrix(2, 1, 1024, 4096, seed=231)
+    m2 = inputs.make_matrix(1, 1, 2048, cols, seed=232)
+    W0, W1, W2 = dev_u8(m0.W), dev_u8(m1.W), dev_u8(m2.W)
+    x0h = torch.empty((1, cols), dtype=torch.bfloat16).pin_memory()
+    x2h = torch.empty((1, cols), dtype=torch.bfloat16).pin_memory()
+    x0d, x2d = torch.empty_like(x0h, device="cuda"), torch.empty_like(x2h, device="cuda")
+    y0 = torch.empty((1, 4096), device="cuda")
+    y1 = torch.empty((1, 1024), device="cuda")
+    y2 = torch.empty((1, 2048), device="cuda")
+    y0h, y1h, y2h = (torch.empty(t.shape).pin_memory() for t in (y0, y1, y2))
+    groups = [(2, 1, [(4096, cols, W0, x0d, y0)], True),
+              (2, 1, [(1024, 4096, W1, y0, y1)], True),
+              (1, 1, [(2048, cols, W2, x2d, y2)], True)]
+    rng = np.random.default_rng(233)
+
+    def new_inputs():
+        xs = [inputs.bf16_codes(rng.standard_normal((1, cols))) for _ in range(2)]
+        for h, x in zip((x0h, x2h), xs):
+            h.view(torch.int16).copy_(torch.from_numpy(x.view(np.int16)))
+        return xs
+
+    new_inputs()
+    step = qmv.Step(groups, before=[(x0d, x0h), (x2d, x2h)], after=[(y0h, y0), (y2h, y2), (y1h, y1)])
+    try:
+        for it in range(4):
+            x0, x2 = new_inputs()
+            step.run()
+            torch.cuda.current_stream().synchronize()
+            got = [t.clone().numpy() for t in (y0h, y1h, y2h)]
+            e0 = torch.empty_like(y0)
+            e1 = torch.empty_like(y1)
+            e2 = torch.empty_like(y2)
+            qmv.matvec_grouped(2, 1, [(4096, cols, W0, to_dev_x(x0), e0)], overlap=True)
+            qmv.matvec_grouped(2, 1, [(1024, 4096, W1, e0, e1)], overlap=True)
+            qmv.matvec_grouped(1, 1, [(2048, cols, W2, to_dev_x(x2), e2)], overlap=True)
+            torch.cuda.synchronize()
+            for g, e, what in zip(got, (e0, e1, e2), ("y0", "y1", "y2")):
+                assert_bits_equal(g, e.cpu().numpy(), f"run {it} {what}")
+            y_ref, absref = oracle.matvec(m0.W, 2, 1, 4096, cols, x0)
+            check_product(got[0], y_ref, absref, what=f"run {it} y0")
+            y_ref, absref = oracle.matvec(m1.W, 2, 1, 1024, 4096, got[0].astype(np.float32))
+            check_product(got[1], y_ref, absref, what=f"run {it} y1")
+    finally:
+        step.close()
