@@ -37,6 +37,11 @@
 //     written by the preceding kernel.
 // f32 activations are split x = hi + lo (two bfloat16s, hi = RN(x)) and take two MMAs each,
 // which keeps 16 significant bits of x.
+// XQ: the runtime's activation-quantized product on an activation image of Q8_0 quants with a
+// float32 scale per block (qmv_quantize_x's bytes): the stage's activation boxes are the quants
+// (batch x 256 bytes) and the scales (batch x 8 floats); quants and levels enter the MMA as
+// exact IEEE halves (m16n8k16 f16), so each block's dot product is the exact integer sum, and
+// acc += (d_w * d_x) * sum, the float32 steps of the dp4a product.
 #include <cstring>
 #include <mutex>
 
@@ -54,7 +59,7 @@ constexpr int kBox = 128;            // q box inner extent in bytes (the 128-byt
 constexpr int kMaxBatch = 8;         // activation vectors per pass (the MMA's N)
 constexpr int kMaxProblems = 8;      // problems per grouped launch
 
-template <int WT, bool F16, bool XBF16, int NW>
+template <int WT, bool F16, bool XBF16, int NW, bool XQ = false>
 struct Cfg {
   static constexpr int kWarps = NW;
   static constexpr int MT = (WT == QMV_Q4_0) ? 2 : 1;           // 16-row MMA tiles per warp tile
@@ -65,7 +70,8 @@ struct Cfg {
   static constexpr int QROW = NQBOX * kBox;                        // q bytes per row per stage
   static constexpr int DROW = kBlocksPerStage * (F16 ? 2 : 4);    // scale bytes per row per stage
   static constexpr int D_STAGE = WROWS * DROW;                     // multiple of 128
-  static constexpr int XROW = kTK * (XBF16 ? 2 : 4);              // activation bytes per vector per stage
+  static constexpr int XROW = XQ ? kTK : kTK * (XBF16 ? 2 : 4);    // activation bytes per vector per stage
+  static constexpr int XDROW = XQ ? kBlocksPerStage * 4 : 0;       // XQ: activation scale bytes per vector
   static constexpr int S = NW >= 16 ? 2 : 3;                       // ring depth (16 warps: 2, to fit)
   static constexpr int Q_WARP = S * Q_STAGE;
   static constexpr int D_WARP = S * D_STAGE;
@@ -78,7 +84,9 @@ struct Cfg {
   static constexpr int OFF_RED = OFF_ZERO + ZERO_BYTES;
   static constexpr int OFF_BAR = OFF_RED + RED_FLOATS * 4;
   static constexpr int OFF_X = OFF_BAR + ((kWarps * S * 8 + 127) / 128) * 128;
-  static int smem_bytes(int batch) { return 1024 + OFF_X + kWarps * S * batch * XROW; }
+  // activation bytes of one stage (quants then scales with XQ), a multiple of 128 (TMA destinations)
+  static __host__ __device__ int x_stage(int batch) { return (batch * (XROW + XDROW) + 127) / 128 * 128; }
+  static int smem_bytes(int batch) { return 1024 + OFF_X + kWarps * S * x_stage(batch); }
 };
 
 struct Problem {
@@ -103,6 +111,7 @@ struct Maps {  // per problem: q (128-byte swizzle), d, and activation tensor ma
   CUtensorMap q[kMaxProblems];
   CUtensorMap d[kMaxProblems];
   CUtensorMap x[kMaxProblems];
+  CUtensorMap xd[kMaxProblems];  // XQ: the activation scales
 };
 
 // Position of a warp in its stream of stages: item (global index), its problem and warp
@@ -125,10 +134,10 @@ __device__ __forceinline__ void cursor_load(Cursor& c, const Params& p, int tile
   c.j = 0;
 }
 
-template <int WT, bool F16, bool XBF16, int NW>
+template <int WT, bool F16, bool XBF16, int NW, bool XQ = false>
 __global__ void __launch_bounds__(NW * 32) matvec_mma_kernel(const __grid_constant__ Maps maps,
                                                              const __grid_constant__ Params p) {
-  using C = Cfg<WT, F16, XBF16, NW>;
+  using C = Cfg<WT, F16, XBF16, NW, XQ>;
   constexpr int kWarps = NW;
   constexpr int MT = C::MT;
   extern __shared__ uint8_t smem_raw[];
@@ -140,7 +149,7 @@ __global__ void __launch_bounds__(NW * 32) matvec_mma_kernel(const __grid_consta
   const int g = lane >> 2;
   const int t = lane & 3;
 
-  const int x_stage = p.batch * C::XROW;
+  const int x_stage = C::x_stage(p.batch);
   uint8_t* qring = smem + warp * C::Q_WARP;
   uint8_t* dring = smem + C::OFF_D + warp * C::D_WARP;
   uint8_t* xring = smem + C::OFF_X + warp * C::S * x_stage;
@@ -151,7 +160,8 @@ __global__ void __launch_bounds__(NW * 32) matvec_mma_kernel(const __grid_consta
   const int tiles_per_item = kWarps / p.ks;
   const int tile_local = warp / p.ks;
   const int kslice = warp % p.ks;
-  const uint32_t stage_tx = (uint32_t)(C::Q_STAGE + C::D_STAGE + x_stage);
+  // bytes the copies of one stage deliver (the activation area may be padded beyond them)
+  const uint32_t stage_tx = (uint32_t)(C::Q_STAGE + C::D_STAGE + p.batch * (C::XROW + C::XDROW));
 
   if (threadIdx.x < C::ZERO_BYTES / 4) reinterpret_cast<uint32_t*>(zero)[threadIdx.x] = 0u;
   if (lane == 0) {
@@ -181,7 +191,12 @@ __global__ void __launch_bounds__(NW * 32) matvec_mma_kernel(const __grid_consta
                       pc.tile * C::WROWS, &bars[ps], pol_stream);
         tma_load_2d(dring + ps * C::D_STAGE, &maps.d[pc.prob], c * C::DROW, pc.tile * C::WROWS, &bars[ps],
                     pol_stream);
-        if (with_x) tma_load_2d_keep(xring + ps * x_stage, &maps.x[pc.prob], c * kTK, 0, &bars[ps]);
+        if (with_x) {
+          tma_load_2d_keep(xring + ps * x_stage, &maps.x[pc.prob], c * kTK, 0, &bars[ps]);
+          if (XQ)
+            tma_load_2d_keep(xring + ps * x_stage + p.batch * C::XROW, &maps.xd[pc.prob], c * kBlocksPerStage, 0,
+                             &bars[ps]);
+        }
       } else {
         mbar_arrive(&bars[ps]);  // a tile past the end of its problem: complete the phase, no data
       }
@@ -213,7 +228,12 @@ __global__ void __launch_bounds__(NW * 32) matvec_mma_kernel(const __grid_consta
   if (threadIdx.x == 0) griddep_launch_dependents();
   if (lane == 0) {
     for (int i = 0; i < pre; ++i)
-      if (pre_valid[i]) tma_load_2d_keep(xring + i * x_stage, &maps.x[pre_prob[i]], pre_c[i] * kTK, 0, &bars[i]);
+      if (pre_valid[i]) {
+        tma_load_2d_keep(xring + i * x_stage, &maps.x[pre_prob[i]], pre_c[i] * kTK, 0, &bars[i]);
+        if (XQ)
+          tma_load_2d_keep(xring + i * x_stage + p.batch * C::XROW, &maps.xd[pre_prob[i]], pre_c[i] * kBlocksPerStage,
+                           0, &bars[i]);
+      }
   }
 
   // ldmatrix: lane supplies row (lane & 7) + 8 * (matrix & 1), 16-byte chunk (matrix >> 1)
@@ -222,7 +242,7 @@ __global__ void __launch_bounds__(NW * 32) matvec_mma_kernel(const __grid_consta
   const int lsub = lm >> 1;
   const int sw = lrow & 7;  // 128-byte swizzle: physical chunk = logical chunk ^ (row & 7)
   // B fragment source of this lane: vector g of the stage's activation box, or the zero area
-  constexpr int XESZ = XBF16 ? 2 : 4;
+  constexpr int XESZ = XQ ? 1 : XBF16 ? 2 : 4;
   const bool xlive = g < p.batch;
   const uint32_t xblk = xlive ? 32 * XESZ : 0;   // byte step per block
   const uint32_t xhalf = xlive ? 16 * XESZ : 0;  // byte step to elements 16..31
@@ -284,6 +304,19 @@ __global__ void __launch_bounds__(NW * 32) matvec_mma_kernel(const __grid_consta
               }
             }
           }
+          // XQ: the activation scales of blocks 2bp, 2bp+1 for vectors 2t, 2t+1 (the fragment's
+          // columns of this thread; 0 past the batch)
+          float dxb[2][2];
+          if (XQ) {
+            const float* xdq = reinterpret_cast<const float*>(xring + cs * x_stage + p.batch * C::XROW);
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb)
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                const int n = 2 * t + j;
+                dxb[hb][j] = n < p.batch ? xdq[n * kBlocksPerStage + 2 * bp + hb] : 0.f;
+              }
+          }
 #pragma unroll
           for (int hb = 0; hb < 2; ++hb) {
             const int k = 2 * bp + hb;
@@ -292,7 +325,9 @@ __global__ void __launch_bounds__(NW * 32) matvec_mma_kernel(const __grid_consta
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const uint32_t a = xs + k * xblk + h * xhalf;
-              if (XBF16) {
+              if (XQ) {
+                q8_word_to_f16_levels(lds_u32(a), xh[h][0], xh[h][1]);  // quants as exact halves
+              } else if (XBF16) {
                 lds_u32x2(a, xh[h][0], xh[h][1]);
               } else {
                 float v[4];
@@ -309,19 +344,33 @@ __global__ void __launch_bounds__(NW * 32) matvec_mma_kernel(const __grid_consta
 #pragma unroll
               for (int mt = 0; mt < MT; ++mt) {
                 uint32_t g01, g23, gh01, gh23, h01, h23, hh01, hh23;
-                q4_word_to_bf16_levels(w[mt][2 * hb], g01, g23, gh01, gh23);      // row g
-                q4_word_to_bf16_levels(w[mt][2 * hb + 1], h01, h23, hh01, hh23);  // row g + 8
                 float c[4] = {0.f, 0.f, 0.f, 0.f};
-                mma_bf16_16816(c, g01, h01, g23, h23, xh[0][0], xh[0][1], c);      // elements 0..15
-                mma_bf16_16816(c, gh01, hh01, gh23, hh23, xh[1][0], xh[1][1], c);  // elements 16..31
-                if (!XBF16) {
-                  mma_bf16_16816(c, g01, h01, g23, h23, xl[0][0], xl[0][1], c);
-                  mma_bf16_16816(c, gh01, hh01, gh23, hh23, xl[1][0], xl[1][1], c);
+                if (XQ) {
+                  q4_word_to_f16_levels(w[mt][2 * hb], g01, g23, gh01, gh23);      // row g
+                  q4_word_to_f16_levels(w[mt][2 * hb + 1], h01, h23, hh01, hh23);  // row g + 8
+                  mma_f16_16816(c, g01, h01, g23, h23, xh[0][0], xh[0][1], c);      // elements 0..15
+                  mma_f16_16816(c, gh01, hh01, gh23, hh23, xh[1][0], xh[1][1], c);  // elements 16..31
+                } else {
+                  q4_word_to_bf16_levels(w[mt][2 * hb], g01, g23, gh01, gh23);      // row g
+                  q4_word_to_bf16_levels(w[mt][2 * hb + 1], h01, h23, hh01, hh23);  // row g + 8
+                  mma_bf16_16816(c, g01, h01, g23, h23, xh[0][0], xh[0][1], c);      // elements 0..15
+                  mma_bf16_16816(c, gh01, hh01, gh23, hh23, xh[1][0], xh[1][1], c);  // elements 16..31
+                  if (!XBF16) {
+                    mma_bf16_16816(c, g01, h01, g23, h23, xl[0][0], xl[0][1], c);
+                    mma_bf16_16816(c, gh01, hh01, gh23, hh23, xl[1][0], xl[1][1], c);
+                  }
                 }
-                acc[mt][0] = fmaf(dsc[mt][0][hb], c[0], acc[mt][0]);
-                acc[mt][1] = fmaf(dsc[mt][0][hb], c[1], acc[mt][1]);
-                acc[mt][2] = fmaf(dsc[mt][1][hb], c[2], acc[mt][2]);
-                acc[mt][3] = fmaf(dsc[mt][1][hb], c[3], acc[mt][3]);
+                if (XQ) {
+                  acc[mt][0] = fmaf(dsc[mt][0][hb] * dxb[hb][0], c[0], acc[mt][0]);
+                  acc[mt][1] = fmaf(dsc[mt][0][hb] * dxb[hb][1], c[1], acc[mt][1]);
+                  acc[mt][2] = fmaf(dsc[mt][1][hb] * dxb[hb][0], c[2], acc[mt][2]);
+                  acc[mt][3] = fmaf(dsc[mt][1][hb] * dxb[hb][1], c[3], acc[mt][3]);
+                } else {
+                  acc[mt][0] = fmaf(dsc[mt][0][hb], c[0], acc[mt][0]);
+                  acc[mt][1] = fmaf(dsc[mt][0][hb], c[1], acc[mt][1]);
+                  acc[mt][2] = fmaf(dsc[mt][1][hb], c[2], acc[mt][2]);
+                  acc[mt][3] = fmaf(dsc[mt][1][hb], c[3], acc[mt][3]);
+                }
               }
             } else {
               // Q8_0: block k = chunks 2k, 2k+1 of the stage (box k / 4)
@@ -329,21 +378,34 @@ __global__ void __launch_bounds__(NW * 32) matvec_mma_kernel(const __grid_consta
               const int chunk = 2 * (k & 3) + lsub;
               ldmatrix_x4(q[0], q[1], q[2], q[3], qs + (k >> 2) * C::Q_BOX_BYTES + lrow * kBox + ((chunk ^ sw) << 4));
               uint32_t g0a, g0b, h0a, h0b, g1a, g1b, h1a, h1b;
-              q8_word_to_bf16_levels(q[0], g0a, g0b);
-              q8_word_to_bf16_levels(q[1], h0a, h0b);
-              q8_word_to_bf16_levels(q[2], g1a, g1b);
-              q8_word_to_bf16_levels(q[3], h1a, h1b);
               float c[4] = {0.f, 0.f, 0.f, 0.f};
-              mma_bf16_16816(c, g0a, h0a, g0b, h0b, xh[0][0], xh[0][1], c);
-              mma_bf16_16816(c, g1a, h1a, g1b, h1b, xh[1][0], xh[1][1], c);
-              if (!XBF16) {
-                mma_bf16_16816(c, g0a, h0a, g0b, h0b, xl[0][0], xl[0][1], c);
-                mma_bf16_16816(c, g1a, h1a, g1b, h1b, xl[1][0], xl[1][1], c);
+              if (XQ) {
+                q8_word_to_f16_levels(q[0], g0a, g0b);
+                q8_word_to_f16_levels(q[1], h0a, h0b);
+                q8_word_to_f16_levels(q[2], g1a, g1b);
+                q8_word_to_f16_levels(q[3], h1a, h1b);
+                mma_f16_16816(c, g0a, h0a, g0b, h0b, xh[0][0], xh[0][1], c);
+                mma_f16_16816(c, g1a, h1a, g1b, h1b, xh[1][0], xh[1][1], c);
+                acc[0][0] = fmaf(dsc[0][0][hb] * dxb[hb][0], c[0], acc[0][0]);
+                acc[0][1] = fmaf(dsc[0][0][hb] * dxb[hb][1], c[1], acc[0][1]);
+                acc[0][2] = fmaf(dsc[0][1][hb] * dxb[hb][0], c[2], acc[0][2]);
+                acc[0][3] = fmaf(dsc[0][1][hb] * dxb[hb][1], c[3], acc[0][3]);
+              } else {
+                q8_word_to_bf16_levels(q[0], g0a, g0b);
+                q8_word_to_bf16_levels(q[1], h0a, h0b);
+                q8_word_to_bf16_levels(q[2], g1a, g1b);
+                q8_word_to_bf16_levels(q[3], h1a, h1b);
+                mma_bf16_16816(c, g0a, h0a, g0b, h0b, xh[0][0], xh[0][1], c);
+                mma_bf16_16816(c, g1a, h1a, g1b, h1b, xh[1][0], xh[1][1], c);
+                if (!XBF16) {
+                  mma_bf16_16816(c, g0a, h0a, g0b, h0b, xl[0][0], xl[0][1], c);
+                  mma_bf16_16816(c, g1a, h1a, g1b, h1b, xl[1][0], xl[1][1], c);
+                }
+                acc[0][0] = fmaf(dsc[0][0][hb], c[0], acc[0][0]);
+                acc[0][1] = fmaf(dsc[0][0][hb], c[1], acc[0][1]);
+                acc[0][2] = fmaf(dsc[0][1][hb], c[2], acc[0][2]);
+                acc[0][3] = fmaf(dsc[0][1][hb], c[3], acc[0][3]);
               }
-              acc[0][0] = fmaf(dsc[0][0][hb], c[0], acc[0][0]);
-              acc[0][1] = fmaf(dsc[0][0][hb], c[1], acc[0][1]);
-              acc[0][2] = fmaf(dsc[0][1][hb], c[2], acc[0][2]);
-              acc[0][3] = fmaf(dsc[0][1][hb], c[3], acc[0][3]);
             }
           }
         }
@@ -414,10 +476,10 @@ struct Plan {
   long cost = -1;
 };
 
-template <int WT, bool F16, bool XBF16, int NW>
+template <int WT, bool F16, bool XBF16, int NW, bool XQ = false>
 cudaError_t plan_typed(const MatrixRef* ms, int n, int batch, const DeviceInfo& dev, Plan* out) {
-  using C = Cfg<WT, F16, XBF16, NW>;
-  auto kern = matvec_mma_kernel<WT, F16, XBF16, NW>;
+  using C = Cfg<WT, F16, XBF16, NW, XQ>;
+  auto kern = matvec_mma_kernel<WT, F16, XBF16, NW, XQ>;
   // per device: the shared-memory limit raised as far as the batches seen need; per device
   // and batch: occupancy known (0 = this warps-per-CTA choice does not fit)
   static std::mutex mu;
@@ -476,10 +538,13 @@ cudaError_t plan_typed(const MatrixRef* ms, int n, int batch, const DeviceInfo& 
   return cudaSuccess;
 }
 
-template <int WT, bool F16, bool XBF16, int NW>
+// XQ: xs[i] is the problem's activation quants (batch x cols bytes), xds[i] their scales
+// (batch x cols / 32 floats).
+template <int WT, bool F16, bool XBF16, int NW, bool XQ = false>
 cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* const* xs, float* const* ys, int n,
-                         int batch, bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
-  using C = Cfg<WT, F16, XBF16, NW>;
+                         int batch, bool pdl, const DeviceInfo& dev, cudaStream_t stream,
+                         const float* const* xds = nullptr) {
+  using C = Cfg<WT, F16, XBF16, NW, XQ>;
   Params p{};
   p.nprob = n;
   p.batch = batch;
@@ -511,6 +576,16 @@ cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* cons
     err = encode_tmap_2d(&maps.d[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, m.d, drow, (uint64_t)m.rows, drow, C::DROW,
                          C::WROWS, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (err != cudaSuccess) return err;
+    if (XQ) {
+      err = encode_tmap_2d(&maps.x[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, xs[i], (uint64_t)m.cols, (uint64_t)batch,
+                           (uint64_t)m.cols, kTK, batch, CU_TENSOR_MAP_SWIZZLE_NONE);
+      if (err != cudaSuccess) return err;
+      err = encode_tmap_2d(&maps.xd[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, xds[i], (uint64_t)(m.cols / 32),
+                           (uint64_t)batch, (uint64_t)(m.cols / 32) * 4, kBlocksPerStage, batch,
+                           CU_TENSOR_MAP_SWIZZLE_NONE);
+      if (err != cudaSuccess) return err;
+      continue;
+    }
     err = encode_tmap_2d(&maps.x[i], XBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, xs[i],
                          (uint64_t)m.cols, (uint64_t)batch, (uint64_t)m.cols * (XBF16 ? 2 : 4), kTK, batch,
                          CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -527,30 +602,30 @@ cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* cons
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, matvec_mma_kernel<WT, F16, XBF16, NW>, maps, p);
+  return cudaLaunchKernelEx(&cfg, matvec_mma_kernel<WT, F16, XBF16, NW, XQ>, maps, p);
 }
 
 // 4 warps per CTA; when that leaves SMs without a CTA (a launch with few tiles), 8 or 16
 // warps per CTA instead if the plan estimates them shorter (ties to fewer warps).  With
 // every SM busy, more warps per CTA measured slower (they share the SM's issue slots).
-template <int WT, bool F16, bool XBF16>
+template <int WT, bool F16, bool XBF16, bool XQ = false>
 cudaError_t launch_best(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, int batch, bool pdl,
-                        const DeviceInfo& dev, cudaStream_t stream) {
+                        const DeviceInfo& dev, cudaStream_t stream, const float* const* xds = nullptr) {
   Plan p4, p8, p16;
-  cudaError_t err = plan_typed<WT, F16, XBF16, 4>(ms, n, batch, dev, &p4);
+  cudaError_t err = plan_typed<WT, F16, XBF16, 4, XQ>(ms, n, batch, dev, &p4);
   if (err != cudaSuccess) return err;
   if (p4.cost >= 0 && p4.grid > dev.sm_count)
-    return launch_typed<WT, F16, XBF16, 4>(p4, ms, xs, ys, n, batch, pdl, dev, stream);
-  err = plan_typed<WT, F16, XBF16, 8>(ms, n, batch, dev, &p8);
+    return launch_typed<WT, F16, XBF16, 4, XQ>(p4, ms, xs, ys, n, batch, pdl, dev, stream, xds);
+  err = plan_typed<WT, F16, XBF16, 8, XQ>(ms, n, batch, dev, &p8);
   if (err != cudaSuccess) return err;
-  err = plan_typed<WT, F16, XBF16, 16>(ms, n, batch, dev, &p16);
+  err = plan_typed<WT, F16, XBF16, 16, XQ>(ms, n, batch, dev, &p16);
   if (err != cudaSuccess) return err;
   auto better = [](const Plan& a, const Plan& b) { return a.cost >= 0 && (b.cost < 0 || a.cost < b.cost); };
   if (better(p16, p8) && better(p16, p4))
-    return launch_typed<WT, F16, XBF16, 16>(p16, ms, xs, ys, n, batch, pdl, dev, stream);
-  if (better(p8, p4)) return launch_typed<WT, F16, XBF16, 8>(p8, ms, xs, ys, n, batch, pdl, dev, stream);
+    return launch_typed<WT, F16, XBF16, 16, XQ>(p16, ms, xs, ys, n, batch, pdl, dev, stream, xds);
+  if (better(p8, p4)) return launch_typed<WT, F16, XBF16, 8, XQ>(p8, ms, xs, ys, n, batch, pdl, dev, stream, xds);
   if (p4.cost < 0) return cudaErrorInvalidConfiguration;
-  return launch_typed<WT, F16, XBF16, 4>(p4, ms, xs, ys, n, batch, pdl, dev, stream);
+  return launch_typed<WT, F16, XBF16, 4, XQ>(p4, ms, xs, ys, n, batch, pdl, dev, stream, xds);
 }
 
 }  // namespace
@@ -560,6 +635,26 @@ bool matvec_mma_supported(const MatrixRef& m) {
 }
 
 int matvec_mma_max_problems() { return kMaxProblems; }
+
+cudaError_t launch_matvec_qx_mma(const MatrixRef& m, const int8_t* xq, const float* xd, int batch, float* y,
+                                 bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
+  if (batch < 1 || !matvec_mma_supported(m)) return cudaErrorInvalidValue;
+  for (int b0 = 0; b0 < batch; b0 += kMaxBatch) {
+    const int nb = (batch - b0) < kMaxBatch ? (batch - b0) : kMaxBatch;
+    const void* xs[1] = {xq + (size_t)b0 * (size_t)m.cols};
+    const float* xds[1] = {xd + (size_t)b0 * (size_t)(m.cols / 32)};
+    float* ys[1] = {y + (size_t)b0 * (size_t)m.rows};
+    cudaError_t err;
+    if (m.wtype == QMV_Q4_0)
+      err = m.scale_f16 ? launch_best<QMV_Q4_0, true, true, true>(&m, xs, ys, 1, nb, pdl, dev, stream, xds)
+                        : launch_best<QMV_Q4_0, false, true, true>(&m, xs, ys, 1, nb, pdl, dev, stream, xds);
+    else
+      err = m.scale_f16 ? launch_best<QMV_Q8_0, true, true, true>(&m, xs, ys, 1, nb, pdl, dev, stream, xds)
+                        : launch_best<QMV_Q8_0, false, true, true>(&m, xs, ys, 1, nb, pdl, dev, stream, xds);
+    if (err != cudaSuccess) return err;
+  }
+  return cudaSuccess;
+}
 
 cudaError_t launch_matvec_mma(const MatrixRef* ms, const void* const* xs, float* const* ys, int n, bool x_bf16,
                               int batch, bool pdl, const DeviceInfo& dev, cudaStream_t stream) {

@@ -476,6 +476,10 @@ int qmv_matvec_qx(int wtype, int scale_dtype, int64_t rows, int64_t cols, const 
   if (current_device_info(&dev) != cudaSuccess) return QMV_E_CUDA;
   const int8_t* xqq = static_cast<const int8_t*>(xq);
   const float* xd = reinterpret_cast<const float*>(static_cast<const uint8_t*>(xq) + LX.d_off);
+  // 2 or more vectors, cols a multiple of 256: the block dots on the tensor core (quants and
+  // levels as exact halves); else the dp4a kernel
+  if (batch >= 2 && matvec_mma_supported(m))
+    return launch_matvec_qx_mma(m, xqq, xd, batch, y, false, dev, stream) == cudaSuccess ? QMV_OK : QMV_E_CUDA;
   return launch_matvec_qx(m, xqq, xd, batch, y, dev, stream) == cudaSuccess ? QMV_OK : QMV_E_CUDA;
 }
 

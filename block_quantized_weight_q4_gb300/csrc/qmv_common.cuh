@@ -123,6 +123,12 @@ __device__ __forceinline__ void tma_load_2d_keep(void* dst_smem, const CUtensorM
 }
 
 // Shared-memory loads by 32-bit shared address (ordered after the barrier waits).
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+  uint32_t a;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(a) : "r"(addr) : "memory");
+  return a;
+}
+
 __device__ __forceinline__ void lds_u32x2(uint32_t addr, uint32_t& a, uint32_t& b) {
   asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(addr) : "memory");
 }

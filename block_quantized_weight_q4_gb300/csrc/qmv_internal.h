@@ -79,6 +79,10 @@ cudaError_t launch_quantize_x(bool x_bf16, int64_t batch, int64_t cols, const vo
 // xq / xd: the quants and scales of the batch x cols Q8_0 / f32 activation image.
 cudaError_t launch_matvec_qx(const MatrixRef& m, const int8_t* xq, const float* xd, int batch, float* y,
                              const DeviceInfo& dev, cudaStream_t stream);
+// The same product on the tensor core (quants and levels as exact halves, mma.sync), cols % 256
+// == 0, batch in passes of up to 8.  pdl: launch as a programmatic dependent.
+cudaError_t launch_matvec_qx_mma(const MatrixRef& m, const int8_t* xq, const float* xd, int batch, float* y,
+                                 bool pdl, const DeviceInfo& dev, cudaStream_t stream);
 // The same product for 1..8 problems of one weight type and scale type in one launch per pass
 // of 8 vectors, each with its float activations (batch x cols, bf16 or f32), which the kernel
 // quantizes itself (the bytes launch_quantize_x writes) into shared memory: needs

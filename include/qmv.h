@@ -349,8 +349,11 @@ int qmv_quantize_x(int x_dtype, int64_t batch, int64_t cols, const void *x, void
  *   y[v][r] = sum_b (d_w[r][b] * d_x[v][b]) * isum        (float32 products and sums),
  * y device, batch x rows float32, row-major, 4-byte aligned, fully overwritten.  Results agree
  * with an exact evaluation to within 1e-3 * sum_b |d_w d_x| sum_j |level_w q_x| per output and
- * do not depend on timing.  Runs in passes of up to 8 vectors (dp4a integer dot products, one
- * warp per 1, 2 or 4 rows).  batch 0 launches nothing.  Asynchronous.  Returns as qmv_matvec. */
+ * do not depend on timing.  Runs in passes of up to 8 vectors: with 2 or more vectors and cols a
+ * multiple of 256 on the tensor core (mma.sync m16n8k16 with the quants and the levels as IEEE
+ * halves, exact, so each block dot is the exact integer sum), else with dp4a integer dot
+ * products (one warp per 1, 2 or 4 rows).  batch 0 launches nothing.  Asynchronous.  Returns as
+ * qmv_matvec. */
 int qmv_matvec_qx(int wtype, int scale_dtype, int64_t rows, int64_t cols, const void *W, const void *xq,
                   float *y, int batch, cudaStream_t stream);
 

@@ -95,11 +95,13 @@ def test_matvec_qx_matches_oracle(qmv, wt, sf, rows, cols, batch):
 
 @pytest.mark.parametrize("wt", [1, 2])
 @pytest.mark.parametrize("batch", [1, 2, 3, 8])
-def test_matvec_qx_exact_case(qmv, wt, batch):
+@pytest.mark.parametrize("cols", [128, 512])
+def test_matvec_qx_exact_case(qmv, wt, batch, cols):
     # power-of-two weight scales and activations k * 2^e (one element per block at +-127):
     # every block term (d_w d_x) * isum is an integer times 2^-10 below 2^24 units, and so is
-    # every partial sum, so the float32 result is exact in any order
-    rows, cols = 9, 128
+    # every partial sum, so the float32 result is exact in any order (cols 512 with 2..8 vectors:
+    # the tensor-core route)
+    rows = 9
     rng = np.random.default_rng(80 + wt + batch)
     if wt == 1:
         q = rng.integers(-127, 128, rows * cols).astype(np.int8).view(np.uint8)
