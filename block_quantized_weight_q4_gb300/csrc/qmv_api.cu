@@ -23,6 +23,7 @@ constexpr long long kTcMinBytes = 40LL << 20;      // launches of this many weig
                                                    // measured faster at 4..8 vectors)
 constexpr long long kTcMinQ8Weights = 64LL << 20;  // and Q8_0 passes of 2-3 vectors over this many weights
 constexpr long long kTcWideMinBytes = 8LL << 20;   // passes of 9..16 vectors in one decode_tc launch
+constexpr long long kTcF32MinBytes = 16LL << 20;   // float32 passes of 2..8 vectors take decode_tc from here
 constexpr long long kQxBdiagMaxBytes = 96LL << 20;  // one-vector activation-quantized groups below this
                                                     // size take the block-diagonal kernel
 constexpr long long kF32SplitMinWeights = 256LL << 10;  // one f32 vector: split hi/lo from this many weights
@@ -289,9 +290,12 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
     bool tc = xb && (nb > 8 || (nb >= kTcMinBatch && nbytes >= kTcMinBytes) ||
                      (wtype == QMV_Q8_0 && nb > 1 && nweights >= kTcMinQ8Weights));
     for (int i = 0; i < nf && tc; ++i) tc = decode_tc_supported(fast[i]);
-    // float32 activations, 2..8 vectors: the tensor-memory kernel on the bf16 pairs hi + lo
-    // (its 16 MMA columns hold both parts of up to 8 vectors)
-    bool tc32 = !xb && nb >= 2 && decode_tc_f32_fits(fast, nf);
+    // float32 activations, 2..8 vectors, launches of 16 MB or more and gated activations: the
+    // tensor-memory kernel on the bf16 pairs hi + lo (its 16 MMA columns hold both parts of up
+    // to 8 vectors); smaller launches the mma.sync kernel, which splits x in its own stages (one
+    // launch: 2048 x 1024 Q4_0 at 8 vectors 3.3 against 7.4 us; 11008 x 4096 17.6 against 20.9 us
+    // the other way)
+    bool tc32 = !xb && nb >= 2 && (glu || nbytes >= kTcF32MinBytes) && decode_tc_f32_fits(fast, nf);
     for (int i = 0; i < nf && tc32; ++i) tc32 = decode_tc_supported(fast[i]);
     Workspace ws;
     if (tc && stream_workspace(dev, stream, &ws) == cudaSuccess) {

@@ -131,11 +131,12 @@ int qmv_matrix_wtype(int file_wtype, uint32_t q8_mask, int class_bit, int shared
  * MMA; below those sizes the mma.sync kernel measured faster and takes the other passes of
  * 2..8 vectors); a pass of one bf16 vector takes the block-diagonal kernel (one MMA
  * column per weight block; IEEE-half operands for the 256-column stages whose activations
- * are exact halves, bfloat16 otherwise).  float32 activations, 2..8 vectors, are first split
- * into bfloat16 pairs hi + lo (hi = RN_bf16(x), lo = RN_bf16(x - hi): 16 bits of x kept) in
- * a 2 MiB buffer of the calling stream (allocated on its first such call; without it, and
- * while the stream is captured before it exists, the mma.sync kernel takes them) and take the
- * tensor-memory kernel (hi and lo as its 16 MMA columns).  One float32 vector takes the
+ * are exact halves, bfloat16 otherwise).  float32 activations, 2..8 vectors, are split into
+ * bfloat16 pairs hi + lo (hi = RN_bf16(x), lo = RN_bf16(x - hi): 16 bits of x kept): on
+ * launches of 16 MB of weights or more (and for gated activations) in a 2 MiB buffer of the
+ * calling stream (allocated on its first such call; without it, and while the stream is
+ * captured before it exists, the mma.sync kernel takes them) for the tensor-memory kernel (hi
+ * and lo as its 16 MMA columns), on smaller launches in the mma.sync kernel's own stages.  One float32 vector takes the
  * block-diagonal kernel (launches under 256K weights the mma.sync kernel, which splits x as
  * above in one launch): under 16 MB of weights it reads x as float32, larger launches after
  * the split into the buffer.  There each warp's stage of 256 or 512 columns is scaled by the

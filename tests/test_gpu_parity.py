@@ -349,11 +349,13 @@ def test_f32_one_vector_wide_magnitudes(qmv, wt, sf):
     check_product(y, y_ref, absref, 1e-5, "wide f32 magnitudes, tight")
 
 
-def test_f32_activations_batch8_graph_replay_bit_identical(qmv):
-    # float32 activations, 8 vectors: the split kernel and the tensor-memory product, eager
-    # on a stream (which creates its buffers) and then replayed in a graph on it
+@pytest.mark.parametrize("rows,cols", [(1100, 2048), (4608, 8192)])
+def test_f32_activations_batch8_graph_replay_bit_identical(qmv, rows, cols):
+    # float32 activations, 8 vectors, eager on a stream (which creates its buffers) and then
+    # replayed in a graph on it: 2.5 MB of weights take the mma.sync kernel (x split in its
+    # stages), 42 MB the split kernel and the tensor-memory product
     import torch
-    rows, cols, batch = 1100, 2048, 8
+    batch = 8
     m = inputs.make_matrix(1, 0, rows, cols, seed=81)
     x = inputs.make_x(batch, cols, False, seed=82)
     y_ref, absref = oracle.matvec(m.W, 1, 0, rows, cols, x)
