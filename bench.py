@@ -64,6 +64,9 @@ def parse():
     ap.add_argument("--x-f32", action="store_true", help="--case: float32 activations (default bfloat16)")
     ap.add_argument("--bf16-weights", action="store_true", help="--case: the prefill kernel's bf16-weights variant")
     ap.add_argument("--qx", action="store_true", help="--case: the activation-quantized product (qmv_matvec_qx_grouped)")
+    ap.add_argument("--qx-image", action="store_true",
+                    help="--case: the activation-quantized product on a quantized image (qmv_quantize_x once, "
+                         "then qmv_matvec_qx per call)")
     ap.add_argument("--case-calls", type=int, default=20, help="--case: calls per timed CUDA graph")
     ap.add_argument("--case-copies", type=int, default=4, help="--case: rotating copies of the matrix")
     return ap.parse_args()
@@ -808,8 +811,12 @@ def run_case(args):
     xd = torch.from_numpy(x).cuda() if args.x_f32 else torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
     y = torch.empty((batch, rows), device="cuda")
 
+    xq = qmv.quantize_x(xd) if args.qx_image else None
+
     def call(i):
-        if args.qx:
+        if args.qx_image:
+            qmv.matvec_qx(wt, sf, rows, cols, Ws[i % ncopy], xq, batch, y)
+        elif args.qx:
             qmv.matvec_qx_grouped(wt, sf, [(rows, cols, Ws[i % ncopy], xd, y)])
         else:
             qmv.matvec_grouped(wt, sf, [(rows, cols, Ws[i % ncopy], xd, y)], bf16_weights=args.bf16_weights)
@@ -823,7 +830,7 @@ def run_case(args):
     torch.cuda.synchronize()
     out = {"case": {"rows": rows, "cols": cols, "wtype": wt, "scale_f16": sf, "batch": batch,
                     "x_dtype": "f32" if args.x_f32 else "bf16", "bf16_weights": bool(args.bf16_weights),
-                    "activation_quantized": bool(args.qx),
+                    "activation_quantized": "image" if args.qx_image else bool(args.qx),
                     "copies": ncopy}}
     if args.case_calls > 0:
         g = torch.cuda.CUDAGraph()

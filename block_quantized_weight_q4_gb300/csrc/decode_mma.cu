@@ -72,7 +72,9 @@ struct Cfg {
   static constexpr int D_STAGE = WROWS * DROW;                     // multiple of 128
   static constexpr int XROW = XQ ? kTK : kTK * (XBF16 ? 2 : 4);    // activation bytes per vector per stage
   static constexpr int XDROW = XQ ? kBlocksPerStage * 4 : 0;       // XQ: activation scale bytes per vector
-  static constexpr int S = NW >= 16 ? 2 : 3;                       // ring depth (16 warps: 2, to fit)
+  // ring depth: 2 (3 measured slower: it halves the CTAs per SM that shared memory allows, e.g.
+  // 14336 x 4096 Q4_0 at 8 vectors 14.0 against 10.0 us)
+  static constexpr int S = 2;
   static constexpr int Q_WARP = S * Q_STAGE;
   static constexpr int D_WARP = S * D_STAGE;
   static constexpr int RED_FLOATS = kWarps * WROWS * 8;

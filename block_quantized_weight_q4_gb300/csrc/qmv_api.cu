@@ -18,12 +18,11 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kPrefillMinBatch = 17;  // from here on the prefill kernel takes bf16 batches
-constexpr int kTcMinBatch = 4;        // decode passes of this many bf16 vectors may go to decode_tc:
-constexpr long long kTcMinBytes = 40LL << 20;      // launches of this many weight bytes (below, mma.sync
-                                                   // measured faster at 4..8 vectors)
-constexpr long long kTcMinQ8Weights = 64LL << 20;  // and Q8_0 passes of 2-3 vectors over this many weights
+constexpr int kTcMinBatch = 8;        // bf16 passes of this many vectors may go to decode_tc:
+constexpr long long kTcMinBytes = 128LL << 20;     // launches of this many weight bytes (below, and at
+                                                   // 2..7 vectors, the mma.sync kernel measured faster)
 constexpr long long kTcWideMinBytes = 8LL << 20;   // passes of 9..16 vectors in one decode_tc launch
-constexpr long long kTcF32MinBytes = 16LL << 20;   // float32 passes of 2..8 vectors take decode_tc from here
+constexpr long long kTcF32MinBytes = 96LL << 20;   // float32 passes of 2..8 vectors take decode_tc from here
 constexpr long long kQxBdiagMaxBytes = 96LL << 20;  // one-vector activation-quantized groups below this
                                                     // size take the block-diagonal kernel
 constexpr long long kF32SplitMinWeights = 256LL << 10;  // one f32 vector: split hi/lo from this many weights
@@ -277,24 +276,23 @@ int qmv_matvec_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const
       }
     }
     if (nf == 0) continue;
-    // bf16 activations: the tensor-memory kernel for passes of 9..16 vectors, passes of 4..8
-    // over 40 MB of weights or more, and Q8_0 passes of 2 or 3 vectors over 64M weights or more
-    // (where it measured faster than the mma.sync kernel), when this stream has its workspace
-    // (created on the stream's first such call, never while it is captured); one bf16 vector:
-    // the block-diagonal kernel; else the mma.sync kernel
+    // bf16 activations: the tensor-memory kernel for passes of 9..16 vectors and passes of 8
+    // over 128 MB of weights, when this stream has its workspace (created on the stream's first
+    // such call, never while it is captured); one bf16 vector: the block-diagonal kernel; else
+    // the mma.sync kernel (2..8 vectors: 14336 x 4096 Q4_0 at 8 vectors 10.0 against 14.7 us,
+    // 151936 x 1024 Q8_0 at 4 vectors 33.8 against 35.6 us; 8 vectors on 175 MB 39.3 against 38.2)
     long long nweights = 0, nbytes = 0;
     for (int i = 0; i < nf; ++i) {
       nweights += fast[i].rows * fast[i].cols;
       nbytes += weight_bytes(fast[i]);
     }
-    bool tc = xb && (nb > 8 || (nb >= kTcMinBatch && nbytes >= kTcMinBytes) ||
-                     (wtype == QMV_Q8_0 && nb > 1 && nweights >= kTcMinQ8Weights));
+    bool tc = xb && (nb > 8 || (nb >= kTcMinBatch && nbytes >= kTcMinBytes));
     for (int i = 0; i < nf && tc; ++i) tc = decode_tc_supported(fast[i]);
-    // float32 activations, 2..8 vectors, launches of 16 MB or more and gated activations: the
+    // float32 activations, 2..8 vectors, launches of 96 MB or more and gated activations: the
     // tensor-memory kernel on the bf16 pairs hi + lo (its 16 MMA columns hold both parts of up
     // to 8 vectors); smaller launches the mma.sync kernel, which splits x in its own stages (one
-    // launch: 2048 x 1024 Q4_0 at 8 vectors 3.3 against 7.4 us; 11008 x 4096 17.6 against 20.9 us
-    // the other way)
+    // launch: 2048 x 1024 Q4_0 at 8 vectors 3.3 against 7.4 us, 28672 x 4096 at 4 vectors 21.8
+    // against 25.7 us; 65536 x 4096 at 8 vectors 61.8 against 50.0 us the other way)
     bool tc32 = !xb && nb >= 2 && (glu || nbytes >= kTcF32MinBytes) && decode_tc_f32_fits(fast, nf);
     for (int i = 0; i < nf && tc32; ++i) tc32 = decode_tc_supported(fast[i]);
     Workspace ws;

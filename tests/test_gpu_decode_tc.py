@@ -1,6 +1,6 @@
 """The decode kernels for 2..16 bf16 vectors vs the oracle: the tensor-memory kernel (passes of
-4..8 vectors over 40 MB of weights, passes of 9..16 vectors over 8 MB, Q8_0 launches of 64M
-weights or more) and, on smaller launches, the mma.sync kernel (passes of up to 8).
+8 vectors over 128 MB of weights, passes of 9..16 vectors over 8 MB) and the mma.sync kernel
+(the other passes of 2..8).
 
 The tensor-memory kernel splits the work into units of 128 rows x 256 columns shared out
 evenly between two CTAs per SM, so a tile's columns may be summed by several CTAs; the parts
@@ -22,7 +22,7 @@ pytestmark = pytest.mark.gpu
 TOL = 1e-3
 TYPES = [(1, 0), (1, 1), (2, 0), (2, 1)]
 # launch sizes from which the tensor-memory kernel takes the bf16 passes
-TC_MIN_BYTES = 40 << 20       # passes of 4..8 vectors
+TC_MIN_BYTES = 128 << 20      # passes of 8 vectors
 TC_WIDE_MIN_BYTES = 8 << 20   # passes of 9..16 vectors, one launch each
 
 
@@ -164,11 +164,11 @@ def test_tc_q8_large_launch_batch1(qmv):
     check_product(y[:, ids], y_ref, absref, TOL, "q8 large b1")
 
 
-@pytest.mark.parametrize("wt,sf,rows,cols", [(1, 0, 20480, 2048), (2, 1, 36864, 2048)])
-@pytest.mark.parametrize("batch", [4, 7, 8])
+@pytest.mark.parametrize("wt,sf,rows,cols", [(1, 0, 122880, 1024), (2, 1, 65536, 4096)])
+@pytest.mark.parametrize("batch", [7, 8])
 def test_tc_large_launch_sampled_rows(qmv, wt, sf, rows, cols, batch):
-    # 47 / 42 MB: the tensor-memory kernel at 4..8 vectors; rows sampled over every part of the
-    # matrix (tiles split between CTAs at every CTA boundary)
+    # 142 / 151 MB: the tensor-memory kernel at 8 vectors (the mma.sync kernel at 7); rows
+    # sampled over every part of the matrix (tiles split between CTAs at every CTA boundary)
     assert weight_bytes(wt, sf, rows, cols) >= TC_MIN_BYTES
     m = inputs.make_matrix(wt, sf, rows, cols, seed=30 + batch)
     x = inputs.make_x(batch, cols, True, seed=31 + batch)
@@ -228,10 +228,11 @@ def test_tc_sixteen_vector_pass_exact_and_repeatable(qmv, batch):
 
 @pytest.mark.parametrize("batch", [6, 11])
 def test_tc_grouped_large_launch(qmv, batch):
-    # a grouped launch of 45 MB (tiles of three problems in one unit list), with overlap
+    # a grouped launch of 45 MB (11 vectors: one 16-vector pass of the tensor-memory kernel, tiles
+    # of three problems in one unit list; 6 vectors: the mma.sync kernel), with overlap
     import torch
     shapes = [(14336, 4096), (4096, 4096), (1000, 4096)]
-    assert sum(weight_bytes(2, 1, r, c) for r, c in shapes) >= TC_MIN_BYTES
+    assert sum(weight_bytes(2, 1, r, c) for r, c in shapes) >= TC_WIDE_MIN_BYTES
     probs, refs = [], []
     for i, (rows, cols) in enumerate(shapes):
         m = inputs.make_matrix(2, 1, rows, cols, seed=60 + i)

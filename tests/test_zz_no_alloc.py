@@ -69,14 +69,14 @@ def test_noalloc_matches_grouped_and_oracle(qmv, wt, sf, batch):
         check_product(base[k], y_ref, absref, TOL, what + " (existing entry point)")
 
 
-@pytest.mark.parametrize("batch", [5, 8])
+@pytest.mark.parametrize("batch", [8])
 def test_noalloc_same_bits_as_grouped_at_tensor_memory_sizes(qmv, batch):
-    # 47 MB of Q8_0 weights, 5..8 vectors: qmv_matvec_grouped takes the tensor-memory kernel
-    # too, with the same grid and the same splits, so the two give the same bits (sampled rows
+    # 142 MB of Q8_0 weights, 8 vectors: qmv_matvec_grouped takes the tensor-memory kernel too,
+    # with the same grid and the same splits, so the two give the same bits (sampled rows
     # against the oracle)
     import torch
-    wt, sf, rows, cols = 1, 0, 20480, 2048
-    assert rows * cols // 32 * 36 >= 40 << 20
+    wt, sf, rows, cols = 1, 0, 122880, 1024
+    assert rows * cols // 32 * 36 >= 128 << 20
     mats, probs = _problems(wt, sf, [(rows, cols)], batch, seed=350 + batch)
     (m, x), = mats
     qmv.matvec_grouped(wt, sf, probs)
