@@ -125,15 +125,14 @@ int qmv_matrix_wtype(int file_wtype, uint32_t q8_mask, int class_bit, int shared
  * below 16 (and 16 in groups of 8 MB of weights or more, and float32 activations) run
  * through the decode kernels (weights decoded to exact levels, one tensor-core dot product
  * per block, f32 scale and accumulate) in passes of up to 8 vectors, or of up to 16 for bf16
- * batches of 9..16 in groups of 8 MB of weights or more: those 16-vector passes, bf16 passes
- * of 4..8 vectors over 40 MB of weights or more, and Q8_0 passes of 2 or 3 bf16 vectors over
- * 64M weights or more take the tensor-memory kernel (levels stored to tensor memory, tcgen05
- * MMA; below those sizes the mma.sync kernel measured faster and takes the other passes of
- * 2..8 vectors); a pass of one bf16 vector takes the block-diagonal kernel (one MMA
+ * batches of 9..16 in groups of 8 MB of weights or more: those 16-vector passes and bf16
+ * passes of 8 vectors over 128 MB of weights take the tensor-memory kernel (levels stored to
+ * tensor memory, tcgen05 MMA); the other passes of 2..8 bf16 vectors the mma.sync kernel,
+ * which measured faster there; a pass of one bf16 vector takes the block-diagonal kernel (one MMA
  * column per weight block; IEEE-half operands for the 256-column stages whose activations
  * are exact halves, bfloat16 otherwise).  float32 activations, 2..8 vectors, are split into
  * bfloat16 pairs hi + lo (hi = RN_bf16(x), lo = RN_bf16(x - hi): 16 bits of x kept): on
- * launches of 16 MB of weights or more (and for gated activations) in a 2 MiB buffer of the
+ * launches of 96 MB of weights or more (and for gated activations) in a 2 MiB buffer of the
  * calling stream (allocated on its first such call; without it, and while the stream is
  * captured before it exists, the mma.sync kernel takes them) for the tensor-memory kernel (hi
  * and lo as its 16 MMA columns), on smaller launches in the mma.sync kernel's own stages.  One float32 vector takes the
