@@ -376,6 +376,8 @@ int qmv_matvec_qx(int wtype, int scale_dtype, int64_t rows, int64_t cols, const 
  *   else QMV_E_ARG.
  * Results agree with those of qmv_quantize_x followed by qmv_matvec_qx within the tolerance stated
  * there (the column slices may be added in a different grouping) and do not depend on timing.
+ * At 2..8 vectors the two-step route (qmv_quantize_x, then qmv_matvec_qx on the tensor core)
+ * measured about twice as fast (65536 x 4096 Q4_0 at 8 vectors: 1.7 + 46 against 95 us).
  * Allocates nothing.  Asynchronous.  Returns as qmv_matvec_grouped. */
 #define QMV_QX_MAX_VEC_COLS 200704
 int qmv_matvec_qx_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const qmv_problem *problems, int n,
