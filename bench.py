@@ -728,14 +728,12 @@ def run_ours(args, world, rank, local):
     e2e_steps = max(10, min(args.steps, 2000))
     stream = torch.cuda.current_stream()
     for it in range(min(e2e_steps, 3 * ncopy)):   # warm-up
-        e2e_steps_objs[it % ncopy].run()
-        stream.synchronize()
+        e2e_steps_objs[it % ncopy].run(stream, wait=True)
     torch.cuda.synchronize()
     barrier(world)
     t0 = time.perf_counter()
     for it in range(e2e_steps):
-        e2e_steps_objs[it % ncopy].run()
-        stream.synchronize()
+        e2e_steps_objs[it % ncopy].run(stream, wait=True)   # the run and the host's wait for y, one call
     e2e_s = (time.perf_counter() - t0) / e2e_steps
     for st in e2e_steps_objs:
         st.close()

@@ -74,6 +74,8 @@ def load_library():
     lib.qmv_step_create.argtypes = [vp, i32, vp, i32, vp, i32, ctypes.POINTER(vp)]
     lib.qmv_step_run.restype = i32
     lib.qmv_step_run.argtypes = [vp, vp]
+    lib.qmv_step_run_wait.restype = i32
+    lib.qmv_step_run_wait.argtypes = [vp, vp]
     lib.qmv_step_destroy.restype = i32
     lib.qmv_step_destroy.argtypes = [vp]
     lib.qmv_gguf_bytes.restype = ctypes.c_size_t
@@ -315,10 +317,15 @@ class Step:
         self._handle = handle
         self._keep = keep
 
-    def run(self, stream=None):
+    def run(self, stream=None, wait=False):
+        """Enqueue one run on `stream` (the current stream by default); wait=True also waits for
+        the stream in the same library call (qmv_step_run_wait)."""
         if self._handle is None:
             raise ValueError("step destroyed")
-        _check(load_library().qmv_step_run(self._handle, _stream(stream)), "qmv_step_run")
+        if wait:
+            _check(load_library().qmv_step_run_wait(self._handle, _stream(stream)), "qmv_step_run_wait")
+        else:
+            _check(load_library().qmv_step_run(self._handle, _stream(stream)), "qmv_step_run")
 
     def close(self):
         if self._handle is not None:

@@ -103,6 +103,12 @@ int qmv_step_run(qmv_step* step, cudaStream_t stream) {
   return cudaGraphLaunch(step->exec, stream) == cudaSuccess ? QMV_OK : QMV_E_CUDA;
 }
 
+int qmv_step_run_wait(qmv_step* step, cudaStream_t stream) {
+  if (step == nullptr) return QMV_E_ARG;
+  if (cudaGraphLaunch(step->exec, stream) != cudaSuccess) return QMV_E_CUDA;
+  return cudaStreamSynchronize(stream) == cudaSuccess ? QMV_OK : QMV_E_CUDA;
+}
+
 int qmv_step_destroy(qmv_step* step) {
   if (step == nullptr) return QMV_OK;
   int st = cudaDeviceSynchronize() == cudaSuccess ? QMV_OK : QMV_E_CUDA;

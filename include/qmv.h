@@ -436,6 +436,12 @@ int qmv_step_create(const qmv_copy *before, int n_before, const qmv_group *group
  * order them.  Returns QMV_OK, QMV_E_ARG (null step) or QMV_E_CUDA. */
 int qmv_step_run(qmv_step *step, cudaStream_t stream);
 
+/* One run of the step on `stream` followed by a wait for the stream (what a decode loop does
+ * before it reads its host results): one call instead of qmv_step_run and a separate
+ * synchronization.  Returns QMV_OK, QMV_E_ARG (null step) or QMV_E_CUDA (a failed launch, or an
+ * error the stream reported). */
+int qmv_step_run_wait(qmv_step *step, cudaStream_t stream);
+
 /* Waits for the device, then frees the step and its workspaces.  NULL is a no-op.  Returns
  * QMV_OK or QMV_E_CUDA. */
 int qmv_step_destroy(qmv_step *step);

@@ -120,6 +120,7 @@ def test_dequant_and_validate_argument_errors(lib):
     bad = (binding.Copy * 1)(binding.Copy(0, FAKE, 64))
     assert lib.qmv_step_create(ctypes.addressof(bad), 1, None, 0, None, 0, ctypes.byref(out)) == binding.E_ARG
     assert lib.qmv_step_run(None, None) == binding.E_ARG
+    assert lib.qmv_step_run_wait(None, None) == binding.E_ARG
     assert lib.qmv_step_destroy(None) == binding.OK
     # qmv_gguf_bytes / qmv_gguf_to_mlb: sizes, then shape, format, null and alignment checks
     assert lib.qmv_gguf_bytes(1, 151936, 896) == 144643072

@@ -83,6 +83,12 @@ def test_step_runs_match_eager_calls_and_oracle(qmv, batch, bf16):
         s.synchronize()
         for i in range(3):
             assert_bits_equal(yh[i].numpy(), got[i].numpy(), f"other stream problem {i}")
+        # a run and its wait in one call
+        for y in yh:
+            y.zero_()
+        step.run(stream=s, wait=True)
+        for i in range(3):
+            assert_bits_equal(yh[i].numpy(), got[i].numpy(), f"run and wait problem {i}")
     finally:
         step.close()
 
