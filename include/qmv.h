@@ -400,6 +400,10 @@ int qmv_quantize_q4_fit(int scale_dtype, int64_t rows, int64_t cols, const float
  * one call (a decode step's host input, its products and its host output, launched together).
  *   qmv_copy  : bytes from src to dst, any mix of device and pinned host pointers (the
  *               direction follows from the addresses); pageable host memory is not allowed.
+ *               A copy between device memory and pinned host memory mapped into the device's
+ *               address space is recorded as a small copy kernel reading or writing the host
+ *               memory directly (cheaper than a copy node for the few KB of a decode step);
+ *               other copies as cudaMemcpyAsync.
  *   qmv_group : the arguments of one qmv_matvec_grouped call.
  * qmv_step_create runs the step once, eagerly, on a private stream (the `before` copies in
  * order, the groups in order, the `after` copies in order): that run sets up the kernels and

@@ -168,3 +168,21 @@ def test_step_with_per_group_copies_and_a_chained_group(qmv):
             check_product(got[1], y_ref, absref, what=f"run {it} y1")
     finally:
         step.close()
+
+
+@pytest.mark.parametrize("nbytes,offset", [(1001, 3), (4096, 16), (65536 + 8, 8)])
+def test_step_copies_of_any_size_and_offset(qmv, nbytes, offset):
+    # host <-> device copies of a step (done by the GPU through the host memory's device address
+    # when both ends allow it): any byte count and alignment, the exact bytes both ways
+    import torch
+    src = torch.randint(0, 256, (nbytes + 64,), dtype=torch.uint8).pin_memory()
+    mid = torch.zeros(nbytes + 64, dtype=torch.uint8, device="cuda")
+    dst = torch.zeros(nbytes + 64, dtype=torch.uint8).pin_memory()
+    a, b = offset, offset + nbytes
+    with qmv.Step([], before=[(mid[a:b], src[a:b])], after=[(dst[a:b], mid[a:b])]) as step:
+        for _ in range(2):
+            src.random_(0, 256)
+            step.run(wait=True)
+            assert torch.equal(dst[a:b], src[a:b])
+            assert torch.equal(mid[a:b].cpu(), src[a:b])
+            assert int(dst[:a].sum()) == 0 and int(dst[b:].sum()) == 0   # nothing outside the range
