@@ -59,7 +59,7 @@ constexpr int kBox = 128;            // q box inner extent in bytes (the 128-byt
 constexpr int kMaxBatch = 8;         // activation vectors per pass (the MMA's N)
 constexpr int kMaxProblems = 8;      // problems per grouped launch
 
-template <int WT, bool F16, bool XBF16, int NW, bool XQ = false>
+template <int WT, bool F16, bool XBF16, int NW, bool XQ = false, bool RS = false>
 struct Cfg {
   static constexpr int kWarps = NW;
   static constexpr int MT = (WT == QMV_Q4_0) ? 2 : 1;           // 16-row MMA tiles per warp tile
@@ -77,15 +77,23 @@ struct Cfg {
   static constexpr int S = 2;
   static constexpr int Q_WARP = S * Q_STAGE;
   static constexpr int D_WARP = S * D_STAGE;
-  static constexpr int RED_FLOATS = kWarps * WROWS * 8;
   static constexpr int ZERO_BYTES = 128;
-  // fixed part: q rings, d rings, zero area, reduction buffer, barriers; the activation
-  // rings (S x batch x XROW per warp) follow
+  // fixed part: q rings, d rings, zero area, reduction area (WROWS x 8 floats per warp, where
+  // a split tile's column slices meet), barriers; the activation rings (S x batch x XROW per
+  // warp) follow.  RS: no reduction area -- the slices meet in the q slot each warp has just
+  // consumed, whose index each warp leaves after the barriers.  That saves 4 KB per CTA and is
+  // taken where it lets an SM hold one CTA more and the launch fills them (65536 x 4096 Q4_0 at
+  // 8 quantized vectors, three to four CTAs per SM: 42.5 against 45.6 us, at 4 bf16 vectors
+  // 36.9 against 39.5 us); in launches whose occupancy it does not raise it measured 2-4% slower
   static constexpr int OFF_D = kWarps * Q_WARP;
   static constexpr int OFF_ZERO = OFF_D + kWarps * D_WARP;
   static constexpr int OFF_RED = OFF_ZERO + ZERO_BYTES;
+  static constexpr int RED_FLOATS = RS ? 0 : kWarps * WROWS * 8;
   static constexpr int OFF_BAR = OFF_RED + RED_FLOATS * 4;
-  static constexpr int OFF_X = OFF_BAR + ((kWarps * S * 8 + 127) / 128) * 128;
+  static constexpr int OFF_SLOT = OFF_BAR + kWarps * S * 8;
+  static constexpr int OFF_X = RS ? (OFF_SLOT + kWarps * 4 + 127) / 128 * 128
+                                  : OFF_BAR + ((kWarps * S * 8 + 127) / 128) * 128;
+  static_assert(WROWS * 8 * 4 <= Q_STAGE, "a q slot holds a warp's partial sums");
   // activation bytes of one stage (quants then scales with XQ), a multiple of 128 (TMA destinations)
   static __host__ __device__ int x_stage(int batch) { return (batch * (XROW + XDROW) + 127) / 128 * 128; }
   static int smem_bytes(int batch) { return 1024 + OFF_X + kWarps * S * x_stage(batch); }
@@ -136,10 +144,10 @@ __device__ __forceinline__ void cursor_load(Cursor& c, const Params& p, int tile
   c.j = 0;
 }
 
-template <int WT, bool F16, bool XBF16, int NW, bool XQ = false>
+template <int WT, bool F16, bool XBF16, int NW, bool XQ = false, bool RS = false>
 __global__ void __launch_bounds__(NW * 32) matvec_mma_kernel(const __grid_constant__ Maps maps,
                                                              const __grid_constant__ Params p) {
-  using C = Cfg<WT, F16, XBF16, NW, XQ>;
+  using C = Cfg<WT, F16, XBF16, NW, XQ, RS>;
   constexpr int kWarps = NW;
   constexpr int MT = C::MT;
   extern __shared__ uint8_t smem_raw[];
@@ -157,6 +165,7 @@ __global__ void __launch_bounds__(NW * 32) matvec_mma_kernel(const __grid_consta
   uint8_t* xring = smem + C::OFF_X + warp * C::S * x_stage;
   uint8_t* zero = smem + C::OFF_ZERO;
   float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
+  int* red_slot = reinterpret_cast<int*>(smem + C::OFF_SLOT);  // RS: per warp, the q slot holding its partial sums
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + warp * C::S;
 
   const int tiles_per_item = kWarps / p.ks;
@@ -431,7 +440,10 @@ __global__ void __launch_bounds__(NW * 32) matvec_mma_kernel(const __grid_consta
           }
         }
       } else {
-        float* my = red + warp * (C::WROWS * 8);  // [rows][8 vectors]
+        // RS: slot cs was consumed above (all lanes, __syncwarp) and is filled again only after
+        // the second __syncthreads below (the next issue(), whose proxy fence orders these
+        // accesses before its copies)
+        float* my = RS ? reinterpret_cast<float*>(qring + cs * C::Q_STAGE) : red + warp * (C::WROWS * 8);
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           my[(16 * mt + g) * 8 + 2 * t] = acc[mt][0];
@@ -439,6 +451,7 @@ __global__ void __launch_bounds__(NW * 32) matvec_mma_kernel(const __grid_consta
           my[(16 * mt + g + 8) * 8 + 2 * t] = acc[mt][2];
           my[(16 * mt + g + 8) * 8 + 2 * t + 1] = acc[mt][3];
         }
+        if (RS && lane == 0) red_slot[warp] = cs;
         __syncthreads();
         if (kslice == 0 && valid && !failed) {
 #pragma unroll
@@ -448,7 +461,12 @@ __global__ void __launch_bounds__(NW * 32) matvec_mma_kernel(const __grid_consta
             const int r = v % C::WROWS;
             if (n < p.batch && row0 + r < P.rows) {
               float sum = 0.f;
-              for (int k = 0; k < p.ks; ++k) sum += red[(warp + k) * (C::WROWS * 8) + r * 8 + n];
+              for (int k = 0; k < p.ks; ++k) {
+                const float* part =
+                    RS ? reinterpret_cast<const float*>(smem + (warp + k) * C::Q_WARP + red_slot[warp + k] * C::Q_STAGE)
+                       : red + (warp + k) * (C::WROWS * 8);
+                sum += part[r * 8 + n];
+              }
               P.y[(size_t)n * P.rows + row0 + r] = sum;
             }
           }
@@ -475,42 +493,68 @@ __global__ void __launch_bounds__(NW * 32) matvec_mma_kernel(const __grid_consta
 // split needs).
 struct Plan {
   int ks = 1, nitems = 0, grid = 0, smem = 0;
+  int per_sm = 0;  // CTAs an SM can hold
+  bool rs = false;  // the kernel without the reduction area (Cfg::RS)
   long cost = -1;
 };
 
-template <int WT, bool F16, bool XBF16, int NW, bool XQ = false>
-cudaError_t plan_typed(const MatrixRef* ms, int n, int batch, const DeviceInfo& dev, Plan* out) {
-  using C = Cfg<WT, F16, XBF16, NW, XQ>;
-  auto kern = matvec_mma_kernel<WT, F16, XBF16, NW, XQ>;
-  // per device: the shared-memory limit raised as far as the batches seen need; per device
-  // and batch: occupancy known (0 = this warps-per-CTA choice does not fit)
+// The kernel's dynamic shared-memory limit raised to at least `smem` on this device (one
+// record per kernel and device, shared by the planner and the launcher).
+template <int WT, bool F16, bool XBF16, int NW, bool XQ, bool RS>
+cudaError_t raise_smem_limit(int device, int smem) {
   static std::mutex mu;
   static int attr_smem[64] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (smem <= attr_smem[device]) return cudaSuccess;
+  const cudaError_t err = cudaFuncSetAttribute(matvec_mma_kernel<WT, F16, XBF16, NW, XQ, RS>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err == cudaSuccess) attr_smem[device] = smem;
+  return err;
+}
+
+template <int WT, bool F16, bool XBF16, int NW, bool XQ = false>
+cudaError_t plan_typed(const MatrixRef* ms, int n, int batch, const DeviceInfo& dev, Plan* out) {
+  using C = Cfg<WT, F16, XBF16, NW, XQ, false>;
+  int smem_rs = 0;  // the RS variant's shared memory (four warps per CTA only)
+  if constexpr (NW == 4) smem_rs = Cfg<WT, F16, XBF16, NW, XQ, true>::smem_bytes(batch);
+  // per device and batch: occupancy known, with the reduction area [0] and without [1] (four
+  // warps per CTA only); 0 = does not fit
+  static std::mutex mu;
   static bool ready[64][kMaxBatch + 1] = {};
-  static int ctas_per_sm[64][kMaxBatch + 1] = {};
+  static int ctas_per_sm[64][kMaxBatch + 1][2] = {};
   if (dev.device < 0 || dev.device >= 64 || batch < 1 || batch > kMaxBatch || n < 1 || n > kMaxProblems)
     return cudaErrorInvalidValue;
-  const int smem = C::smem_bytes(batch);
   {
     std::lock_guard<std::mutex> lock(mu);
     if (!ready[dev.device][batch]) {
       int k = 0;
-      if ((size_t)smem <= dev.smem_optin) {
-        if (smem > attr_smem[dev.device]) {
-          const cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-          if (err != cudaSuccess) return err;
-          attr_smem[dev.device] = smem;
-        }
-        const cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&k, kern, NW * 32, smem);
+      if ((size_t)C::smem_bytes(batch) <= dev.smem_optin) {
+        cudaError_t err = raise_smem_limit<WT, F16, XBF16, NW, XQ, false>(dev.device, C::smem_bytes(batch));
+        if (err != cudaSuccess) return err;
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&k, matvec_mma_kernel<WT, F16, XBF16, NW, XQ, false>,
+                                                            NW * 32, C::smem_bytes(batch));
         if (err != cudaSuccess) return err;
       }
-      ctas_per_sm[dev.device][batch] = k;
+      ctas_per_sm[dev.device][batch][0] = k;
+      k = 0;
+      if constexpr (NW == 4) {
+        if ((size_t)smem_rs <= dev.smem_optin) {
+          cudaError_t err = raise_smem_limit<WT, F16, XBF16, NW, XQ, true>(dev.device, smem_rs);
+          if (err != cudaSuccess) return err;
+          err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&k, matvec_mma_kernel<WT, F16, XBF16, NW, XQ, true>,
+                                                              NW * 32, smem_rs);
+          if (err != cudaSuccess) return err;
+        }
+      }
+      ctas_per_sm[dev.device][batch][1] = k;
       ready[dev.device][batch] = true;
     }
   }
   *out = Plan{};
-  if (ctas_per_sm[dev.device][batch] == 0) return cudaSuccess;  // does not fit: cost stays -1
-  const long slots = (long)ctas_per_sm[dev.device][batch] * dev.sm_count;
+  const int occ = ctas_per_sm[dev.device][batch][0];
+  const int occ_slot = ctas_per_sm[dev.device][batch][1];
+  if (occ == 0) return cudaSuccess;  // does not fit: cost stays -1
+  const long slots = (long)occ * dev.sm_count;
   long min_chunks = 1L << 30;
   for (int i = 0; i < n; ++i)
     if (ms[i].cols / kTK < min_chunks) min_chunks = ms[i].cols / kTK;
@@ -535,18 +579,27 @@ cudaError_t plan_typed(const MatrixRef* ms, int n, int batch, const DeviceInfo& 
       best.grid = (int)grid;
     }
   }
-  best.smem = smem;
+  best.smem = C::smem_bytes(batch);
+  best.per_sm = occ;
+  // without the reduction area an SM may hold more CTAs: taken when the items fill them
+  if (occ_slot > occ && best.nitems >= (long)occ_slot * dev.sm_count) {
+    best.rs = true;
+    best.smem = smem_rs;
+    best.per_sm = occ_slot;
+    best.grid = occ_slot * dev.sm_count;
+  }
   *out = best;
   return cudaSuccess;
 }
 
 // XQ: xs[i] is the problem's activation quants (batch x cols bytes), xds[i] their scales
 // (batch x cols / 32 floats).
-template <int WT, bool F16, bool XBF16, int NW, bool XQ = false>
+template <int WT, bool F16, bool XBF16, int NW, bool XQ = false, bool RS = false>
 cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* const* xs, float* const* ys, int n,
                          int batch, bool pdl, const DeviceInfo& dev, cudaStream_t stream,
                          const float* const* xds = nullptr) {
-  using C = Cfg<WT, F16, XBF16, NW, XQ>;
+  using C = Cfg<WT, F16, XBF16, NW, XQ, RS>;
+  if (plan.rs != RS || plan.smem < C::smem_bytes(batch)) return cudaErrorInvalidValue;
   Params p{};
   p.nprob = n;
   p.batch = batch;
@@ -594,17 +647,31 @@ cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* cons
     if (err != cudaSuccess) return err;
   }
 
+  // A grid smaller than the SMs can hold: each CTA asks for enough shared memory that an SM
+  // holds no more CTAs than the grid needs per SM, so the hardware spreads the CTAs over all
+  // SMs instead of filling some (14336 x 4096 Q4_0 at 4 bf16 vectors, 344 CTAs, four per SM
+  // allowed: 11.0 against 9.2 us with at most three)
+  int smem = plan.smem;
+  const int need = (plan.grid + dev.sm_count - 1) / dev.sm_count;
+  if (need < plan.per_sm && dev.smem_per_sm > 0) {
+    const size_t spread = (dev.smem_per_sm / (size_t)(need + 1) + 128 - dev.smem_reserved + 127) / 128 * 128;
+    if (spread > (size_t)smem && spread <= dev.smem_optin) smem = (int)spread;
+  }
+  if (smem > plan.smem) {
+    const cudaError_t err = raise_smem_limit<WT, F16, XBF16, NW, XQ, RS>(dev.device, smem);
+    if (err != cudaSuccess) return err;
+  }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(plan.grid);
   cfg.blockDim = dim3(NW * 32);
-  cfg.dynamicSmemBytes = plan.smem;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, matvec_mma_kernel<WT, F16, XBF16, NW, XQ>, maps, p);
+  return cudaLaunchKernelEx(&cfg, matvec_mma_kernel<WT, F16, XBF16, NW, XQ, RS>, maps, p);
 }
 
 // 4 warps per CTA; when that leaves SMs without a CTA (a launch with few tiles), 8 or 16
@@ -616,8 +683,11 @@ cudaError_t launch_best(const MatrixRef* ms, const void* const* xs, float* const
   Plan p4, p8, p16;
   cudaError_t err = plan_typed<WT, F16, XBF16, 4, XQ>(ms, n, batch, dev, &p4);
   if (err != cudaSuccess) return err;
-  if (p4.cost >= 0 && p4.grid > dev.sm_count)
-    return launch_typed<WT, F16, XBF16, 4, XQ>(p4, ms, xs, ys, n, batch, pdl, dev, stream, xds);
+  auto launch4 = [&]() {
+    return p4.rs ? launch_typed<WT, F16, XBF16, 4, XQ, true>(p4, ms, xs, ys, n, batch, pdl, dev, stream, xds)
+                 : launch_typed<WT, F16, XBF16, 4, XQ>(p4, ms, xs, ys, n, batch, pdl, dev, stream, xds);
+  };
+  if (p4.cost >= 0 && p4.grid > dev.sm_count) return launch4();
   err = plan_typed<WT, F16, XBF16, 8, XQ>(ms, n, batch, dev, &p8);
   if (err != cudaSuccess) return err;
   err = plan_typed<WT, F16, XBF16, 16, XQ>(ms, n, batch, dev, &p16);
@@ -627,7 +697,7 @@ cudaError_t launch_best(const MatrixRef* ms, const void* const* xs, float* const
     return launch_typed<WT, F16, XBF16, 16, XQ>(p16, ms, xs, ys, n, batch, pdl, dev, stream, xds);
   if (better(p8, p4)) return launch_typed<WT, F16, XBF16, 8, XQ>(p8, ms, xs, ys, n, batch, pdl, dev, stream, xds);
   if (p4.cost < 0) return cudaErrorInvalidConfiguration;
-  return launch_typed<WT, F16, XBF16, 4, XQ>(p4, ms, xs, ys, n, batch, pdl, dev, stream, xds);
+  return launch4();
 }
 
 }  // namespace
@@ -638,21 +708,30 @@ bool matvec_mma_supported(const MatrixRef& m) {
 
 int matvec_mma_max_problems() { return kMaxProblems; }
 
-cudaError_t launch_matvec_qx_mma(const MatrixRef& m, const int8_t* xq, const float* xd, int batch, float* y,
-                                 bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
-  if (batch < 1 || !matvec_mma_supported(m)) return cudaErrorInvalidValue;
+cudaError_t launch_matvec_qx_mma(const MatrixRef* ms, const int8_t* const* xq, const float* const* xd, int n,
+                                 int batch, float* const* ys, bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
+  if (batch < 1 || n < 1 || n > kMaxProblems) return cudaErrorInvalidValue;
+  for (int i = 0; i < n; ++i)
+    if (!matvec_mma_supported(ms[i]) || ms[i].wtype != ms[0].wtype || ms[i].scale_f16 != ms[0].scale_f16)
+      return cudaErrorInvalidValue;
+  const MatrixRef& m = ms[0];
   for (int b0 = 0; b0 < batch; b0 += kMaxBatch) {
     const int nb = (batch - b0) < kMaxBatch ? (batch - b0) : kMaxBatch;
-    const void* xs[1] = {xq + (size_t)b0 * (size_t)m.cols};
-    const float* xds[1] = {xd + (size_t)b0 * (size_t)(m.cols / 32)};
-    float* ys[1] = {y + (size_t)b0 * (size_t)m.rows};
+    const void* xs[kMaxProblems];
+    const float* xds[kMaxProblems];
+    float* yp[kMaxProblems];
+    for (int i = 0; i < n; ++i) {
+      xs[i] = xq[i] + (size_t)b0 * (size_t)ms[i].cols;
+      xds[i] = xd[i] + (size_t)b0 * (size_t)(ms[i].cols / 32);
+      yp[i] = ys[i] + (size_t)b0 * (size_t)ms[i].rows;
+    }
     cudaError_t err;
     if (m.wtype == QMV_Q4_0)
-      err = m.scale_f16 ? launch_best<QMV_Q4_0, true, true, true>(&m, xs, ys, 1, nb, pdl, dev, stream, xds)
-                        : launch_best<QMV_Q4_0, false, true, true>(&m, xs, ys, 1, nb, pdl, dev, stream, xds);
+      err = m.scale_f16 ? launch_best<QMV_Q4_0, true, true, true>(ms, xs, yp, n, nb, pdl, dev, stream, xds)
+                        : launch_best<QMV_Q4_0, false, true, true>(ms, xs, yp, n, nb, pdl, dev, stream, xds);
     else
-      err = m.scale_f16 ? launch_best<QMV_Q8_0, true, true, true>(&m, xs, ys, 1, nb, pdl, dev, stream, xds)
-                        : launch_best<QMV_Q8_0, false, true, true>(&m, xs, ys, 1, nb, pdl, dev, stream, xds);
+      err = m.scale_f16 ? launch_best<QMV_Q8_0, true, true, true>(ms, xs, yp, n, nb, pdl, dev, stream, xds)
+                        : launch_best<QMV_Q8_0, false, true, true>(ms, xs, yp, n, nb, pdl, dev, stream, xds);
     if (err != cudaSuccess) return err;
   }
   return cudaSuccess;

@@ -300,6 +300,16 @@ cudaError_t reset_workspaces() {
   return cudaDeviceSynchronize();
 }
 
+size_t split_buffer_bytes() { return kSplitBytes; }
+
+cudaError_t stream_split_buffer(const DeviceInfo& dev, cudaStream_t stream, uint8_t** base) {
+  Workspace xw;
+  const cudaError_t err = cached_workspace(g_xws, dev, stream, kSplitBytes, 0, &xw);
+  if (err != cudaSuccess) return err;
+  *base = reinterpret_cast<uint8_t*>(xw.partials);
+  return cudaSuccess;
+}
+
 cudaError_t prepare_stream_workspaces(const DeviceInfo& dev, cudaStream_t stream) {
   Workspace w;
   cudaError_t err = cached_workspace(g_ws, dev, stream, kStreamWorkspaceBytes, kStreamCounters, &w);

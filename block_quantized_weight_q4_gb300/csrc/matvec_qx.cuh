@@ -242,8 +242,8 @@ cudaError_t launch_wtype(const MatrixRef& m, const int8_t* xq, const float* xd, 
 
 // ------------------------------------------------------------------------ fused activations
 // The same product for several problems in one launch, each with its float activations (bf16
-// or f32) quantized inside the kernel with the runtime's rule (act_q8_block, the bytes
-// qmv_quantize_x writes) into shared memory, from where the loop above reads them.  CTAs are
+// or f32) quantized inside the kernel with the runtime's rule (the bytes qmv_quantize_x
+// writes) into shared memory, from where the loop above reads them.  CTAs are
 // persistent (one wave, by occupancy) and walk items of kWarps / ks row groups, problem after
 // problem; a CTA quantizes a problem's activations when it first meets them (problems that
 // share one x pointer share one quantization), so the quantizer's work is spread over all the
@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(kWarps * 32, MinCtas<R, NV>::value)
     if (b0 < nb) cur.load(P.q, P.d, row, nb, b0);  // weights: independent of the preceding kernel
     if (first) griddep_wait();  // the activations may be the preceding kernel's output
     if (P.x != quantized) {
-      // the runtime's rule (act_q8_block) with each block spread over four consecutive lanes,
+      // the runtime's rule with each block spread over four consecutive lanes,
       // eight values each (few registers next to the prefetched tile): the block's amax by two
       // shuffles, then every lane the same scale and its eight quants
       __syncthreads();  // the previous activations are no longer read

@@ -86,6 +86,13 @@ cudaError_t current_device_info(DeviceInfo* info) {
     int optin = 0;
     if ((err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return err;
     d.smem_optin = (size_t)optin;
+    int per_sm = 0, reserved = 0;
+    if ((err = cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess)
+      return err;
+    if ((err = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess)
+      return err;
+    d.smem_per_sm = (size_t)per_sm;
+    d.smem_reserved = (size_t)reserved;
     void* sym = nullptr;
     if ((err = cudaGetSymbolAddress(&sym, g_device_status)) != cudaSuccess) return err;
     d.status = static_cast<int*>(sym);
@@ -481,7 +488,8 @@ int qmv_matvec_qx(int wtype, int scale_dtype, int64_t rows, int64_t cols, const 
   // 2 or more vectors, cols a multiple of 256: the block dots on the tensor core (quants and
   // levels as exact halves); else the dp4a kernel
   if (batch >= 2 && matvec_mma_supported(m))
-    return launch_matvec_qx_mma(m, xqq, xd, batch, y, false, dev, stream) == cudaSuccess ? QMV_OK : QMV_E_CUDA;
+    return launch_matvec_qx_mma(&m, &xqq, &xd, 1, batch, &y, false, dev, stream) == cudaSuccess ? QMV_OK
+                                                                                                 : QMV_E_CUDA;
   return launch_matvec_qx(m, xqq, xd, batch, y, dev, stream) == cudaSuccess ? QMV_OK : QMV_E_CUDA;
 }
 
@@ -527,6 +535,52 @@ int qmv_matvec_qx_grouped(int wtype, int scale_dtype, int x_dtype, int batch, co
                                   stream) == cudaSuccess
                ? QMV_OK
                : QMV_E_CUDA;
+  // two or more vectors, every problem's cols a multiple of 256, the images within the stream's
+  // split buffer: a quantizer launch writes each distinct activation array's image there (the
+  // bytes qmv_quantize_x writes), then the tensor-core mode of the mma.sync kernel, launched as
+  // its programmatic dependent, takes the block dots (65536 x 4096 Q4_0 at 8 vectors: about half
+  // the dp4a kernel's time, whose CTAs each quantize the activations again)
+  bool two_step = batch >= 2;
+  for (int i = 0; i < n && two_step; ++i) two_step = matvec_mma_supported(ms[i]);
+  if (two_step) {
+    QxImages im{};
+    int owner[QMV_MAX_GROUP];  // the image problem i reads
+    int nim = 0;
+    size_t need = 0;
+    auto round256 = [](size_t b) { return (b + 255) / 256 * 256; };
+    for (int i = 0; i < n; ++i) {
+      owner[i] = -1;
+      for (int j = 0; j < i && owner[i] < 0; ++j)
+        if (xs[j] == xs[i] && ms[j].cols == ms[i].cols) owner[i] = owner[j];
+      if (owner[i] >= 0) continue;
+      owner[i] = nim;
+      im.x[nim] = xs[i];
+      im.nblk[nim] = (long long)batch * (ms[i].cols / 32);
+      need += round256((size_t)batch * (size_t)ms[i].cols) + round256((size_t)im.nblk[nim] * 4);
+      ++nim;
+    }
+    // (a stream captured before its first such call has no buffer yet: the dp4a kernel then)
+    uint8_t* base = nullptr;
+    two_step = need <= split_buffer_bytes() && stream_split_buffer(dev, stream, &base) == cudaSuccess;
+    if (two_step) {
+      for (int k = 0; k < nim; ++k) {
+        im.q[k] = base;
+        base += round256((size_t)im.nblk[k] * 32);
+        im.d[k] = reinterpret_cast<float*>(base);
+        base += round256((size_t)im.nblk[k] * 4);
+      }
+      if (launch_quantize_x_group(x_dtype == QMV_X_BF16, im, nim, (flags & QMV_FLAG_OVERLAP) != 0, stream) !=
+          cudaSuccess)
+        return QMV_E_CUDA;
+      const int8_t* xq[QMV_MAX_GROUP];
+      const float* xd[QMV_MAX_GROUP];
+      for (int i = 0; i < n; ++i) {
+        xq[i] = reinterpret_cast<const int8_t*>(im.q[owner[i]]);
+        xd[i] = im.d[owner[i]];
+      }
+      return launch_matvec_qx_mma(ms, xq, xd, n, batch, ys, true, dev, stream) == cudaSuccess ? QMV_OK : QMV_E_CUDA;
+    }
+  }
   return launch_matvec_qx_fused(ms, xs, ys, n, x_dtype == QMV_X_BF16, batch, (flags & QMV_FLAG_OVERLAP) != 0, dev,
                                 stream) == cudaSuccess
              ? QMV_OK

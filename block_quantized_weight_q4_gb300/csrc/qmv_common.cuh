@@ -376,43 +376,16 @@ __device__ __forceinline__ void split_bf16_pair(float v, uint16_t& hi, uint16_t&
 
 
 // ---------------------------------------------------------------------------- activation rule
-// The runtime's activation quantizer on one block of 32 values (Krafla page, "Quantization
-// rule", Q8_0 with a float32 scale): amax = max |x|; amax < 1e-30 gives the zero block (d = 0,
-// every quant 0); else d = amax / 127 and q = trunc(x * (127 / amax) + copysign(0.5, x)),
-// clamped to +-127; each step one float32 operation rounded to nearest.  w[g] holds quants
-// 4g..4g+3 (byte k = quant 4g + k); returns d.
-__device__ __forceinline__ float act_q8_block(const float (&x)[32], uint32_t (&w)[8]) {
-  float amax = 0.f;
-#pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    const float a = fabsf(x[e]);
-    if (a > amax) amax = a;
-  }
-  float inv = 0.f, d = 0.f;  // the zero block
-  if (!(amax < 1e-30f)) {
-    inv = __fdiv_rn(127.0f, amax);
-    d = __fdiv_rn(amax, 127.0f);
-  }
-#pragma unroll
-  for (int g = 0; g < 8; ++g) {
-    uint32_t packed = 0;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      // inv = 0 gives trunc(+-0.5) = 0 with no branch; the conversion truncates
-      const float xe = x[4 * g + k];
-      int v = (int)__fadd_rn(__fmul_rn(xe, inv), copysignf(0.5f, xe));
-      v = v > 127 ? 127 : (v < -127 ? -127 : v);
-      packed |= (uint32_t)(v & 0xFF) << (8 * k);
-    }
-    w[g] = packed;
-  }
-  return d;
-}
-
-// The same rule on NCH blocks at once, each held by four lanes (lanes 4g .. 4g+3 of the warp hold
-// block g of chunk h, 8 values each, v[h]): each block's amax by two xor shuffles (the same
-// maximum as act_q8_block's); the divisions 127 / amax and amax / 127 of all NCH blocks in one
-// pass over the four lanes (lane 4g + 2h + r divides for chunk h, r = 0: d, r = 1: 1 / d), then
+// The runtime's activation quantizer (Krafla page, "Quantization rule", Q8_0 with a float32
+// scale) on a block of 32 values: amax = max |x|; amax < 1e-30 gives the zero block (d = 0, every
+// quant 0); else d = amax / 127 and q = trunc(x * (127 / amax) + copysign(0.5, x)), clamped to
+// +-127; each step one float32 operation rounded to nearest.  The kernels that apply it hold a
+// block in four lanes, eight values each.
+//
+// The rule on NCH blocks at once, each held by four lanes (lanes 4g .. 4g+3 of the warp hold
+// block g of chunk h, 8 values each, v[h]): each block's amax by two xor shuffles (the maximum
+// does not depend on the order; NaN is skipped); the divisions 127 / amax and amax / 127 of all
+// NCH blocks in one pass over the four lanes (lane 4g + 2h + r divides for chunk h, r = 0: d, r = 1: 1 / d), then
 // each value's quant by the same float32 steps, returned as IEEE half pairs (exact: |q| <= 127),
 // hq[h][i] = (q(v[h][2i]) low, q(v[h][2i+1]) high), and d[h] the block's scale.
 template <int NCH>
@@ -453,39 +426,11 @@ __device__ __forceinline__ void act_q8_lane_quarters(const float (&v)[NCH][8], u
       for (int j = 0; j < 2; ++j) {
         // the rule's clamp to +-127 never acts here: |x| <= amax gives |x * inv| <= 127 (1 + 2^-23)
         // and a sum below 128 before the truncation; a value that is not finite gives NaN, whose
-        // conversion is 0, as in act_q8_block
+        // conversion is 0 with or without the clamp
         const float xe = v[h][2 * i + j];
         q[j] = (float)(int)__fadd_rn(__fmul_rn(xe, inv), copysignf(0.5f, xe));
       }
       asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(hq[h][i]) : "f"(q[1]), "f"(q[0]));
-    }
-  }
-}
-
-// 32 activations (float32, or bfloat16 widened exactly) starting at element `first` of x.
-template <bool BF16>
-__device__ __forceinline__ void load_act_block(const void* __restrict__ x, long long first, float (&v)[32]) {
-  if (BF16) {
-    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + first);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4 u = __ldg(p + i);
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        v[8 * i + 2 * k] = __uint_as_float(w[k] << 16);  // element 2k: the low half
-        v[8 * i + 2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
-      }
-    }
-  } else {
-    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(x) + first);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float4 f = __ldg(p + i);
-      v[4 * i] = f.x;
-      v[4 * i + 1] = f.y;
-      v[4 * i + 2] = f.z;
-      v[4 * i + 3] = f.w;
     }
   }
 }

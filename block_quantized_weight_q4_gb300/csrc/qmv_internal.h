@@ -22,6 +22,8 @@ struct DeviceInfo {
   int sm_count;
   int cc_major, cc_minor;
   size_t smem_optin;
+  size_t smem_per_sm;     // shared memory of one SM
+  size_t smem_reserved;   // of it, what the system keeps per resident CTA
   int* status;  // device address of this device's status word
 };
 
@@ -75,14 +77,32 @@ cudaError_t launch_gguf_to_mlb(int wtype, int64_t rows, int64_t cols, const void
 // The activation quantizer (Q8_0 rule, f32 scale) into xq (q at xq, d at xq + d_off).
 cudaError_t launch_quantize_x(bool x_bf16, int64_t batch, int64_t cols, const void* x, uint8_t* xq, int64_t d_off,
                               int64_t q_bytes, cudaStream_t stream);
+// The same rule for up to 8 activation arrays in one launch (x[i]: nblk[i] blocks of 32, bf16 or
+// f32; the quants to q[i], the scales to d[i]).  The kernel lets the next launch start at once
+// (its dependents wait for it to finish); pdl: launch as a programmatic dependent (x is read
+// only after the preceding kernel has finished).
+struct QxImages {
+  static constexpr int kMax = 8;
+  const void* x[kMax];
+  uint8_t* q[kMax];
+  float* d[kMax];
+  long long nblk[kMax];
+};
+cudaError_t launch_quantize_x_group(bool x_bf16, const QxImages& a, int n, bool pdl, cudaStream_t stream);
 // The activation-quantized product y[v][r] = sum_b d_w d_x (integer dot of levels and quants);
 // xq / xd: the quants and scales of the batch x cols Q8_0 / f32 activation image.
 cudaError_t launch_matvec_qx(const MatrixRef& m, const int8_t* xq, const float* xd, int batch, float* y,
                              const DeviceInfo& dev, cudaStream_t stream);
 // The same product on the tensor core (quants and levels as exact halves, mma.sync), cols % 256
-// == 0, batch in passes of up to 8.  pdl: launch as a programmatic dependent.
-cudaError_t launch_matvec_qx_mma(const MatrixRef& m, const int8_t* xq, const float* xd, int batch, float* y,
-                                 bool pdl, const DeviceInfo& dev, cudaStream_t stream);
+// == 0, for 1..matvec_mma_max_problems() problems of one weight type and scale type (problem i:
+// ms[i], its image xq[i] / xd[i], ys[i]), batch in passes of up to 8.  pdl: launch as a
+// programmatic dependent.
+cudaError_t launch_matvec_qx_mma(const MatrixRef* ms, const int8_t* const* xq, const float* const* xd, int n,
+                                 int batch, float* const* ys, bool pdl, const DeviceInfo& dev, cudaStream_t stream);
+// The stream's split buffer (split_buffer_bytes(), 256-byte aligned, allocated on first use and
+// kept), which the float32 split routes and the grouped activation-quantized route write into.
+size_t split_buffer_bytes();
+cudaError_t stream_split_buffer(const DeviceInfo& dev, cudaStream_t stream, uint8_t** base);
 // The same product for 1..8 problems of one weight type and scale type in one launch per pass
 // of 8 vectors, each with its float activations (batch x cols, bf16 or f32), which the kernel
 // quantizes itself (the bytes launch_quantize_x writes) into shared memory: needs

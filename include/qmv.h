@@ -364,8 +364,14 @@ int qmv_matvec_qx(int wtype, int scale_dtype, int64_t rows, int64_t cols, const 
  * vector (batch 1) in groups under 96 MB of weights with every problem's cols a multiple of 256
  * runs the block-diagonal kernel: each warp quantizes the 256-column chunks it streams (four
  * lanes to a block of 32), and the quants and the levels enter the tensor core as IEEE halves,
- * whose block dot products are the exact integer sums.  Every other batch and group (the larger
- * groups measured faster there) runs the dp4a kernel, whose CTAs each quantize their problem's
+ * whose block dot products are the exact integer sums.  Two or more vectors with every
+ * problem's cols a multiple of 256 take two launches: a quantizer writes the image of each
+ * distinct activation array (qmv_quantize_x's bytes) into the calling stream's split buffer
+ * (2 MiB of device memory, allocated on the stream's first such call and kept), and the
+ * tensor-core mode of qmv_matvec_qx, launched as its programmatic dependent (its weight loads
+ * overlap the quantizer), reads them there.  Every other batch and group (one vector on
+ * larger groups, where it measured faster; images beyond the buffer; a stream captured before
+ * it has its buffer) runs the dp4a kernel, whose CTAs each quantize their problem's
  * activations into shared memory (a few KB per vector) and read them from there.  All n
  * problems share wtype, scale_dtype, x_dtype and batch; each has its own rows, cols, W, x and y
  * (problems of one layer that read the same activations: pass the same x).
@@ -376,9 +382,7 @@ int qmv_matvec_qx(int wtype, int scale_dtype, int64_t rows, int64_t cols, const 
  *   else QMV_E_ARG.
  * Results agree with those of qmv_quantize_x followed by qmv_matvec_qx within the tolerance stated
  * there (the column slices may be added in a different grouping) and do not depend on timing.
- * At 2..8 vectors the two-step route (qmv_quantize_x, then qmv_matvec_qx on the tensor core)
- * measured about twice as fast (65536 x 4096 Q4_0 at 8 vectors: 1.7 + 46 against 95 us).
- * Allocates nothing.  Asynchronous.  Returns as qmv_matvec_grouped. */
+ * Allocates nothing but the split buffer.  Asynchronous.  Returns as qmv_matvec_grouped. */
 #define QMV_QX_MAX_VEC_COLS 200704
 int qmv_matvec_qx_grouped(int wtype, int scale_dtype, int x_dtype, int batch, const qmv_problem *problems, int n,
                           unsigned flags, cudaStream_t stream);

@@ -238,6 +238,28 @@ def test_workload_full_size(qmv, name):
         del Wd, out
 
 
+@pytest.mark.parametrize("wt,sf,rows,cols,batch", [
+    (2, 1, 65536, 4096, 4),    # mma.sync kernel, four CTAs per SM without the reduction area (split tiles meet in q slots)
+    (2, 1, 65536, 4096, 6),
+    (2, 1, 14336, 4096, 2),    # fewer CTAs than the SMs hold: spread by their shared-memory request
+    (1, 0, 151936, 1024, 4),
+])
+def test_small_batch_large_launches_sampled_and_repeatable(qmv, wt, sf, rows, cols, batch):
+    import torch
+    rng = np.random.default_rng(rows + batch)
+    m = inputs.make_matrix(wt, sf, rows, cols, seed=rows + cols + wt + batch)
+    x = inputs.make_x(batch, cols, True, seed=rows + batch)
+    Wd, xd = dev_u8(m.W), dev_x(x)
+    y1 = qmv.matvec(wt, sf, rows, cols, Wd, xd)
+    y2 = qmv.matvec(wt, sf, rows, cols, Wd, xd)
+    torch.cuda.synchronize()
+    y1 = y1.cpu().numpy()
+    assert_bits_equal(y1, y2.cpu().numpy(), f"repeat {rows}x{cols} b{batch}")
+    ids = sample_rows(rows, rng)
+    y_ref, absref = oracle.matvec_rows(m.W, wt, sf, rows, cols, x, ids)
+    check_product(y1[:, ids], y_ref, absref, TOL, f"{rows}x{cols} b{batch}")
+
+
 # ---------------------------------------------------------------- grouped launches
 @pytest.mark.parametrize("wt,sf", TYPES)
 @pytest.mark.parametrize("batch", [1, 5, 8])

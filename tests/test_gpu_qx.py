@@ -127,6 +127,8 @@ def test_matvec_qx_exact_case(qmv, wt, batch, cols):
     (1, 0, 11008, 4096, 8),    # Q8_0, two rows per warp
     (2, 0, 4096, 11008, 1),    # one row per warp, 344 blocks per row
     (1, 1, 151936, 1024, 1),   # the Q8_0 classifier shape
+    (2, 1, 65536, 4096, 8),    # tensor-core mode, four CTAs per SM, split tiles meeting in the q slots
+    (1, 0, 151936, 1024, 8),
 ])
 def test_matvec_qx_full_size_sampled_rows(qmv, wt, sf, rows, cols, batch):
     import torch
@@ -301,6 +303,9 @@ def test_matvec_qx_grouped_repeat_overlap_and_graph_bit_identical(qmv):
     y2 = torch.empty_like(y1)
     g = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream()
+    with torch.cuda.stream(s):  # the stream's first call creates its split buffer (not while captured)
+        qmv.matvec_qx_grouped(2, 1, [(rows, cols, W, xd, y2)])
+    torch.cuda.synchronize()
     with torch.cuda.graph(g, stream=s):
         xd.copy_(xsrc)   # the activations come from the kernel just before the product
         qmv.matvec_qx_grouped(2, 1, [(rows, cols, W, xd, y2)], overlap=True)
@@ -317,4 +322,68 @@ def test_matvec_qx_grouped_repeat_overlap_and_graph_bit_identical(qmv):
     y_ref, absref = oracle.matvec_qx(sub_matrix(m, ids), 2, 1, ids.size, cols, xq.cpu().numpy(), batch)
     check_product(first[:, ids], y_ref, absref, tol=1e-4, what="fused")
     check_product(y3.cpu().numpy()[:, ids], y_ref, absref, tol=1e-4, what="two-step")
+    assert qmv.last_error() == 0
+
+
+@pytest.mark.parametrize("wt", [1, 2])
+@pytest.mark.parametrize("batch", [2, 8, 11])
+def test_matvec_qx_grouped_two_step_exact_case(qmv, wt, batch):
+    # two or more vectors, cols multiples of 256 (the quantizer launch, then the mma.sync
+    # kernel's tensor-core mode on the images in the stream's split buffer): the exact case
+    # (integer block sums, power-of-two scales) bit for bit, with two problems sharing one
+    # activation array, one with its own, and 11 vectors taking two passes
+    import torch
+    rng = np.random.default_rng(140 + wt + batch)
+    mats = []
+    for rows, cols in [(33, 512), (100, 512), (17, 256)]:
+        if wt == 1:
+            q = rng.integers(-127, 128, rows * cols).astype(np.int8).view(np.uint8)
+        else:
+            q = rng.integers(0, 256, rows * cols // 2).astype(np.uint8)
+        d = np.full(rows * cols // 32, 2.0 ** -6, np.float32).view(np.uint32)
+        W = inputs.assemble(wt, 0, rows, cols, q, d)
+        mats.append(inputs.Matrix(wt, 0, rows, cols, W, q, d.reshape(rows, cols // 32)))
+    xs = []
+    for cols in (512, 256):
+        k = rng.integers(-127, 128, (batch, cols // 32, 32))
+        k[:, :, 7] = 127
+        k[:, ::5] = 0  # zero blocks
+        xs.append((k * 2.0 ** -4).reshape(batch, cols).astype(np.float32))
+    x512 = dev_x(xs[0])
+    probs = [(m.rows, m.cols, dev_u8(m.W), x512 if m.cols == 512 else dev_x(xs[1]),
+              torch.full((batch, m.rows), 9.0, device="cuda")) for m in mats]
+    qmv.matvec_qx_grouped(wt, 0, probs)
+    torch.cuda.synchronize()
+    for m, p in zip(mats, probs):
+        y_ref, _ = oracle_qx(m, xs[0] if m.cols == 512 else xs[1], False)
+        assert np.array_equal(p[4].cpu().numpy().astype(np.float64), y_ref), \
+            f"exact two-step qx {wt} b{batch} {m.rows}x{m.cols}"
+    assert qmv.last_error() == 0
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_matvec_qx_grouped_two_step_equals_quantize_then_product(qmv, bf16):
+    # one problem of 2..8 vectors: the grouped call's two launches are qmv_quantize_x and
+    # qmv_matvec_qx's tensor-core mode, so the results are the same bits; a stream captured before
+    # its first call (no split buffer yet) takes the dp4a kernel, within the tolerance
+    import torch
+    rows, cols, batch = 3000, 2048, 6
+    m = inputs.make_matrix(2, 1, rows, cols, seed=71)
+    x = activations(np.random.default_rng(72), batch, cols)
+    xin = inputs.bf16_codes(x) if bf16 else x
+    W, xd = dev_u8(m.W), dev_x(xin)
+    y1 = torch.empty((batch, rows), device="cuda")
+    qmv.matvec_qx_grouped(2, 1, [(rows, cols, W, xd, y1)])
+    y2 = qmv.matvec_qx(2, 1, rows, cols, W, qmv.quantize_x(xd), batch)
+    torch.cuda.synchronize()
+    assert_bits_equal(y1.cpu().numpy(), y2.cpu().numpy(), "grouped two-step against the two calls")
+    y3 = torch.empty_like(y1)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=torch.cuda.Stream()):
+        qmv.matvec_qx_grouped(2, 1, [(rows, cols, W, xd, y3)])
+    g.replay()
+    torch.cuda.synchronize()
+    y_ref, absref = oracle_qx(m, x, bf16)
+    check_product(y3.cpu().numpy(), y_ref, absref, tol=1e-4, what="captured without a split buffer")
+    check_product(y1.cpu().numpy(), y_ref, absref, tol=1e-4, what="two-step")
     assert qmv.last_error() == 0
