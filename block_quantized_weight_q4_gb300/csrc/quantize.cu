@@ -4,10 +4,10 @@
 //   Q8_0 (per block of 32): amax = max |x|.  amax < 1e-30: d = 0 and every quant 0.
 //     f32 scale: d = amax / 127, q = trunc(x * (127 / amax) + copysign(0.5, x)).
 //     f16 scale: d = the f16 nearest amax / 127 (ties to even; a d beyond the f16 range is
-//     refused), q = trunc(x * (1 / d) + copysign(0.5, x)) against that d (d rounding to
+//     refused), q = trunc(x * (1 / d) + copysign(0.5, x)) with the f16 d (d rounding to
 //     f16 zero gives the zero block).  q clamped to +-127.
 //   Q4_0, the "round" rule: d = (element of largest magnitude, the first of equals) / -8,
-//     rounded to the nearest f16 first with f16 scales (refused beyond the f16 range);
+//     first rounded to f16 (to nearest) with f16 scales (refused beyond the f16 range);
 //     nibble = min(15, trunc(x * (1 / d) + 8.5)), kept at or above 0; 1 / d taken as 0
 //     for d = 0.  Element j's nibble is the low half of byte j, element j + 16's the high.
 // Every product, quotient and sum is one IEEE float32 operation rounded to nearest even

@@ -3,24 +3,29 @@
  * matrices on NVIDIA GB300 (sm_103a).
  *
  * Format (Krafla ".mlb model format v1" page, sections "Body", "Q8_0", "Q4_0"):
- *   A rows x cols matrix (cols a multiple of 32) is two arrays written one after the
- *   other, each zero-padded to a multiple of 64 bytes (the pad after the last array is
- *   optional and never read here):
+ *   A rows x cols matrix (cols a multiple of 32) is stored as its q array, then its d
+ *   array, each array's length rounded up to a 64-byte boundary with zero bytes (the tail
+ *   of the last array is never read here, so whether a file carries it does not matter):
  *     q : Q8_0: rows*cols int8 quants, row-major.
  *         Q4_0: rows*cols/2 bytes; block k of row r is the 16 bytes at r*cols/2 + 16k;
- *               byte j holds element j in its low nibble and element j+16 in its high
- *               nibble; the weight is (nibble - 8) * d.
- *     d : rows*cols/32 scales, one per block of 32 consecutive weights of a row (scale
- *         index r*cols/32 + k); float32, or IEEE binary16 when the file's scale_f16
- *         flag is 1.  Q8_0 weight = q * d.
- *   The product is y[r] = sum_c W[r][c] * x[c] ("one row per output").
+ *               the low four bits of byte j are the block's element j, the high four bits
+ *               its element j+16; the weight is (nibble - 8) * d.
+ *     d : rows*cols/32 scales: the scale of row r's k-th run of 32 weights at index
+ *         r*cols/32 + k; float32, or IEEE binary16 when the file's scale_f16 flag is 1.
+ *         Q8_0 weight = q * d.
+ *   Row r of the matrix gives output r: y[r] = sum_c W[r][c] * x[c].
  *
  * Conventions for every entry point:
  *   - W points at the q array.  The d array starts at W + qmv_scale_offset(...), i.e.
  *     at q's size rounded up to 64 bytes, exactly as in the file.  W must be a device
  *     pointer aligned to 16 bytes (the file format gives 64).
  *   - x is batch x cols, row-major, float32 or bfloat16; y is batch x rows float32,
- *     row-major.  Device pointers, 16-byte aligned for x and out, 4 for y.
+ *     row-major.  Device pointers, 16-byte aligned for x and out, 4 for y.  The y of the
+ *     products (qmv_matvec, qmv_matvec_grouped, qmv_matvec_grouped_noalloc, qmv_matvec_qx,
+ *     qmv_matvec_qx_grouped) may instead be pinned host memory that the device addresses
+ *     directly (cudaHostAlloc or cudaHostRegister memory under unified addressing, the same
+ *     address on both sides): the kernels only store to y, and their stores then cross to
+ *     the host, which saves a copy after the launch.
  *   - All memory is owned by the caller; the library allocates no device memory per
  *     call.  Work is enqueued on `stream` (0 = the legacy default stream) of the calling
  *     thread's current device, and the call returns without waiting, except where noted.
@@ -101,7 +106,7 @@ extern "C" {
 #define QMV_CLASS_W2 64
 
 /* Bytes of a matrix image: q, its padding to 64, then d (no trailing pad).
- * Overflow-checked ("All size arithmetic is overflow-checked").  Returns 0 for an
+ * Every size is computed with overflow checks, as the page requires.  Returns 0 for an
  * invalid wtype, scale_dtype or shape.  Host only. */
 size_t qmv_weight_bytes(int wtype, int scale_dtype, int64_t rows, int64_t cols);
 
@@ -115,8 +120,8 @@ int64_t qmv_scale_offset(int wtype, int scale_dtype, int64_t rows, int64_t cols)
  * QMV_Q4_0, or -1 for an unknown file_wtype or class bit.  Host only. */
 int qmv_matrix_wtype(int file_wtype, uint32_t q8_mask, int class_bit, int shared_classifier);
 
-/* y = W x for a batch of activation vectors (Krafla page, "Matrices are stored row by
- * row, one row per output: y[r] = sum_c W[r][c] x[c]").
+/* y = W x for a batch of activation vectors (Krafla page, "Body": row r of a matrix gives
+ * output r, y[r] = sum_c W[r][c] x[c]).
  *   W     : device, the matrix image described above (q array first).
  *   x     : device, batch x cols, x_dtype (QMV_X_F32 or QMV_X_BF16), row-major.
  *   y     : device, batch x rows float32, row-major; fully overwritten.
@@ -275,19 +280,19 @@ int qmv_matvec_glu(int wtype, int scale_dtype, int64_t rows, int64_t cols, const
                    const void *x, int x_dtype, int act, void *h, unsigned flags, cudaStream_t stream);
 
 /* out[r][c] = level * d as float32, with one float32 multiplication rounded to nearest
- * even (Krafla page, "Q8_0" and "Q4_0"; f16 scales are first converted exactly to
- * float32, "The runtime converts f16 scales to f32 exactly").  No flush of subnormals;
+ * even (Krafla page, "Q8_0" and "Q4_0"; an f16 scale is first widened to float32, which is
+ * exact, as the runtime does when it loads a file).  No flush of subnormals;
  * NaN and infinite scales propagate by IEEE rules.
  *   out : device, rows x cols float32, row-major, 16-byte aligned; fully overwritten.
  * Returns as qmv_matvec. */
 int qmv_dequant(int wtype, int scale_dtype, int64_t rows, int64_t cols, const void *W,
                 float *out, cudaStream_t stream);
 
-/* The loader's quant check (Krafla page, "Q8_0": "The loader rejects any byte equal to
- * -128", reported as ML_E_FORMAT).  Scans the q array on the device and writes to
+/* The loader's quant check (Krafla page, "Q8_0": a file whose Q8_0 quants contain the byte
+ * -128 fails to load, with ML_E_FORMAT).  Scans the q array on the device and writes to
  * *first_bad (device, 8-byte aligned) the smallest byte index into q that holds -128,
- * or -1 when there is none.  Q4_0 has no invalid nibble ("Any d and nibbles are valid
- * input to the runtime"), so for Q4_0 it writes -1.  Asynchronous: the caller reads
+ * or -1 when there is none.  Q4_0 has no invalid nibble (the page accepts every scale and
+ * every nibble), so for Q4_0 it writes -1.  Asynchronous: the caller reads
  * *first_bad after the stream has reached this point.  Returns as qmv_matvec. */
 int qmv_validate(int wtype, int scale_dtype, int64_t rows, int64_t cols, const void *W,
                  int64_t *first_bad, cudaStream_t stream);
@@ -300,7 +305,7 @@ int qmv_validate(int wtype, int scale_dtype, int64_t rows, int64_t cols, const v
  *     f16 scale: d = the f16 nearest amax / 127, q = trunc(x * (1 / d) + copysign(0.5, x))
  *     (a d that rounds to f16 zero gives the zero block); q clamped to +-127.
  *   Q4_0 ("round" rule): d = (element of largest magnitude, the first of equals) / -8,
- *     rounded to the nearest f16 first with f16 scales; nibble = trunc(x * (1 / d) + 8.5)
+ *     first rounded to f16 (to nearest) with f16 scales; nibble = trunc(x * (1 / d) + 8.5)
  *     kept in 0..15, with 1 / d = 0 for d = 0.
  * Each operation is one float32 operation rounded to nearest even, so the bytes equal those
  * of the rules evaluated in that order.  src is meant to be finite (what a NaN or an
@@ -392,9 +397,10 @@ int qmv_matvec_qx_grouped(int wtype, int scale_dtype, int x_dtype, int batch, co
  * m = the element of largest magnitude (the first of equals); for the candidate levels
  * L = -(60 + 2k)/10, k = 0..12 (-6 .. -8.4): s = m / L, l_j = clamp(rint(x_j / s), -8, 7)
  * (ties to even), d = sum(x^3 l) / sum(x^2 l^2) (0 when the denominator is 0), and the
- * candidate with the smallest sum(x^2 (x - d l)^2) wins (the first on ties); a block whose
- * largest magnitude is below 1e-6 is fitted divided by it and d multiplied back; the zero block
- * is d = 0 with every level 0; with f16 scales the winning d is rounded to the nearest f16.
+ * candidate with the smallest sum(x^2 (x - d l)^2) wins (the first on ties); a block with
+ * max |x| under 1e-6 is divided by that maximum before the fit and d multiplied by it after;
+ * the zero block is d = 0 with every level 0; with f16 scales only the winning d goes to f16
+ * (to nearest).
  * Every step is one float32 operation rounded to nearest, sums in element order.  About 13x
  * the round rule's arithmetic per block.  Returns as qmv_quantize. */
 int qmv_quantize_q4_fit(int scale_dtype, int64_t rows, int64_t cols, const float *src, void *W,

@@ -5,9 +5,8 @@
  * leg of the benchmark may load this file's library.  It shares no code, header,
  * table or constant with the CUDA library, and the CUDA library never calls it.
  *
- * Source of every definition below: the Krafla ".mlb model format v1" page
- * (jonpark0.github.io/krafla/file-format.html), sections "Body", "Q8_0", "Q4_0",
- * "Quantization rule" and "Validation done by the loader".  Size arithmetic is also
+ * Source of every definition below: the Krafla ".mlb model format v1" page, sections
+ * "Body", "Q8_0", "Q4_0", "Quantization rule" and "Validation done by the loader".  Size arithmetic is also
  * checked against the worked byte counts of the minfer "02 - GGUF load" page, §2.3-2.4.
  *
  * Everything is written the slow, obvious way: one weight at a time, values taken
@@ -60,8 +59,9 @@
 #define ORACLE_Q4_0 2
 
 /* ---------------------------------------------------------------------------
- * Size arithmetic ("Body": a quantized matrix is two arrays, q then d; each array is
- * zero-padded to a multiple of 64 bytes; the padding after the last array is optional).
+ * Size arithmetic ("Body": a quantized matrix is its q array followed by its d array, each
+ * array's length rounded up to a 64-byte boundary with zeros; a file may leave out the tail
+ * of the last array, which is never read).
  * ------------------------------------------------------------------------- */
 
 static int64_t round_up_64(int64_t n) { return ((n + 63) / 64) * 64; }
@@ -115,8 +115,8 @@ int64_t oracle_scale_offset(int wtype, int scale_f16, int64_t rows, int64_t cols
 /* Value of an IEEE 754 binary16 code, from the format's definition: sign bit,
  * 5-bit biased exponent (bias 15), 10-bit fraction; exponent 0 is subnormal
  * (fraction * 2^-24), exponent 31 is infinity or NaN.  Every binary16 value is a
- * float32 value, so the result is exact ("The runtime converts f16 scales to f32
- * exactly when it loads the file"). */
+ * float32 value, so the result is exact (the page has the runtime widen f16 scales to
+ * f32, exactly, on loading). */
 float oracle_f16_value(uint16_t h)
 {
     int sign = (h >> 15) & 1;
@@ -135,7 +135,7 @@ float oracle_f16_value(uint16_t h)
 }
 
 /* binary16 code nearest to v, ties to even (IEEE default rounding).  Used by the
- * writer rules with f16 scales ("rounded to the nearest f16"). */
+ * writer rules with f16 scales, which round d to f16 (to nearest). */
 uint16_t oracle_f16_bits_rne(float v)
 {
     if (isnan(v)) return 0x7e00;
@@ -196,8 +196,8 @@ static uint32_t bits_from_f32(float f)
  * ------------------------------------------------------------------------- */
 
 /* Integer level of weight (r, c).  Q8_0: the int8 byte (rows*cols bytes, row-major).
- * Q4_0: block k = c/32 of row r is 16 bytes at r*cols/2 + 16k; byte j holds element j
- * in its low nibble and element j+16 in its high nibble; level = nibble - 8. */
+ * Q4_0: block k = c/32 of row r is 16 bytes at r*cols/2 + 16k; element j of the block is
+ * the low four bits of byte j, element j+16 the high four bits; level = nibble - 8. */
 int oracle_level(const uint8_t *W, int wtype, int64_t cols, int64_t r, int64_t c)
 {
     if (wtype == ORACLE_Q8_0) {
@@ -243,8 +243,8 @@ int oracle_dequant(int wtype, int scale_f16, int64_t rows, int64_t cols, const u
 }
 
 /* ---------------------------------------------------------------------------
- * The product y[r] = sum_c W[r][c] * x[c]  ("Matrices are stored row by row, one row
- * per output"), for a batch of activation vectors.  x is batch x cols row-major, f32
+ * The product y[r] = sum_c W[r][c] * x[c]  ("Body": row r of a matrix gives output r), for
+ * a batch of activation vectors.  x is batch x cols row-major, f32
  * or bf16 (x_bf16 = 1); y and absref are batch x n_rows row-major, double.
  * Each weight is level * d evaluated exactly in double (level has 8 bits, d 24), each
  * activation is converted exactly to double, and the sum runs in double in column order.
@@ -302,9 +302,9 @@ int oracle_matvec(int wtype, int scale_f16, int64_t rows, int64_t cols, const ui
 }
 
 /* ---------------------------------------------------------------------------
- * Validation ("Validation done by the loader": a Q8 quant equal to -128 is a format
- * error, because the x86 kernels negate weights and -128 has no int8 negation).
- * Q4_0 has no invalid nibble ("Any d and nibbles are valid input to the runtime").
+ * Validation ("Validation done by the loader": a Q8_0 quant of -128 makes the file a format
+ * error: the x86 kernels flip the sign of weights, and -128 has no int8 opposite).  Every
+ * Q4_0 nibble and every scale is accepted.
  * ------------------------------------------------------------------------- */
 int oracle_validate(int wtype, int scale_f16, int64_t rows, int64_t cols, const uint8_t *W)
 {
@@ -332,8 +332,8 @@ static float clamp127(float t)
 
 /* One Q8_0 block of 32 floats.  f32 scale: amax = max |x|; amax < 1e-30 gives d = 0,
  * q = 0; otherwise d = amax / 127 and q = trunc(x * (127 / amax) + copysign(0.5, x)),
- * clamped to +-127.  f16 scale: d = amax / 127 rounded to the nearest f16 (a d above
- * 65504 is refused), then q = trunc(x * (1 / d) + copysign(0.5, x)) against that d.
+ * clamped to +-127.  f16 scale: d = amax / 127 rounded to f16, to nearest (a d above
+ * 65504 is refused), then q = trunc(x * (1 / d) + copysign(0.5, x)) with the f16 d.
  * Reading for a d that rounds to f16 zero (1 / d infinite): the block is stored as the
  * zero block (parity unpinned: writer-only corner).  d_bits receives the stored scale
  * bits (f32 bits, or the f16 code in the low half). */
@@ -381,8 +381,8 @@ int oracle_quant_q8_block(const float *x, int scale_f16, int8_t *q, uint32_t *d_
 /* One Q4_0 block with the "--q4-rule round" rule: d = (element of largest magnitude) /
  * -8; level = min(15, trunc(x * (1 / d) + 8.5)) - 8.  Readings (parity unpinned,
  * writer-only): the first index wins a tie of magnitudes; an all-zero block (d = 0)
- * uses 1/d = 0, so every level is trunc(8.5) - 8 = 0; with f16 scales d is rounded to
- * the nearest f16 first, as the Q8_0 f16 rule and the best-fit writer do, and the
+ * uses 1/d = 0, so every level is trunc(8.5) - 8 = 0; with f16 scales d is first rounded
+ * to f16 (to nearest), as the Q8_0 f16 rule and the best-fit writer do, and the
  * nibble is also kept at or above 0 (the rounded d can push x/d a hair past -8).
  * qs receives the 16 packed bytes (element j low nibble, element j+16 high nibble). */
 int oracle_quant_q4_round_block(const float *x, int scale_f16, uint8_t *qs, uint32_t *d_bits)
@@ -573,7 +573,7 @@ int oracle_gguf_to_mlb(int wtype, int64_t rows, int64_t cols, const uint8_t *ggu
 /* ---------------------------------------------------------------------------
  * The FFN's gated activation feeding the down projection (Krafla page, "Body": w1 is the gate
  * and w3 the up projection, hidden_dim x dim, w2 the down projection, dim x hidden_dim; header
- * field act: 0 = SiLU, 1 = GELU with the tanh approximation).  Reading: the down projection's
+ * field act: 0 = SiLU, 1 = GELU in its tanh form).  Reading: the down projection's
  * input is h = act(w1 x) * (w3 x), element by element, and the product is y = w2 h.
  *   SiLU(g) = g / (1 + e^-g);   GELU_tanh(g) = g/2 * (1 + tanh(sqrt(2/pi) * (g + 0.044715 g^3))).
  * gate and up are batch x cols float32 (the products w1 x, w3 x); h is evaluated in double.
@@ -623,12 +623,11 @@ int oracle_matvec_glu(int wtype, int scale_f16, int64_t rows, int64_t cols, cons
 
 /* ---------------------------------------------------------------------------
  * The Q4_0 best-fit writer (Krafla page, "Quantization rule": the search tools/mlb.py runs
- * per block).  The page fixes: the block's largest-magnitude element is mapped to each level
- * from -6 to -8.4 in steps of 0.2 (levels clamped to [-8, 7]); for each candidate d is the
- * least-squares fit to those levels with every element weighted by x^2; the candidate with
- * the smallest weighted error wins; a block whose largest magnitude is below 1e-6 is scaled
- * up to 1 for the fit and its d scaled back; d may be negative; with f16 scales the fitted d
- * is rounded to the nearest f16.  Readings (parity pinned only by the invariants in the
+ * per block).  What the page fixes: 13 candidates send the element of largest magnitude
+ * to the levels -6, -6.2, ..., -8.4 (all levels clamped to [-8, 7]); each candidate's d is
+ * the x^2-weighted least-squares scale for its levels; the lowest weighted error picks the
+ * candidate; blocks with max |x| under 1e-6 are brought to unit size for the fit and d is
+ * scaled back; d can come out negative; f16 scales round the chosen d to f16 (to nearest).  Readings (parity pinned only by the invariants in the
  * tests, not by printed values): every step is one float32 operation rounded to nearest even,
  * in this order --
  *   m = the element of largest magnitude (the first of equals), a = |m|;

@@ -56,7 +56,7 @@ def test_q8_mask_dispatch(lib):
     assert m(2, 4 | 64, 4) == 1 and m(2, 4 | 64, 64) == 1 and m(2, 4 | 64, 32) == 2
     # a Q8_0 file stores everything as Q8_0
     assert all(m(1, 0, c) == 1 for c in (1, 2, 4, 8, 16, 32, 64))
-    # shared classifier: tok_emb is Q8_0 if bit 1 or bit 2 is set
+    # with a shared classifier, tok_emb takes Q8_0 when the mask has bit 1 or bit 2
     assert m(2, 2, 1, True) == 1 and m(2, 2, 1, False) == 2 and m(2, 1, 1, True) == 1
     assert m(2, 0, 3) == -1 and m(5, 0, 2) == -1
 

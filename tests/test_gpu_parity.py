@@ -53,7 +53,7 @@ def test_dequant_bit_exact(qmv, wt, sf, rows, cols):
 
 @pytest.mark.parametrize("wt,sf", TYPES)
 def test_dequant_special_scales(qmv, wt, sf):
-    # "Any d and nibbles are valid input": negative, zero, subnormal, huge, inf, NaN scales
+    # every scale is valid input: negative, zero, subnormal, huge, inf, NaN scales
     rows, cols = 4, 256
     m = inputs.make_matrix(wt, sf, rows, cols, seed=5)
     if sf:

@@ -203,7 +203,7 @@ def test_prefill_bf16_weights_one_hot_is_bf16_of_dequant(qmv, wt, sf):
 
 @pytest.mark.parametrize("wt,sf", TYPES)
 def test_prefill_special_scales(qmv, wt, sf):
-    # "Any d and nibbles are valid input": infinite and NaN scales propagate (hi carries them,
+    # every scale is valid input: infinite and NaN scales propagate (hi carries them,
     # lo is zero); zero, negative and f16-subnormal scales (as weights: normal bfloat16 values)
     # and small normal f32 scales meet the bar like any other
     rows, cols, batch = 64, 512, 32

@@ -186,3 +186,36 @@ def test_step_copies_of_any_size_and_offset(qmv, nbytes, offset):
             assert torch.equal(dst[a:b], src[a:b])
             assert torch.equal(mid[a:b].cpu(), src[a:b])
             assert int(dst[:a].sum()) == 0 and int(dst[b:].sum()) == 0   # nothing outside the range
+
+
+@pytest.mark.parametrize("batch,bf16", [(1, True), (3, False), (32, True)])
+def test_products_store_y_into_pinned_host_memory(qmv, batch, bf16):
+    # y in pinned host memory that the device addresses directly: the kernels' stores go there;
+    # eager calls and a compiled step without a copy back give the bits of device-memory y
+    import torch
+    shapes = [(2, 1, 1024, 4096), (2, 1, 3072, 4096)]
+    ms = [inputs.make_matrix(wt, sf, r, c, seed=240 + i) for i, (wt, sf, r, c) in enumerate(shapes)]
+    Ws = [dev_u8(m.W) for m in ms]
+    rng = np.random.default_rng(250 + batch)
+    x = inputs.bf16_codes(rng.standard_normal((batch, 4096))) if bf16 else \
+        rng.standard_normal((batch, 4096)).astype(np.float32)
+    xd = to_dev_x(x)
+    yd = [torch.empty((batch, r), device="cuda") for (_, _, r, _) in shapes]
+    yh = [torch.full((batch, r), 7.0).pin_memory() for (_, _, r, _) in shapes]
+    qmv.matvec_grouped(2, 1, [(r, 4096, Ws[i], xd, yd[i]) for i, (_, _, r, _) in enumerate(shapes)])
+    qmv.matvec_grouped(2, 1, [(r, 4096, Ws[i], xd, yh[i]) for i, (_, _, r, _) in enumerate(shapes)], overlap=True)
+    torch.cuda.synchronize()
+    for i in range(2):
+        assert_bits_equal(yh[i].numpy(), yd[i].cpu().numpy(), f"eager, problem {i}")
+        y_ref, absref = oracle.matvec(ms[i].W, 2, 1, shapes[i][2], 4096, x)
+        check_product(yh[i].numpy(), y_ref, absref, what=f"host y, problem {i}")
+    xh = torch.from_numpy(x.view(np.int16) if bf16 else x).pin_memory()
+    xs = torch.empty_like(xh, device="cuda")
+    xsv = xs.view(torch.bfloat16) if bf16 else xs
+    for y in yh:
+        y.fill_(7.0)
+    with qmv.Step([(2, 1, [(r, 4096, Ws[i], xsv, yh[i]) for i, (_, _, r, _) in enumerate(shapes)], True)],
+                  before=[(xs, xh)]) as step:
+        step.run(wait=True)
+        for i in range(2):
+            assert_bits_equal(yh[i].numpy(), yd[i].cpu().numpy(), f"step, problem {i}")

@@ -149,7 +149,7 @@ def test_dequant_single_rounding_with_f32_scale():
 
 
 def test_nonfinite_and_negative_scales_are_valid_input():
-    # "Any d and nibbles are valid input": negative, zero, inf and NaN scales decode by IEEE.
+    # every scale is valid input: negative, zero, inf and NaN scales decode by IEEE.
     q = np.array([0x80 | 0x08] * 16, dtype=np.uint8)  # low nibble 8 (level 0), high 8 (level 0)
     q[0] = 0x9F  # element 0 level 7, element 16 level 1
     for dval in (-3.0, 0.0, np.inf, -np.inf, np.nan):
