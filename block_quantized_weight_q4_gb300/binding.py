@@ -78,6 +78,14 @@ def load_library():
     lib.qmv_step_run_wait.argtypes = [vp, vp]
     lib.qmv_step_destroy.restype = i32
     lib.qmv_step_destroy.argtypes = [vp]
+    lib.qmv_step_create_gated.restype = i32
+    lib.qmv_step_create_gated.argtypes = [vp, i32, vp, i32, vp, i32, ctypes.POINTER(vp)]
+    lib.qmv_step_open.restype = i32
+    lib.qmv_step_open.argtypes = [vp]
+    lib.qmv_step_wait.restype = i32
+    lib.qmv_step_wait.argtypes = [vp, ctypes.c_longlong]
+    lib.qmv_step_open_wait.restype = i32
+    lib.qmv_step_open_wait.argtypes = [vp, vp, vp, ctypes.c_longlong]
     lib.qmv_gguf_bytes.restype = ctypes.c_size_t
     lib.qmv_gguf_bytes.argtypes = [i32, i64, i64]
     lib.qmv_gguf_to_mlb.restype = i32
@@ -298,9 +306,13 @@ class Step:
     matvec_grouped.  Creating the
     step runs it once.  The tensors are kept alive with the step; a run reads and writes the
     same buffers.  Runs of one step must not overlap in time.  close() (or leaving a `with`
-    block) waits for the device and frees the step."""
+    block) waits for the device and frees the step.
 
-    def __init__(self, groups, before=(), after=()):
+    gated=True (qmv_step_create_gated): each run waits on the device until open() (its `before`
+    copies: pinned host to device memory), and wait() spins on the host until the opened runs
+    are done; a decode loop enqueues the next run before it needs it and only opens it then."""
+
+    def __init__(self, groups, before=(), after=(), gated=False):
         keep = [list(before), list(after)]
         garr = (Group * max(len(groups), 1))()
         for i, grp in enumerate(groups):
@@ -311,9 +323,10 @@ class Step:
                             _flags(overlap, len(grp) > 5 and bool(grp[5])))
         b, a = _copies(list(before)), _copies(list(after))
         handle = ctypes.c_void_p()
-        st = load_library().qmv_step_create(ctypes.addressof(b), len(before), ctypes.addressof(garr), len(groups),
-                                            ctypes.addressof(a), len(after), ctypes.byref(handle))
-        _check(st, "qmv_step_create")
+        create = load_library().qmv_step_create_gated if gated else load_library().qmv_step_create
+        st = create(ctypes.addressof(b), len(before), ctypes.addressof(garr), len(groups),
+                    ctypes.addressof(a), len(after), ctypes.byref(handle))
+        _check(st, "qmv_step_create_gated" if gated else "qmv_step_create")
         self._handle = handle
         self._keep = keep
 
@@ -326,6 +339,26 @@ class Step:
             _check(load_library().qmv_step_run_wait(self._handle, _stream(stream)), "qmv_step_run_wait")
         else:
             _check(load_library().qmv_step_run(self._handle, _stream(stream)), "qmv_step_run")
+
+    def open(self):
+        """Open the oldest enqueued run of a gated step (qmv_step_open)."""
+        if self._handle is None:
+            raise ValueError("step destroyed")
+        _check(load_library().qmv_step_open(self._handle), "qmv_step_open")
+
+    def wait(self, timeout_us=0):
+        """Wait on the host until the opened runs of a gated step are done (qmv_step_wait)."""
+        if self._handle is None:
+            raise ValueError("step destroyed")
+        _check(load_library().qmv_step_wait(self._handle, int(timeout_us)), "qmv_step_wait")
+
+    def open_wait(self, next_step=None, stream=None, timeout_us=0):
+        """open(), then next_step.run(stream) when given, then wait(): one library call
+        (qmv_step_open_wait), a decode loop's step with the next run enqueued behind it."""
+        if self._handle is None or (next_step is not None and next_step._handle is None):
+            raise ValueError("step destroyed")
+        _check(load_library().qmv_step_open_wait(self._handle, None if next_step is None else next_step._handle,
+                                                 _stream(stream), int(timeout_us)), "qmv_step_open_wait")
 
     def close(self):
         if self._handle is not None:

@@ -456,6 +456,40 @@ int qmv_step_run(qmv_step *step, cudaStream_t stream);
  * error the stream reported). */
 int qmv_step_run_wait(qmv_step *step, cudaStream_t stream);
 
+/* A gated step: the same step (created, checked and recorded the same way), whose runs each
+ * start with a gate kernel that waits on the device until the host opens the run, and end with
+ * a kernel that reports the run done to the host through pinned host memory.  A decode loop
+ * then enqueues the next run (qmv_step_run) while the current one computes, and after its
+ * host-side work (the next token) only opens it: the graph's launch leaves the critical path,
+ * and the first products load their first weights while the run waits for the host (they
+ * launch as programmatic dependents of the gate).  Every `before` copy must go from pinned host
+ * memory the device addresses directly to device memory (the gate kernel copies them once the
+ * run is opened), at most 8, else QMV_E_ARG; the step's results can be stored straight into
+ * such host memory by the products (see the conventions above) or copied by `after` copies.
+ *   qmv_step_run  : enqueues a run; it holds its stream at the gate until opened.  A run that
+ *                   is never opened proceeds after one second with stale inputs and records
+ *                   QMV_E_TIMEOUT in the status word (qmv_check_device).
+ *   qmv_step_open : opens the oldest enqueued run that is not yet open (host memory write,
+ *                   release order after the caller's writes of the inputs); QMV_E_ARG for a
+ *                   step that is not gated or has no enqueued run left to open.
+ *   qmv_step_wait : waits on the host (spinning) until every opened run has finished, at most
+ *                   timeout_us microseconds (10 s when <= 0): QMV_OK, QMV_E_TIMEOUT, or QMV_E_ARG
+ *                   for a step that is not gated.  After QMV_OK the run's host results are
+ *                   visible to the calling thread.
+ *   qmv_step_run_wait on a gated step enqueues, opens and waits.
+ * Runs of one gated step follow each other on one stream.  qmv_step_destroy opens the runs
+ * still closed before it waits for the device.  The gate's counters are 64 bytes of pinned
+ * host memory and 8 bytes of device memory, allocated at creation. */
+int qmv_step_create_gated(const qmv_copy *before, int n_before, const qmv_group *groups, int n_groups,
+                          const qmv_copy *after, int n_after, qmv_step **step);
+int qmv_step_open(qmv_step *step);
+int qmv_step_wait(qmv_step *step, long long timeout_us);
+/* A decode loop's step in one call: qmv_step_open(step), then qmv_step_run(next, stream) when
+ * next is not NULL (the following token's run, which waits at its gate), then
+ * qmv_step_wait(step, timeout_us).  Both steps gated, else QMV_E_ARG; otherwise the first
+ * failing call's status. */
+int qmv_step_open_wait(qmv_step *step, qmv_step *next, cudaStream_t stream, long long timeout_us);
+
 /* Waits for the device, then frees the step and its workspaces.  NULL is a no-op.  Returns
  * QMV_OK or QMV_E_CUDA. */
 int qmv_step_destroy(qmv_step *step);

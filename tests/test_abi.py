@@ -122,6 +122,13 @@ def test_dequant_and_validate_argument_errors(lib):
     assert lib.qmv_step_run(None, None) == binding.E_ARG
     assert lib.qmv_step_run_wait(None, None) == binding.E_ARG
     assert lib.qmv_step_destroy(None) == binding.OK
+    # the gated step: the same argument checks, and open / wait need a step
+    assert lib.qmv_step_create_gated(None, 0, None, 0, None, 0, None) == binding.E_ARG
+    assert lib.qmv_step_create_gated(ctypes.addressof(bad), 1, None, 0, None, 0, ctypes.byref(out)) == binding.E_ARG
+    assert out.value is None
+    assert lib.qmv_step_open(None) == binding.E_ARG
+    assert lib.qmv_step_wait(None, 0) == binding.E_ARG
+    assert lib.qmv_step_open_wait(None, None, None, 0) == binding.E_ARG
     # qmv_gguf_bytes / qmv_gguf_to_mlb: sizes, then shape, format, null and alignment checks
     assert lib.qmv_gguf_bytes(1, 151936, 896) == 144643072
     assert lib.qmv_gguf_bytes(2, 151936, 896) == 76575744

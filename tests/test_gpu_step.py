@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 
 import oracle
-from block_quantized_weight_q4_gb300 import inputs
+from block_quantized_weight_q4_gb300 import binding, inputs
 from helpers import assert_bits_equal, check_product, dev_u8
 
 pytestmark = pytest.mark.gpu
@@ -219,3 +219,94 @@ def test_products_store_y_into_pinned_host_memory(qmv, batch, bf16):
         step.run(wait=True)
         for i in range(2):
             assert_bits_equal(yh[i].numpy(), yd[i].cpu().numpy(), f"step, problem {i}")
+
+
+def test_gated_step_pipelined_runs_match_eager_calls(qmv):
+    # a gated step as a decode loop drives it: the next run is enqueued while the current one
+    # computes and opened only after the host has the current result and has written the next
+    # input; every run's y (stored by the products into pinned host memory) must equal the
+    # eager calls' bits for that input
+    import torch
+    shapes = [(2, 1, 4096, 4096), (2, 1, 1024, 4096)]
+    ms = [inputs.make_matrix(wt, sf, r, c, seed=260 + i) for i, (wt, sf, r, c) in enumerate(shapes)]
+    Ws = [dev_u8(m.W) for m in ms]
+    xh = torch.empty((1, 4096), dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty_like(xh, device="cuda")
+    yh = [torch.empty((1, r)).pin_memory() for (_, _, r, _) in shapes]
+    groups = [(2, 1, [(shapes[0][2], 4096, Ws[0], xd, yh[0])], True),
+              (2, 1, [(shapes[1][2], 4096, Ws[1], xd, yh[1])], True)]
+    rng = np.random.default_rng(270)
+    xs = [inputs.bf16_codes(rng.standard_normal((1, 4096))) for _ in range(5)]
+
+    def put(x):
+        xh.view(torch.int16).copy_(torch.from_numpy(x.view(np.int16)))
+
+    put(xs[0])
+    expect = []
+    for x in xs:
+        xe = to_dev_x(x)
+        ye = [torch.empty((1, r), device="cuda") for (_, _, r, _) in shapes]
+        for i, (_, _, r, _) in enumerate(shapes):
+            qmv.matvec_grouped(2, 1, [(r, 4096, Ws[i], xe, ye[i])], overlap=True)
+        torch.cuda.synchronize()
+        expect.append([y.cpu().numpy() for y in ye])
+    s = torch.cuda.Stream()
+    with qmv.Step(groups, before=[(xd, xh)], gated=True) as step:
+        step.run(stream=s)
+        for it, x in enumerate(xs):
+            put(x)
+            step.open()
+            if it + 1 < len(xs):
+                step.run(stream=s)       # the next run waits at its gate
+            step.wait()
+            for i in range(2):
+                assert_bits_equal(yh[i].numpy(), expect[it][i], f"gated run {it}, problem {i}")
+        # the one-call forms: a run, its opening and the wait; the opening, the next run and the wait
+        put(xs[2])
+        step.run(stream=s, wait=True)
+        for i in range(2):
+            assert_bits_equal(yh[i].numpy(), expect[2][i], f"gated run_wait, problem {i}")
+        step.run(stream=s)
+        for it in (3, 4):
+            put(xs[it])
+            step.open_wait(step if it == 3 else None, stream=s)
+            for i in range(2):
+                assert_bits_equal(yh[i].numpy(), expect[it][i], f"gated open_wait {it}, problem {i}")
+    y_ref, absref = oracle.matvec(ms[1].W, 2, 1, 1024, 4096, xs[4])   # the last run's input
+    check_product(yh[1].numpy(), y_ref, absref, what="gated step against the oracle")
+
+
+def test_gated_step_waits_and_reports(qmv):
+    # the host's wait is bounded: an opened run still queued behind other work makes it run out
+    # (QMV_E_TIMEOUT), and a later wait sees the run done; a run never opened holds its stream
+    # until its gate's one-second bound, which the status word reports
+    import torch
+    m = inputs.make_matrix(2, 1, 256, 512, seed=280)
+    W = dev_u8(m.W)
+    xh = torch.zeros((1, 512), dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty_like(xh, device="cuda")
+    yh = torch.full((1, 256), 5.0).pin_memory()
+    s = torch.cuda.Stream()
+    step = qmv.Step([(2, 1, [(256, 512, W, xd, yh)], False)], before=[(xd, xh)], gated=True)
+    try:
+        with pytest.raises(qmv.QmvError) as e:
+            step.open()                      # no run enqueued
+        assert e.value.status == binding.E_ARG
+        with torch.cuda.stream(s):
+            torch.cuda._sleep(50_000_000)    # tens of milliseconds of other work ahead of the run
+        step.run(stream=s)
+        step.open()
+        with pytest.raises(qmv.QmvError) as e:
+            step.wait(timeout_us=2000)
+        assert e.value.status == binding.E_TIMEOUT
+        step.wait()
+        assert float(yh.abs().max()) == 0.0  # x = 0 gives y = 0
+        assert qmv.last_error() == 0
+        step.run(stream=s)
+        assert not s.query()                 # held at the gate
+        step.run(stream=s)                   # never opened
+        s.synchronize()                      # returns after the gate's bound
+        assert qmv.last_error() == binding.E_TIMEOUT
+    finally:
+        step.close()
+    assert qmv.last_error() == 0
