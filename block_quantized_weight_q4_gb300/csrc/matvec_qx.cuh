@@ -341,12 +341,9 @@ __global__ void __launch_bounds__(kWarps * 32, MinCtas<R, NV>::value)
 #pragma unroll
           for (int e = 0; e < 8; ++e) vals[e] = 0.f;
         }
-        float amax = 0.f;
+        float amax = 0.f;  // fmaxf skips a NaN operand
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float a = fabsf(vals[e]);
-          if (a > amax) amax = a;
-        }
+        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(vals[e]));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
         float inv = 0.f, dv = 0.f;  // the zero block

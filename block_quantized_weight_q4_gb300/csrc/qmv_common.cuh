@@ -397,16 +397,11 @@ __device__ __forceinline__ void act_q8_lane_quarters(const float (&v)[NCH][8], u
 #pragma unroll
   for (int h = 0; h < NCH; ++h) {
     float m = 0.f;
+    // fmaxf returns the operand that is not NaN, so a NaN value is skipped, and m never is NaN
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float a = fabsf(v[h][e]);
-      if (a > m) m = a;
-    }
+    for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[h][e]));
 #pragma unroll
-    for (int o = 1; o <= 2; o <<= 1) {
-      const float b = __shfl_xor_sync(0xffffffffu, m, o);
-      if (b > m) m = b;
-    }
+    for (int o = 1; o <= 2; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     amax[h] = m;
   }
   const int r = lane & 1;

@@ -360,17 +360,11 @@ __global__ void __launch_bounds__(128) quantize_x_group_kernel(const __grid_cons
     const float4 f0 = __ldg(p), f1 = __ldg(p + 1);
     v[0] = f0.x, v[1] = f0.y, v[2] = f0.z, v[3] = f0.w, v[4] = f1.x, v[5] = f1.y, v[6] = f1.z, v[7] = f1.w;
   }
-  float amax = 0.f;
+  float amax = 0.f;  // fmaxf skips a NaN operand, so amax never is NaN
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const float m = fabsf(v[e]);
-    if (m > amax) amax = m;
-  }
+  for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[e]));
 #pragma unroll
-  for (int o = 1; o <= 2; o <<= 1) {
-    const float m = __shfl_xor_sync(0xffffffffu, amax, o);
-    if (m > amax) amax = m;
-  }
+  for (int o = 1; o <= 2; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   // lane 4g divides for d = amax / 127, lane 4g + 1 for 127 / amax; the zero block (amax below
   // 1e-30) has d = 0 and its inverse taken as 0
   const int lane = threadIdx.x & 31;
