@@ -27,7 +27,8 @@
 //     batch read a zero area instead.
 //   * Scale and accumulate.  acc += d[row][block] * fragment, float32 FFMA.
 //   * Split-K.  Warps of one item that share a tile add their partial sums through shared
-//     memory in a fixed order; one warp writes y.
+//     memory in a fixed order (a reduction area, or, in the variant without one, the q slot
+//     each warp has just consumed); one warp writes y.
 //   * Groups.  One launch may carry up to 8 problems of the same types and batch (for
 //     example the projections of a layer that read the same input); items of all problems
 //     form one list that the persistent CTAs walk.
