@@ -387,3 +387,33 @@ def test_matvec_qx_grouped_two_step_equals_quantize_then_product(qmv, bf16):
     check_product(y3.cpu().numpy(), y_ref, absref, tol=1e-4, what="captured without a split buffer")
     check_product(y1.cpu().numpy(), y_ref, absref, tol=1e-4, what="two-step")
     assert qmv.last_error() == 0
+
+
+def test_matvec_qx_grouped_two_step_edge_cases(qmv):
+    # two problems reading one activation pointer with different cols (two images of the same
+    # memory), and a group whose images exceed the stream's 2 MiB split buffer (the dp4a kernel
+    # then quantizes them itself): both against the oracle
+    import torch
+    rng = np.random.default_rng(160)
+    ma = inputs.make_matrix(2, 1, 40, 512, seed=161)
+    mb = inputs.make_matrix(2, 1, 24, 256, seed=162)
+    batch = 3
+    x = activations(rng, batch, 512)
+    xd = dev_x(x)
+    ya = torch.full((batch, 40), 9.0, device="cuda")
+    yb = torch.full((batch, 24), 9.0, device="cuda")
+    qmv.matvec_qx_grouped(2, 1, [(40, 512, dev_u8(ma.W), xd, ya), (24, 256, dev_u8(mb.W), xd, yb)])
+    torch.cuda.synchronize()
+    xb_view = x.reshape(-1)[:batch * 256].reshape(batch, 256)   # the same memory as [batch][256]
+    for m, xv, y in ((ma, x, ya), (mb, xb_view, yb)):
+        y_ref, absref = oracle_qx(m, xv, False)
+        check_product(y.cpu().numpy(), y_ref, absref, tol=1e-4, what=f"shared pointer {m.rows}x{m.cols}")
+    # 128 vectors of 16384 columns: 2.36 MB of images
+    mc = inputs.make_matrix(1, 0, 16, 16384, seed=163)
+    xc = activations(rng, 128, 16384)
+    yc = torch.full((128, 16), 9.0, device="cuda")
+    qmv.matvec_qx_grouped(1, 0, [(16, 16384, dev_u8(mc.W), dev_x(xc), yc)])
+    torch.cuda.synchronize()
+    y_ref, absref = oracle_qx(mc, xc, False)
+    check_product(yc.cpu().numpy(), y_ref, absref, tol=1e-4, what="images beyond the split buffer")
+    assert qmv.last_error() == 0
