@@ -402,7 +402,9 @@ def test_matvec_qx_grouped_two_step_edge_cases(qmv):
     xd = dev_x(x)
     ya = torch.full((batch, 40), 9.0, device="cuda")
     yb = torch.full((batch, 24), 9.0, device="cuda")
-    qmv.matvec_qx_grouped(2, 1, [(40, 512, dev_u8(ma.W), xd, ya), (24, 256, dev_u8(mb.W), xd, yb)])
+    xd256 = xd.view(-1)[:batch * 256].view(batch, 256)          # the same pointer, 256 columns
+    assert xd256.data_ptr() == xd.data_ptr()
+    qmv.matvec_qx_grouped(2, 1, [(40, 512, dev_u8(ma.W), xd, ya), (24, 256, dev_u8(mb.W), xd256, yb)])
     torch.cuda.synchronize()
     xb_view = x.reshape(-1)[:batch * 256].reshape(batch, 256)   # the same memory as [batch][256]
     for m, xv, y in ((ma, x, ya), (mb, xb_view, yb)):
