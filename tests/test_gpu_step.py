@@ -310,3 +310,39 @@ def test_gated_step_waits_and_reports(qmv):
     finally:
         step.close()
     assert qmv.last_error() == 0
+
+
+def test_gated_step_with_after_copies_and_without_before_copies(qmv):
+    # a gated step whose results go back through `after` copies (the done kernel then follows the
+    # copy), one with no `before` copies (the input already on the device: the gate only waits),
+    # and the refusal of a `before` copy that is not pinned host -> device memory
+    import torch
+    m = inputs.make_matrix(2, 1, 512, 1024, seed=290)
+    W = dev_u8(m.W)
+    rng = np.random.default_rng(291)
+    x = inputs.bf16_codes(rng.standard_normal((1, 1024)))
+    xh = torch.from_numpy(x.view(np.int16)).pin_memory()
+    xd = torch.empty_like(xh, device="cuda")
+    yd = torch.empty((1, 512), device="cuda")
+    yh = torch.zeros((1, 512)).pin_memory()
+    xe = to_dev_x(x)
+    ye = torch.empty((1, 512), device="cuda")
+    qmv.matvec_grouped(2, 1, [(512, 1024, W, xe, ye)], overlap=True)
+    torch.cuda.synchronize()
+    want = ye.cpu().numpy()
+    xdb = xd.view(torch.bfloat16)
+    with qmv.Step([(2, 1, [(512, 1024, W, xdb, yd)], True)], before=[(xd, xh)], after=[(yh, yd)],
+                  gated=True) as step:
+        for _ in range(2):
+            yh.zero_()
+            step.run(wait=True)
+            assert_bits_equal(yh.numpy(), want, "gated step with an after copy")
+    xdb.copy_(xe)
+    yd.zero_()
+    with qmv.Step([(2, 1, [(512, 1024, W, xdb, yd)], True)], gated=True) as step:
+        step.run(wait=True)
+        assert_bits_equal(yd.cpu().numpy(), want, "gated step without before copies")
+    with pytest.raises(qmv.QmvError) as e:
+        qmv.Step([(2, 1, [(512, 1024, W, xdb, yd)], True)], before=[(xd, xe.view(torch.int16))], gated=True)
+    assert e.value.status == binding.E_ARG
+    assert qmv.last_error() == 0
