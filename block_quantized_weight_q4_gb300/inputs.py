@@ -28,7 +28,7 @@ import numpy as np
 Q8_0 = 1
 Q4_0 = 2
 
-# q8_mask class bits ("q8_mask bits, one per matrix class")
+# q8_mask class bits (the header's mask has a bit for each class of matrix)
 CLASS_TOK_EMB = 1
 CLASS_WCLS = 2
 CLASS_WQ_WK = 4

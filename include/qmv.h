@@ -95,8 +95,8 @@ extern "C" {
 #define QMV_E_CUDA 6    /* a CUDA call failed (launch error, no device, no sm_103a) */
 #define QMV_E_TIMEOUT 7 /* a kernel's bounded wait ran out (see qmv_check_device)   */
 
-/* q8_mask class bits (Krafla page, header offset 72, "q8_mask bits, one per matrix
- * class").  wq/wk also cover wg and lqkv; wv covers lz; wo covers lout. */
+/* q8_mask class bits (Krafla page, header offset 72: the mask has a bit for each class of
+ * matrix).  wq/wk also cover wg and lqkv; wv covers lz; wo covers lout. */
 #define QMV_CLASS_TOK_EMB 1
 #define QMV_CLASS_WCLS 2
 #define QMV_CLASS_WQ_WK 4
@@ -397,7 +397,7 @@ int qmv_matvec_qx_grouped(int wtype, int scale_dtype, int x_dtype, int batch, co
  * m = the element of largest magnitude (the first of equals); for the candidate levels
  * L = -(60 + 2k)/10, k = 0..12 (-6 .. -8.4): s = m / L, l_j = clamp(rint(x_j / s), -8, 7)
  * (ties to even), d = sum(x^3 l) / sum(x^2 l^2) (0 when the denominator is 0), and the
- * candidate with the smallest sum(x^2 (x - d l)^2) wins (the first on ties); a block with
+ * lowest sum(x^2 (x - d l)^2) picks the candidate (the first on ties); a block with
  * max |x| under 1e-6 is divided by that maximum before the fit and d multiplied by it after;
  * the zero block is d = 0 with every level 0; with f16 scales only the winning d goes to f16
  * (to nearest).
