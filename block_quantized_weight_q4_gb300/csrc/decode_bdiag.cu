@@ -122,6 +122,7 @@ struct Params {
   int nitems;
   int* status;
   // gated pair: problem 0 is the w1 / w3 pair (rows = w1's rows, 16 of each per warp tile)
+  int early;      // the weights may be read before the preceding kernel has finished
   int act;        // 0 SiLU, 1 GELU-tanh
   uint16_t* h;    // the down projection's activations: hi parts at h[r], lo parts at h[rows + r]
   Problem pr[kMaxProblems];
@@ -387,6 +388,8 @@ __global__ void __launch_bounds__(NW * 32) matvec_bdiag_kernel(const __grid_cons
   int pre_c[C::S], pre_prob[C::S];
   bool pre_valid[C::S];
   int pre = 0;
+  // launched early without leave to read the weights meanwhile: nothing global before the wait
+  if (!p.early) griddep_wait();
   while (pre < kPre && pc.item < p.nitems) {
     pre_c[pre] = pc.c0 + (pc.j << p.lgks);
     pre_prob[pre] = pc.prob;
@@ -797,6 +800,7 @@ cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* cons
   p.ks = plan.ks;
   p.lgks = 31 - __builtin_clz((unsigned)plan.ks);
   p.act = act;
+  p.early = pdl ? 1 : 0;
   p.h = h;
   const int tpi = NW / plan.ks;
   int items = 0;
@@ -853,11 +857,13 @@ cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* cons
   cfg.blockDim = dim3(NW * 32);
   cfg.dynamicSmemBytes = plan.smem;
   cfg.stream = stream;
+  // always a programmatic dependent: the CTAs start and set up during the preceding kernel's
+  // tail; without pdl they wait for it before their first global access (p.early = 0)
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, matvec_bdiag_kernel<WT, F16, NW, CH, XS, GLU, XF, RD, XH, XQ>, maps, p);
 }
 

@@ -32,10 +32,11 @@
 //   * Groups.  One launch may carry up to 8 problems of the same types and batch (for
 //     example the projections of a layer that read the same input); items of all problems
 //     form one list that the persistent CTAs walk.
-//   * Overlap with the preceding kernel (optional, programmatic dependent launch).  The
-//     weight boxes of the first stages are requested before griddepcontrol.wait; the
-//     activations are read and y is written only after it.  The weights must then not be
-//     written by the preceding kernel.
+//   * Launched as a programmatic dependent of the preceding kernel: the CTAs start and set up
+//     during its tail.  With the overlap flag the weight boxes of the first stages are also
+//     requested before griddepcontrol.wait (the weights must then not be written by the
+//     preceding kernel); without it nothing global is touched before the wait.  The
+//     activations are read and y is written only after it.
 // f32 activations are split x = hi + lo (two bfloat16s, hi = RN(x)) and take two MMAs each,
 // which keeps 16 significant bits of x.
 // XQ: the runtime's activation-quantized product on an activation image of Q8_0 quants with a
@@ -114,6 +115,7 @@ struct Params {
   int batch;    // 1..8
   int ks;       // column slices per tile (1, 2, 4, 8, 16); at most every problem's nchunks
   int nitems;
+  int early;    // the weights may be read before the preceding kernel has finished
   int* status;
   Problem pr[kMaxProblems];
 };
@@ -226,6 +228,8 @@ __global__ void __launch_bounds__(NW * 32) matvec_mma_kernel(const __grid_consta
   int pre_c[C::S], pre_prob[C::S];
   bool pre_valid[C::S];
   int pre = 0;
+  // launched early without leave to read the weights meanwhile: nothing global before the wait
+  if (!p.early) griddep_wait();
   while (pre < C::S - 1 && pc.item < p.nitems) {
     pre_c[pre] = pc.c0 + pc.j;
     pre_prob[pre] = pc.prob;
@@ -606,6 +610,7 @@ cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* cons
   p.batch = batch;
   p.status = dev.status;
   p.ks = plan.ks;
+  p.early = pdl ? 1 : 0;
   const int tpi = NW / plan.ks;
   int items = 0;
   for (int i = 0; i < n; ++i) {
@@ -667,11 +672,13 @@ cudaError_t launch_typed(const Plan& plan, const MatrixRef* ms, const void* cons
   cfg.blockDim = dim3(NW * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
+  // always a programmatic dependent: the CTAs start and set up during the preceding kernel's
+  // tail; without pdl they wait for it before their first global access (p.early = 0)
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, matvec_mma_kernel<WT, F16, XBF16, NW, XQ, RS>, maps, p);
 }
 

@@ -442,3 +442,41 @@ def test_one_vector_stages_rounded_to_half_and_exact(qmv, route):
     check_product(yg, y_exp, absref, 1e-6, f"{route}: rounded stages 1, exact stages x")
     rel = (y_ref[0] - yg[0].astype(np.float64)) / absref[0]
     assert np.all(rel > 2.0 ** -12 * 0.7) and np.all(rel < 2.0 ** -12), f"{route}: {rel.min()} .. {rel.max()}"
+
+
+def test_no_overlap_flag_reads_weights_written_just_before(qmv):
+    # without the overlap flag a product may start during the preceding kernel's tail but must
+    # read the weights that kernel writes: each replay writes one of two matrices into W with a
+    # kernel right before the product (batch 1 and batch 4 routes), and y must be that matrix's
+    import torch
+    ma = inputs.make_matrix(2, 1, 2048, 4096, seed=70)
+    mb = inputs.make_matrix(2, 1, 2048, 4096, seed=71)
+    srcs = [dev_u8(ma.W), dev_u8(mb.W)]
+    W = torch.zeros_like(srcs[0])
+    for batch in (1, 4):
+        x = inputs.make_x(batch, 4096, True, seed=72 + batch)
+        xd = dev_x(x)
+        want = []
+        for s in srcs:
+            yw = torch.empty((batch, 2048), device="cuda")
+            qmv.matvec_grouped(2, 1, [(2048, 4096, s, xd, yw)])
+            want.append(yw)
+        torch.cuda.synchronize()
+        ys = [torch.empty((batch, 2048), device="cuda") for _ in range(4)]
+        g = torch.cuda.CUDAGraph()
+        st = torch.cuda.Stream()
+        with torch.cuda.stream(st):
+            qmv.matvec_grouped(2, 1, [(2048, 4096, W, xd, ys[0])])
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=st):
+            for i in range(4):
+                torch.bitwise_or(srcs[i % 2], 0, out=W)      # a kernel writes the weights
+                qmv.matvec_grouped(2, 1, [(2048, 4096, W, xd, ys[i])])
+        for _ in range(3):
+            W.zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            for i in range(4):
+                assert_bits_equal(ys[i].cpu().numpy(), want[i % 2].cpu().numpy(), f"b{batch} product {i}")
+    y_ref, absref = oracle.matvec(mb.W, 2, 1, 2048, 4096, x)
+    check_product(ys[1].cpu().numpy(), y_ref, absref, TOL, "no overlap flag, batch 4")
