@@ -101,6 +101,7 @@ struct Params {
   int xsplit;  // 1: x[i] is 16 rows of bfloat16, hi parts of the vectors in rows 0..7, lo in 8..15
   int grid;
   long long units;
+  int early;  // the weights may be read before the preceding kernel has finished
   int* status;
   float* partials;              // [2 * grid][NV][kTileRows] parts of split tiles (NV: the kernel's)
   unsigned* counters;           // [grid] arrivals, zero between launches
@@ -258,6 +259,8 @@ __global__ void __maxnreg__(NV > 8 ? 128 : 120) decode_tc_kernel(const __grid_co
   using C = Cfg<WT, F16>;
   constexpr int S = C::S;
   constexpr int kPart = NV * kTileRows;  // floats of one part of a split tile
+  // launched early without leave to read the weights meanwhile: nothing global before the wait
+  if (!p.early) griddep_wait();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);  // 1024-aligned: swizzle atoms
@@ -597,6 +600,7 @@ cudaError_t launch_typed(const MatrixRef* ms, const void* const* xs, float* cons
   p.nprob = n;
   p.batch = batch;
   p.xsplit = xsplit ? 1 : 0;
+  p.early = pdl ? 1 : 0;
   p.status = dev.status;
   p.partials = ws.partials;
   p.counters = ws.counters;
@@ -648,11 +652,13 @@ cudaError_t launch_typed(const MatrixRef* ms, const void* const* xs, float* cons
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = stream;
+  // always a programmatic dependent: the CTAs start during the preceding kernel's tail; without
+  // pdl they wait for it before their first global access (p.early = 0)
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, maps, p);
 }
 

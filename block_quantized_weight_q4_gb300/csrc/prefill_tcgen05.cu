@@ -109,6 +109,7 @@ struct PParams {
   int ksplit;          // column ranges per tile (1: no workspace used)
   unsigned* counters;  // per tile arrival counters, zero between launches
   float* parts;        // per (tile, split): npad x 128 partial sums, vector-major
+  int early;           // the weights may be read before the preceding kernel has finished
 };
 
 __device__ __forceinline__ unsigned atomic_add_acq_rel_u32(unsigned* addr, unsigned v) {
@@ -358,6 +359,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   using C = PCfg<WT, F16>;
   constexpr int kKS = Ring<HILO>::kKS;
   constexpr int kSC = Ring<HILO>::kStageCols;
+  // launched early without leave to read the weights meanwhile: nothing global (and no tensor
+  // memory) before the wait
+  if (!p.early) griddep_wait();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);  // 1024-aligned: swizzle atoms
@@ -754,6 +758,7 @@ static cudaError_t launch_prefill_typed(const MatrixRef& m, const void* x, float
   p.batch = batch;
   p.npad = (batch + 15) / 16 * 16;
   p.status = dev.status;
+  p.early = pdl ? 1 : 0;
   // X ring: as many stages as the shared memory left by the raw ring holds, in an even
   // number (the two MMA warps take alternate stages, so with an even depth each slot always
   // serves the same warp and no warp can wait for a phase two ahead of the slot's barrier,
@@ -783,11 +788,12 @@ static cudaError_t launch_prefill_typed(const MatrixRef& m, const void* x, float
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::smem_bytes(p.xs, p.npad);
   cfg.stream = stream;
+  // always a programmatic dependent (without pdl the kernel waits before its first global access)
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, tq, td, tx, p);
 }
 
