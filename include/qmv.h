@@ -189,9 +189,10 @@ typedef struct qmv_problem {
  *   precedes it on the stream finishes (a programmatic dependent launch).  Activations are
  *   read, and y written, only after the preceding kernel has completed; the WEIGHTS however
  *   may be read earlier, so they must not be written by the immediately preceding kernel
- *   (true for model weights after loading).  Without the flag the decode kernels of batches
- *   1..8 still launch as programmatic dependents (their CTAs start and set up during the
- *   preceding kernel's tail) but touch no global memory before that kernel has completed.
+ *   (true for model weights after loading).  Without the flag the decode and prefill kernels
+ *   still launch as programmatic dependents (their CTAs start and set up during the preceding
+ *   kernel's tail) but touch no global memory, and allocate no tensor memory, before that
+ *   kernel has completed.
  * QMV_FLAG_BF16_WEIGHTS: for the problems that take the prefill kernel (16 or more bf16
  *   vectors), round each dequantized weight once to bfloat16 instead of passing it as hi + lo
  *   parts: one MMA per 16 columns instead of two.  Each term then carries a relative error of
