@@ -2,7 +2,10 @@
 // on a private stream (which sets up the kernels and that stream's workspaces and checks the
 // arguments), then recorded as a CUDA graph and replayed by one call per step.  The graph's
 // kernels hold the private stream's workspace pointers, so a step owns its workspaces and two
-// steps never share them.
+// steps never share them.  A gated step's graph starts with a kernel that waits until the host
+// opens the run (a count in pinned host memory) and then copies the step's inputs from pinned
+// host memory, and ends with a kernel that reports the run done the same way: a decode loop
+// enqueues the next token's run while the current one computes and only opens it later.
 #include <chrono>
 #include <new>
 
